@@ -1,0 +1,256 @@
+/*
+ * GEMM oracle -- TEST INFRASTRUCTURE ONLY.
+ *
+ * Only the tests, the smoke check and the benchmark's CPU-baseline leg may
+ * load this library. It shares no code with the CUDA path.
+ *
+ * What it computes (plain definition, no blocking or reordering):
+ *
+ *   D[i][j] = alpha * sum_{k=0}^{K-1} A(i,k) * B(k,j) + beta * C[i][j]
+ *
+ * in IEEE double precision, over the exact values of the fp16/bf16 inputs.
+ * The accumulate-into-D form is the one the tensor-core pages state for one
+ * MMA (gpu-kernels part 6, "Tensor Cores, layouts, and swizzling", opening
+ * paragraph: D = A.B + C; zhenwei tcgen05 page, "Overview" and the
+ * interactive K-step walk-through: the first K step overwrites, later steps
+ * add); alpha/beta are the BLAS reading of "D = alpha.A.B + beta.C" with
+ * beta == 0 never reading C.
+ *
+ * Operand storage (the "major-ness" of the tcgen05 descriptor pages,
+ * gauravjain "LBO, SBO and SWZ for a tcgen05 tile", section 1):
+ *   A is logical M x K.  K-major: A[m*lda + k].  MN-major: A[k*lda + m].
+ *   B is logical K x N.  K-major: B[n*ldb + k].  MN-major: B[k*ldb + n].
+ *   C and D are row-major M x N with leading dimension ldc.
+ *
+ * Alongside D it returns the error scale used by the parity tolerance:
+ *   S[i][j] = |alpha| * sum_k |A(i,k) * B(k,j)| + |beta * C[i][j]|.
+ *
+ * Rounding to an output format (oracle_round_*) is round-to-nearest-even
+ * from the double value in one step (no double rounding through float).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { ORC_F16 = 0, ORC_BF16 = 1, ORC_F32 = 2 };
+
+/* IEEE binary16: 1 sign, 5 exponent (bias 15), 10 fraction bits. */
+static double decode_f16(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int f = h & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);                 /* subnormal: f * 2^-14 * 2^-10 */
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(f | 0x400), e - 25);    /* 1.f * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+/* bfloat16 is the upper half of an IEEE binary32. */
+static double decode_bf16(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float x;
+    memcpy(&x, &u, sizeof x);
+    return (double)x;
+}
+
+static double decode_f32(uint32_t u)
+{
+    float x;
+    memcpy(&x, &u, sizeof x);
+    return (double)x;
+}
+
+static double load(const void *p, int fmt, int64_t idx)
+{
+    switch (fmt) {
+    case ORC_F16: return decode_f16(((const uint16_t *)p)[idx]);
+    case ORC_BF16: return decode_bf16(((const uint16_t *)p)[idx]);
+    default: return decode_f32(((const uint32_t *)p)[idx]);
+    }
+}
+
+static double a_at(const void *A, int fmt, int major, int64_t lda, int64_t m, int64_t k)
+{
+    return load(A, fmt, major == 0 ? m * lda + k : k * lda + m);
+}
+
+static double b_at(const void *B, int fmt, int major, int64_t ldb, int64_t k, int64_t n)
+{
+    return load(B, fmt, major == 0 ? n * ldb + k : k * ldb + n);
+}
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/*
+ * Full product. D and S are row-major M x N doubles (S may be NULL).
+ * The loop order is i-k-j: row i of D accumulates A(i,k) * row k of B,
+ * k = 0, 1, ..., K-1 in that order.
+ */
+int oracle_gemm(int64_t M, int64_t N, int64_t K,
+                const void *A, int in_fmt, int a_major, int64_t lda,
+                const void *B, int b_major, int64_t ldb,
+                const void *C, int c_fmt, int64_t ldc,
+                double alpha, double beta,
+                double *D, double *S, int nthreads)
+{
+    if (M < 0 || N < 0 || K < 0)
+        return 1;
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    int64_t i;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (i = 0; i < M; ++i) {
+        double *acc = (double *)calloc((size_t)(N > 0 ? N : 1), sizeof(double));
+        double *sab = (double *)calloc((size_t)(N > 0 ? N : 1), sizeof(double));
+        for (int64_t k = 0; k < K; ++k) {
+            double a = a_at(A, in_fmt, a_major, lda, i, k);
+            for (int64_t j = 0; j < N; ++j) {
+                double p = a * b_at(B, in_fmt, b_major, ldb, k, j);
+                acc[j] += p;
+                sab[j] += fabs(p);
+            }
+        }
+        for (int64_t j = 0; j < N; ++j) {
+            double c = (beta != 0.0 && C) ? load(C, c_fmt, i * ldc + j) : 0.0;
+            D[i * N + j] = alpha * acc[j] + beta * c;
+            if (S)
+                S[i * N + j] = fabs(alpha) * sab[j] + fabs(beta * c);
+        }
+        free(acc);
+        free(sab);
+    }
+    return 0;
+}
+
+/*
+ * Selected entries only: out_D[e] and out_S[e] for (rows[e], cols[e]).
+ * Each entry is the same k = 0..K-1 sum as oracle_gemm, one dot product at
+ * a time, so full-size problems can be checked on a sample.
+ */
+int oracle_gemm_entries(int64_t M, int64_t N, int64_t K,
+                        const void *A, int in_fmt, int a_major, int64_t lda,
+                        const void *B, int b_major, int64_t ldb,
+                        const void *C, int c_fmt, int64_t ldc,
+                        double alpha, double beta,
+                        int64_t n_entries, const int64_t *rows, const int64_t *cols,
+                        double *out_D, double *out_S, int nthreads)
+{
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    int bad = 0;
+    int64_t e;
+#pragma omp parallel for schedule(dynamic, 16) reduction(| : bad)
+    for (e = 0; e < n_entries; ++e) {
+        int64_t i = rows[e], j = cols[e];
+        if (i < 0 || i >= M || j < 0 || j >= N) {
+            bad |= 1;
+            continue;
+        }
+        double acc = 0.0, sab = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double p = a_at(A, in_fmt, a_major, lda, i, k) * b_at(B, in_fmt, b_major, ldb, k, j);
+            acc += p;
+            sab += fabs(p);
+        }
+        double c = (beta != 0.0 && C) ? load(C, c_fmt, i * ldc + j) : 0.0;
+        out_D[e] = alpha * acc + beta * c;
+        if (out_S)
+            out_S[e] = fabs(alpha) * sab + fabs(beta * c);
+    }
+    return bad;
+}
+
+/*
+ * Round-to-nearest-even of x to a binary format with p significand bits
+ * (hidden bit included), minimum normal exponent emin and maximum exponent
+ * emax; subnormals are kept, overflow goes to infinity.
+ */
+static double round_rne(double x, int p, int emin, int emax)
+{
+    if (x == 0.0 || isnan(x) || isinf(x))
+        return x;
+    int e2;
+    frexp(x, &e2);                 /* |x| in [2^(e2-1), 2^e2) */
+    int lead = e2 - 1;
+    if (lead < emin)
+        lead = emin;               /* subnormal range: fixed quantum */
+    int q = lead - (p - 1);        /* exponent of one unit in the last place */
+    double r = nearbyint(ldexp(x, -q)) ;  /* default rounding mode: ties to even */
+    double y = ldexp(r, q);
+    double maxf = ldexp(ldexp(1.0, p) - 1.0, emax - (p - 1));
+    if (fabs(y) > maxf)
+        return x > 0 ? INFINITY : -INFINITY;
+    return y;
+}
+
+double oracle_round(double x, int fmt)
+{
+    switch (fmt) {
+    case ORC_F16: return round_rne(x, 11, -14, 15);
+    case ORC_BF16: return round_rne(x, 8, -126, 127);
+    default: return round_rne(x, 24, -126, 127);
+    }
+}
+
+/* Round n doubles and write the output format's bit patterns. */
+void oracle_round_bits(const double *x, int64_t n, int fmt, void *out)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        double y = oracle_round(x[i], fmt);
+        if (fmt == ORC_F32) {
+            float f = (float)y;    /* exact: y is already a binary32 value */
+            uint32_t u;
+            memcpy(&u, &f, sizeof u);
+            ((uint32_t *)out)[i] = u;
+        } else if (fmt == ORC_BF16) {
+            float f = (float)y;    /* exact: bf16 values are binary32 values */
+            uint32_t u;
+            memcpy(&u, &f, sizeof u);
+            ((uint16_t *)out)[i] = (uint16_t)(u >> 16);
+        } else {
+            /* encode binary16 from the exact value y */
+            uint16_t s = signbit(y) ? 0x8000 : 0;
+            double a = fabs(y);
+            uint16_t h;
+            if (isnan(y))
+                h = 0x7e00;
+            else if (isinf(a))
+                h = 0x7c00;
+            else if (a < ldexp(1.0, -14))
+                h = (uint16_t)nearbyint(ldexp(a, 24));   /* exact multiple of 2^-24 */
+            else {
+                int e2;
+                double m = frexp(a, &e2);                /* a = m * 2^e2, m in [0.5,1) */
+                int e = e2 - 1 + 15;
+                uint16_t f = (uint16_t)(ldexp(m, 11) - 1024.0);
+                h = (uint16_t)((e << 10) | f);
+            }
+            ((uint16_t *)out)[i] = (uint16_t)(s | h);
+        }
+    }
+}

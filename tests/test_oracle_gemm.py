@@ -1,0 +1,201 @@
+"""Pins of the fp64 GEMM oracle: exact integer products, identities, a hand case,
+brute force in exact rationals, an independent library matmul, and the rounding."""
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import seeded_inputs as si
+from oracle import gemm as G
+
+
+def _vals(bits, fmt):
+    return si.bits_to_float64(bits, fmt)
+
+
+# ---------------------------------------------------------------------------
+# Exact cases.
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("a_major,b_major", [("K", "K"), ("K", "MN"), ("MN", "K"), ("MN", "MN")])
+@pytest.mark.parametrize("fmt", ["f16", "bf16"])
+def test_integer_inputs_give_the_exact_integer_product(a_major, b_major, fmt):
+    M, N, K = 37, 29, 64
+    A = si.matrix_bits(1, M, K, "int4", fmt, transpose=(a_major == "MN"))
+    B = si.matrix_bits(2, K, N, "int4", fmt, transpose=(b_major == "K"))
+    D, S = G.gemm(M, N, K, A, B, in_fmt=fmt, a_major=a_major, b_major=b_major)
+    Ai = si.logical_values(1, M, K, "int4").astype(np.int64)
+    Bi = si.logical_values(2, K, N, "int4").astype(np.int64)
+    assert np.array_equal(D, (Ai @ Bi).astype(np.float64))
+    assert np.array_equal(S, (np.abs(Ai) @ np.abs(Bi)).astype(np.float64))
+
+
+def test_identity_gives_b_exactly():
+    K = N = 48
+    eye = si.to_storage(np.eye(K), "bf16")
+    B = si.matrix_bits(7, K, N, "uniform", "bf16")
+    D, _ = G.gemm(K, N, K, eye, B, in_fmt="bf16", a_major="K", b_major="MN")
+    assert np.array_equal(D, _vals(B, "bf16"))
+
+
+def test_single_k16_slice_integer():
+    # the K = 16 extent of one kind::f16 MMA
+    M, N, K = 128, 128, 16
+    A = si.matrix_bits(3, M, K, "int4", "f16")
+    B = si.matrix_bits(4, K, N, "int4", "f16", transpose=True)
+    D, _ = G.gemm(M, N, K, A, B, in_fmt="f16", a_major="K", b_major="K")
+    ref = si.logical_values(3, M, K, "int4") @ si.logical_values(4, K, N, "int4")
+    assert np.array_equal(D, ref)
+
+
+def test_hand_case_4x4():
+    # A = [[1,2,0,-1],[0,1,3,0],[2,0,0,1],[-1,1,1,1]], B = [[1,0,2,0],[0,1,0,3],[4,0,1,0],[0,2,0,1]]
+    A = np.array([[1, 2, 0, -1], [0, 1, 3, 0], [2, 0, 0, 1], [-1, 1, 1, 1]], dtype=np.float64)
+    B = np.array([[1, 0, 2, 0], [0, 1, 0, 3], [4, 0, 1, 0], [0, 2, 0, 1]], dtype=np.float64)
+    expect = np.array([[1, 0, 2, 5], [12, 1, 3, 3], [2, 2, 4, 1], [3, 3, -1, 4]], dtype=np.float64)
+    C = np.full((4, 4), 0.5)
+    D, S = G.gemm(4, 4, 4, si.to_storage(A, "f16"), si.to_storage(B, "f16"), in_fmt="f16",
+                  a_major="K", b_major="MN", C=si.to_storage(C, "f32"), c_fmt="f32",
+                  alpha=2.0, beta=-1.0)
+    assert np.array_equal(D, 2.0 * expect - 0.5)
+    assert S[0, 3] == 2.0 * (0 * 0 + 2 * 3 + 0 * 0 + 1 * 1) + 0.5
+
+
+def test_beta_zero_never_reads_c():
+    A = si.matrix_bits(1, 8, 8, "uniform", "bf16")
+    B = si.matrix_bits(2, 8, 8, "uniform", "bf16")
+    nan_c = np.full((8, 8), np.nan)
+    D1, _ = G.gemm(8, 8, 8, A, B, C=si.to_storage(nan_c, "f32"), beta=0.0)
+    D2, _ = G.gemm(8, 8, 8, A, B)
+    assert np.array_equal(D1, D2) and np.isfinite(D1).all()
+
+
+def test_k_zero_is_beta_c():
+    C = si.matrix_bits(9, 5, 6, "uniform", "f32")
+    empty = np.zeros(0, dtype=np.uint16)
+    D, S = G.gemm(5, 6, 0, empty, empty, C=C, c_fmt="f32", alpha=3.0, beta=0.25)
+    assert np.array_equal(D, 0.25 * _vals(C, "f32"))
+
+
+# ---------------------------------------------------------------------------
+# Brute force in exact rationals on tiny inputs; a plausible slip must fail.
+# ---------------------------------------------------------------------------
+
+def _exact(Av, Bv, Cv, alpha, beta):
+    M, K = Av.shape
+    N = Bv.shape[1]
+    out = np.empty((M, N))
+    for i in range(M):
+        for j in range(N):
+            s = sum(Fraction(Av[i, k]) * Fraction(Bv[k, j]) for k in range(K))
+            out[i, j] = float(Fraction(alpha) * s + Fraction(beta) * Fraction(Cv[i, j]))
+    return out
+
+
+@pytest.mark.parametrize("a_major,b_major", [("K", "MN"), ("MN", "K")])
+def test_matches_exact_rationals(a_major, b_major):
+    M, N, K = 5, 7, 9
+    A = si.matrix_bits(11, M, K, "uniform", "bf16", transpose=(a_major == "MN"))
+    B = si.matrix_bits(12, K, N, "normal", "bf16", transpose=(b_major == "K"))
+    C = si.matrix_bits(13, M, N, "uniform", "f32")
+    Av = _vals(si.matrix_bits(11, M, K, "uniform", "bf16"), "bf16")
+    Bv = _vals(si.matrix_bits(12, K, N, "normal", "bf16"), "bf16")
+    Cv = _vals(C, "f32")
+    D, _ = G.gemm(M, N, K, A, B, a_major=a_major, b_major=b_major, C=C, alpha=0.75, beta=-1.5)
+    ex = _exact(Av, Bv, Cv, 0.75, -1.5)
+    assert np.allclose(D, ex, rtol=1e-14, atol=1e-15)
+    Dt, _ = G.gemm(M, N, K, A, B, a_major=a_major, b_major=b_major, C=C, alpha=0.75, beta=1.5)
+    assert not np.allclose(Dt, ex)                  # a sign slip on beta is caught
+
+
+def test_square_transposed_operand_is_caught():
+    n = 16
+    A = si.matrix_bits(21, n, n, "uniform", "bf16")
+    B = si.matrix_bits(22, n, n, "uniform", "bf16")
+    D_k, _ = G.gemm(n, n, n, A, B, a_major="K", b_major="MN")
+    D_t, _ = G.gemm(n, n, n, A, B, a_major="MN", b_major="MN")
+    assert not np.allclose(D_k, D_t)
+    ex = _vals(A, "bf16") @ _vals(B, "bf16")
+    assert np.allclose(D_k, ex, rtol=1e-13)
+
+
+def test_matches_torch_float64_matmul():
+    M, N, K = 70, 90, 130
+    A = si.matrix_bits(31, M, K, "normal", "bf16", scale=0.1)
+    B = si.matrix_bits(32, K, N, "normal", "bf16", scale=0.1, transpose=True)
+    C = si.matrix_bits(33, M, N, "uniform", "f32")
+    D, S = G.gemm(M, N, K, A, B, a_major="K", b_major="K", C=C, alpha=1.25, beta=0.5)
+    At = torch.from_numpy(_vals(A, "bf16"))
+    Bt = torch.from_numpy(_vals(B, "bf16")).T
+    ref = 1.25 * (At @ Bt) + 0.5 * torch.from_numpy(_vals(C, "f32"))
+    assert np.allclose(D, ref.numpy(), rtol=1e-12, atol=1e-12)
+    absref = 1.25 * (At.abs() @ Bt.abs()) + 0.5 * torch.from_numpy(_vals(C, "f32")).abs()
+    assert np.allclose(S, absref.numpy(), rtol=1e-12)
+
+
+def test_entries_match_full_product():
+    M, N, K = 33, 41, 57
+    A = si.matrix_bits(41, M, K, "uniform", "f16", transpose=True)
+    B = si.matrix_bits(42, K, N, "uniform", "f16")
+    C = si.matrix_bits(43, M, N, "uniform", "f16")
+    D, S = G.gemm(M, N, K, A, B, in_fmt="f16", a_major="MN", b_major="MN", C=C, c_fmt="f16",
+                  alpha=-0.5, beta=2.0)
+    rng = np.random.default_rng(0)
+    rows, cols = rng.integers(0, M, 200), rng.integers(0, N, 200)
+    De, Se = G.gemm_entries(M, N, K, A, B, rows, cols, in_fmt="f16", a_major="MN", b_major="MN",
+                            C=C, c_fmt="f16", alpha=-0.5, beta=2.0)
+    assert np.array_equal(De, D[rows, cols]) and np.array_equal(Se, S[rows, cols])
+    with pytest.raises(ValueError):
+        G.gemm_entries(M, N, K, A, B, [M], [0], in_fmt="f16", a_major="MN", b_major="MN")
+
+
+def test_leading_dimensions():
+    M, N, K = 9, 10, 11
+    A = si.matrix_bits(51, M, K, "uniform", "bf16", ld=24)
+    B = si.matrix_bits(52, K, N, "uniform", "bf16", ld=16)
+    C = si.matrix_bits(53, M, N, "uniform", "f32", ld=12)
+    D, _ = G.gemm(M, N, K, A, B, a_major="K", b_major="MN", lda=24, ldb=16, C=C, ldc=12, beta=1.0)
+    ref = _vals(A, "bf16")[:, :K] @ _vals(B, "bf16")[:, :N] + _vals(C, "f32")[:, :N]
+    assert np.allclose(D, ref, rtol=1e-13)
+
+
+# ---------------------------------------------------------------------------
+# Output rounding: round-to-nearest-even in one step.
+# ---------------------------------------------------------------------------
+
+def test_round_f16_and_f32_match_correctly_rounded_casts():
+    rng = np.random.default_rng(1)
+    x = np.concatenate([rng.normal(size=3000) * 10.0 ** rng.integers(-9, 5, 3000),
+                        [0.0, -0.0, 65504.0, 65520.0, 1e6, -1e6, 2.0 ** -24, 2.0 ** -25, 3 * 2.0 ** -26]])
+    r16 = G.round_to(x, "f16")
+    assert np.array_equal(r16, x.astype(np.float16).astype(np.float64))
+    r32 = G.round_to(x, "f32")
+    assert np.array_equal(r32, x.astype(np.float32).astype(np.float64))
+    assert np.array_equal(G.round_bits(x, "f16"), x.astype(np.float16).view(np.uint16))
+    assert np.array_equal(G.round_bits(x, "f32"), x.astype(np.float32).view(np.uint32))
+
+
+def test_round_bf16_ties_and_no_double_rounding():
+    one = 1.0
+    cases = {
+        one + 2.0 ** -8: one,                              # tie -> even (down)
+        one + 3 * 2.0 ** -8: one + 2.0 ** -6,              # tie -> even (up)
+        one + 2.0 ** -8 + 2.0 ** -30: one + 2.0 ** -7,     # just above the tie; via f32 it would tie
+        -(one + 2.0 ** -8 + 2.0 ** -30): -(one + 2.0 ** -7),
+        2.0 ** 127 * (2 - 2.0 ** -8): float("inf"),        # rounds past the largest finite bf16
+        2.0 ** -133: 2.0 ** -133,                          # subnormal, exact
+        3 * 2.0 ** -134: 2.0 ** -132,                      # subnormal tie 1.5 steps -> even (2 steps)
+    }
+    for x, want in cases.items():
+        assert G.round_to(np.array([x]), "bf16")[0] == want, x
+    bits = G.round_bits(np.array([1.0, -2.0, 1.0 + 2.0 ** -7]), "bf16")
+    assert list(bits) == [0x3F80, 0xC000, 0x3F81]
+
+
+def test_ulp_and_tolerance():
+    assert G.ulp(np.array([1.0]), "bf16")[0] == 2.0 ** -7
+    assert G.ulp(np.array([1.0]), "f16")[0] == 2.0 ** -10
+    assert G.ulp(np.array([1.5]), "f32")[0] == 2.0 ** -23
+    assert G.ulp(np.array([0.0]), "f16")[0] == 2.0 ** -24
+    assert G.tolerance(np.array([1000.0]), np.array([1.0]), "bf16")[0] == 1.0 + 2.0 ** -7
