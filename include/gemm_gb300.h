@@ -1,0 +1,222 @@
+/*
+ * gemm_gb300.h -- C ABI of the GB300 (sm_103a) tcgen05 GEMM library.
+ *
+ * The library computes, for fp16 or bf16 inputs with fp32 accumulation,
+ *
+ *     D = alpha * A * B + beta * C
+ *
+ * The product is the tensor-core operation D = A.B + C that the pages build
+ * on ("Tensor Cores, layouts, and swizzling", opening section; "06 Blackwell
+ * Tensor Core - tcgen05 MMA", "Overview" and the K-step walk-through: the
+ * first K step writes the accumulator, later steps add to it). alpha and
+ * beta follow BLAS: beta == 0 never reads C.
+ *
+ * Operand layouts ("LBO, SBO and SWZ for a tcgen05 tile", section 1:
+ * K-major and MN-major operands):
+ *   A is logical M x K.   GEMM_K_MAJOR: A[m*lda + k]  GEMM_MN_MAJOR: A[k*lda + m]
+ *   B is logical K x N.   GEMM_K_MAJOR: B[n*ldb + k]  GEMM_MN_MAJOR: B[k*ldb + n]
+ *   C and D are row-major M x N: C[m*ldc + n], D[m*ldd + n]; C has D's type.
+ *
+ * Ownership: every pointer is a device pointer owned by the caller; the
+ * library allocates no device memory on any call. Calls are asynchronous
+ * on `stream` (a cudaStream_t; NULL is the legacy default stream). A call
+ * that fails validation returns its error at once and enqueues nothing.
+ *
+ * Requirements (TMA rules, "Tensor Cores, layouts, and swizzling", TMA
+ * section: global strides are multiples of 16 bytes and below 2^40):
+ *   - A, B, C, D 16-byte aligned; lda, ldb multiples of 8 elements; ldc and
+ *     ldd multiples of 16 bytes of the output type;
+ *   - M, N, K >= 0, each below 2^31; leading dimensions at least the
+ *     stored row length;
+ *   - M == 0 or N == 0: nothing to do (GEMM_OK). K == 0: D = beta * C.
+ *   - C == D (in place) is allowed; C may be NULL when beta == 0.
+ * Violations return GEMM_ERR_INVALID_ARG or GEMM_ERR_ALIGNMENT.
+ *
+ * Device-side errors: every wait inside the kernels is bounded. A wait that
+ * runs out records a code in a device status word and the kernel returns
+ * early; gemm_last_device_status() reads (and clears) that word.
+ */
+#ifndef GEMM_GB300_H
+#define GEMM_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;                  /* cudaStream_t is struct CUstream_st* */
+typedef struct CUstream_st *gemm_stream_t;
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = 1,        /* bad size, pointer, enum or option */
+    GEMM_ERR_ALIGNMENT = 2,          /* pointer or leading dimension breaks a TMA rule */
+    GEMM_ERR_UNSUPPORTED = 3,        /* valid request this build does not implement */
+    GEMM_ERR_CUDA = 4,               /* a CUDA runtime/driver call failed */
+    GEMM_ERR_TIMEOUT = 5             /* a bounded device wait ran out */
+} gemm_status_t;
+
+typedef enum { GEMM_K_MAJOR = 0, GEMM_MN_MAJOR = 1 } gemm_major_t;
+
+typedef enum { GEMM_OUT_F32 = 0, GEMM_OUT_BF16 = 1, GEMM_OUT_F16 = 2 } gemm_out_t;
+
+/* Shared-memory swizzle of an operand tile ("Swizzling explained properly",
+ * "32B, 64B and 128B swizzles"; raw descriptor codes on the LBO/SBO page,
+ * section 4). GEMM_SWIZZLE_AUTO lets the library choose (SW128). */
+typedef enum {
+    GEMM_SWIZZLE_AUTO = 0,
+    GEMM_SWIZZLE_32B = 1,
+    GEMM_SWIZZLE_64B = 2,
+    GEMM_SWIZZLE_128B = 3
+} gemm_swizzle_t;
+
+/*
+ * Optional tuning/testing knobs (pass NULL for defaults). Every field 0
+ * means "library default".
+ *   cta_group     1: one CTA per 128-row tile (tcgen05.mma.cta_group::1);
+ *                 2: CTA pairs own 256-row tiles (cta_group::2).
+ *   tile_n        MMA N per tile: 64, 128 or 256 (cta_group::2: 256).
+ *   swizzle_a/b   operand swizzle (gemm_swizzle_t).
+ *   epilogue_swizzle  1 (default) stages output tiles in SW128 layout;
+ *                 -1 stages them unswizzled (bank-conflict ablation).
+ *   max_ctas      cap on resident CTAs of the persistent grid.
+ *   group_m       tile-raster group height in tiles (L2 reuse).
+ *   timeout_ms    bound on each device wait (default 2000 ms).
+ */
+typedef struct {
+    int cta_group;
+    int tile_n;
+    int swizzle_a;
+    int swizzle_b;
+    int epilogue_swizzle;
+    int max_ctas;
+    int group_m;
+    int timeout_ms;
+} gemm_options_t;
+
+/* One problem of a grouped call. All share the call's majors, types,
+ * alpha and beta; each has its own sizes, pointers and leading dims. */
+typedef struct {
+    int64_t M, N, K;
+    const void *A;
+    const void *B;
+    const void *C;
+    void *D;
+    int64_t lda, ldb, ldc, ldd;
+} gemm_problem_t;
+
+/*
+ * gemm_bf16 / gemm_f16: one GEMM, inputs bf16 / fp16, fp32 accumulation,
+ * output d_type. Tiles of 128 x tile_n (256 x tile_n for CTA pairs) are
+ * dealt round-robin to a persistent grid of one CTA per SM; operands reach
+ * shared memory by TMA in swizzled layouts, tcgen05.mma accumulates in
+ * Tensor Memory, and a warp-specialised epilogue applies alpha/beta and
+ * stores D by TMA.
+ */
+gemm_status_t gemm_bf16(int64_t M, int64_t N, int64_t K,
+                        const void *A, gemm_major_t a_major, int64_t lda,
+                        const void *B, gemm_major_t b_major, int64_t ldb,
+                        const void *C, int64_t ldc,
+                        void *D, int64_t ldd, gemm_out_t d_type,
+                        float alpha, float beta, gemm_stream_t stream);
+
+gemm_status_t gemm_f16(int64_t M, int64_t N, int64_t K,
+                       const void *A, gemm_major_t a_major, int64_t lda,
+                       const void *B, gemm_major_t b_major, int64_t ldb,
+                       const void *C, int64_t ldc,
+                       void *D, int64_t ldd, gemm_out_t d_type,
+                       float alpha, float beta, gemm_stream_t stream);
+
+/* The same with explicit options (opts may be NULL). in_type: 0 fp16, 1 bf16. */
+gemm_status_t gemm_ex(int in_type, int64_t M, int64_t N, int64_t K,
+                      const void *A, gemm_major_t a_major, int64_t lda,
+                      const void *B, gemm_major_t b_major, int64_t ldb,
+                      const void *C, int64_t ldc,
+                      void *D, int64_t ldd, gemm_out_t d_type,
+                      float alpha, float beta, const gemm_options_t *opts,
+                      gemm_stream_t stream);
+
+/*
+ * Grouped GEMM: num_problems independent problems in one launch. The
+ * host list is read during the call; the library writes the device-side
+ * problem list, one TMA descriptor per operand per problem and the tile
+ * prefix sums into `workspace` (device memory owned by the caller, at
+ * least gemm_grouped_workspace_size(num_problems) bytes, 128-byte
+ * aligned) with an asynchronous copy on `stream`, then launches one
+ * persistent kernel whose scheduler walks the concatenated tile list.
+ * The workspace must stay untouched until the launch completes.
+ */
+size_t gemm_grouped_workspace_size(int num_problems);
+
+gemm_status_t gemm_bf16_grouped(const gemm_problem_t *problems, int num_problems,
+                                gemm_major_t a_major, gemm_major_t b_major,
+                                gemm_out_t d_type, float alpha, float beta,
+                                void *workspace, size_t workspace_bytes,
+                                gemm_stream_t stream);
+
+gemm_status_t gemm_f16_grouped(const gemm_problem_t *problems, int num_problems,
+                               gemm_major_t a_major, gemm_major_t b_major,
+                               gemm_out_t d_type, float alpha, float beta,
+                               void *workspace, size_t workspace_bytes,
+                               gemm_stream_t stream);
+
+/* Synchronises `stream`, reads the device status word of this library,
+ * clears it, and returns GEMM_OK or GEMM_ERR_TIMEOUT (GEMM_ERR_CUDA if the
+ * read fails). `detail` (may be NULL) receives the raw word: bits 0-7 the
+ * role that gave up (1 producer, 2 MMA, 3 epilogue), bits 8-15 the wait. */
+gemm_status_t gemm_last_device_status(gemm_stream_t stream, uint32_t *detail);
+
+const char *gemm_status_string(gemm_status_t status);
+
+/* Number of this library's kernels launched since the library loaded. */
+uint64_t gemm_launch_count(void);
+
+/* ---------------------------------------------------------------------
+ * Inspection entry points (tests): they expose the device-side builders
+ * so their output can be compared bit for bit with an independent model.
+ * ------------------------------------------------------------------- */
+
+/*
+ * Runs the device-side descriptor builder on the GPU and writes, for each
+ * of the n_slices K=16 slices of one operand stage, the 64-bit shared-
+ * memory matrix descriptor the GEMM kernel would hand to tcgen05.mma
+ * ("LBO, SBO and SWZ for a tcgen05 tile", section 3: start, LBO, SBO, MBO
+ * and SWZ fields), followed by the 32-bit instruction descriptor for
+ * (M = 128 * cta_group, N = tile_n, in_type, f32 accumulate, majors) in the
+ * low half of word n_slices. `out` is device memory of n_slices + 1 words.
+ *   major: gemm_major_t of the operand; swizzle: gemm_swizzle_t (not AUTO);
+ *   rows: MN extent of the stage (128 for A; tile_n or tile_n/2 for B);
+ *   bk: K extent of the stage (32 or 64); stage_addr: shared-memory byte
+ *   address of the stage (1024-aligned).
+ */
+gemm_status_t gemm_debug_descriptors(int major, int swizzle, int rows, int bk,
+                                     uint32_t stage_addr, int n_slices,
+                                     int cta_group, int tile_n, int in_type,
+                                     int a_major, int b_major,
+                                     uint64_t *out, gemm_stream_t stream);
+
+/*
+ * Loads one operand stage exactly as the GEMM producer does (TMA boxes in
+ * the given swizzle into a 1024-aligned shared buffer) and copies the raw
+ * shared-memory bytes to `out` (device memory, rows * bk * 2 bytes).
+ *   src: device matrix of 16-bit elements, stored with leading dimension ld
+ *   (K-major: rows_total x K with K contiguous; MN-major: K x rows_total
+ *   with the MN index contiguous); (mn0, k0): the stage's origin.
+ */
+gemm_status_t gemm_debug_stage_image(const void *src, int major, int swizzle,
+                                     int64_t rows_total, int64_t k_total, int64_t ld,
+                                     int rows, int bk, int64_t mn0, int64_t k0,
+                                     void *out, gemm_stream_t stream);
+
+/* Test hook: the next GEMM launch makes its MMA warp wait on a barrier
+ * that nothing arrives at, with a wait bound of `timeout_ms`; every role
+ * then gives up and the kernel exits with GEMM_ERR_TIMEOUT recorded. */
+void gemm_debug_inject_timeout(int timeout_ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_GB300_H */

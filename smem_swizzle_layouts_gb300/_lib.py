@@ -1,0 +1,178 @@
+"""ctypes binding of ``libgemm_gb300.so`` (argument marshalling only).
+
+The names mirror the C ABI in ``include/gemm_gb300.h``. Tensor arguments may
+be torch tensors (their ``data_ptr()`` is passed) or plain integers
+(addresses). ``stream`` may be a ``torch.cuda.Stream``, an integer handle or
+None (torch's current stream). Every non-OK status raises ``GemmError``.
+There is no fallback: if the library is missing, importing this module fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgemm_gb300.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with `python smem_swizzle_layouts_gb300/build.py` "
+        "(or __graft_entry__.build()); there is no CPU fallback")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = range(6)
+K_MAJOR, MN_MAJOR = 0, 1
+OUT_F32, OUT_BF16, OUT_F16 = 0, 1, 2
+SWIZZLE_AUTO, SWIZZLE_32B, SWIZZLE_64B, SWIZZLE_128B = 0, 1, 2, 3
+
+_i64, _vp, _f, _int, _u32, _u64 = (ctypes.c_int64, ctypes.c_void_p, ctypes.c_float, ctypes.c_int,
+                                   ctypes.c_uint32, ctypes.c_uint64)
+
+
+class GemmOptions(ctypes.Structure):
+    _fields_ = [("cta_group", _int), ("tile_n", _int), ("swizzle_a", _int), ("swizzle_b", _int),
+                ("epilogue_swizzle", _int), ("max_ctas", _int), ("group_m", _int),
+                ("timeout_ms", _int)]
+
+
+class GemmProblem(ctypes.Structure):
+    _fields_ = [("M", _i64), ("N", _i64), ("K", _i64), ("A", _vp), ("B", _vp), ("C", _vp),
+                ("D", _vp), ("lda", _i64), ("ldb", _i64), ("ldc", _i64), ("ldd", _i64)]
+
+
+_single = [_i64, _i64, _i64, _vp, _int, _i64, _vp, _int, _i64, _vp, _i64, _vp, _i64, _int, _f, _f, _vp]
+_lib.gemm_bf16.argtypes = _single
+_lib.gemm_f16.argtypes = _single
+_lib.gemm_ex.argtypes = [_int] + _single[:-1] + [ctypes.POINTER(GemmOptions), _vp]
+_grouped = [ctypes.POINTER(GemmProblem), _int, _int, _int, _int, _f, _f, _vp, ctypes.c_size_t, _vp]
+_lib.gemm_bf16_grouped.argtypes = _grouped
+_lib.gemm_f16_grouped.argtypes = _grouped
+_lib.gemm_grouped_workspace_size.argtypes = [_int]
+_lib.gemm_grouped_workspace_size.restype = ctypes.c_size_t
+_lib.gemm_last_device_status.argtypes = [_vp, ctypes.POINTER(_u32)]
+_lib.gemm_status_string.argtypes = [_int]
+_lib.gemm_status_string.restype = ctypes.c_char_p
+_lib.gemm_launch_count.restype = _u64
+_lib.gemm_debug_descriptors.argtypes = [_int, _int, _int, _int, _u32, _int, _int, _int, _int, _int, _int,
+                                        _vp, _vp]
+_lib.gemm_debug_stage_image.argtypes = [_vp, _int, _int, _i64, _i64, _i64, _int, _int, _i64, _i64, _vp, _vp]
+_lib.gemm_debug_inject_timeout.argtypes = [_int]
+_lib.gemm_debug_inject_timeout.restype = None
+for _name in ("gemm_bf16", "gemm_f16", "gemm_ex", "gemm_bf16_grouped", "gemm_f16_grouped",
+              "gemm_last_device_status", "gemm_debug_descriptors", "gemm_debug_stage_image"):
+    getattr(_lib, _name).restype = _int
+
+EXPORTED = ("gemm_bf16", "gemm_f16", "gemm_ex", "gemm_grouped_workspace_size", "gemm_bf16_grouped",
+            "gemm_f16_grouped", "gemm_last_device_status", "gemm_status_string", "gemm_launch_count",
+            "gemm_debug_descriptors", "gemm_debug_stage_image", "gemm_debug_inject_timeout")
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {gemm_status_string(status)} (status {status})")
+
+
+def _addr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(s) -> int | None:
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(status: int, where: str) -> None:
+    if status != OK:
+        raise GemmError(status, where)
+
+
+def _opts(options) -> ctypes.POINTER(GemmOptions) | None:
+    if options is None:
+        return None
+    if isinstance(options, GemmOptions):
+        return ctypes.pointer(options)
+    return ctypes.pointer(GemmOptions(**options))
+
+
+def gemm_status_string(status: int) -> str:
+    return _lib.gemm_status_string(status).decode()
+
+
+def gemm_launch_count() -> int:
+    return int(_lib.gemm_launch_count())
+
+
+def gemm_bf16(M, N, K, A, a_major, lda, B, b_major, ldb, C, ldc, D, ldd, d_type, alpha, beta, stream=None):
+    _check(_lib.gemm_bf16(M, N, K, _addr(A), a_major, lda, _addr(B), b_major, ldb, _addr(C), ldc,
+                          _addr(D), ldd, d_type, alpha, beta, _stream(stream)), "gemm_bf16")
+
+
+def gemm_f16(M, N, K, A, a_major, lda, B, b_major, ldb, C, ldc, D, ldd, d_type, alpha, beta, stream=None):
+    _check(_lib.gemm_f16(M, N, K, _addr(A), a_major, lda, _addr(B), b_major, ldb, _addr(C), ldc,
+                         _addr(D), ldd, d_type, alpha, beta, _stream(stream)), "gemm_f16")
+
+
+def gemm_ex(in_type, M, N, K, A, a_major, lda, B, b_major, ldb, C, ldc, D, ldd, d_type, alpha, beta,
+            options=None, stream=None):
+    _check(_lib.gemm_ex(in_type, M, N, K, _addr(A), a_major, lda, _addr(B), b_major, ldb, _addr(C), ldc,
+                        _addr(D), ldd, d_type, alpha, beta, _opts(options), _stream(stream)), "gemm_ex")
+
+
+def gemm_grouped_workspace_size(num_problems: int) -> int:
+    return int(_lib.gemm_grouped_workspace_size(num_problems))
+
+
+def _problem_array(problems):
+    arr = (GemmProblem * len(problems))()
+    for i, q in enumerate(problems):
+        arr[i] = GemmProblem(q["M"], q["N"], q["K"], _addr(q.get("A")), _addr(q.get("B")),
+                             _addr(q.get("C")), _addr(q.get("D")), q["lda"], q["ldb"], q.get("ldc", 0),
+                             q["ldd"])
+    return arr
+
+
+def gemm_bf16_grouped(problems, a_major, b_major, d_type, alpha, beta, workspace, workspace_bytes,
+                      stream=None):
+    arr = _problem_array(problems)
+    _check(_lib.gemm_bf16_grouped(arr, len(problems), a_major, b_major, d_type, alpha, beta,
+                                  _addr(workspace), workspace_bytes, _stream(stream)), "gemm_bf16_grouped")
+
+
+def gemm_f16_grouped(problems, a_major, b_major, d_type, alpha, beta, workspace, workspace_bytes,
+                     stream=None):
+    arr = _problem_array(problems)
+    _check(_lib.gemm_f16_grouped(arr, len(problems), a_major, b_major, d_type, alpha, beta,
+                                 _addr(workspace), workspace_bytes, _stream(stream)), "gemm_f16_grouped")
+
+
+def gemm_last_device_status(stream=None) -> tuple[int, int]:
+    """(status, raw status word); clears the word."""
+    detail = _u32(0)
+    st = _lib.gemm_last_device_status(_stream(stream), ctypes.byref(detail))
+    return st, int(detail.value)
+
+
+def gemm_debug_descriptors(major, swizzle, rows, bk, stage_addr, n_slices, cta_group, tile_n, in_type,
+                           a_major, b_major, out, stream=None):
+    _check(_lib.gemm_debug_descriptors(major, swizzle, rows, bk, stage_addr, n_slices, cta_group, tile_n,
+                                       in_type, a_major, b_major, _addr(out), _stream(stream)),
+           "gemm_debug_descriptors")
+
+
+def gemm_debug_stage_image(src, major, swizzle, rows_total, k_total, ld, rows, bk, mn0, k0, out, stream=None):
+    _check(_lib.gemm_debug_stage_image(_addr(src), major, swizzle, rows_total, k_total, ld, rows, bk, mn0, k0,
+                                       _addr(out), _stream(stream)), "gemm_debug_stage_image")
+
+
+def gemm_debug_inject_timeout(timeout_ms: int) -> None:
+    _lib.gemm_debug_inject_timeout(timeout_ms)

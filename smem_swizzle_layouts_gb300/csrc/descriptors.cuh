@@ -1,0 +1,99 @@
+// Descriptor builder for tcgen05.mma operands.
+//
+// Shared-memory matrix descriptor ("LBO, SBO and SWZ for a tcgen05 tile",
+// section 3): matrix start, leading-dimension byte offset (LBO) and stride
+// byte offset (SBO) in 16-byte units, matrix base offset (MBO) and the
+// swizzle code as raw 3-bit fields. Bit positions follow the public PTX
+// description of the tcgen05 shared-memory descriptor (the page's field table
+// did not survive): start [0,14), LBO [16,30), SBO [32,46), the fixed value
+// 0b001 at [46,49), MBO [49,52), LBO mode 52, swizzle [61,64).
+//
+// Instruction descriptor for kind::f16 ("06 Blackwell Tensor Core - tcgen05
+// MMA", "How tcgen05.mma Executes": idesc carries M, N, the A/B and D types
+// and the operand majors): D format [4,6), A format [7,10), B format
+// [10,13), A major 15, B major 16, N>>3 at [17,23), M>>4 at [24,29).
+//
+// Operand stage packing (what the producer's TMA boxes build, 1024-aligned):
+//   K-major  (rows x BK): boxes of W/2 K-elements x rows, one after another
+//            along K; each 8-row group of W-byte rows is one swizzle atom.
+//            SBO = 8 W (next 8-row group), LBO unused (encoded 1), and the
+//            K=16 slice j starts at (32 j / W) * rows * W + (32 j mod W).
+//   MN-major (BK x rows): boxes of W/2 MN-elements x BK K-rows, one after
+//            another along MN. LBO = BK W (next MN atom), SBO = 8 W (next
+//            8-row K band), slice j starts at j * 2 * SBO.
+// Stages start on 1024-byte boundaries, so MBO is always 0 (the start of a
+// K slice inside a K-major row moves only bits below 128, page section 3).
+#pragma once
+
+#include <cstdint>
+
+#ifndef G300_HD
+#define G300_HD __host__ __device__ __forceinline__
+#endif
+
+namespace g300 {
+
+// Swizzle "bits" B: 1 = 32 B, 2 = 64 B, 3 = 128 B rows ("Swizzling explained
+// properly": Swizzle<B,4,3>).
+G300_HD uint32_t swizzle_row_bytes(int bits) { return 16u << bits; }
+
+// Raw descriptor code of a swizzle mode (LBO/SBO page, section 4):
+// none 0, SW32 6, SW64 4, SW128 2.
+G300_HD uint32_t swizzle_code(int bits)
+{
+    return bits == 3 ? 2u : bits == 2 ? 4u : bits == 1 ? 6u : 0u;
+}
+
+G300_HD uint64_t make_smem_desc(uint32_t smem_addr, uint32_t lbo_bytes, uint32_t sbo_bytes,
+                                uint32_t swz_code)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;  // fixed 0b001
+    d |= static_cast<uint64_t>(swz_code & 7u) << 61;
+    return d;
+}
+
+struct OperandPacking {
+    uint32_t lbo;
+    uint32_t sbo;
+    uint32_t swz;
+};
+
+G300_HD OperandPacking operand_packing(int mn_major, int swz_bits, int bk)
+{
+    const uint32_t W = swizzle_row_bytes(swz_bits);
+    OperandPacking p;
+    p.lbo = mn_major ? static_cast<uint32_t>(bk) * W : 16u;
+    p.sbo = 8u * W;
+    p.swz = swizzle_code(swz_bits);
+    return p;
+}
+
+// Byte offset of K slice j (16 elements of a 16-bit type) from the stage start.
+G300_HD uint32_t slice_byte_offset(int mn_major, int swz_bits, int rows, int j)
+{
+    const uint32_t W = swizzle_row_bytes(swz_bits);
+    if (mn_major)
+        return static_cast<uint32_t>(j) * 16u * W;
+    const uint32_t off = 32u * static_cast<uint32_t>(j);
+    return (off / W) * static_cast<uint32_t>(rows) * W + off % W;
+}
+
+// kind::f16 instruction descriptor, fp32 accumulator.
+G300_HD uint32_t make_idesc_f16(int M, int N, int in_bf16, int a_mn_major, int b_mn_major)
+{
+    uint32_t d = 0;
+    d |= 1u << 4;  // D format: f32
+    d |= static_cast<uint32_t>(in_bf16 & 1) << 7;
+    d |= static_cast<uint32_t>(in_bf16 & 1) << 10;
+    d |= static_cast<uint32_t>(a_mn_major & 1) << 15;
+    d |= static_cast<uint32_t>(b_mn_major & 1) << 16;
+    d |= static_cast<uint32_t>((N >> 3) & 0x3F) << 17;
+    d |= static_cast<uint32_t>((M >> 4) & 0x1F) << 24;
+    return d;
+}
+
+}  // namespace g300

@@ -1,0 +1,694 @@
+// C ABI of the tcgen05 GEMM library: argument checks, TMA tensor-map
+// encoding, kernel-variant choice and launch. Declarations and contracts are
+// in include/gemm_gb300.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/gemm_gb300.h"
+#include "gemm_kernel.cuh"
+#include "launch.cuh"
+#include "variants.h"
+
+using namespace g300;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// Device status word written by the kernels' bounded waits.
+__device__ unsigned int g_status_word;
+
+std::atomic<uint64_t> g_launches{0};
+std::atomic<int> g_inject_timeout_ms{0};
+
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+unsigned int *g_status_ptr[kMaxDevices] = {};
+int g_sms[kMaxDevices] = {};
+
+struct Variant {
+    int cg, bn, bk, stages;
+    bool grouped;
+    cudaError_t (*launch)(const LaunchArgs &);
+    cudaError_t (*resident)(int *);
+    int resident_cache[kMaxDevices];
+};
+
+#define G300_VARIANT_ROW(CG, BN, BK, ST, GR) \
+    {CG, BN, BK, ST, GR, &launch_gemm<CG, BN, BK, ST, GR>, &resident_ctas<CG, BN, BK, ST, GR>, {0}},
+Variant g_variants[] = {G300_VARIANTS(G300_VARIANT_ROW)};
+#undef G300_VARIANT_ROW
+
+gemm_status_t cuda_fail(cudaError_t e)
+{
+    (void)e;
+    return GEMM_ERR_CUDA;
+}
+
+gemm_status_t device_state(int *dev_out, unsigned int **status_out, int *sms_out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices)
+        return GEMM_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return GEMM_ERR_CUDA;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    if (!g_status_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        g_status_ptr[dev] = static_cast<unsigned int *>(p);
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        g_sms[dev] = sms;
+    }
+    *dev_out = dev;
+    *status_out = g_status_ptr[dev];
+    *sms_out = g_sms[dev];
+    return GEMM_OK;
+}
+
+int resident_for(Variant &v, int dev)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (v.resident_cache[dev] == 0) {
+        int n = 0;
+        if (v.resident(&n) != cudaSuccess || n <= 0)
+            n = -1;
+        v.resident_cache[dev] = n;
+    }
+    return v.resident_cache[dev];
+}
+
+Variant *find_variant(int cg, int bn, int bk, bool grouped)
+{
+    for (auto &v : g_variants)
+        if (v.cg == cg && v.bn == bn && v.bk == bk && v.grouped == grouped)
+            return &v;
+    return nullptr;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int out_bytes(int d_type) { return d_type == GEMM_OUT_F32 ? 4 : 2; }
+
+CUtensorMapDataType out_dtype(int d_type)
+{
+    return d_type == GEMM_OUT_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+           : d_type == GEMM_OUT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+}
+
+CUtensorMapSwizzle tma_swizzle(int bits)
+{
+    return bits == 3 ? CU_TENSOR_MAP_SWIZZLE_128B
+           : bits == 2 ? CU_TENSOR_MAP_SWIZZLE_64B
+           : bits == 1 ? CU_TENSOR_MAP_SWIZZLE_32B
+                       : CU_TENSOR_MAP_SWIZZLE_NONE;
+}
+
+gemm_status_t encode_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *ptr, uint64_t inner,
+                        uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner,
+                        uint32_t box_outer, CUtensorMapSwizzle swz,
+                        CUtensorMapL2promotion l2 = CU_TENSOR_MAP_L2_PROMOTION_L2_256B)
+{
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_stride_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swz, l2, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_INVALID_ARG;
+}
+
+// Operand tile map: boxes of one swizzled row (W/2 elements) along the
+// contiguous dimension, `rows` (K-major) or `bk` (MN-major) along the other.
+gemm_status_t encode_operand(CUtensorMap *m, int in_bf16, const void *ptr, int mn_major,
+                             int swz_bits, int64_t mn_total, int64_t k_total, int64_t ld, int rows,
+                             int bk)
+{
+    const CUtensorMapDataType dt =
+        in_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const uint32_t per = (16u << swz_bits) / 2u;
+    if (!mn_major)
+        return encode_2d(m, dt, ptr, static_cast<uint64_t>(k_total), static_cast<uint64_t>(mn_total),
+                         static_cast<uint64_t>(ld) * 2u, per, static_cast<uint32_t>(rows),
+                         tma_swizzle(swz_bits));
+    return encode_2d(m, dt, ptr, static_cast<uint64_t>(mn_total), static_cast<uint64_t>(k_total),
+                     static_cast<uint64_t>(ld) * 2u, per, static_cast<uint32_t>(bk),
+                     tma_swizzle(swz_bits));
+}
+
+// Output (and C) map: 32-row boxes of 128 bytes.
+gemm_status_t encode_output(CUtensorMap *m, int d_type, const void *ptr, int64_t M, int64_t N,
+                            int64_t ld, int epi_swizzle)
+{
+    const int ob = out_bytes(d_type);
+    return encode_2d(m, out_dtype(d_type), ptr, static_cast<uint64_t>(N), static_cast<uint64_t>(M),
+                     static_cast<uint64_t>(ld) * ob, static_cast<uint32_t>(128 / ob), 32u,
+                     epi_swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_NONE);
+}
+
+struct Plan {
+    int cg, bn, bk;
+    int a_swz, b_swz;
+    int epi_swizzle;
+    int max_ctas;
+    int group_m;
+    unsigned long long timeout_ns;
+};
+
+int swz_bits_of(int opt) { return opt; }  // gemm_swizzle_t 1/2/3 == swizzle bits
+
+// Choose the tile configuration; fills `plan` or returns an error for options
+// this build cannot honour.
+gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int sms,
+                        const gemm_options_t *o, bool grouped, Plan *plan)
+{
+    gemm_options_t opt = {};
+    if (o)
+        opt = *o;
+    if (opt.cta_group < 0 || opt.cta_group > 2 || opt.tile_n < 0 || opt.swizzle_a < 0 ||
+        opt.swizzle_a > 3 || opt.swizzle_b < 0 || opt.swizzle_b > 3 || opt.max_ctas < 0 ||
+        opt.group_m < 0 || opt.timeout_ms < 0 || opt.epilogue_swizzle < -1 ||
+        opt.epilogue_swizzle > 1)
+        return GEMM_ERR_INVALID_ARG;
+
+    int cg = opt.cta_group;
+    if (cg == 0) {
+        // CTA pairs for large problems: each SM then loads half of B.
+        cg = (!grouped && M >= 2048 && N >= 2048) ? 2 : 1;
+    }
+    int bn = opt.tile_n;
+    if (bn == 0) {
+        if (cg == 2) {
+            bn = 256;
+        } else {
+            // largest N tile that does not waste more than a quarter of a tile
+            // on N and still gives every SM a tile when it can
+            const int64_t tiles_m = (M + 127) / 128;
+            int best = 64;
+            double best_score = -1.0;
+            for (int cand : {256, 128, 64}) {
+                const int64_t tn = (N + cand - 1) / cand;
+                const double waste = static_cast<double>(tn * cand) / static_cast<double>(N);
+                const double fill =
+                    std::min<double>(1.0, static_cast<double>(tiles_m * tn) / static_cast<double>(sms));
+                const double score = fill / waste + (cand == 256 ? 0.02 : cand == 128 ? 0.01 : 0.0);
+                if (score > best_score) {
+                    best_score = score;
+                    best = cand;
+                }
+            }
+            bn = best;
+        }
+    }
+    const int bk = (!grouped && cg == 1 && bn == 128 && K <= 32 && opt.tile_n == 0) ? 32 : 64;
+    if (!find_variant(cg, bn, bk, grouped))
+        return GEMM_ERR_UNSUPPORTED;
+
+    auto pick_swz = [&](int requested, int mn_major) -> int {
+        if (requested)
+            return swz_bits_of(requested);
+        if (!mn_major && bk == 32)
+            return 2;  // a 64-byte K row: SW64
+        return 3;
+    };
+    plan->cg = cg;
+    plan->bn = bn;
+    plan->bk = bk;
+    plan->a_swz = pick_swz(opt.swizzle_a, a_mn);
+    plan->b_swz = pick_swz(opt.swizzle_b, b_mn);
+    // a K-major swizzled row may not be wider than the K block; an MN-major
+    // atom may not be wider than the tile's MN extent
+    auto fits = [&](int bits, int mn_major, int rows) {
+        const int per = (16 << bits) / 2;
+        return mn_major ? (rows % per == 0) : (bk % per == 0);
+    };
+    if (!fits(plan->a_swz, a_mn, 128) || !fits(plan->b_swz, b_mn, bn / cg))
+        return GEMM_ERR_UNSUPPORTED;
+    plan->epi_swizzle = opt.epilogue_swizzle == -1 ? 0 : 1;
+    plan->max_ctas = opt.max_ctas;
+    plan->group_m = opt.group_m ? opt.group_m : 8;
+    plan->timeout_ns = static_cast<unsigned long long>(opt.timeout_ms ? opt.timeout_ms : 2000) * 1000000ull;
+    return GEMM_OK;
+}
+
+int grid_for(const Plan &pl, Variant &v, int dev, int sms, int64_t tiles)
+{
+    int cap = resident_for(v, dev);
+    if (cap <= 0)
+        cap = sms;
+    if (pl.max_ctas > 0)
+        cap = std::min(cap, pl.max_ctas);
+    const int64_t per_cluster = pl.cg;
+    int64_t clusters = std::min<int64_t>(tiles, cap / per_cluster);
+    if (clusters < 1)
+        clusters = 1;
+    return static_cast<int>(clusters * per_cluster);
+}
+
+void fill_common(KParams &p, const Plan &pl, int in_bf16, int a_mn, int b_mn, int d_type,
+                 float alpha, float beta, unsigned int *status)
+{
+    p.alpha = alpha;
+    p.beta = beta;
+    p.a_mn = a_mn;
+    p.b_mn = b_mn;
+    p.a_swz = pl.a_swz;
+    p.b_swz = pl.b_swz;
+    p.in_bf16 = in_bf16;
+    p.out_type = d_type;
+    p.epi_swizzle = pl.epi_swizzle;
+    p.group_m = pl.group_m;
+    p.timeout_ns = pl.timeout_ns;
+    p.status = status;
+    const int inj = g_inject_timeout_ms.exchange(0);
+    p.inject_timeout = inj > 0;
+    if (inj > 0)
+        p.timeout_ns = static_cast<unsigned long long>(inj) * 1000000ull;
+}
+
+bool valid_enum(int major) { return major == GEMM_K_MAJOR || major == GEMM_MN_MAJOR; }
+
+// Checks shared by single and grouped problems.
+gemm_status_t check_problem(int64_t M, int64_t N, int64_t K, const void *A, int a_mn, int64_t lda,
+                            const void *B, int b_mn, int64_t ldb, const void *C, int64_t ldc,
+                            const void *D, int64_t ldd, int d_type, float beta)
+{
+    const int64_t lim = (static_cast<int64_t>(1) << 31) - 1;
+    if (M < 0 || N < 0 || K < 0 || M > lim || N > lim || K > lim)
+        return GEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0)
+        return GEMM_OK;
+    const int ob = out_bytes(d_type);
+    if (!D || ldd < N)
+        return GEMM_ERR_INVALID_ARG;
+    if (!aligned16(D) || (ldd * ob) % 16 != 0 || ldd * ob >= (static_cast<int64_t>(1) << 40))
+        return GEMM_ERR_ALIGNMENT;
+    if (K > 0) {
+        if (!A || !B)
+            return GEMM_ERR_INVALID_ARG;
+        if (lda < (a_mn ? M : K) || ldb < (b_mn ? N : K))
+            return GEMM_ERR_INVALID_ARG;
+        if (!aligned16(A) || !aligned16(B) || lda % 8 != 0 || ldb % 8 != 0 ||
+            lda * 2 >= (static_cast<int64_t>(1) << 40) || ldb * 2 >= (static_cast<int64_t>(1) << 40))
+            return GEMM_ERR_ALIGNMENT;
+    }
+    if (beta != 0.0f) {
+        if (!C || ldc < N)
+            return GEMM_ERR_INVALID_ARG;
+        if (!aligned16(C) || (ldc * ob) % 16 != 0 || ldc * ob >= (static_cast<int64_t>(1) << 40))
+            return GEMM_ERR_ALIGNMENT;
+    }
+    return GEMM_OK;
+}
+
+gemm_status_t run_single(int in_bf16, int64_t M, int64_t N, int64_t K, const void *A, int a_major,
+                         int64_t lda, const void *B, int b_major, int64_t ldb, const void *C,
+                         int64_t ldc, void *D, int64_t ldd, int d_type, float alpha, float beta,
+                         const gemm_options_t *opts, cudaStream_t stream)
+{
+    if (!valid_enum(a_major) || !valid_enum(b_major) || d_type < 0 || d_type > 2)
+        return GEMM_ERR_INVALID_ARG;
+    const int a_mn = a_major, b_mn = b_major;
+    gemm_status_t s = check_problem(M, N, K, A, a_mn, lda, B, b_mn, ldb, C, ldc, D, ldd, d_type, beta);
+    if (s != GEMM_OK || M == 0 || N == 0)
+        return s;
+    int dev = 0, sms = 0;
+    unsigned int *status = nullptr;
+    if ((s = device_state(&dev, &status, &sms)) != GEMM_OK)
+        return s;
+    Plan pl;
+    if ((s = make_plan(M, N, K, a_mn, b_mn, sms, opts, false, &pl)) != GEMM_OK)
+        return s;
+    Variant *v = find_variant(pl.cg, pl.bn, pl.bk, false);
+
+    LaunchArgs la;
+    std::memset(&la, 0, sizeof(la));
+    if (K > 0) {
+        if ((s = encode_operand(&la.a, in_bf16, A, a_mn, pl.a_swz, M, K, lda, 128, pl.bk)) != GEMM_OK)
+            return s;
+        if ((s = encode_operand(&la.b, in_bf16, B, b_mn, pl.b_swz, N, K, ldb, pl.bn / pl.cg, pl.bk)) !=
+            GEMM_OK)
+            return s;
+    }
+    if ((s = encode_output(&la.d, d_type, D, M, N, ldd, pl.epi_swizzle)) != GEMM_OK)
+        return s;
+    if (beta != 0.0f) {
+        if ((s = encode_output(&la.c, d_type, C, M, N, ldc, pl.epi_swizzle)) != GEMM_OK)
+            return s;
+    } else {
+        la.c = la.d;
+    }
+    KParams &p = la.p;
+    std::memset(&p, 0, sizeof(p));
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.K = static_cast<int>(K);
+    p.tiles_m = static_cast<int>((M + 128 * pl.cg - 1) / (128 * pl.cg));
+    p.tiles_n = static_cast<int>((N + pl.bn - 1) / pl.bn);
+    const int64_t tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
+    if (tiles >= (static_cast<int64_t>(1) << 31))
+        return GEMM_ERR_UNSUPPORTED;
+    p.num_tiles = static_cast<int>(tiles);
+    fill_common(p, pl, in_bf16, a_mn, b_mn, d_type, alpha, beta, status);
+    la.grid = grid_for(pl, *v, dev, sms, tiles);
+    la.stream = stream;
+    cudaError_t e = v->launch(la);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    g_launches.fetch_add(1);
+    return GEMM_OK;
+}
+
+// Device-side problem table followed by four tensor maps per problem.
+size_t table_bytes(int n) { return (static_cast<size_t>(n) * sizeof(GroupedProblemDev) + 127) & ~size_t(127); }
+
+gemm_status_t run_grouped(int in_bf16, const gemm_problem_t *probs, int n, int a_major, int b_major,
+                          int d_type, float alpha, float beta, void *ws, size_t ws_bytes,
+                          const gemm_options_t *opts, cudaStream_t stream)
+{
+    if (n < 0 || (n > 0 && !probs) || !valid_enum(a_major) || !valid_enum(b_major) || d_type < 0 ||
+        d_type > 2)
+        return GEMM_ERR_INVALID_ARG;
+    if (n == 0)
+        return GEMM_OK;
+    if (!ws || ws_bytes < gemm_grouped_workspace_size(n))
+        return GEMM_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(ws) & 127u) != 0)
+        return GEMM_ERR_ALIGNMENT;
+    const int a_mn = a_major, b_mn = b_major;
+    int64_t maxM = 0, maxN = 0, maxK = 0;
+    for (int i = 0; i < n; ++i) {
+        const gemm_problem_t &q = probs[i];
+        gemm_status_t s = check_problem(q.M, q.N, q.K, q.A, a_mn, q.lda, q.B, b_mn, q.ldb, q.C, q.ldc,
+                                        q.D, q.ldd, d_type, beta);
+        if (s != GEMM_OK)
+            return s;
+        maxM = std::max(maxM, q.M);
+        maxN = std::max(maxN, q.N);
+        maxK = std::max(maxK, q.K);
+    }
+    int dev = 0, sms = 0;
+    unsigned int *status = nullptr;
+    gemm_status_t s = device_state(&dev, &status, &sms);
+    if (s != GEMM_OK)
+        return s;
+    gemm_options_t o = {};
+    if (opts)
+        o = *opts;
+    if (o.tile_n == 0)
+        o.tile_n = (maxN >= 192) ? 256 : 128;
+    if (o.cta_group == 0)
+        o.cta_group = 1;
+    Plan pl;
+    if ((s = make_plan(maxM, maxN, maxK, a_mn, b_mn, sms, &o, true, &pl)) != GEMM_OK)
+        return s;
+    Variant *v = find_variant(pl.cg, pl.bn, pl.bk, true);
+
+    const size_t tb = table_bytes(n);
+    std::vector<unsigned char> host(gemm_grouped_workspace_size(n), 0);
+    auto *table = reinterpret_cast<GroupedProblemDev *>(host.data());
+    auto *maps = reinterpret_cast<CUtensorMap *>(host.data() + tb);
+    int64_t tiles = 0;
+    for (int i = 0; i < n; ++i) {
+        const gemm_problem_t &q = probs[i];
+        GroupedProblemDev &g = table[i];
+        g.M = static_cast<int>(q.M);
+        g.N = static_cast<int>(q.N);
+        g.K = static_cast<int>(q.K);
+        const bool empty = q.M == 0 || q.N == 0;
+        g.tiles_m = empty ? 0 : static_cast<int>((q.M + 128 * pl.cg - 1) / (128 * pl.cg));
+        g.tiles_n = empty ? 0 : static_cast<int>((q.N + pl.bn - 1) / pl.bn);
+        g.tile_start = static_cast<int>(tiles);
+        tiles += static_cast<int64_t>(g.tiles_m) * g.tiles_n;
+        if (tiles >= (static_cast<int64_t>(1) << 31))
+            return GEMM_ERR_UNSUPPORTED;
+        if (empty)
+            continue;
+        CUtensorMap *m = maps + 4 * i;
+        if (q.K > 0) {
+            if ((s = encode_operand(&m[0], in_bf16, q.A, a_mn, pl.a_swz, q.M, q.K, q.lda, 128, pl.bk)) != GEMM_OK)
+                return s;
+            if ((s = encode_operand(&m[1], in_bf16, q.B, b_mn, pl.b_swz, q.N, q.K, q.ldb, pl.bn / pl.cg,
+                                    pl.bk)) != GEMM_OK)
+                return s;
+        }
+        if ((s = encode_output(&m[3], d_type, q.D, q.M, q.N, q.ldd, pl.epi_swizzle)) != GEMM_OK)
+            return s;
+        if (beta != 0.0f) {
+            if ((s = encode_output(&m[2], d_type, q.C, q.M, q.N, q.ldc, pl.epi_swizzle)) != GEMM_OK)
+                return s;
+        } else {
+            m[2] = m[3];
+        }
+    }
+    if (tiles == 0)
+        return GEMM_OK;
+    // pageable source: the copy is staged before this call returns
+    cudaError_t e = cudaMemcpyAsync(ws, host.data(), host.size(), cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+
+    LaunchArgs la;
+    std::memset(&la, 0, sizeof(la));
+    KParams &p = la.p;
+    p.num_tiles = static_cast<int>(tiles);
+    p.problems = reinterpret_cast<const GroupedProblemDev *>(ws);
+    p.maps = reinterpret_cast<const CUtensorMap *>(static_cast<unsigned char *>(ws) + tb);
+    p.num_problems = n;
+    fill_common(p, pl, in_bf16, a_mn, b_mn, d_type, alpha, beta, status);
+    la.grid = grid_for(pl, *v, dev, sms, tiles);
+    la.stream = stream;
+    e = v->launch(la);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    g_launches.fetch_add(1);
+    return GEMM_OK;
+}
+
+// ---------------------------------------------------------------- inspection kernels
+
+__global__ void debug_descriptor_kernel(int major, int swz_bits, int rows, int bk, uint32_t stage_addr,
+                                        int n_slices, int umma_m, int tile_n, int in_bf16, int a_mn,
+                                        int b_mn, uint64_t *out)
+{
+    if (threadIdx.x != 0 || blockIdx.x != 0)
+        return;
+    // the same arithmetic as the MMA role: stage descriptor + slice offset / 16
+    const OperandPacking pk = operand_packing(major, swz_bits, bk);
+    const uint64_t d0 = make_smem_desc(stage_addr, pk.lbo, pk.sbo, pk.swz);
+    for (int j = 0; j < n_slices; ++j)
+        out[j] = d0 + (slice_byte_offset(major, swz_bits, rows, j) >> 4);
+    out[n_slices] = make_idesc_f16(umma_m, tile_n, in_bf16, a_mn, b_mn);
+}
+
+__global__ void debug_stage_kernel(const __grid_constant__ CUtensorMap map, int mn_major, int swz_bits,
+                                   int rows, int bk, int mn0, int k0, uint8_t *out,
+                                   unsigned int *status)
+{
+    extern __shared__ __align__(1024) uint8_t sm_raw[];
+    const uint32_t raw = smem_u32(sm_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t bytes = static_cast<uint32_t>(rows * bk * 2);
+    const uint32_t bar = base + bytes;
+    __shared__ int ok_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+        ok_flag = 0;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx(bar, bytes);
+        load_operand_stage<1>(&map, base, bar, mn_major, swz_bits, rows, bk, mn0, k0);
+        const uint64_t t0 = globaltimer_ns();
+        bool ok = true;
+        while (!mbar_try_wait(bar, 0)) {
+            if (globaltimer_ns() - t0 > 1000000000ull) {
+                ok = false;
+                atomicCAS(status, 0u, kRoleProducer | kWaitFull);
+                break;
+            }
+        }
+        ok_flag = ok ? 1 : 0;
+        if (!ok) {
+            // let the copy land before the CTA can exit
+            const uint64_t t1 = globaltimer_ns();
+            while (globaltimer_ns() - t1 < 20000ull)
+                __nanosleep(1000);
+        }
+    }
+    __syncthreads();
+    if (!ok_flag)
+        return;
+    const uint8_t *src = sm_raw + (base - raw);
+    for (uint32_t i = threadIdx.x * 16u; i < bytes; i += blockDim.x * 16u)
+        *reinterpret_cast<uint4 *>(out + i) = *reinterpret_cast<const uint4 *>(src + i);
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- C ABI
+
+extern "C" {
+
+gemm_status_t gemm_bf16(int64_t M, int64_t N, int64_t K, const void *A, gemm_major_t a_major,
+                        int64_t lda, const void *B, gemm_major_t b_major, int64_t ldb, const void *C,
+                        int64_t ldc, void *D, int64_t ldd, gemm_out_t d_type, float alpha, float beta,
+                        gemm_stream_t stream)
+{
+    return run_single(1, M, N, K, A, a_major, lda, B, b_major, ldb, C, ldc, D, ldd, d_type, alpha, beta,
+                      nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_f16(int64_t M, int64_t N, int64_t K, const void *A, gemm_major_t a_major,
+                       int64_t lda, const void *B, gemm_major_t b_major, int64_t ldb, const void *C,
+                       int64_t ldc, void *D, int64_t ldd, gemm_out_t d_type, float alpha, float beta,
+                       gemm_stream_t stream)
+{
+    return run_single(0, M, N, K, A, a_major, lda, B, b_major, ldb, C, ldc, D, ldd, d_type, alpha, beta,
+                      nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_ex(int in_type, int64_t M, int64_t N, int64_t K, const void *A, gemm_major_t a_major,
+                      int64_t lda, const void *B, gemm_major_t b_major, int64_t ldb, const void *C,
+                      int64_t ldc, void *D, int64_t ldd, gemm_out_t d_type, float alpha, float beta,
+                      const gemm_options_t *opts, gemm_stream_t stream)
+{
+    if (in_type != 0 && in_type != 1)
+        return GEMM_ERR_INVALID_ARG;
+    return run_single(in_type, M, N, K, A, a_major, lda, B, b_major, ldb, C, ldc, D, ldd, d_type, alpha,
+                      beta, opts, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t gemm_grouped_workspace_size(int num_problems)
+{
+    if (num_problems <= 0)
+        return 0;
+    return table_bytes(num_problems) + static_cast<size_t>(num_problems) * 4 * sizeof(CUtensorMap);
+}
+
+gemm_status_t gemm_bf16_grouped(const gemm_problem_t *problems, int num_problems, gemm_major_t a_major,
+                                gemm_major_t b_major, gemm_out_t d_type, float alpha, float beta,
+                                void *workspace, size_t workspace_bytes, gemm_stream_t stream)
+{
+    return run_grouped(1, problems, num_problems, a_major, b_major, d_type, alpha, beta, workspace,
+                       workspace_bytes, nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_f16_grouped(const gemm_problem_t *problems, int num_problems, gemm_major_t a_major,
+                               gemm_major_t b_major, gemm_out_t d_type, float alpha, float beta,
+                               void *workspace, size_t workspace_bytes, gemm_stream_t stream)
+{
+    return run_grouped(0, problems, num_problems, a_major, b_major, d_type, alpha, beta, workspace,
+                       workspace_bytes, nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_last_device_status(gemm_stream_t stream, uint32_t *detail)
+{
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(v)) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    if (v != 0 && cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    if (detail)
+        *detail = v;
+    return v ? GEMM_ERR_TIMEOUT : GEMM_OK;
+}
+
+const char *gemm_status_string(gemm_status_t s)
+{
+    switch (s) {
+    case GEMM_OK: return "ok";
+    case GEMM_ERR_INVALID_ARG: return "invalid argument";
+    case GEMM_ERR_ALIGNMENT: return "pointer or leading dimension breaks a TMA alignment rule";
+    case GEMM_ERR_UNSUPPORTED: return "unsupported configuration";
+    case GEMM_ERR_CUDA: return "CUDA call failed";
+    case GEMM_ERR_TIMEOUT: return "a bounded device wait ran out";
+    }
+    return "unknown status";
+}
+
+uint64_t gemm_launch_count(void) { return g_launches.load(); }
+
+gemm_status_t gemm_debug_descriptors(int major, int swizzle, int rows, int bk, uint32_t stage_addr,
+                                     int n_slices, int cta_group, int tile_n, int in_type, int a_major,
+                                     int b_major, uint64_t *out, gemm_stream_t stream)
+{
+    if (!valid_enum(major) || swizzle < 1 || swizzle > 3 || rows <= 0 || bk <= 0 || n_slices < 0 ||
+        (cta_group != 1 && cta_group != 2) || tile_n <= 0 || !out || (in_type != 0 && in_type != 1) ||
+        !valid_enum(a_major) || !valid_enum(b_major))
+        return GEMM_ERR_INVALID_ARG;
+    debug_descriptor_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        major, swizzle, rows, bk, stage_addr, n_slices, 128 * cta_group, tile_n, in_type, a_major, b_major,
+        out);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    g_launches.fetch_add(1);
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_debug_stage_image(const void *src, int major, int swizzle, int64_t rows_total,
+                                     int64_t k_total, int64_t ld, int rows, int bk, int64_t mn0, int64_t k0,
+                                     void *out, gemm_stream_t stream)
+{
+    if (!src || !out || !valid_enum(major) || swizzle < 1 || swizzle > 3 || rows <= 0 || rows > 256 ||
+        bk <= 0 || bk > 256 || rows_total <= 0 || k_total <= 0 || mn0 < 0 || k0 < 0 ||
+        mn0 > INT32_MAX || k0 > INT32_MAX || rows_total > INT32_MAX || k_total > INT32_MAX)
+        return GEMM_ERR_INVALID_ARG;
+    const int per = (16 << swizzle) / 2;
+    if (major == GEMM_K_MAJOR ? (bk % per != 0) : (rows % per != 0))
+        return GEMM_ERR_UNSUPPORTED;
+    if (ld < (major == GEMM_K_MAJOR ? k_total : rows_total))
+        return GEMM_ERR_INVALID_ARG;
+    // the TMA box's inner coordinate must start on a 16-byte boundary
+    if (!aligned16(src) || !aligned16(out) || ld % 8 != 0 || (major == GEMM_K_MAJOR ? k0 : mn0) % 8 != 0)
+        return GEMM_ERR_ALIGNMENT;
+    int dev = 0, sms = 0;
+    unsigned int *status = nullptr;
+    gemm_status_t s = device_state(&dev, &status, &sms);
+    if (s != GEMM_OK)
+        return s;
+    CUtensorMap map;
+    if ((s = encode_operand(&map, 1, src, major, swizzle, rows_total, k_total, ld, rows, bk)) != GEMM_OK)
+        return s;
+    const int smem = rows * bk * 2 + 1024 + 64;
+    cudaError_t e = cudaFuncSetAttribute(debug_stage_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    debug_stage_kernel<<<1, 128, smem, reinterpret_cast<cudaStream_t>(stream)>>>(
+        map, major, swizzle, rows, bk, static_cast<int>(mn0), static_cast<int>(k0),
+        static_cast<uint8_t *>(out), status);
+    e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    g_launches.fetch_add(1);
+    return GEMM_OK;
+}
+
+void gemm_debug_inject_timeout(int timeout_ms) { g_inject_timeout_ms.store(timeout_ms > 0 ? timeout_ms : 0); }
+
+}  // extern "C"

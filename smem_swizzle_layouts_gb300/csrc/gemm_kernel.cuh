@@ -1,0 +1,679 @@
+// Persistent, warp-specialised tcgen05 GEMM for sm_103a.
+//
+//   D = alpha * A * B + beta * C,  fp16/bf16 in, fp32 accumulate in TMEM.
+//
+// One CTA (cta_group::1) or one CTA pair (cta_group::2, cluster of 2) per
+// SM / SM pair walks a static round-robin list of output tiles. Six warps:
+//   warp 0     TMA producer: one thread fills an S-stage shared-memory ring
+//              (full/empty mbarriers, "Tensor Cores, layouts, and swizzling",
+//              TMA section and 6.6.1: expect_tx bytes, parity (k/S)&1);
+//   warp 1     TMEM allocator and MMA issuer: one thread issues
+//              tcgen05.mma for every K=16 slice and commits completion to
+//              mbarriers ("06 Blackwell Tensor Core - tcgen05 MMA", "How
+//              tcgen05.mma Executes"); the accumulator is double-buffered
+//              in TMEM (2 x BN fp32 columns) so the epilogue of tile i
+//              overlaps the main loop of tile i+1;
+//   warps 2-5  epilogue: warp w reads TMEM lanes 32*(w%4)..+31 (the lane
+//              quarter rule of "Tensor Cores, layouts, and swizzling",
+//              tcgen05 section) with tcgen05.ld, applies alpha/beta against
+//              C (TMA-loaded), converts, stages 32-row chunks in a
+//              swizzled shared-memory buffer and writes them with TMA stores.
+//
+// CTA pairs: the even CTA holds accumulator rows 0-127 and the odd CTA rows
+// 128-255 ("How cta_group Sets the Operation Scope", cta_group::2, M=256).
+// Each CTA TMA-loads its own 128 rows of A and its own half of the tile's N
+// columns of B into its own shared memory (no multicast); completion bytes
+// of both land on the even CTA's full barrier, whose one thread issues the
+// M=256 MMAs and commits their completion to the even CTA's barriers. The
+// even CTA forwards each release to the odd CTA with a remote
+// mbarrier.arrive: its producer, once a stage is free again, and its first
+// epilogue warp, once an accumulator is complete. The odd CTA's epilogue
+// warps release accumulators by remote arrives on the even CTA's barrier.
+//
+// Every mbarrier wait is bounded: past the time limit the waiting role
+// records a code in the status word, raises a CTA-wide abort flag and
+// returns; the kernel then drains in-flight copies and MMAs (with short
+// bounds), frees TMEM and exits.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+#include "descriptors.cuh"
+#include "ptx.cuh"
+
+namespace g300 {
+
+constexpr int kThreads = 192;
+constexpr int kEpiWarps = 4;
+constexpr int kEpiBufBytes = 32 * 128;  // one 32-row x 128 B staging chunk
+
+// Roles in the status word (bits 0-7) and waits (bits 8-15).
+enum : uint32_t {
+    kRoleProducer = 1,
+    kRoleMma = 2,
+    kRoleEpilogue = 3,
+    kWaitEmpty = 1 << 8,
+    kWaitFull = 2 << 8,
+    kWaitAccEmpty = 3 << 8,
+    kWaitAccFull = 4 << 8,
+    kWaitEpiC = 5 << 8,
+    kWaitInjected = 6 << 8,
+    kWaitDrain = 7 << 8,
+};
+
+struct GroupedProblemDev {
+    int M, N, K;
+    int tiles_m, tiles_n;
+    int tile_start;  // first linear tile of this problem
+    int pad0, pad1;
+};
+
+struct KParams {
+    int M, N, K;
+    int tiles_m, tiles_n, num_tiles;
+    float alpha, beta;
+    int a_mn, b_mn;        // 0 K-major, 1 MN-major
+    int a_swz, b_swz;      // swizzle bits: 1 SW32, 2 SW64, 3 SW128
+    int in_bf16;           // 0 fp16, 1 bf16
+    int out_type;          // 0 f32, 1 bf16, 2 f16
+    int epi_swizzle;       // 1: staging chunks in SW128 layout; 0: plain rows
+    int group_m;           // raster group height (tiles)
+    unsigned long long timeout_ns;
+    int inject_timeout;
+    unsigned int *status;
+    const GroupedProblemDev *problems;  // grouped launches only
+    const CUtensorMap *maps;            // [num_problems][4]: A, B, C, D
+    int num_problems;
+};
+
+template <int CG, int BN, int BK, int STAGES>
+struct Cfg {
+    static constexpr int BM = 128;             // accumulator rows per CTA (TMEM lanes)
+    static constexpr int BN_LOCAL = BN / CG;   // B columns loaded by each CTA
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BN_LOCAL * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int TX_BYTES = STAGE_BYTES * CG;  // bytes landing on one full barrier
+    static constexpr int EPI_OFF = STAGES * STAGE_BYTES;
+    static constexpr int EPI_BYTES = kEpiWarps * 2 * kEpiBufBytes;
+    static constexpr int BAR_OFF = EPI_OFF + EPI_BYTES;
+    // full[S], empty[S], acc_full[2], acc_empty[2], epi[4][2], drain, inject
+    static constexpr int NUM_BARS = 2 * STAGES + 2 + 2 + 2 * kEpiWarps + 2;
+    static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
+    static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack to align the base
+    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int UMMA_M = BM * CG;
+    static constexpr int KSLICES = BK / 16;
+    static_assert(STAGE_BYTES % 1024 == 0, "stages must stay 1024-aligned");
+    static_assert(A_BYTES % 1024 == 0, "B tile must start 1024-aligned");
+    static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0,
+                  "TMEM allocation: power of two, 32..512 columns");
+    static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+    static_assert(CG == 1 || BN % 32 == 0, "pair tiles split N in halves of whole atoms");
+};
+
+// ---------------------------------------------------------------- waits
+
+struct Waiter {
+    unsigned long long timeout_ns;
+    volatile uint32_t *abort_flag;
+    unsigned int *status;
+    bool cluster_scope;
+
+    __device__ __forceinline__ bool probe(uint32_t bar, uint32_t parity) const
+    {
+        return cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+    }
+
+    __device__ __forceinline__ void fail(uint32_t code) const
+    {
+        *abort_flag = 1u;
+        atomicCAS(status, 0u, code);
+    }
+
+    // Waits for the phase of parity `parity`; false if it gave up (timeout or abort).
+    __device__ bool wait(uint32_t bar, uint32_t parity, uint32_t code) const
+    {
+        if (probe(bar, parity))
+            return true;
+        const uint64_t t0 = globaltimer_ns();
+        while (true) {
+            for (int i = 0; i < 8; ++i)
+                if (probe(bar, parity))
+                    return true;
+            if (*abort_flag)
+                return false;
+            if (globaltimer_ns() - t0 > timeout_ns) {
+                fail(code);
+                return false;
+            }
+        }
+    }
+
+    // Short wait used while tearing down; never records a code.
+    __device__ bool drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) const
+    {
+        const uint64_t t0 = globaltimer_ns();
+        while (!probe(bar, parity))
+            if (globaltimer_ns() - t0 > limit_ns)
+                return false;
+        return true;
+    }
+};
+
+// ---------------------------------------------------------------- tiles
+
+struct TileInfo {
+    int prob;
+    int m_blk, n_blk;
+    int M, N, K;
+};
+
+template <bool GROUPED>
+__device__ __forceinline__ void decode_tile(const KParams &p, int t, TileInfo &ti)
+{
+    int tiles_m, tiles_n, local;
+    if constexpr (GROUPED) {
+        int lo = 0, hi = p.num_problems - 1;
+        while (lo < hi) {  // last problem whose first tile is <= t
+            const int mid = (lo + hi + 1) >> 1;
+            if (p.problems[mid].tile_start <= t)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        const GroupedProblemDev &g = p.problems[lo];
+        ti.prob = lo;
+        ti.M = g.M;
+        ti.N = g.N;
+        ti.K = g.K;
+        tiles_m = g.tiles_m;
+        tiles_n = g.tiles_n;
+        local = t - g.tile_start;
+    } else {
+        ti.prob = 0;
+        ti.M = p.M;
+        ti.N = p.N;
+        ti.K = p.K;
+        tiles_m = p.tiles_m;
+        tiles_n = p.tiles_n;
+        local = t;
+    }
+    // Raster in groups of group_m tile rows so that CTAs running at the same
+    // time share A row panels and B column panels in L2.
+    const int per_group = p.group_m * tiles_n;
+    const int g = local / per_group;
+    const int first_m = g * p.group_m;
+    const int rows_in_group = min(tiles_m - first_m, p.group_m);
+    const int r = local - g * per_group;
+    ti.m_blk = first_m + r % rows_in_group;
+    ti.n_blk = r / rows_in_group;
+}
+
+// Issue the TMA boxes of one operand stage (see descriptors.cuh for the packing).
+template <int CG>
+__device__ __forceinline__ void load_operand_stage(const CUtensorMap *map, uint32_t dst,
+                                                   uint32_t bar, int mn_major, int swz_bits,
+                                                   int rows, int bk, int mn0, int k0)
+{
+    const int W = 16 << swz_bits;
+    const int per = W / 2;  // 16-bit elements per swizzled row
+    if (!mn_major) {
+        for (int b = 0; b < bk / per; ++b) {
+            if constexpr (CG == 1)
+                tma_load_2d(dst + b * rows * W, map, bar, k0 + b * per, mn0);
+            else
+                tma_load_2d_pair(dst + b * rows * W, map, bar, k0 + b * per, mn0);
+        }
+    } else {
+        for (int b = 0; b < rows / per; ++b) {
+            if constexpr (CG == 1)
+                tma_load_2d(dst + b * bk * W, map, bar, mn0 + b * per, k0);
+            else
+                tma_load_2d_pair(dst + b * bk * W, map, bar, mn0 + b * per, k0);
+        }
+    }
+}
+
+__device__ __forceinline__ int ceil_div_i(int a, int b) { return (a + b - 1) / b; }
+
+// ---------------------------------------------------------------- roles
+
+template <int CG, int BN, int BK, int STAGES, bool GROUPED>
+__device__ void role_producer(const KParams &p, const CUtensorMap *tmA, const CUtensorMap *tmB,
+                              uint32_t smem, uint32_t bar_full, uint32_t bar_empty,
+                              uint32_t rank, const Waiter &w)
+{
+    using C = Cfg<CG, BN, BK, STAGES>;
+    const uint32_t full_target = (CG == 2) ? mapa_shared(bar_full, 0) : bar_full;
+    const uint32_t peer_empty = (CG == 2 && rank == 0) ? mapa_shared(bar_empty, 1) : 0u;
+    const int cluster_id = blockIdx.x / CG, num_clusters = gridDim.x / CG;
+    int stage = 0;
+    uint32_t phase = 0;
+    int issued = 0;
+    bool ok = true;
+    int last_prob = -1;
+    for (int t = cluster_id; t < p.num_tiles && ok; t += num_clusters) {
+        TileInfo ti;
+        decode_tile<GROUPED>(p, t, ti);
+        const CUtensorMap *mA = tmA, *mB = tmB;
+        if constexpr (GROUPED) {
+            mA = p.maps + 4 * ti.prob;
+            mB = mA + 1;
+            if (ti.prob != last_prob) {
+                fence_tensormap_acquire(mA);
+                fence_tensormap_acquire(mB);
+                last_prob = ti.prob;
+            }
+        }
+        const int num_kb = ceil_div_i(ti.K, BK);
+        const int m0 = ti.m_blk * C::UMMA_M + C::BM * static_cast<int>(rank);
+        const int n0 = ti.n_blk * BN + C::BN_LOCAL * static_cast<int>(rank);
+        for (int kb = 0; kb < num_kb; ++kb) {
+            if (!w.wait(bar_empty + 8 * stage, phase ^ 1u, kRoleProducer | kWaitEmpty)) {
+                ok = false;
+                break;
+            }
+            // pass a real release (not the first trip round the ring) on to the odd CTA
+            if (CG == 2 && rank == 0 && issued >= STAGES)
+                mbar_arrive_cluster(peer_empty + 8 * stage);
+            if (rank == 0)
+                mbar_arrive_expect_tx(bar_full + 8 * stage, C::TX_BYTES);
+            const uint32_t sA = smem + stage * C::STAGE_BYTES;
+            const uint32_t fb = full_target + 8 * stage;
+            load_operand_stage<CG>(mA, sA, fb, p.a_mn, p.a_swz, C::BM, BK, m0, kb * BK);
+            load_operand_stage<CG>(mB, sA + C::A_BYTES, fb, p.b_mn, p.b_swz, C::BN_LOCAL, BK, n0,
+                                   kb * BK);
+            ++issued;
+            if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+    if (!ok && CG == 1) {
+        // Let the loads still in flight land before the CTA can exit.
+        const int n = issued < STAGES ? issued : STAGES;
+        for (int i = 1; i <= n; ++i) {
+            int s = stage - i, ph = static_cast<int>(phase);
+            if (s < 0) {
+                s += STAGES;
+                ph ^= 1;
+            }
+            w.drain(bar_full + 8 * s, static_cast<uint32_t>(ph), 20000000ull);
+        }
+    }
+}
+
+template <int CG, int BN, int BK, int STAGES, bool GROUPED>
+__device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uint32_t bar_empty,
+                         uint32_t bar_acc_full, uint32_t bar_acc_empty, uint32_t bar_inject,
+                         uint32_t tmem_base, const Waiter &w)
+{
+    using C = Cfg<CG, BN, BK, STAGES>;
+    if (p.inject_timeout) {
+        // Test hook: wait on a barrier nothing arrives at; the bound runs out.
+        w.wait(bar_inject, 0u, kRoleMma | kWaitInjected);
+        return;
+    }
+    const uint32_t idesc = make_idesc_f16(C::UMMA_M, BN, p.in_bf16, p.a_mn, p.b_mn);
+    const OperandPacking pa = operand_packing(p.a_mn, p.a_swz, BK);
+    const OperandPacking pb = operand_packing(p.b_mn, p.b_swz, BK);
+    const uint64_t a_desc0 = make_smem_desc(smem, pa.lbo, pa.sbo, pa.swz);
+    const uint64_t b_desc0 = make_smem_desc(smem + C::A_BYTES, pb.lbo, pb.sbo, pb.swz);
+    uint32_t a_off[C::KSLICES], b_off[C::KSLICES];
+#pragma unroll
+    for (int j = 0; j < C::KSLICES; ++j) {
+        a_off[j] = slice_byte_offset(p.a_mn, p.a_swz, C::BM, j) >> 4;
+        b_off[j] = slice_byte_offset(p.b_mn, p.b_swz, C::BN_LOCAL, j) >> 4;
+    }
+    const int cluster_id = blockIdx.x / CG, num_clusters = gridDim.x / CG;
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
+        TileInfo ti;
+        decode_tile<GROUPED>(p, t, ti);
+        const int num_kb = ceil_div_i(ti.K, BK);
+        if (num_kb == 0)
+            continue;  // K == 0: the epilogue writes beta * C without the accumulator
+        if (!w.wait(bar_acc_empty + 8 * acc, acc_phase ^ 1u, kRoleMma | kWaitAccEmpty))
+            return;
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < num_kb; ++kb) {
+            if (!w.wait(bar_full + 8 * stage, phase, kRoleMma | kWaitFull))
+                return;
+            tc_fence_after_sync();
+            const uint64_t sdelta = static_cast<uint64_t>((stage * C::STAGE_BYTES) >> 4);
+#pragma unroll
+            for (int j = 0; j < C::KSLICES; ++j)
+                mma_f16<CG>(d_tmem, a_desc0 + sdelta + a_off[j], b_desc0 + sdelta + b_off[j], idesc,
+                            (kb | j) != 0);
+            mma_commit<CG>(bar_empty + 8 * stage);
+            if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        mma_commit<CG>(bar_acc_full + 8 * acc);
+        acc ^= 1;
+        if (acc == 0)
+            acc_phase ^= 1u;
+    }
+}
+
+// Convert 8 fp32 values to a 16-byte chunk of the output type.
+__device__ __forceinline__ void pack_out(const float *v, int out_type, uint32_t (&o)[4])
+{
+    if (out_type == 1) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+            o[i] = *reinterpret_cast<uint32_t *>(&h);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __half2 h = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+            o[i] = *reinterpret_cast<uint32_t *>(&h);
+        }
+    }
+}
+
+__device__ __forceinline__ void unpack_in(const uint32_t (&c)[4], int out_type, float *v)
+{
+    if (out_type == 1) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162 *>(&c[i]);
+            float2 f = __bfloat1622float2(h);
+            v[2 * i] = f.x;
+            v[2 * i + 1] = f.y;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __half2 h = *reinterpret_cast<const __half2 *>(&c[i]);
+            float2 f = __half22float2(h);
+            v[2 * i] = f.x;
+            v[2 * i + 1] = f.y;
+        }
+    }
+}
+
+// One 32-row x 128-byte chunk: fp32 output covers 32 columns, 16-bit output 64.
+// `acc` holds this thread's row (lane) of the chunk in fp32.
+template <int CW>
+__device__ __forceinline__ void epilogue_chunk_math(float (&acc)[CW], const KParams &p,
+                                                    uint32_t sbuf, int lane, bool use_c)
+{
+    const uint32_t row = sbuf + static_cast<uint32_t>(lane) * 128u;
+    const uint32_t key = p.epi_swizzle ? static_cast<uint32_t>(lane & 7) : 0u;
+    constexpr int PER16 = (CW == 32) ? 4 : 8;  // elements per 16-byte unit
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const uint32_t addr = row + ((static_cast<uint32_t>(u) ^ key) << 4);
+        float *v = acc + u * PER16;
+#pragma unroll
+        for (int e = 0; e < PER16; ++e)
+            v[e] *= p.alpha;
+        if (use_c) {
+            uint32_t c[4];
+            ld_shared_v4(addr, c[0], c[1], c[2], c[3]);
+            if constexpr (CW == 32) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    v[e] = fmaf(p.beta, __uint_as_float(c[e]), v[e]);
+            } else {
+                float cf[8];
+                unpack_in(c, p.out_type, cf);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    v[e] = fmaf(p.beta, cf[e], v[e]);
+            }
+        }
+        uint32_t o[4];
+        if constexpr (CW == 32) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                o[e] = __float_as_uint(v[e]);
+        } else {
+            pack_out(v, p.out_type, o);
+        }
+        st_shared_v4(addr, o[0], o[1], o[2], o[3]);
+    }
+}
+
+template <int CG, int BN, int BK, int STAGES, bool GROUPED, int CW>
+__device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CUtensorMap *tmD,
+                              uint32_t epi_base, uint32_t bar_acc_full, uint32_t bar_acc_empty,
+                              uint32_t bar_epi, uint32_t tmem_base, uint32_t rank, int warp,
+                              int lane, const Waiter &w)
+{
+    using C = Cfg<CG, BN, BK, STAGES>;
+    const int q = warp & 3;   // TMEM lane quarter = accumulator rows 32q..32q+31
+    const int ew = warp - 2;  // staging slot
+    const uint32_t buf0 = epi_base + static_cast<uint32_t>(ew * 2 * kEpiBufBytes);
+    const uint32_t ebar0 = bar_epi + static_cast<uint32_t>(16 * ew);
+    const bool use_c = p.beta != 0.0f;
+    const uint32_t acc_empty_target = (CG == 2) ? mapa_shared(bar_acc_empty, 0) : bar_acc_empty;
+    const uint32_t peer_acc_full = (CG == 2 && rank == 0) ? mapa_shared(bar_acc_full, 1) : 0u;
+    const int cluster_id = blockIdx.x / CG, num_clusters = gridDim.x / CG;
+    uint32_t epi_phase[2] = {0u, 0u};
+    int sel = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
+        TileInfo ti;
+        decode_tile<GROUPED>(p, t, ti);
+        const CUtensorMap *mC = tmC, *mD = tmD;
+        if constexpr (GROUPED) {
+            mC = p.maps + 4 * ti.prob + 2;
+            mD = mC + 1;
+            fence_tensormap_acquire(mC);
+            fence_tensormap_acquire(mD);
+        }
+        const bool has_acc = ti.K > 0;
+        const int m0 = ti.m_blk * C::UMMA_M + C::BM * static_cast<int>(rank) + 32 * q;
+        if (has_acc) {
+            bool ok = w.wait(bar_acc_full + 8 * acc, acc_phase, kRoleEpilogue | kWaitAccFull);
+            if (!__all_sync(0xffffffffu, ok))
+                return;
+            if (CG == 2 && rank == 0 && ew == 0 && lane == 0)
+                mbar_arrive_cluster(peer_acc_full + 8 * acc);  // the odd CTA's half is complete too
+            tc_fence_after_sync();
+        }
+        for (int c = 0; c < BN / CW; ++c) {
+            const int col0 = ti.n_blk * BN + c * CW;
+            if (col0 >= ti.N)
+                break;
+            const uint32_t sbuf = buf0 + static_cast<uint32_t>(sel * kEpiBufBytes);
+            const uint32_t sbar = ebar0 + static_cast<uint32_t>(8 * sel);
+            // the store issued from this buffer two chunks ago must have read it
+            if (lane == 0)
+                bulk_wait_group_read<1>();
+            __syncwarp();
+            if (use_c && lane == 0) {
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(sbar, kEpiBufBytes);
+                tma_load_2d(sbuf, mC, sbar, col0, m0);
+            }
+            __syncwarp();  // tcgen05.ld is .sync.aligned: the warp must be converged
+            float v[CW];
+            if (has_acc) {
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
+                                       static_cast<uint32_t>(acc * BN + c * CW);
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(taddr, r);
+                if constexpr (CW == 64) {
+                    uint32_t r2[32];
+                    tmem_ld_32x32b_x32(taddr + 32, r2);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        v[i] = __uint_as_float(r[i]);
+                        v[32 + i] = __uint_as_float(r2[i]);
+                    }
+                } else {
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        v[i] = __uint_as_float(r[i]);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < CW; ++i)
+                    v[i] = 0.0f;
+            }
+            if (use_c) {
+                bool ok = w.wait(sbar, epi_phase[sel], kRoleEpilogue | kWaitEpiC);
+                epi_phase[sel] ^= 1u;
+                if (!__all_sync(0xffffffffu, ok))
+                    return;
+            }
+            epilogue_chunk_math<CW>(v, p, sbuf, lane, use_c);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_2d(mD, sbuf, col0, m0);
+                bulk_commit_group();
+            }
+            sel ^= 1;
+        }
+        if (has_acc) {
+            // all tcgen05.ld of this accumulator have completed (wait::ld above)
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+                if constexpr (CG == 2)
+                    mbar_arrive_cluster(acc_empty_target + 8 * acc);
+                else
+                    mbar_arrive(bar_acc_empty + 8 * acc);
+            }
+            acc ^= 1;
+            if (acc == 0)
+                acc_phase ^= 1u;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- kernel
+
+template <int CG, int BN, int BK, int STAGES, bool GROUPED>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmC,
+                        const __grid_constant__ CUtensorMap tmD, const __grid_constant__ KParams p)
+{
+    using C = Cfg<CG, BN, BK, STAGES>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (base - raw);
+
+    const int warp = static_cast<int>(threadIdx.x >> 5);
+    const int lane = static_cast<int>(threadIdx.x & 31);
+    uint32_t rank = 0;
+    if constexpr (CG == 2)
+        rank = cluster_ctarank() & 1u;
+
+    const uint32_t bar_full = base + C::BAR_OFF;
+    const uint32_t bar_empty = bar_full + 8 * STAGES;
+    const uint32_t bar_acc_full = bar_empty + 8 * STAGES;
+    const uint32_t bar_acc_empty = bar_acc_full + 16;
+    const uint32_t bar_epi = bar_acc_empty + 16;
+    const uint32_t bar_drain = bar_epi + 8 * 2 * kEpiWarps;
+    const uint32_t bar_inject = bar_drain + 8;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + C::MISC_OFF + 4);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar_acc_full + 8 * b, 1);
+            mbar_init(bar_acc_empty + 8 * b, kEpiWarps * CG);
+        }
+        for (int i = 0; i < 2 * kEpiWarps; ++i)
+            mbar_init(bar_epi + 8 * i, 1);
+        mbar_init(bar_drain, 1);
+        mbar_init(bar_inject, 1);
+        *abort_flag = 0u;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0 && !GROUPED) {
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+        prefetch_tensormap(&tmD);
+    }
+    if (warp == 1) {
+        tmem_alloc<CG>(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish<CG>();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if constexpr (CG == 2)
+        cluster_sync_all();  // the peer's barriers exist before anything signals them
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    Waiter w;
+    w.timeout_ns = p.timeout_ns;
+    w.abort_flag = abort_flag;
+    w.status = p.status;
+    w.cluster_scope = (CG == 2);
+
+    const uint32_t stage_base = base;
+    if (warp == 0) {
+        if (lane == 0)
+            role_producer<CG, BN, BK, STAGES, GROUPED>(p, &tmA, &tmB, stage_base, bar_full,
+                                                       bar_empty, rank, w);
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) {
+            role_mma<CG, BN, BK, STAGES, GROUPED>(p, stage_base, bar_full, bar_empty,
+                                                  bar_acc_full, bar_acc_empty, bar_inject,
+                                                  tmem_base, w);
+            // every MMA issued by this thread has completed before TMEM is freed
+            mma_commit<CG>(bar_drain);
+            w.drain(bar_drain, 0u, 100000000ull);
+        }
+    } else {
+        if (p.out_type == 0)
+            role_epilogue<CG, BN, BK, STAGES, GROUPED, 32>(p, &tmC, &tmD, base + C::EPI_OFF,
+                                                           bar_acc_full, bar_acc_empty, bar_epi,
+                                                           tmem_base, rank, warp, lane, w);
+        else
+            role_epilogue<CG, BN, BK, STAGES, GROUPED, 64>(p, &tmC, &tmD, base + C::EPI_OFF,
+                                                           bar_acc_full, bar_acc_empty, bar_epi,
+                                                           tmem_base, rank, warp, lane, w);
+        if (lane == 0)
+            bulk_wait_group<0>();  // stores have finished reading shared memory
+    }
+    __syncwarp();
+
+    if (*abort_flag) {
+        // give copies and MMAs still in flight time to land before teardown
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 20000ull)
+            __nanosleep(1000);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if constexpr (CG == 2)
+        cluster_sync_all();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc<CG>(tmem_base, C::TMEM_COLS);
+    }
+}
+
+}  // namespace g300

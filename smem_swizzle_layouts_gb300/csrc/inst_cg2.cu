@@ -1,0 +1,4 @@
+// Instantiations: CTA pairs on 256-row tiles (tcgen05 cta_group::2), single problem.
+#include "launch.cuh"
+
+G300_INSTANTIATE(2, 256, 64, 6, false)

@@ -1,0 +1,28 @@
+// The compiled kernel variants (tile shape, pipeline depth, CTA pairing).
+#pragma once
+
+#include <cuda_runtime.h>
+
+namespace g300 {
+
+struct LaunchArgs;
+
+template <int CG, int BN, int BK, int STAGES, bool GROUPED>
+cudaError_t launch_gemm(const LaunchArgs &a);
+
+template <int CG, int BN, int BK, int STAGES, bool GROUPED>
+cudaError_t resident_ctas(int *ctas);
+
+// X(cta_group, BN, BK, stages, grouped). BN is the MMA N of one tile;
+// stages fill ~192 KB of shared memory next to 32 KB of epilogue staging.
+#define G300_VARIANTS(X)        \
+    X(1, 256, 64, 4, false)     \
+    X(1, 128, 64, 6, false)     \
+    X(1, 64, 64, 8, false)      \
+    X(1, 128, 32, 8, false)     \
+    X(2, 256, 64, 6, false)     \
+    X(1, 256, 64, 4, true)      \
+    X(1, 128, 64, 6, true)      \
+    X(2, 256, 64, 6, true)
+
+}  // namespace g300
