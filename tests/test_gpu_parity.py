@@ -43,15 +43,20 @@ def _out_bits(t, fmt):
     return a.view(torch.int16).numpy().view(np.uint16)
 
 
+def _ru(x, m):
+    return max(m, (x + m - 1) // m * m)
+
+
 def run_case(g, M, N, K, *, in_fmt="bf16", a_major="K", b_major="K", out="f32", alpha=1.0, beta=0.0,
              dist="uniform", scale=1.0, seed=0, pad=0, options=None, inplace=False, exact=False,
              sample=None):
     """Run one GEMM through the C ABI and compare with the oracle; returns max |err|."""
     if options and options.get("cta_group") == 2 and os.environ.get("GEMM_TEST_NO_PAIRS"):
         pytest.skip("CTA-pair cases disabled for this run")
-    lda = (K if a_major == "K" else M) + pad
-    ldb = (K if b_major == "K" else N) + pad
-    ldd = N + (pad if out == "f32" else 2 * pad)
+    # leading dimensions rounded up to the 16-byte TMA stride rule, plus optional padding
+    lda = _ru(K if a_major == "K" else M, 8) + pad
+    ldb = _ru(K if b_major == "K" else N, 8) + pad
+    ldd = _ru(N, 4 if out == "f32" else 8) + pad
     A = si.matrix_bits(seed, M, K, dist, in_fmt, scale=scale, transpose=(a_major == "MN"), ld=lda)
     B = si.matrix_bits(seed + 1, K, N, dist, in_fmt, scale=scale, transpose=(b_major == "K"), ld=ldb)
     C = si.matrix_bits(seed + 2, M, N, dist, out, scale=scale, ld=ldd) if beta != 0.0 else None
@@ -305,17 +310,18 @@ def test_config4_skinny(g, M, N, K):
 def _grouped(g, Ms, N, K, *, out="bf16", a_major="K", b_major="K", alpha=1.0, beta=0.0, seed=40,
              dist="uniform", sample=None, options=None):
     probs, host = [], []
+    ldd = _ru(N, 4 if out == "f32" else 8)
     for i, M in enumerate(Ms):
-        lda = K if a_major == "K" else M
-        ldb = K if b_major == "K" else N
-        A = si.matrix_bits(seed + 3 * i, M, K, dist, "bf16", transpose=(a_major == "MN"))
-        B = si.matrix_bits(seed + 3 * i + 1, K, N, dist, "bf16", transpose=(b_major == "K"))
-        C = si.matrix_bits(seed + 3 * i + 2, M, N, dist, out) if beta != 0.0 else None
+        lda = _ru(K if a_major == "K" else M, 8)
+        ldb = _ru(K if b_major == "K" else N, 8)
+        A = si.matrix_bits(seed + 3 * i, M, K, dist, "bf16", transpose=(a_major == "MN"), ld=lda)
+        B = si.matrix_bits(seed + 3 * i + 1, K, N, dist, "bf16", transpose=(b_major == "K"), ld=ldb)
+        C = si.matrix_bits(seed + 3 * i + 2, M, N, dist, out, ld=ldd) if beta != 0.0 else None
         At, Bt = _to_dev(A, "bf16"), _to_dev(B, "bf16")
         Ct = _to_dev(C, out) if C is not None else None
-        Dt = torch.full((max(M, 1), N), float("nan"), dtype=TDT[out], device=DEV)
-        probs.append(dict(M=M, N=N, K=K, A=At, B=Bt, C=Ct, D=Dt, lda=max(lda, 8), ldb=max(ldb, 8),
-                          ldc=N if C is not None else 0, ldd=N))
+        Dt = torch.full((max(M, 1), ldd), float("nan"), dtype=TDT[out], device=DEV)
+        probs.append(dict(M=M, N=N, K=K, A=At, B=Bt, C=Ct, D=Dt, lda=lda, ldb=ldb,
+                          ldc=ldd if C is not None else 0, ldd=ldd))
         host.append((A, B, C, Dt, lda, ldb))
     ws_bytes = g.gemm_grouped_workspace_size(len(Ms))
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=DEV)
@@ -326,8 +332,8 @@ def _grouped(g, Ms, N, K, *, out="bf16", a_major="K", b_major="K", alpha=1.0, be
     for i, (M, (A, B, C, Dt, lda, ldb)) in enumerate(zip(Ms, host)):
         if M == 0:
             continue
-        got = si.bits_to_float64(_out_bits(Dt, out), out)
-        kw = dict(in_fmt="bf16", a_major=a_major, b_major=b_major, lda=lda, ldb=ldb, C=C, c_fmt=out, ldc=N,
+        got = si.bits_to_float64(_out_bits(Dt, out)[:, :N], out)
+        kw = dict(in_fmt="bf16", a_major=a_major, b_major=b_major, lda=lda, ldb=ldb, C=C, c_fmt=out, ldc=ldd,
                   alpha=alpha, beta=beta)
         if sample:
             r, c = sample_entries(M, N, n=256, seed=i)
