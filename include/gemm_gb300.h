@@ -78,22 +78,37 @@ typedef enum {
  *   cta_group     1: one CTA per 128-row tile (tcgen05.mma.cta_group::1);
  *                 2: CTA pairs own 256-row tiles (cta_group::2).
  *   tile_n        MMA N per tile: 64, 128 or 256 (cta_group::2: 256).
+ *   block_k       K elements per pipeline stage: 32, 64 or 128 where built.
  *   swizzle_a/b   operand swizzle (gemm_swizzle_t).
  *   epilogue_swizzle  1 (default) stages output tiles in SW128 layout;
  *                 -1 stages them unswizzled (bank-conflict ablation).
  *   max_ctas      cap on resident CTAs of the persistent grid.
  *   group_m       tile-raster group height in tiles (L2 reuse).
  *   timeout_ms    bound on each device wait (default 2000 ms).
+ *   flags         tuning switches. CTA pairs signal stage and accumulator
+ *                 releases to both CTAs with one multicast tcgen05.commit;
+ *                 bit 0 instead forwards them from the even CTA with remote
+ *                 mbarrier arrives (ablation), bit 1 makes every wait
+ *                 acquire at cluster scope (ablation). Bit 2 starts each
+ *                 tile's K loop at a per-CTA offset so that CTAs sharing an
+ *                 operand panel read different parts of it at a time.
+ *   stats         diagnostics: NULL, or device memory of 16 uint64 per CTA
+ *                 of the grid (at least 16 * number of SMs), where each CTA
+ *                 writes cycles its roles spent waiting (slots 0-1 producer,
+ *                 2-4 and 8-9 MMA issuer, 5-7 first epilogue warp).
  */
 typedef struct {
     int cta_group;
     int tile_n;
+    int block_k;
     int swizzle_a;
     int swizzle_b;
     int epilogue_swizzle;
     int max_ctas;
     int group_m;
     int timeout_ms;
+    int flags;
+    unsigned long long *stats;
 } gemm_options_t;
 
 /* One problem of a grouped call. All share the call's majors, types,

@@ -174,6 +174,8 @@ struct Plan {
     int max_ctas;
     int group_m;
     unsigned long long timeout_ns;
+    int flags;
+    unsigned long long *stats;
 };
 
 int swz_bits_of(int opt) { return opt; }  // gemm_swizzle_t 1/2/3 == swizzle bits
@@ -189,7 +191,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
     if (opt.cta_group < 0 || opt.cta_group > 2 || opt.tile_n < 0 || opt.swizzle_a < 0 ||
         opt.swizzle_a > 3 || opt.swizzle_b < 0 || opt.swizzle_b > 3 || opt.max_ctas < 0 ||
         opt.group_m < 0 || opt.timeout_ms < 0 || opt.epilogue_swizzle < -1 ||
-        opt.epilogue_swizzle > 1)
+        opt.epilogue_swizzle > 1 || opt.flags < 0 || opt.flags > 7 || opt.block_k < 0)
         return GEMM_ERR_INVALID_ARG;
 
     int cg = opt.cta_group;
@@ -221,7 +223,16 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
             bn = best;
         }
     }
-    const int bk = (!grouped && cg == 1 && bn == 128 && K <= 32 && opt.tile_n == 0) ? 32 : 64;
+    // K block per stage: the per-stage cost of a TMA refill is nearly fixed, so
+    // the deepest stages that still leave three of them in flight win; the
+    // 128 x 256 single-CTA tile keeps BK = 64 to hold four stages.
+    int bk = opt.block_k;
+    if (bk == 0) {
+        if (!grouped && cg == 1 && bn == 128 && K <= 32 && opt.tile_n == 0)
+            bk = 32;
+        else
+            bk = (cg == 1 && bn == 256) ? 64 : 128;
+    }
     if (!find_variant(cg, bn, bk, grouped))
         return GEMM_ERR_UNSUPPORTED;
 
@@ -249,6 +260,8 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
     plan->max_ctas = opt.max_ctas;
     plan->group_m = opt.group_m ? opt.group_m : 8;
     plan->timeout_ns = static_cast<unsigned long long>(opt.timeout_ms ? opt.timeout_ms : 2000) * 1000000ull;
+    plan->flags = opt.flags;
+    plan->stats = opt.stats;
     return GEMM_OK;
 }
 
@@ -280,6 +293,8 @@ void fill_common(KParams &p, const Plan &pl, int in_bf16, int a_mn, int b_mn, in
     p.epi_swizzle = pl.epi_swizzle;
     p.group_m = pl.group_m;
     p.timeout_ns = pl.timeout_ns;
+    p.flags = pl.flags;
+    p.stats = pl.stats;
     p.status = status;
     const int inj = g_inject_timeout_ms.exchange(0);
     p.inject_timeout = inj > 0;

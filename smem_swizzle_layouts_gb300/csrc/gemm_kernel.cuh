@@ -88,7 +88,41 @@ struct KParams {
     const GroupedProblemDev *problems;  // grouped launches only
     const CUtensorMap *maps;            // [num_problems][4]: A, B, C, D
     int num_problems;
+    int flags;                  // kFlag* tuning switches
+    unsigned long long *stats;  // optional per-CTA wait counters (kStat* slots), or null
 };
+
+// Diagnostics: per-CTA counters written when KParams::stats is set.
+enum : int {
+    kStatProducerWaitCycles = 0,
+    kStatProducerBlocked = 1,
+    kStatMmaFullWaitCycles = 2,
+    kStatMmaAccEmptyWaitCycles = 3,
+    kStatMmaLoopCycles = 4,
+    kStatEpiAccFullWaitCycles = 5,
+    kStatEpiCWaitCycles = 6,
+    kStatEpiLoopCycles = 7,
+    kStatMmaFullBlocked = 8,
+    kStatTiles = 9,
+    kStatSlots = 16,
+};
+
+enum : int {
+    kFlagPairForward = 1,      // CTA pairs: forward releases with remote arrives (ablation)
+    kFlagAllClusterWaits = 2,  // CTA pairs: cluster-scope acquire on every wait (ablation)
+    kFlagRotateK = 4,          // start each tile's K loop at a per-cluster offset
+};
+
+// K block processed at iteration `it` of a tile: with kFlagRotateK the
+// cluster starts at its own offset, so CTAs that share an operand panel do not
+// all read the same K block of it at the same moment.
+__device__ __forceinline__ int kblock_at(int it, int num_kb, int flags, int cluster_id)
+{
+    if (!(flags & kFlagRotateK))
+        return it;
+    const int r = it + (cluster_id * 7) % num_kb;
+    return r >= num_kb ? r - num_kb : r;
+}
 
 template <int CG, int BN, int BK, int STAGES>
 struct Cfg {
@@ -122,11 +156,12 @@ struct Waiter {
     unsigned long long timeout_ns;
     volatile uint32_t *abort_flag;
     unsigned int *status;
-    bool cluster_scope;
+    bool all_cluster_scope;  // tuning flag: cluster-scope acquire on every wait
 
-    __device__ __forceinline__ bool probe(uint32_t bar, uint32_t parity) const
+    __device__ __forceinline__ bool probe(uint32_t bar, uint32_t parity, bool cluster) const
     {
-        return cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+        return (cluster || all_cluster_scope) ? mbar_try_wait_cluster(bar, parity)
+                                              : mbar_try_wait(bar, parity);
     }
 
     __device__ __forceinline__ void fail(uint32_t code) const
@@ -136,14 +171,16 @@ struct Waiter {
     }
 
     // Waits for the phase of parity `parity`; false if it gave up (timeout or abort).
-    __device__ bool wait(uint32_t bar, uint32_t parity, uint32_t code) const
+    // `cluster`: the phase is completed by an arrive from another CTA of the
+    // cluster, so the wait acquires at cluster scope.
+    __device__ bool wait(uint32_t bar, uint32_t parity, uint32_t code, bool cluster = false) const
     {
-        if (probe(bar, parity))
+        if (probe(bar, parity, cluster))
             return true;
         const uint64_t t0 = globaltimer_ns();
         while (true) {
             for (int i = 0; i < 8; ++i)
-                if (probe(bar, parity))
+                if (probe(bar, parity, cluster))
                     return true;
             if (*abort_flag)
                 return false;
@@ -158,7 +195,7 @@ struct Waiter {
     __device__ bool drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) const
     {
         const uint64_t t0 = globaltimer_ns();
-        while (!probe(bar, parity))
+        while (!probe(bar, parity, true))
             if (globaltimer_ns() - t0 > limit_ns)
                 return false;
         return true;
@@ -166,6 +203,35 @@ struct Waiter {
 };
 
 // ---------------------------------------------------------------- tiles
+//
+// Kernel parameters live in the __grid_constant__ parameter block. Every
+// inline-asm statement below clobbers "memory", so any field read through
+// `p` inside a loop would be reloaded after each asm; the roles therefore
+// copy what they need into registers once, before their loops.
+
+struct Sched {
+    int num_tiles;
+    int M, N, K;
+    int tiles_m, tiles_n;
+    int group_m;
+    int num_problems;
+    const GroupedProblemDev *problems;
+};
+
+__device__ __forceinline__ Sched make_sched(const KParams &p)
+{
+    Sched s;
+    s.num_tiles = p.num_tiles;
+    s.M = p.M;
+    s.N = p.N;
+    s.K = p.K;
+    s.tiles_m = p.tiles_m;
+    s.tiles_n = p.tiles_n;
+    s.group_m = p.group_m;
+    s.num_problems = p.num_problems;
+    s.problems = p.problems;
+    return s;
+}
 
 struct TileInfo {
     int prob;
@@ -174,7 +240,7 @@ struct TileInfo {
 };
 
 template <bool GROUPED>
-__device__ __forceinline__ void decode_tile(const KParams &p, int t, TileInfo &ti)
+__device__ __forceinline__ void decode_tile(const Sched &p, int t, TileInfo &ti)
 {
     int tiles_m, tiles_n, local;
     if constexpr (GROUPED) {
@@ -186,7 +252,7 @@ __device__ __forceinline__ void decode_tile(const KParams &p, int t, TileInfo &t
             else
                 hi = mid - 1;
         }
-        const GroupedProblemDev &g = p.problems[lo];
+        const GroupedProblemDev g = p.problems[lo];
         ti.prob = lo;
         ti.M = g.M;
         ti.N = g.N;
@@ -214,29 +280,55 @@ __device__ __forceinline__ void decode_tile(const KParams &p, int t, TileInfo &t
     ti.n_blk = r / rows_in_group;
 }
 
-// Issue the TMA boxes of one operand stage (see descriptors.cuh for the packing).
+// Geometry of the TMA boxes that fill one operand of a stage (the packing of
+// descriptors.cuh): box b lands at dst + b * smem_step and starts at
+// (k0 + b * k_step, mn0) for K-major operands or (mn0 + b * mn_step, k0) for
+// MN-major ones.
+struct OperandBoxes {
+    int nbox;
+    uint32_t smem_step;
+    int step;
+    int mn_major;
+};
+
+__device__ __forceinline__ OperandBoxes operand_boxes(int mn_major, int swz_bits, int rows, int bk)
+{
+    const int W = 16 << swz_bits;
+    const int per = W / 2;  // 16-bit elements per swizzled row
+    OperandBoxes o;
+    o.mn_major = mn_major;
+    o.step = per;
+    if (!mn_major) {
+        o.nbox = bk / per;
+        o.smem_step = static_cast<uint32_t>(rows * W);
+    } else {
+        o.nbox = rows / per;
+        o.smem_step = static_cast<uint32_t>(bk * W);
+    }
+    return o;
+}
+
+template <int CG>
+__device__ __forceinline__ void issue_box(const CUtensorMap *map, uint32_t dst, uint32_t bar,
+                                          const OperandBoxes &o, int b, int mn0, int k0)
+{
+    const int x = o.mn_major ? mn0 + b * o.step : k0 + b * o.step;
+    const int y = o.mn_major ? k0 : mn0;
+    if constexpr (CG == 1)
+        tma_load_2d(dst + static_cast<uint32_t>(b) * o.smem_step, map, bar, x, y);
+    else
+        tma_load_2d_pair(dst + static_cast<uint32_t>(b) * o.smem_step, map, bar, x, y);
+}
+
+// Issue every TMA box of one operand stage (used by the inspection kernel).
 template <int CG>
 __device__ __forceinline__ void load_operand_stage(const CUtensorMap *map, uint32_t dst,
                                                    uint32_t bar, int mn_major, int swz_bits,
                                                    int rows, int bk, int mn0, int k0)
 {
-    const int W = 16 << swz_bits;
-    const int per = W / 2;  // 16-bit elements per swizzled row
-    if (!mn_major) {
-        for (int b = 0; b < bk / per; ++b) {
-            if constexpr (CG == 1)
-                tma_load_2d(dst + b * rows * W, map, bar, k0 + b * per, mn0);
-            else
-                tma_load_2d_pair(dst + b * rows * W, map, bar, k0 + b * per, mn0);
-        }
-    } else {
-        for (int b = 0; b < rows / per; ++b) {
-            if constexpr (CG == 1)
-                tma_load_2d(dst + b * bk * W, map, bar, mn0 + b * per, k0);
-            else
-                tma_load_2d_pair(dst + b * bk * W, map, bar, mn0 + b * per, k0);
-        }
-    }
+    const OperandBoxes o = operand_boxes(mn_major, swz_bits, rows, bk);
+    for (int b = 0; b < o.nbox; ++b)
+        issue_box<CG>(map, dst, bar, o, b, mn0, k0);
 }
 
 __device__ __forceinline__ int ceil_div_i(int a, int b) { return (a + b - 1) / b; }
@@ -249,6 +341,15 @@ __device__ void role_producer(const KParams &p, const CUtensorMap *tmA, const CU
                               uint32_t rank, const Waiter &w)
 {
     using C = Cfg<CG, BN, BK, STAGES>;
+    const Sched sched = make_sched(p);
+    const int flags = p.flags;
+    unsigned long long *const stats = p.stats;
+    const CUtensorMap *const maps = p.maps;
+    const OperandBoxes boxA = operand_boxes(p.a_mn, p.a_swz, C::BM, BK);
+    const OperandBoxes boxB = operand_boxes(p.b_mn, p.b_swz, C::BN_LOCAL, BK);
+    const int nbox = boxA.nbox > boxB.nbox ? boxA.nbox : boxB.nbox;
+    const bool forward = CG == 2 && rank == 0 && (flags & kFlagPairForward);
+
     const uint32_t full_target = (CG == 2) ? mapa_shared(bar_full, 0) : bar_full;
     const uint32_t peer_empty = (CG == 2 && rank == 0) ? mapa_shared(bar_empty, 1) : 0u;
     const int cluster_id = blockIdx.x / CG, num_clusters = gridDim.x / CG;
@@ -257,12 +358,13 @@ __device__ void role_producer(const KParams &p, const CUtensorMap *tmA, const CU
     int issued = 0;
     bool ok = true;
     int last_prob = -1;
-    for (int t = cluster_id; t < p.num_tiles && ok; t += num_clusters) {
+    unsigned long long st_wait = 0, st_blocked = 0;
+    for (int t = cluster_id; t < sched.num_tiles && ok; t += num_clusters) {
         TileInfo ti;
-        decode_tile<GROUPED>(p, t, ti);
+        decode_tile<GROUPED>(sched, t, ti);
         const CUtensorMap *mA = tmA, *mB = tmB;
         if constexpr (GROUPED) {
-            mA = p.maps + 4 * ti.prob;
+            mA = maps + 4 * ti.prob;
             mB = mA + 1;
             if (ti.prob != last_prob) {
                 fence_tensormap_acquire(mA);
@@ -274,26 +376,43 @@ __device__ void role_producer(const KParams &p, const CUtensorMap *tmA, const CU
         const int m0 = ti.m_blk * C::UMMA_M + C::BM * static_cast<int>(rank);
         const int n0 = ti.n_blk * BN + C::BN_LOCAL * static_cast<int>(rank);
         for (int kb = 0; kb < num_kb; ++kb) {
-            if (!w.wait(bar_empty + 8 * stage, phase ^ 1u, kRoleProducer | kWaitEmpty)) {
-                ok = false;
-                break;
+            if (stats) {
+                const long long t0 = clock64();
+                const bool ready = mbar_try_wait(bar_empty + 8 * stage, phase ^ 1u);
+                ok = ready || w.wait(bar_empty + 8 * stage, phase ^ 1u, kRoleProducer | kWaitEmpty, rank != 0);
+                st_wait += static_cast<unsigned long long>(clock64() - t0);
+                st_blocked += ready ? 0 : 1;
+            } else {
+                ok = w.wait(bar_empty + 8 * stage, phase ^ 1u, kRoleProducer | kWaitEmpty, rank != 0);
             }
+            if (!ok)
+                break;
             // pass a real release (not the first trip round the ring) on to the odd CTA
-            if (CG == 2 && rank == 0 && issued >= STAGES)
+            if (forward && issued >= STAGES)
                 mbar_arrive_cluster(peer_empty + 8 * stage);
             if (rank == 0)
                 mbar_arrive_expect_tx(bar_full + 8 * stage, C::TX_BYTES);
             const uint32_t sA = smem + stage * C::STAGE_BYTES;
+            const uint32_t sB = sA + C::A_BYTES;
             const uint32_t fb = full_target + 8 * stage;
-            load_operand_stage<CG>(mA, sA, fb, p.a_mn, p.a_swz, C::BM, BK, m0, kb * BK);
-            load_operand_stage<CG>(mB, sA + C::A_BYTES, fb, p.b_mn, p.b_swz, C::BN_LOCAL, BK, n0,
-                                   kb * BK);
+            const int k0 = kblock_at(kb, num_kb, flags, cluster_id) * BK;
+            // A and B boxes alternate, so both operands of the stage are in flight together
+            for (int b = 0; b < nbox; ++b) {
+                if (b < boxA.nbox)
+                    issue_box<CG>(mA, sA, fb, boxA, b, m0, k0);
+                if (b < boxB.nbox)
+                    issue_box<CG>(mB, sB, fb, boxB, b, n0, k0);
+            }
             ++issued;
             if (++stage == STAGES) {
                 stage = 0;
                 phase ^= 1u;
             }
         }
+    }
+    if (stats) {
+        stats[blockIdx.x * kStatSlots + kStatProducerWaitCycles] = st_wait;
+        stats[blockIdx.x * kStatSlots + kStatProducerBlocked] = st_blocked;
     }
     if (!ok && CG == 1) {
         // Let the loads still in flight land before the CTA can exit.
@@ -320,6 +439,9 @@ __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uin
         w.wait(bar_inject, 0u, kRoleMma | kWaitInjected);
         return;
     }
+    const Sched sched = make_sched(p);
+    unsigned long long *const stats = p.stats;
+    const bool multicast = CG == 2 && !(p.flags & kFlagPairForward);
     const uint32_t idesc = make_idesc_f16(C::UMMA_M, BN, p.in_bf16, p.a_mn, p.b_mn);
     const OperandPacking pa = operand_packing(p.a_mn, p.a_swz, BK);
     const OperandPacking pb = operand_packing(p.b_mn, p.b_swz, BK);
@@ -336,35 +458,65 @@ __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uin
     uint32_t phase = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
+    unsigned long long st_full = 0, st_acc = 0, st_blocked = 0, st_tiles = 0;
+    const long long t_start = clock64();
+    for (int t = cluster_id; t < sched.num_tiles; t += num_clusters) {
         TileInfo ti;
-        decode_tile<GROUPED>(p, t, ti);
+        decode_tile<GROUPED>(sched, t, ti);
         const int num_kb = ceil_div_i(ti.K, BK);
         if (num_kb == 0)
             continue;  // K == 0: the epilogue writes beta * C without the accumulator
-        if (!w.wait(bar_acc_empty + 8 * acc, acc_phase ^ 1u, kRoleMma | kWaitAccEmpty))
-            return;
+        {
+            const long long t0 = stats ? clock64() : 0;
+            if (!w.wait(bar_acc_empty + 8 * acc, acc_phase ^ 1u, kRoleMma | kWaitAccEmpty, CG == 2))
+                return;
+            if (stats)
+                st_acc += static_cast<unsigned long long>(clock64() - t0);
+            ++st_tiles;
+        }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         for (int kb = 0; kb < num_kb; ++kb) {
-            if (!w.wait(bar_full + 8 * stage, phase, kRoleMma | kWaitFull))
+            if (stats) {
+                const long long t0 = clock64();
+                const bool ready = mbar_try_wait(bar_full + 8 * stage, phase);
+                if (!ready && !w.wait(bar_full + 8 * stage, phase, kRoleMma | kWaitFull))
+                    return;
+                st_full += static_cast<unsigned long long>(clock64() - t0);
+                st_blocked += ready ? 0 : 1;
+            } else if (!w.wait(bar_full + 8 * stage, phase, kRoleMma | kWaitFull)) {
                 return;
+            }
             tc_fence_after_sync();
             const uint64_t sdelta = static_cast<uint64_t>((stage * C::STAGE_BYTES) >> 4);
 #pragma unroll
             for (int j = 0; j < C::KSLICES; ++j)
                 mma_f16<CG>(d_tmem, a_desc0 + sdelta + a_off[j], b_desc0 + sdelta + b_off[j], idesc,
                             (kb | j) != 0);
-            mma_commit<CG>(bar_empty + 8 * stage);
+            if (multicast)
+                mma_commit_pair_multicast(bar_empty + 8 * stage);
+            else
+                mma_commit<CG>(bar_empty + 8 * stage);
             if (++stage == STAGES) {
                 stage = 0;
                 phase ^= 1u;
             }
         }
-        mma_commit<CG>(bar_acc_full + 8 * acc);
+        if (multicast)
+            mma_commit_pair_multicast(bar_acc_full + 8 * acc);
+        else
+            mma_commit<CG>(bar_acc_full + 8 * acc);
         acc ^= 1;
         if (acc == 0)
             acc_phase ^= 1u;
+    }
+    if (stats) {
+        unsigned long long *o = stats + blockIdx.x * kStatSlots;
+        o[kStatMmaFullWaitCycles] = st_full;
+        o[kStatMmaAccEmptyWaitCycles] = st_acc;
+        o[kStatMmaLoopCycles] = static_cast<unsigned long long>(clock64() - t_start);
+        o[kStatMmaFullBlocked] = st_blocked;
+        o[kStatTiles] = st_tiles;
     }
 }
 
@@ -407,44 +559,50 @@ __device__ __forceinline__ void unpack_in(const uint32_t (&c)[4], int out_type, 
     }
 }
 
+struct EpiConst {
+    float alpha, beta;
+    int out_type;
+    uint32_t key_mask;  // 7 when staging rows are SW128-swizzled, else 0
+};
+
 // One 32-row x 128-byte chunk: fp32 output covers 32 columns, 16-bit output 64.
 // `acc` holds this thread's row (lane) of the chunk in fp32.
 template <int CW>
-__device__ __forceinline__ void epilogue_chunk_math(float (&acc)[CW], const KParams &p,
+__device__ __forceinline__ void epilogue_chunk_math(float (&acc)[CW], const EpiConst &e,
                                                     uint32_t sbuf, int lane, bool use_c)
 {
     const uint32_t row = sbuf + static_cast<uint32_t>(lane) * 128u;
-    const uint32_t key = p.epi_swizzle ? static_cast<uint32_t>(lane & 7) : 0u;
+    const uint32_t key = static_cast<uint32_t>(lane) & e.key_mask;
     constexpr int PER16 = (CW == 32) ? 4 : 8;  // elements per 16-byte unit
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
         const uint32_t addr = row + ((static_cast<uint32_t>(u) ^ key) << 4);
         float *v = acc + u * PER16;
 #pragma unroll
-        for (int e = 0; e < PER16; ++e)
-            v[e] *= p.alpha;
+        for (int i = 0; i < PER16; ++i)
+            v[i] *= e.alpha;
         if (use_c) {
             uint32_t c[4];
             ld_shared_v4(addr, c[0], c[1], c[2], c[3]);
             if constexpr (CW == 32) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    v[e] = fmaf(p.beta, __uint_as_float(c[e]), v[e]);
+                for (int i = 0; i < 4; ++i)
+                    v[i] = fmaf(e.beta, __uint_as_float(c[i]), v[i]);
             } else {
                 float cf[8];
-                unpack_in(c, p.out_type, cf);
+                unpack_in(c, e.out_type, cf);
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    v[e] = fmaf(p.beta, cf[e], v[e]);
+                for (int i = 0; i < 8; ++i)
+                    v[i] = fmaf(e.beta, cf[i], v[i]);
             }
         }
         uint32_t o[4];
         if constexpr (CW == 32) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                o[e] = __float_as_uint(v[e]);
+            for (int i = 0; i < 4; ++i)
+                o[i] = __float_as_uint(v[i]);
         } else {
-            pack_out(v, p.out_type, o);
+            pack_out(v, e.out_type, o);
         }
         st_shared_v4(addr, o[0], o[1], o[2], o[3]);
     }
@@ -457,11 +615,20 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
                               int lane, const Waiter &w)
 {
     using C = Cfg<CG, BN, BK, STAGES>;
+    const Sched sched = make_sched(p);
+    unsigned long long *const stats = p.stats;
+    const CUtensorMap *const maps = p.maps;
+    EpiConst ec;
+    ec.alpha = p.alpha;
+    ec.beta = p.beta;
+    ec.out_type = p.out_type;
+    ec.key_mask = p.epi_swizzle ? 7u : 0u;
+    const bool forward = CG == 2 && rank == 0 && (p.flags & kFlagPairForward);
     const int q = warp & 3;   // TMEM lane quarter = accumulator rows 32q..32q+31
     const int ew = warp - 2;  // staging slot
     const uint32_t buf0 = epi_base + static_cast<uint32_t>(ew * 2 * kEpiBufBytes);
     const uint32_t ebar0 = bar_epi + static_cast<uint32_t>(16 * ew);
-    const bool use_c = p.beta != 0.0f;
+    const bool use_c = ec.beta != 0.0f;
     const uint32_t acc_empty_target = (CG == 2) ? mapa_shared(bar_acc_empty, 0) : bar_acc_empty;
     const uint32_t peer_acc_full = (CG == 2 && rank == 0) ? mapa_shared(bar_acc_full, 1) : 0u;
     const int cluster_id = blockIdx.x / CG, num_clusters = gridDim.x / CG;
@@ -469,12 +636,14 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
     int sel = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
+    unsigned long long st_accw = 0, st_cw = 0;
+    const long long t_start = clock64();
+    for (int t = cluster_id; t < sched.num_tiles; t += num_clusters) {
         TileInfo ti;
-        decode_tile<GROUPED>(p, t, ti);
+        decode_tile<GROUPED>(sched, t, ti);
         const CUtensorMap *mC = tmC, *mD = tmD;
         if constexpr (GROUPED) {
-            mC = p.maps + 4 * ti.prob + 2;
+            mC = maps + 4 * ti.prob + 2;
             mD = mC + 1;
             fence_tensormap_acquire(mC);
             fence_tensormap_acquire(mD);
@@ -482,10 +651,13 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
         const bool has_acc = ti.K > 0;
         const int m0 = ti.m_blk * C::UMMA_M + C::BM * static_cast<int>(rank) + 32 * q;
         if (has_acc) {
-            bool ok = w.wait(bar_acc_full + 8 * acc, acc_phase, kRoleEpilogue | kWaitAccFull);
+            const long long tw = stats ? clock64() : 0;
+            bool ok = w.wait(bar_acc_full + 8 * acc, acc_phase, kRoleEpilogue | kWaitAccFull, rank != 0);
+            if (stats)
+                st_accw += static_cast<unsigned long long>(clock64() - tw);
             if (!__all_sync(0xffffffffu, ok))
                 return;
-            if (CG == 2 && rank == 0 && ew == 0 && lane == 0)
+            if (forward && ew == 0 && lane == 0)
                 mbar_arrive_cluster(peer_acc_full + 8 * acc);  // the odd CTA's half is complete too
             tc_fence_after_sync();
         }
@@ -532,12 +704,15 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
                     v[i] = 0.0f;
             }
             if (use_c) {
+                const long long tw = stats ? clock64() : 0;
                 bool ok = w.wait(sbar, epi_phase[sel], kRoleEpilogue | kWaitEpiC);
+                if (stats)
+                    st_cw += static_cast<unsigned long long>(clock64() - tw);
                 epi_phase[sel] ^= 1u;
                 if (!__all_sync(0xffffffffu, ok))
                     return;
             }
-            epilogue_chunk_math<CW>(v, p, sbuf, lane, use_c);
+            epilogue_chunk_math<CW>(v, ec, sbuf, lane, use_c);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -560,6 +735,12 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
             if (acc == 0)
                 acc_phase ^= 1u;
         }
+    }
+    if (stats && ew == 0 && lane == 0) {
+        unsigned long long *o = stats + blockIdx.x * kStatSlots;
+        o[kStatEpiAccFullWaitCycles] = st_accw;
+        o[kStatEpiCWaitCycles] = st_cw;
+        o[kStatEpiLoopCycles] = static_cast<unsigned long long>(clock64() - t_start);
     }
 }
 
@@ -630,7 +811,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     w.timeout_ns = p.timeout_ns;
     w.abort_flag = abort_flag;
     w.status = p.status;
-    w.cluster_scope = (CG == 2);
+    w.all_cluster_scope = (CG == 2) && (p.flags & kFlagAllClusterWaits);
 
     const uint32_t stage_base = base;
     if (warp == 0) {

@@ -3,5 +3,7 @@
 
 G300_INSTANTIATE(1, 256, 64, 4, false)
 G300_INSTANTIATE(1, 128, 64, 6, false)
+G300_INSTANTIATE(1, 128, 128, 3, false)
 G300_INSTANTIATE(1, 64, 64, 8, false)
+G300_INSTANTIATE(1, 64, 128, 4, false)
 G300_INSTANTIATE(1, 128, 32, 8, false)

@@ -2,3 +2,4 @@
 #include "launch.cuh"
 
 G300_INSTANTIATE(2, 256, 64, 6, false)
+G300_INSTANTIATE(2, 256, 128, 3, false)

@@ -2,5 +2,5 @@
 #include "launch.cuh"
 
 G300_INSTANTIATE(1, 256, 64, 4, true)
-G300_INSTANTIATE(1, 128, 64, 6, true)
-G300_INSTANTIATE(2, 256, 64, 6, true)
+G300_INSTANTIATE(1, 128, 128, 3, true)
+G300_INSTANTIATE(2, 256, 128, 3, true)

@@ -249,6 +249,17 @@ __device__ __forceinline__ void mma_commit(uint32_t bar)
                      : "memory");
 }
 
+// CTA pairs: arrive once on the barrier at the same shared-memory offset in
+// both CTAs of the pair (cluster ranks 0 and 1) when this thread's tcgen05
+// operations have completed.
+__device__ __forceinline__ void mma_commit_pair_multicast(uint32_t bar)
+{
+    asm volatile("{\n\t.reg .b16 m;\n\tmov.b16 m, 3;\n\t"
+                 "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+                 " [%0], m;\n\t}" ::"r"(bar)
+                 : "memory");
+}
+
 // 32 lanes x 32 consecutive 32-bit columns: thread t gets lane (base lane + t).
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32])
 {

@@ -18,11 +18,14 @@ cudaError_t resident_ctas(int *ctas);
 #define G300_VARIANTS(X)        \
     X(1, 256, 64, 4, false)     \
     X(1, 128, 64, 6, false)     \
+    X(1, 128, 128, 3, false)    \
     X(1, 64, 64, 8, false)      \
+    X(1, 64, 128, 4, false)     \
     X(1, 128, 32, 8, false)     \
     X(2, 256, 64, 6, false)     \
+    X(2, 256, 128, 3, false)    \
     X(1, 256, 64, 4, true)      \
-    X(1, 128, 64, 6, true)      \
-    X(2, 256, 64, 6, true)
+    X(1, 128, 128, 3, true)     \
+    X(2, 256, 128, 3, true)
 
 }  // namespace g300

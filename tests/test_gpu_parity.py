@@ -113,7 +113,7 @@ def sample_entries(M, N, n=2048, seed=0):
 
 @pytest.mark.parametrize("major", ["K", "MN"])
 @pytest.mark.parametrize("mode", ["sw32", "sw64", "sw128"])
-@pytest.mark.parametrize("rows,bk", [(128, 64), (256, 64), (128, 32), (64, 64)])
+@pytest.mark.parametrize("rows,bk", [(128, 64), (256, 64), (128, 32), (64, 64), (128, 128)])
 def test_device_descriptor_words_match_oracle(g, major, mode, rows, bk):
     W = L.swizzle_width(mode)
     if major == "K" and W > 2 * bk:
@@ -165,7 +165,7 @@ def _stage_image(g, major, mode, rows, bk, rows_total=None, k_total=None, mn0=0,
 
 @pytest.mark.parametrize("major", ["K", "MN"])
 @pytest.mark.parametrize("mode", ["sw32", "sw64", "sw128"])
-@pytest.mark.parametrize("rows,bk", [(128, 64), (128, 32), (256, 64)])
+@pytest.mark.parametrize("rows,bk", [(128, 64), (128, 32), (256, 64), (128, 128)])
 def test_tma_stage_image_matches_swizzle_map(g, major, mode, rows, bk):
     W = L.swizzle_width(mode)
     if (major == "K" and W > 2 * bk) or (major == "MN" and rows % (W // 2)):
@@ -236,19 +236,23 @@ def test_ragged_shapes(g, M, N, K, out):
     run_case(g, M, N, K, out=out, dist="normal", a_major="K", b_major="MN")
 
 
-@pytest.mark.parametrize("cg,tile_n", [(1, 64), (1, 128), (1, 256), (2, 256)])
-@pytest.mark.parametrize("a_major,b_major", [("K", "K"), ("MN", "MN")])
-def test_tile_configs(g, cg, tile_n, a_major, b_major):
+@pytest.mark.parametrize("cg,tile_n,bk", [(1, 64, 64), (1, 64, 128), (1, 128, 64), (1, 128, 128), (1, 256, 64),
+                                          (2, 256, 64), (2, 256, 128)])
+@pytest.mark.parametrize("a_major,b_major", [("K", "K"), ("MN", "MN"), ("K", "MN")])
+def test_tile_configs(g, cg, tile_n, bk, a_major, b_major):
     run_case(g, 520, 600, 264, a_major=a_major, b_major=b_major, dist="normal",
-             options=dict(cta_group=cg, tile_n=tile_n))
+             options=dict(cta_group=cg, tile_n=tile_n, block_k=bk))
+    run_case(g, 384, 320, 200, a_major=a_major, b_major=b_major, dist="int4", exact=True,
+             options=dict(cta_group=cg, tile_n=tile_n, block_k=bk))
 
 
 @pytest.mark.parametrize("swz_a", [1, 2, 3])
 @pytest.mark.parametrize("swz_b", [1, 2, 3])
 @pytest.mark.parametrize("a_major,b_major", [("K", "MN"), ("MN", "K")])
-def test_swizzle_modes(g, swz_a, swz_b, a_major, b_major):
-    run_case(g, 256, 256, 192, a_major=a_major, b_major=b_major, dist="int4", exact=True,
-             options=dict(swizzle_a=swz_a, swizzle_b=swz_b, tile_n=128))
+@pytest.mark.parametrize("bk", [64, 128])
+def test_swizzle_modes(g, swz_a, swz_b, a_major, b_major, bk):
+    run_case(g, 256, 256, 320, a_major=a_major, b_major=b_major, dist="int4", exact=True,
+             options=dict(swizzle_a=swz_a, swizzle_b=swz_b, tile_n=128, block_k=bk))
 
 
 def test_unswizzled_epilogue_staging(g):
@@ -278,6 +282,12 @@ def test_padded_leading_dimensions(g):
 
 def test_k_zero_gives_beta_c(g):
     run_case(g, 130, 70, 0, out="f32", alpha=2.0, beta=0.5)
+
+
+@pytest.mark.parametrize("M,N,K,tn", [(1000, 136, 1000, 128), (128, 1000, 520, 64), (384, 512, 64, 256)])
+def test_rotated_k_start(g, M, N, K, tn):
+    run_case(g, M, N, K, dist="int4", exact=True, options=dict(tile_n=tn, flags=4))
+    run_case(g, M, N, K, dist="normal", out="bf16", beta=1.0, options=dict(tile_n=tn, flags=4))
 
 
 def test_k_tail_and_single_column(g):
@@ -358,6 +368,14 @@ def test_config5_grouped_64_problems(g):
     rng = np.random.default_rng(5)
     Ms = [int(x) for x in rng.integers(1, 33, 64) * 128]
     _grouped(g, Ms, 4096, 2048, out="bf16", dist="uniform", seed=100, sample=True)
+
+
+@pytest.mark.parametrize("flags", [0, 1, 2, 3, 4, 5])
+def test_pair_signalling_modes(g, flags):
+    # multicast commits (0), forwarded releases (1), cluster-scope waits (2), both (3), rotated K (4, 5)
+    run_case(g, 640, 768, 320, a_major="K", b_major="MN", dist="int4", exact=True,
+             options=dict(cta_group=2, flags=flags))
+    run_case(g, 512, 512, 256, out="bf16", beta=0.5, dist="normal", options=dict(cta_group=2, flags=flags))
 
 
 # ---------------------------------------------------------------- bounded waits
