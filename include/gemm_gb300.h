@@ -177,6 +177,33 @@ gemm_status_t gemm_f16_grouped(const gemm_problem_t *problems, int num_problems,
                                void *workspace, size_t workspace_bytes,
                                gemm_stream_t stream);
 
+/*
+ * gemm_bf16_grouped_noalloc: the grouped bf16 GEMM for callers that cannot
+ * allocate device memory when they launch it -- for instance code running
+ * while a stream is being captured into a CUDA graph, programs whose memory
+ * pool owns the whole device, or latency-bound loops that may not enter the
+ * driver's allocator. There is no counterpart on the pages; it is a service
+ * of this library. Instead of a caller workspace, the problem table and TMA
+ * descriptors go into a fixed array inside the library (about 68 KB, room for
+ * GEMM_NOALLOC_MAX_PROBLEMS problems) that every GPU which loads the library
+ * keeps until the process exits. The call allocates nothing, host or device.
+ *   - Same arguments and results as gemm_bf16_grouped, minus the workspace.
+ *   - num_problems > GEMM_NOALLOC_MAX_PROBLEMS returns GEMM_ERR_INVALID_ARG
+ *     and enqueues nothing.
+ *   - The first call on a device looks up the array's device address there
+ *     (with that device current); make that first call before any stream
+ *     capture.
+ *   - All calls share the array and each call rewrites the part it uses, so
+ *     calls whose kernels may overlap on the GPU (other streams, or no
+ *     ordering between them) race: order them on one stream or synchronise.
+ */
+#define GEMM_NOALLOC_MAX_PROBLEMS 128
+
+gemm_status_t gemm_bf16_grouped_noalloc(const gemm_problem_t *problems, int num_problems,
+                                        gemm_major_t a_major, gemm_major_t b_major,
+                                        gemm_out_t d_type, float alpha, float beta,
+                                        gemm_stream_t stream);
+
 /* Synchronises `stream`, reads the device status word of this library,
  * clears it, and returns GEMM_OK or GEMM_ERR_TIMEOUT (GEMM_ERR_CUDA if the
  * read fails). `detail` (may be NULL) receives the raw word: bits 0-7 the

@@ -48,6 +48,7 @@ _lib.gemm_ex.argtypes = [_int] + _single[:-1] + [ctypes.POINTER(GemmOptions), _v
 _grouped = [ctypes.POINTER(GemmProblem), _int, _int, _int, _int, _f, _f, _vp, ctypes.c_size_t, _vp]
 _lib.gemm_bf16_grouped.argtypes = _grouped
 _lib.gemm_f16_grouped.argtypes = _grouped
+_lib.gemm_bf16_grouped_noalloc.argtypes = [ctypes.POINTER(GemmProblem), _int, _int, _int, _int, _f, _f, _vp]
 _lib.gemm_grouped_workspace_size.argtypes = [_int]
 _lib.gemm_grouped_workspace_size.restype = ctypes.c_size_t
 _lib.gemm_last_device_status.argtypes = [_vp, ctypes.POINTER(_u32)]
@@ -59,12 +60,12 @@ _lib.gemm_debug_descriptors.argtypes = [_int, _int, _int, _int, _u32, _int, _int
 _lib.gemm_debug_stage_image.argtypes = [_vp, _int, _int, _i64, _i64, _i64, _int, _int, _i64, _i64, _vp, _vp]
 _lib.gemm_debug_inject_timeout.argtypes = [_int]
 _lib.gemm_debug_inject_timeout.restype = None
-for _name in ("gemm_bf16", "gemm_f16", "gemm_ex", "gemm_bf16_grouped", "gemm_f16_grouped",
+for _name in ("gemm_bf16", "gemm_f16", "gemm_ex", "gemm_bf16_grouped", "gemm_f16_grouped", "gemm_bf16_grouped_noalloc",
               "gemm_last_device_status", "gemm_debug_descriptors", "gemm_debug_stage_image"):
     getattr(_lib, _name).restype = _int
 
 EXPORTED = ("gemm_bf16", "gemm_f16", "gemm_ex", "gemm_grouped_workspace_size", "gemm_bf16_grouped",
-            "gemm_f16_grouped", "gemm_last_device_status", "gemm_status_string", "gemm_launch_count",
+            "gemm_f16_grouped", "gemm_bf16_grouped_noalloc", "gemm_last_device_status", "gemm_status_string", "gemm_launch_count",
             "gemm_debug_descriptors", "gemm_debug_stage_image", "gemm_debug_inject_timeout")
 
 
@@ -156,6 +157,16 @@ def gemm_f16_grouped(problems, a_major, b_major, d_type, alpha, beta, workspace,
     arr = _problem_array(problems)
     _check(_lib.gemm_f16_grouped(arr, len(problems), a_major, b_major, d_type, alpha, beta,
                                  _addr(workspace), workspace_bytes, _stream(stream)), "gemm_f16_grouped")
+
+
+NOALLOC_MAX_PROBLEMS = 128
+
+
+def gemm_bf16_grouped_noalloc(problems, a_major, b_major, d_type, alpha, beta, stream=None):
+    """Grouped bf16 GEMM whose table lives in the library's fixed scratch (no allocation)."""
+    arr = _problem_array(problems)
+    _check(_lib.gemm_bf16_grouped_noalloc(arr, len(problems), a_major, b_major, d_type, alpha, beta,
+                                          _stream(stream)), "gemm_bf16_grouped_noalloc")
 
 
 def gemm_last_device_status(stream=None) -> tuple[int, int]:

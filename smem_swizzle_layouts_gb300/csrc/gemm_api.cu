@@ -561,6 +561,148 @@ __global__ void debug_stage_kernel(const __grid_constant__ CUtensorMap map, int 
         *reinterpret_cast<uint4 *>(out + i) = *reinterpret_cast<const uint4 *>(src + i);
 }
 
+// ---------------------------------------------------------------- grouped GEMM without allocation
+//
+// Some callers cannot allocate device memory at the moment they launch a
+// GEMM: code running while a stream is being captured into a CUDA graph
+// (an allocation there breaks or serialises the capture), allocators that
+// own the whole device pool and forbid side allocations, or real-time loops
+// that may not block in the driver's allocator. For them the grouped GEMM's
+// workspace (problem table plus one TMA descriptor per operand per problem)
+// lives in the fixed array below, sized for kNoAllocMaxProblems problems.
+// Every GPU that loads the library holds it until the process exits.
+
+constexpr int kNoAllocMaxProblems = GEMM_NOALLOC_MAX_PROBLEMS;
+constexpr size_t kNoAllocScratchBytes =
+    ((static_cast<size_t>(kNoAllocMaxProblems) * sizeof(GroupedProblemDev) + 127) & ~size_t(127)) +
+    static_cast<size_t>(kNoAllocMaxProblems) * 4 * sizeof(CUtensorMap);
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Host staging for the table; guarded by g_noalloc_mu. A pageable-source copy
+// has consumed its source when cudaMemcpyAsync returns, so it can be reused.
+static unsigned char g_noalloc_host[kNoAllocScratchBytes];
+std::mutex g_noalloc_mu;
+unsigned char *g_noalloc_dev[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device. In host code the
+// array's name only stands in for the symbol, so the address is looked up once
+// per device (with that device current) and cached.
+gemm_status_t noalloc_scratch(int dev, unsigned char **out)
+{
+    if (!g_noalloc_dev[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr)
+            return GEMM_ERR_CUDA;
+        g_noalloc_dev[dev] = static_cast<unsigned char *>(ptr);
+    }
+    *out = g_noalloc_dev[dev];
+    return GEMM_OK;
+}
+
+gemm_status_t run_grouped_noalloc(int in_bf16, const gemm_problem_t *probs, int n, int a_major,
+                                  int b_major, int d_type, float alpha, float beta,
+                                  cudaStream_t stream)
+{
+    if (n < 0 || (n > 0 && !probs) || !valid_enum(a_major) || !valid_enum(b_major) || d_type < 0 ||
+        d_type > 2)
+        return GEMM_ERR_INVALID_ARG;
+    if (n > kNoAllocMaxProblems)
+        return GEMM_ERR_INVALID_ARG;  // more problems than the fixed scratch holds
+    if (n == 0)
+        return GEMM_OK;
+    const int a_mn = a_major, b_mn = b_major;
+    int64_t maxM = 0, maxN = 0, maxK = 0;
+    for (int i = 0; i < n; ++i) {
+        const gemm_problem_t &q = probs[i];
+        gemm_status_t s = check_problem(q.M, q.N, q.K, q.A, a_mn, q.lda, q.B, b_mn, q.ldb, q.C, q.ldc,
+                                        q.D, q.ldd, d_type, beta);
+        if (s != GEMM_OK)
+            return s;
+        maxM = std::max(maxM, q.M);
+        maxN = std::max(maxN, q.N);
+        maxK = std::max(maxK, q.K);
+    }
+    int dev = 0, sms = 0;
+    unsigned int *status = nullptr;
+    gemm_status_t s = device_state(&dev, &status, &sms);
+    if (s != GEMM_OK)
+        return s;
+    gemm_options_t o = {};
+    o.tile_n = (maxN >= 192) ? 256 : 128;
+    o.cta_group = 1;
+    Plan pl;
+    if ((s = make_plan(maxM, maxN, maxK, a_mn, b_mn, sms, &o, true, &pl)) != GEMM_OK)
+        return s;
+    Variant *v = find_variant(pl.cg, pl.bn, pl.bk, true);
+
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    unsigned char *ws = nullptr;
+    if ((s = noalloc_scratch(dev, &ws)) != GEMM_OK)
+        return s;
+    const size_t tb = table_bytes(n);
+    const size_t used = tb + static_cast<size_t>(n) * 4 * sizeof(CUtensorMap);
+    // the whole used region is rewritten on every call: nothing is left over
+    // from an earlier call with more problems or other pointers
+    std::memset(g_noalloc_host, 0, used);
+    auto *table = reinterpret_cast<GroupedProblemDev *>(g_noalloc_host);
+    auto *maps = reinterpret_cast<CUtensorMap *>(g_noalloc_host + tb);
+    int64_t tiles = 0;
+    for (int i = 0; i < n; ++i) {
+        const gemm_problem_t &q = probs[i];
+        GroupedProblemDev &g = table[i];
+        g.M = static_cast<int>(q.M);
+        g.N = static_cast<int>(q.N);
+        g.K = static_cast<int>(q.K);
+        const bool empty = q.M == 0 || q.N == 0;
+        g.tiles_m = empty ? 0 : static_cast<int>((q.M + 128 * pl.cg - 1) / (128 * pl.cg));
+        g.tiles_n = empty ? 0 : static_cast<int>((q.N + pl.bn - 1) / pl.bn);
+        g.tile_start = static_cast<int>(tiles);
+        tiles += static_cast<int64_t>(g.tiles_m) * g.tiles_n;
+        if (tiles >= (static_cast<int64_t>(1) << 31))
+            return GEMM_ERR_UNSUPPORTED;
+        if (empty)
+            continue;
+        CUtensorMap *m = maps + 4 * i;
+        if (q.K > 0) {
+            if ((s = encode_operand(&m[0], in_bf16, q.A, a_mn, pl.a_swz, q.M, q.K, q.lda, 128, pl.bk)) != GEMM_OK)
+                return s;
+            if ((s = encode_operand(&m[1], in_bf16, q.B, b_mn, pl.b_swz, q.N, q.K, q.ldb, pl.bn / pl.cg,
+                                    pl.bk)) != GEMM_OK)
+                return s;
+        }
+        if ((s = encode_output(&m[3], d_type, q.D, q.M, q.N, q.ldd, pl.epi_swizzle)) != GEMM_OK)
+            return s;
+        if (beta != 0.0f) {
+            if ((s = encode_output(&m[2], d_type, q.C, q.M, q.N, q.ldc, pl.epi_swizzle)) != GEMM_OK)
+                return s;
+        } else {
+            m[2] = m[3];
+        }
+    }
+    if (tiles == 0)
+        return GEMM_OK;
+    cudaError_t e = cudaMemcpyAsync(ws, g_noalloc_host, used, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+
+    LaunchArgs la;
+    std::memset(&la, 0, sizeof(la));
+    KParams &p = la.p;
+    p.num_tiles = static_cast<int>(tiles);
+    p.problems = reinterpret_cast<const GroupedProblemDev *>(ws);
+    p.maps = reinterpret_cast<const CUtensorMap *>(ws + tb);
+    p.num_problems = n;
+    fill_common(p, pl, in_bf16, a_mn, b_mn, d_type, alpha, beta, status);
+    la.grid = grid_for(pl, *v, dev, sms, tiles);
+    la.stream = stream;
+    e = v->launch(la);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    g_launches.fetch_add(1);
+    return GEMM_OK;
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------- C ABI
@@ -617,6 +759,14 @@ gemm_status_t gemm_f16_grouped(const gemm_problem_t *problems, int num_problems,
 {
     return run_grouped(0, problems, num_problems, a_major, b_major, d_type, alpha, beta, workspace,
                        workspace_bytes, nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_bf16_grouped_noalloc(const gemm_problem_t *problems, int num_problems,
+                                        gemm_major_t a_major, gemm_major_t b_major, gemm_out_t d_type,
+                                        float alpha, float beta, gemm_stream_t stream)
+{
+    return run_grouped_noalloc(1, problems, num_problems, a_major, b_major, d_type, alpha, beta,
+                               reinterpret_cast<cudaStream_t>(stream));
 }
 
 gemm_status_t gemm_last_device_status(gemm_stream_t stream, uint32_t *detail)
