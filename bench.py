@@ -81,11 +81,15 @@ def _peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+KERNEL_SOURCES = ("gemm_kernel.cuh", "ptx.cuh", "descriptors.cuh")
+
+
 def _source_hash():
+    """Hash of the device-code sources; a stored ncu traffic figure is valid only for this hash."""
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "smem_swizzle_layouts_gb300", "csrc", "*"))):
-        with open(p, "rb") as f:
-            h.update(os.path.basename(p).encode())
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "smem_swizzle_layouts_gb300", "csrc", name), "rb") as f:
+            h.update(name.encode())
             h.update(f.read())
     return h.hexdigest()[:16]
 
@@ -104,9 +108,9 @@ def _profiled_traffic(workload):
 
 
 class ClockSampler:
-    """nvidia-smi samples (200 ms) while the timed region runs."""
+    """nvidia-smi samples (every 20 ms); only those taken inside the timed region count."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -119,7 +123,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except OSError:
@@ -127,7 +131,10 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        setattr(self, which, time.time())
 
     def stop(self):
         if self.proc is None:
@@ -140,22 +147,38 @@ class ClockSampler:
         self.thread.join(timeout=2)
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        t0, t1 = getattr(self, "t_start", 0.0), getattr(self, "t_end", float("inf"))
+        inside = [ln for t, ln in self.lines if t0 <= t <= t1 + 0.02]
+        for ln in inside:
             parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                mx = float(parts[2])
+                sm.append(float(parts[2]))
+                mx = float(parts[3])
             except ValueError:
                 continue
-            for name, val in zip(names, parts[5:9]):
+            for name, val in zip(names, parts[6:10]):
                 if val.lower() in ("active", "1"):
                     reasons.add(name)
         if not sm:
-            return None
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "no nvidia-smi sample fell inside the timed region"}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
                 "samples": len(sm)}
+
+
+def max_over_ranks(value: float, device) -> float:
+    """The slowest rank's time: all-reduce MAX over the process group."""
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world_size: int, max_ms: float) -> float:
+    """Whole-job rate: the units all ranks processed over the slowest rank's time (per second)."""
+    return units_per_rank * world_size / (max_ms / 1e3)
 
 
 def _torch_inputs(wl, dev, pinned=False):
@@ -212,8 +235,9 @@ def _run_ours(args, wl_name, wl, ws, rank, local):
     sampler = ClockSampler(local)
     barrier()
     sampler.start()
-    time.sleep(0.3)
+    time.sleep(0.5)  # nvidia-smi is up and sampling before the timed region starts
     launches0 = g.gemm_launch_count()
+    sampler.mark("t_start")
     t_begin = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
@@ -224,6 +248,7 @@ def _run_ours(args, wl_name, wl, ws, rank, local):
             ends[i].record(stream)
         t_end.record(stream)
     barrier()
+    sampler.mark("t_end")
     launches = g.gemm_launch_count() - launches0
     clocks = sampler.stop()
     st, word = g.gemm_last_device_status(stream)
@@ -232,9 +257,7 @@ def _run_ours(args, wl_name, wl, ws, rank, local):
     total_ms = t_begin.elapsed_time(t_end)
     per_launch = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     if ws > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+        total_ms = max_over_ranks(total_ms, dev)
 
     # ---- end to end through the public API with host buffers
     hA, hB, hC = host
@@ -299,7 +322,7 @@ def _oracle_rows_rate(wl, bits, target_s, max_rows=None, fixed_rows=None):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
@@ -347,8 +370,7 @@ def main():
     if ws > 1:
         torch.distributed.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
     r = _run_ours(args, args.workload, wl, ws, rank, local)
-    per_rank_units = flops * args.steps
-    value = per_rank_units * ws / (r["total_ms"] / 1e3) / 1e12
+    value = job_throughput(flops * args.steps, ws, r["total_ms"]) / 1e12
     kernel_ms = statistics.mean(r["per_launch"])
     achieved = flops / (kernel_ms / 1e3) / 1e12
     peaks, peak_src = _peaks()
