@@ -52,17 +52,21 @@ WORKLOADS = {
         desc="4096^3 bf16, A and B K-major, N(0,1)*0.1, bf16 out, SW128, cta_group::1"),
     "skinny_m16384_n128_k8192": dict(
         M=16384, N=128, K=8192, a_major="K", b_major="K", out="bf16", alpha=1.0, beta=0.0, dist="normal",
-        scale=1.0, seed=30, options=None, desc="M=16384 N=128 K=8192 bf16, N(0,1), bf16 out"),
+        scale=1.0, seed=30, options=None, bound="hbm", desc="M=16384 N=128 K=8192 bf16, N(0,1), bf16 out"),
     "skinny_m128_n16384_k4096": dict(
         M=128, N=16384, K=4096, a_major="K", b_major="K", out="bf16", alpha=1.0, beta=0.0, dist="normal",
-        scale=1.0, seed=31, options=None, desc="M=128 N=16384 K=4096 bf16, N(0,1), bf16 out"),
+        scale=1.0, seed=31, options=None, bound="hbm", desc="M=128 N=16384 K=4096 bf16, N(0,1), bf16 out"),
+    "grouped64_n4096_k2048": dict(
+        kind="grouped", M=0, N=4096, K=2048, problems=64, m_seed=5, a_major="K", b_major="K", out="bf16",
+        alpha=1.0, beta=0.0, dist="uniform", scale=1.0, seed=100, options=None,
+        desc="64 independent bf16 problems, M_i uniform in {128..4096} step 128 (rng 5), N=4096, K=2048, "
+             "U[-1,1], bf16 out, one launch over a device-side problem list"),
     "single_tile_128x128x32_f16": dict(
         M=128, N=128, K=32, a_major="K", b_major="MN", out="f32", alpha=1.0, beta=0.0, dist="uniform",
         scale=1.0, seed=0, options=None, in_fmt="f16",
         desc="D[128x128] fp32 = A[128x32] fp16 K-major x B[32x128] fp16 MN-major, two m128n128k16 MMAs"),
 }
 DEFAULT_WORKLOAD = "square8192_pair_f32_beta1"
-GROUPED = "grouped64_n4096_k2048"
 
 
 def _dist_env():
@@ -197,6 +201,81 @@ def _torch_inputs(wl, dev, pinned=False):
     return (A, B, C), host, devt
 
 
+class GemmJob:
+    """One GEMM per step through gemm_ex."""
+
+    def __init__(self, wl, dev, stream, options):
+        import torch
+        import smem_swizzle_layouts_gb300 as g
+        self.g, self.wl, self.stream = g, wl, stream
+        tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[wl["out"]]
+        self.M, self.N, self.K = wl["M"], wl["N"], wl["K"]
+        self.in_type = 1 if wl.get("in_fmt", "bf16") == "bf16" else 0
+        self.bits, host, devt = _torch_inputs(wl, dev, pinned=True)
+        self.A, self.B, self.C = devt
+        self.D = torch.empty(self.M, self.N, dtype=tdt, device=dev)
+        self.hD = torch.empty(self.M, self.N, dtype=tdt).pin_memory()
+        self.pairs = [(h, d) for h, d in zip(host, devt) if h is not None]
+        self.am = 0 if wl["a_major"] == "K" else 1
+        self.bm = 0 if wl["b_major"] == "K" else 1
+        self.dt = {"f32": 0, "bf16": 1, "f16": 2}[wl["out"]]
+        self.options = options
+        self.flops = 2.0 * self.M * self.N * self.K
+
+    def step(self):
+        self.g.gemm_ex(self.in_type, self.M, self.N, self.K, self.A, self.am, self.A.stride(0), self.B, self.bm,
+                       self.B.stride(0), self.C, self.N if self.C is not None else 0, self.D, self.N, self.dt,
+                       self.wl["alpha"], self.wl["beta"], options=self.options, stream=self.stream)
+
+    def outputs(self):
+        return [(self.D, self.hD)]
+
+    def oracle_rate(self, target_s, fixed_rows=None):
+        return _oracle_rows_rate(self.wl, self.bits, target_s, fixed_rows=fixed_rows)
+
+
+class GroupedJob:
+    """One grouped launch over a 64-problem list per step (gemm_bf16_grouped)."""
+
+    def __init__(self, wl, dev, stream, options):
+        import torch
+        import smem_swizzle_layouts_gb300 as g
+        self.g, self.wl, self.stream = g, wl, stream
+        N, K = wl["N"], wl["K"]
+        rng = np.random.default_rng(wl["m_seed"])
+        self.Ms = [int(x) * 128 for x in rng.integers(1, 33, wl["problems"])]
+        self.N, self.K = N, K
+        self.hA, self.hB, self.hD, self.probs, self.bits = [], [], [], [], []
+        self.pairs, self.outs = [], []
+        for i, M in enumerate(self.Ms):
+            A = si.matrix_bits(wl["seed"] + 3 * i, M, K, wl["dist"], "bf16")
+            B = si.matrix_bits(wl["seed"] + 3 * i + 1, K, N, wl["dist"], "bf16", transpose=True)
+            hA = si.torch_from_bits(A, "bf16").pin_memory()
+            hB = si.torch_from_bits(B, "bf16").pin_memory()
+            dA, dB = hA.to(dev), hB.to(dev)
+            dD = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+            hD = torch.empty(M, N, dtype=torch.bfloat16).pin_memory()
+            self.pairs += [(hA, dA), (hB, dB)]
+            self.outs.append((dD, hD))
+            self.bits.append((A, B))
+            self.probs.append(dict(M=M, N=N, K=K, A=dA, B=dB, C=None, D=dD, lda=K, ldb=K, ldc=0, ldd=N))
+        self.ws_bytes = g.gemm_grouped_workspace_size(len(self.Ms))
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+        self.flops = float(sum(2.0 * M * N * K for M in self.Ms))
+
+    def step(self):
+        self.g.gemm_bf16_grouped(self.probs, 0, 0, 1, self.wl["alpha"], self.wl["beta"], self.ws, self.ws_bytes,
+                                 stream=self.stream)
+
+    def outputs(self):
+        return self.outs
+
+    def oracle_rate(self, target_s, fixed_rows=None):
+        A, B = self.bits[0]
+        sub = dict(self.wl, M=self.Ms[0], a_major="K", b_major="K", out="bf16", beta=0.0)
+        return _oracle_rows_rate(sub, (A, B, None), target_s, fixed_rows=fixed_rows)
+
+
 def _run_ours(args, wl_name, wl, ws, rank, local):
     import torch
     import smem_swizzle_layouts_gb300 as g
@@ -204,18 +283,10 @@ def _run_ours(args, wl_name, wl, ws, rank, local):
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(device=dev)
-    tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[wl["out"]]
-    M, N, K = wl["M"], wl["N"], wl["K"]
-    in_type = 1 if wl.get("in_fmt", "bf16") == "bf16" else 0
-    bits, host, (At, Bt, Ct) = _torch_inputs(wl, dev, pinned=True)
-    D = torch.empty(M, N, dtype=tdt, device=dev)
-    lda, ldb = At.stride(0), Bt.stride(0)
-    am, bm = (0 if wl["a_major"] == "K" else 1), (0 if wl["b_major"] == "K" else 1)
-    dt = {"f32": 0, "bf16": 1, "f16": 2}[wl["out"]]
-
-    def step(Aa, Bb, Cc, Dd):
-        g.gemm_ex(in_type, M, N, K, Aa, am, lda, Bb, bm, ldb, Cc, N if Cc is not None else 0, Dd, N, dt,
-                  wl["alpha"], wl["beta"], options=wl["options"], stream=stream)
+    options = wl.get("options")
+    if args.options:
+        options = dict(options or {}, **json.loads(args.options))
+    job = (GroupedJob if wl.get("kind") == "grouped" else GemmJob)(wl, dev, stream, options)
 
     def barrier():
         if ws > 1:
@@ -224,7 +295,7 @@ def _run_ours(args, wl_name, wl, ws, rank, local):
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
-            step(At, Bt, Ct, D)
+            job.step()
     st, word = g.gemm_last_device_status(stream)
     if st != g.OK:
         raise RuntimeError(f"device status {st} ({word:#x}) during warm-up")
@@ -244,7 +315,7 @@ def _run_ours(args, wl_name, wl, ws, rank, local):
         t_begin.record(stream)
         for i in range(args.steps):
             starts[i].record(stream)
-            step(At, Bt, Ct, D)
+            job.step()
             ends[i].record(stream)
         t_end.record(stream)
     barrier()
@@ -260,8 +331,6 @@ def _run_ours(args, wl_name, wl, ws, rank, local):
         total_ms = max_over_ranks(total_ms, dev)
 
     # ---- end to end through the public API with host buffers
-    hA, hB, hC = host
-    hD = torch.empty(M, N, dtype=tdt).pin_memory()
     e2e_steps = max(1, min(args.steps, 10))
     barrier()
     with torch.cuda.stream(stream):
@@ -269,20 +338,18 @@ def _run_ours(args, wl_name, wl, ws, rank, local):
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(e2e_steps):
-            At.copy_(hA, non_blocking=True)
-            Bt.copy_(hB, non_blocking=True)
-            if Ct is not None:
-                Ct.copy_(hC, non_blocking=True)
-            step(At, Bt, Ct, D)
-            hD.copy_(D, non_blocking=True)
+            for h, d in job.pairs:
+                d.copy_(h, non_blocking=True)
+            job.step()
+            for d, h in job.outputs():
+                h.copy_(d, non_blocking=True)
         e1.record(stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    h2d = At.numel() * At.element_size() + Bt.numel() * Bt.element_size() + (
-        Ct.numel() * Ct.element_size() if Ct is not None else 0)
-    d2h = D.numel() * D.element_size()
+    h2d = sum(d.numel() * d.element_size() for _, d in job.pairs)
+    d2h = sum(d.numel() * d.element_size() for d, _ in job.outputs())
     return dict(total_ms=total_ms, per_launch=per_launch, launches=launches, clocks=clocks, e2e_ms=e2e_ms,
-                h2d=h2d, d2h=d2h, bits=bits)
+                h2d=h2d, d2h=d2h, job=job, options=options)
 
 
 def _oracle_rows_rate(wl, bits, target_s, max_rows=None, fixed_rows=None):
@@ -319,6 +386,45 @@ def _oracle_rows_rate(wl, bits, target_s, max_rows=None, fixed_rows=None):
     return 2.0 * R * N * K / t, R, t, threads
 
 
+def _algorithmic_bytes(wl, job):
+    """Minimum HBM bytes of one step: read A, B (and C), write D once."""
+    ob = 4 if wl["out"] == "f32" else 2
+    if wl.get("kind") == "grouped":
+        N, K = wl["N"], wl["K"]
+        return float(sum((M * K + K * N) * 2 + M * N * ob for M in job.Ms))
+    M, N, K = wl["M"], wl["N"], wl["K"]
+    return float((M * K + K * N) * 2 + M * N * ob * (2 if wl["beta"] != 0.0 else 1))
+
+
+def _reference_line(args, wl, config, metric):
+    """The oracle timed on the host cores on a bounded row sample of the workload."""
+    if wl.get("kind") == "grouped":
+        rng = np.random.default_rng(wl["m_seed"])
+        M0 = int(rng.integers(1, 33, wl["problems"])[0]) * 128
+        sub = dict(wl, M=M0)
+        A = si.matrix_bits(wl["seed"], M0, wl["K"], wl["dist"], "bf16")
+        B = si.matrix_bits(wl["seed"] + 1, wl["K"], wl["N"], wl["dist"], "bf16", transpose=True)
+        bits, rows_of = (A, B, None), f"problem 0 (M={M0})"
+    else:
+        sub, bits, rows_of = wl, _torch_inputs_host_only(wl), f"{wl['M']} rows"
+    # calibrate a row sample so that warm-up + timed steps take about two minutes
+    per_step = max(0.5, 120.0 / (args.warmup + args.steps))
+    _, R, _, threads = _oracle_rows_rate(sub, bits, target_s=per_step)
+    rates = []
+    for i in range(args.warmup + args.steps):
+        rate, R, t, threads = _oracle_rows_rate(sub, bits, target_s=0.0, fixed_rows=R)
+        if i >= args.warmup:
+            rates.append(rate)
+    value = statistics.median(rates) / 1e12
+    sample = f"first {R} of {rows_of} per step ({2.0 * R * sub['N'] * sub['K']:.3e} flop)"
+    return {"impl": "reference", "metric": metric, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -328,69 +434,63 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--options", default="", help="JSON overrides of the workload's gemm options (ablations)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
 
     ws, rank, local = _dist_env()
     wl = WORKLOADS[args.workload]
-    flops = 2.0 * wl["M"] * wl["N"] * wl["K"]
     config = {"workload": args.workload, "desc": wl["desc"], "M": wl["M"], "N": wl["N"], "K": wl["K"],
               "a_major": wl["a_major"], "b_major": wl["b_major"], "out": wl["out"], "alpha": wl["alpha"],
               "beta": wl["beta"], "inputs": f"{wl['dist']} x{wl['scale']}, seed {wl['seed']}",
-              "l2": "operands larger than L2 (no flush)" if flops >= 2 * 4096 ** 3 else
-                    "operands resident; no flush between steps",
               "parallelism": f"replicas x{max(ws, args.gpus)}"}
+    if args.options:
+        config["options"] = json.loads(args.options)
     metric = "GEMM TFLOP/s (bf16 in, fp32 accum)"
 
     if args.impl == "reference":
-        if rank != 0:
-            return
-        bits = _torch_inputs_host_only(wl)
-        # calibrate a row sample so that warm-up + timed steps take about two minutes
-        per_step = max(0.5, 120.0 / (args.warmup + args.steps))
-        _, R, _, threads = _oracle_rows_rate(wl, bits, target_s=per_step)
-        rates = []
-        for i in range(args.warmup + args.steps):
-            rate, R, t, threads = _oracle_rows_rate(wl, bits, target_s=0.0, fixed_rows=R)
-            if i >= args.warmup:
-                rates.append(rate)
-        value = statistics.median(rates) / 1e12
-        sample = f"first {R} of {wl['M']} rows of the workload per step ({2.0 * R * wl['N'] * wl['K']:.3e} flop)"
-        line = {"impl": "reference", "metric": metric, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
-                "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
-                "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                                 "sample": sample},
-                "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-        print(json.dumps(line))
+        if rank == 0:
+            print(json.dumps(_reference_line(args, wl, config, metric)))
         return
 
     import torch
     if ws > 1:
         torch.distributed.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
     r = _run_ours(args, args.workload, wl, ws, rank, local)
+    job = r["job"]
+    flops = job.flops
+    bytes_alg = _algorithmic_bytes(wl, job)
+    config["l2"] = ("operands larger than L2 (129 MB): no flush between steps" if bytes_alg > 129e6 else
+                    "operands fit in L2; steps run back to back without a flush")
     value = job_throughput(flops * args.steps, ws, r["total_ms"]) / 1e12
     kernel_ms = statistics.mean(r["per_launch"])
-    achieved = flops / (kernel_ms / 1e3) / 1e12
     peaks, peak_src = _peaks()
-    peak = float(peaks.get("bf16_tflops", 1900.0))
-    traffic = _profiled_traffic(args.workload)
+    traffic = _profiled_traffic(args.workload) if not args.options else None
+    if wl.get("bound") == "hbm":
+        achieved = bytes_alg / (kernel_ms / 1e3) / 1e9
+        peak = float(peaks.get("hbm_gbs", 6800.0))
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "peak_source": f"{peak_src} hbm_gbs", "traffic": traffic, "kernel_ms": kernel_ms,
+                "algorithmic_bytes": bytes_alg}
+    else:
+        achieved = flops / (kernel_ms / 1e3) / 1e12
+        peak = float(peaks.get("bf16_tflops", 1900.0))
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_source": f"{peak_src} bf16_tflops (burst)",
+                "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
+                "traffic": traffic, "kernel_ms": kernel_ms, "algorithmic_bytes": bytes_alg}
     line = {"metric": metric, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": r["total_ms"] / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config,
             "e2e": {"value": flops / (r["e2e_ms"] / 1e3) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
                     "ms_per_step": r["e2e_ms"]},
-            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak, "peak_source": f"{peak_src} bf16_tflops (burst)",
-                         "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
-                         "traffic": traffic, "kernel_ms": kernel_ms},
-            "gpu_launches": r["launches"], "clocks": r["clocks"]}
+            "roofline": roof, "gpu_launches": r["launches"], "clocks": r["clocks"]}
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        rate, R, t, threads = _oracle_rows_rate(wl, r["bits"], target_s=args.cpu_seconds)
+        rate, R, t, threads = job.oracle_rate(args.cpu_seconds)
         line["cpu_baseline"] = {"value": rate / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                                "sample": f"first {R} of {wl['M']} rows of the same workload, {t:.1f} s"}
+                                "sample": f"first {R} rows of the same workload ({t:.1f} s)"}
     if rank == 0:
         print(json.dumps(line))
     if ws > 1:
