@@ -221,11 +221,13 @@ class GemmJob:
         self.dt = {"f32": 0, "bf16": 1, "f16": 2}[wl["out"]]
         self.options = options
         self.flops = 2.0 * self.M * self.N * self.K
+        # arguments marshalled once; each step is one call into the C ABI
+        self.call = g.GemmCall(self.in_type, self.M, self.N, self.K, self.A, self.am, self.A.stride(0), self.B,
+                               self.bm, self.B.stride(0), self.C, self.N if self.C is not None else 0, self.D,
+                               self.N, self.dt, wl["alpha"], wl["beta"], options=options, stream=stream)
 
     def step(self):
-        self.g.gemm_ex(self.in_type, self.M, self.N, self.K, self.A, self.am, self.A.stride(0), self.B, self.bm,
-                       self.B.stride(0), self.C, self.N if self.C is not None else 0, self.D, self.N, self.dt,
-                       self.wl["alpha"], self.wl["beta"], options=self.options, stream=self.stream)
+        self.call()
 
     def outputs(self):
         return [(self.D, self.hD)]

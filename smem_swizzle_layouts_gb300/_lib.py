@@ -132,6 +132,26 @@ def gemm_ex(in_type, M, N, K, A, a_major, lda, B, b_major, ldb, C, ldc, D, ldd, 
                         _addr(D), ldd, d_type, alpha, beta, _opts(options), _stream(stream)), "gemm_ex")
 
 
+class GemmCall:
+    """gemm_ex with its arguments marshalled once, for repeated launches on the same buffers.
+
+    Calling the object launches the GEMM again; it converts nothing per call.
+    """
+
+    def __init__(self, in_type, M, N, K, A, a_major, lda, B, b_major, ldb, C, ldc, D, ldd, d_type, alpha, beta,
+                 options=None, stream=None):
+        self._opts_ref = _opts(options)  # keeps the options struct alive
+        self._args = (_int(in_type), _i64(M), _i64(N), _i64(K), _vp(_addr(A)), _int(a_major), _i64(lda),
+                      _vp(_addr(B)), _int(b_major), _i64(ldb), _vp(_addr(C)), _i64(ldc), _vp(_addr(D)),
+                      _i64(ldd), _int(d_type), _f(alpha), _f(beta), self._opts_ref, _vp(_stream(stream)))
+        self._fn = _lib.gemm_ex
+
+    def __call__(self):
+        st = self._fn(*self._args)
+        if st != OK:
+            raise GemmError(st, "gemm_ex")
+
+
 def gemm_grouped_workspace_size(num_problems: int) -> int:
     return int(_lib.gemm_grouped_workspace_size(num_problems))
 

@@ -3,3 +3,4 @@
 
 G300_INSTANTIATE(2, 256, 64, 6, false)
 G300_INSTANTIATE(2, 256, 128, 3, false)
+G300_INSTANTIATE(2, 128, 128, 4, false)

@@ -5,6 +5,8 @@
 
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "gemm_kernel.cuh"
 
 namespace g300 {
@@ -16,13 +18,37 @@ struct LaunchArgs {
     cudaStream_t stream;
 };
 
+// Opt a kernel into its dynamic shared memory once per device (the attribute
+// is per device; setting it on every launch costs host time on short GEMMs).
+// `done` is the caller's per-variant record: one bit per device 0..127.
+template <typename Kern>
+cudaError_t ensure_smem_attribute(Kern kern, int bytes, std::atomic<uint64_t> (&done)[2])
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= 128)
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    const uint64_t bit = uint64_t(1) << (dev & 63);
+    if (done[dev >> 6].load(std::memory_order_acquire) & bit)
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess)
+        done[dev >> 6].fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
+
+// One record per kernel variant.
+template <int CG, int BN, int BK, int STAGES, bool GROUPED>
+std::atomic<uint64_t> smem_attribute_set[2] = {{0}, {0}};
+
 template <int CG, int BN, int BK, int STAGES, bool GROUPED>
 cudaError_t launch_gemm(const LaunchArgs &a)
 {
     using C = Cfg<CG, BN, BK, STAGES>;
     auto kern = gemm_tcgen05_kernel<CG, BN, BK, STAGES, GROUPED>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM_BYTES);
+    cudaError_t e = ensure_smem_attribute(kern, C::SMEM_BYTES, smem_attribute_set<CG, BN, BK, STAGES, GROUPED>);
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};
@@ -48,8 +74,7 @@ cudaError_t resident_ctas(int *ctas)
 {
     using C = Cfg<CG, BN, BK, STAGES>;
     auto kern = gemm_tcgen05_kernel<CG, BN, BK, STAGES, GROUPED>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM_BYTES);
+    cudaError_t e = ensure_smem_attribute(kern, C::SMEM_BYTES, smem_attribute_set<CG, BN, BK, STAGES, GROUPED>);
     if (e != cudaSuccess)
         return e;
     if (CG == 1) {

@@ -24,6 +24,7 @@ cudaError_t resident_ctas(int *ctas);
     X(1, 128, 32, 8, false)     \
     X(2, 256, 64, 6, false)     \
     X(2, 256, 128, 3, false)    \
+    X(2, 128, 128, 4, false)    \
     X(1, 256, 64, 4, true)      \
     X(1, 128, 128, 3, true)     \
     X(2, 256, 128, 3, true)

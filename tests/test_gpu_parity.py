@@ -237,7 +237,7 @@ def test_ragged_shapes(g, M, N, K, out):
 
 
 @pytest.mark.parametrize("cg,tile_n,bk", [(1, 64, 64), (1, 64, 128), (1, 128, 64), (1, 128, 128), (1, 256, 64),
-                                          (2, 256, 64), (2, 256, 128)])
+                                          (2, 256, 64), (2, 256, 128), (2, 128, 128)])
 @pytest.mark.parametrize("a_major,b_major", [("K", "K"), ("MN", "MN"), ("K", "MN")])
 def test_tile_configs(g, cg, tile_n, bk, a_major, b_major):
     run_case(g, 520, 600, 264, a_major=a_major, b_major=b_major, dist="normal",
@@ -310,9 +310,10 @@ def test_config3_square_8192_pair_fp32_beta(g):
 
 
 @pytest.mark.parametrize("M,N,K", [(16384, 128, 8192), (128, 16384, 4096)])
-def test_config4_skinny(g, M, N, K):
+@pytest.mark.parametrize("cg", [1, 2])
+def test_config4_skinny(g, M, N, K, cg):
     run_case(g, M, N, K, a_major="K", b_major="K", out="bf16", dist="normal", seed=30,
-             sample=sample_entries(M, N, n=1024))
+             sample=sample_entries(M, N, n=1024), options=dict(cta_group=cg))
 
 
 # ---------------------------------------------------------------- grouped
