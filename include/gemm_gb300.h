@@ -64,12 +64,15 @@ typedef enum { GEMM_OUT_F32 = 0, GEMM_OUT_BF16 = 1, GEMM_OUT_F16 = 2 } gemm_out_
 
 /* Shared-memory swizzle of an operand tile ("Swizzling explained properly",
  * "32B, 64B and 128B swizzles"; raw descriptor codes on the LBO/SBO page,
- * section 4). GEMM_SWIZZLE_AUTO lets the library choose (SW128). */
+ * section 4). GEMM_SWIZZLE_AUTO lets the library choose (SW128);
+ * GEMM_SWIZZLE_NONE stores plain 8-row x 16-byte core matrices (descriptor
+ * code 0, LBO and SBO alone define the layout). */
 typedef enum {
     GEMM_SWIZZLE_AUTO = 0,
     GEMM_SWIZZLE_32B = 1,
     GEMM_SWIZZLE_64B = 2,
-    GEMM_SWIZZLE_128B = 3
+    GEMM_SWIZZLE_128B = 3,
+    GEMM_SWIZZLE_NONE = 4
 } gemm_swizzle_t;
 
 /*

@@ -24,7 +24,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = range(6)
 K_MAJOR, MN_MAJOR = 0, 1
 OUT_F32, OUT_BF16, OUT_F16 = 0, 1, 2
-SWIZZLE_AUTO, SWIZZLE_32B, SWIZZLE_64B, SWIZZLE_128B = 0, 1, 2, 3
+SWIZZLE_AUTO, SWIZZLE_32B, SWIZZLE_64B, SWIZZLE_128B, SWIZZLE_NONE = 0, 1, 2, 3, 4
 
 _i64, _vp, _f, _int, _u32, _u64 = (ctypes.c_int64, ctypes.c_void_p, ctypes.c_float, ctypes.c_int,
                                    ctypes.c_uint32, ctypes.c_uint64)

@@ -21,6 +21,10 @@
 //   MN-major (BK x rows): boxes of W/2 MN-elements x BK K-rows, one after
 //            another along MN. LBO = BK W (next MN atom), SBO = 8 W (next
 //            8-row K band), slice j starts at j * 2 * SBO.
+// Without swizzle (bits 0, W = 16) the 16-byte core-matrix cells are the
+// atoms: K-major LBO = rows * 16 (next K cell, one box away), SBO = 128 (next
+// 8-row group); MN-major LBO = 128 (next 8-row K band), SBO = BK * 16 (next
+// 8-element MN group, one box away).
 // Stages start on 1024-byte boundaries, so MBO is always 0 (the start of a
 // K slice inside a K-major row moves only bits below 128, page section 3).
 #pragma once
@@ -62,13 +66,18 @@ struct OperandPacking {
     uint32_t swz;
 };
 
-G300_HD OperandPacking operand_packing(int mn_major, int swz_bits, int bk)
+G300_HD OperandPacking operand_packing(int mn_major, int swz_bits, int rows, int bk)
 {
     const uint32_t W = swizzle_row_bytes(swz_bits);
     OperandPacking p;
+    p.swz = swizzle_code(swz_bits);
+    if (swz_bits == 0) {
+        p.lbo = mn_major ? 128u : static_cast<uint32_t>(rows) * 16u;
+        p.sbo = mn_major ? static_cast<uint32_t>(bk) * 16u : 128u;
+        return p;
+    }
     p.lbo = mn_major ? static_cast<uint32_t>(bk) * W : 16u;
     p.sbo = 8u * W;
-    p.swz = swizzle_code(swz_bits);
     return p;
 }
 

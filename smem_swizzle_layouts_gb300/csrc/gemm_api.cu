@@ -216,7 +216,8 @@ struct Plan {
     unsigned long long *stats;
 };
 
-int swz_bits_of(int opt) { return opt; }  // gemm_swizzle_t 1/2/3 == swizzle bits
+// gemm_swizzle_t -> swizzle bits (B of Swizzle<B,4,3>): 32B 1, 64B 2, 128B 3, none 0.
+int swz_bits_of(int opt) { return opt == GEMM_SWIZZLE_NONE ? 0 : opt; }
 
 // Choose the tile configuration; fills `plan` or returns an error for options
 // this build cannot honour.
@@ -227,7 +228,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
     if (o)
         opt = *o;
     if (opt.cta_group < 0 || opt.cta_group > 2 || opt.tile_n < 0 || opt.swizzle_a < 0 ||
-        opt.swizzle_a > 3 || opt.swizzle_b < 0 || opt.swizzle_b > 3 || opt.max_ctas < 0 ||
+        opt.swizzle_a > 4 || opt.swizzle_b < 0 || opt.swizzle_b > 4 || opt.max_ctas < 0 ||
         opt.group_m < 0 || opt.timeout_ms < 0 || opt.epilogue_swizzle < -1 ||
         opt.epilogue_swizzle > 1 || opt.flags < 0 || opt.flags > 7 || opt.block_k < 0)
         return GEMM_ERR_INVALID_ARG;
@@ -539,7 +540,7 @@ __global__ void debug_descriptor_kernel(int major, int swz_bits, int rows, int b
     if (threadIdx.x != 0 || blockIdx.x != 0)
         return;
     // the same arithmetic as the MMA role: stage descriptor + slice offset / 16
-    const OperandPacking pk = operand_packing(major, swz_bits, bk);
+    const OperandPacking pk = operand_packing(major, swz_bits, rows, bk);
     const uint64_t d0 = make_smem_desc(stage_addr, pk.lbo, pk.sbo, pk.swz);
     for (int j = 0; j < n_slices; ++j)
         out[j] = d0 + (slice_byte_offset(major, swz_bits, rows, j) >> 4);
@@ -831,12 +832,12 @@ gemm_status_t gemm_debug_descriptors(int major, int swizzle, int rows, int bk, u
                                      int n_slices, int cta_group, int tile_n, int in_type, int a_major,
                                      int b_major, uint64_t *out, gemm_stream_t stream)
 {
-    if (!valid_enum(major) || swizzle < 1 || swizzle > 3 || rows <= 0 || bk <= 0 || n_slices < 0 ||
+    if (!valid_enum(major) || swizzle < 1 || swizzle > 4 || rows <= 0 || bk <= 0 || n_slices < 0 ||
         (cta_group != 1 && cta_group != 2) || tile_n <= 0 || !out || (in_type != 0 && in_type != 1) ||
         !valid_enum(a_major) || !valid_enum(b_major))
         return GEMM_ERR_INVALID_ARG;
     debug_descriptor_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        major, swizzle, rows, bk, stage_addr, n_slices, 128 * cta_group, tile_n, in_type, a_major, b_major,
+        major, swz_bits_of(swizzle), rows, bk, stage_addr, n_slices, 128 * cta_group, tile_n, in_type, a_major, b_major,
         out);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
@@ -849,11 +850,12 @@ gemm_status_t gemm_debug_stage_image(const void *src, int major, int swizzle, in
                                      int64_t k_total, int64_t ld, int rows, int bk, int64_t mn0, int64_t k0,
                                      void *out, gemm_stream_t stream)
 {
-    if (!src || !out || !valid_enum(major) || swizzle < 1 || swizzle > 3 || rows <= 0 || rows > 256 ||
+    if (!src || !out || !valid_enum(major) || swizzle < 1 || swizzle > 4 || rows <= 0 || rows > 256 ||
         bk <= 0 || bk > 256 || rows_total <= 0 || k_total <= 0 || mn0 < 0 || k0 < 0 ||
         mn0 > INT32_MAX || k0 > INT32_MAX || rows_total > INT32_MAX || k_total > INT32_MAX)
         return GEMM_ERR_INVALID_ARG;
-    const int per = (16 << swizzle) / 2;
+    const int bits = swz_bits_of(swizzle);
+    const int per = (16 << bits) / 2;
     if (major == GEMM_K_MAJOR ? (bk % per != 0) : (rows % per != 0))
         return GEMM_ERR_UNSUPPORTED;
     if (ld < (major == GEMM_K_MAJOR ? k_total : rows_total))
@@ -867,14 +869,14 @@ gemm_status_t gemm_debug_stage_image(const void *src, int major, int swizzle, in
     if (s != GEMM_OK)
         return s;
     CUtensorMap map;
-    if ((s = encode_operand(&map, 1, src, major, swizzle, rows_total, k_total, ld, rows, bk)) != GEMM_OK)
+    if ((s = encode_operand(&map, 1, src, major, bits, rows_total, k_total, ld, rows, bk)) != GEMM_OK)
         return s;
     const int smem = rows * bk * 2 + 1024 + 64;
     cudaError_t e = cudaFuncSetAttribute(debug_stage_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess)
         return cuda_fail(e);
     debug_stage_kernel<<<1, 128, smem, reinterpret_cast<cudaStream_t>(stream)>>>(
-        map, major, swizzle, rows, bk, static_cast<int>(mn0), static_cast<int>(k0),
+        map, major, bits, rows, bk, static_cast<int>(mn0), static_cast<int>(k0),
         static_cast<uint8_t *>(out), status);
     e = cudaGetLastError();
     if (e != cudaSuccess)

@@ -77,7 +77,7 @@ struct KParams {
     int tiles_m, tiles_n, num_tiles;
     float alpha, beta;
     int a_mn, b_mn;        // 0 K-major, 1 MN-major
-    int a_swz, b_swz;      // swizzle bits: 1 SW32, 2 SW64, 3 SW128
+    int a_swz, b_swz;      // swizzle bits: 0 none, 1 SW32, 2 SW64, 3 SW128
     int in_bf16;           // 0 fp16, 1 bf16
     int out_type;          // 0 f32, 1 bf16, 2 f16
     int epi_swizzle;       // 1: staging chunks in SW128 layout; 0: plain rows
@@ -443,8 +443,8 @@ __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uin
     unsigned long long *const stats = p.stats;
     const bool multicast = CG == 2 && !(p.flags & kFlagPairForward);
     const uint32_t idesc = make_idesc_f16(C::UMMA_M, BN, p.in_bf16, p.a_mn, p.b_mn);
-    const OperandPacking pa = operand_packing(p.a_mn, p.a_swz, BK);
-    const OperandPacking pb = operand_packing(p.b_mn, p.b_swz, BK);
+    const OperandPacking pa = operand_packing(p.a_mn, p.a_swz, C::BM, BK);
+    const OperandPacking pb = operand_packing(p.b_mn, p.b_swz, C::BN_LOCAL, BK);
     const uint64_t a_desc0 = make_smem_desc(smem, pa.lbo, pa.sbo, pa.swz);
     const uint64_t b_desc0 = make_smem_desc(smem + C::A_BYTES, pb.lbo, pb.sbo, pb.swz);
     uint32_t a_off[C::KSLICES], b_off[C::KSLICES];

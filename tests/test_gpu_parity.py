@@ -29,6 +29,7 @@ def g():
 
 
 DEV = "cuda:0"
+SWZ_PARAM = {"sw32": 1, "sw64": 2, "sw128": 3, "none": 4}  # gemm_swizzle_t
 TDT = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}
 
 
@@ -112,7 +113,7 @@ def sample_entries(M, N, n=2048, seed=0):
 # ---------------------------------------------------------------- address tables (bit-exact)
 
 @pytest.mark.parametrize("major", ["K", "MN"])
-@pytest.mark.parametrize("mode", ["sw32", "sw64", "sw128"])
+@pytest.mark.parametrize("mode", ["sw32", "sw64", "sw128", "none"])
 @pytest.mark.parametrize("rows,bk", [(128, 64), (256, 64), (128, 32), (64, 64), (128, 128)])
 def test_device_descriptor_words_match_oracle(g, major, mode, rows, bk):
     W = L.swizzle_width(mode)
@@ -123,7 +124,7 @@ def test_device_descriptor_words_match_oracle(g, major, mode, rows, bk):
     n = bk // 16
     out = torch.zeros(n + 1, dtype=torch.int64, device=DEV)
     base = 3 * 1024 * 16
-    g.gemm_debug_descriptors(0 if major == "K" else 1, L.MODE_BITS[mode], rows, bk, base, n, 1, 128, 1,
+    g.gemm_debug_descriptors(0 if major == "K" else 1, SWZ_PARAM[mode], rows, bk, base, n, 1, 128, 1,
                              0, 1, out)
     words = [int(x) & (2 ** 64 - 1) for x in out.cpu().tolist()]
     for j in range(n):
@@ -155,7 +156,7 @@ def _stage_image(g, major, mode, rows, bk, rows_total=None, k_total=None, mn0=0,
     ld = stored.shape[1]
     src = torch.from_numpy(stored.view(np.int16)).to(DEV)
     out = torch.zeros(rows * bk, dtype=torch.int16, device=DEV)
-    g.gemm_debug_stage_image(src, 0 if major == "K" else 1, L.MODE_BITS[mode], rows_total, k_total, ld,
+    g.gemm_debug_stage_image(src, 0 if major == "K" else 1, SWZ_PARAM[mode], rows_total, k_total, ld,
                              rows, bk, mn0, k0, out)
     torch.cuda.synchronize()
     st, word = g.gemm_last_device_status()
@@ -164,7 +165,7 @@ def _stage_image(g, major, mode, rows, bk, rows_total=None, k_total=None, mn0=0,
 
 
 @pytest.mark.parametrize("major", ["K", "MN"])
-@pytest.mark.parametrize("mode", ["sw32", "sw64", "sw128"])
+@pytest.mark.parametrize("mode", ["sw32", "sw64", "sw128", "none"])
 @pytest.mark.parametrize("rows,bk", [(128, 64), (128, 32), (256, 64), (128, 128)])
 def test_tma_stage_image_matches_swizzle_map(g, major, mode, rows, bk):
     W = L.swizzle_width(mode)
@@ -246,13 +247,20 @@ def test_tile_configs(g, cg, tile_n, bk, a_major, b_major):
              options=dict(cta_group=cg, tile_n=tile_n, block_k=bk))
 
 
-@pytest.mark.parametrize("swz_a", [1, 2, 3])
-@pytest.mark.parametrize("swz_b", [1, 2, 3])
+@pytest.mark.parametrize("swz_a", [1, 2, 3, 4])
+@pytest.mark.parametrize("swz_b", [1, 2, 3, 4])
 @pytest.mark.parametrize("a_major,b_major", [("K", "MN"), ("MN", "K")])
 @pytest.mark.parametrize("bk", [64, 128])
 def test_swizzle_modes(g, swz_a, swz_b, a_major, b_major, bk):
     run_case(g, 256, 256, 320, a_major=a_major, b_major=b_major, dist="int4", exact=True,
              options=dict(swizzle_a=swz_a, swizzle_b=swz_b, tile_n=128, block_k=bk))
+
+
+@pytest.mark.parametrize("cg", [1, 2])
+def test_no_swizzle_operands_all_majors(g, cg):
+    for am, bm in (("K", "K"), ("K", "MN"), ("MN", "K"), ("MN", "MN")):
+        run_case(g, 300, 264, 200, a_major=am, b_major=bm, dist="int4", exact=True,
+                 options=dict(cta_group=cg, swizzle_a=4, swizzle_b=4))
 
 
 def test_unswizzled_epilogue_staging(g):
