@@ -61,6 +61,11 @@ WORKLOADS = {
         alpha=1.0, beta=0.0, dist="uniform", scale=1.0, seed=100, options=None,
         desc="64 independent bf16 problems, M_i uniform in {128..4096} step 128 (rng 5), N=4096, K=2048, "
              "U[-1,1], bf16 out, one launch over a device-side problem list"),
+    "square8192_fp8_pair": dict(
+        M=8192, N=8192, K=8192, a_major="K", b_major="K", out="bf16", alpha=1.0, beta=0.0, dist="uniform",
+        scale=1.0, seed=40, options=dict(cta_group=2, tile_n=256), in_fmt="e4m3", b_fmt="e4m3", peak_ratio=2.0,
+        desc="8192^3 fp8 E4M3 x E4M3 (kind::f8f6f4), A and B K-major, U[-1,1], fp32 accumulate, bf16 out, "
+             "cta_group::2 CTA pairs"),
     "single_tile_128x128x32_f16": dict(
         M=128, N=128, K=32, a_major="K", b_major="MN", out="f32", alpha=1.0, beta=0.0, dist="uniform",
         scale=1.0, seed=0, options=None, in_fmt="f16",
@@ -189,11 +194,12 @@ def _torch_inputs(wl, dev, pinned=False):
     import torch
     in_fmt = wl.get("in_fmt", "bf16")
     M, N, K = wl["M"], wl["N"], wl["K"]
+    b_fmt = wl.get("b_fmt", in_fmt)
     A = si.matrix_bits(wl["seed"], M, K, wl["dist"], in_fmt, scale=wl["scale"], transpose=wl["a_major"] == "MN")
-    B = si.matrix_bits(wl["seed"] + 1, K, N, wl["dist"], in_fmt, scale=wl["scale"], transpose=wl["b_major"] == "K")
+    B = si.matrix_bits(wl["seed"] + 1, K, N, wl["dist"], b_fmt, scale=wl["scale"], transpose=wl["b_major"] == "K")
     C = (si.matrix_bits(wl["seed"] + 2, M, N, wl["dist"], wl["out"], scale=wl["scale"])
          if wl["beta"] != 0.0 else None)
-    host = [si.torch_from_bits(A, in_fmt), si.torch_from_bits(B, in_fmt),
+    host = [si.torch_from_bits(A, in_fmt), si.torch_from_bits(B, b_fmt),
             si.torch_from_bits(C, wl["out"]) if C is not None else None]
     if pinned:
         host = [h.pin_memory() if h is not None else None for h in host]
@@ -222,9 +228,13 @@ class GemmJob:
         self.options = options
         self.flops = 2.0 * self.M * self.N * self.K
         # arguments marshalled once; each step is one call into the C ABI
+        fp8 = None
+        if wl.get("in_fmt") in ("e4m3", "e5m2"):
+            codes = {"e4m3": g.FP8_E4M3, "e5m2": g.FP8_E5M2}
+            fp8 = (codes[wl["in_fmt"]], codes[wl.get("b_fmt", wl["in_fmt"])])
         self.call = g.GemmCall(self.in_type, self.M, self.N, self.K, self.A, self.am, self.A.stride(0), self.B,
                                self.bm, self.B.stride(0), self.C, self.N if self.C is not None else 0, self.D,
-                               self.N, self.dt, wl["alpha"], wl["beta"], options=options, stream=stream)
+                               self.N, self.dt, wl["alpha"], wl["beta"], options=options, stream=stream, fp8=fp8)
 
     def step(self):
         self.call()
@@ -449,7 +459,9 @@ def main():
               "parallelism": f"replicas x{max(ws, args.gpus)}"}
     if args.options:
         config["options"] = json.loads(args.options)
-    metric = "GEMM TFLOP/s (bf16 in, fp32 accum)"
+    metric = "GEMM TFLOP/s (bf16 in, fp32 accum) and % of GB300 dense BF16 tensor peak"
+    if wl.get("in_fmt") in ("e4m3", "e5m2"):
+        metric = "GEMM TFLOP/s (fp8 in, fp32 accum) and % of GB300 dense FP8 tensor peak"
 
     if args.impl == "reference":
         if rank == 0:
@@ -477,14 +489,17 @@ def main():
                 "algorithmic_bytes": bytes_alg}
     else:
         achieved = flops / (kernel_ms / 1e3) / 1e12
-        peak = float(peaks.get("bf16_tflops", 1900.0))
+        ratio = float(wl.get("peak_ratio", 1.0))  # fp8: nominal 4.5 / 2.25 PFLOP/s dense over bf16
+        peak = float(peaks.get("bf16_tflops", 1900.0)) * ratio
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "peak_source": f"{peak_src} bf16_tflops (burst)",
-                "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
+                "peak_source": f"{peak_src} bf16_tflops (burst)" + (f" x {ratio:g} (nominal fp8/bf16 ratio)"
+                                                                     if ratio != 1.0 else ""),
+                "frac_of_sustained": achieved / (float(peaks.get("bf16_tflops_sustained", peak)) * ratio),
                 "traffic": traffic, "kernel_ms": kernel_ms, "algorithmic_bytes": bytes_alg}
     line = {"metric": metric, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": r["total_ms"] / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config,
+            "scaling": "weak", "vs_baseline": None, "dtype": wl.get("in_fmt", "bf16"), "data": "synthetic",
+            "config": config,
             "e2e": {"value": flops / (r["e2e_ms"] / 1e3) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
                     "ms_per_step": r["e2e_ms"]},

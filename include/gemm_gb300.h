@@ -156,6 +156,33 @@ gemm_status_t gemm_ex(int in_type, int64_t M, int64_t N, int64_t K,
                       float alpha, float beta, const gemm_options_t *opts,
                       gemm_stream_t stream);
 
+/* 8-bit float operand formats (tcgen05.mma kind::f8f6f4). */
+typedef enum { GEMM_FP8_E4M3 = 0, GEMM_FP8_E5M2 = 1 } gemm_fp8_t;
+
+/*
+ * gemm_fp8 / gemm_fp8_ex: the same GEMM with 8-bit float operands, A and B
+ * each E4M3 or E5M2 (they may differ), fp32 accumulation, output d_type.
+ * The descriptors are the same as for 16-bit operands: one 16-byte core-matrix
+ * cell holds 16 fp8 values ("LBO, SBO and SWZ for a tcgen05 tile", section 4)
+ * and one MMA consumes 32 of them along K. Leading dimensions lda and ldb are
+ * counted in elements (bytes) and must be multiples of 16; the other rules
+ * are those above. opts may be NULL.
+ */
+gemm_status_t gemm_fp8(int64_t M, int64_t N, int64_t K,
+                       const void *A, gemm_fp8_t a_format, gemm_major_t a_major, int64_t lda,
+                       const void *B, gemm_fp8_t b_format, gemm_major_t b_major, int64_t ldb,
+                       const void *C, int64_t ldc,
+                       void *D, int64_t ldd, gemm_out_t d_type,
+                       float alpha, float beta, gemm_stream_t stream);
+
+gemm_status_t gemm_fp8_ex(int64_t M, int64_t N, int64_t K,
+                          const void *A, gemm_fp8_t a_format, gemm_major_t a_major, int64_t lda,
+                          const void *B, gemm_fp8_t b_format, gemm_major_t b_major, int64_t ldb,
+                          const void *C, int64_t ldc,
+                          void *D, int64_t ldd, gemm_out_t d_type,
+                          float alpha, float beta, const gemm_options_t *opts,
+                          gemm_stream_t stream);
+
 /*
  * Grouped GEMM: num_problems independent problems in one launch. The
  * host list is read during the call; the library writes the device-side

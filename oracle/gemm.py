@@ -21,7 +21,7 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-FMT = {"f16": 0, "bf16": 1, "f32": 2}
+FMT = {"f16": 0, "bf16": 1, "f32": 2, "e4m3": 3, "e5m2": 4}
 MAJOR = {"K": 0, "MN": 1}
 
 
@@ -43,11 +43,11 @@ def _load():
             lib = ctypes.CDLL(_LIB)
             i64, vp, dp = ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p
             lib.oracle_gemm.argtypes = [i64, i64, i64, vp, ctypes.c_int, ctypes.c_int, i64,
-                                        vp, ctypes.c_int, i64, vp, ctypes.c_int, i64,
+                                        vp, ctypes.c_int, ctypes.c_int, i64, vp, ctypes.c_int, i64,
                                         ctypes.c_double, ctypes.c_double, dp, dp, ctypes.c_int]
             lib.oracle_gemm.restype = ctypes.c_int
             lib.oracle_gemm_entries.argtypes = [i64, i64, i64, vp, ctypes.c_int, ctypes.c_int, i64,
-                                                vp, ctypes.c_int, i64, vp, ctypes.c_int, i64,
+                                                vp, ctypes.c_int, ctypes.c_int, i64, vp, ctypes.c_int, i64,
                                                 ctypes.c_double, ctypes.c_double, i64, vp, vp,
                                                 dp, dp, ctypes.c_int]
             lib.oracle_gemm_entries.restype = ctypes.c_int
@@ -56,6 +56,8 @@ def _load():
             lib.oracle_round_bits.argtypes = [dp, i64, ctypes.c_int, vp]
             lib.oracle_round_bits.restype = None
             lib.oracle_num_threads.restype = ctypes.c_int
+            lib.oracle_decode.argtypes = [ctypes.c_int, ctypes.c_uint32]
+            lib.oracle_decode.restype = ctypes.c_double
             _lib = lib
     return _lib
 
@@ -68,7 +70,7 @@ def num_threads() -> int:
     return _load().oracle_num_threads()
 
 
-def gemm(M, N, K, A, B, *, in_fmt="bf16", a_major="K", b_major="K", lda=None, ldb=None,
+def gemm(M, N, K, A, B, *, in_fmt="bf16", b_fmt=None, a_major="K", b_major="K", lda=None, ldb=None,
          C=None, c_fmt="f32", ldc=None, alpha=1.0, beta=0.0, threads=0):
     """Full fp64 product. ``A``, ``B``, ``C`` are bit-pattern arrays in storage layout.
 
@@ -85,7 +87,8 @@ def gemm(M, N, K, A, B, *, in_fmt="bf16", a_major="K", b_major="K", lda=None, ld
         ldc = ldc if ldc is not None else N
     D = np.empty((M, N), dtype=np.float64)
     S = np.empty((M, N), dtype=np.float64)
-    rc = lib.oracle_gemm(M, N, K, _ptr(A), FMT[in_fmt], MAJOR[a_major], lda, _ptr(B), MAJOR[b_major], ldb,
+    rc = lib.oracle_gemm(M, N, K, _ptr(A), FMT[in_fmt], MAJOR[a_major], lda, _ptr(B), FMT[b_fmt or in_fmt],
+                         MAJOR[b_major], ldb,
                          _ptr(C), FMT[c_fmt], ldc or 0, float(alpha), float(beta),
                          _ptr(D), _ptr(S), int(threads))
     if rc:
@@ -93,7 +96,7 @@ def gemm(M, N, K, A, B, *, in_fmt="bf16", a_major="K", b_major="K", lda=None, ld
     return D, S
 
 
-def gemm_entries(M, N, K, A, B, rows, cols, *, in_fmt="bf16", a_major="K", b_major="K", lda=None,
+def gemm_entries(M, N, K, A, B, rows, cols, *, in_fmt="bf16", b_fmt=None, a_major="K", b_major="K", lda=None,
                  ldb=None, C=None, c_fmt="f32", ldc=None, alpha=1.0, beta=0.0, threads=0):
     """fp64 result and tolerance scale at the listed (rows[e], cols[e]) entries only."""
     lib = _load()
@@ -110,12 +113,19 @@ def gemm_entries(M, N, K, A, B, rows, cols, *, in_fmt="bf16", a_major="K", b_maj
     D = np.empty(n, dtype=np.float64)
     S = np.empty(n, dtype=np.float64)
     rc = lib.oracle_gemm_entries(M, N, K, _ptr(A), FMT[in_fmt], MAJOR[a_major], lda, _ptr(B),
-                                 MAJOR[b_major], ldb, _ptr(C), FMT[c_fmt], ldc or 0,
+                                 FMT[b_fmt or in_fmt], MAJOR[b_major], ldb, _ptr(C), FMT[c_fmt], ldc or 0,
                                  float(alpha), float(beta), n, _ptr(rows), _ptr(cols),
                                  _ptr(D), _ptr(S), int(threads))
     if rc:
         raise ValueError("oracle_gemm_entries: entry out of range")
     return D, S
+
+
+def decode(bits, fmt: str) -> np.ndarray:
+    """Exact values of stored bit patterns in format ``fmt``."""
+    lib = _load()
+    b = np.asarray(bits).reshape(-1)
+    return np.array([lib.oracle_decode(FMT[fmt], int(x)) for x in b], dtype=np.float64).reshape(np.shape(bits))
 
 
 def round_to(x, fmt: str) -> np.ndarray:

@@ -8,7 +8,8 @@
  *
  *   D[i][j] = alpha * sum_{k=0}^{K-1} A(i,k) * B(k,j) + beta * C[i][j]
  *
- * in IEEE double precision, over the exact values of the fp16/bf16 inputs.
+ * in IEEE double precision, over the exact values of the fp16/bf16 (or fp8
+ * E4M3/E5M2, A and B each in its own format) inputs.
  * The accumulate-into-D form is the one the tensor-core pages state for one
  * MMA (gpu-kernels part 6, "Tensor Cores, layouts, and swizzling", opening
  * paragraph: D = A.B + C; zhenwei tcgen05 page, "Overview" and the
@@ -36,7 +37,7 @@
 #include <omp.h>
 #endif
 
-enum { ORC_F16 = 0, ORC_BF16 = 1, ORC_F32 = 2 };
+enum { ORC_F16 = 0, ORC_BF16 = 1, ORC_F32 = 2, ORC_E4M3 = 3, ORC_E5M2 = 4 };
 
 /* IEEE binary16: 1 sign, 5 exponent (bias 15), 10 fraction bits. */
 static double decode_f16(uint16_t h)
@@ -63,6 +64,60 @@ static double decode_bf16(uint16_t b)
     return (double)x;
 }
 
+/*
+ * 8-bit floats (the fp8 family a 16-byte core-matrix cell holds 16 of, "LBO,
+ * SBO and SWZ for a tcgen05 tile", section 4; the MMA kind selects the A/B
+ * type family, "06 Blackwell Tensor Core - tcgen05 MMA"):
+ *   E4M3: 1 sign, 4 exponent (bias 7), 3 fraction bits; no infinities, the
+ *         all-ones exponent and fraction is NaN; largest finite 448.
+ *   E5M2: 1 sign, 5 exponent (bias 15), 2 fraction bits, IEEE-style
+ *         infinities and NaNs; largest finite 57344.
+ */
+static double decode_e4m3(uint8_t b)
+{
+    int sign = (b >> 7) & 1;
+    int e = (b >> 3) & 0xf;
+    int f = b & 7;
+    double v;
+    if (e == 15 && f == 7)
+        v = NAN;
+    else if (e == 0)
+        v = ldexp((double)f, -9);                  /* f * 2^-6 * 2^-3 */
+    else
+        v = ldexp((double)(f | 8), e - 10);        /* 1.f * 2^(e-7) */
+    return sign ? -v : v;
+}
+
+static double decode_e5m2(uint8_t b)
+{
+    int sign = (b >> 7) & 1;
+    int e = (b >> 2) & 0x1f;
+    int f = b & 3;
+    double v;
+    if (e == 31)
+        v = f ? NAN : INFINITY;
+    else if (e == 0)
+        v = ldexp((double)f, -16);                 /* f * 2^-14 * 2^-2 */
+    else
+        v = ldexp((double)(f | 4), e - 17);        /* 1.f * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+double oracle_decode(int fmt, uint32_t bits)
+{
+    switch (fmt) {
+    case ORC_F16: return decode_f16((uint16_t)bits);
+    case ORC_BF16: return decode_bf16((uint16_t)bits);
+    case ORC_E4M3: return decode_e4m3((uint8_t)bits);
+    case ORC_E5M2: return decode_e5m2((uint8_t)bits);
+    default: {
+        float x;
+        memcpy(&x, &bits, sizeof x);
+        return (double)x;
+    }
+    }
+}
+
 static double decode_f32(uint32_t u)
 {
     float x;
@@ -75,6 +130,8 @@ static double load(const void *p, int fmt, int64_t idx)
     switch (fmt) {
     case ORC_F16: return decode_f16(((const uint16_t *)p)[idx]);
     case ORC_BF16: return decode_bf16(((const uint16_t *)p)[idx]);
+    case ORC_E4M3: return decode_e4m3(((const uint8_t *)p)[idx]);
+    case ORC_E5M2: return decode_e5m2(((const uint8_t *)p)[idx]);
     default: return decode_f32(((const uint32_t *)p)[idx]);
     }
 }
@@ -105,7 +162,7 @@ int oracle_num_threads(void)
  */
 int oracle_gemm(int64_t M, int64_t N, int64_t K,
                 const void *A, int in_fmt, int a_major, int64_t lda,
-                const void *B, int b_major, int64_t ldb,
+                const void *B, int b_fmt, int b_major, int64_t ldb,
                 const void *C, int c_fmt, int64_t ldc,
                 double alpha, double beta,
                 double *D, double *S, int nthreads)
@@ -126,7 +183,7 @@ int oracle_gemm(int64_t M, int64_t N, int64_t K,
         for (int64_t k = 0; k < K; ++k) {
             double a = a_at(A, in_fmt, a_major, lda, i, k);
             for (int64_t j = 0; j < N; ++j) {
-                double p = a * b_at(B, in_fmt, b_major, ldb, k, j);
+                double p = a * b_at(B, b_fmt, b_major, ldb, k, j);
                 acc[j] += p;
                 sab[j] += fabs(p);
             }
@@ -150,7 +207,7 @@ int oracle_gemm(int64_t M, int64_t N, int64_t K,
  */
 int oracle_gemm_entries(int64_t M, int64_t N, int64_t K,
                         const void *A, int in_fmt, int a_major, int64_t lda,
-                        const void *B, int b_major, int64_t ldb,
+                        const void *B, int b_fmt, int b_major, int64_t ldb,
                         const void *C, int c_fmt, int64_t ldc,
                         double alpha, double beta,
                         int64_t n_entries, const int64_t *rows, const int64_t *cols,
@@ -173,7 +230,7 @@ int oracle_gemm_entries(int64_t M, int64_t N, int64_t K,
         }
         double acc = 0.0, sab = 0.0;
         for (int64_t k = 0; k < K; ++k) {
-            double p = a_at(A, in_fmt, a_major, lda, i, k) * b_at(B, in_fmt, b_major, ldb, k, j);
+            double p = a_at(A, in_fmt, a_major, lda, i, k) * b_at(B, b_fmt, b_major, ldb, k, j);
             acc += p;
             sab += fabs(p);
         }

@@ -352,37 +352,45 @@ def stage_element_offset(major: str, mode: str, rows: int, bk: int, esize: int, 
 def stage_slice_desc(major: str, mode: str, rows: int, bk: int, esize: int, j: int, base: int) -> SmemDesc:
     """Descriptor of K slice j of a stage packed by ``stage_element_offset``.
 
+    One MMA slice spans 32 bytes of K per row: 16 elements of a 16-bit type
+    (kind::f16) or 32 of an 8-bit type (kind::f8f6f4). For MN-major operands
+    the slice is that many K rows, i.e. kper / 8 bands of SBO.
     Without swizzle the 16 B cells are the atoms: K-major then needs LBO =
     the distance between K cells (one box, rows*16 B) and SBO = 128 B between
     8-row groups; MN-major needs SBO = one box (BK*16 B) between 8-element MN
     groups and LBO = 128 B between 8-row K bands.
     """
     W = swizzle_width(mode)
-    kbytes = 16 * esize  # one K=16 slice of a 16-bit type: 32 bytes
+    kbytes = 32                 # K bytes per row consumed by one MMA
+    kper = kbytes // esize      # K elements per MMA slice
     if major == "K":
         off = j * kbytes
         start = base + (off // W) * rows * W + off % W
         lbo = rows * 16 if mode == "none" else 16
         return SmemDesc(start=start, lbo=lbo, sbo=8 * W, base_offset=0, swz=SWZ_CODE[mode])
     if mode == "none":
-        return SmemDesc(start=base + j * 2 * 128, lbo=128, sbo=bk * 16, base_offset=0, swz=0)
+        return SmemDesc(start=base + j * (kper // 8) * 128, lbo=128, sbo=bk * 16, base_offset=0, swz=0)
     sbo = 8 * W
-    return SmemDesc(start=base + j * 2 * sbo, lbo=bk * W, sbo=sbo, base_offset=0, swz=SWZ_CODE[mode])
+    return SmemDesc(start=base + j * (kper // 8) * sbo, lbo=bk * W, sbo=sbo, base_offset=0, swz=SWZ_CODE[mode])
 
 
 # ---------------------------------------------------------------------------
 # Instruction descriptor for kind::f16 (reading c2 above).
 # ---------------------------------------------------------------------------
 
-FMT_F16, FMT_BF16 = 0, 1
+FMT_F16, FMT_BF16 = 0, 1        # kind::f16 A/B formats
+FMT_E4M3, FMT_E5M2 = 0, 1       # kind::f8f6f4 A/B formats
 DFMT_F16, DFMT_F32 = 0, 1
 
 
-def encode_idesc(m: int, n: int, ab_fmt: int, d_fmt: int, a_mn_major: int, b_mn_major: int) -> int:
+def encode_idesc(m: int, n: int, ab_fmt: int, d_fmt: int, a_mn_major: int, b_mn_major: int,
+                 b_fmt: int | None = None) -> int:
+    """Instruction descriptor; ``b_fmt`` defaults to A's format."""
+    b_fmt = ab_fmt if b_fmt is None else b_fmt
     word = 0
     word |= (d_fmt & 3) << 4
     word |= (ab_fmt & 7) << 7
-    word |= (ab_fmt & 7) << 10
+    word |= (b_fmt & 7) << 10
     word |= (a_mn_major & 1) << 15
     word |= (b_mn_major & 1) << 16
     word |= ((n >> 3) & 0x3F) << 17

@@ -78,7 +78,16 @@ def _draw(seed: int, dist: str, start: int, count: int, scale: float) -> np.ndar
 
 
 def to_storage(x: np.ndarray, dtype: str) -> np.ndarray:
-    """Round float64 values to ``dtype`` ('f16', 'bf16', 'f32'); return the bit patterns."""
+    """Round float64 values to ``dtype`` ('f16', 'bf16', 'f32', 'e4m3', 'e5m2'); return the bits.
+
+    fp8 rounding (ties to even, through float32) uses PyTorch's float8_e4m3fn and
+    float8_e5m2 conversions; the inputs stay far inside both formats' ranges.
+    """
+    if dtype in ("e4m3", "e5m2"):
+        import torch
+        tdt = torch.float8_e4m3fn if dtype == "e4m3" else torch.float8_e5m2
+        t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(tdt)
+        return t.view(torch.uint8).numpy().copy()
     if dtype == "f16":
         return x.astype(np.float16).view(np.uint16)
     if dtype == "f32":
@@ -110,7 +119,7 @@ def matrix_bits(seed: int, rows: int, cols: int, dist: str, dtype: str,
     The result is a 2-D array of the stored shape (with the padding columns).
     """
     n = rows * cols
-    bits_dtype = np.uint32 if dtype == "f32" else np.uint16
+    bits_dtype = np.uint32 if dtype == "f32" else (np.uint8 if dtype in ("e4m3", "e5m2") else np.uint16)
     flat = np.empty(n, dtype=bits_dtype)
     for s in range(0, n, _CHUNK):
         c = min(_CHUNK, n - s)
@@ -136,6 +145,10 @@ def bits_to_float64(bits: np.ndarray, dtype: str) -> np.ndarray:
         return bits.view(np.float32).astype(np.float64)
     if dtype == "bf16":
         return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    if dtype in ("e4m3", "e5m2"):
+        import torch
+        tdt = torch.float8_e4m3fn if dtype == "e4m3" else torch.float8_e5m2
+        return torch.from_numpy(np.ascontiguousarray(bits, dtype=np.uint8)).view(tdt).double().numpy()
     raise ValueError(dtype)
 
 
@@ -148,4 +161,6 @@ def torch_from_bits(bits: np.ndarray, dtype: str):
         return t.view(torch.float16 if dtype == "f16" else torch.bfloat16)
     if dtype == "f32":
         return torch.from_numpy(b.view(np.int32)).view(torch.float32)
+    if dtype in ("e4m3", "e5m2"):
+        return torch.from_numpy(b.view(np.uint8))  # raw bytes; the library reads them as fp8
     raise ValueError(dtype)

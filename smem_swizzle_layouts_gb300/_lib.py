@@ -24,6 +24,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = range(6)
 K_MAJOR, MN_MAJOR = 0, 1
 OUT_F32, OUT_BF16, OUT_F16 = 0, 1, 2
+FP8_E4M3, FP8_E5M2 = 0, 1
 SWIZZLE_AUTO, SWIZZLE_32B, SWIZZLE_64B, SWIZZLE_128B, SWIZZLE_NONE = 0, 1, 2, 3, 4
 
 _i64, _vp, _f, _int, _u32, _u64 = (ctypes.c_int64, ctypes.c_void_p, ctypes.c_float, ctypes.c_int,
@@ -45,6 +46,9 @@ _single = [_i64, _i64, _i64, _vp, _int, _i64, _vp, _int, _i64, _vp, _i64, _vp, _
 _lib.gemm_bf16.argtypes = _single
 _lib.gemm_f16.argtypes = _single
 _lib.gemm_ex.argtypes = [_int] + _single[:-1] + [ctypes.POINTER(GemmOptions), _vp]
+_fp8 = [_i64, _i64, _i64, _vp, _int, _int, _i64, _vp, _int, _int, _i64, _vp, _i64, _vp, _i64, _int, _f, _f]
+_lib.gemm_fp8.argtypes = _fp8 + [_vp]
+_lib.gemm_fp8_ex.argtypes = _fp8 + [ctypes.POINTER(GemmOptions), _vp]
 _grouped = [ctypes.POINTER(GemmProblem), _int, _int, _int, _int, _f, _f, _vp, ctypes.c_size_t, _vp]
 _lib.gemm_bf16_grouped.argtypes = _grouped
 _lib.gemm_f16_grouped.argtypes = _grouped
@@ -60,11 +64,13 @@ _lib.gemm_debug_descriptors.argtypes = [_int, _int, _int, _int, _u32, _int, _int
 _lib.gemm_debug_stage_image.argtypes = [_vp, _int, _int, _i64, _i64, _i64, _int, _int, _i64, _i64, _vp, _vp]
 _lib.gemm_debug_inject_timeout.argtypes = [_int]
 _lib.gemm_debug_inject_timeout.restype = None
-for _name in ("gemm_bf16", "gemm_f16", "gemm_ex", "gemm_bf16_grouped", "gemm_f16_grouped", "gemm_bf16_grouped_noalloc",
+for _name in ("gemm_bf16", "gemm_f16", "gemm_ex", "gemm_fp8", "gemm_fp8_ex", "gemm_bf16_grouped", "gemm_f16_grouped",
+              "gemm_bf16_grouped_noalloc",
               "gemm_last_device_status", "gemm_debug_descriptors", "gemm_debug_stage_image"):
     getattr(_lib, _name).restype = _int
 
-EXPORTED = ("gemm_bf16", "gemm_f16", "gemm_ex", "gemm_grouped_workspace_size", "gemm_bf16_grouped",
+EXPORTED = ("gemm_bf16", "gemm_f16", "gemm_ex", "gemm_fp8", "gemm_fp8_ex", "gemm_grouped_workspace_size",
+            "gemm_bf16_grouped",
             "gemm_f16_grouped", "gemm_bf16_grouped_noalloc", "gemm_last_device_status", "gemm_status_string", "gemm_launch_count",
             "gemm_debug_descriptors", "gemm_debug_stage_image", "gemm_debug_inject_timeout")
 
@@ -139,17 +145,37 @@ class GemmCall:
     """
 
     def __init__(self, in_type, M, N, K, A, a_major, lda, B, b_major, ldb, C, ldc, D, ldd, d_type, alpha, beta,
-                 options=None, stream=None):
+                 options=None, stream=None, fp8=None):
+        """``in_type`` 0 fp16 / 1 bf16; or ``fp8=(a_format, b_format)`` for gemm_fp8_ex."""
         self._opts_ref = _opts(options)  # keeps the options struct alive
-        self._args = (_int(in_type), _i64(M), _i64(N), _i64(K), _vp(_addr(A)), _int(a_major), _i64(lda),
-                      _vp(_addr(B)), _int(b_major), _i64(ldb), _vp(_addr(C)), _i64(ldc), _vp(_addr(D)),
-                      _i64(ldd), _int(d_type), _f(alpha), _f(beta), self._opts_ref, _vp(_stream(stream)))
-        self._fn = _lib.gemm_ex
+        tail = (_vp(_addr(C)), _i64(ldc), _vp(_addr(D)), _i64(ldd), _int(d_type), _f(alpha), _f(beta),
+                self._opts_ref, _vp(_stream(stream)))
+        if fp8 is not None:
+            self._args = (_i64(M), _i64(N), _i64(K), _vp(_addr(A)), _int(fp8[0]), _int(a_major), _i64(lda),
+                          _vp(_addr(B)), _int(fp8[1]), _int(b_major), _i64(ldb)) + tail
+            self._fn = _lib.gemm_fp8_ex
+        else:
+            self._args = (_int(in_type), _i64(M), _i64(N), _i64(K), _vp(_addr(A)), _int(a_major), _i64(lda),
+                          _vp(_addr(B)), _int(b_major), _i64(ldb)) + tail
+            self._fn = _lib.gemm_ex
 
     def __call__(self):
         st = self._fn(*self._args)
         if st != OK:
-            raise GemmError(st, "gemm_ex")
+            raise GemmError(st, self._fn.__name__)
+
+
+def gemm_fp8(M, N, K, A, a_format, a_major, lda, B, b_format, b_major, ldb, C, ldc, D, ldd, d_type, alpha, beta,
+             stream=None):
+    _check(_lib.gemm_fp8(M, N, K, _addr(A), a_format, a_major, lda, _addr(B), b_format, b_major, ldb, _addr(C),
+                         ldc, _addr(D), ldd, d_type, alpha, beta, _stream(stream)), "gemm_fp8")
+
+
+def gemm_fp8_ex(M, N, K, A, a_format, a_major, lda, B, b_format, b_major, ldb, C, ldc, D, ldd, d_type, alpha,
+                beta, options=None, stream=None):
+    _check(_lib.gemm_fp8_ex(M, N, K, _addr(A), a_format, a_major, lda, _addr(B), b_format, b_major, ldb,
+                            _addr(C), ldc, _addr(D), ldd, d_type, alpha, beta, _opts(options), _stream(stream)),
+           "gemm_fp8_ex")
 
 
 def gemm_grouped_workspace_size(num_problems: int) -> int:

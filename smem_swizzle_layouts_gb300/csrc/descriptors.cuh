@@ -81,28 +81,37 @@ G300_HD OperandPacking operand_packing(int mn_major, int swz_bits, int rows, int
     return p;
 }
 
-// Byte offset of K slice j (16 elements of a 16-bit type) from the stage start.
-G300_HD uint32_t slice_byte_offset(int mn_major, int swz_bits, int rows, int j)
+// Byte offset of K slice j from the stage start. One MMA consumes 32 bytes of
+// K per row: 16 elements of a 16-bit type (kind::f16) or 32 of an 8-bit type
+// (kind::f8f6f4, esize 1). MN-major operands store one K row per W bytes
+// (16 without swizzle), so a slice there is 32 / esize rows.
+G300_HD uint32_t slice_byte_offset(int mn_major, int swz_bits, int rows, int j, int esize = 2)
 {
     const uint32_t W = swizzle_row_bytes(swz_bits);
     if (mn_major)
-        return static_cast<uint32_t>(j) * 16u * W;
+        return static_cast<uint32_t>(j) * (32u / static_cast<uint32_t>(esize)) * W;
     const uint32_t off = 32u * static_cast<uint32_t>(j);
     return (off / W) * static_cast<uint32_t>(rows) * W + off % W;
 }
 
-// kind::f16 instruction descriptor, fp32 accumulator.
-G300_HD uint32_t make_idesc_f16(int M, int N, int in_bf16, int a_mn_major, int b_mn_major)
+// Instruction descriptor, fp32 accumulator. A/B format codes depend on the
+// kind: kind::f16 0 = f16, 1 = bf16; kind::f8f6f4 0 = E4M3, 1 = E5M2.
+G300_HD uint32_t make_idesc(int M, int N, int a_fmt, int b_fmt, int a_mn_major, int b_mn_major)
 {
     uint32_t d = 0;
     d |= 1u << 4;  // D format: f32
-    d |= static_cast<uint32_t>(in_bf16 & 1) << 7;
-    d |= static_cast<uint32_t>(in_bf16 & 1) << 10;
+    d |= static_cast<uint32_t>(a_fmt & 7) << 7;
+    d |= static_cast<uint32_t>(b_fmt & 7) << 10;
     d |= static_cast<uint32_t>(a_mn_major & 1) << 15;
     d |= static_cast<uint32_t>(b_mn_major & 1) << 16;
     d |= static_cast<uint32_t>((N >> 3) & 0x3F) << 17;
     d |= static_cast<uint32_t>((M >> 4) & 0x1F) << 24;
     return d;
+}
+
+G300_HD uint32_t make_idesc_f16(int M, int N, int in_bf16, int a_mn_major, int b_mn_major)
+{
+    return make_idesc(M, N, in_bf16, in_bf16, a_mn_major, b_mn_major);
 }
 
 }  // namespace g300

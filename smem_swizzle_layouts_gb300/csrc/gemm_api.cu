@@ -36,13 +36,14 @@ int g_sms[kMaxDevices] = {};
 struct Variant {
     int cg, bn, bk, stages;
     bool grouped;
+    int esize;
     cudaError_t (*launch)(const LaunchArgs &);
     cudaError_t (*resident)(int *);
     int resident_cache[kMaxDevices];
 };
 
-#define G300_VARIANT_ROW(CG, BN, BK, ST, GR) \
-    {CG, BN, BK, ST, GR, &launch_gemm<CG, BN, BK, ST, GR>, &resident_ctas<CG, BN, BK, ST, GR>, {0}},
+#define G300_VARIANT_ROW(CG, BN, BK, ST, GR, ES) \
+    {CG, BN, BK, ST, GR, ES, &launch_gemm<CG, BN, BK, ST, GR, ES>, &resident_ctas<CG, BN, BK, ST, GR, ES>, {0}},
 Variant g_variants[] = {G300_VARIANTS(G300_VARIANT_ROW)};
 #undef G300_VARIANT_ROW
 
@@ -97,13 +98,23 @@ int resident_for(Variant &v, int dev)
     return v.resident_cache[dev];
 }
 
-Variant *find_variant(int cg, int bn, int bk, bool grouped)
+Variant *find_variant(int cg, int bn, int bk, bool grouped, int esize = 2)
 {
     for (auto &v : g_variants)
-        if (v.cg == cg && v.bn == bn && v.bk == bk && v.grouped == grouped)
+        if (v.cg == cg && v.bn == bn && v.bk == bk && v.grouped == grouped && v.esize == esize)
             return &v;
     return nullptr;
 }
+
+// Operand element type of a call: storage code for the tensor maps (0 fp16,
+// 1 bf16, 2 fp8 bytes), element size, and the MMA format code of A and B.
+struct InFmt {
+    int dcode, esize, a_fmt, b_fmt;
+};
+
+InFmt fmt16(int in_bf16) { return InFmt{in_bf16, 2, in_bf16, in_bf16}; }
+
+InFmt fmt8(int a_fmt, int b_fmt) { return InFmt{2, 1, a_fmt, b_fmt}; }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -178,19 +189,21 @@ gemm_status_t encode_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *ptr,
 
 // Operand tile map: boxes of one swizzled row (W/2 elements) along the
 // contiguous dimension, `rows` (K-major) or `bk` (MN-major) along the other.
-gemm_status_t encode_operand(CUtensorMap *m, int in_bf16, const void *ptr, int mn_major,
+gemm_status_t encode_operand(CUtensorMap *m, int dcode, const void *ptr, int mn_major,
                              int swz_bits, int64_t mn_total, int64_t k_total, int64_t ld, int rows,
                              int bk)
 {
-    const CUtensorMapDataType dt =
-        in_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    const uint32_t per = (16u << swz_bits) / 2u;
+    const CUtensorMapDataType dt = dcode == 2   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                   : dcode == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const uint32_t esize = dcode == 2 ? 1u : 2u;
+    const uint32_t per = (16u << swz_bits) / esize;
     if (!mn_major)
         return encode_2d(m, dt, ptr, static_cast<uint64_t>(k_total), static_cast<uint64_t>(mn_total),
-                         static_cast<uint64_t>(ld) * 2u, per, static_cast<uint32_t>(rows),
+                         static_cast<uint64_t>(ld) * esize, per, static_cast<uint32_t>(rows),
                          tma_swizzle(swz_bits));
     return encode_2d(m, dt, ptr, static_cast<uint64_t>(mn_total), static_cast<uint64_t>(k_total),
-                     static_cast<uint64_t>(ld) * 2u, per, static_cast<uint32_t>(bk),
+                     static_cast<uint64_t>(ld) * esize, per, static_cast<uint32_t>(bk),
                      tma_swizzle(swz_bits));
 }
 
@@ -222,7 +235,7 @@ int swz_bits_of(int opt) { return opt == GEMM_SWIZZLE_NONE ? 0 : opt; }
 // Choose the tile configuration; fills `plan` or returns an error for options
 // this build cannot honour.
 gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int sms,
-                        const gemm_options_t *o, bool grouped, Plan *plan)
+                        const gemm_options_t *o, bool grouped, Plan *plan, int esize = 2)
 {
     gemm_options_t opt = {};
     if (o)
@@ -258,19 +271,21 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
     // 128 x 256 single-CTA tile keeps BK = 64 to hold four stages.
     int bk = opt.block_k;
     if (bk == 0) {
-        if (!grouped && cg == 1 && bn == 128 && K <= 32 && opt.tile_n == 0)
+        if (esize == 1)
+            bk = (cg == 1 && bn == 256) ? 128 : 256;  // the same stage bytes as bf16
+        else if (!grouped && cg == 1 && bn == 128 && K <= 32 && opt.tile_n == 0)
             bk = 32;
         else
             bk = (cg == 1 && bn == 256) ? 64 : 128;
     }
-    if (!find_variant(cg, bn, bk, grouped))
+    if (!find_variant(cg, bn, bk, grouped, esize))
         return GEMM_ERR_UNSUPPORTED;
 
     auto pick_swz = [&](int requested, int mn_major) -> int {
         if (requested)
             return swz_bits_of(requested);
-        if (!mn_major && bk == 32)
-            return 2;  // a 64-byte K row: SW64
+        if (!mn_major && bk * esize < 128)
+            return bk * esize >= 64 ? 2 : 1;  // a K row narrower than 128 bytes: SW64 / SW32
         return 3;
     };
     plan->cg = cg;
@@ -281,7 +296,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
     // a K-major swizzled row may not be wider than the K block; an MN-major
     // atom may not be wider than the tile's MN extent
     auto fits = [&](int bits, int mn_major, int rows) {
-        const int per = (16 << bits) / 2;
+        const int per = (16 << bits) / esize;
         return mn_major ? (rows % per == 0) : (bk % per == 0);
     };
     if (!fits(plan->a_swz, a_mn, 128) || !fits(plan->b_swz, b_mn, bn / cg))
@@ -309,7 +324,7 @@ int grid_for(const Plan &pl, Variant &v, int dev, int sms, int64_t tiles)
     return static_cast<int>(clusters * per_cluster);
 }
 
-void fill_common(KParams &p, const Plan &pl, int in_bf16, int a_mn, int b_mn, int d_type,
+void fill_common(KParams &p, const Plan &pl, const InFmt &f, int a_mn, int b_mn, int d_type,
                  float alpha, float beta, unsigned int *status)
 {
     p.alpha = alpha;
@@ -318,7 +333,8 @@ void fill_common(KParams &p, const Plan &pl, int in_bf16, int a_mn, int b_mn, in
     p.b_mn = b_mn;
     p.a_swz = pl.a_swz;
     p.b_swz = pl.b_swz;
-    p.in_bf16 = in_bf16;
+    p.a_fmt = f.a_fmt;
+    p.b_fmt = f.b_fmt;
     p.out_type = d_type;
     p.epi_swizzle = pl.epi_swizzle;
     p.group_m = pl.group_m;
@@ -337,7 +353,7 @@ bool valid_enum(int major) { return major == GEMM_K_MAJOR || major == GEMM_MN_MA
 // Checks shared by single and grouped problems.
 gemm_status_t check_problem(int64_t M, int64_t N, int64_t K, const void *A, int a_mn, int64_t lda,
                             const void *B, int b_mn, int64_t ldb, const void *C, int64_t ldc,
-                            const void *D, int64_t ldd, int d_type, float beta)
+                            const void *D, int64_t ldd, int d_type, float beta, int esize = 2)
 {
     const int64_t lim = (static_cast<int64_t>(1) << 31) - 1;
     if (M < 0 || N < 0 || K < 0 || M > lim || N > lim || K > lim)
@@ -354,8 +370,8 @@ gemm_status_t check_problem(int64_t M, int64_t N, int64_t K, const void *A, int 
             return GEMM_ERR_INVALID_ARG;
         if (lda < (a_mn ? M : K) || ldb < (b_mn ? N : K))
             return GEMM_ERR_INVALID_ARG;
-        if (!aligned16(A) || !aligned16(B) || lda % 8 != 0 || ldb % 8 != 0 ||
-            lda * 2 >= (static_cast<int64_t>(1) << 40) || ldb * 2 >= (static_cast<int64_t>(1) << 40))
+        if (!aligned16(A) || !aligned16(B) || (lda * esize) % 16 != 0 || (ldb * esize) % 16 != 0 ||
+            lda * esize >= (static_cast<int64_t>(1) << 40) || ldb * esize >= (static_cast<int64_t>(1) << 40))
             return GEMM_ERR_ALIGNMENT;
     }
     if (beta != 0.0f) {
@@ -367,7 +383,7 @@ gemm_status_t check_problem(int64_t M, int64_t N, int64_t K, const void *A, int 
     return GEMM_OK;
 }
 
-gemm_status_t run_single(int in_bf16, int64_t M, int64_t N, int64_t K, const void *A, int a_major,
+gemm_status_t run_single(const InFmt &f, int64_t M, int64_t N, int64_t K, const void *A, int a_major,
                          int64_t lda, const void *B, int b_major, int64_t ldb, const void *C,
                          int64_t ldc, void *D, int64_t ldd, int d_type, float alpha, float beta,
                          const gemm_options_t *opts, cudaStream_t stream)
@@ -375,7 +391,7 @@ gemm_status_t run_single(int in_bf16, int64_t M, int64_t N, int64_t K, const voi
     if (!valid_enum(a_major) || !valid_enum(b_major) || d_type < 0 || d_type > 2)
         return GEMM_ERR_INVALID_ARG;
     const int a_mn = a_major, b_mn = b_major;
-    gemm_status_t s = check_problem(M, N, K, A, a_mn, lda, B, b_mn, ldb, C, ldc, D, ldd, d_type, beta);
+    gemm_status_t s = check_problem(M, N, K, A, a_mn, lda, B, b_mn, ldb, C, ldc, D, ldd, d_type, beta, f.esize);
     if (s != GEMM_OK || M == 0 || N == 0)
         return s;
     int dev = 0, sms = 0;
@@ -383,16 +399,16 @@ gemm_status_t run_single(int in_bf16, int64_t M, int64_t N, int64_t K, const voi
     if ((s = device_state(&dev, &status, &sms)) != GEMM_OK)
         return s;
     Plan pl;
-    if ((s = make_plan(M, N, K, a_mn, b_mn, sms, opts, false, &pl)) != GEMM_OK)
+    if ((s = make_plan(M, N, K, a_mn, b_mn, sms, opts, false, &pl, f.esize)) != GEMM_OK)
         return s;
-    Variant *v = find_variant(pl.cg, pl.bn, pl.bk, false);
+    Variant *v = find_variant(pl.cg, pl.bn, pl.bk, false, f.esize);
 
     LaunchArgs la;
     std::memset(&la, 0, sizeof(la));
     if (K > 0) {
-        if ((s = encode_operand(&la.a, in_bf16, A, a_mn, pl.a_swz, M, K, lda, 128, pl.bk)) != GEMM_OK)
+        if ((s = encode_operand(&la.a, f.dcode, A, a_mn, pl.a_swz, M, K, lda, 128, pl.bk)) != GEMM_OK)
             return s;
-        if ((s = encode_operand(&la.b, in_bf16, B, b_mn, pl.b_swz, N, K, ldb, pl.bn / pl.cg, pl.bk)) !=
+        if ((s = encode_operand(&la.b, f.dcode, B, b_mn, pl.b_swz, N, K, ldb, pl.bn / pl.cg, pl.bk)) !=
             GEMM_OK)
             return s;
     }
@@ -415,7 +431,7 @@ gemm_status_t run_single(int in_bf16, int64_t M, int64_t N, int64_t K, const voi
     if (tiles >= (static_cast<int64_t>(1) << 31))
         return GEMM_ERR_UNSUPPORTED;
     p.num_tiles = static_cast<int>(tiles);
-    fill_common(p, pl, in_bf16, a_mn, b_mn, d_type, alpha, beta, status);
+    fill_common(p, pl, f, a_mn, b_mn, d_type, alpha, beta, status);
     la.grid = grid_for(pl, *v, dev, sms, tiles);
     la.stream = stream;
     cudaError_t e = v->launch(la);
@@ -492,9 +508,9 @@ gemm_status_t run_grouped(int in_bf16, const gemm_problem_t *probs, int n, int a
             continue;
         CUtensorMap *m = maps + 4 * i;
         if (q.K > 0) {
-            if ((s = encode_operand(&m[0], in_bf16, q.A, a_mn, pl.a_swz, q.M, q.K, q.lda, 128, pl.bk)) != GEMM_OK)
+            if ((s = encode_operand(&m[0], fmt16(in_bf16).dcode, q.A, a_mn, pl.a_swz, q.M, q.K, q.lda, 128, pl.bk)) != GEMM_OK)
                 return s;
-            if ((s = encode_operand(&m[1], in_bf16, q.B, b_mn, pl.b_swz, q.N, q.K, q.ldb, pl.bn / pl.cg,
+            if ((s = encode_operand(&m[1], fmt16(in_bf16).dcode, q.B, b_mn, pl.b_swz, q.N, q.K, q.ldb, pl.bn / pl.cg,
                                     pl.bk)) != GEMM_OK)
                 return s;
         }
@@ -521,7 +537,7 @@ gemm_status_t run_grouped(int in_bf16, const gemm_problem_t *probs, int n, int a
     p.problems = reinterpret_cast<const GroupedProblemDev *>(ws);
     p.maps = reinterpret_cast<const CUtensorMap *>(static_cast<unsigned char *>(ws) + tb);
     p.num_problems = n;
-    fill_common(p, pl, in_bf16, a_mn, b_mn, d_type, alpha, beta, status);
+    fill_common(p, pl, fmt16(in_bf16), a_mn, b_mn, d_type, alpha, beta, status);
     la.grid = grid_for(pl, *v, dev, sms, tiles);
     la.stream = stream;
     e = v->launch(la);
@@ -534,8 +550,8 @@ gemm_status_t run_grouped(int in_bf16, const gemm_problem_t *probs, int n, int a
 // ---------------------------------------------------------------- inspection kernels
 
 __global__ void debug_descriptor_kernel(int major, int swz_bits, int rows, int bk, uint32_t stage_addr,
-                                        int n_slices, int umma_m, int tile_n, int in_bf16, int a_mn,
-                                        int b_mn, uint64_t *out)
+                                        int n_slices, int umma_m, int tile_n, int fmt, int esize,
+                                        int a_mn, int b_mn, uint64_t *out)
 {
     if (threadIdx.x != 0 || blockIdx.x != 0)
         return;
@@ -543,8 +559,8 @@ __global__ void debug_descriptor_kernel(int major, int swz_bits, int rows, int b
     const OperandPacking pk = operand_packing(major, swz_bits, rows, bk);
     const uint64_t d0 = make_smem_desc(stage_addr, pk.lbo, pk.sbo, pk.swz);
     for (int j = 0; j < n_slices; ++j)
-        out[j] = d0 + (slice_byte_offset(major, swz_bits, rows, j) >> 4);
-    out[n_slices] = make_idesc_f16(umma_m, tile_n, in_bf16, a_mn, b_mn);
+        out[j] = d0 + (slice_byte_offset(major, swz_bits, rows, j, esize) >> 4);
+    out[n_slices] = make_idesc(umma_m, tile_n, fmt, fmt, a_mn, b_mn);
 }
 
 __global__ void debug_stage_kernel(const __grid_constant__ CUtensorMap map, int mn_major, int swz_bits,
@@ -695,9 +711,9 @@ gemm_status_t run_grouped_noalloc(int in_bf16, const gemm_problem_t *probs, int 
             continue;
         CUtensorMap *m = maps + 4 * i;
         if (q.K > 0) {
-            if ((s = encode_operand(&m[0], in_bf16, q.A, a_mn, pl.a_swz, q.M, q.K, q.lda, 128, pl.bk)) != GEMM_OK)
+            if ((s = encode_operand(&m[0], fmt16(in_bf16).dcode, q.A, a_mn, pl.a_swz, q.M, q.K, q.lda, 128, pl.bk)) != GEMM_OK)
                 return s;
-            if ((s = encode_operand(&m[1], in_bf16, q.B, b_mn, pl.b_swz, q.N, q.K, q.ldb, pl.bn / pl.cg,
+            if ((s = encode_operand(&m[1], fmt16(in_bf16).dcode, q.B, b_mn, pl.b_swz, q.N, q.K, q.ldb, pl.bn / pl.cg,
                                     pl.bk)) != GEMM_OK)
                 return s;
         }
@@ -723,7 +739,7 @@ gemm_status_t run_grouped_noalloc(int in_bf16, const gemm_problem_t *probs, int 
     p.problems = reinterpret_cast<const GroupedProblemDev *>(ws);
     p.maps = reinterpret_cast<const CUtensorMap *>(ws + tb);
     p.num_problems = n;
-    fill_common(p, pl, in_bf16, a_mn, b_mn, d_type, alpha, beta, status);
+    fill_common(p, pl, fmt16(in_bf16), a_mn, b_mn, d_type, alpha, beta, status);
     la.grid = grid_for(pl, *v, dev, sms, tiles);
     la.stream = stream;
     e = v->launch(la);
@@ -744,7 +760,7 @@ gemm_status_t gemm_bf16(int64_t M, int64_t N, int64_t K, const void *A, gemm_maj
                         int64_t ldc, void *D, int64_t ldd, gemm_out_t d_type, float alpha, float beta,
                         gemm_stream_t stream)
 {
-    return run_single(1, M, N, K, A, a_major, lda, B, b_major, ldb, C, ldc, D, ldd, d_type, alpha, beta,
+    return run_single(fmt16(1), M, N, K, A, a_major, lda, B, b_major, ldb, C, ldc, D, ldd, d_type, alpha, beta,
                       nullptr, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -753,7 +769,7 @@ gemm_status_t gemm_f16(int64_t M, int64_t N, int64_t K, const void *A, gemm_majo
                        int64_t ldc, void *D, int64_t ldd, gemm_out_t d_type, float alpha, float beta,
                        gemm_stream_t stream)
 {
-    return run_single(0, M, N, K, A, a_major, lda, B, b_major, ldb, C, ldc, D, ldd, d_type, alpha, beta,
+    return run_single(fmt16(0), M, N, K, A, a_major, lda, B, b_major, ldb, C, ldc, D, ldd, d_type, alpha, beta,
                       nullptr, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -764,8 +780,30 @@ gemm_status_t gemm_ex(int in_type, int64_t M, int64_t N, int64_t K, const void *
 {
     if (in_type != 0 && in_type != 1)
         return GEMM_ERR_INVALID_ARG;
-    return run_single(in_type, M, N, K, A, a_major, lda, B, b_major, ldb, C, ldc, D, ldd, d_type, alpha,
+    return run_single(fmt16(in_type), M, N, K, A, a_major, lda, B, b_major, ldb, C, ldc, D, ldd, d_type, alpha,
                       beta, opts, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_fp8_ex(int64_t M, int64_t N, int64_t K, const void *A, gemm_fp8_t a_format,
+                          gemm_major_t a_major, int64_t lda, const void *B, gemm_fp8_t b_format,
+                          gemm_major_t b_major, int64_t ldb, const void *C, int64_t ldc, void *D,
+                          int64_t ldd, gemm_out_t d_type, float alpha, float beta,
+                          const gemm_options_t *opts, gemm_stream_t stream)
+{
+    if ((a_format != GEMM_FP8_E4M3 && a_format != GEMM_FP8_E5M2) ||
+        (b_format != GEMM_FP8_E4M3 && b_format != GEMM_FP8_E5M2))
+        return GEMM_ERR_INVALID_ARG;
+    return run_single(fmt8(a_format, b_format), M, N, K, A, a_major, lda, B, b_major, ldb, C, ldc, D, ldd,
+                      d_type, alpha, beta, opts, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_fp8(int64_t M, int64_t N, int64_t K, const void *A, gemm_fp8_t a_format,
+                       gemm_major_t a_major, int64_t lda, const void *B, gemm_fp8_t b_format,
+                       gemm_major_t b_major, int64_t ldb, const void *C, int64_t ldc, void *D, int64_t ldd,
+                       gemm_out_t d_type, float alpha, float beta, gemm_stream_t stream)
+{
+    return gemm_fp8_ex(M, N, K, A, a_format, a_major, lda, B, b_format, b_major, ldb, C, ldc, D, ldd, d_type,
+                       alpha, beta, nullptr, stream);
 }
 
 size_t gemm_grouped_workspace_size(int num_problems)
@@ -833,12 +871,15 @@ gemm_status_t gemm_debug_descriptors(int major, int swizzle, int rows, int bk, u
                                      int b_major, uint64_t *out, gemm_stream_t stream)
 {
     if (!valid_enum(major) || swizzle < 1 || swizzle > 4 || rows <= 0 || bk <= 0 || n_slices < 0 ||
-        (cta_group != 1 && cta_group != 2) || tile_n <= 0 || !out || (in_type != 0 && in_type != 1) ||
+        (cta_group != 1 && cta_group != 2) || tile_n <= 0 || !out || in_type < 0 || in_type > 3 ||
         !valid_enum(a_major) || !valid_enum(b_major))
         return GEMM_ERR_INVALID_ARG;
+    // in_type 0 fp16, 1 bf16 (kind::f16); 2 E4M3, 3 E5M2 (kind::f8f6f4)
+    const int esize = in_type >= 2 ? 1 : 2;
+    const int fmt = in_type >= 2 ? in_type - 2 : in_type;
     debug_descriptor_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        major, swz_bits_of(swizzle), rows, bk, stage_addr, n_slices, 128 * cta_group, tile_n, in_type, a_major, b_major,
-        out);
+        major, swz_bits_of(swizzle), rows, bk, stage_addr, n_slices, 128 * cta_group, tile_n, fmt, esize,
+        a_major, b_major, out);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return cuda_fail(e);

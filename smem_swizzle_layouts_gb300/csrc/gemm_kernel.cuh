@@ -78,7 +78,7 @@ struct KParams {
     float alpha, beta;
     int a_mn, b_mn;        // 0 K-major, 1 MN-major
     int a_swz, b_swz;      // swizzle bits: 0 none, 1 SW32, 2 SW64, 3 SW128
-    int in_bf16;           // 0 fp16, 1 bf16
+    int a_fmt, b_fmt;      // MMA operand formats (kind::f16: 0 fp16, 1 bf16; kind::f8f6f4: 0 E4M3, 1 E5M2)
     int out_type;          // 0 f32, 1 bf16, 2 f16
     int epi_swizzle;       // 1: staging chunks in SW128 layout; 0: plain rows
     int group_m;           // raster group height (tiles)
@@ -124,12 +124,14 @@ __device__ __forceinline__ int kblock_at(int it, int num_kb, int flags, int clus
     return r >= num_kb ? r - num_kb : r;
 }
 
-template <int CG, int BN, int BK, int STAGES>
+// ESIZE: bytes per operand element, 2 (fp16/bf16, tcgen05 kind::f16) or
+// 1 (fp8, kind::f8f6f4). BK counts elements of K per stage.
+template <int CG, int BN, int BK, int STAGES, int ESIZE = 2>
 struct Cfg {
     static constexpr int BM = 128;             // accumulator rows per CTA (TMEM lanes)
     static constexpr int BN_LOCAL = BN / CG;   // B columns loaded by each CTA
-    static constexpr int A_BYTES = BM * BK * 2;
-    static constexpr int B_BYTES = BN_LOCAL * BK * 2;
+    static constexpr int A_BYTES = BM * BK * ESIZE;
+    static constexpr int B_BYTES = BN_LOCAL * BK * ESIZE;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TX_BYTES = STAGE_BYTES * CG;  // bytes landing on one full barrier
     static constexpr int EPI_OFF = STAGES * STAGE_BYTES;
@@ -141,7 +143,7 @@ struct Cfg {
     static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack to align the base
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int UMMA_M = BM * CG;
-    static constexpr int KSLICES = BK / 16;
+    static constexpr int KSLICES = BK * ESIZE / 32;  // MMAs per stage (32 bytes of K each)
     static_assert(STAGE_BYTES % 1024 == 0, "stages must stay 1024-aligned");
     static_assert(A_BYTES % 1024 == 0, "B tile must start 1024-aligned");
     static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0,
@@ -291,10 +293,11 @@ struct OperandBoxes {
     int mn_major;
 };
 
-__device__ __forceinline__ OperandBoxes operand_boxes(int mn_major, int swz_bits, int rows, int bk)
+__device__ __forceinline__ OperandBoxes operand_boxes(int mn_major, int swz_bits, int rows, int bk,
+                                                      int esize)
 {
     const int W = 16 << swz_bits;
-    const int per = W / 2;  // 16-bit elements per swizzled row
+    const int per = W / esize;  // elements per swizzled row
     OperandBoxes o;
     o.mn_major = mn_major;
     o.step = per;
@@ -324,9 +327,9 @@ __device__ __forceinline__ void issue_box(const CUtensorMap *map, uint32_t dst, 
 template <int CG>
 __device__ __forceinline__ void load_operand_stage(const CUtensorMap *map, uint32_t dst,
                                                    uint32_t bar, int mn_major, int swz_bits,
-                                                   int rows, int bk, int mn0, int k0)
+                                                   int rows, int bk, int mn0, int k0, int esize = 2)
 {
-    const OperandBoxes o = operand_boxes(mn_major, swz_bits, rows, bk);
+    const OperandBoxes o = operand_boxes(mn_major, swz_bits, rows, bk, esize);
     for (int b = 0; b < o.nbox; ++b)
         issue_box<CG>(map, dst, bar, o, b, mn0, k0);
 }
@@ -335,18 +338,18 @@ __device__ __forceinline__ int ceil_div_i(int a, int b) { return (a + b - 1) / b
 
 // ---------------------------------------------------------------- roles
 
-template <int CG, int BN, int BK, int STAGES, bool GROUPED>
+template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE>
 __device__ void role_producer(const KParams &p, const CUtensorMap *tmA, const CUtensorMap *tmB,
                               uint32_t smem, uint32_t bar_full, uint32_t bar_empty,
                               uint32_t rank, const Waiter &w)
 {
-    using C = Cfg<CG, BN, BK, STAGES>;
+    using C = Cfg<CG, BN, BK, STAGES, ESIZE>;
     const Sched sched = make_sched(p);
     const int flags = p.flags;
     unsigned long long *const stats = p.stats;
     const CUtensorMap *const maps = p.maps;
-    const OperandBoxes boxA = operand_boxes(p.a_mn, p.a_swz, C::BM, BK);
-    const OperandBoxes boxB = operand_boxes(p.b_mn, p.b_swz, C::BN_LOCAL, BK);
+    const OperandBoxes boxA = operand_boxes(p.a_mn, p.a_swz, C::BM, BK, ESIZE);
+    const OperandBoxes boxB = operand_boxes(p.b_mn, p.b_swz, C::BN_LOCAL, BK, ESIZE);
     const int nbox = boxA.nbox > boxB.nbox ? boxA.nbox : boxB.nbox;
     const bool forward = CG == 2 && rank == 0 && (flags & kFlagPairForward);
 
@@ -428,12 +431,12 @@ __device__ void role_producer(const KParams &p, const CUtensorMap *tmA, const CU
     }
 }
 
-template <int CG, int BN, int BK, int STAGES, bool GROUPED>
+template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE>
 __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uint32_t bar_empty,
                          uint32_t bar_acc_full, uint32_t bar_acc_empty, uint32_t bar_inject,
                          uint32_t tmem_base, const Waiter &w)
 {
-    using C = Cfg<CG, BN, BK, STAGES>;
+    using C = Cfg<CG, BN, BK, STAGES, ESIZE>;
     if (p.inject_timeout) {
         // Test hook: wait on a barrier nothing arrives at; the bound runs out.
         w.wait(bar_inject, 0u, kRoleMma | kWaitInjected);
@@ -442,7 +445,7 @@ __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uin
     const Sched sched = make_sched(p);
     unsigned long long *const stats = p.stats;
     const bool multicast = CG == 2 && !(p.flags & kFlagPairForward);
-    const uint32_t idesc = make_idesc_f16(C::UMMA_M, BN, p.in_bf16, p.a_mn, p.b_mn);
+    const uint32_t idesc = make_idesc(C::UMMA_M, BN, p.a_fmt, p.b_fmt, p.a_mn, p.b_mn);
     const OperandPacking pa = operand_packing(p.a_mn, p.a_swz, C::BM, BK);
     const OperandPacking pb = operand_packing(p.b_mn, p.b_swz, C::BN_LOCAL, BK);
     const uint64_t a_desc0 = make_smem_desc(smem, pa.lbo, pa.sbo, pa.swz);
@@ -450,8 +453,8 @@ __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uin
     uint32_t a_off[C::KSLICES], b_off[C::KSLICES];
 #pragma unroll
     for (int j = 0; j < C::KSLICES; ++j) {
-        a_off[j] = slice_byte_offset(p.a_mn, p.a_swz, C::BM, j) >> 4;
-        b_off[j] = slice_byte_offset(p.b_mn, p.b_swz, C::BN_LOCAL, j) >> 4;
+        a_off[j] = slice_byte_offset(p.a_mn, p.a_swz, C::BM, j, ESIZE) >> 4;
+        b_off[j] = slice_byte_offset(p.b_mn, p.b_swz, C::BN_LOCAL, j, ESIZE) >> 4;
     }
     const int cluster_id = blockIdx.x / CG, num_clusters = gridDim.x / CG;
     int stage = 0;
@@ -490,9 +493,14 @@ __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uin
             tc_fence_after_sync();
             const uint64_t sdelta = static_cast<uint64_t>((stage * C::STAGE_BYTES) >> 4);
 #pragma unroll
-            for (int j = 0; j < C::KSLICES; ++j)
-                mma_f16<CG>(d_tmem, a_desc0 + sdelta + a_off[j], b_desc0 + sdelta + b_off[j], idesc,
-                            (kb | j) != 0);
+            for (int j = 0; j < C::KSLICES; ++j) {
+                if constexpr (ESIZE == 2)
+                    mma_f16<CG>(d_tmem, a_desc0 + sdelta + a_off[j], b_desc0 + sdelta + b_off[j], idesc,
+                                (kb | j) != 0);
+                else
+                    mma_f8<CG>(d_tmem, a_desc0 + sdelta + a_off[j], b_desc0 + sdelta + b_off[j], idesc,
+                               (kb | j) != 0);
+            }
             if (multicast)
                 mma_commit_pair_multicast(bar_empty + 8 * stage);
             else
@@ -608,13 +616,13 @@ __device__ __forceinline__ void epilogue_chunk_math(float (&acc)[CW], const EpiC
     }
 }
 
-template <int CG, int BN, int BK, int STAGES, bool GROUPED, int CW>
+template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int CW>
 __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CUtensorMap *tmD,
                               uint32_t epi_base, uint32_t bar_acc_full, uint32_t bar_acc_empty,
                               uint32_t bar_epi, uint32_t tmem_base, uint32_t rank, int warp,
                               int lane, const Waiter &w)
 {
-    using C = Cfg<CG, BN, BK, STAGES>;
+    using C = Cfg<CG, BN, BK, STAGES, ESIZE>;
     const Sched sched = make_sched(p);
     unsigned long long *const stats = p.stats;
     const CUtensorMap *const maps = p.maps;
@@ -746,14 +754,14 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
 
 // ---------------------------------------------------------------- kernel
 
-template <int CG, int BN, int BK, int STAGES, bool GROUPED>
+template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC,
                         const __grid_constant__ CUtensorMap tmD, const __grid_constant__ KParams p)
 {
-    using C = Cfg<CG, BN, BK, STAGES>;
+    using C = Cfg<CG, BN, BK, STAGES, ESIZE>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -816,11 +824,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t stage_base = base;
     if (warp == 0) {
         if (lane == 0)
-            role_producer<CG, BN, BK, STAGES, GROUPED>(p, &tmA, &tmB, stage_base, bar_full,
-                                                       bar_empty, rank, w);
+            role_producer<CG, BN, BK, STAGES, GROUPED, ESIZE>(p, &tmA, &tmB, stage_base, bar_full,
+                                                              bar_empty, rank, w);
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {
-            role_mma<CG, BN, BK, STAGES, GROUPED>(p, stage_base, bar_full, bar_empty,
+            role_mma<CG, BN, BK, STAGES, GROUPED, ESIZE>(p, stage_base, bar_full, bar_empty,
                                                   bar_acc_full, bar_acc_empty, bar_inject,
                                                   tmem_base, w);
             // every MMA issued by this thread has completed before TMEM is freed
@@ -829,11 +837,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         if (p.out_type == 0)
-            role_epilogue<CG, BN, BK, STAGES, GROUPED, 32>(p, &tmC, &tmD, base + C::EPI_OFF,
+            role_epilogue<CG, BN, BK, STAGES, GROUPED, ESIZE, 32>(p, &tmC, &tmD, base + C::EPI_OFF,
                                                            bar_acc_full, bar_acc_empty, bar_epi,
                                                            tmem_base, rank, warp, lane, w);
         else
-            role_epilogue<CG, BN, BK, STAGES, GROUPED, 64>(p, &tmC, &tmD, base + C::EPI_OFF,
+            role_epilogue<CG, BN, BK, STAGES, GROUPED, ESIZE, 64>(p, &tmC, &tmD, base + C::EPI_OFF,
                                                            bar_acc_full, bar_acc_empty, bar_epi,
                                                            tmem_base, rank, warp, lane, w);
         if (lane == 0)

@@ -7,26 +7,30 @@ namespace g300 {
 
 struct LaunchArgs;
 
-template <int CG, int BN, int BK, int STAGES, bool GROUPED>
+template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE>
 cudaError_t launch_gemm(const LaunchArgs &a);
 
-template <int CG, int BN, int BK, int STAGES, bool GROUPED>
+template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE>
 cudaError_t resident_ctas(int *ctas);
 
-// X(cta_group, BN, BK, stages, grouped). BN is the MMA N of one tile;
-// stages fill ~192 KB of shared memory next to 32 KB of epilogue staging.
+// X(cta_group, BN, BK, stages, grouped, element bytes). BN is the MMA N of one
+// tile, BK counts elements; stages fill ~192 KB of shared memory next to 32 KB
+// of epilogue staging. Element bytes 2 = fp16/bf16, 1 = fp8.
 #define G300_VARIANTS(X)        \
-    X(1, 256, 64, 4, false)     \
-    X(1, 128, 64, 6, false)     \
-    X(1, 128, 128, 3, false)    \
-    X(1, 64, 64, 8, false)      \
-    X(1, 64, 128, 4, false)     \
-    X(1, 128, 32, 8, false)     \
-    X(2, 256, 64, 6, false)     \
-    X(2, 256, 128, 3, false)    \
-    X(2, 128, 128, 4, false)    \
-    X(1, 256, 64, 4, true)      \
-    X(1, 128, 128, 3, true)     \
-    X(2, 256, 128, 3, true)
+    X(1, 256, 64, 4, false, 2)     \
+    X(1, 128, 64, 6, false, 2)     \
+    X(1, 128, 128, 3, false, 2)    \
+    X(1, 64, 64, 8, false, 2)      \
+    X(1, 64, 128, 4, false, 2)     \
+    X(1, 128, 32, 8, false, 2)     \
+    X(2, 256, 64, 6, false, 2)     \
+    X(2, 256, 128, 3, false, 2)    \
+    X(2, 128, 128, 4, false, 2)    \
+    X(1, 256, 64, 4, true, 2)      \
+    X(1, 128, 128, 3, true, 2)     \
+    X(2, 256, 128, 3, true, 2)  \
+    X(2, 256, 256, 3, false, 1) \
+    X(1, 256, 128, 4, false, 1) \
+    X(1, 128, 256, 3, false, 1)
 
 }  // namespace g300

@@ -48,32 +48,41 @@ def _ru(x, m):
     return max(m, (x + m - 1) // m * m)
 
 
-def run_case(g, M, N, K, *, in_fmt="bf16", a_major="K", b_major="K", out="f32", alpha=1.0, beta=0.0,
-             dist="uniform", scale=1.0, seed=0, pad=0, options=None, inplace=False, exact=False,
+FP8 = {"e4m3": 0, "e5m2": 1}
+
+
+def run_case(g, M, N, K, *, in_fmt="bf16", b_fmt=None, a_major="K", b_major="K", out="f32", alpha=1.0,
+             beta=0.0, dist="uniform", scale=1.0, seed=0, pad=0, options=None, inplace=False, exact=False,
              sample=None):
     """Run one GEMM through the C ABI and compare with the oracle; returns max |err|."""
     if options and options.get("cta_group") == 2 and os.environ.get("GEMM_TEST_NO_PAIRS"):
         pytest.skip("CTA-pair cases disabled for this run")
+    b_fmt = b_fmt or in_fmt
+    fp8 = in_fmt in FP8
     # leading dimensions rounded up to the 16-byte TMA stride rule, plus optional padding
-    lda = _ru(K if a_major == "K" else M, 8) + pad
-    ldb = _ru(K if b_major == "K" else N, 8) + pad
+    lda = _ru(K if a_major == "K" else M, 16 if fp8 else 8) + pad
+    ldb = _ru(K if b_major == "K" else N, 16 if fp8 else 8) + pad
     ldd = _ru(N, 4 if out == "f32" else 8) + pad
     A = si.matrix_bits(seed, M, K, dist, in_fmt, scale=scale, transpose=(a_major == "MN"), ld=lda)
-    B = si.matrix_bits(seed + 1, K, N, dist, in_fmt, scale=scale, transpose=(b_major == "K"), ld=ldb)
+    B = si.matrix_bits(seed + 1, K, N, dist, b_fmt, scale=scale, transpose=(b_major == "K"), ld=ldb)
     C = si.matrix_bits(seed + 2, M, N, dist, out, scale=scale, ld=ldd) if beta != 0.0 else None
-    At, Bt = _to_dev(A, in_fmt), _to_dev(B, in_fmt)
+    At, Bt = _to_dev(A, in_fmt), _to_dev(B, b_fmt)
     Ct = _to_dev(C, out) if C is not None else None
     Dt = Ct if inplace else torch.full((M, ldd), float("nan"), dtype=TDT[out], device=DEV)
-    in_type = 1 if in_fmt == "bf16" else 0
-    g.gemm_ex(in_type, M, N, K, At, 0 if a_major == "K" else 1, lda, Bt, 0 if b_major == "K" else 1, ldb,
-              Ct, ldd if C is not None else 0, Dt, ldd, {"f32": 0, "bf16": 1, "f16": 2}[out], alpha, beta,
-              options=options)
+    am, bm, dt = (0 if a_major == "K" else 1), (0 if b_major == "K" else 1), {"f32": 0, "bf16": 1, "f16": 2}[out]
+    if fp8:
+        g.gemm_fp8_ex(M, N, K, At, FP8[in_fmt], am, lda, Bt, FP8[b_fmt], bm, ldb, Ct, ldd if C is not None else 0,
+                      Dt, ldd, dt, alpha, beta, options=options)
+    else:
+        in_type = 1 if in_fmt == "bf16" else 0
+        g.gemm_ex(in_type, M, N, K, At, am, lda, Bt, bm, ldb, Ct, ldd if C is not None else 0, Dt, ldd, dt,
+                  alpha, beta, options=options)
     st, word = g.gemm_last_device_status()
     assert st == g.OK, f"device status word {word:#x}"
     got_bits = _out_bits(Dt, out)[:, :N]
     got = si.bits_to_float64(got_bits, out)
-    kw = dict(in_fmt=in_fmt, a_major=a_major, b_major=b_major, lda=lda, ldb=ldb, C=C, c_fmt=out, ldc=ldd,
-              alpha=alpha, beta=beta)
+    kw = dict(in_fmt=in_fmt, b_fmt=b_fmt, a_major=a_major, b_major=b_major, lda=lda, ldb=ldb, C=C, c_fmt=out,
+              ldc=ldd, alpha=alpha, beta=beta)
     if sample is None:
         ref, S = og.gemm(M, N, K, A, B, **kw)
         rows, cols = slice(None), slice(None)
@@ -377,6 +386,51 @@ def test_config5_grouped_64_problems(g):
     rng = np.random.default_rng(5)
     Ms = [int(x) for x in rng.integers(1, 33, 64) * 128]
     _grouped(g, Ms, 4096, 2048, out="bf16", dist="uniform", seed=100, sample=True)
+
+
+# ---------------------------------------------------------------- fp8 operands (kind::f8f6f4)
+
+@pytest.mark.parametrize("major", ["K", "MN"])
+@pytest.mark.parametrize("mode", ["sw64", "sw128", "none"])
+@pytest.mark.parametrize("rows,bk", [(128, 128), (128, 256), (256, 128)])
+def test_fp8_descriptor_words_match_oracle(g, major, mode, rows, bk):
+    W = L.swizzle_width(mode)
+    if (major == "K" and W > bk) or (major == "MN" and rows % W):
+        pytest.skip("box wider than the stage")
+    n = bk // 32
+    out = torch.zeros(n + 1, dtype=torch.int64, device=DEV)
+    g.gemm_debug_descriptors(0 if major == "K" else 1, SWZ_PARAM[mode], rows, bk, 8192, n, 1, 256, 2, 0, 1, out)
+    words = [int(x) & (2 ** 64 - 1) for x in out.cpu().tolist()]
+    for j in range(n):
+        assert words[j] == L.encode_smem_desc(L.stage_slice_desc(major, mode, rows, bk, 1, j, 8192)), j
+    assert words[n] & 0xFFFFFFFF == L.encode_idesc(128, 256, L.FMT_E4M3, L.DFMT_F32, 0, 1)
+
+
+@pytest.mark.parametrize("fa,fb", [("e4m3", "e4m3"), ("e4m3", "e5m2"), ("e5m2", "e4m3"), ("e5m2", "e5m2")])
+@pytest.mark.parametrize("a_major,b_major", [("K", "K"), ("K", "MN"), ("MN", "K"), ("MN", "MN")])
+def test_fp8_integer_exact(g, fa, fb, a_major, b_major):
+    run_case(g, 384, 320, 512, in_fmt=fa, b_fmt=fb, a_major=a_major, b_major=b_major, dist="int4", exact=True)
+
+
+@pytest.mark.parametrize("cg,tile_n", [(1, 128), (1, 256), (2, 256)])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_fp8_tiles_ragged(g, cg, tile_n, out):
+    run_case(g, 520, 600, 272, in_fmt="e4m3", b_fmt="e4m3", a_major="K", b_major="MN", out=out, dist="uniform",
+             options=dict(cta_group=cg, tile_n=tile_n))
+    run_case(g, 300, 264, 160, in_fmt="e5m2", b_fmt="e4m3", out=out, dist="int4", exact=True,
+             beta=0.5 if out == "f32" else 0.0, options=dict(cta_group=cg, tile_n=tile_n))
+
+
+@pytest.mark.parametrize("swz", [1, 2, 4])
+def test_fp8_swizzle_modes(g, swz):
+    run_case(g, 256, 256, 256, in_fmt="e4m3", a_major="K", b_major="MN", dist="int4", exact=True,
+             options=dict(swizzle_a=swz, swizzle_b=swz, tile_n=128))
+
+
+def test_fp8_square_8192_pair_sampled(g):
+    M = N = K = 8192
+    run_case(g, M, N, K, in_fmt="e4m3", a_major="K", b_major="K", out="bf16", dist="uniform", seed=40,
+             options=dict(cta_group=2), sample=sample_entries(M, N, n=1024))
 
 
 @pytest.mark.parametrize("flags", [0, 1, 2, 3, 4, 5])

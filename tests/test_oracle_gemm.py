@@ -199,3 +199,46 @@ def test_ulp_and_tolerance():
     assert G.ulp(np.array([1.5]), "f32")[0] == 2.0 ** -23
     assert G.ulp(np.array([0.0]), "f16")[0] == 2.0 ** -24
     assert G.tolerance(np.array([1000.0]), np.array([1.0]), "bf16")[0] == 1.0 + 2.0 ** -7
+
+
+# ---------------------------------------------------------------------------
+# fp8 operands (E4M3 / E5M2): decoding against format facts and an
+# independent codec, and exact products.
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("fmt,tdt", [("e4m3", "float8_e4m3fn"), ("e5m2", "float8_e5m2")])
+def test_fp8_decode_matches_torch_for_every_code(fmt, tdt):
+    codes = np.arange(256, dtype=np.uint8)
+    ours = G.decode(codes, fmt)
+    theirs = torch.from_numpy(codes).view(getattr(torch, tdt)).double().numpy()
+    same = (ours == theirs) | (np.isnan(ours) & np.isnan(theirs))
+    assert same.all()
+
+
+def test_fp8_format_facts():
+    # E4M3: 1.0 = 0x38, largest finite 0x7E = 448, smallest normal 0x08 = 2^-6,
+    # smallest subnormal 0x01 = 2^-9, 0x7F is NaN, no infinity
+    d = G.decode(np.array([0x38, 0xB8, 0x7E, 0x08, 0x01, 0x7F, 0x78], dtype=np.uint8), "e4m3")
+    assert list(d[:5]) == [1.0, -1.0, 448.0, 2.0 ** -6, 2.0 ** -9] and np.isnan(d[5]) and d[6] == 256.0
+    # E5M2: 1.0 = 0x3C, largest finite 0x7B = 57344, 0x7C = inf, smallest subnormal 2^-16
+    d = G.decode(np.array([0x3C, 0x7B, 0x7C, 0x01, 0x04, 0x7D], dtype=np.uint8), "e5m2")
+    assert list(d[:5]) == [1.0, 57344.0, np.inf, 2.0 ** -16, 2.0 ** -14] and np.isnan(d[5])
+
+
+@pytest.mark.parametrize("fa,fb", [("e4m3", "e4m3"), ("e4m3", "e5m2"), ("e5m2", "e5m2")])
+def test_fp8_integer_products_are_exact(fa, fb):
+    M, N, K = 24, 40, 96
+    A = si.matrix_bits(61, M, K, "int4", fa)
+    B = si.matrix_bits(62, K, N, "int4", fb, transpose=True)
+    D, _ = G.gemm(M, N, K, A, B, in_fmt=fa, b_fmt=fb, a_major="K", b_major="K")
+    ref = si.logical_values(61, M, K, "int4").astype(np.int64) @ si.logical_values(62, K, N, "int4").astype(np.int64)
+    assert np.array_equal(D, ref.astype(np.float64))
+
+
+def test_fp8_mixed_formats_match_float64_matmul():
+    M, N, K = 17, 33, 64
+    A = si.matrix_bits(71, M, K, "normal", "e4m3")
+    B = si.matrix_bits(72, K, N, "normal", "e5m2")
+    D, _ = G.gemm(M, N, K, A, B, in_fmt="e4m3", b_fmt="e5m2", a_major="K", b_major="MN")
+    ref = si.bits_to_float64(A, "e4m3") @ si.bits_to_float64(B, "e5m2")
+    assert np.allclose(D, ref, rtol=1e-13, atol=1e-13)

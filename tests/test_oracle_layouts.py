@@ -361,3 +361,26 @@ def test_reload_traffic(golden):
     assert round(b / 1e9, 2) == g["gmem_to_smem_gb"]
     assert b == int(g["reloads"]) * m * k * e * 2
     assert round(m * n * 4 / 1e6) == g["c_fp32_mb"]
+
+
+@pytest.mark.parametrize("major", ["K", "MN"])
+@pytest.mark.parametrize("mode", ["none", "sw32", "sw64", "sw128"])
+@pytest.mark.parametrize("rows,bk", [(128, 128), (256, 128), (128, 256)])
+def test_fp8_stage_packing_matches_descriptor_for_every_slice(major, mode, rows, bk):
+    # one MMA slice of an 8-bit type is 32 elements of K (32 bytes per row)
+    if major == "K" and L.swizzle_width(mode) > bk:
+        pytest.skip("K-major swizzle row wider than the K block")
+    seen = set()
+    for j in range(bk // 32):
+        d = L.stage_slice_desc(major, mode, rows, bk, 1, j, P_BASE)
+        for mn in range(rows):
+            for kk in range(32):
+                addr = L.desc_element_addr(d, major, 1, mn, kk)
+                assert addr == P_BASE + L.stage_element_offset(major, mode, rows, bk, 1, mn, 32 * j + kk)
+                seen.add(addr)
+    assert len(seen) == rows * bk
+
+
+def test_idesc_mixed_ab_formats():
+    w = L.encode_idesc(128, 128, L.FMT_E4M3, L.DFMT_F32, 0, 1, b_fmt=L.FMT_E5M2)
+    assert (w >> 7) & 7 == 0 and (w >> 10) & 7 == 1 and (w >> 16) & 1 == 1
