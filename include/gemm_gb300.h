@@ -80,7 +80,11 @@ typedef enum {
  * means "library default".
  *   cta_group     1: one CTA per 128-row tile (tcgen05.mma.cta_group::1);
  *                 2: CTA pairs own 256-row tiles (cta_group::2).
- *   tile_n        MMA N per tile: 64, 128 or 256 (cta_group::2: 256).
+ *   tile_m        accumulator rows per CTA: 128, or 64 (cta_group::1 only:
+ *                 tcgen05.mma M = 64 with the TMEM accumulator in Layout F,
+ *                 "06 Blackwell Tensor Core - tcgen05 MMA", cta_group::1
+ *                 M = 64; default for M <= 64 with 16-bit operands).
+ *   tile_n        MMA N per tile: 64, 128 or 256 (cta_group::2: 128 or 256).
  *   block_k       K elements per pipeline stage: 32, 64 or 128 where built.
  *   swizzle_a/b   operand swizzle (gemm_swizzle_t).
  *   epilogue_swizzle  1 (default) stages output tiles in SW128 layout;
@@ -102,6 +106,7 @@ typedef enum {
  */
 typedef struct {
     int cta_group;
+    int tile_m;
     int tile_n;
     int block_k;
     int swizzle_a;

@@ -32,7 +32,7 @@ _i64, _vp, _f, _int, _u32, _u64 = (ctypes.c_int64, ctypes.c_void_p, ctypes.c_flo
 
 
 class GemmOptions(ctypes.Structure):
-    _fields_ = [("cta_group", _int), ("tile_n", _int), ("block_k", _int), ("swizzle_a", _int), ("swizzle_b", _int),
+    _fields_ = [("cta_group", _int), ("tile_m", _int), ("tile_n", _int), ("block_k", _int), ("swizzle_a", _int), ("swizzle_b", _int),
                 ("epilogue_swizzle", _int), ("max_ctas", _int), ("group_m", _int),
                 ("timeout_ms", _int), ("flags", _int), ("stats", _vp)]
 

@@ -37,13 +37,14 @@ struct Variant {
     int cg, bn, bk, stages;
     bool grouped;
     int esize;
+    int bm;
     cudaError_t (*launch)(const LaunchArgs &);
     cudaError_t (*resident)(int *);
     int resident_cache[kMaxDevices];
 };
 
-#define G300_VARIANT_ROW(CG, BN, BK, ST, GR, ES) \
-    {CG, BN, BK, ST, GR, ES, &launch_gemm<CG, BN, BK, ST, GR, ES>, &resident_ctas<CG, BN, BK, ST, GR, ES>, {0}},
+#define G300_VARIANT_ROW(CG, BN, BK, ST, GR, ES, BM) \
+    {CG, BN, BK, ST, GR, ES, BM, &launch_gemm<CG, BN, BK, ST, GR, ES, BM>, &resident_ctas<CG, BN, BK, ST, GR, ES, BM>, {0}},
 Variant g_variants[] = {G300_VARIANTS(G300_VARIANT_ROW)};
 #undef G300_VARIANT_ROW
 
@@ -98,10 +99,10 @@ int resident_for(Variant &v, int dev)
     return v.resident_cache[dev];
 }
 
-Variant *find_variant(int cg, int bn, int bk, bool grouped, int esize = 2)
+Variant *find_variant(int cg, int bn, int bk, bool grouped, int esize = 2, int bm = 128)
 {
     for (auto &v : g_variants)
-        if (v.cg == cg && v.bn == bn && v.bk == bk && v.grouped == grouped && v.esize == esize)
+        if (v.cg == cg && v.bn == bn && v.bk == bk && v.grouped == grouped && v.esize == esize && v.bm == bm)
             return &v;
     return nullptr;
 }
@@ -207,19 +208,21 @@ gemm_status_t encode_operand(CUtensorMap *m, int dcode, const void *ptr, int mn_
                      tma_swizzle(swz_bits));
 }
 
-// Output (and C) map: 32-row boxes of 128 bytes.
+// Output (and C) map: boxes of 128 bytes x the rows one epilogue warp owns
+// (32 for 128-row tiles, 16 for 64-row tiles).
 gemm_status_t encode_output(CUtensorMap *m, int d_type, const void *ptr, int64_t M, int64_t N,
-                            int64_t ld, int epi_swizzle)
+                            int64_t ld, int epi_swizzle, int rows = 32)
 {
     const int ob = out_bytes(d_type);
     return encode_2d(m, out_dtype(d_type), ptr, static_cast<uint64_t>(N), static_cast<uint64_t>(M),
-                     static_cast<uint64_t>(ld) * ob, static_cast<uint32_t>(128 / ob), 32u,
+                     static_cast<uint64_t>(ld) * ob, static_cast<uint32_t>(128 / ob), static_cast<uint32_t>(rows),
                      epi_swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                      CU_TENSOR_MAP_L2_PROMOTION_NONE);
 }
 
 struct Plan {
     int cg, bn, bk;
+    int bm;  // accumulator rows per CTA: 128, or 64 (M = 64 MMAs)
     int a_swz, b_swz;
     int epi_swizzle;
     int max_ctas;
@@ -246,7 +249,13 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
         opt.epilogue_swizzle > 1 || opt.flags < 0 || opt.flags > 7 || opt.block_k < 0)
         return GEMM_ERR_INVALID_ARG;
 
+    if (opt.tile_m != 0 && opt.tile_m != 64 && opt.tile_m != 128)
+        return GEMM_ERR_INVALID_ARG;
     int cg = opt.cta_group;
+    if (opt.tile_m == 64 && cg == 2)
+        return GEMM_ERR_UNSUPPORTED;
+    if (opt.tile_m == 64)
+        cg = 1;
     if (cg == 0) {
         // CTA pairs for large problems: each SM then loads half of B.
         cg = (!grouped && M >= 2048 && N >= 2048) ? 2 : 1;
@@ -278,7 +287,13 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
         else
             bk = (cg == 1 && bn == 256) ? 64 : 128;
     }
-    if (!find_variant(cg, bn, bk, grouped, esize))
+    // 64-row tiles (M = 64 MMAs) when asked, or for problems of at most 64 rows
+    // (compiled for 128- and 256-wide N tiles)
+    const int bm = opt.tile_m ? opt.tile_m
+                              : (cg == 1 && M <= 64 && esize == 2 && !grouped && bn >= 128 ? 64 : 128);
+    if (bm == 64 && opt.block_k == 0)
+        bk = bn == 256 ? 64 : 128;
+    if (!find_variant(cg, bn, bk, grouped, esize, bm))
         return GEMM_ERR_UNSUPPORTED;
 
     auto pick_swz = [&](int requested, int mn_major) -> int {
@@ -299,8 +314,9 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
         const int per = (16 << bits) / esize;
         return mn_major ? (rows % per == 0) : (bk % per == 0);
     };
-    if (!fits(plan->a_swz, a_mn, 128) || !fits(plan->b_swz, b_mn, bn / cg))
+    if (!fits(plan->a_swz, a_mn, bm) || !fits(plan->b_swz, b_mn, bn / cg))
         return GEMM_ERR_UNSUPPORTED;
+    plan->bm = bm;
     plan->epi_swizzle = opt.epilogue_swizzle == -1 ? 0 : 1;
     plan->max_ctas = opt.max_ctas;
     plan->group_m = opt.group_m ? opt.group_m : 8;
@@ -401,21 +417,21 @@ gemm_status_t run_single(const InFmt &f, int64_t M, int64_t N, int64_t K, const 
     Plan pl;
     if ((s = make_plan(M, N, K, a_mn, b_mn, sms, opts, false, &pl, f.esize)) != GEMM_OK)
         return s;
-    Variant *v = find_variant(pl.cg, pl.bn, pl.bk, false, f.esize);
+    Variant *v = find_variant(pl.cg, pl.bn, pl.bk, false, f.esize, pl.bm);
 
     LaunchArgs la;
     std::memset(&la, 0, sizeof(la));
     if (K > 0) {
-        if ((s = encode_operand(&la.a, f.dcode, A, a_mn, pl.a_swz, M, K, lda, 128, pl.bk)) != GEMM_OK)
+        if ((s = encode_operand(&la.a, f.dcode, A, a_mn, pl.a_swz, M, K, lda, pl.bm, pl.bk)) != GEMM_OK)
             return s;
         if ((s = encode_operand(&la.b, f.dcode, B, b_mn, pl.b_swz, N, K, ldb, pl.bn / pl.cg, pl.bk)) !=
             GEMM_OK)
             return s;
     }
-    if ((s = encode_output(&la.d, d_type, D, M, N, ldd, pl.epi_swizzle)) != GEMM_OK)
+    if ((s = encode_output(&la.d, d_type, D, M, N, ldd, pl.epi_swizzle, pl.bm / 4)) != GEMM_OK)
         return s;
     if (beta != 0.0f) {
-        if ((s = encode_output(&la.c, d_type, C, M, N, ldc, pl.epi_swizzle)) != GEMM_OK)
+        if ((s = encode_output(&la.c, d_type, C, M, N, ldc, pl.epi_swizzle, pl.bm / 4)) != GEMM_OK)
             return s;
     } else {
         la.c = la.d;
@@ -425,7 +441,7 @@ gemm_status_t run_single(const InFmt &f, int64_t M, int64_t N, int64_t K, const 
     p.M = static_cast<int>(M);
     p.N = static_cast<int>(N);
     p.K = static_cast<int>(K);
-    p.tiles_m = static_cast<int>((M + 128 * pl.cg - 1) / (128 * pl.cg));
+    p.tiles_m = static_cast<int>((M + pl.bm * pl.cg - 1) / (pl.bm * pl.cg));
     p.tiles_n = static_cast<int>((N + pl.bn - 1) / pl.bn);
     const int64_t tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
     if (tiles >= (static_cast<int64_t>(1) << 31))

@@ -125,10 +125,13 @@ __device__ __forceinline__ int kblock_at(int it, int num_kb, int flags, int clus
 }
 
 // ESIZE: bytes per operand element, 2 (fp16/bf16, tcgen05 kind::f16) or
-// 1 (fp8, kind::f8f6f4). BK counts elements of K per stage.
-template <int CG, int BN, int BK, int STAGES, int ESIZE = 2>
+// 1 (fp8, kind::f8f6f4). BK counts elements of K per stage. BMT: accumulator
+// rows per CTA, 128 (row m in TMEM lane m) or 64 (cta_group::1 only, Layout F:
+// rows 16g..16g+15 in lanes 32g+a..32g+a+15; the two accumulators of the
+// double buffer take lane alignments a = 0 and 16 and share their columns).
+template <int CG, int BN, int BK, int STAGES, int ESIZE = 2, int BMT = 128>
 struct Cfg {
-    static constexpr int BM = 128;             // accumulator rows per CTA (TMEM lanes)
+    static constexpr int BM = BMT;             // accumulator rows per CTA
     static constexpr int BN_LOCAL = BN / CG;   // B columns loaded by each CTA
     static constexpr int A_BYTES = BM * BK * ESIZE;
     static constexpr int B_BYTES = BN_LOCAL * BK * ESIZE;
@@ -141,8 +144,10 @@ struct Cfg {
     static constexpr int NUM_BARS = 2 * STAGES + 2 + 2 + 2 * kEpiWarps + 2;
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack to align the base
-    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int TMEM_COLS = BMT == 64 ? BN : 2 * BN;
     static constexpr int UMMA_M = BM * CG;
+    static constexpr int EPI_ROWS = BM / 4;    // output rows per epilogue warp
+    static_assert(BMT == 128 || (BMT == 64 && CG == 1), "64-row tiles are single-CTA");
     static constexpr int KSLICES = BK * ESIZE / 32;  // MMAs per stage (32 bytes of K each)
     static_assert(STAGE_BYTES % 1024 == 0, "stages must stay 1024-aligned");
     static_assert(A_BYTES % 1024 == 0, "B tile must start 1024-aligned");
@@ -338,12 +343,12 @@ __device__ __forceinline__ int ceil_div_i(int a, int b) { return (a + b - 1) / b
 
 // ---------------------------------------------------------------- roles
 
-template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE>
+template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT>
 __device__ void role_producer(const KParams &p, const CUtensorMap *tmA, const CUtensorMap *tmB,
                               uint32_t smem, uint32_t bar_full, uint32_t bar_empty,
                               uint32_t rank, const Waiter &w)
 {
-    using C = Cfg<CG, BN, BK, STAGES, ESIZE>;
+    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT>;
     const Sched sched = make_sched(p);
     const int flags = p.flags;
     unsigned long long *const stats = p.stats;
@@ -431,12 +436,12 @@ __device__ void role_producer(const KParams &p, const CUtensorMap *tmA, const CU
     }
 }
 
-template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE>
+template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT>
 __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uint32_t bar_empty,
                          uint32_t bar_acc_full, uint32_t bar_acc_empty, uint32_t bar_inject,
                          uint32_t tmem_base, const Waiter &w)
 {
-    using C = Cfg<CG, BN, BK, STAGES, ESIZE>;
+    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT>;
     if (p.inject_timeout) {
         // Test hook: wait on a barrier nothing arrives at; the bound runs out.
         w.wait(bar_inject, 0u, kRoleMma | kWaitInjected);
@@ -478,7 +483,8 @@ __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uin
             ++st_tiles;
         }
         tc_fence_after_sync();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        const uint32_t d_tmem = C::BM == 64 ? tmem_base + (static_cast<uint32_t>(16 * acc) << 16)
+                                            : tmem_base + static_cast<uint32_t>(acc * BN);
         for (int kb = 0; kb < num_kb; ++kb) {
             if (stats) {
                 const long long t0 = clock64();
@@ -577,10 +583,10 @@ struct EpiConst {
 // `acc` holds this thread's row (lane) of the chunk in fp32.
 template <int CW>
 __device__ __forceinline__ void epilogue_chunk_math(float (&acc)[CW], const EpiConst &e,
-                                                    uint32_t sbuf, int lane, bool use_c)
+                                                    uint32_t sbuf, int r, bool use_c)
 {
-    const uint32_t row = sbuf + static_cast<uint32_t>(lane) * 128u;
-    const uint32_t key = static_cast<uint32_t>(lane) & e.key_mask;
+    const uint32_t row = sbuf + static_cast<uint32_t>(r) * 128u;
+    const uint32_t key = static_cast<uint32_t>(r) & e.key_mask;
     constexpr int PER16 = (CW == 32) ? 4 : 8;  // elements per 16-byte unit
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
@@ -616,13 +622,13 @@ __device__ __forceinline__ void epilogue_chunk_math(float (&acc)[CW], const EpiC
     }
 }
 
-template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int CW>
+template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int CW>
 __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CUtensorMap *tmD,
                               uint32_t epi_base, uint32_t bar_acc_full, uint32_t bar_acc_empty,
                               uint32_t bar_epi, uint32_t tmem_base, uint32_t rank, int warp,
                               int lane, const Waiter &w)
 {
-    using C = Cfg<CG, BN, BK, STAGES, ESIZE>;
+    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT>;
     const Sched sched = make_sched(p);
     unsigned long long *const stats = p.stats;
     const CUtensorMap *const maps = p.maps;
@@ -632,7 +638,8 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
     ec.out_type = p.out_type;
     ec.key_mask = p.epi_swizzle ? 7u : 0u;
     const bool forward = CG == 2 && rank == 0 && (p.flags & kFlagPairForward);
-    const int q = warp & 3;   // TMEM lane quarter = accumulator rows 32q..32q+31
+    const int q = warp & 3;   // TMEM lane quarter 32q..32q+31 = output rows EPI_ROWS*q..
+    constexpr int R = C::EPI_ROWS;
     const int ew = warp - 2;  // staging slot
     const uint32_t buf0 = epi_base + static_cast<uint32_t>(ew * 2 * kEpiBufBytes);
     const uint32_t ebar0 = bar_epi + static_cast<uint32_t>(16 * ew);
@@ -657,7 +664,11 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
             fence_tensormap_acquire(mD);
         }
         const bool has_acc = ti.K > 0;
-        const int m0 = ti.m_blk * C::UMMA_M + C::BM * static_cast<int>(rank) + 32 * q;
+        const int m0 = ti.m_blk * C::UMMA_M + C::BM * static_cast<int>(rank) + R * q;
+        // 128-row tiles: thread t holds row t. 64-row tiles (Layout F): the
+        // accumulator with lane alignment 16*acc sits in threads 16*acc..+15.
+        const bool active = C::BM == 128 || (lane >> 4) == acc;
+        const int trow = C::BM == 128 ? lane : (lane & 15);
         if (has_acc) {
             const long long tw = stats ? clock64() : 0;
             bool ok = w.wait(bar_acc_full + 8 * acc, acc_phase, kRoleEpilogue | kWaitAccFull, rank != 0);
@@ -681,14 +692,14 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
             __syncwarp();
             if (use_c && lane == 0) {
                 fence_proxy_async_smem();
-                mbar_arrive_expect_tx(sbar, kEpiBufBytes);
+                mbar_arrive_expect_tx(sbar, R * 128);
                 tma_load_2d(sbuf, mC, sbar, col0, m0);
             }
             __syncwarp();  // tcgen05.ld is .sync.aligned: the warp must be converged
             float v[CW];
             if (has_acc) {
-                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
-                                       static_cast<uint32_t>(acc * BN + c * CW);
+                const uint32_t col = static_cast<uint32_t>((C::BM == 128 ? acc * BN : 0) + c * CW);
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + col;
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(taddr, r);
                 if constexpr (CW == 64) {
@@ -720,7 +731,8 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
                 if (!__all_sync(0xffffffffu, ok))
                     return;
             }
-            epilogue_chunk_math<CW>(v, ec, sbuf, lane, use_c);
+            if (active)
+                epilogue_chunk_math<CW>(v, ec, sbuf, trow, use_c);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -754,14 +766,14 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
 
 // ---------------------------------------------------------------- kernel
 
-template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE>
+template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC,
                         const __grid_constant__ CUtensorMap tmD, const __grid_constant__ KParams p)
 {
-    using C = Cfg<CG, BN, BK, STAGES, ESIZE>;
+    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -824,11 +836,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t stage_base = base;
     if (warp == 0) {
         if (lane == 0)
-            role_producer<CG, BN, BK, STAGES, GROUPED, ESIZE>(p, &tmA, &tmB, stage_base, bar_full,
+            role_producer<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT>(p, &tmA, &tmB, stage_base, bar_full,
                                                               bar_empty, rank, w);
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {
-            role_mma<CG, BN, BK, STAGES, GROUPED, ESIZE>(p, stage_base, bar_full, bar_empty,
+            role_mma<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT>(p, stage_base, bar_full, bar_empty,
                                                   bar_acc_full, bar_acc_empty, bar_inject,
                                                   tmem_base, w);
             // every MMA issued by this thread has completed before TMEM is freed
@@ -837,11 +849,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         if (p.out_type == 0)
-            role_epilogue<CG, BN, BK, STAGES, GROUPED, ESIZE, 32>(p, &tmC, &tmD, base + C::EPI_OFF,
+            role_epilogue<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, 32>(p, &tmC, &tmD, base + C::EPI_OFF,
                                                            bar_acc_full, bar_acc_empty, bar_epi,
                                                            tmem_base, rank, warp, lane, w);
         else
-            role_epilogue<CG, BN, BK, STAGES, GROUPED, ESIZE, 64>(p, &tmC, &tmD, base + C::EPI_OFF,
+            role_epilogue<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, 64>(p, &tmC, &tmD, base + C::EPI_OFF,
                                                            bar_acc_full, bar_acc_empty, bar_epi,
                                                            tmem_base, rank, warp, lane, w);
         if (lane == 0)

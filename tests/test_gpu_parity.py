@@ -388,6 +388,28 @@ def test_config5_grouped_64_problems(g):
     _grouped(g, Ms, 4096, 2048, out="bf16", dist="uniform", seed=100, sample=True)
 
 
+# ---------------------------------------------------------------- 64-row tiles (M = 64, TMEM Layout F)
+
+@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("a_major,b_major", [("K", "K"), ("MN", "MN"), ("K", "MN")])
+@pytest.mark.parametrize("max_ctas", [0, 1])
+def test_m64_tiles_exact(g, tile_n, a_major, b_major, max_ctas):
+    # max_ctas = 1: one CTA walks every tile, alternating the lane-0 and lane-16 accumulators
+    run_case(g, 200, 520, 264, a_major=a_major, b_major=b_major, dist="int4", exact=True,
+             options=dict(tile_m=64, tile_n=tile_n, max_ctas=max_ctas))
+
+
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_m64_tiles_alpha_beta_ragged(g, out):
+    run_case(g, 130, 264, 200, out=out, alpha=0.5, beta=-1.0, dist="normal",
+             options=dict(tile_m=64, max_ctas=2))
+
+
+def test_small_m_defaults_to_64_row_tiles(g):
+    run_case(g, 48, 1000, 520, dist="normal", out="bf16")
+    run_case(g, 64, 16384, 512, dist="int4", exact=True)
+
+
 # ---------------------------------------------------------------- fp8 operands (kind::f8f6f4)
 
 @pytest.mark.parametrize("major", ["K", "MN"])
