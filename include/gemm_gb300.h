@@ -212,6 +212,14 @@ gemm_status_t gemm_f16_grouped(const gemm_problem_t *problems, int num_problems,
                                void *workspace, size_t workspace_bytes,
                                gemm_stream_t stream);
 
+/* The grouped call with explicit options (opts may be NULL; tile_m, timeout
+ * and flags as for gemm_ex). in_type: 0 fp16, 1 bf16. */
+gemm_status_t gemm_grouped_ex(int in_type, const gemm_problem_t *problems, int num_problems,
+                              gemm_major_t a_major, gemm_major_t b_major,
+                              gemm_out_t d_type, float alpha, float beta,
+                              void *workspace, size_t workspace_bytes,
+                              const gemm_options_t *opts, gemm_stream_t stream);
+
 /*
  * gemm_bf16_grouped_noalloc: the grouped bf16 GEMM for callers that cannot
  * allocate device memory when they launch it -- for instance code running

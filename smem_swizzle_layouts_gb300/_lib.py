@@ -52,6 +52,7 @@ _lib.gemm_fp8_ex.argtypes = _fp8 + [ctypes.POINTER(GemmOptions), _vp]
 _grouped = [ctypes.POINTER(GemmProblem), _int, _int, _int, _int, _f, _f, _vp, ctypes.c_size_t, _vp]
 _lib.gemm_bf16_grouped.argtypes = _grouped
 _lib.gemm_f16_grouped.argtypes = _grouped
+_lib.gemm_grouped_ex.argtypes = [_int] + _grouped[:-1] + [ctypes.POINTER(GemmOptions), _vp]
 _lib.gemm_bf16_grouped_noalloc.argtypes = [ctypes.POINTER(GemmProblem), _int, _int, _int, _int, _f, _f, _vp]
 _lib.gemm_grouped_workspace_size.argtypes = [_int]
 _lib.gemm_grouped_workspace_size.restype = ctypes.c_size_t
@@ -70,7 +71,7 @@ for _name in ("gemm_bf16", "gemm_f16", "gemm_ex", "gemm_fp8", "gemm_fp8_ex", "ge
     getattr(_lib, _name).restype = _int
 
 EXPORTED = ("gemm_bf16", "gemm_f16", "gemm_ex", "gemm_fp8", "gemm_fp8_ex", "gemm_grouped_workspace_size",
-            "gemm_bf16_grouped",
+            "gemm_bf16_grouped", "gemm_grouped_ex",
             "gemm_f16_grouped", "gemm_bf16_grouped_noalloc", "gemm_last_device_status", "gemm_status_string", "gemm_launch_count",
             "gemm_debug_descriptors", "gemm_debug_stage_image", "gemm_debug_inject_timeout")
 
@@ -203,6 +204,14 @@ def gemm_f16_grouped(problems, a_major, b_major, d_type, alpha, beta, workspace,
     arr = _problem_array(problems)
     _check(_lib.gemm_f16_grouped(arr, len(problems), a_major, b_major, d_type, alpha, beta,
                                  _addr(workspace), workspace_bytes, _stream(stream)), "gemm_f16_grouped")
+
+
+def gemm_grouped_ex(in_type, problems, a_major, b_major, d_type, alpha, beta, workspace, workspace_bytes,
+                    options=None, stream=None):
+    arr = _problem_array(problems)
+    _check(_lib.gemm_grouped_ex(in_type, arr, len(problems), a_major, b_major, d_type, alpha, beta,
+                                _addr(workspace), workspace_bytes, _opts(options), _stream(stream)),
+           "gemm_grouped_ex")
 
 
 NOALLOC_MAX_PROBLEMS = 128

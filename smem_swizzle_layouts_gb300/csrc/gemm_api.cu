@@ -493,10 +493,10 @@ gemm_status_t run_grouped(int in_bf16, const gemm_problem_t *probs, int n, int a
     gemm_options_t o = {};
     if (opts)
         o = *opts;
-    if (o.tile_n == 0)
-        o.tile_n = (maxN >= 192) ? 256 : 128;
     if (o.cta_group == 0)
         o.cta_group = 1;
+    if (o.tile_n == 0)  // grouped pairs are built for 256-wide tiles only
+        o.tile_n = (maxN >= 192 || o.cta_group == 2) ? 256 : 128;
     Plan pl;
     if ((s = make_plan(maxM, maxN, maxK, a_mn, b_mn, sms, &o, true, &pl)) != GEMM_OK)
         return s;
@@ -851,6 +851,17 @@ gemm_status_t gemm_bf16_grouped_noalloc(const gemm_problem_t *problems, int num_
 {
     return run_grouped_noalloc(1, problems, num_problems, a_major, b_major, d_type, alpha, beta,
                                reinterpret_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_grouped_ex(int in_type, const gemm_problem_t *problems, int num_problems,
+                              gemm_major_t a_major, gemm_major_t b_major, gemm_out_t d_type, float alpha,
+                              float beta, void *workspace, size_t workspace_bytes, const gemm_options_t *opts,
+                              gemm_stream_t stream)
+{
+    if (in_type != 0 && in_type != 1)
+        return GEMM_ERR_INVALID_ARG;
+    return run_grouped(in_type, problems, num_problems, a_major, b_major, d_type, alpha, beta, workspace,
+                       workspace_bytes, opts, reinterpret_cast<cudaStream_t>(stream));
 }
 
 gemm_status_t gemm_last_device_status(gemm_stream_t stream, uint32_t *detail)

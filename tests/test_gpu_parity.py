@@ -337,6 +337,7 @@ def test_config4_skinny(g, M, N, K, cg):
 
 def _grouped(g, Ms, N, K, *, out="bf16", a_major="K", b_major="K", alpha=1.0, beta=0.0, seed=40,
              dist="uniform", sample=None, options=None):
+    """Grouped GEMM through the C ABI (gemm_bf16_grouped, or gemm_grouped_ex with options)."""
     probs, host = [], []
     ldd = _ru(N, 4 if out == "f32" else 8)
     for i, M in enumerate(Ms):
@@ -353,8 +354,11 @@ def _grouped(g, Ms, N, K, *, out="bf16", a_major="K", b_major="K", alpha=1.0, be
         host.append((A, B, C, Dt, lda, ldb))
     ws_bytes = g.gemm_grouped_workspace_size(len(Ms))
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=DEV)
-    g.gemm_bf16_grouped(probs, 0 if a_major == "K" else 1, 0 if b_major == "K" else 1,
-                        {"f32": 0, "bf16": 1, "f16": 2}[out], alpha, beta, ws, ws_bytes)
+    am, bm, dt = (0 if a_major == "K" else 1), (0 if b_major == "K" else 1), {"f32": 0, "bf16": 1, "f16": 2}[out]
+    if options:
+        g.gemm_grouped_ex(1, probs, am, bm, dt, alpha, beta, ws, ws_bytes, options=options)
+    else:
+        g.gemm_bf16_grouped(probs, am, bm, dt, alpha, beta, ws, ws_bytes)
     st, word = g.gemm_last_device_status()
     assert st == g.OK, hex(word)
     for i, (M, (A, B, C, Dt, lda, ldb)) in enumerate(zip(Ms, host)):
@@ -378,14 +382,21 @@ def test_grouped_small_varied(g):
     _grouped(g, [64, 300, 128], 136, 72, out="f32", alpha=0.5, beta=-1.0, a_major="MN", b_major="MN")
 
 
+def test_grouped_cta_pairs_with_odd_row_tiles(g):
+    # pair tiles are 256 rows; 128-row and ragged problems leave the odd CTA partly idle
+    _grouped(g, [128, 384, 200, 512, 0, 136], 264, 192, out="bf16", options=dict(cta_group=2))
+    _grouped(g, [256, 130], 136, 320, out="f32", beta=1.0, a_major="MN", b_major="MN", options=dict(cta_group=2))
+
+
 def test_grouped_k_zero_problem(g):
     _grouped(g, [128, 256], 128, 0, out="f32", beta=2.0)
 
 
-def test_config5_grouped_64_problems(g):
+@pytest.mark.parametrize("cg", [1, 2])
+def test_config5_grouped_64_problems(g, cg):
     rng = np.random.default_rng(5)
     Ms = [int(x) for x in rng.integers(1, 33, 64) * 128]
-    _grouped(g, Ms, 4096, 2048, out="bf16", dist="uniform", seed=100, sample=True)
+    _grouped(g, Ms, 4096, 2048, out="bf16", dist="uniform", seed=100, sample=True, options=dict(cta_group=cg))
 
 
 # ---------------------------------------------------------------- 64-row tiles (M = 64, TMEM Layout F)
