@@ -225,6 +225,10 @@ class GemmJob:
         self.am = 0 if wl["a_major"] == "K" else 1
         self.bm = 0 if wl["b_major"] == "K" else 1
         self.dt = {"f32": 0, "bf16": 1, "f16": 2}[wl["out"]]
+        if options and options.get("workspace") is True:
+            # stream-K workspace, zeroed once ("workspace": true in the options)
+            options = dict(options, workspace=torch.zeros(g.gemm_streamk_workspace_size(), dtype=torch.uint8,
+                                                          device=dev))
         self.options = options
         self.flops = 2.0 * self.M * self.N * self.K
         # arguments marshalled once; each step is one call into the C ABI

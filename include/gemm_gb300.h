@@ -102,7 +102,33 @@ typedef enum {
  *   stats         diagnostics: NULL, or device memory of 16 uint64 per CTA
  *                 of the grid (at least 16 * number of SMs), where each CTA
  *                 writes cycles its roles spent waiting (slots 0-1 producer,
- *                 2-4 and 8-9 MMA issuer, 5-7 first epilogue warp).
+ *                 2-4 and 8-9 MMA issuer, 5-7 and 10-12 first epilogue warp:
+ *                 10-11 stream-K flag waits and partial-sum gathers, 12 the
+ *                 cycles after its last accumulator became ready).
+ *   stream_k      K-split scheduling of single (not grouped) problems with
+ *                 128-row tiles, so that a last, partly filled wave of tiles
+ *                 does not leave SMs idle: the tiles of whole waves run one
+ *                 per cluster as usual, and the K blocks of the remaining
+ *                 tiles (the ragged wave plus one full wave, or every tile
+ *                 when there are fewer tiles than two waves) are divided
+ *                 evenly among all clusters. A cluster that holds the first
+ *                 K block of a split tile adds the others' fp32 partial sums
+ *                 (left in `workspace`) and writes the tile; the result
+ *                 differs from the unsplit one only by summation order.
+ *                 The pages have no counterpart; it is a scheduling service
+ *                 of this library.
+ *                   0 (default) auto: split when `workspace` is given and a
+ *                     ragged last wave follows 2 to 7 full waves;
+ *                  -1 never; 1 always the split above; 2 split every tile;
+ *                   3 split only the tiles of the ragged last wave.
+ *                 A split needs at least as many K blocks in the split tiles
+ *                 as clusters in the grid, else the launch runs unsplit.
+ *   workspace / workspace_bytes  device memory for stream_k (NULL: no
+ *                 split): at least gemm_streamk_workspace_size() bytes,
+ *                 256-byte aligned, set to zero once before its first use
+ *                 (the library leaves it reusable: each launch tags its
+ *                 flags with a new value). Calls that may run at the same
+ *                 time, on different streams, need different workspaces.
  */
 typedef struct {
     int cta_group;
@@ -117,7 +143,15 @@ typedef struct {
     int timeout_ms;
     int flags;
     unsigned long long *stats;
+    int stream_k;
+    void *workspace;
+    size_t workspace_bytes;
 } gemm_options_t;
+
+/* Bytes of stream-K workspace for any single GEMM on the current device:
+ * one 4 x uint32 flag row and one 128 x 256 fp32 partial-sum slot per SM.
+ * 0 if the device cannot be queried. */
+size_t gemm_streamk_workspace_size(void);
 
 /* One problem of a grouped call. All share the call's majors, types,
  * alpha and beta; each has its own sizes, pointers and leading dims. */
@@ -294,6 +328,20 @@ gemm_status_t gemm_debug_stage_image(const void *src, int major, int swizzle,
                                      int64_t rows_total, int64_t k_total, int64_t ld,
                                      int rows, int bk, int64_t mn0, int64_t k0,
                                      void *out, gemm_stream_t stream);
+
+/*
+ * Host-side listing of the stream-K schedule (no GPU needed): the split the
+ * library would choose for `tiles` tiles of `kb_per_tile` K blocks on a
+ * grid of `clusters` clusters under stream_k `mode`, and the units of
+ * cluster `cluster` in the order its roles run them -- the same code the
+ * kernel's roles execute. Writes 6 int32 per unit to `out` (room for
+ * max_units): tile, first K block, end K block (-1: the whole tile), kind
+ * (0 whole, 1 contributor, 2 head), and for a head the first and last
+ * contributing cluster (else 0, -1). Returns the number of units, or -1
+ * when the launch would stay data-parallel (no units listed).
+ */
+int gemm_debug_streamk_units(int mode, int64_t tiles, int clusters, int kb_per_tile, int cluster,
+                             int32_t *out, int max_units);
 
 /* Test hook: the next GEMM launch makes its MMA warp wait on a barrier
  * that nothing arrives at, with a wait bound of `timeout_ms`; every role

@@ -34,7 +34,8 @@ _i64, _vp, _f, _int, _u32, _u64 = (ctypes.c_int64, ctypes.c_void_p, ctypes.c_flo
 class GemmOptions(ctypes.Structure):
     _fields_ = [("cta_group", _int), ("tile_m", _int), ("tile_n", _int), ("block_k", _int), ("swizzle_a", _int), ("swizzle_b", _int),
                 ("epilogue_swizzle", _int), ("max_ctas", _int), ("group_m", _int),
-                ("timeout_ms", _int), ("flags", _int), ("stats", _vp)]
+                ("timeout_ms", _int), ("flags", _int), ("stats", _vp),
+                ("stream_k", _int), ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t)]
 
 
 class GemmProblem(ctypes.Structure):
@@ -56,6 +57,8 @@ _lib.gemm_grouped_ex.argtypes = [_int] + _grouped[:-1] + [ctypes.POINTER(GemmOpt
 _lib.gemm_bf16_grouped_noalloc.argtypes = [ctypes.POINTER(GemmProblem), _int, _int, _int, _int, _f, _f, _vp]
 _lib.gemm_grouped_workspace_size.argtypes = [_int]
 _lib.gemm_grouped_workspace_size.restype = ctypes.c_size_t
+_lib.gemm_streamk_workspace_size.argtypes = []
+_lib.gemm_streamk_workspace_size.restype = ctypes.c_size_t
 _lib.gemm_last_device_status.argtypes = [_vp, ctypes.POINTER(_u32)]
 _lib.gemm_status_string.argtypes = [_int]
 _lib.gemm_status_string.restype = ctypes.c_char_p
@@ -63,6 +66,8 @@ _lib.gemm_launch_count.restype = _u64
 _lib.gemm_debug_descriptors.argtypes = [_int, _int, _int, _int, _u32, _int, _int, _int, _int, _int, _int,
                                         _vp, _vp]
 _lib.gemm_debug_stage_image.argtypes = [_vp, _int, _int, _i64, _i64, _i64, _int, _int, _i64, _i64, _vp, _vp]
+_lib.gemm_debug_streamk_units.argtypes = [_int, _i64, _int, _int, _int, ctypes.POINTER(ctypes.c_int32), _int]
+_lib.gemm_debug_streamk_units.restype = _int
 _lib.gemm_debug_inject_timeout.argtypes = [_int]
 _lib.gemm_debug_inject_timeout.restype = None
 for _name in ("gemm_bf16", "gemm_f16", "gemm_ex", "gemm_fp8", "gemm_fp8_ex", "gemm_bf16_grouped", "gemm_f16_grouped",
@@ -70,10 +75,12 @@ for _name in ("gemm_bf16", "gemm_f16", "gemm_ex", "gemm_fp8", "gemm_fp8_ex", "ge
               "gemm_last_device_status", "gemm_debug_descriptors", "gemm_debug_stage_image"):
     getattr(_lib, _name).restype = _int
 
-EXPORTED = ("gemm_bf16", "gemm_f16", "gemm_ex", "gemm_fp8", "gemm_fp8_ex", "gemm_grouped_workspace_size",
+EXPORTED = ("gemm_bf16", "gemm_f16", "gemm_ex", "gemm_fp8", "gemm_fp8_ex", "gemm_streamk_workspace_size",
+            "gemm_grouped_workspace_size",
             "gemm_bf16_grouped", "gemm_grouped_ex",
             "gemm_f16_grouped", "gemm_bf16_grouped_noalloc", "gemm_last_device_status", "gemm_status_string", "gemm_launch_count",
-            "gemm_debug_descriptors", "gemm_debug_stage_image", "gemm_debug_inject_timeout")
+            "gemm_debug_descriptors", "gemm_debug_stage_image", "gemm_debug_streamk_units",
+            "gemm_debug_inject_timeout")
 
 
 class GemmError(RuntimeError):
@@ -112,6 +119,11 @@ def _opts(options) -> ctypes.POINTER(GemmOptions) | None:
     opts = dict(options)
     if "stats" in opts:
         opts["stats"] = _addr(opts["stats"])
+    if "workspace" in opts:
+        ws = opts["workspace"]
+        opts["workspace"] = _addr(ws)
+        if "workspace_bytes" not in opts and ws is not None:
+            opts["workspace_bytes"] = ws.numel() * ws.element_size()
     return ctypes.pointer(GemmOptions(**opts))
 
 
@@ -177,6 +189,21 @@ def gemm_fp8_ex(M, N, K, A, a_format, a_major, lda, B, b_format, b_major, ldb, C
     _check(_lib.gemm_fp8_ex(M, N, K, _addr(A), a_format, a_major, lda, _addr(B), b_format, b_major, ldb,
                             _addr(C), ldc, _addr(D), ldd, d_type, alpha, beta, _opts(options), _stream(stream)),
            "gemm_fp8_ex")
+
+
+def gemm_debug_streamk_units(mode, tiles, clusters, kb_per_tile, cluster):
+    """The stream-K units of one cluster as (tile, kb0, kb1, kind, c_lo, c_hi) tuples, or None when unsplit."""
+    n = _lib.gemm_debug_streamk_units(mode, tiles, clusters, kb_per_tile, cluster, None, 0)
+    if n < 0:
+        return None
+    buf = (ctypes.c_int32 * (6 * max(n, 1)))()
+    _lib.gemm_debug_streamk_units(mode, tiles, clusters, kb_per_tile, cluster, buf, n)
+    return [tuple(buf[6 * i:6 * i + 6]) for i in range(n)]
+
+
+def gemm_streamk_workspace_size() -> int:
+    """Bytes of stream-K workspace for any single GEMM on the current device."""
+    return int(_lib.gemm_streamk_workspace_size())
 
 
 def gemm_grouped_workspace_size(num_problems: int) -> int:

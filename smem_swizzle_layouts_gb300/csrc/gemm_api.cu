@@ -27,6 +27,9 @@ __device__ unsigned int g_status_word;
 
 std::atomic<uint64_t> g_launches{0};
 std::atomic<int> g_inject_timeout_ms{0};
+// Tag of the latest stream-K launch; a split tile's head accepts a partial
+// sum only when the contributor's flag carries its own launch's tag.
+std::atomic<uint32_t> g_sk_epoch{0};
 
 std::mutex g_mu;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -230,6 +233,9 @@ struct Plan {
     unsigned long long timeout_ns;
     int flags;
     unsigned long long *stats;
+    int stream_k;
+    void *workspace;
+    size_t workspace_bytes;
 };
 
 // gemm_swizzle_t -> swizzle bits (B of Swizzle<B,4,3>): 32B 1, 64B 2, 128B 3, none 0.
@@ -246,8 +252,11 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
     if (opt.cta_group < 0 || opt.cta_group > 2 || opt.tile_n < 0 || opt.swizzle_a < 0 ||
         opt.swizzle_a > 4 || opt.swizzle_b < 0 || opt.swizzle_b > 4 || opt.max_ctas < 0 ||
         opt.group_m < 0 || opt.timeout_ms < 0 || opt.epilogue_swizzle < -1 ||
-        opt.epilogue_swizzle > 1 || opt.flags < 0 || opt.flags > 7 || opt.block_k < 0)
+        opt.epilogue_swizzle > 1 || opt.flags < 0 || opt.flags > 7 || opt.block_k < 0 ||
+        opt.stream_k < -1 || opt.stream_k > 3)
         return GEMM_ERR_INVALID_ARG;
+    if (opt.workspace && (reinterpret_cast<uintptr_t>(opt.workspace) & 255u) != 0)
+        return GEMM_ERR_ALIGNMENT;
 
     if (opt.tile_m != 0 && opt.tile_m != 64 && opt.tile_m != 128)
         return GEMM_ERR_INVALID_ARG;
@@ -323,7 +332,36 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
     plan->timeout_ns = static_cast<unsigned long long>(opt.timeout_ms ? opt.timeout_ms : 2000) * 1000000ull;
     plan->flags = opt.flags;
     plan->stats = opt.stats;
+    plan->stream_k = opt.stream_k;
+    plan->workspace = opt.workspace;
+    plan->workspace_bytes = opt.workspace_bytes;
     return GEMM_OK;
+}
+
+// Stream-K workspace: a row of 4 flags per CTA, then one 128 x BN fp32 slot per CTA.
+size_t sk_flag_bytes(int ctas) { return (static_cast<size_t>(ctas) * 4 * sizeof(uint32_t) + 1023) & ~size_t(1023); }
+
+size_t sk_bytes(int ctas, int bn) { return sk_flag_bytes(ctas) + static_cast<size_t>(ctas) * 128 * bn * sizeof(float); }
+
+// Stream-K split of `tiles` tiles of `kbt` K blocks over `clusters` clusters:
+// the number of tiles that stay data-parallel, or -1 for no split.
+int64_t sk_split(int mode, int64_t tiles, int64_t clusters, int64_t kbt)
+{
+    if (mode < 0 || kbt <= 0 || clusters <= 1)
+        return -1;
+    // auto: a ragged last wave after at least two full ones (fewer tiles than
+    // that leave split tiles whose short head pieces cannot hide the gather of
+    // partial sums; eight waves or more lose little to the ragged one)
+    if (mode == 0 && (tiles % clusters == 0 || tiles < 2 * clusters || tiles >= 8 * clusters))
+        return -1;
+    int64_t sk = tiles;
+    if (mode == 3 && tiles > clusters)
+        sk = tiles % clusters ? tiles % clusters : clusters;  // the ragged wave alone
+    else if (mode != 2 && tiles >= 2 * clusters)
+        sk = clusters + tiles % clusters;  // the ragged wave and one full wave
+    if (sk * kbt < clusters)
+        return -1;  // fewer K blocks than clusters: some would have no work
+    return tiles - sk;
 }
 
 int grid_for(const Plan &pl, Variant &v, int dev, int sms, int64_t tiles)
@@ -449,6 +487,26 @@ gemm_status_t run_single(const InFmt &f, int64_t M, int64_t N, int64_t K, const 
     p.num_tiles = static_cast<int>(tiles);
     fill_common(p, pl, f, a_mn, b_mn, d_type, alpha, beta, status);
     la.grid = grid_for(pl, *v, dev, sms, tiles);
+    if (pl.workspace && pl.bm == 128 && K > 0) {
+        // stream-K runs on every resident cluster
+        const int full = grid_for(pl, *v, dev, sms, static_cast<int64_t>(1) << 40);
+        const int64_t kbt = (K + pl.bk - 1) / pl.bk;
+        const int64_t dp = sk_split(pl.stream_k, tiles, full / pl.cg, kbt);
+        if (dp >= 0) {
+            if (pl.workspace_bytes < sk_bytes(full, pl.bn))
+                return GEMM_ERR_INVALID_ARG;
+            uint32_t epoch = g_sk_epoch.fetch_add(1) + 1;
+            if (epoch == 0)
+                epoch = g_sk_epoch.fetch_add(1) + 1;
+            la.grid = full;
+            p.sk_dp_tiles = static_cast<int>(dp);
+            p.kb_per_tile = static_cast<int>(kbt);
+            p.sk_iters = (tiles - dp) * kbt;
+            p.sk_flags = static_cast<uint32_t *>(pl.workspace);
+            p.sk_partials = reinterpret_cast<float *>(static_cast<unsigned char *>(pl.workspace) + sk_flag_bytes(full));
+            p.sk_epoch = epoch;
+        }
+    }
     la.stream = stream;
     cudaError_t e = v->launch(la);
     if (e != cudaSuccess)
@@ -822,6 +880,15 @@ gemm_status_t gemm_fp8(int64_t M, int64_t N, int64_t K, const void *A, gemm_fp8_
                        alpha, beta, nullptr, stream);
 }
 
+size_t gemm_streamk_workspace_size(void)
+{
+    int dev = 0, sms = 0;
+    unsigned int *status = nullptr;
+    if (device_state(&dev, &status, &sms) != GEMM_OK || sms <= 0)
+        return 0;
+    return sk_bytes(sms, 256);
+}
+
 size_t gemm_grouped_workspace_size(int num_problems)
 {
     if (num_problems <= 0)
@@ -951,6 +1018,45 @@ gemm_status_t gemm_debug_stage_image(const void *src, int major, int swizzle, in
         return cuda_fail(e);
     g_launches.fetch_add(1);
     return GEMM_OK;
+}
+
+int gemm_debug_streamk_units(int mode, int64_t tiles, int clusters, int kb_per_tile, int cluster, int32_t *out,
+                             int max_units)
+{
+    if (tiles < 0 || tiles >= (static_cast<int64_t>(1) << 31) || clusters < 1 || kb_per_tile < 1 || cluster < 0 ||
+        cluster >= clusters || max_units < 0 || (max_units > 0 && !out))
+        return -1;
+    const int64_t dp = sk_split(mode, tiles, clusters, kb_per_tile);
+    if (dp < 0)
+        return -1;
+    Sched sc;
+    std::memset(&sc, 0, sizeof(sc));
+    sc.num_tiles = static_cast<int>(tiles);
+    sc.sk_dp = static_cast<int>(dp);
+    sc.kbt = kb_per_tile;
+    sc.sk_iters = (tiles - dp) * kb_per_tile;
+    UnitIter it(sc, cluster, clusters);
+    Unit u;
+    int n = 0;
+    while (it.next(u)) {
+        if (n < max_units) {
+            int32_t *o = out + 6 * n;
+            const int kind = unit_kind(u, sc.kbt);
+            o[0] = u.tile;
+            o[1] = u.kb0;
+            o[2] = u.kb1;
+            o[3] = kind;
+            o[4] = 0;
+            o[5] = -1;
+            if (kind == kUnitHead) {
+                const long long first = static_cast<long long>(u.tile - sc.sk_dp) * sc.kbt;
+                o[4] = sk_owner(first + u.kb1, sc.sk_iters, clusters);
+                o[5] = sk_owner(first + sc.kbt - 1, sc.sk_iters, clusters);
+            }
+        }
+        ++n;
+    }
+    return n;
 }
 
 void gemm_debug_inject_timeout(int timeout_ms) { g_inject_timeout_ms.store(timeout_ms > 0 ? timeout_ms : 0); }

@@ -63,6 +63,7 @@ enum : uint32_t {
     kWaitEpiC = 5 << 8,
     kWaitInjected = 6 << 8,
     kWaitDrain = 7 << 8,
+    kWaitPartial = 8 << 8,
 };
 
 struct GroupedProblemDev {
@@ -90,6 +91,23 @@ struct KParams {
     int num_problems;
     int flags;                  // kFlag* tuning switches
     unsigned long long *stats;  // optional per-CTA wait counters (kStat* slots), or null
+    // Stream-K (single problems). Tiles [0, sk_dp_tiles) run data-parallel,
+    // one whole tile per unit; the K iterations of the remaining tiles
+    // (sk_iters = (num_tiles - sk_dp_tiles) * kb_per_tile) are split evenly
+    // across the clusters. A tile cut between clusters is finished by the one
+    // holding its first K block (its head). The others leave their fp32
+    // partial sums in sk_partials (slot cluster * CG + rank, 128 x BN) and
+    // raise their flags (sk_flags[(cluster * CG + rank) * 4 + warp] =
+    // sk_epoch). A head is always its cluster's last unit, so the other TMEM
+    // accumulator buffer is free while the head's MMAs run: the epilogue
+    // warps gather the partial sums into it meanwhile and add both buffers
+    // in the head's epilogue.
+    int sk_dp_tiles;
+    int kb_per_tile;
+    long long sk_iters;
+    float *sk_partials;
+    unsigned int *sk_flags;
+    unsigned int sk_epoch;
 };
 
 // Diagnostics: per-CTA counters written when KParams::stats is set.
@@ -104,6 +122,9 @@ enum : int {
     kStatEpiLoopCycles = 7,
     kStatMmaFullBlocked = 8,
     kStatTiles = 9,
+    kStatEpiPartialWaitCycles = 10,  // stream-K head: waiting for contributors' flags
+    kStatEpiPartialCycles = 11,      // stream-K head: gathering partial sums into TMEM
+    kStatEpiTailCycles = 12,         // from the last accumulator-full wait to the end
     kStatSlots = 16,
 };
 
@@ -198,6 +219,26 @@ struct Waiter {
         }
     }
 
+    // Waits until a global flag holds `value` (acquire at GPU scope).
+    __device__ bool wait_flag(const uint32_t *flag, uint32_t value, uint32_t code) const
+    {
+        if (ld_acquire_gpu(flag) == value)
+            return true;
+        const uint64_t t0 = globaltimer_ns();
+        while (true) {
+            for (int i = 0; i < 4; ++i)
+                if (ld_acquire_gpu(flag) == value)
+                    return true;
+            if (*abort_flag)
+                return false;
+            if (globaltimer_ns() - t0 > timeout_ns) {
+                fail(code);
+                return false;
+            }
+            __nanosleep(64);
+        }
+    }
+
     // Short wait used while tearing down; never records a code.
     __device__ bool drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) const
     {
@@ -223,6 +264,9 @@ struct Sched {
     int group_m;
     int num_problems;
     const GroupedProblemDev *problems;
+    int sk_dp;          // data-parallel tiles
+    int kbt;            // K blocks per tile (stream-K)
+    long long sk_iters; // stream-K iterations
 };
 
 __device__ __forceinline__ Sched make_sched(const KParams &p)
@@ -237,7 +281,73 @@ __device__ __forceinline__ Sched make_sched(const KParams &p)
     s.group_m = p.group_m;
     s.num_problems = p.num_problems;
     s.problems = p.problems;
+    s.sk_dp = p.sk_iters > 0 ? p.sk_dp_tiles : p.num_tiles;
+    s.kbt = p.kb_per_tile > 0 ? p.kb_per_tile : 1;
+    s.sk_iters = p.sk_iters;
     return s;
+}
+
+// One unit of a cluster's work: a tile and the K blocks [kb0, kb1) of it to
+// accumulate (kb1 < 0: all of the tile's K blocks).
+struct Unit {
+    int tile, kb0, kb1;
+};
+
+// A cluster's units in order: its data-parallel tiles c, c+G, ... below
+// sk_dp, then its share [c*S/G, (c+1)*S/G) of the S stream-K iterations, cut
+// at tile boundaries. Every role of every CTA of the cluster walks the same
+// sequence.
+struct UnitIter {
+    int G, dp, dp_next, kbt;
+    long long pos, end;
+
+    __host__ __device__ __forceinline__ UnitIter(const Sched &s, int c, int g)
+    {
+        G = g;
+        dp = s.sk_dp;
+        dp_next = c;
+        kbt = s.kbt;
+        pos = s.sk_iters * c / g;
+        end = s.sk_iters * (c + 1) / g;
+    }
+
+    __host__ __device__ __forceinline__ bool next(Unit &u)
+    {
+        if (dp_next < dp) {
+            u.tile = dp_next;
+            u.kb0 = 0;
+            u.kb1 = -1;
+            dp_next += G;
+            return true;
+        }
+        if (pos >= end)
+            return false;
+        const long long t = pos / kbt;
+        const int k0 = static_cast<int>(pos - t * kbt);
+        const long long left = end - pos;
+        const int k1 = static_cast<int>(left < static_cast<long long>(kbt - k0) ? k0 + left : kbt);
+        u.tile = dp + static_cast<int>(t);
+        u.kb0 = k0;
+        u.kb1 = k1;
+        pos += k1 - k0;
+        return true;
+    }
+};
+
+// Cluster whose stream-K share holds iteration i (shares start at floor(c*S/G)).
+__host__ __device__ __forceinline__ int sk_owner(long long i, long long S, int G)
+{
+    return static_cast<int>(((i + 1) * G - 1) / S);
+}
+
+// Part a unit plays in a split tile.
+enum : int { kUnitWhole = 0, kUnitContributor = 1, kUnitHead = 2 };
+
+__host__ __device__ __forceinline__ int unit_kind(const Unit &u, int kbt)
+{
+    if (u.kb1 < 0 || (u.kb0 == 0 && u.kb1 == kbt))
+        return kUnitWhole;
+    return u.kb0 > 0 ? kUnitContributor : kUnitHead;
 }
 
 struct TileInfo {
@@ -367,9 +477,11 @@ __device__ void role_producer(const KParams &p, const CUtensorMap *tmA, const CU
     bool ok = true;
     int last_prob = -1;
     unsigned long long st_wait = 0, st_blocked = 0;
-    for (int t = cluster_id; t < sched.num_tiles && ok; t += num_clusters) {
+    UnitIter units(sched, cluster_id, num_clusters);
+    Unit u;
+    while (ok && units.next(u)) {
         TileInfo ti;
-        decode_tile<GROUPED>(sched, t, ti);
+        decode_tile<GROUPED>(sched, u.tile, ti);
         const CUtensorMap *mA = tmA, *mB = tmB;
         if constexpr (GROUPED) {
             mA = maps + 4 * ti.prob;
@@ -381,9 +493,11 @@ __device__ void role_producer(const KParams &p, const CUtensorMap *tmA, const CU
             }
         }
         const int num_kb = ceil_div_i(ti.K, BK);
+        const int kb_lo = u.kb0, kb_hi = u.kb1 < 0 ? num_kb : u.kb1;
+        const bool whole = u.kb1 < 0;
         const int m0 = ti.m_blk * C::UMMA_M + C::BM * static_cast<int>(rank);
         const int n0 = ti.n_blk * BN + C::BN_LOCAL * static_cast<int>(rank);
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = kb_lo; kb < kb_hi; ++kb) {
             if (stats) {
                 const long long t0 = clock64();
                 const bool ready = mbar_try_wait(bar_empty + 8 * stage, phase ^ 1u);
@@ -403,7 +517,7 @@ __device__ void role_producer(const KParams &p, const CUtensorMap *tmA, const CU
             const uint32_t sA = smem + stage * C::STAGE_BYTES;
             const uint32_t sB = sA + C::A_BYTES;
             const uint32_t fb = full_target + 8 * stage;
-            const int k0 = kblock_at(kb, num_kb, flags, cluster_id) * BK;
+            const int k0 = (whole ? kblock_at(kb, num_kb, flags, cluster_id) : kb) * BK;
             // A and B boxes alternate, so both operands of the stage are in flight together
             for (int b = 0; b < nbox; ++b) {
                 if (b < boxA.nbox)
@@ -468,11 +582,14 @@ __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uin
     uint32_t acc_phase = 0;
     unsigned long long st_full = 0, st_acc = 0, st_blocked = 0, st_tiles = 0;
     const long long t_start = clock64();
-    for (int t = cluster_id; t < sched.num_tiles; t += num_clusters) {
+    UnitIter units(sched, cluster_id, num_clusters);
+    Unit u;
+    while (units.next(u)) {
         TileInfo ti;
-        decode_tile<GROUPED>(sched, t, ti);
+        decode_tile<GROUPED>(sched, u.tile, ti);
         const int num_kb = ceil_div_i(ti.K, BK);
-        if (num_kb == 0)
+        const int kb_lo = u.kb0, kb_hi = u.kb1 < 0 ? num_kb : u.kb1;
+        if (kb_hi <= kb_lo)
             continue;  // K == 0: the epilogue writes beta * C without the accumulator
         {
             const long long t0 = stats ? clock64() : 0;
@@ -485,7 +602,7 @@ __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uin
         tc_fence_after_sync();
         const uint32_t d_tmem = C::BM == 64 ? tmem_base + (static_cast<uint32_t>(16 * acc) << 16)
                                             : tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = kb_lo; kb < kb_hi; ++kb) {
             if (stats) {
                 const long long t0 = clock64();
                 const bool ready = mbar_try_wait(bar_full + 8 * stage, phase);
@@ -500,12 +617,13 @@ __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uin
             const uint64_t sdelta = static_cast<uint64_t>((stage * C::STAGE_BYTES) >> 4);
 #pragma unroll
             for (int j = 0; j < C::KSLICES; ++j) {
+                // the first MMA of a unit overwrites the accumulator, the rest add
                 if constexpr (ESIZE == 2)
                     mma_f16<CG>(d_tmem, a_desc0 + sdelta + a_off[j], b_desc0 + sdelta + b_off[j], idesc,
-                                (kb | j) != 0);
+                                ((kb - kb_lo) | j) != 0);
                 else
                     mma_f8<CG>(d_tmem, a_desc0 + sdelta + a_off[j], b_desc0 + sdelta + b_off[j], idesc,
-                               (kb | j) != 0);
+                               ((kb - kb_lo) | j) != 0);
             }
             if (multicast)
                 mma_commit_pair_multicast(bar_empty + 8 * stage);
@@ -622,6 +740,69 @@ __device__ __forceinline__ void epilogue_chunk_math(float (&acc)[CW], const EpiC
     }
 }
 
+// Stream-K head gather, one epilogue warp (TMEM lane quarter q, rows
+// 32q..32q+31): waits for the flags of the clusters that hold the rest of
+// split tile `ua`, then writes the sum of their fp32 partial sums into TMEM
+// accumulator buffer `buf` (the first n32 32-column groups), the buffer the
+// head's own MMAs do not use. False if a flag did not come in time.
+template <int CG, int BN>
+__device__ bool sk_gather(const Sched &sched, const Unit &ua, int n32, int buf, uint32_t tmem_base, int q,
+                          int prow, const float4 *partials, const uint32_t *sk_flags, uint32_t epoch, int rank,
+                          int num_clusters, const Waiter &w, unsigned long long *st_wait)
+{
+    const long long S = sched.sk_iters;
+    const long long first = static_cast<long long>(ua.tile - sched.sk_dp) * sched.kbt;
+    const int c_lo = sk_owner(first + ua.kb1, S, num_clusters);
+    const int c_hi = sk_owner(first + sched.kbt - 1, S, num_clusters);
+    const long long t0 = st_wait ? clock64() : 0;
+    bool ok = true;
+    for (int cc = c_lo; cc <= c_hi && ok; ++cc) {
+        if (S * cc / num_clusters == S * (cc + 1) / num_clusters)
+            continue;  // empty share: nothing to wait for
+        ok = w.wait_flag(sk_flags + (cc * CG + rank) * 4 + q, epoch, kRoleEpilogue | kWaitPartial);
+    }
+    if (!__all_sync(0xffffffffu, ok))
+        return false;
+    if (st_wait)
+        *st_wait += static_cast<unsigned long long>(clock64() - t0);
+    constexpr int kSlotVec = 128 * BN / 4;  // float4 per slot
+    constexpr int kGroups = 2;              // 32-column groups per batch of loads
+    const uint32_t tbase = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(buf * BN);
+    for (int c0 = 0; c0 < n32; c0 += kGroups) {
+        float v[kGroups][32];
+#pragma unroll
+        for (int b = 0; b < kGroups; ++b)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                v[b][i] = 0.0f;
+#pragma unroll 1
+        for (int cc = c_lo; cc <= c_hi; ++cc) {
+            if (S * cc / num_clusters == S * (cc + 1) / num_clusters)
+                continue;
+            const float4 *slot = partials + static_cast<size_t>(cc * CG + rank) * kSlotVec + prow;
+#pragma unroll
+            for (int b = 0; b < kGroups; ++b) {
+                // groups past n32 reload the last one (in the slot) and are not stored
+                const int cb = min(c0 + b, n32 - 1);
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+                    const float4 x = __ldcg(slot + (cb * 8 + g) * 128);
+                    v[b][4 * g] += x.x;
+                    v[b][4 * g + 1] += x.y;
+                    v[b][4 * g + 2] += x.z;
+                    v[b][4 * g + 3] += x.w;
+                }
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < kGroups; ++b)
+            if (c0 + b < n32)
+                tmem_st_32x32b_x32(tbase + static_cast<uint32_t>((c0 + b) * 32), v[b]);
+    }
+    tmem_st_wait();  // the head's epilogue (this warp) reads the buffer back
+    return true;
+}
+
 template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int CW>
 __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CUtensorMap *tmD,
                               uint32_t epi_base, uint32_t bar_acc_full, uint32_t bar_acc_empty,
@@ -651,11 +832,38 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
     int sel = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
-    unsigned long long st_accw = 0, st_cw = 0;
+    unsigned long long st_accw = 0, st_cw = 0, st_pw = 0, st_pe = 0;
+    long long t_last_acc = 0;
     const long long t_start = clock64();
-    for (int t = cluster_id; t < sched.num_tiles; t += num_clusters) {
+    // stream-K: this CTA's partial-sum slot, and its row in every slot
+    constexpr bool kStreamK = C::BM == 128 && !GROUPED;
+    const bool split = kStreamK && sched.sk_iters > 0;
+    float4 *const partials = reinterpret_cast<float4 *>(p.sk_partials);
+    uint32_t *const sk_flags = p.sk_flags;
+    const uint32_t epoch = p.sk_epoch;
+    const int prow = R * q + lane;
+    constexpr int kSlotVec = 128 * BN / 4;  // float4 per slot
+    UnitIter units(sched, cluster_id, num_clusters);
+    Unit u;
+    while (units.next(u)) {
         TileInfo ti;
-        decode_tile<GROUPED>(sched, t, ti);
+        decode_tile<GROUPED>(sched, u.tile, ti);
+        // a contributor leaves its partial sum for the tile's head; the head
+        // adds those partials (gathered into the spare accumulator buffer)
+        const int kind = split ? unit_kind(u, sched.kbt) : kUnitWhole;
+        const bool contributor = kind == kUnitContributor;
+        const bool head = kind == kUnitHead;
+        if (head) {
+            const int n_cols = min(BN, ti.N - ti.n_blk * BN);
+            const long long t0 = stats ? clock64() : 0;
+            const bool ok = sk_gather<CG, BN>(sched, u, (n_cols + 31) / 32, acc ^ 1, tmem_base, q, prow, partials,
+                                              sk_flags, epoch, static_cast<int>(rank), num_clusters, w,
+                                              stats ? &st_pw : nullptr);
+            if (stats)
+                st_pe += static_cast<unsigned long long>(clock64() - t0);
+            if (!ok)
+                return;
+        }
         const CUtensorMap *mC = tmC, *mD = tmD;
         if constexpr (GROUPED) {
             mC = maps + 4 * ti.prob + 2;
@@ -672,13 +880,52 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
         if (has_acc) {
             const long long tw = stats ? clock64() : 0;
             bool ok = w.wait(bar_acc_full + 8 * acc, acc_phase, kRoleEpilogue | kWaitAccFull, rank != 0);
-            if (stats)
-                st_accw += static_cast<unsigned long long>(clock64() - tw);
+            if (stats) {
+                t_last_acc = clock64();
+                st_accw += static_cast<unsigned long long>(t_last_acc - tw);
+            }
             if (!__all_sync(0xffffffffu, ok))
                 return;
             if (forward && ew == 0 && lane == 0)
                 mbar_arrive_cluster(peer_acc_full + 8 * acc);  // the odd CTA's half is complete too
             tc_fence_after_sync();
+        }
+        if (contributor) {
+            // contributor: the accumulator goes to this CTA's slot as fp32,
+            // laid out [column / 4][row][4] so that a warp writes 512
+            // contiguous bytes per store
+            float4 *const slot = partials + static_cast<size_t>(blockIdx.x) * kSlotVec;
+            for (int c = 0; c < BN / CW; ++c) {
+                if (ti.n_blk * BN + c * CW >= ti.N)
+                    break;
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
+                                       static_cast<uint32_t>(acc * BN + c * CW);
+                uint32_t r[32];
+#pragma unroll
+                for (int h = 0; h < CW / 32; ++h) {
+                    tmem_ld_32x32b_x32(taddr + 32 * h, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int g = 0; g < 8; ++g)
+                        __stcg(slot + (c * (CW / 4) + h * 8 + g) * 128 + prow,
+                               make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
+                                           __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3])));
+                }
+            }
+            tc_fence_before_sync();
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) {
+                st_release_gpu(sk_flags + blockIdx.x * 4 + q, epoch);
+                if constexpr (CG == 2)
+                    mbar_arrive_cluster(acc_empty_target + 8 * acc);
+                else
+                    mbar_arrive(bar_acc_empty + 8 * acc);
+            }
+            acc ^= 1;
+            if (acc == 0)
+                acc_phase ^= 1u;
+            continue;
         }
         for (int c = 0; c < BN / CW; ++c) {
             const int col0 = ti.n_blk * BN + c * CW;
@@ -722,6 +969,20 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
                 for (int i = 0; i < CW; ++i)
                     v[i] = 0.0f;
             }
+            if (head) {
+                // the contributors' partial sums, gathered into the other buffer
+                const uint32_t paddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
+                                       static_cast<uint32_t>((acc ^ 1) * BN + c * CW);
+#pragma unroll
+                for (int h = 0; h < CW / 32; ++h) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(paddr + 32 * h, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        v[32 * h + i] += __uint_as_float(r[i]);
+                }
+            }
             if (use_c) {
                 const long long tw = stats ? clock64() : 0;
                 bool ok = w.wait(sbar, epi_phase[sel], kRoleEpilogue | kWaitEpiC);
@@ -760,7 +1021,11 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
         unsigned long long *o = stats + blockIdx.x * kStatSlots;
         o[kStatEpiAccFullWaitCycles] = st_accw;
         o[kStatEpiCWaitCycles] = st_cw;
-        o[kStatEpiLoopCycles] = static_cast<unsigned long long>(clock64() - t_start);
+        const long long t_end = clock64();
+        o[kStatEpiLoopCycles] = static_cast<unsigned long long>(t_end - t_start);
+        o[kStatEpiPartialWaitCycles] = st_pw;
+        o[kStatEpiPartialCycles] = st_pe;
+        o[kStatEpiTailCycles] = static_cast<unsigned long long>(t_last_acc ? t_end - t_last_acc : 0);
     }
 }
 
