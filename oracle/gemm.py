@@ -58,6 +58,15 @@ def _load():
             lib.oracle_num_threads.restype = ctypes.c_int
             lib.oracle_decode.argtypes = [ctypes.c_int, ctypes.c_uint32]
             lib.oracle_decode.restype = ctypes.c_double
+            lib.oracle_decode_e8m0.argtypes = [ctypes.c_uint8]
+            lib.oracle_decode_e8m0.restype = ctypes.c_double
+            mx = [i64, i64, i64, vp, ctypes.c_int, ctypes.c_int, i64, vp, i64,
+                  vp, ctypes.c_int, ctypes.c_int, i64, vp, i64, vp, ctypes.c_int, i64,
+                  ctypes.c_double, ctypes.c_double]
+            lib.oracle_gemm_mx.argtypes = mx + [dp, dp, ctypes.c_int]
+            lib.oracle_gemm_mx.restype = ctypes.c_int
+            lib.oracle_gemm_mx_entries.argtypes = mx + [i64, vp, vp, dp, dp, ctypes.c_int]
+            lib.oracle_gemm_mx_entries.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -119,6 +128,63 @@ def gemm_entries(M, N, K, A, B, rows, cols, *, in_fmt="bf16", b_fmt=None, a_majo
     if rc:
         raise ValueError("oracle_gemm_entries: entry out of range")
     return D, S
+
+
+def _mx_common(M, N, K, A, B, SA, SB, a_major, b_major, lda, ldb, C, ldc):
+    A = np.ascontiguousarray(A)
+    B = np.ascontiguousarray(B)
+    SA = np.ascontiguousarray(SA, dtype=np.uint8)
+    SB = np.ascontiguousarray(SB, dtype=np.uint8)
+    lda = lda if lda is not None else (K if a_major == "K" else M)
+    ldb = ldb if ldb is not None else (K if b_major == "K" else N)
+    if C is not None:
+        C = np.ascontiguousarray(C)
+        ldc = ldc if ldc is not None else N
+    return A, B, SA, SB, lda, ldb, C, ldc
+
+
+def gemm_mx(M, N, K, A, B, SA, SB, *, in_fmt="e4m3", b_fmt=None, a_major="K", b_major="K", lda=None, ldb=None,
+            C=None, c_fmt="f32", ldc=None, alpha=1.0, beta=0.0, threads=0):
+    """Block-scaled (MXFP8) fp64 product; ``SA`` is M x ceil(K/32) and ``SB`` N x ceil(K/32) E8M0 codes.
+
+    Returns (D, S) as ``gemm`` does.
+    """
+    lib = _load()
+    A, B, SA, SB, lda, ldb, C, ldc = _mx_common(M, N, K, A, B, SA, SB, a_major, b_major, lda, ldb, C, ldc)
+    D = np.empty((M, N), dtype=np.float64)
+    S = np.empty((M, N), dtype=np.float64)
+    rc = lib.oracle_gemm_mx(M, N, K, _ptr(A), FMT[in_fmt], MAJOR[a_major], lda, _ptr(SA), SA.shape[1],
+                            _ptr(B), FMT[b_fmt or in_fmt], MAJOR[b_major], ldb, _ptr(SB), SB.shape[1],
+                            _ptr(C), FMT[c_fmt], ldc or 0, float(alpha), float(beta), _ptr(D), _ptr(S),
+                            int(threads))
+    if rc:
+        raise ValueError("oracle_gemm_mx rejected its arguments")
+    return D, S
+
+
+def gemm_mx_entries(M, N, K, A, B, SA, SB, rows, cols, *, in_fmt="e4m3", b_fmt=None, a_major="K", b_major="K",
+                    lda=None, ldb=None, C=None, c_fmt="f32", ldc=None, alpha=1.0, beta=0.0, threads=0):
+    """The block-scaled product at the listed entries only."""
+    lib = _load()
+    A, B, SA, SB, lda, ldb, C, ldc = _mx_common(M, N, K, A, B, SA, SB, a_major, b_major, lda, ldb, C, ldc)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    cols = np.ascontiguousarray(cols, dtype=np.int64)
+    D = np.empty(rows.size, dtype=np.float64)
+    S = np.empty(rows.size, dtype=np.float64)
+    rc = lib.oracle_gemm_mx_entries(M, N, K, _ptr(A), FMT[in_fmt], MAJOR[a_major], lda, _ptr(SA), SA.shape[1],
+                                    _ptr(B), FMT[b_fmt or in_fmt], MAJOR[b_major], ldb, _ptr(SB), SB.shape[1],
+                                    _ptr(C), FMT[c_fmt], ldc or 0, float(alpha), float(beta), rows.size,
+                                    _ptr(rows), _ptr(cols), _ptr(D), _ptr(S), int(threads))
+    if rc:
+        raise ValueError("oracle_gemm_mx_entries: bad arguments")
+    return D, S
+
+
+def decode_e8m0(codes) -> np.ndarray:
+    """Values 2^(e - 127) of E8M0 scale codes (255: NaN)."""
+    lib = _load()
+    c = np.asarray(codes).reshape(-1)
+    return np.array([lib.oracle_decode_e8m0(int(x)) for x in c], dtype=np.float64).reshape(np.shape(codes))
 
 
 def decode(bits, fmt: str) -> np.ndarray:

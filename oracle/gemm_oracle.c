@@ -243,6 +243,105 @@ int oracle_gemm_entries(int64_t M, int64_t N, int64_t K,
 }
 
 /*
+ * Block-scaled product (MXFP8, the block-scaled tcgen05 MMA of "06 Blackwell
+ * Tensor Core - tcgen05 MMA": A(i,k) is scaled by SFA[i][k/32] and B(k,j) by
+ * SFB[j][k/32]; the block of 32 elements and the E8M0 scale type follow the
+ * OCP Microscaling (MX) definition of MXFP8 that the page names):
+ *
+ *   D[i][j] = alpha * sum_k (sa(i, k/32) * A(i,k)) * (sb(j, k/32) * B(k,j)) + beta * C[i][j]
+ *
+ * sa, sb hold E8M0 codes, row-major: sa[i * ldsa + b] for row i of A and
+ * block b, sb[j * ldsb + b] for column j of B (ld >= ceil(K/32)). A code e
+ * means 2^(e - 127); 255 is NaN. S is the tolerance scale as for oracle_gemm,
+ * over the scaled products. Same loop order as oracle_gemm.
+ */
+double oracle_decode_e8m0(uint8_t e)
+{
+    return e == 255 ? NAN : ldexp(1.0, (int)e - 127);
+}
+
+int oracle_gemm_mx(int64_t M, int64_t N, int64_t K,
+                   const void *A, int in_fmt, int a_major, int64_t lda, const uint8_t *sa, int64_t ldsa,
+                   const void *B, int b_fmt, int b_major, int64_t ldb, const uint8_t *sb, int64_t ldsb,
+                   const void *C, int c_fmt, int64_t ldc,
+                   double alpha, double beta,
+                   double *D, double *S, int nthreads)
+{
+    if (M < 0 || N < 0 || K < 0 || ldsa < (K + 31) / 32 || ldsb < (K + 31) / 32)
+        return 1;
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    int64_t i;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (i = 0; i < M; ++i) {
+        double *acc = (double *)calloc((size_t)(N > 0 ? N : 1), sizeof(double));
+        double *sab = (double *)calloc((size_t)(N > 0 ? N : 1), sizeof(double));
+        for (int64_t k = 0; k < K; ++k) {
+            double a = oracle_decode_e8m0(sa[i * ldsa + k / 32]) * a_at(A, in_fmt, a_major, lda, i, k);
+            for (int64_t j = 0; j < N; ++j) {
+                double p = a * (oracle_decode_e8m0(sb[j * ldsb + k / 32]) * b_at(B, b_fmt, b_major, ldb, k, j));
+                acc[j] += p;
+                sab[j] += fabs(p);
+            }
+        }
+        for (int64_t j = 0; j < N; ++j) {
+            double c = (beta != 0.0 && C) ? load(C, c_fmt, i * ldc + j) : 0.0;
+            D[i * N + j] = alpha * acc[j] + beta * c;
+            if (S)
+                S[i * N + j] = fabs(alpha) * sab[j] + fabs(beta * c);
+        }
+        free(acc);
+        free(sab);
+    }
+    return 0;
+}
+
+/* The block-scaled product at selected entries (rows[e], cols[e]) only. */
+int oracle_gemm_mx_entries(int64_t M, int64_t N, int64_t K,
+                           const void *A, int in_fmt, int a_major, int64_t lda, const uint8_t *sa, int64_t ldsa,
+                           const void *B, int b_fmt, int b_major, int64_t ldb, const uint8_t *sb, int64_t ldsb,
+                           const void *C, int c_fmt, int64_t ldc,
+                           double alpha, double beta,
+                           int64_t n_entries, const int64_t *rows, const int64_t *cols,
+                           double *out_D, double *out_S, int nthreads)
+{
+    if (ldsa < (K + 31) / 32 || ldsb < (K + 31) / 32)
+        return 1;
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    int bad = 0;
+    int64_t e;
+#pragma omp parallel for schedule(dynamic, 16) reduction(| : bad)
+    for (e = 0; e < n_entries; ++e) {
+        int64_t i = rows[e], j = cols[e];
+        if (i < 0 || i >= M || j < 0 || j >= N) {
+            bad |= 1;
+            continue;
+        }
+        double acc = 0.0, sab = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double p = (oracle_decode_e8m0(sa[i * ldsa + k / 32]) * a_at(A, in_fmt, a_major, lda, i, k)) *
+                       (oracle_decode_e8m0(sb[j * ldsb + k / 32]) * b_at(B, b_fmt, b_major, ldb, k, j));
+            acc += p;
+            sab += fabs(p);
+        }
+        double c = (beta != 0.0 && C) ? load(C, c_fmt, i * ldc + j) : 0.0;
+        out_D[e] = alpha * acc + beta * c;
+        if (out_S)
+            out_S[e] = fabs(alpha) * sab + fabs(beta * c);
+    }
+    return bad;
+}
+
+/*
  * Round-to-nearest-even of x to a binary format with p significand bits
  * (hidden bit included), minimum normal exponent emin and maximum exponent
  * emax; subnormals are kept, overflow goes to infinity.

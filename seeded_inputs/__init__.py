@@ -164,3 +164,25 @@ def torch_from_bits(bits: np.ndarray, dtype: str):
     if dtype in ("e4m3", "e5m2"):
         return torch.from_numpy(b.view(np.uint8))  # raw bytes; the library reads them as fp8
     raise ValueError(dtype)
+
+
+def scale_codes(seed: int, rows: int, nblocks: int, lo: int = 124, hi: int = 130) -> np.ndarray:
+    """Seeded E8M0 scale codes, ``rows x nblocks`` uint8, uniform in [lo, hi]."""
+    z = splitmix64(seed, 0, rows * nblocks)
+    span = np.uint64(hi - lo + 1)
+    return ((z >> np.uint64(32)) % span + np.uint64(lo)).astype(np.uint8).reshape(rows, nblocks)
+
+
+def mx_scale_atoms(codes: np.ndarray, rows: int, K: int) -> np.ndarray:
+    """Arrange row-major scale codes (``rows x ceil(K/32)``) in the 512-byte atoms of the
+    block-scaled GEMM's ABI: atom (r // 128) * ceil(K/128) + k // 128, byte
+    16 * (r % 32) + 4 * ((r % 128) // 32) + (k // 32) % 4. Unused entries are 127."""
+    nb = (K + 31) // 32
+    groups = (K + 127) // 128
+    blocks = (rows + 127) // 128
+    out = np.full(blocks * groups * 512, 127, dtype=np.uint8)
+    r = np.arange(rows)[:, None]
+    b = np.arange(nb)[None, :]
+    idx = ((r // 128) * groups + b // 4) * 512 + 16 * (r % 32) + 4 * ((r % 128) // 32) + b % 4
+    out[idx.reshape(-1)] = codes[:rows, :nb].reshape(-1)
+    return out

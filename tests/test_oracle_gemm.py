@@ -242,3 +242,90 @@ def test_fp8_mixed_formats_match_float64_matmul():
     D, _ = G.gemm(M, N, K, A, B, in_fmt="e4m3", b_fmt="e5m2", a_major="K", b_major="MN")
     ref = si.bits_to_float64(A, "e4m3") @ si.bits_to_float64(B, "e5m2")
     assert np.allclose(D, ref, rtol=1e-13, atol=1e-13)
+
+
+# ---------------------------------------------------------------------------
+# Block-scaled (MXFP8) product: one E8M0 scale per 32 elements of K.
+# ---------------------------------------------------------------------------
+
+def test_e8m0_decode_is_a_power_of_two_and_255_is_nan():
+    d = G.decode_e8m0(np.array([0, 1, 126, 127, 128, 254, 255], dtype=np.uint8))
+    assert list(d[:6]) == [2.0 ** -127, 2.0 ** -126, 0.5, 1.0, 2.0, 2.0 ** 127]
+    assert np.isnan(d[6])
+
+
+def test_mx_unit_scales_reduce_to_the_fp8_product():
+    M, N, K = 9, 13, 100
+    A = si.matrix_bits(81, M, K, "normal", "e4m3")
+    B = si.matrix_bits(82, K, N, "normal", "e5m2", transpose=True)
+    ones_a = np.full((M, 4), 127, np.uint8)
+    ones_b = np.full((N, 4), 127, np.uint8)
+    D, S = G.gemm_mx(M, N, K, A, B, ones_a, ones_b, in_fmt="e4m3", b_fmt="e5m2")
+    D0, S0 = G.gemm(M, N, K, A, B, in_fmt="e4m3", b_fmt="e5m2")
+    assert np.array_equal(D, D0) and np.array_equal(S, S0)
+
+
+def test_mx_hand_case_in_exact_rationals():
+    # one output, K = 70: blocks [0,32), [32,64) and the partial block [64,70)
+    K = 70
+    A = si.matrix_bits(83, 1, K, "normal", "e4m3")
+    B = si.matrix_bits(84, K, 1, "normal", "e4m3", transpose=True)
+    sa = np.array([[125, 130, 127]], np.uint8)
+    sb = np.array([[129, 126, 131]], np.uint8)
+    a = _vals(A, "e4m3").reshape(-1)
+    b = _vals(B, "e4m3").reshape(-1)
+    want = Fraction(0)
+    for k in range(K):
+        blk = k // 32
+        want += (Fraction(2) ** (int(sa[0, blk]) - 127) * Fraction(a[k])) * \
+                (Fraction(2) ** (int(sb[0, blk]) - 127) * Fraction(b[k]))
+    D, _ = G.gemm_mx(1, 1, K, A, B, sa, sb, alpha=1.0)
+    assert Fraction(D[0, 0]) == want
+
+
+@pytest.mark.parametrize("a_major,b_major", [("K", "K"), ("MN", "K"), ("K", "MN")])
+def test_mx_integer_inputs_with_power_of_two_scales_are_exact(a_major, b_major):
+    M, N, K = 20, 36, 160
+    A = si.matrix_bits(85, M, K, "int4", "e4m3", transpose=(a_major == "MN"))
+    B = si.matrix_bits(86, K, N, "int4", "e4m3", transpose=(b_major == "K"))
+    sa = si.scale_codes(87, M, K // 32)
+    sb = si.scale_codes(88, N, K // 32)
+    D, _ = G.gemm_mx(M, N, K, A, B, sa, sb, a_major=a_major, b_major=b_major)
+    a = si.logical_values(85, M, K, "int4")
+    b = si.logical_values(86, K, N, "int4")
+    ref = np.zeros((M, N))
+    for blk in range(K // 32):
+        s = slice(32 * blk, 32 * blk + 32)
+        ref += np.exp2(sa[:, blk:blk + 1] - 127.0) * (a[:, s] @ b[s, :]) * np.exp2(sb[:, blk][None, :] - 127.0)
+    assert np.array_equal(D, ref)
+    # swapping the roles of the two scale tables (a transposed reading) is caught
+    D_bad, _ = G.gemm_mx(M, N, K, A, B, sa[:, ::-1], sb, a_major=a_major, b_major=b_major)
+    assert not np.array_equal(D_bad, ref)
+
+
+def test_mx_entries_match_full_product():
+    M, N, K = 40, 24, 96
+    A = si.matrix_bits(89, M, K, "normal", "e4m3")
+    B = si.matrix_bits(90, K, N, "normal", "e4m3", transpose=True)
+    sa = si.scale_codes(91, M, 3)
+    sb = si.scale_codes(92, N, 3)
+    C = si.matrix_bits(93, M, N, "normal", "f32")
+    D, S = G.gemm_mx(M, N, K, A, B, sa, sb, C=C, alpha=0.5, beta=-2.0)
+    rows = np.array([0, 39, 17, 5]); cols = np.array([0, 23, 11, 20])
+    De, Se = G.gemm_mx_entries(M, N, K, A, B, sa, sb, rows, cols, C=C, alpha=0.5, beta=-2.0)
+    assert np.array_equal(De, D[rows, cols]) and np.array_equal(Se, S[rows, cols])
+
+
+def test_mx_scale_atom_layout_by_hand():
+    # the atom arrangement the block-scaled ABI documents, checked at hand-picked positions
+    rows, K = 300, 260                       # 3 row blocks, 9 scale blocks in 3 K groups
+    codes = np.zeros((rows, 9), np.uint8)
+    codes[33, 5] = 201                       # row block 0, K group 1, byte 16*1 + 4*1 + 1
+    codes[130, 8] = 202                      # row block 1, K group 2, byte 16*2 + 4*0 + 0
+    codes[299, 0] = 203                      # row block 2, K group 0, byte 16*11 + 4*1 + 0
+    atoms = si.mx_scale_atoms(codes, rows, K)
+    assert atoms.size == 3 * 3 * 512
+    assert atoms[(0 * 3 + 1) * 512 + 21] == 201
+    assert atoms[(1 * 3 + 2) * 512 + 32] == 202
+    assert atoms[(2 * 3 + 0) * 512 + 180] == 203
+    assert (atoms == 201).sum() == 1 and (atoms == 202).sum() == 1 and (atoms == 203).sum() == 1
