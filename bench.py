@@ -66,6 +66,11 @@ WORKLOADS = {
         scale=1.0, seed=40, options=dict(cta_group=2, tile_n=256), in_fmt="e4m3", b_fmt="e4m3", peak_ratio=2.0,
         desc="8192^3 fp8 E4M3 x E4M3 (kind::f8f6f4), A and B K-major, U[-1,1], fp32 accumulate, bf16 out, "
              "cta_group::2 CTA pairs"),
+    "square8192_mxfp8": dict(
+        M=8192, N=8192, K=8192, a_major="K", b_major="K", out="bf16", alpha=1.0, beta=0.0, dist="uniform",
+        scale=1.0, seed=50, options=None, in_fmt="e4m3", b_fmt="e4m3", mx=True, peak_ratio=2.0,
+        desc="8192^3 block-scaled fp8 (MXFP8: E4M3 with one E8M0 scale per 32 elements of K, codes U{124..130}; "
+             "tcgen05 kind::mxf8f6f4), A and B K-major, U[-1,1], fp32 accumulate, bf16 out, 128x128 tiles"),
     "single_tile_128x128x32_f16": dict(
         M=128, N=128, K=32, a_major="K", b_major="MN", out="f32", alpha=1.0, beta=0.0, dist="uniform",
         scale=1.0, seed=0, options=None, in_fmt="f16",
@@ -190,6 +195,12 @@ def job_throughput(units_per_rank: float, world_size: int, max_ms: float) -> flo
     return units_per_rank * world_size / (max_ms / 1e3)
 
 
+def _mx_codes(wl):
+    """Seeded E8M0 scale codes of a block-scaled workload (row-major, one per 32 elements of K)."""
+    nb = (wl["K"] + 31) // 32
+    return si.scale_codes(wl["seed"] + 3, wl["M"], nb), si.scale_codes(wl["seed"] + 4, wl["N"], nb)
+
+
 def _torch_inputs(wl, dev, pinned=False):
     import torch
     in_fmt = wl.get("in_fmt", "bf16")
@@ -236,9 +247,18 @@ class GemmJob:
         if wl.get("in_fmt") in ("e4m3", "e5m2"):
             codes = {"e4m3": g.FP8_E4M3, "e5m2": g.FP8_E5M2}
             fp8 = (codes[wl["in_fmt"]], codes[wl.get("b_fmt", wl["in_fmt"])])
+        scales = None
+        if wl.get("mx"):
+            sa, sb = _mx_codes(wl)
+            self.bits = self.bits + (sa, sb)
+            host_s = [torch.from_numpy(si.mx_scale_atoms(c, n, self.K)).pin_memory()
+                      for c, n in ((sa, self.M), (sb, self.N))]
+            scales = [h.to(dev) for h in host_s]
+            self.pairs += list(zip(host_s, scales))
         self.call = g.GemmCall(self.in_type, self.M, self.N, self.K, self.A, self.am, self.A.stride(0), self.B,
                                self.bm, self.B.stride(0), self.C, self.N if self.C is not None else 0, self.D,
-                               self.N, self.dt, wl["alpha"], wl["beta"], options=options, stream=stream, fp8=fp8)
+                               self.N, self.dt, wl["alpha"], wl["beta"], options=options, stream=stream, fp8=fp8,
+                               scales=scales)
 
     def step(self):
         self.call()
@@ -371,7 +391,8 @@ def _run_ours(args, wl_name, wl, ws, rank, local):
 def _oracle_rows_rate(wl, bits, target_s, max_rows=None, fixed_rows=None):
     """Time the oracle on the first R rows of the workload; returns (flop/s, rows, seconds, threads)."""
     from oracle import gemm as og
-    A, B, C = bits
+    A, B, C = bits[:3]
+    scales = bits[3:] if len(bits) > 3 else None
     M, N, K = wl["M"], wl["N"], wl["K"]
     in_fmt = wl.get("in_fmt", "bf16")
     threads = og.num_threads()
@@ -384,9 +405,13 @@ def _oracle_rows_rate(wl, bits, target_s, max_rows=None, fixed_rows=None):
     def run(R):
         Ar, lda = rows_of(R)
         Cr = C[:R] if C is not None else None
+        kw = dict(in_fmt=in_fmt, b_fmt=wl.get("b_fmt", in_fmt), a_major=wl["a_major"], b_major=wl["b_major"],
+                  lda=lda, C=Cr, c_fmt=wl["out"], ldc=N, alpha=wl["alpha"], beta=wl["beta"], threads=threads)
         t0 = time.perf_counter()
-        og.gemm(R, N, K, Ar, B, in_fmt=in_fmt, a_major=wl["a_major"], b_major=wl["b_major"], lda=lda,
-                C=Cr, c_fmt=wl["out"], ldc=N, alpha=wl["alpha"], beta=wl["beta"], threads=threads)
+        if scales is not None:
+            og.gemm_mx(R, N, K, Ar, B, scales[0][:R], scales[1], **kw)
+        else:
+            og.gemm(R, N, K, Ar, B, **kw)
         return time.perf_counter() - t0
 
     if fixed_rows:
@@ -409,7 +434,9 @@ def _algorithmic_bytes(wl, job):
         N, K = wl["N"], wl["K"]
         return float(sum((M * K + K * N) * 2 + M * N * ob for M in job.Ms))
     M, N, K = wl["M"], wl["N"], wl["K"]
-    return float((M * K + K * N) * 2 + M * N * ob * (2 if wl["beta"] != 0.0 else 1))
+    eb = 1 if wl.get("in_fmt") in ("e4m3", "e5m2") else 2
+    sf = (M + N) * ((K + 31) // 32) if wl.get("mx") else 0  # one scale byte per 32 elements of K
+    return float((M * K + K * N) * eb + sf + M * N * ob * (2 if wl["beta"] != 0.0 else 1))
 
 
 def _reference_line(args, wl, config, metric):
@@ -466,6 +493,8 @@ def main():
     metric = "GEMM TFLOP/s (bf16 in, fp32 accum) and % of GB300 dense BF16 tensor peak"
     if wl.get("in_fmt") in ("e4m3", "e5m2"):
         metric = "GEMM TFLOP/s (fp8 in, fp32 accum) and % of GB300 dense FP8 tensor peak"
+    if wl.get("mx"):
+        metric = "GEMM TFLOP/s (MXFP8 block-scaled fp8 in, fp32 accum) and % of GB300 dense FP8 tensor peak"
 
     if args.impl == "reference":
         if rank == 0:
@@ -522,9 +551,12 @@ def _torch_inputs_host_only(wl):
     in_fmt = wl.get("in_fmt", "bf16")
     M, N, K = wl["M"], wl["N"], wl["K"]
     A = si.matrix_bits(wl["seed"], M, K, wl["dist"], in_fmt, scale=wl["scale"], transpose=wl["a_major"] == "MN")
-    B = si.matrix_bits(wl["seed"] + 1, K, N, wl["dist"], in_fmt, scale=wl["scale"], transpose=wl["b_major"] == "K")
+    B = si.matrix_bits(wl["seed"] + 1, K, N, wl["dist"], wl.get("b_fmt", in_fmt), scale=wl["scale"],
+                       transpose=wl["b_major"] == "K")
     C = (si.matrix_bits(wl["seed"] + 2, M, N, wl["dist"], wl["out"], scale=wl["scale"])
          if wl["beta"] != 0.0 else None)
+    if wl.get("mx"):
+        return (A, B, C) + _mx_codes(wl)
     return A, B, C
 
 

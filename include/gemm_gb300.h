@@ -99,6 +99,9 @@ typedef enum {
  *                 acquire at cluster scope (ablation). Bit 2 starts each
  *                 tile's K loop at a per-CTA offset so that CTAs sharing an
  *                 operand panel read different parts of it at a time.
+ *                 Bit 3 gives the operand loads an L2 evict_last policy and
+ *                 the C loads and D stores evict_first (ablation; no
+ *                 measured effect at 4096^3 or 8192^3).
  *   stats         diagnostics: NULL, or device memory of 16 uint64 per CTA
  *                 of the grid (at least 16 * number of SMs), where each CTA
  *                 writes cycles its roles spent waiting (slots 0-1 producer,
@@ -221,6 +224,41 @@ gemm_status_t gemm_fp8_ex(int64_t M, int64_t N, int64_t K,
                           void *D, int64_t ldd, gemm_out_t d_type,
                           float alpha, float beta, const gemm_options_t *opts,
                           gemm_stream_t stream);
+
+/*
+ * gemm_mxfp8: block-scaled fp8 GEMM (MXFP8: tcgen05 kind::mxf8f6f4 with
+ * scale_vec::1X; "06 Blackwell Tensor Core - tcgen05 MMA", block-scaled
+ * MMA: scale factors go from global memory to shared memory, then by
+ * tcgen05.cp into TMEM, where the MMA reads them next to A and B).
+ *   D = alpha * sum_k (sa[m, k/32] * A[m,k]) * (sb[n, k/32] * B[k,n]) + beta * C
+ * A and B are E4M3 or E5M2 exactly as for gemm_fp8_ex; every 32 consecutive
+ * elements of K of a row of A (column of B) share one scale, an 8-bit E8M0
+ * code e meaning 2^(e - 127) (255 is NaN). The scales are stored in 512-byte
+ * atoms, each covering 128 rows (of A; columns of B) x 4 scale blocks (128
+ * elements of K): row r and K element k live in atom
+ * (r / 128) * ceil(K / 128) + k / 128, at byte
+ * 16 * (r % 32) + 4 * ((r % 128) / 32) + (k / 32) % 4 of it -- the layout
+ * tcgen05.cp copies into TMEM, replicated over the four lane quarters.
+ * SFA and SFB are device pointers, 16-byte aligned, of
+ * gemm_mx_scale_bytes(M, K) and gemm_mx_scale_bytes(N, K) bytes; entries
+ * for rows past M (N) or blocks past K are read but multiply only zeros.
+ * Tiles are 128 x 128 with one CTA each, 256 elements of K per pipeline
+ * stage (block_k may ask for 128; anything else in opts that asks for other
+ * tiles returns GEMM_ERR_UNSUPPORTED); stream_k applies as for gemm_ex.
+ */
+gemm_status_t gemm_mxfp8(int64_t M, int64_t N, int64_t K,
+                         const void *A, gemm_fp8_t a_format, gemm_major_t a_major, int64_t lda,
+                         const void *SFA,
+                         const void *B, gemm_fp8_t b_format, gemm_major_t b_major, int64_t ldb,
+                         const void *SFB,
+                         const void *C, int64_t ldc,
+                         void *D, int64_t ldd, gemm_out_t d_type,
+                         float alpha, float beta, const gemm_options_t *opts,
+                         gemm_stream_t stream);
+
+/* Bytes of one scale tensor of gemm_mxfp8 for `rows` rows (M for SFA, N for
+ * SFB) and K: ceil(rows / 128) * ceil(K / 128) * 512; 0 if either is <= 0. */
+size_t gemm_mx_scale_bytes(int64_t rows, int64_t K);
 
 /*
  * Grouped GEMM: num_problems independent problems in one launch. The

@@ -109,6 +109,29 @@ G300_HD uint32_t make_idesc(int M, int N, int a_fmt, int b_fmt, int a_mn_major, 
     return d;
 }
 
+// Instruction descriptor of a block-scaled fp8 MMA (kind::mxf8f6f4): the
+// same shape, format and major fields, the scale format UE8M0 at bit 23, and
+// no D-format field: bits [4,6) and [29,31) carry the scale factor IDs of B
+// and A (the byte of each 32-bit scale column this MMA uses), added per MMA
+// by idesc_sf_ids.
+G300_HD uint32_t make_idesc_mx(int M, int N, int a_fmt, int b_fmt, int a_mn_major, int b_mn_major)
+{
+    uint32_t d = 0;
+    d |= static_cast<uint32_t>(a_fmt & 7) << 7;
+    d |= static_cast<uint32_t>(b_fmt & 7) << 10;
+    d |= static_cast<uint32_t>(a_mn_major & 1) << 15;
+    d |= static_cast<uint32_t>(b_mn_major & 1) << 16;
+    d |= static_cast<uint32_t>((N >> 3) & 0x3F) << 17;
+    d |= 1u << 23;  // scale format UE8M0
+    d |= static_cast<uint32_t>((M >> 4) & 0x1F) << 24;
+    return d;
+}
+
+G300_HD uint32_t idesc_sf_ids(uint32_t idesc, int a_sf_id, int b_sf_id)
+{
+    return idesc | (static_cast<uint32_t>(b_sf_id & 3) << 4) | (static_cast<uint32_t>(a_sf_id & 3) << 29);
+}
+
 G300_HD uint32_t make_idesc_f16(int M, int N, int in_bf16, int a_mn_major, int b_mn_major)
 {
     return make_idesc(M, N, in_bf16, in_bf16, a_mn_major, b_mn_major);

@@ -41,13 +41,14 @@ struct Variant {
     bool grouped;
     int esize;
     int bm;
+    bool mx;  // block-scaled fp8
     cudaError_t (*launch)(const LaunchArgs &);
     cudaError_t (*resident)(int *);
     int resident_cache[kMaxDevices];
 };
 
-#define G300_VARIANT_ROW(CG, BN, BK, ST, GR, ES, BM) \
-    {CG, BN, BK, ST, GR, ES, BM, &launch_gemm<CG, BN, BK, ST, GR, ES, BM>, &resident_ctas<CG, BN, BK, ST, GR, ES, BM>, {0}},
+#define G300_VARIANT_ROW(CG, BN, BK, ST, GR, ES, BM, MX) \
+    {CG, BN, BK, ST, GR, ES, BM, MX, &launch_gemm<CG, BN, BK, ST, GR, ES, BM, MX>, &resident_ctas<CG, BN, BK, ST, GR, ES, BM, MX>, {0}},
 Variant g_variants[] = {G300_VARIANTS(G300_VARIANT_ROW)};
 #undef G300_VARIANT_ROW
 
@@ -102,23 +103,29 @@ int resident_for(Variant &v, int dev)
     return v.resident_cache[dev];
 }
 
-Variant *find_variant(int cg, int bn, int bk, bool grouped, int esize = 2, int bm = 128)
+Variant *find_variant(int cg, int bn, int bk, bool grouped, int esize = 2, int bm = 128, bool mx = false)
 {
     for (auto &v : g_variants)
-        if (v.cg == cg && v.bn == bn && v.bk == bk && v.grouped == grouped && v.esize == esize && v.bm == bm)
+        if (v.cg == cg && v.bn == bn && v.bk == bk && v.grouped == grouped && v.esize == esize && v.bm == bm &&
+            v.mx == mx)
             return &v;
     return nullptr;
 }
 
 // Operand element type of a call: storage code for the tensor maps (0 fp16,
-// 1 bf16, 2 fp8 bytes), element size, and the MMA format code of A and B.
+// 1 bf16, 2 fp8 bytes), element size, the MMA format code of A and B, and
+// whether the operands carry block scales.
 struct InFmt {
     int dcode, esize, a_fmt, b_fmt;
+    bool mx;
 };
 
-InFmt fmt16(int in_bf16) { return InFmt{in_bf16, 2, in_bf16, in_bf16}; }
+InFmt fmt16(int in_bf16) { return InFmt{in_bf16, 2, in_bf16, in_bf16, false}; }
 
-InFmt fmt8(int a_fmt, int b_fmt) { return InFmt{2, 1, a_fmt, b_fmt}; }
+InFmt fmt8(int a_fmt, int b_fmt) { return InFmt{2, 1, a_fmt, b_fmt, false}; }
+
+// Block-scaled fp8: the same operand bytes plus E8M0 scale atoms.
+InFmt fmtmx(int a_fmt, int b_fmt) { return InFmt{2, 1, a_fmt, b_fmt, true}; }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -244,7 +251,7 @@ int swz_bits_of(int opt) { return opt == GEMM_SWIZZLE_NONE ? 0 : opt; }
 // Choose the tile configuration; fills `plan` or returns an error for options
 // this build cannot honour.
 gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int sms,
-                        const gemm_options_t *o, bool grouped, Plan *plan, int esize = 2)
+                        const gemm_options_t *o, bool grouped, Plan *plan, int esize = 2, bool mx = false)
 {
     gemm_options_t opt = {};
     if (o)
@@ -252,7 +259,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
     if (opt.cta_group < 0 || opt.cta_group > 2 || opt.tile_n < 0 || opt.swizzle_a < 0 ||
         opt.swizzle_a > 4 || opt.swizzle_b < 0 || opt.swizzle_b > 4 || opt.max_ctas < 0 ||
         opt.group_m < 0 || opt.timeout_ms < 0 || opt.epilogue_swizzle < -1 ||
-        opt.epilogue_swizzle > 1 || opt.flags < 0 || opt.flags > 7 || opt.block_k < 0 ||
+        opt.epilogue_swizzle > 1 || opt.flags < 0 || opt.flags > 15 || opt.block_k < 0 ||
         opt.stream_k < -1 || opt.stream_k > 3)
         return GEMM_ERR_INVALID_ARG;
     if (opt.workspace && (reinterpret_cast<uintptr_t>(opt.workspace) & 255u) != 0)
@@ -298,11 +305,22 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
     }
     // 64-row tiles (M = 64 MMAs) when asked, or for problems of at most 64 rows
     // (compiled for 128- and 256-wide N tiles)
-    const int bm = opt.tile_m ? opt.tile_m
-                              : (cg == 1 && M <= 64 && esize == 2 && !grouped && bn >= 128 ? 64 : 128);
+    int bm = opt.tile_m ? opt.tile_m
+                        : (cg == 1 && M <= 64 && esize == 2 && !grouped && bn >= 128 ? 64 : 128);
     if (bm == 64 && opt.block_k == 0)
         bk = bn == 256 ? 64 : 128;
-    if (!find_variant(cg, bn, bk, grouped, esize, bm))
+    if (mx) {
+        // block-scaled tiles are built as one CTA of 128 x 128, 256 (or 128)
+        // elements of K per stage
+        if (opt.cta_group > 1 || (opt.tile_m && opt.tile_m != 128) || (opt.tile_n && opt.tile_n != 128) ||
+            (opt.block_k && opt.block_k != 128 && opt.block_k != 256))
+            return GEMM_ERR_UNSUPPORTED;
+        cg = 1;
+        bn = 128;
+        bk = opt.block_k ? opt.block_k : 256;
+        bm = 128;
+    }
+    if (!find_variant(cg, bn, bk, grouped, esize, bm, mx))
         return GEMM_ERR_UNSUPPORTED;
 
     auto pick_swz = [&](int requested, int mn_major) -> int {
@@ -440,7 +458,8 @@ gemm_status_t check_problem(int64_t M, int64_t N, int64_t K, const void *A, int 
 gemm_status_t run_single(const InFmt &f, int64_t M, int64_t N, int64_t K, const void *A, int a_major,
                          int64_t lda, const void *B, int b_major, int64_t ldb, const void *C,
                          int64_t ldc, void *D, int64_t ldd, int d_type, float alpha, float beta,
-                         const gemm_options_t *opts, cudaStream_t stream)
+                         const gemm_options_t *opts, cudaStream_t stream, const void *sfa = nullptr,
+                         const void *sfb = nullptr)
 {
     if (!valid_enum(a_major) || !valid_enum(b_major) || d_type < 0 || d_type > 2)
         return GEMM_ERR_INVALID_ARG;
@@ -448,14 +467,20 @@ gemm_status_t run_single(const InFmt &f, int64_t M, int64_t N, int64_t K, const 
     gemm_status_t s = check_problem(M, N, K, A, a_mn, lda, B, b_mn, ldb, C, ldc, D, ldd, d_type, beta, f.esize);
     if (s != GEMM_OK || M == 0 || N == 0)
         return s;
+    if (f.mx && K > 0) {
+        if (!sfa || !sfb)
+            return GEMM_ERR_INVALID_ARG;
+        if (!aligned16(sfa) || !aligned16(sfb))
+            return GEMM_ERR_ALIGNMENT;
+    }
     int dev = 0, sms = 0;
     unsigned int *status = nullptr;
     if ((s = device_state(&dev, &status, &sms)) != GEMM_OK)
         return s;
     Plan pl;
-    if ((s = make_plan(M, N, K, a_mn, b_mn, sms, opts, false, &pl, f.esize)) != GEMM_OK)
+    if ((s = make_plan(M, N, K, a_mn, b_mn, sms, opts, false, &pl, f.esize, f.mx)) != GEMM_OK)
         return s;
-    Variant *v = find_variant(pl.cg, pl.bn, pl.bk, false, f.esize, pl.bm);
+    Variant *v = find_variant(pl.cg, pl.bn, pl.bk, false, f.esize, pl.bm, f.mx);
 
     LaunchArgs la;
     std::memset(&la, 0, sizeof(la));
@@ -486,6 +511,11 @@ gemm_status_t run_single(const InFmt &f, int64_t M, int64_t N, int64_t K, const 
         return GEMM_ERR_UNSUPPORTED;
     p.num_tiles = static_cast<int>(tiles);
     fill_common(p, pl, f, a_mn, b_mn, d_type, alpha, beta, status);
+    if (f.mx) {
+        p.sfa = static_cast<const uint8_t *>(sfa);
+        p.sfb = static_cast<const uint8_t *>(sfb);
+        p.sf_groups = static_cast<int>((K + 127) / 128);
+    }
     la.grid = grid_for(pl, *v, dev, sms, tiles);
     if (pl.workspace && pl.bm == 128 && K > 0) {
         // stream-K runs on every resident cluster
@@ -878,6 +908,26 @@ gemm_status_t gemm_fp8(int64_t M, int64_t N, int64_t K, const void *A, gemm_fp8_
 {
     return gemm_fp8_ex(M, N, K, A, a_format, a_major, lda, B, b_format, b_major, ldb, C, ldc, D, ldd, d_type,
                        alpha, beta, nullptr, stream);
+}
+
+size_t gemm_mx_scale_bytes(int64_t rows, int64_t K)
+{
+    if (rows <= 0 || K <= 0)
+        return 0;
+    return static_cast<size_t>((rows + 127) / 128) * static_cast<size_t>((K + 127) / 128) * 512;
+}
+
+gemm_status_t gemm_mxfp8(int64_t M, int64_t N, int64_t K, const void *A, gemm_fp8_t a_format,
+                         gemm_major_t a_major, int64_t lda, const void *SFA, const void *B, gemm_fp8_t b_format,
+                         gemm_major_t b_major, int64_t ldb, const void *SFB, const void *C, int64_t ldc, void *D,
+                         int64_t ldd, gemm_out_t d_type, float alpha, float beta, const gemm_options_t *opts,
+                         gemm_stream_t stream)
+{
+    if ((a_format != GEMM_FP8_E4M3 && a_format != GEMM_FP8_E5M2) ||
+        (b_format != GEMM_FP8_E4M3 && b_format != GEMM_FP8_E5M2))
+        return GEMM_ERR_INVALID_ARG;
+    return run_single(fmtmx(a_format, b_format), M, N, K, A, a_major, lda, B, b_major, ldb, C, ldc, D, ldd, d_type,
+                      alpha, beta, opts, reinterpret_cast<cudaStream_t>(stream), SFA, SFB);
 }
 
 size_t gemm_streamk_workspace_size(void)

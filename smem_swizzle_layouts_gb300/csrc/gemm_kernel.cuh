@@ -108,6 +108,11 @@ struct KParams {
     float *sk_partials;
     unsigned int *sk_flags;
     unsigned int sk_epoch;
+    // Block-scaled operands: E8M0 scale atoms of A and B (512 bytes per 128
+    // rows x 128 elements of K, row block i and K group g at (i * sf_groups + g) * 512)
+    const uint8_t *sfa;
+    const uint8_t *sfb;
+    int sf_groups;
 };
 
 // Diagnostics: per-CTA counters written when KParams::stats is set.
@@ -132,6 +137,7 @@ enum : int {
     kFlagPairForward = 1,      // CTA pairs: forward releases with remote arrives (ablation)
     kFlagAllClusterWaits = 2,  // CTA pairs: cluster-scope acquire on every wait (ablation)
     kFlagRotateK = 4,          // start each tile's K loop at a per-cluster offset
+    kFlagCacheHints = 8,       // operands evict_last, C loads and D stores evict_first in L2
 };
 
 // K block processed at iteration `it` of a tile: with kFlagRotateK the
@@ -150,22 +156,36 @@ __device__ __forceinline__ int kblock_at(int it, int num_kb, int flags, int clus
 // rows per CTA, 128 (row m in TMEM lane m) or 64 (cta_group::1 only, Layout F:
 // rows 16g..16g+15 in lanes 32g+a..32g+a+15; the two accumulators of the
 // double buffer take lane alignments a = 0 and 16 and share their columns).
-template <int CG, int BN, int BK, int STAGES, int ESIZE = 2, int BMT = 128>
+template <int CG, int BN, int BK, int STAGES, int ESIZE = 2, int BMT = 128, bool MX = false>
 struct Cfg {
     static constexpr int BM = BMT;             // accumulator rows per CTA
     static constexpr int BN_LOCAL = BN / CG;   // B columns loaded by each CTA
     static constexpr int A_BYTES = BM * BK * ESIZE;
     static constexpr int B_BYTES = BN_LOCAL * BK * ESIZE;
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    // Block-scaled stages also carry the scale atoms of their K range: one
+    // 512-byte atom covers 128 rows x 4 scale blocks (128 elements of K)
+    static constexpr int KGROUPS = MX ? BK / 128 : 0;
+    static constexpr int SF_A_BYTES = 512 * KGROUPS * (BM / 128);
+    static constexpr int SF_B_BYTES = 512 * KGROUPS * (BN_LOCAL / 128);
+    static constexpr int SF_OFF = A_BYTES + B_BYTES;  // within a stage
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SF_A_BYTES + SF_B_BYTES;
     static constexpr int TX_BYTES = STAGE_BYTES * CG;  // bytes landing on one full barrier
     static constexpr int EPI_OFF = STAGES * STAGE_BYTES;
-    static constexpr int EPI_BYTES = kEpiWarps * 2 * kEpiBufBytes;
+    // staging chunks per epilogue warp: two (a store may still read one while
+    // the next is filled); block-scaled tiles keep one, to leave room for the
+    // scale atoms of three 256-element K stages
+    static constexpr int EPI_BUFS = MX ? 1 : 2;
+    static constexpr int EPI_BYTES = kEpiWarps * EPI_BUFS * kEpiBufBytes;
     static constexpr int BAR_OFF = EPI_OFF + EPI_BYTES;
     // full[S], empty[S], acc_full[2], acc_empty[2], epi[4][2], drain, inject
     static constexpr int NUM_BARS = 2 * STAGES + 2 + 2 + 2 * kEpiWarps + 2;
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack to align the base
-    static constexpr int TMEM_COLS = BMT == 64 ? BN : 2 * BN;
+    // TMEM: two accumulators, then (block-scaled) per stage 4 columns of A
+    // scales and 4 of B scales for each K group
+    static constexpr int SF_COL0 = 2 * BN;
+    static constexpr int SF_COLS = 8 * KGROUPS;
+    static constexpr int TMEM_COLS = BMT == 64 ? BN : MX ? 512 : 2 * BN;
     static constexpr int UMMA_M = BM * CG;
     static constexpr int EPI_ROWS = BM / 4;    // output rows per epilogue warp
     static_assert(BMT == 128 || (BMT == 64 && CG == 1), "64-row tiles are single-CTA");
@@ -176,6 +196,9 @@ struct Cfg {
                   "TMEM allocation: power of two, 32..512 columns");
     static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
     static_assert(CG == 1 || BN % 32 == 0, "pair tiles split N in halves of whole atoms");
+    static_assert(!MX || (CG == 1 && BMT == 128 && BN == 128 && ESIZE == 1 && BK % 128 == 0 &&
+                          SF_COL0 + STAGES * SF_COLS <= 512),
+                  "block-scaled tiles: one CTA, 128 x 128, fp8, whole 128-element K groups");
 };
 
 // ---------------------------------------------------------------- waits
@@ -438,6 +461,19 @@ __device__ __forceinline__ void issue_box(const CUtensorMap *map, uint32_t dst, 
         tma_load_2d_pair(dst + static_cast<uint32_t>(b) * o.smem_step, map, bar, x, y);
 }
 
+// issue_box with an L2 eviction policy.
+template <int CG>
+__device__ __forceinline__ void issue_box_hint(const CUtensorMap *map, uint32_t dst, uint32_t bar,
+                                               const OperandBoxes &o, int b, int mn0, int k0, uint64_t policy)
+{
+    const int x = o.mn_major ? mn0 + b * o.step : k0 + b * o.step;
+    const int y = o.mn_major ? k0 : mn0;
+    if constexpr (CG == 1)
+        tma_load_2d_hint(dst + static_cast<uint32_t>(b) * o.smem_step, map, bar, x, y, policy);
+    else
+        tma_load_2d_pair_hint(dst + static_cast<uint32_t>(b) * o.smem_step, map, bar, x, y, policy);
+}
+
 // Issue every TMA box of one operand stage (used by the inspection kernel).
 template <int CG>
 __device__ __forceinline__ void load_operand_stage(const CUtensorMap *map, uint32_t dst,
@@ -453,12 +489,12 @@ __device__ __forceinline__ int ceil_div_i(int a, int b) { return (a + b - 1) / b
 
 // ---------------------------------------------------------------- roles
 
-template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT>
+template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, bool MX>
 __device__ void role_producer(const KParams &p, const CUtensorMap *tmA, const CUtensorMap *tmB,
                               uint32_t smem, uint32_t bar_full, uint32_t bar_empty,
                               uint32_t rank, const Waiter &w)
 {
-    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT>;
+    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, MX>;
     const Sched sched = make_sched(p);
     const int flags = p.flags;
     unsigned long long *const stats = p.stats;
@@ -467,6 +503,12 @@ __device__ void role_producer(const KParams &p, const CUtensorMap *tmA, const CU
     const OperandBoxes boxB = operand_boxes(p.b_mn, p.b_swz, C::BN_LOCAL, BK, ESIZE);
     const int nbox = boxA.nbox > boxB.nbox ? boxA.nbox : boxB.nbox;
     const bool forward = CG == 2 && rank == 0 && (flags & kFlagPairForward);
+    const uint8_t *const sfa = p.sfa;
+    const uint8_t *const sfb = p.sfb;
+    const int sf_groups = p.sf_groups;
+    // operand tiles are re-read by other tiles of the wave: keep them in L2
+    const bool hints = (flags & kFlagCacheHints) != 0;
+    const uint64_t keep = hints ? l2_policy_evict_last() : 0;
 
     const uint32_t full_target = (CG == 2) ? mapa_shared(bar_full, 0) : bar_full;
     const uint32_t peer_empty = (CG == 2 && rank == 0) ? mapa_shared(bar_empty, 1) : 0u;
@@ -519,11 +561,34 @@ __device__ void role_producer(const KParams &p, const CUtensorMap *tmA, const CU
             const uint32_t fb = full_target + 8 * stage;
             const int k0 = (whole ? kblock_at(kb, num_kb, flags, cluster_id) : kb) * BK;
             // A and B boxes alternate, so both operands of the stage are in flight together
-            for (int b = 0; b < nbox; ++b) {
-                if (b < boxA.nbox)
-                    issue_box<CG>(mA, sA, fb, boxA, b, m0, k0);
-                if (b < boxB.nbox)
-                    issue_box<CG>(mB, sB, fb, boxB, b, n0, k0);
+            if (hints) {
+                for (int b = 0; b < nbox; ++b) {
+                    if (b < boxA.nbox)
+                        issue_box_hint<CG>(mA, sA, fb, boxA, b, m0, k0, keep);
+                    if (b < boxB.nbox)
+                        issue_box_hint<CG>(mB, sB, fb, boxB, b, n0, k0, keep);
+                }
+            } else {
+                for (int b = 0; b < nbox; ++b) {
+                    if (b < boxA.nbox)
+                        issue_box<CG>(mA, sA, fb, boxA, b, m0, k0);
+                    if (b < boxB.nbox)
+                        issue_box<CG>(mB, sB, fb, boxB, b, n0, k0);
+                }
+            }
+            if constexpr (MX) {
+                // the scale atoms of this K range, for the tile's A rows and B columns
+                const uint32_t sSF = sA + C::SF_OFF;
+                const int g0 = k0 / 128;
+#pragma unroll
+                for (int g = 0; g < C::KGROUPS; ++g) {
+                    // a group past K (the tail of the last stage) multiplies only
+                    // the zeros TMA fills in: any valid atom serves, take the last
+                    const int gg = min(g0 + g, sf_groups - 1);
+                    bulk_load(sSF + 512 * g, sfa + (static_cast<size_t>(m0 / 128) * sf_groups + gg) * 512, 512, fb);
+                    bulk_load(sSF + C::SF_A_BYTES + 512 * g, sfb + (static_cast<size_t>(n0 / 128) * sf_groups + gg) * 512,
+                              512, fb);
+                }
             }
             ++issued;
             if (++stage == STAGES) {
@@ -550,12 +615,12 @@ __device__ void role_producer(const KParams &p, const CUtensorMap *tmA, const CU
     }
 }
 
-template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT>
+template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, bool MX>
 __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uint32_t bar_empty,
                          uint32_t bar_acc_full, uint32_t bar_acc_empty, uint32_t bar_inject,
                          uint32_t tmem_base, const Waiter &w)
 {
-    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT>;
+    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, MX>;
     if (p.inject_timeout) {
         // Test hook: wait on a barrier nothing arrives at; the bound runs out.
         w.wait(bar_inject, 0u, kRoleMma | kWaitInjected);
@@ -564,7 +629,8 @@ __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uin
     const Sched sched = make_sched(p);
     unsigned long long *const stats = p.stats;
     const bool multicast = CG == 2 && !(p.flags & kFlagPairForward);
-    const uint32_t idesc = make_idesc(C::UMMA_M, BN, p.a_fmt, p.b_fmt, p.a_mn, p.b_mn);
+    const uint32_t idesc = MX ? make_idesc_mx(C::UMMA_M, BN, p.a_fmt, p.b_fmt, p.a_mn, p.b_mn)
+                              : make_idesc(C::UMMA_M, BN, p.a_fmt, p.b_fmt, p.a_mn, p.b_mn);
     const OperandPacking pa = operand_packing(p.a_mn, p.a_swz, C::BM, BK);
     const OperandPacking pb = operand_packing(p.b_mn, p.b_swz, C::BN_LOCAL, BK);
     const uint64_t a_desc0 = make_smem_desc(smem, pa.lbo, pa.sbo, pa.swz);
@@ -615,15 +681,34 @@ __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uin
             }
             tc_fence_after_sync();
             const uint64_t sdelta = static_cast<uint64_t>((stage * C::STAGE_BYTES) >> 4);
+            if constexpr (MX) {
+                // scale atoms -> this stage's TMEM scale columns; the MMAs below
+                // are issued after the copies by this thread and run after them
+                const uint32_t sSF = smem + stage * C::STAGE_BYTES + C::SF_OFF;
+                const uint32_t tsf = tmem_base + static_cast<uint32_t>(C::SF_COL0 + stage * C::SF_COLS);
 #pragma unroll
-            for (int j = 0; j < C::KSLICES; ++j) {
-                // the first MMA of a unit overwrites the accumulator, the rest add
-                if constexpr (ESIZE == 2)
-                    mma_f16<CG>(d_tmem, a_desc0 + sdelta + a_off[j], b_desc0 + sdelta + b_off[j], idesc,
-                                ((kb - kb_lo) | j) != 0);
-                else
-                    mma_f8<CG>(d_tmem, a_desc0 + sdelta + a_off[j], b_desc0 + sdelta + b_off[j], idesc,
-                               ((kb - kb_lo) | j) != 0);
+                for (int g = 0; g < C::KGROUPS; ++g) {
+                    tmem_cp_32x128b_warpx4(tsf + 8 * g, make_smem_desc(sSF + 512 * g, 128, 128, 0));
+                    tmem_cp_32x128b_warpx4(tsf + 8 * g + 4,
+                                           make_smem_desc(sSF + C::SF_A_BYTES + 512 * g, 128, 128, 0));
+                }
+#pragma unroll
+                for (int j = 0; j < C::KSLICES; ++j) {
+                    const uint32_t ts = tsf + 8 * (j >> 2);
+                    mma_mx<CG>(d_tmem, a_desc0 + sdelta + a_off[j], b_desc0 + sdelta + b_off[j],
+                               idesc_sf_ids(idesc, j & 3, j & 3), ts, ts + 4, ((kb - kb_lo) | j) != 0);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < C::KSLICES; ++j) {
+                    // the first MMA of a unit overwrites the accumulator, the rest add
+                    if constexpr (ESIZE == 2)
+                        mma_f16<CG>(d_tmem, a_desc0 + sdelta + a_off[j], b_desc0 + sdelta + b_off[j], idesc,
+                                    ((kb - kb_lo) | j) != 0);
+                    else
+                        mma_f8<CG>(d_tmem, a_desc0 + sdelta + a_off[j], b_desc0 + sdelta + b_off[j], idesc,
+                                   ((kb - kb_lo) | j) != 0);
+                }
             }
             if (multicast)
                 mma_commit_pair_multicast(bar_empty + 8 * stage);
@@ -803,13 +888,13 @@ __device__ bool sk_gather(const Sched &sched, const Unit &ua, int n32, int buf, 
     return true;
 }
 
-template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int CW>
+template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, bool MX, int CW>
 __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CUtensorMap *tmD,
                               uint32_t epi_base, uint32_t bar_acc_full, uint32_t bar_acc_empty,
                               uint32_t bar_epi, uint32_t tmem_base, uint32_t rank, int warp,
                               int lane, const Waiter &w)
 {
-    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT>;
+    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, MX>;
     const Sched sched = make_sched(p);
     unsigned long long *const stats = p.stats;
     const CUtensorMap *const maps = p.maps;
@@ -822,9 +907,12 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
     const int q = warp & 3;   // TMEM lane quarter 32q..32q+31 = output rows EPI_ROWS*q..
     constexpr int R = C::EPI_ROWS;
     const int ew = warp - 2;  // staging slot
-    const uint32_t buf0 = epi_base + static_cast<uint32_t>(ew * 2 * kEpiBufBytes);
+    const uint32_t buf0 = epi_base + static_cast<uint32_t>(ew * C::EPI_BUFS * kEpiBufBytes);
     const uint32_t ebar0 = bar_epi + static_cast<uint32_t>(16 * ew);
     const bool use_c = ec.beta != 0.0f;
+    // C and D pass through once: let them leave L2 first
+    const bool hints = (p.flags & kFlagCacheHints) != 0;
+    const uint64_t stream_once = hints ? l2_policy_evict_first() : 0;
     const uint32_t acc_empty_target = (CG == 2) ? mapa_shared(bar_acc_empty, 0) : bar_acc_empty;
     const uint32_t peer_acc_full = (CG == 2 && rank == 0) ? mapa_shared(bar_acc_full, 1) : 0u;
     const int cluster_id = blockIdx.x / CG, num_clusters = gridDim.x / CG;
@@ -933,14 +1021,17 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
                 break;
             const uint32_t sbuf = buf0 + static_cast<uint32_t>(sel * kEpiBufBytes);
             const uint32_t sbar = ebar0 + static_cast<uint32_t>(8 * sel);
-            // the store issued from this buffer two chunks ago must have read it
+            // the store issued from this buffer (EPI_BUFS chunks ago) must have read it
             if (lane == 0)
-                bulk_wait_group_read<1>();
+                bulk_wait_group_read<C::EPI_BUFS - 1>();
             __syncwarp();
             if (use_c && lane == 0) {
                 fence_proxy_async_smem();
                 mbar_arrive_expect_tx(sbar, R * 128);
-                tma_load_2d(sbuf, mC, sbar, col0, m0);
+                if (hints)
+                    tma_load_2d_hint(sbuf, mC, sbar, col0, m0, stream_once);
+                else
+                    tma_load_2d(sbuf, mC, sbar, col0, m0);
             }
             __syncwarp();  // tcgen05.ld is .sync.aligned: the warp must be converged
             float v[CW];
@@ -997,10 +1088,14 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                tma_store_2d(mD, sbuf, col0, m0);
+                if (hints)
+                    tma_store_2d_hint(mD, sbuf, col0, m0, stream_once);
+                else
+                    tma_store_2d(mD, sbuf, col0, m0);
                 bulk_commit_group();
             }
-            sel ^= 1;
+            if constexpr (C::EPI_BUFS == 2)
+                sel ^= 1;
         }
         if (has_acc) {
             // all tcgen05.ld of this accumulator have completed (wait::ld above)
@@ -1031,14 +1126,14 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
 
 // ---------------------------------------------------------------- kernel
 
-template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT>
+template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, bool MX>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC,
                         const __grid_constant__ CUtensorMap tmD, const __grid_constant__ KParams p)
 {
-    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT>;
+    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, MX>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -1101,11 +1196,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t stage_base = base;
     if (warp == 0) {
         if (lane == 0)
-            role_producer<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT>(p, &tmA, &tmB, stage_base, bar_full,
+            role_producer<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, MX>(p, &tmA, &tmB, stage_base, bar_full,
                                                               bar_empty, rank, w);
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {
-            role_mma<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT>(p, stage_base, bar_full, bar_empty,
+            role_mma<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, MX>(p, stage_base, bar_full, bar_empty,
                                                   bar_acc_full, bar_acc_empty, bar_inject,
                                                   tmem_base, w);
             // every MMA issued by this thread has completed before TMEM is freed
@@ -1114,11 +1209,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         if (p.out_type == 0)
-            role_epilogue<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, 32>(p, &tmC, &tmD, base + C::EPI_OFF,
+            role_epilogue<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, MX, 32>(p, &tmC, &tmD, base + C::EPI_OFF,
                                                            bar_acc_full, bar_acc_empty, bar_epi,
                                                            tmem_base, rank, warp, lane, w);
         else
-            role_epilogue<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, 64>(p, &tmC, &tmD, base + C::EPI_OFF,
+            role_epilogue<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, MX, 64>(p, &tmC, &tmD, base + C::EPI_OFF,
                                                            bar_acc_full, bar_acc_empty, bar_epi,
                                                            tmem_base, rank, warp, lane, w);
         if (lane == 0)

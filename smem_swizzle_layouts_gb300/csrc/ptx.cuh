@@ -137,6 +137,58 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void *map, 
                  : "memory");
 }
 
+// L2 eviction policies for the cache-hinted copies below.
+__device__ __forceinline__ uint64_t l2_policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// tma_load_2d / tma_load_2d_pair with an L2 eviction policy.
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void *map, uint32_t bar, int c0, int c1,
+                                                 uint64_t policy)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "l"(policy)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const void *map, uint32_t bar, int c0,
+                                                      int c1, uint64_t policy)
+{
+    asm volatile("cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::"
+                 "complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "l"(policy)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_store_2d_hint(const void *map, uint32_t src, int c0, int c1, uint64_t policy)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group.L2::cache_hint"
+                 " [%0, {%2, %3}], [%1], %4;" ::"l"(reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(c0), "r"(c1), "l"(policy)
+                 : "memory");
+}
+
+// Contiguous global -> shared copy of `bytes` (a multiple of 16; both
+// addresses 16-byte aligned), completing on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
 // 2-D tiled store from shared memory; out-of-range parts of the box are dropped.
 __device__ __forceinline__ void tma_store_2d(const void *map, uint32_t src, int c0, int c1)
 {
@@ -277,6 +329,28 @@ __device__ __forceinline__ void mma_commit_pair_multicast(uint32_t bar)
                  "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
                  " [%0], m;\n\t}" ::"r"(bar)
                  : "memory");
+}
+
+// Block-scaled fp8 MMA (kind::mxf8f6f4, one scale per 32 elements of K):
+// sfa / sfb are the TMEM addresses of the A and B scale columns; the scale
+// factor IDs in idesc pick the byte of each 32-bit column.
+template <int CG>
+__device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t sfa, uint32_t sfb, uint32_t accumulate)
+{
+    static_assert(CG == 1, "block-scaled MMAs are issued per CTA here");
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], "
+                 "p;\n\t}" ::"r"(d_tmem),
+                 "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+                 : "memory");
+}
+
+// Copy 32 rows x 16 bytes from shared memory (descriptor `sdesc`) into 4
+// TMEM columns of lanes 0-31, replicated into all four lane quarters.
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc)
+{
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread t gets lane (base lane + t).
