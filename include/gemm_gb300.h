@@ -242,9 +242,12 @@ gemm_status_t gemm_fp8_ex(int64_t M, int64_t N, int64_t K,
  * SFA and SFB are device pointers, 16-byte aligned, of
  * gemm_mx_scale_bytes(M, K) and gemm_mx_scale_bytes(N, K) bytes; entries
  * for rows past M (N) or blocks past K are read but multiply only zeros.
- * Tiles are 128 x 128 with one CTA each, 256 elements of K per pipeline
- * stage (block_k may ask for 128; anything else in opts that asks for other
- * tiles returns GEMM_ERR_UNSUPPORTED); stream_k applies as for gemm_ex.
+ * Tiles are 128 x 128 per CTA: single CTAs (default), or CTA pairs
+ * (cta_group 2) sharing a 256 x 128 tile, where each CTA holds the scales
+ * of its own A rows and a copy of the tile's B scales. 256
+ * elements of K per pipeline stage (single CTAs may ask block_k = 128);
+ * options asking for other tiles return GEMM_ERR_UNSUPPORTED. stream_k
+ * applies as for gemm_ex.
  */
 gemm_status_t gemm_mxfp8(int64_t M, int64_t N, int64_t K,
                          const void *A, gemm_fp8_t a_format, gemm_major_t a_major, int64_t lda,

@@ -218,6 +218,15 @@ gemm_status_t encode_operand(CUtensorMap *m, int dcode, const void *ptr, int mn_
                      tma_swizzle(swz_bits));
 }
 
+// Scale-atom map of a block-scaled operand: the atoms viewed as rows of 256
+// bytes (atom a = rows 2a, 2a + 1), one atom per 256 x 2 box.
+gemm_status_t encode_scales(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K)
+{
+    const uint64_t atoms = static_cast<uint64_t>((rows + 127) / 128) * static_cast<uint64_t>((K + 127) / 128);
+    return encode_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, ptr, 256, 2 * atoms, 256, 256, 2,
+                     CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 // Output (and C) map: boxes of 128 bytes x the rows one epilogue warp owns
 // (32 for 128-row tiles, 16 for 64-row tiles).
 gemm_status_t encode_output(CUtensorMap *m, int d_type, const void *ptr, int64_t M, int64_t N,
@@ -310,12 +319,14 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
     if (bm == 64 && opt.block_k == 0)
         bk = bn == 256 ? 64 : 128;
     if (mx) {
-        // block-scaled tiles are built as one CTA of 128 x 128, 256 (or 128)
-        // elements of K per stage
-        if (opt.cta_group > 1 || (opt.tile_m && opt.tile_m != 128) || (opt.tile_n && opt.tile_n != 128) ||
+        // block-scaled tiles: 128 x 128 per CTA (CTA pairs: 256 x 128),
+        // 256 (single CTAs also 128) elements of K per stage
+        if ((opt.tile_m && opt.tile_m != 128) || (opt.tile_n && opt.tile_n != 128) ||
             (opt.block_k && opt.block_k != 128 && opt.block_k != 256))
             return GEMM_ERR_UNSUPPORTED;
-        cg = 1;
+        // single CTAs by default: 256 x 128 pair tiles measured slower (1773 vs
+        // 1931 TFLOP/s at 8192^3), their MMAs being no wider per SM
+        cg = opt.cta_group ? opt.cta_group : 1;
         bn = 128;
         bk = opt.block_k ? opt.block_k : 256;
         bm = 128;
@@ -323,18 +334,19 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
     if (!find_variant(cg, bn, bk, grouped, esize, bm, mx))
         return GEMM_ERR_UNSUPPORTED;
 
-    auto pick_swz = [&](int requested, int mn_major) -> int {
+    // the widest swizzle whose row fits the stage: along K for K-major
+    // operands, along the tile's MN extent for MN-major ones
+    auto pick_swz = [&](int requested, int mn_major, int rows) -> int {
         if (requested)
             return swz_bits_of(requested);
-        if (!mn_major && bk * esize < 128)
-            return bk * esize >= 64 ? 2 : 1;  // a K row narrower than 128 bytes: SW64 / SW32
-        return 3;
+        const int span = (mn_major ? rows : bk) * esize;
+        return span >= 128 ? 3 : span >= 64 ? 2 : 1;
     };
     plan->cg = cg;
     plan->bn = bn;
     plan->bk = bk;
-    plan->a_swz = pick_swz(opt.swizzle_a, a_mn);
-    plan->b_swz = pick_swz(opt.swizzle_b, b_mn);
+    plan->a_swz = pick_swz(opt.swizzle_a, a_mn, bm);
+    plan->b_swz = pick_swz(opt.swizzle_b, b_mn, bn / cg);
     // a K-major swizzled row may not be wider than the K block; an MN-major
     // atom may not be wider than the tile's MN extent
     auto fits = [&](int bits, int mn_major, int rows) {
@@ -511,9 +523,9 @@ gemm_status_t run_single(const InFmt &f, int64_t M, int64_t N, int64_t K, const 
         return GEMM_ERR_UNSUPPORTED;
     p.num_tiles = static_cast<int>(tiles);
     fill_common(p, pl, f, a_mn, b_mn, d_type, alpha, beta, status);
-    if (f.mx) {
-        p.sfa = static_cast<const uint8_t *>(sfa);
-        p.sfb = static_cast<const uint8_t *>(sfb);
+    if (f.mx && K > 0) {
+        if ((s = encode_scales(&la.sfa, sfa, M, K)) != GEMM_OK || (s = encode_scales(&la.sfb, sfb, N, K)) != GEMM_OK)
+            return s;
         p.sf_groups = static_cast<int>((K + 127) / 128);
     }
     la.grid = grid_for(pl, *v, dev, sms, tiles);

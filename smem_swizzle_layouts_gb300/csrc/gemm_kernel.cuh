@@ -108,10 +108,8 @@ struct KParams {
     float *sk_partials;
     unsigned int *sk_flags;
     unsigned int sk_epoch;
-    // Block-scaled operands: E8M0 scale atoms of A and B (512 bytes per 128
-    // rows x 128 elements of K, row block i and K group g at (i * sf_groups + g) * 512)
-    const uint8_t *sfa;
-    const uint8_t *sfb;
+    // Block-scaled operands: K groups (128 elements) per row block of the
+    // scale tensors; atom (i * sf_groups + g) holds row block i, K group g
     int sf_groups;
 };
 
@@ -166,7 +164,7 @@ struct Cfg {
     // 512-byte atom covers 128 rows x 4 scale blocks (128 elements of K)
     static constexpr int KGROUPS = MX ? BK / 128 : 0;
     static constexpr int SF_A_BYTES = 512 * KGROUPS * (BM / 128);
-    static constexpr int SF_B_BYTES = 512 * KGROUPS * (BN_LOCAL / 128);
+    static constexpr int SF_B_BYTES = 512 * KGROUPS * (BN / 128);  // every column of the tile, in each CTA
     static constexpr int SF_OFF = A_BYTES + B_BYTES;  // within a stage
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SF_A_BYTES + SF_B_BYTES;
     static constexpr int TX_BYTES = STAGE_BYTES * CG;  // bytes landing on one full barrier
@@ -196,9 +194,9 @@ struct Cfg {
                   "TMEM allocation: power of two, 32..512 columns");
     static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
     static_assert(CG == 1 || BN % 32 == 0, "pair tiles split N in halves of whole atoms");
-    static_assert(!MX || (CG == 1 && BMT == 128 && BN == 128 && ESIZE == 1 && BK % 128 == 0 &&
+    static_assert(!MX || (BMT == 128 && BN == 128 && ESIZE == 1 && BK % 128 == 0 &&
                           SF_COL0 + STAGES * SF_COLS <= 512),
-                  "block-scaled tiles: one CTA, 128 x 128, fp8, whole 128-element K groups");
+                  "block-scaled tiles: 128 x 128 per CTA (256 x 128 per pair), fp8, whole 128-element K groups");
 };
 
 // ---------------------------------------------------------------- waits
@@ -491,6 +489,7 @@ __device__ __forceinline__ int ceil_div_i(int a, int b) { return (a + b - 1) / b
 
 template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, bool MX>
 __device__ void role_producer(const KParams &p, const CUtensorMap *tmA, const CUtensorMap *tmB,
+                              const CUtensorMap *tmSFA, const CUtensorMap *tmSFB,
                               uint32_t smem, uint32_t bar_full, uint32_t bar_empty,
                               uint32_t rank, const Waiter &w)
 {
@@ -503,8 +502,6 @@ __device__ void role_producer(const KParams &p, const CUtensorMap *tmA, const CU
     const OperandBoxes boxB = operand_boxes(p.b_mn, p.b_swz, C::BN_LOCAL, BK, ESIZE);
     const int nbox = boxA.nbox > boxB.nbox ? boxA.nbox : boxB.nbox;
     const bool forward = CG == 2 && rank == 0 && (flags & kFlagPairForward);
-    const uint8_t *const sfa = p.sfa;
-    const uint8_t *const sfb = p.sfb;
     const int sf_groups = p.sf_groups;
     // operand tiles are re-read by other tiles of the wave: keep them in L2
     const bool hints = (flags & kFlagCacheHints) != 0;
@@ -577,17 +574,33 @@ __device__ void role_producer(const KParams &p, const CUtensorMap *tmA, const CU
                 }
             }
             if constexpr (MX) {
-                // the scale atoms of this K range, for the tile's A rows and B columns
+                // the scale atoms of this K range: this CTA's A rows, and every B
+                // column of the tile (the pair's MMA reads all of them from each
+                // CTA). The scale tensors are viewed as rows of 256 bytes, one
+                // atom being rows 2a and 2a + 1, so that pair CTAs signal the
+                // even CTA's barrier like the operand boxes do.
                 const uint32_t sSF = sA + C::SF_OFF;
                 const int g0 = k0 / 128;
+                const int ra = m0 / 128, rb = ti.n_blk * BN / 128;
 #pragma unroll
                 for (int g = 0; g < C::KGROUPS; ++g) {
                     // a group past K (the tail of the last stage) multiplies only
                     // the zeros TMA fills in: any valid atom serves, take the last
                     const int gg = min(g0 + g, sf_groups - 1);
-                    bulk_load(sSF + 512 * g, sfa + (static_cast<size_t>(m0 / 128) * sf_groups + gg) * 512, 512, fb);
-                    bulk_load(sSF + C::SF_A_BYTES + 512 * g, sfb + (static_cast<size_t>(n0 / 128) * sf_groups + gg) * 512,
-                              512, fb);
+                    const int atom_a = ra * sf_groups + gg;
+                    if constexpr (CG == 1)
+                        tma_load_2d(sSF + 512 * g, tmSFA, fb, 0, 2 * atom_a);
+                    else
+                        tma_load_2d_pair(sSF + 512 * g, tmSFA, fb, 0, 2 * atom_a);
+#pragma unroll
+                    for (int h = 0; h < BN / 128; ++h) {
+                        const int atom_b = (rb + h) * sf_groups + gg;
+                        const uint32_t dst = sSF + C::SF_A_BYTES + 512 * (g * (BN / 128) + h);
+                        if constexpr (CG == 1)
+                            tma_load_2d(dst, tmSFB, fb, 0, 2 * atom_b);
+                        else
+                            tma_load_2d_pair(dst, tmSFB, fb, 0, 2 * atom_b);
+                    }
                 }
             }
             ++issued;
@@ -688,9 +701,9 @@ __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uin
                 const uint32_t tsf = tmem_base + static_cast<uint32_t>(C::SF_COL0 + stage * C::SF_COLS);
 #pragma unroll
                 for (int g = 0; g < C::KGROUPS; ++g) {
-                    tmem_cp_32x128b_warpx4(tsf + 8 * g, make_smem_desc(sSF + 512 * g, 128, 128, 0));
-                    tmem_cp_32x128b_warpx4(tsf + 8 * g + 4,
-                                           make_smem_desc(sSF + C::SF_A_BYTES + 512 * g, 128, 128, 0));
+                    tmem_cp_32x128b_warpx4<CG>(tsf + 8 * g, make_smem_desc(sSF + 512 * g, 128, 128, 0));
+                    tmem_cp_32x128b_warpx4<CG>(tsf + 8 * g + 4,
+                                               make_smem_desc(sSF + C::SF_A_BYTES + 512 * g, 128, 128, 0));
                 }
 #pragma unroll
                 for (int j = 0; j < C::KSLICES; ++j) {
@@ -1131,7 +1144,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC,
-                        const __grid_constant__ CUtensorMap tmD, const __grid_constant__ KParams p)
+                        const __grid_constant__ CUtensorMap tmD,
+                        const __grid_constant__ CUtensorMap tmSFA,
+                        const __grid_constant__ CUtensorMap tmSFB, const __grid_constant__ KParams p)
 {
     using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, MX>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -1175,6 +1190,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
         prefetch_tensormap(&tmD);
+        if constexpr (MX) {
+            prefetch_tensormap(&tmSFA);
+            prefetch_tensormap(&tmSFB);
+        }
     }
     if (warp == 1) {
         tmem_alloc<CG>(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -1196,7 +1215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t stage_base = base;
     if (warp == 0) {
         if (lane == 0)
-            role_producer<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, MX>(p, &tmA, &tmB, stage_base, bar_full,
+            role_producer<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, MX>(p, &tmA, &tmB, &tmSFA, &tmSFB, stage_base, bar_full,
                                                               bar_empty, rank, w);
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {

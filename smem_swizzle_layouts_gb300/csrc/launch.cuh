@@ -13,6 +13,7 @@ namespace g300 {
 
 struct LaunchArgs {
     CUtensorMap a, b, c, d;
+    CUtensorMap sfa, sfb;  // block-scaled operands' scale atoms (else unused)
     KParams p;
     int grid;  // CTAs (a multiple of the cluster size)
     cudaStream_t stream;
@@ -65,7 +66,7 @@ cudaError_t launch_gemm(const LaunchArgs &a)
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, kern, a.a, a.b, a.c, a.d, a.p);
+    return cudaLaunchKernelEx(&cfg, kern, a.a, a.b, a.c, a.d, a.sfa, a.sfb, a.p);
 }
 
 // Largest number of CTAs of this variant that can be resident at once.

@@ -179,16 +179,6 @@ __device__ __forceinline__ void tma_store_2d_hint(const void *map, uint32_t src,
                  : "memory");
 }
 
-// Contiguous global -> shared copy of `bytes` (a multiple of 16; both
-// addresses 16-byte aligned), completing on `bar`.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     dst),
-                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-                 : "memory");
-}
-
 // 2-D tiled store from shared memory; out-of-range parts of the box are dropped.
 __device__ __forceinline__ void tma_store_2d(const void *map, uint32_t src, int c0, int c1)
 {
@@ -334,23 +324,36 @@ __device__ __forceinline__ void mma_commit_pair_multicast(uint32_t bar)
 // Block-scaled fp8 MMA (kind::mxf8f6f4, one scale per 32 elements of K):
 // sfa / sfb are the TMEM addresses of the A and B scale columns; the scale
 // factor IDs in idesc pick the byte of each 32-bit column.
+// CTA pairs: the scales of each CTA's accumulator rows come from its own TMEM.
 template <int CG>
 __device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                        uint32_t sfa, uint32_t sfb, uint32_t accumulate)
 {
-    static_assert(CG == 1, "block-scaled MMAs are issued per CTA here");
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], "
-                 "p;\n\t}" ::"r"(d_tmem),
-                 "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
-                 : "memory");
+    if constexpr (CG == 1)
+        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+                     "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], "
+                     "[%5], p;\n\t}" ::"r"(d_tmem),
+                     "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+                     : "memory");
+    else
+        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+                     "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], "
+                     "[%5], p;\n\t}" ::"r"(d_tmem),
+                     "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+                     : "memory");
 }
 
 // Copy 32 rows x 16 bytes from shared memory (descriptor `sdesc`) into 4
-// TMEM columns of lanes 0-31, replicated into all four lane quarters.
+// TMEM columns of lanes 0-31, replicated into all four lane quarters. For a
+// CTA pair (issued by the even CTA) each CTA copies from its own shared
+// memory at the descriptor's offset into its own TMEM.
+template <int CG>
 __device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc)
 {
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+    if constexpr (CG == 1)
+        asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+    else
+        asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread t gets lane (base lane + t).

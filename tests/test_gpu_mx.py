@@ -128,6 +128,25 @@ def test_mx_block_k_128_exact(g, M, N, K):
     run_mx(g, M, N, K, exact=True, seed=M + K + 1, options=dict(block_k=128))
 
 
+@pytest.mark.parametrize("M,N,K", [(256, 128, 256), (300, 200, 600), (700, 390, 1000), (2048, 2048, 512)])
+def test_mx_cta_pairs_exact(g, M, N, K):
+    # 256 x 128 pair tiles: each CTA's TMEM holds its own A rows' scales and a
+    # copy of the tile's B scales (ragged M leaves the odd CTA past the last atom row)
+    run_mx(g, M, N, K, exact=True, seed=3 * M + K, options=dict(cta_group=2))
+
+
+@pytest.mark.parametrize("a_major,b_major", [("MN", "MN"), ("K", "MN")])
+def test_mx_cta_pairs_majors_and_e5m2(g, a_major, b_major):
+    run_mx(g, 512, 384, 768, a_major=a_major, b_major=b_major, a_fmt="e5m2", b_fmt="e4m3", exact=True, seed=29,
+           options=dict(cta_group=2))
+
+
+def test_mx_cta_pairs_stream_k_and_tolerance(g):
+    ws = torch.zeros(g.gemm_streamk_workspace_size(), dtype=torch.uint8, device=DEV)
+    run_mx(g, 700, 300, 1500, exact=True, seed=31, options=dict(cta_group=2, workspace=ws, stream_k=2, max_ctas=6))
+    run_mx(g, 1024, 640, 1024, dist="normal", out="bf16", alpha=1.5, beta=0.5, seed=37, options=dict(cta_group=2))
+
+
 def test_mx_stream_k_exact(g):
     ws = torch.zeros(g.gemm_streamk_workspace_size(), dtype=torch.uint8, device=DEV)
     run_mx(g, 700, 300, 1500, exact=True, seed=19, options=dict(workspace=ws, stream_k=2, max_ctas=5))
@@ -161,6 +180,6 @@ def test_mx_argument_errors(g):
         call(S, S, tile_n=256)
     assert ei.value.status == g.ERR_UNSUPPORTED
     with pytest.raises(g.GemmError) as ei:
-        call(S, S, cta_group=2)
+        call(S, S, cta_group=2, block_k=128)
     assert ei.value.status == g.ERR_UNSUPPORTED
     assert g.gemm_mx_scale_bytes(300, 260) == 3 * 3 * 512 and g.gemm_mx_scale_bytes(0, 5) == 0
