@@ -67,6 +67,14 @@ def _load():
             lib.oracle_gemm_mx.restype = ctypes.c_int
             lib.oracle_gemm_mx_entries.argtypes = mx + [i64, vp, vp, dp, dp, ctypes.c_int]
             lib.oracle_gemm_mx_entries.restype = ctypes.c_int
+            lib.oracle_decode_e2m1.argtypes = [ctypes.c_uint8]
+            lib.oracle_decode_e2m1.restype = ctypes.c_double
+            lib.oracle_decode_ue4m3.argtypes = [ctypes.c_uint8]
+            lib.oracle_decode_ue4m3.restype = ctypes.c_double
+            lib.oracle_gemm_fp4.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, ctypes.c_int,
+                                            ctypes.c_int, vp, ctypes.c_int, i64, ctypes.c_double, ctypes.c_double,
+                                            dp, dp, ctypes.c_int]
+            lib.oracle_gemm_fp4.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -178,6 +186,45 @@ def gemm_mx_entries(M, N, K, A, B, SA, SB, rows, cols, *, in_fmt="e4m3", b_fmt=N
     if rc:
         raise ValueError("oracle_gemm_mx_entries: bad arguments")
     return D, S
+
+
+def gemm_fp4(M, N, K, A, B, SA, SB, *, block, scale="ue4m3", lda=None, ldb=None, C=None, c_fmt="f32", ldc=None,
+             alpha=1.0, beta=0.0, threads=0):
+    """Block-scaled fp4 fp64 product. ``A`` (M x lda/2 bytes) and ``B`` (N x ldb/2 bytes) hold packed E2M1,
+    K-major; ``SA`` is M x ceil(K/block) and ``SB`` N x ceil(K/block) scale codes (UE4M3 or E8M0).
+    Returns (D, S) as ``gemm`` does."""
+    lib = _load()
+    A = np.ascontiguousarray(A, dtype=np.uint8)
+    B = np.ascontiguousarray(B, dtype=np.uint8)
+    SA = np.ascontiguousarray(SA, dtype=np.uint8)
+    SB = np.ascontiguousarray(SB, dtype=np.uint8)
+    lda = lda if lda is not None else K
+    ldb = ldb if ldb is not None else K
+    if C is not None:
+        C = np.ascontiguousarray(C)
+        ldc = ldc if ldc is not None else N
+    D = np.empty((M, N), dtype=np.float64)
+    S = np.empty((M, N), dtype=np.float64)
+    rc = lib.oracle_gemm_fp4(M, N, K, _ptr(A), lda, _ptr(SA), SA.shape[1], _ptr(B), ldb, _ptr(SB), SB.shape[1],
+                             int(block), 1 if scale == "e8m0" else 0, _ptr(C), FMT[c_fmt], ldc or 0, float(alpha),
+                             float(beta), _ptr(D), _ptr(S), int(threads))
+    if rc:
+        raise ValueError("oracle_gemm_fp4 rejected its arguments")
+    return D, S
+
+
+def decode_e2m1(codes) -> np.ndarray:
+    """Values of 4-bit E2M1 codes."""
+    lib = _load()
+    c = np.asarray(codes).reshape(-1)
+    return np.array([lib.oracle_decode_e2m1(int(x)) for x in c], dtype=np.float64).reshape(np.shape(codes))
+
+
+def decode_ue4m3(codes) -> np.ndarray:
+    """Values of UE4M3 scale codes (0x7F: NaN)."""
+    lib = _load()
+    c = np.asarray(codes).reshape(-1)
+    return np.array([lib.oracle_decode_ue4m3(int(x)) for x in c], dtype=np.float64).reshape(np.shape(codes))
 
 
 def decode_e8m0(codes) -> np.ndarray:

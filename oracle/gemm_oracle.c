@@ -342,6 +342,83 @@ int oracle_gemm_mx_entries(int64_t M, int64_t N, int64_t K,
 }
 
 /*
+ * Block-scaled fp4 (NVFP4 / MXFP4, the fp4 members of the same block-scaled
+ * MMA family): E2M1 elements, packed two to a byte (element 2i of a row in
+ * the low nibble of byte i, 2i+1 in the high nibble), one scale per `block`
+ * consecutive elements of K (16 with UE4M3 scales, 32 with E8M0):
+ *
+ *   D[i][j] = alpha * sum_k (sa(i, k/block) * A(i,k)) * (sb(j, k/block) * B(k,j)) + beta * C[i][j]
+ *
+ * A is M x K and B is stored N x K, both K-major, lda / ldb in elements
+ * (even). E2M1 (OCP Microscaling): sign, 2 exponent bits (bias 1), 1
+ * mantissa bit: 0, 0.5, 1, 1.5, 2, 3, 4, 6. UE4M3: the E4M3 encoding without
+ * its sign bit, 2^(e-7) * (1 + m/8), e = 0 subnormal 2^-6 * m/8, 0x7F NaN.
+ */
+double oracle_decode_e2m1(uint8_t nibble)
+{
+    const int s = (nibble >> 3) & 1, e = (nibble >> 1) & 3, m = nibble & 1;
+    const double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return s ? -v : v;
+}
+
+double oracle_decode_ue4m3(uint8_t code)
+{
+    const int e = (code >> 3) & 15, m = code & 7;
+    if (code == 0x7F)
+        return NAN;
+    return e == 0 ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+}
+
+static double fp4_at(const uint8_t *X, int64_t ld, int64_t row, int64_t k)
+{
+    const uint8_t byte = X[(row * ld + k) / 2];
+    return oracle_decode_e2m1((k & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15));
+}
+
+static double fp4_scale(const uint8_t *s, int64_t lds, int64_t row, int64_t blk, int scale_e8m0)
+{
+    const uint8_t c = s[row * lds + blk];
+    return scale_e8m0 ? oracle_decode_e8m0(c) : oracle_decode_ue4m3(c);
+}
+
+int oracle_gemm_fp4(int64_t M, int64_t N, int64_t K,
+                    const uint8_t *A, int64_t lda, const uint8_t *sa, int64_t ldsa,
+                    const uint8_t *B, int64_t ldb, const uint8_t *sb, int64_t ldsb,
+                    int block, int scale_e8m0,
+                    const void *C, int c_fmt, int64_t ldc,
+                    double alpha, double beta,
+                    double *D, double *S, int nthreads)
+{
+    if (M < 0 || N < 0 || K < 0 || (block != 16 && block != 32) || (lda & 1) || (ldb & 1) ||
+        ldsa < (K + block - 1) / block || ldsb < (K + block - 1) / block)
+        return 1;
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    int64_t i;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (i = 0; i < M; ++i) {
+        for (int64_t j = 0; j < N; ++j) {
+            double acc = 0.0, sab = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double p = (fp4_scale(sa, ldsa, i, k / block, scale_e8m0) * fp4_at(A, lda, i, k)) *
+                           (fp4_scale(sb, ldsb, j, k / block, scale_e8m0) * fp4_at(B, ldb, j, k));
+                acc += p;
+                sab += fabs(p);
+            }
+            double c = (beta != 0.0 && C) ? load(C, c_fmt, i * ldc + j) : 0.0;
+            D[i * N + j] = alpha * acc + beta * c;
+            if (S)
+                S[i * N + j] = fabs(alpha) * sab + fabs(beta * c);
+        }
+    }
+    return 0;
+}
+
+/*
  * Round-to-nearest-even of x to a binary format with p significand bits
  * (hidden bit included), minimum normal exponent emin and maximum exponent
  * emax; subnormals are kept, overflow goes to infinity.

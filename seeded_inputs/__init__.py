@@ -173,12 +173,26 @@ def scale_codes(seed: int, rows: int, nblocks: int, lo: int = 124, hi: int = 130
     return ((z >> np.uint64(32)) % span + np.uint64(lo)).astype(np.uint8).reshape(rows, nblocks)
 
 
-def mx_scale_atoms(codes: np.ndarray, rows: int, K: int) -> np.ndarray:
-    """Arrange row-major scale codes (``rows x ceil(K/32)``) in the 512-byte atoms of the
-    block-scaled GEMM's ABI: atom (r // 128) * ceil(K/128) + k // 128, byte
-    16 * (r % 32) + 4 * ((r % 128) // 32) + (k // 32) % 4. Unused entries are 127."""
-    nb = (K + 31) // 32
-    groups = (K + 127) // 128
+def fp4_codes(seed: int, rows: int, cols: int) -> np.ndarray:
+    """Seeded 4-bit E2M1 codes, ``rows x cols`` uint8 in [0, 15] (all sixteen codes)."""
+    z = splitmix64(seed, 0, rows * cols)
+    return ((z >> np.uint64(32)) % np.uint64(16)).astype(np.uint8).reshape(rows, cols)
+
+
+def pack_fp4(codes: np.ndarray) -> np.ndarray:
+    """Pack 4-bit codes two to a byte along each row: element 2i in the low nibble of byte i."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    if codes.shape[1] % 2:
+        codes = np.concatenate([codes, np.zeros((codes.shape[0], 1), np.uint8)], axis=1)
+    return (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+
+
+def mx_scale_atoms(codes: np.ndarray, rows: int, K: int, block: int = 32) -> np.ndarray:
+    """Arrange row-major scale codes (``rows x ceil(K/block)``) in the 512-byte atoms of the
+    block-scaled GEMM's ABI: atom (r // 128) * ceil(K/(4 block)) + k // (4 block), byte
+    16 * (r % 32) + 4 * ((r % 128) // 32) + (k // block) % 4. Unused entries are 127."""
+    nb = (K + block - 1) // block
+    groups = (nb + 3) // 4
     blocks = (rows + 127) // 128
     out = np.full(blocks * groups * 512, 127, dtype=np.uint8)
     r = np.arange(rows)[:, None]

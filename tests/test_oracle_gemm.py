@@ -329,3 +329,69 @@ def test_mx_scale_atom_layout_by_hand():
     assert atoms[(1 * 3 + 2) * 512 + 32] == 202
     assert atoms[(2 * 3 + 0) * 512 + 180] == 203
     assert (atoms == 201).sum() == 1 and (atoms == 202).sum() == 1 and (atoms == 203).sum() == 1
+
+
+# ---------------------------------------------------------------------------
+# Block-scaled fp4 (NVFP4: UE4M3 per 16; MXFP4: E8M0 per 32), packed E2M1.
+# ---------------------------------------------------------------------------
+
+E2M1_TABLE = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]  # the eight E2M1 magnitudes (OCP Microscaling)
+
+
+def test_e2m1_decode_matches_the_format_table():
+    d = G.decode_e2m1(np.arange(16, dtype=np.uint8))
+    assert list(d[:8]) == E2M1_TABLE
+    assert list(-d[8:]) == E2M1_TABLE and all(np.signbit(d[8:]))
+
+
+def test_ue4m3_decode_matches_torch_e4m3_for_every_unsigned_code():
+    codes = np.arange(0x7F, dtype=np.uint8)
+    want = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(G.decode_ue4m3(codes), want)
+    assert np.isnan(G.decode_ue4m3(np.array([0x7F], np.uint8))[0])
+
+
+def test_fp4_nibble_order_hand_case():
+    # one output, K = 2: A = [1, 2], B = [3, 0.5]: 1*3 + 2*0.5 = 4 (the swapped order would give 6.5)
+    A = np.array([[0x2 | (0x4 << 4)]], np.uint8)      # codes 2 (1.0) low, 4 (2.0) high
+    B = np.array([[0x5 | (0x1 << 4)]], np.uint8)      # codes 5 (3.0) low, 1 (0.5) high
+    one16 = np.array([[0x38]], np.uint8)              # UE4M3 1.0
+    D, _ = G.gemm_fp4(1, 1, 2, A, B, one16, one16, block=16, scale="ue4m3")
+    assert D[0, 0] == 4.0
+    one32 = np.array([[127]], np.uint8)
+    D, _ = G.gemm_fp4(1, 1, 2, A, B, one32, one32, block=32, scale="e8m0")
+    assert D[0, 0] == 4.0
+
+
+@pytest.mark.parametrize("block,scale", [(16, "ue4m3"), (32, "e8m0")])
+def test_fp4_products_with_scales_are_exact(block, scale):
+    M, N, K = 12, 20, 192
+    ca, cb = si.fp4_codes(101, M, K), si.fp4_codes(102, N, K)
+    nb = K // block
+    rng = np.random.default_rng(103)
+    if scale == "ue4m3":
+        pool = np.array([(e << 3) | m for e in (5, 6, 7, 8, 9) for m in (0, 4)], np.uint8)
+        sa, sb = rng.choice(pool, (M, nb)), rng.choice(pool, (N, nb))
+        dec = lambda c: np.array([[2.0 ** (int(x) // 8 - 7) * (1 + (int(x) % 8) / 8) for x in r] for r in c])
+    else:
+        sa, sb = si.scale_codes(104, M, nb), si.scale_codes(105, N, nb)
+        dec = lambda c: np.exp2(c.astype(np.float64) - 127.0)
+    D, _ = G.gemm_fp4(M, N, K, si.pack_fp4(ca), si.pack_fp4(cb), sa, sb, block=block, scale=scale)
+    table = np.array(E2M1_TABLE + [-v for v in E2M1_TABLE])
+    a, b = table[ca], table[cb]
+    ref = np.zeros((M, N))
+    for blk in range(nb):
+        s = slice(block * blk, block * blk + block)
+        ref += dec(sa)[:, blk:blk + 1] * (a[:, s] @ b[:, s].T) * dec(sb)[:, blk][None, :]
+    assert np.array_equal(D, ref)
+
+
+def test_fp4_block_size_matters():
+    # the same codes read with 16- and 32-element blocks differ once the scales differ per block
+    M, N, K = 4, 4, 64
+    ca, cb = si.fp4_codes(111, M, K), si.fp4_codes(112, N, K)
+    s16 = np.tile(np.array([[0x38, 0x40, 0x38, 0x40]], np.uint8), (M, 1))   # 1, 2, 1, 2 per 16
+    D16, _ = G.gemm_fp4(M, N, K, si.pack_fp4(ca), si.pack_fp4(cb), s16, np.tile(s16[:1], (N, 1)), block=16)
+    D16u, _ = G.gemm_fp4(M, N, K, si.pack_fp4(ca), si.pack_fp4(cb), np.full((M, 4), 0x38, np.uint8),
+                         np.full((N, 4), 0x38, np.uint8), block=16)
+    assert not np.array_equal(D16, D16u)
