@@ -71,6 +71,16 @@ WORKLOADS = {
         scale=1.0, seed=50, options=None, in_fmt="e4m3", b_fmt="e4m3", mx=True, peak_ratio=2.0,
         desc="8192^3 block-scaled fp8 (MXFP8: E4M3 with one E8M0 scale per 32 elements of K, codes U{124..130}; "
              "tcgen05 kind::mxf8f6f4), A and B K-major, U[-1,1], fp32 accumulate, bf16 out, 128x128 tiles"),
+    "square8192_nvfp4": dict(
+        M=8192, N=8192, K=8192, a_major="K", b_major="K", out="bf16", alpha=1.0, beta=0.0, dist="fp4",
+        scale=1.0, seed=60, options=None, fp4="nvfp4", peak_ratio=6.0,
+        desc="8192^3 block-scaled fp4 (NVFP4: packed E2M1, all sixteen codes, one UE4M3 scale per 16 elements "
+             "of K from {1/4..6}; tcgen05 kind::mxf4nvf4), A and B K-major, fp32 accumulate, bf16 out, 128x128 tiles"),
+    "square8192_mxfp4": dict(
+        M=8192, N=8192, K=8192, a_major="K", b_major="K", out="bf16", alpha=1.0, beta=0.0, dist="fp4",
+        scale=1.0, seed=70, options=None, fp4="mxfp4", peak_ratio=6.0,
+        desc="8192^3 block-scaled fp4 (MXFP4: packed E2M1, all sixteen codes, one E8M0 scale per 32 elements "
+             "of K, codes U{124..130}; tcgen05 kind::mxf4), A and B K-major, fp32 accumulate, bf16 out, 128x128 tiles"),
     "single_tile_128x128x32_f16": dict(
         M=128, N=128, K=32, a_major="K", b_major="MN", out="f32", alpha=1.0, beta=0.0, dist="uniform",
         scale=1.0, seed=0, options=None, in_fmt="f16",
@@ -195,6 +205,25 @@ def job_throughput(units_per_rank: float, world_size: int, max_ms: float) -> flo
     return units_per_rank * world_size / (max_ms / 1e3)
 
 
+FP4_KINDS = {"nvfp4": (0, 16, "ue4m3"), "mxfp4": (1, 32, "e8m0")}
+UE4M3_POOL = np.array([(e << 3) | m for e in (5, 6, 7, 8, 9) for m in (0, 4)], np.uint8)  # 1/4 .. 6
+
+
+def _fp4_inputs(wl):
+    """Packed E2M1 operands (M x K/2, N x K/2 bytes) and row-major scale codes of an fp4 workload."""
+    code, block, scale = FP4_KINDS[wl["fp4"]]
+    M, N, K = wl["M"], wl["N"], wl["K"]
+    A = si.pack_fp4(si.fp4_codes(wl["seed"], M, K))
+    B = si.pack_fp4(si.fp4_codes(wl["seed"] + 1, N, K))
+    nb = (K + block - 1) // block
+    if scale == "ue4m3":
+        z = si.scale_codes(wl["seed"] + 2, M + N, nb, 0, len(UE4M3_POOL) - 1)
+        sa, sb = UE4M3_POOL[z[:M]], UE4M3_POOL[z[M:]]
+    else:
+        sa, sb = si.scale_codes(wl["seed"] + 2, M, nb), si.scale_codes(wl["seed"] + 3, N, nb)
+    return A, B, sa, sb
+
+
 def _mx_codes(wl):
     """Seeded E8M0 scale codes of a block-scaled workload (row-major, one per 32 elements of K)."""
     nb = (wl["K"] + 31) // 32
@@ -228,7 +257,19 @@ class GemmJob:
         tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[wl["out"]]
         self.M, self.N, self.K = wl["M"], wl["N"], wl["K"]
         self.in_type = 1 if wl.get("in_fmt", "bf16") == "bf16" else 0
-        self.bits, host, devt = _torch_inputs(wl, dev, pinned=True)
+        fp4_scales = None
+        if wl.get("fp4"):
+            code, block, scale = FP4_KINDS[wl["fp4"]]
+            A4, B4, sa, sb = _fp4_inputs(wl)
+            fill = 0x38 if scale == "ue4m3" else 127
+            host = [torch.from_numpy(A4.reshape(-1)).pin_memory(), torch.from_numpy(B4.reshape(-1)).pin_memory(), None]
+            devt = [h.to(dev) if h is not None else None for h in host]
+            host_s = [torch.from_numpy(si.mx_scale_atoms(c, n, self.K, block, fill)).pin_memory()
+                      for c, n in ((sa, self.M), (sb, self.N))]
+            fp4_scales = [h.to(dev) for h in host_s]
+            self.bits = (A4, B4, None, sa, sb)
+        else:
+            self.bits, host, devt = _torch_inputs(wl, dev, pinned=True)
         self.A, self.B, self.C = devt
         self.D = torch.empty(self.M, self.N, dtype=tdt, device=dev)
         self.hD = torch.empty(self.M, self.N, dtype=tdt).pin_memory()
@@ -248,6 +289,9 @@ class GemmJob:
             codes = {"e4m3": g.FP8_E4M3, "e5m2": g.FP8_E5M2}
             fp8 = (codes[wl["in_fmt"]], codes[wl.get("b_fmt", wl["in_fmt"])])
         scales = None
+        if fp4_scales is not None:
+            self.pairs += list(zip(host_s, fp4_scales))
+            scales = fp4_scales
         if wl.get("mx"):
             sa, sb = _mx_codes(wl)
             self.bits = self.bits + (sa, sb)
@@ -255,10 +299,12 @@ class GemmJob:
                       for c, n in ((sa, self.M), (sb, self.N))]
             scales = [h.to(dev) for h in host_s]
             self.pairs += list(zip(host_s, scales))
-        self.call = g.GemmCall(self.in_type, self.M, self.N, self.K, self.A, self.am, self.A.stride(0), self.B,
-                               self.bm, self.B.stride(0), self.C, self.N if self.C is not None else 0, self.D,
+        lda = self.K if wl.get("fp4") else self.A.stride(0)
+        ldb = self.K if wl.get("fp4") else self.B.stride(0)
+        self.call = g.GemmCall(self.in_type, self.M, self.N, self.K, self.A, self.am, lda, self.B,
+                               self.bm, ldb, self.C, self.N if self.C is not None else 0, self.D,
                                self.N, self.dt, wl["alpha"], wl["beta"], options=options, stream=stream, fp8=fp8,
-                               scales=scales)
+                               scales=scales, fp4=FP4_KINDS[wl["fp4"]][0] if wl.get("fp4") else None)
 
     def step(self):
         self.call()
@@ -408,7 +454,11 @@ def _oracle_rows_rate(wl, bits, target_s, max_rows=None, fixed_rows=None):
         kw = dict(in_fmt=in_fmt, b_fmt=wl.get("b_fmt", in_fmt), a_major=wl["a_major"], b_major=wl["b_major"],
                   lda=lda, C=Cr, c_fmt=wl["out"], ldc=N, alpha=wl["alpha"], beta=wl["beta"], threads=threads)
         t0 = time.perf_counter()
-        if scales is not None:
+        if wl.get("fp4"):
+            _, block, scale = FP4_KINDS[wl["fp4"]]
+            og.gemm_fp4(R, N, K, A[:R], B, scales[0][:R], scales[1], block=block, scale=scale, C=None,
+                        alpha=wl["alpha"], beta=wl["beta"], threads=threads)
+        elif scales is not None:
             og.gemm_mx(R, N, K, Ar, B, scales[0][:R], scales[1], **kw)
         else:
             og.gemm(R, N, K, Ar, B, **kw)
@@ -434,8 +484,9 @@ def _algorithmic_bytes(wl, job):
         N, K = wl["N"], wl["K"]
         return float(sum((M * K + K * N) * 2 + M * N * ob for M in job.Ms))
     M, N, K = wl["M"], wl["N"], wl["K"]
-    eb = 1 if wl.get("in_fmt") in ("e4m3", "e5m2") else 2
-    sf = (M + N) * ((K + 31) // 32) if wl.get("mx") else 0  # one scale byte per 32 elements of K
+    eb = 1 if wl.get("in_fmt") in ("e4m3", "e5m2") else 0.5 if wl.get("fp4") else 2
+    block = FP4_KINDS[wl["fp4"]][1] if wl.get("fp4") else 32
+    sf = (M + N) * ((K + block - 1) // block) if (wl.get("mx") or wl.get("fp4")) else 0  # one scale byte per block
     return float((M * K + K * N) * eb + sf + M * N * ob * (2 if wl["beta"] != 0.0 else 1))
 
 
@@ -449,7 +500,7 @@ def _reference_line(args, wl, config, metric):
         B = si.matrix_bits(wl["seed"] + 1, wl["K"], wl["N"], wl["dist"], "bf16", transpose=True)
         bits, rows_of = (A, B, None), f"problem 0 (M={M0})"
     else:
-        sub, bits, rows_of = wl, _torch_inputs_host_only(wl), f"{wl['M']} rows"
+        sub, bits, rows_of = wl, _host_bits(wl), f"{wl['M']} rows"
     # calibrate a row sample so that warm-up + timed steps take about two minutes
     per_step = max(0.5, 120.0 / (args.warmup + args.steps))
     _, R, _, threads = _oracle_rows_rate(sub, bits, target_s=per_step)
@@ -495,6 +546,9 @@ def main():
         metric = "GEMM TFLOP/s (fp8 in, fp32 accum) and % of GB300 dense FP8 tensor peak"
     if wl.get("mx"):
         metric = "GEMM TFLOP/s (MXFP8 block-scaled fp8 in, fp32 accum) and % of GB300 dense FP8 tensor peak"
+    if wl.get("fp4"):
+        metric = (f"GEMM TFLOP/s ({wl['fp4'].upper()} block-scaled fp4 in, fp32 accum) and % of GB300 dense "
+                  "FP4 tensor peak")
 
     if args.impl == "reference":
         if rank == 0:
@@ -522,16 +576,17 @@ def main():
                 "algorithmic_bytes": bytes_alg}
     else:
         achieved = flops / (kernel_ms / 1e3) / 1e12
-        ratio = float(wl.get("peak_ratio", 1.0))  # fp8: nominal 4.5 / 2.25 PFLOP/s dense over bf16
+        ratio = float(wl.get("peak_ratio", 1.0))  # nominal dense peaks over bf16: fp8 4.5/2.25, fp4 13.5/2.25
         peak = float(peaks.get("bf16_tflops", 1900.0)) * ratio
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "peak_source": f"{peak_src} bf16_tflops (burst)" + (f" x {ratio:g} (nominal fp8/bf16 ratio)"
-                                                                     if ratio != 1.0 else ""),
+                "peak_source": f"{peak_src} bf16_tflops (burst)" + (
+                    f" x {ratio:g} (nominal {'fp4' if wl.get('fp4') else 'fp8'}/bf16 dense ratio)" if ratio != 1.0 else ""),
                 "frac_of_sustained": achieved / (float(peaks.get("bf16_tflops_sustained", peak)) * ratio),
                 "traffic": traffic, "kernel_ms": kernel_ms, "algorithmic_bytes": bytes_alg}
     line = {"metric": metric, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": r["total_ms"] / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": wl.get("in_fmt", "bf16"), "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": "e2m1" if wl.get("fp4") else wl.get("in_fmt", "bf16"),
+            "data": "synthetic",
             "config": config,
             "e2e": {"value": flops / (r["e2e_ms"] / 1e3) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
@@ -558,6 +613,14 @@ def _torch_inputs_host_only(wl):
     if wl.get("mx"):
         return (A, B, C) + _mx_codes(wl)
     return A, B, C
+
+
+def _host_bits(wl):
+    """Host-side inputs of a workload for the oracle legs."""
+    if wl.get("fp4"):
+        A4, B4, sa, sb = _fp4_inputs(wl)
+        return (A4, B4, None, sa, sb)
+    return _torch_inputs_host_only(wl)
 
 
 if __name__ == "__main__":

@@ -241,7 +241,8 @@ gemm_status_t gemm_fp8_ex(int64_t M, int64_t N, int64_t K,
  * tcgen05.cp copies into TMEM, replicated over the four lane quarters.
  * SFA and SFB are device pointers, 16-byte aligned, of
  * gemm_mx_scale_bytes(M, K) and gemm_mx_scale_bytes(N, K) bytes; entries
- * for rows past M (N) or blocks past K are read but multiply only zeros.
+ * for rows past M (N) or blocks past K are read and multiply only zeros, so
+ * they must not be NaN (255).
  * Tiles are 128 x 128 per CTA: single CTAs (default), or CTA pairs
  * (cta_group 2) sharing a 256 x 128 tile, where each CTA holds the scales
  * of its own A rows and a copy of the tile's B scales. 256
@@ -262,6 +263,46 @@ gemm_status_t gemm_mxfp8(int64_t M, int64_t N, int64_t K,
 /* Bytes of one scale tensor of gemm_mxfp8 for `rows` rows (M for SFA, N for
  * SFB) and K: ceil(rows / 128) * ceil(K / 128) * 512; 0 if either is <= 0. */
 size_t gemm_mx_scale_bytes(int64_t rows, int64_t K);
+
+/* Block-scaled fp4 formats of gemm_fp4 (E2M1 elements in both). */
+typedef enum {
+    GEMM_FP4_NVFP4 = 0, /* one UE4M3 scale per 16 elements of K (kind::mxf4nvf4, scale_vec::4X) */
+    GEMM_FP4_MXFP4 = 1  /* one E8M0 scale per 32 elements of K (kind::mxf4, scale_vec::2X) */
+} gemm_fp4_scale_t;
+
+/*
+ * gemm_fp4: block-scaled fp4 GEMM, the fp4 members of the block-scaled MMA
+ * family of "06 Blackwell Tensor Core - tcgen05 MMA" (scales through
+ * tcgen05.cp into TMEM, as for gemm_mxfp8).
+ *   D = alpha * sum_k (sa[m, k/b] * A[m,k]) * (sb[n, k/b] * B[k,n]) + beta * C
+ * with block b = 16 (NVFP4) or 32 (MXFP4). A (M x K) and B (stored N x K)
+ * are K-major, E2M1 packed two to a byte: element 2i of a row in the low
+ * nibble of byte i, 2i+1 in the high nibble. K, lda and ldb count elements;
+ * K must be even and lda, ldb multiples of 32 (16-byte rows). Scale codes:
+ * UE4M3 (unsigned E4M3: 2^(e-7) * (1 + m/8), e = 0 subnormal) for NVFP4,
+ * E8M0 (2^(e-127)) for MXFP4, in the 512-byte atoms of gemm_mxfp8, one atom
+ * per 128 rows x 4 blocks: row r and element k live in atom
+ * (r / 128) * ceil(K / (4b)) + k / (4b), at byte
+ * 16 * (r % 32) + 4 * ((r % 128) / 32) + (k / b) % 4. SFA and SFB hold
+ * gemm_fp4_scale_bytes(M, K, kind) and gemm_fp4_scale_bytes(N, K, kind)
+ * bytes, 16-byte aligned; entries for rows past M (N) or blocks past K
+ * multiply only zeros but must be finite scales (a NaN code there, UE4M3
+ * 0x7F or E8M0 255, makes the whole result NaN). Tiles are 128 x 128 with
+ * one CTA each; stream_k
+ * applies as for gemm_ex; other tile options return GEMM_ERR_UNSUPPORTED.
+ */
+gemm_status_t gemm_fp4(int64_t M, int64_t N, int64_t K,
+                       const void *A, int64_t lda, const void *SFA,
+                       const void *B, int64_t ldb, const void *SFB,
+                       gemm_fp4_scale_t kind,
+                       const void *C, int64_t ldc,
+                       void *D, int64_t ldd, gemm_out_t d_type,
+                       float alpha, float beta, const gemm_options_t *opts,
+                       gemm_stream_t stream);
+
+/* Bytes of one scale tensor of gemm_fp4 for `rows` rows and K elements:
+ * ceil(rows / 128) * ceil(K / (4 * block)) * 512; 0 for bad arguments. */
+size_t gemm_fp4_scale_bytes(int64_t rows, int64_t K, gemm_fp4_scale_t kind);
 
 /*
  * Grouped GEMM: num_problems independent problems in one launch. The

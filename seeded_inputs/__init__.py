@@ -187,14 +187,15 @@ def pack_fp4(codes: np.ndarray) -> np.ndarray:
     return (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
 
 
-def mx_scale_atoms(codes: np.ndarray, rows: int, K: int, block: int = 32) -> np.ndarray:
+def mx_scale_atoms(codes: np.ndarray, rows: int, K: int, block: int = 32, fill: int = 127) -> np.ndarray:
     """Arrange row-major scale codes (``rows x ceil(K/block)``) in the 512-byte atoms of the
     block-scaled GEMM's ABI: atom (r // 128) * ceil(K/(4 block)) + k // (4 block), byte
-    16 * (r % 32) + 4 * ((r % 128) // 32) + (k // block) % 4. Unused entries are 127."""
+    16 * (r % 32) + 4 * ((r % 128) // 32) + (k // block) % 4. Unused entries hold ``fill``
+    (127 is 1.0 as E8M0; UE4M3 needs 0x38 for 1.0, its 0x7F being NaN)."""
     nb = (K + block - 1) // block
     groups = (nb + 3) // 4
     blocks = (rows + 127) // 128
-    out = np.full(blocks * groups * 512, 127, dtype=np.uint8)
+    out = np.full(blocks * groups * 512, fill, dtype=np.uint8)
     r = np.arange(rows)[:, None]
     b = np.arange(nb)[None, :]
     idx = ((r // 128) * groups + b // 4) * 512 + 16 * (r % 32) + 4 * ((r % 128) // 32) + b % 4

@@ -25,6 +25,7 @@ OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = ran
 K_MAJOR, MN_MAJOR = 0, 1
 OUT_F32, OUT_BF16, OUT_F16 = 0, 1, 2
 FP8_E4M3, FP8_E5M2 = 0, 1
+FP4_NVFP4, FP4_MXFP4 = 0, 1
 SWIZZLE_AUTO, SWIZZLE_32B, SWIZZLE_64B, SWIZZLE_128B, SWIZZLE_NONE = 0, 1, 2, 3, 4
 
 _i64, _vp, _f, _int, _u32, _u64 = (ctypes.c_int64, ctypes.c_void_p, ctypes.c_float, ctypes.c_int,
@@ -52,6 +53,10 @@ _lib.gemm_fp8.argtypes = _fp8 + [_vp]
 _lib.gemm_fp8_ex.argtypes = _fp8 + [ctypes.POINTER(GemmOptions), _vp]
 _lib.gemm_mxfp8.argtypes = [_i64, _i64, _i64, _vp, _int, _int, _i64, _vp, _vp, _int, _int, _i64, _vp, _vp, _i64, _vp,
                             _i64, _int, _f, _f, ctypes.POINTER(GemmOptions), _vp]
+_lib.gemm_fp4.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _vp, _i64, _vp, _int, _vp, _i64, _vp, _i64, _int, _f,
+                          _f, ctypes.POINTER(GemmOptions), _vp]
+_lib.gemm_fp4_scale_bytes.argtypes = [_i64, _i64, _int]
+_lib.gemm_fp4_scale_bytes.restype = ctypes.c_size_t
 _lib.gemm_mx_scale_bytes.argtypes = [_i64, _i64]
 _lib.gemm_mx_scale_bytes.restype = ctypes.c_size_t
 _grouped = [ctypes.POINTER(GemmProblem), _int, _int, _int, _int, _f, _f, _vp, ctypes.c_size_t, _vp]
@@ -74,13 +79,14 @@ _lib.gemm_debug_streamk_units.argtypes = [_int, _i64, _int, _int, _int, ctypes.P
 _lib.gemm_debug_streamk_units.restype = _int
 _lib.gemm_debug_inject_timeout.argtypes = [_int]
 _lib.gemm_debug_inject_timeout.restype = None
-for _name in ("gemm_bf16", "gemm_f16", "gemm_ex", "gemm_fp8", "gemm_fp8_ex", "gemm_mxfp8", "gemm_bf16_grouped",
+for _name in ("gemm_bf16", "gemm_f16", "gemm_ex", "gemm_fp8", "gemm_fp8_ex", "gemm_mxfp8", "gemm_fp4", "gemm_bf16_grouped",
               "gemm_f16_grouped",
               "gemm_bf16_grouped_noalloc",
               "gemm_last_device_status", "gemm_debug_descriptors", "gemm_debug_stage_image"):
     getattr(_lib, _name).restype = _int
 
 EXPORTED = ("gemm_bf16", "gemm_f16", "gemm_ex", "gemm_fp8", "gemm_fp8_ex", "gemm_mxfp8", "gemm_mx_scale_bytes",
+            "gemm_fp4", "gemm_fp4_scale_bytes",
             "gemm_streamk_workspace_size",
             "gemm_grouped_workspace_size",
             "gemm_bf16_grouped", "gemm_grouped_ex",
@@ -164,13 +170,18 @@ class GemmCall:
     """
 
     def __init__(self, in_type, M, N, K, A, a_major, lda, B, b_major, ldb, C, ldc, D, ldd, d_type, alpha, beta,
-                 options=None, stream=None, fp8=None, scales=None):
+                 options=None, stream=None, fp8=None, scales=None, fp4=None):
         """``in_type`` 0 fp16 / 1 bf16; or ``fp8=(a_format, b_format)`` for gemm_fp8_ex, plus
-        ``scales=(SFA, SFB)`` for the block-scaled gemm_mxfp8."""
+        ``scales=(SFA, SFB)`` for the block-scaled gemm_mxfp8; or ``fp4=kind`` with ``scales``
+        for gemm_fp4 (majors ignored: K-major)."""
         self._opts_ref = _opts(options)  # keeps the options struct alive
         tail = (_vp(_addr(C)), _i64(ldc), _vp(_addr(D)), _i64(ldd), _int(d_type), _f(alpha), _f(beta),
                 self._opts_ref, _vp(_stream(stream)))
-        if scales is not None:
+        if fp4 is not None:
+            self._args = (_i64(M), _i64(N), _i64(K), _vp(_addr(A)), _i64(lda), _vp(_addr(scales[0])),
+                          _vp(_addr(B)), _i64(ldb), _vp(_addr(scales[1])), _int(fp4)) + tail
+            self._fn = _lib.gemm_fp4
+        elif scales is not None:
             self._args = (_i64(M), _i64(N), _i64(K), _vp(_addr(A)), _int(fp8[0]), _int(a_major), _i64(lda),
                           _vp(_addr(scales[0])), _vp(_addr(B)), _int(fp8[1]), _int(b_major), _i64(ldb),
                           _vp(_addr(scales[1]))) + tail
@@ -208,6 +219,16 @@ def gemm_mxfp8(M, N, K, A, a_format, a_major, lda, SFA, B, b_format, b_major, ld
     _check(_lib.gemm_mxfp8(M, N, K, _addr(A), a_format, a_major, lda, _addr(SFA), _addr(B), b_format, b_major, ldb,
                            _addr(SFB), _addr(C), ldc, _addr(D), ldd, d_type, alpha, beta, _opts(options),
                            _stream(stream)), "gemm_mxfp8")
+
+
+def gemm_fp4(M, N, K, A, lda, SFA, B, ldb, SFB, kind, C, ldc, D, ldd, d_type, alpha, beta, options=None,
+             stream=None):
+    _check(_lib.gemm_fp4(M, N, K, _addr(A), lda, _addr(SFA), _addr(B), ldb, _addr(SFB), kind, _addr(C), ldc,
+                         _addr(D), ldd, d_type, alpha, beta, _opts(options), _stream(stream)), "gemm_fp4")
+
+
+def gemm_fp4_scale_bytes(rows: int, K: int, kind: int) -> int:
+    return int(_lib.gemm_fp4_scale_bytes(rows, K, kind))
 
 
 def gemm_mx_scale_bytes(rows: int, K: int) -> int:

@@ -109,12 +109,14 @@ G300_HD uint32_t make_idesc(int M, int N, int a_fmt, int b_fmt, int a_mn_major, 
     return d;
 }
 
-// Instruction descriptor of a block-scaled fp8 MMA (kind::mxf8f6f4): the
-// same shape, format and major fields, the scale format UE8M0 at bit 23, and
-// no D-format field: bits [4,6) and [29,31) carry the scale factor IDs of B
-// and A (the byte of each 32-bit scale column this MMA uses), added per MMA
-// by idesc_sf_ids.
-G300_HD uint32_t make_idesc_mx(int M, int N, int a_fmt, int b_fmt, int a_mn_major, int b_mn_major)
+// Instruction descriptor of a block-scaled MMA (kind::mxf8f6f4, mxf4,
+// mxf4nvf4): the same shape, format and major fields (E2M1 is format 1 in the
+// fp4 kinds), the scale format at bit 23 (1 UE8M0, 0 UE4M3), and no D-format
+// field: bits [4,6) and [29,31) carry the scale factor IDs of B and A (the
+// first byte of each 32-bit scale column this MMA uses), added per MMA by
+// idesc_sf_ids.
+G300_HD uint32_t make_idesc_mx(int M, int N, int a_fmt, int b_fmt, int a_mn_major, int b_mn_major,
+                               bool scale_ue8m0 = true)
 {
     uint32_t d = 0;
     d |= static_cast<uint32_t>(a_fmt & 7) << 7;
@@ -122,7 +124,7 @@ G300_HD uint32_t make_idesc_mx(int M, int N, int a_fmt, int b_fmt, int a_mn_majo
     d |= static_cast<uint32_t>(a_mn_major & 1) << 15;
     d |= static_cast<uint32_t>(b_mn_major & 1) << 16;
     d |= static_cast<uint32_t>((N >> 3) & 0x3F) << 17;
-    d |= 1u << 23;  // scale format UE8M0
+    d |= (scale_ue8m0 ? 1u : 0u) << 23;
     d |= static_cast<uint32_t>((M >> 4) & 0x1F) << 24;
     return d;
 }

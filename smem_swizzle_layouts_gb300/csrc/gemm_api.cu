@@ -41,14 +41,14 @@ struct Variant {
     bool grouped;
     int esize;
     int bm;
-    bool mx;  // block-scaled fp8
+    int sf;  // scale kind (kScale*)
     cudaError_t (*launch)(const LaunchArgs &);
     cudaError_t (*resident)(int *);
     int resident_cache[kMaxDevices];
 };
 
-#define G300_VARIANT_ROW(CG, BN, BK, ST, GR, ES, BM, MX) \
-    {CG, BN, BK, ST, GR, ES, BM, MX, &launch_gemm<CG, BN, BK, ST, GR, ES, BM, MX>, &resident_ctas<CG, BN, BK, ST, GR, ES, BM, MX>, {0}},
+#define G300_VARIANT_ROW(CG, BN, BK, ST, GR, ES, BM, SF) \
+    {CG, BN, BK, ST, GR, ES, BM, SF, &launch_gemm<CG, BN, BK, ST, GR, ES, BM, SF>, &resident_ctas<CG, BN, BK, ST, GR, ES, BM, SF>, {0}},
 Variant g_variants[] = {G300_VARIANTS(G300_VARIANT_ROW)};
 #undef G300_VARIANT_ROW
 
@@ -103,29 +103,32 @@ int resident_for(Variant &v, int dev)
     return v.resident_cache[dev];
 }
 
-Variant *find_variant(int cg, int bn, int bk, bool grouped, int esize = 2, int bm = 128, bool mx = false)
+Variant *find_variant(int cg, int bn, int bk, bool grouped, int esize = 2, int bm = 128, int sf = kScaleNone)
 {
     for (auto &v : g_variants)
         if (v.cg == cg && v.bn == bn && v.bk == bk && v.grouped == grouped && v.esize == esize && v.bm == bm &&
-            v.mx == mx)
+            v.sf == sf)
             return &v;
     return nullptr;
 }
 
 // Operand element type of a call: storage code for the tensor maps (0 fp16,
-// 1 bf16, 2 fp8 bytes), element size, the MMA format code of A and B, and
-// whether the operands carry block scales.
+// 1 bf16, 2 bytes: fp8 or packed fp4), element size, the MMA format code of
+// A and B, and the block-scale kind (kScale*).
 struct InFmt {
     int dcode, esize, a_fmt, b_fmt;
-    bool mx;
+    int sf;
 };
 
-InFmt fmt16(int in_bf16) { return InFmt{in_bf16, 2, in_bf16, in_bf16, false}; }
+InFmt fmt16(int in_bf16) { return InFmt{in_bf16, 2, in_bf16, in_bf16, kScaleNone}; }
 
-InFmt fmt8(int a_fmt, int b_fmt) { return InFmt{2, 1, a_fmt, b_fmt, false}; }
+InFmt fmt8(int a_fmt, int b_fmt) { return InFmt{2, 1, a_fmt, b_fmt, kScaleNone}; }
 
 // Block-scaled fp8: the same operand bytes plus E8M0 scale atoms.
-InFmt fmtmx(int a_fmt, int b_fmt) { return InFmt{2, 1, a_fmt, b_fmt, true}; }
+InFmt fmtmx(int a_fmt, int b_fmt) { return InFmt{2, 1, a_fmt, b_fmt, kScaleMx8}; }
+
+// Block-scaled fp4: packed E2M1 bytes (format code 1 in the fp4 kinds).
+InFmt fmtfp4(int sf) { return InFmt{2, 1, 1, 1, sf}; }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -220,9 +223,10 @@ gemm_status_t encode_operand(CUtensorMap *m, int dcode, const void *ptr, int mn_
 
 // Scale-atom map of a block-scaled operand: the atoms viewed as rows of 256
 // bytes (atom a = rows 2a, 2a + 1), one atom per 256 x 2 box.
-gemm_status_t encode_scales(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K)
+gemm_status_t encode_scales(CUtensorMap *m, const void *ptr, int64_t rows, int64_t k_bytes, int sf)
 {
-    const uint64_t atoms = static_cast<uint64_t>((rows + 127) / 128) * static_cast<uint64_t>((K + 127) / 128);
+    const int64_t per = sf_atom_kbytes(sf);
+    const uint64_t atoms = static_cast<uint64_t>((rows + 127) / 128) * static_cast<uint64_t>((k_bytes + per - 1) / per);
     return encode_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, ptr, 256, 2 * atoms, 256, 256, 2,
                      CU_TENSOR_MAP_SWIZZLE_NONE);
 }
@@ -260,7 +264,7 @@ int swz_bits_of(int opt) { return opt == GEMM_SWIZZLE_NONE ? 0 : opt; }
 // Choose the tile configuration; fills `plan` or returns an error for options
 // this build cannot honour.
 gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int sms,
-                        const gemm_options_t *o, bool grouped, Plan *plan, int esize = 2, bool mx = false)
+                        const gemm_options_t *o, bool grouped, Plan *plan, int esize = 2, int sf = kScaleNone)
 {
     gemm_options_t opt = {};
     if (o)
@@ -318,20 +322,22 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
                         : (cg == 1 && M <= 64 && esize == 2 && !grouped && bn >= 128 ? 64 : 128);
     if (bm == 64 && opt.block_k == 0)
         bk = bn == 256 ? 64 : 128;
-    if (mx) {
-        // block-scaled tiles: 128 x 128 per CTA (CTA pairs: 256 x 128),
-        // 256 (single CTAs also 128) elements of K per stage
+    if (sf != kScaleNone) {
+        // block-scaled tiles: 128 x 128 per CTA (MXFP8 CTA pairs: 256 x 128);
+        // K bytes per stage: MXFP8 256 (single CTAs also 128), NVFP4 128, MXFP4 256
+        const int bk_fixed = sf == kScaleNv4 ? 128 : 256;
         if ((opt.tile_m && opt.tile_m != 128) || (opt.tile_n && opt.tile_n != 128) ||
-            (opt.block_k && opt.block_k != 128 && opt.block_k != 256))
+            (opt.block_k && opt.block_k != bk_fixed && !(sf == kScaleMx8 && opt.block_k == 128)) ||
+            (sf != kScaleMx8 && opt.cta_group > 1))
             return GEMM_ERR_UNSUPPORTED;
         // single CTAs by default: 256 x 128 pair tiles measured slower (1773 vs
         // 1931 TFLOP/s at 8192^3), their MMAs being no wider per SM
         cg = opt.cta_group ? opt.cta_group : 1;
         bn = 128;
-        bk = opt.block_k ? opt.block_k : 256;
+        bk = opt.block_k ? opt.block_k : bk_fixed;
         bm = 128;
     }
-    if (!find_variant(cg, bn, bk, grouped, esize, bm, mx))
+    if (!find_variant(cg, bn, bk, grouped, esize, bm, sf))
         return GEMM_ERR_UNSUPPORTED;
 
     // the widest swizzle whose row fits the stage: along K for K-major
@@ -479,7 +485,7 @@ gemm_status_t run_single(const InFmt &f, int64_t M, int64_t N, int64_t K, const 
     gemm_status_t s = check_problem(M, N, K, A, a_mn, lda, B, b_mn, ldb, C, ldc, D, ldd, d_type, beta, f.esize);
     if (s != GEMM_OK || M == 0 || N == 0)
         return s;
-    if (f.mx && K > 0) {
+    if (f.sf != kScaleNone && K > 0) {
         if (!sfa || !sfb)
             return GEMM_ERR_INVALID_ARG;
         if (!aligned16(sfa) || !aligned16(sfb))
@@ -490,9 +496,9 @@ gemm_status_t run_single(const InFmt &f, int64_t M, int64_t N, int64_t K, const 
     if ((s = device_state(&dev, &status, &sms)) != GEMM_OK)
         return s;
     Plan pl;
-    if ((s = make_plan(M, N, K, a_mn, b_mn, sms, opts, false, &pl, f.esize, f.mx)) != GEMM_OK)
+    if ((s = make_plan(M, N, K, a_mn, b_mn, sms, opts, false, &pl, f.esize, f.sf)) != GEMM_OK)
         return s;
-    Variant *v = find_variant(pl.cg, pl.bn, pl.bk, false, f.esize, pl.bm, f.mx);
+    Variant *v = find_variant(pl.cg, pl.bn, pl.bk, false, f.esize, pl.bm, f.sf);
 
     LaunchArgs la;
     std::memset(&la, 0, sizeof(la));
@@ -523,10 +529,11 @@ gemm_status_t run_single(const InFmt &f, int64_t M, int64_t N, int64_t K, const 
         return GEMM_ERR_UNSUPPORTED;
     p.num_tiles = static_cast<int>(tiles);
     fill_common(p, pl, f, a_mn, b_mn, d_type, alpha, beta, status);
-    if (f.mx && K > 0) {
-        if ((s = encode_scales(&la.sfa, sfa, M, K)) != GEMM_OK || (s = encode_scales(&la.sfb, sfb, N, K)) != GEMM_OK)
+    if (f.sf != kScaleNone && K > 0) {
+        if ((s = encode_scales(&la.sfa, sfa, M, K, f.sf)) != GEMM_OK ||
+            (s = encode_scales(&la.sfb, sfb, N, K, f.sf)) != GEMM_OK)
             return s;
-        p.sf_groups = static_cast<int>((K + 127) / 128);
+        p.sf_groups = static_cast<int>((K + sf_atom_kbytes(f.sf) - 1) / sf_atom_kbytes(f.sf));
     }
     la.grid = grid_for(pl, *v, dev, sms, tiles);
     if (pl.workspace && pl.bm == 128 && K > 0) {
@@ -940,6 +947,29 @@ gemm_status_t gemm_mxfp8(int64_t M, int64_t N, int64_t K, const void *A, gemm_fp
         return GEMM_ERR_INVALID_ARG;
     return run_single(fmtmx(a_format, b_format), M, N, K, A, a_major, lda, B, b_major, ldb, C, ldc, D, ldd, d_type,
                       alpha, beta, opts, reinterpret_cast<cudaStream_t>(stream), SFA, SFB);
+}
+
+size_t gemm_fp4_scale_bytes(int64_t rows, int64_t K, gemm_fp4_scale_t kind)
+{
+    if (rows <= 0 || K <= 0 || (kind != GEMM_FP4_NVFP4 && kind != GEMM_FP4_MXFP4))
+        return 0;
+    const int64_t per = kind == GEMM_FP4_NVFP4 ? 64 : 128;  // K elements per atom (4 blocks)
+    return static_cast<size_t>((rows + 127) / 128) * static_cast<size_t>((K + per - 1) / per) * 512;
+}
+
+gemm_status_t gemm_fp4(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *SFA,
+                       const void *B, int64_t ldb, const void *SFB, gemm_fp4_scale_t kind, const void *C,
+                       int64_t ldc, void *D, int64_t ldd, gemm_out_t d_type, float alpha, float beta,
+                       const gemm_options_t *opts, gemm_stream_t stream)
+{
+    if (kind != GEMM_FP4_NVFP4 && kind != GEMM_FP4_MXFP4)
+        return GEMM_ERR_INVALID_ARG;
+    // packed operands: two elements per byte, so K and the leading dimensions go in bytes
+    if (K < 0 || (K & 1) || lda < 0 || ldb < 0 || (lda & 1) || (ldb & 1))
+        return GEMM_ERR_INVALID_ARG;
+    return run_single(fmtfp4(kind == GEMM_FP4_NVFP4 ? kScaleNv4 : kScaleMx4), M, N, K / 2, A, GEMM_K_MAJOR, lda / 2,
+                      B, GEMM_K_MAJOR, ldb / 2, C, ldc, D, ldd, d_type, alpha, beta, opts,
+                      reinterpret_cast<cudaStream_t>(stream), SFA, SFB);
 }
 
 size_t gemm_streamk_workspace_size(void)

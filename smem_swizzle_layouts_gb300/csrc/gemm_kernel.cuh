@@ -149,12 +149,24 @@ __device__ __forceinline__ int kblock_at(int it, int num_kb, int flags, int clus
     return r >= num_kb ? r - num_kb : r;
 }
 
+// Block-scaled operand kinds (the SF template argument). A scale atom holds
+// 4 scale blocks of 128 rows; its K extent in bytes is 4 x block x element
+// bytes: MXFP8 (E8M0 per 32 fp8) 128, NVFP4 (UE4M3 per 16 E2M1) 32, MXFP4
+// (E8M0 per 32 E2M1) 64. fp4 operands are packed two to a byte, and their
+// tiles count K in bytes (one 32-byte slice = one K = 64 MMA).
+enum : int { kScaleNone = 0, kScaleMx8 = 1, kScaleNv4 = 2, kScaleMx4 = 3 };
+
+__host__ __device__ constexpr int sf_atom_kbytes(int sf)
+{
+    return sf == kScaleMx8 ? 128 : sf == kScaleNv4 ? 32 : 64;
+}
+
 // ESIZE: bytes per operand element, 2 (fp16/bf16, tcgen05 kind::f16) or
 // 1 (fp8, kind::f8f6f4). BK counts elements of K per stage. BMT: accumulator
 // rows per CTA, 128 (row m in TMEM lane m) or 64 (cta_group::1 only, Layout F:
 // rows 16g..16g+15 in lanes 32g+a..32g+a+15; the two accumulators of the
 // double buffer take lane alignments a = 0 and 16 and share their columns).
-template <int CG, int BN, int BK, int STAGES, int ESIZE = 2, int BMT = 128, bool MX = false>
+template <int CG, int BN, int BK, int STAGES, int ESIZE = 2, int BMT = 128, int SF = 0>
 struct Cfg {
     static constexpr int BM = BMT;             // accumulator rows per CTA
     static constexpr int BN_LOCAL = BN / CG;   // B columns loaded by each CTA
@@ -162,7 +174,7 @@ struct Cfg {
     static constexpr int B_BYTES = BN_LOCAL * BK * ESIZE;
     // Block-scaled stages also carry the scale atoms of their K range: one
     // 512-byte atom covers 128 rows x 4 scale blocks (128 elements of K)
-    static constexpr int KGROUPS = MX ? BK / 128 : 0;
+    static constexpr int KGROUPS = SF ? BK / sf_atom_kbytes(SF) : 0;  // scale atoms per stage and row block
     static constexpr int SF_A_BYTES = 512 * KGROUPS * (BM / 128);
     static constexpr int SF_B_BYTES = 512 * KGROUPS * (BN / 128);  // every column of the tile, in each CTA
     static constexpr int SF_OFF = A_BYTES + B_BYTES;  // within a stage
@@ -172,7 +184,7 @@ struct Cfg {
     // staging chunks per epilogue warp: two (a store may still read one while
     // the next is filled); block-scaled tiles keep one, to leave room for the
     // scale atoms of three 256-element K stages
-    static constexpr int EPI_BUFS = MX ? 1 : 2;
+    static constexpr int EPI_BUFS = SF ? 1 : 2;
     static constexpr int EPI_BYTES = kEpiWarps * EPI_BUFS * kEpiBufBytes;
     static constexpr int BAR_OFF = EPI_OFF + EPI_BYTES;
     // full[S], empty[S], acc_full[2], acc_empty[2], epi[4][2], drain, inject
@@ -183,7 +195,7 @@ struct Cfg {
     // scales and 4 of B scales for each K group
     static constexpr int SF_COL0 = 2 * BN;
     static constexpr int SF_COLS = 8 * KGROUPS;
-    static constexpr int TMEM_COLS = BMT == 64 ? BN : MX ? 512 : 2 * BN;
+    static constexpr int TMEM_COLS = BMT == 64 ? BN : SF ? 512 : 2 * BN;
     static constexpr int UMMA_M = BM * CG;
     static constexpr int EPI_ROWS = BM / 4;    // output rows per epilogue warp
     static_assert(BMT == 128 || (BMT == 64 && CG == 1), "64-row tiles are single-CTA");
@@ -194,9 +206,9 @@ struct Cfg {
                   "TMEM allocation: power of two, 32..512 columns");
     static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
     static_assert(CG == 1 || BN % 32 == 0, "pair tiles split N in halves of whole atoms");
-    static_assert(!MX || (BMT == 128 && BN == 128 && ESIZE == 1 && BK % 128 == 0 &&
+    static_assert(!SF || (BMT == 128 && BN == 128 && ESIZE == 1 && BK % sf_atom_kbytes(SF) == 0 &&
                           SF_COL0 + STAGES * SF_COLS <= 512),
-                  "block-scaled tiles: 128 x 128 per CTA (256 x 128 per pair), fp8, whole 128-element K groups");
+                  "block-scaled tiles: 128 x 128 per CTA (256 x 128 per pair), byte operands, whole scale atoms");
 };
 
 // ---------------------------------------------------------------- waits
@@ -487,13 +499,13 @@ __device__ __forceinline__ int ceil_div_i(int a, int b) { return (a + b - 1) / b
 
 // ---------------------------------------------------------------- roles
 
-template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, bool MX>
+template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF>
 __device__ void role_producer(const KParams &p, const CUtensorMap *tmA, const CUtensorMap *tmB,
                               const CUtensorMap *tmSFA, const CUtensorMap *tmSFB,
                               uint32_t smem, uint32_t bar_full, uint32_t bar_empty,
                               uint32_t rank, const Waiter &w)
 {
-    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, MX>;
+    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF>;
     const Sched sched = make_sched(p);
     const int flags = p.flags;
     unsigned long long *const stats = p.stats;
@@ -573,14 +585,14 @@ __device__ void role_producer(const KParams &p, const CUtensorMap *tmA, const CU
                         issue_box<CG>(mB, sB, fb, boxB, b, n0, k0);
                 }
             }
-            if constexpr (MX) {
+            if constexpr (SF) {
                 // the scale atoms of this K range: this CTA's A rows, and every B
                 // column of the tile (the pair's MMA reads all of them from each
                 // CTA). The scale tensors are viewed as rows of 256 bytes, one
                 // atom being rows 2a and 2a + 1, so that pair CTAs signal the
                 // even CTA's barrier like the operand boxes do.
                 const uint32_t sSF = sA + C::SF_OFF;
-                const int g0 = k0 / 128;
+                const int g0 = k0 / sf_atom_kbytes(SF);
                 const int ra = m0 / 128, rb = ti.n_blk * BN / 128;
 #pragma unroll
                 for (int g = 0; g < C::KGROUPS; ++g) {
@@ -628,12 +640,12 @@ __device__ void role_producer(const KParams &p, const CUtensorMap *tmA, const CU
     }
 }
 
-template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, bool MX>
+template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF>
 __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uint32_t bar_empty,
                          uint32_t bar_acc_full, uint32_t bar_acc_empty, uint32_t bar_inject,
                          uint32_t tmem_base, const Waiter &w)
 {
-    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, MX>;
+    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF>;
     if (p.inject_timeout) {
         // Test hook: wait on a barrier nothing arrives at; the bound runs out.
         w.wait(bar_inject, 0u, kRoleMma | kWaitInjected);
@@ -642,7 +654,7 @@ __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uin
     const Sched sched = make_sched(p);
     unsigned long long *const stats = p.stats;
     const bool multicast = CG == 2 && !(p.flags & kFlagPairForward);
-    const uint32_t idesc = MX ? make_idesc_mx(C::UMMA_M, BN, p.a_fmt, p.b_fmt, p.a_mn, p.b_mn)
+    const uint32_t idesc = SF ? make_idesc_mx(C::UMMA_M, BN, p.a_fmt, p.b_fmt, p.a_mn, p.b_mn, SF != kScaleNv4)
                               : make_idesc(C::UMMA_M, BN, p.a_fmt, p.b_fmt, p.a_mn, p.b_mn);
     const OperandPacking pa = operand_packing(p.a_mn, p.a_swz, C::BM, BK);
     const OperandPacking pb = operand_packing(p.b_mn, p.b_swz, C::BN_LOCAL, BK);
@@ -694,7 +706,7 @@ __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uin
             }
             tc_fence_after_sync();
             const uint64_t sdelta = static_cast<uint64_t>((stage * C::STAGE_BYTES) >> 4);
-            if constexpr (MX) {
+            if constexpr (SF) {
                 // scale atoms -> this stage's TMEM scale columns; the MMAs below
                 // are issued after the copies by this thread and run after them
                 const uint32_t sSF = smem + stage * C::STAGE_BYTES + C::SF_OFF;
@@ -705,11 +717,15 @@ __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uin
                     tmem_cp_32x128b_warpx4<CG>(tsf + 8 * g + 4,
                                                make_smem_desc(sSF + C::SF_A_BYTES + 512 * g, 128, 128, 0));
                 }
+                // each 32-byte K slice (one MMA) reads the atom holding its blocks
+                // and, by its scale factor ID, the first of its bytes in each column
+                constexpr int kPerAtom = sf_atom_kbytes(SF) / 32;  // MMAs per atom: 4, 1, 2
 #pragma unroll
                 for (int j = 0; j < C::KSLICES; ++j) {
-                    const uint32_t ts = tsf + 8 * (j >> 2);
-                    mma_mx<CG>(d_tmem, a_desc0 + sdelta + a_off[j], b_desc0 + sdelta + b_off[j],
-                               idesc_sf_ids(idesc, j & 3, j & 3), ts, ts + 4, ((kb - kb_lo) | j) != 0);
+                    const uint32_t ts = tsf + 8 * (j / kPerAtom);
+                    const int id = (j % kPerAtom) * (4 / kPerAtom);
+                    mma_scaled<CG, SF>(d_tmem, a_desc0 + sdelta + a_off[j], b_desc0 + sdelta + b_off[j],
+                                       idesc_sf_ids(idesc, id, id), ts, ts + 4, ((kb - kb_lo) | j) != 0);
                 }
             } else {
 #pragma unroll
@@ -901,13 +917,13 @@ __device__ bool sk_gather(const Sched &sched, const Unit &ua, int n32, int buf, 
     return true;
 }
 
-template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, bool MX, int CW>
+template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF, int CW>
 __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CUtensorMap *tmD,
                               uint32_t epi_base, uint32_t bar_acc_full, uint32_t bar_acc_empty,
                               uint32_t bar_epi, uint32_t tmem_base, uint32_t rank, int warp,
                               int lane, const Waiter &w)
 {
-    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, MX>;
+    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF>;
     const Sched sched = make_sched(p);
     unsigned long long *const stats = p.stats;
     const CUtensorMap *const maps = p.maps;
@@ -1139,7 +1155,7 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
 
 // ---------------------------------------------------------------- kernel
 
-template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, bool MX>
+template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
@@ -1148,7 +1164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap tmSFA,
                         const __grid_constant__ CUtensorMap tmSFB, const __grid_constant__ KParams p)
 {
-    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, MX>;
+    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -1190,7 +1206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
         prefetch_tensormap(&tmD);
-        if constexpr (MX) {
+        if constexpr (SF) {
             prefetch_tensormap(&tmSFA);
             prefetch_tensormap(&tmSFB);
         }
@@ -1215,11 +1231,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t stage_base = base;
     if (warp == 0) {
         if (lane == 0)
-            role_producer<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, MX>(p, &tmA, &tmB, &tmSFA, &tmSFB, stage_base, bar_full,
+            role_producer<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF>(p, &tmA, &tmB, &tmSFA, &tmSFB, stage_base, bar_full,
                                                               bar_empty, rank, w);
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {
-            role_mma<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, MX>(p, stage_base, bar_full, bar_empty,
+            role_mma<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF>(p, stage_base, bar_full, bar_empty,
                                                   bar_acc_full, bar_acc_empty, bar_inject,
                                                   tmem_base, w);
             // every MMA issued by this thread has completed before TMEM is freed
@@ -1228,11 +1244,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         if (p.out_type == 0)
-            role_epilogue<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, MX, 32>(p, &tmC, &tmD, base + C::EPI_OFF,
+            role_epilogue<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, 32>(p, &tmC, &tmD, base + C::EPI_OFF,
                                                            bar_acc_full, bar_acc_empty, bar_epi,
                                                            tmem_base, rank, warp, lane, w);
         else
-            role_epilogue<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, MX, 64>(p, &tmC, &tmD, base + C::EPI_OFF,
+            role_epilogue<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, 64>(p, &tmC, &tmD, base + C::EPI_OFF,
                                                            bar_acc_full, bar_acc_empty, bar_epi,
                                                            tmem_base, rank, warp, lane, w);
         if (lane == 0)

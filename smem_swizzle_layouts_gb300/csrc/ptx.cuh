@@ -321,27 +321,40 @@ __device__ __forceinline__ void mma_commit_pair_multicast(uint32_t bar)
                  : "memory");
 }
 
-// Block-scaled fp8 MMA (kind::mxf8f6f4, one scale per 32 elements of K):
+// Block-scaled MMA: SF 1 = kind::mxf8f6f4 scale_vec::1X (fp8, one scale per
+// 32 elements), 2 = kind::mxf4nvf4 scale_vec::4X (packed E2M1, one UE4M3
+// scale per 16), 3 = kind::mxf4 scale_vec::2X (packed E2M1, one E8M0 per 32).
 // sfa / sfb are the TMEM addresses of the A and B scale columns; the scale
-// factor IDs in idesc pick the byte of each 32-bit column.
-// CTA pairs: the scales of each CTA's accumulator rows come from its own TMEM.
-template <int CG>
-__device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                       uint32_t sfa, uint32_t sfb, uint32_t accumulate)
+// factor IDs in idesc pick the first byte used in each 32-bit column. CTA
+// pairs: the scales of each CTA's accumulator rows come from its own TMEM.
+#define G300_MMA_SCALED(CGS, KIND)                                                                     \
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"                                    \
+                 "tcgen05.mma.cta_group::" CGS "." KIND " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem), \
+                 "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)                  \
+                 : "memory")
+
+template <int CG, int SF>
+__device__ __forceinline__ void mma_scaled(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t sfa, uint32_t sfb, uint32_t accumulate)
 {
-    if constexpr (CG == 1)
-        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
-                     "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], "
-                     "[%5], p;\n\t}" ::"r"(d_tmem),
-                     "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
-                     : "memory");
-    else
-        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
-                     "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], "
-                     "[%5], p;\n\t}" ::"r"(d_tmem),
-                     "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
-                     : "memory");
+    static_assert(SF >= 1 && SF <= 3, "block-scaled kinds 1..3");
+    if constexpr (CG == 1) {
+        if constexpr (SF == 1)
+            G300_MMA_SCALED("1", "kind::mxf8f6f4.block_scale.scale_vec::1X");
+        else if constexpr (SF == 2)
+            G300_MMA_SCALED("1", "kind::mxf4nvf4.block_scale.scale_vec::4X");
+        else
+            G300_MMA_SCALED("1", "kind::mxf4.block_scale.scale_vec::2X");
+    } else {
+        if constexpr (SF == 1)
+            G300_MMA_SCALED("2", "kind::mxf8f6f4.block_scale.scale_vec::1X");
+        else if constexpr (SF == 2)
+            G300_MMA_SCALED("2", "kind::mxf4nvf4.block_scale.scale_vec::4X");
+        else
+            G300_MMA_SCALED("2", "kind::mxf4.block_scale.scale_vec::2X");
+    }
 }
+#undef G300_MMA_SCALED
 
 // Copy 32 rows x 16 bytes from shared memory (descriptor `sdesc`) into 4
 // TMEM columns of lanes 0-31, replicated into all four lane quarters. For a
