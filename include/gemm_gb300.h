@@ -412,6 +412,17 @@ gemm_status_t gemm_debug_stage_image(const void *src, int major, int swizzle,
                                      void *out, gemm_stream_t stream);
 
 /*
+ * Host-side tile plan (no GPU needed): the configuration a call would launch
+ * on a device with `sms` SMs. kind: 0 fp16/bf16, 1 fp8, 2 MXFP8, 3 NVFP4,
+ * 4 MXFP4 (K in elements); grouped: nonzero for the grouped entry points.
+ * Writes 8 int32: cta_group, tile N, K per stage (bytes for fp4), rows per
+ * CTA, swizzle bits of A and B (0 none, 1 32B, 2 64B, 3 128B), epilogue
+ * swizzle, group height. Returns the status the call's planning would.
+ */
+gemm_status_t gemm_debug_plan(int64_t M, int64_t N, int64_t K, int kind, int a_major, int b_major, int grouped,
+                              const gemm_options_t *opts, int sms, int32_t *out);
+
+/*
  * Host-side listing of the stream-K schedule (no GPU needed): the split the
  * library would choose for `tiles` tiles of `kb_per_tile` K blocks on a
  * grid of `clusters` clusters under stream_k `mode`, and the units of

@@ -75,6 +75,9 @@ _lib.gemm_launch_count.restype = _u64
 _lib.gemm_debug_descriptors.argtypes = [_int, _int, _int, _int, _u32, _int, _int, _int, _int, _int, _int,
                                         _vp, _vp]
 _lib.gemm_debug_stage_image.argtypes = [_vp, _int, _int, _i64, _i64, _i64, _int, _int, _i64, _i64, _vp, _vp]
+_lib.gemm_debug_plan.argtypes = [_i64, _i64, _i64, _int, _int, _int, _int, ctypes.POINTER(GemmOptions), _int,
+                                 ctypes.POINTER(ctypes.c_int32)]
+_lib.gemm_debug_plan.restype = _int
 _lib.gemm_debug_streamk_units.argtypes = [_int, _i64, _int, _int, _int, ctypes.POINTER(ctypes.c_int32), _int]
 _lib.gemm_debug_streamk_units.restype = _int
 _lib.gemm_debug_inject_timeout.argtypes = [_int]
@@ -91,7 +94,7 @@ EXPORTED = ("gemm_bf16", "gemm_f16", "gemm_ex", "gemm_fp8", "gemm_fp8_ex", "gemm
             "gemm_grouped_workspace_size",
             "gemm_bf16_grouped", "gemm_grouped_ex",
             "gemm_f16_grouped", "gemm_bf16_grouped_noalloc", "gemm_last_device_status", "gemm_status_string", "gemm_launch_count",
-            "gemm_debug_descriptors", "gemm_debug_stage_image", "gemm_debug_streamk_units",
+            "gemm_debug_descriptors", "gemm_debug_stage_image", "gemm_debug_plan", "gemm_debug_streamk_units",
             "gemm_debug_inject_timeout")
 
 
@@ -134,7 +137,7 @@ def _opts(options) -> ctypes.POINTER(GemmOptions) | None:
     if "workspace" in opts:
         ws = opts["workspace"]
         opts["workspace"] = _addr(ws)
-        if "workspace_bytes" not in opts and ws is not None:
+        if "workspace_bytes" not in opts and ws is not None and not isinstance(ws, int):
             opts["workspace_bytes"] = ws.numel() * ws.element_size()
     return ctypes.pointer(GemmOptions(**opts))
 
@@ -233,6 +236,17 @@ def gemm_fp4_scale_bytes(rows: int, K: int, kind: int) -> int:
 
 def gemm_mx_scale_bytes(rows: int, K: int) -> int:
     return int(_lib.gemm_mx_scale_bytes(rows, K))
+
+
+PLAN_FIELDS = ("cta_group", "tile_n", "block_k", "tile_m", "swizzle_a", "swizzle_b", "epilogue_swizzle", "group_m")
+
+
+def gemm_debug_plan(M, N, K, kind=0, a_major=0, b_major=0, grouped=False, options=None, sms=148):
+    """The tile plan a call would launch (host only), as a dict; raises GemmError for rejected options."""
+    out = (ctypes.c_int32 * 8)()
+    _check(_lib.gemm_debug_plan(M, N, K, kind, a_major, b_major, int(grouped), _opts(options), sms, out),
+           "gemm_debug_plan")
+    return dict(zip(PLAN_FIELDS, list(out)))
 
 
 def gemm_debug_streamk_units(mode, tiles, clusters, kb_per_tile, cluster):

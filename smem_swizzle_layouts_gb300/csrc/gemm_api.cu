@@ -1112,6 +1112,31 @@ gemm_status_t gemm_debug_stage_image(const void *src, int major, int swizzle, in
     return GEMM_OK;
 }
 
+gemm_status_t gemm_debug_plan(int64_t M, int64_t N, int64_t K, int kind, int a_major, int b_major, int grouped,
+                              const gemm_options_t *opts, int sms, int32_t *out)
+{
+    if (!out || sms <= 0 || kind < 0 || kind > 4 || !valid_enum(a_major) || !valid_enum(b_major) || M < 0 ||
+        N < 0 || K < 0)
+        return GEMM_ERR_INVALID_ARG;
+    // kind: 0 fp16/bf16, 1 fp8, 2 MXFP8, 3 NVFP4, 4 MXFP4 (fp4: K counted in elements, planned in bytes)
+    const int esize = kind == 0 ? 2 : 1;
+    const int sf = kind == 2 ? kScaleMx8 : kind == 3 ? kScaleNv4 : kind == 4 ? kScaleMx4 : kScaleNone;
+    const int64_t k_plan = kind >= 3 ? K / 2 : K;
+    Plan pl;
+    const gemm_status_t s = make_plan(M, N, k_plan, a_major, b_major, sms, opts, grouped != 0, &pl, esize, sf);
+    if (s != GEMM_OK)
+        return s;
+    out[0] = pl.cg;
+    out[1] = pl.bn;
+    out[2] = pl.bk;
+    out[3] = pl.bm;
+    out[4] = pl.a_swz;
+    out[5] = pl.b_swz;
+    out[6] = pl.epi_swizzle;
+    out[7] = pl.group_m;
+    return GEMM_OK;
+}
+
 int gemm_debug_streamk_units(int mode, int64_t tiles, int clusters, int kb_per_tile, int cluster, int32_t *out,
                              int max_units)
 {

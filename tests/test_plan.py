@@ -1,0 +1,96 @@
+"""Tile planning, on the host (gemm_debug_plan runs the library's own planner; no GPU).
+
+Each case pins one rule of the planner: CTA pairs for large problems, the
+64-row tiles for tiny M, the K depth per stage of each operand format, the
+widest swizzle that fits a stage, the fixed tiles of the block-scaled
+formats, and the options it must refuse.
+"""
+import pytest
+
+SMS = 148
+BF16, FP8, MXFP8, NVFP4, MXFP4 = 0, 1, 2, 3, 4
+K_MAJOR, MN_MAJOR = 0, 1
+
+
+@pytest.fixture(scope="module")
+def g():
+    from smem_swizzle_layouts_gb300 import _lib
+    return _lib
+
+
+def plan(g, M, N, K, kind=BF16, a=K_MAJOR, b=K_MAJOR, sms=SMS, **opts):
+    return g.gemm_debug_plan(M, N, K, kind, a, b, options=opts or None, sms=sms)
+
+
+def test_large_bf16_uses_cta_pairs_with_256_wide_tiles_and_two_swizzle_rows_of_k(g):
+    p = plan(g, 8192, 8192, 8192, b=MN_MAJOR)
+    assert (p["cta_group"], p["tile_n"], p["block_k"], p["tile_m"]) == (2, 256, 128, 128)
+    assert (p["swizzle_a"], p["swizzle_b"]) == (3, 3)
+
+
+def test_pairs_only_from_2048_rows_and_columns(g):
+    assert plan(g, 2048, 2048, 512)["cta_group"] == 2
+    assert plan(g, 2047, 8192, 512)["cta_group"] == 1
+    assert plan(g, 8192, 2047, 512)["cta_group"] == 1
+    assert plan(g, 4096, 128, 4096, cta_group=2)["tile_n"] == 128  # narrow N: 128-wide pair tiles
+
+
+def test_single_cta_256_wide_tiles_keep_four_stages_of_64(g):
+    p = plan(g, 4096, 4096, 4096, cta_group=1, tile_n=256)
+    assert (p["tile_n"], p["block_k"], p["swizzle_a"]) == (256, 64, 3)
+
+
+def test_single_cta_tile_width_follows_the_sm_count(g):
+    # 256-wide tiles only when they still fill every SM
+    assert plan(g, 8192, 8192, 1024, cta_group=1)["tile_n"] == 256
+    assert plan(g, 4096, 512, 1024, cta_group=1)["tile_n"] == 128     # 32 x 2 tiles of 256 < 148 SMs
+    assert plan(g, 4096, 64, 1024)["tile_n"] == 64
+
+
+def test_tiny_m_uses_64_row_tiles(g):
+    p = plan(g, 64, 4096, 4096)
+    assert (p["tile_m"], p["cta_group"], p["tile_n"], p["block_k"]) == (64, 1, 128, 128)
+    assert plan(g, 65, 4096, 4096)["tile_m"] == 128
+    with pytest.raises(g.GemmError) as ei:
+        plan(g, 64, 4096, 4096, tile_m=64, cta_group=2)
+    assert ei.value.status == g.ERR_UNSUPPORTED
+
+
+def test_short_k_rows_get_narrower_swizzles(g):
+    # a K-major row of 64 bytes (32 bf16) cannot fill a 128-byte swizzle row
+    p = plan(g, 512, 512, 32)
+    assert (p["block_k"], p["swizzle_a"], p["swizzle_b"]) == (32, 2, 2)
+    assert plan(g, 512, 512, 4096, swizzle_a=4, swizzle_b=1)["swizzle_a"] == 0   # explicit no-swizzle
+
+
+def test_fp8_stage_depth_in_bytes_matches_bf16(g):
+    assert plan(g, 8192, 8192, 8192, FP8)["block_k"] == 256
+    assert plan(g, 8192, 8192, 8192, FP8, cta_group=1, tile_n=256)["block_k"] == 128
+
+
+def test_mn_major_swizzle_fits_the_tile_extent(g):
+    # fp8 pairs of 128-wide tiles: each CTA holds 64 columns of B, one 64-byte swizzle row
+    p = plan(g, 4096, 4096, 4096, MXFP8, a=MN_MAJOR, b=MN_MAJOR, cta_group=2)
+    assert (p["cta_group"], p["tile_n"], p["swizzle_a"], p["swizzle_b"]) == (2, 128, 3, 2)
+
+
+def test_block_scaled_formats_have_fixed_tiles(g):
+    assert plan(g, 8192, 8192, 8192, MXFP8) == dict(cta_group=1, tile_n=128, block_k=256, tile_m=128, swizzle_a=3,
+                                                    swizzle_b=3, epilogue_swizzle=1, group_m=8)
+    assert plan(g, 8192, 8192, 8192, MXFP8, block_k=128)["block_k"] == 128
+    assert plan(g, 8192, 8192, 8192, NVFP4)["block_k"] == 128    # bytes: 256 E2M1 per stage
+    assert plan(g, 8192, 8192, 8192, MXFP4)["block_k"] == 256
+    for kind, opts in [(MXFP8, dict(tile_n=256)), (NVFP4, dict(cta_group=2)), (MXFP4, dict(block_k=128)),
+                       (NVFP4, dict(tile_m=64))]:
+        with pytest.raises(g.GemmError) as ei:
+            plan(g, 4096, 4096, 4096, kind, **opts)
+        assert ei.value.status == g.ERR_UNSUPPORTED, (kind, opts)
+
+
+def test_invalid_options_are_rejected(g):
+    for opts, status in [(dict(flags=16), g.ERR_INVALID_ARG), (dict(stream_k=4), g.ERR_INVALID_ARG),
+                         (dict(swizzle_a=5), g.ERR_INVALID_ARG), (dict(tile_m=96), g.ERR_INVALID_ARG),
+                         (dict(workspace=0x1010), g.ERR_ALIGNMENT), (dict(tile_n=96), g.ERR_UNSUPPORTED)]:
+        with pytest.raises(g.GemmError) as ei:
+            plan(g, 1024, 1024, 1024, **opts)
+        assert ei.value.status == status, opts
