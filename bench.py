@@ -247,6 +247,16 @@ def _torch_inputs(wl, dev, pinned=False):
     return (A, B, C), host, devt
 
 
+class _DeviceSet:
+    """Device buffers and a launch for one slot of the end-to-end pipeline."""
+
+    def __init__(self, pairs, step, outs):
+        self.pairs, self.step, self._outs = pairs, step, outs
+
+    def outputs(self):
+        return self._outs
+
+
 class GemmJob:
     """One GEMM per step through gemm_ex."""
 
@@ -301,16 +311,31 @@ class GemmJob:
             self.pairs += list(zip(host_s, scales))
         lda = self.K if wl.get("fp4") else self.A.stride(0)
         ldb = self.K if wl.get("fp4") else self.B.stride(0)
-        self.call = g.GemmCall(self.in_type, self.M, self.N, self.K, self.A, self.am, lda, self.B,
-                               self.bm, ldb, self.C, self.N if self.C is not None else 0, self.D,
-                               self.N, self.dt, wl["alpha"], wl["beta"], options=options, stream=stream, fp8=fp8,
-                               scales=scales, fp4=FP4_KINDS[wl["fp4"]][0] if wl.get("fp4") else None)
+        fp4 = FP4_KINDS[wl["fp4"]][0] if wl.get("fp4") else None
+
+        def make_call(A, B, C, D, sc):
+            return g.GemmCall(self.in_type, self.M, self.N, self.K, A, self.am, lda, B, self.bm, ldb, C,
+                              self.N if C is not None else 0, D, self.N, self.dt, wl["alpha"], wl["beta"],
+                              options=options, stream=stream, fp8=fp8, scales=sc, fp4=fp4)
+
+        self._make_call, self._scales = make_call, scales
+        self.call = make_call(self.A, self.B, self.C, self.D, scales)
 
     def step(self):
         self.call()
 
     def outputs(self):
         return [(self.D, self.hD)]
+
+    def second_set(self):
+        """A second set of device buffers (same host buffers) with its own pre-marshalled call."""
+        import torch
+        twin = {id(d): torch.empty_like(d) for _, d in self.pairs}
+        D2 = torch.empty_like(self.D)
+        call = self._make_call(twin[id(self.A)], twin[id(self.B)],
+                               twin[id(self.C)] if self.C is not None else None, D2,
+                               [twin[id(s)] for s in self._scales] if self._scales else None)
+        return _DeviceSet([(h, twin[id(d)]) for h, d in self.pairs], call, [(D2, self.hD)])
 
     def oracle_rate(self, target_s, fixed_rows=None):
         return _oracle_rows_rate(self.wl, self.bits, target_s, fixed_rows=fixed_rows)
@@ -351,6 +376,19 @@ class GroupedJob:
 
     def outputs(self):
         return self.outs
+
+    def second_set(self):
+        """A second set of device buffers (same host buffers) with its own problem list and workspace."""
+        import torch
+        twin = {id(d): torch.empty_like(d) for _, d in self.pairs}
+        outs = [(torch.empty_like(d), h) for d, h in self.outs]
+        probs = [dict(q, A=twin[id(q["A"])], B=twin[id(q["B"])], D=o[0]) for q, o in zip(self.probs, outs)]
+        ws = torch.empty_like(self.ws)
+        wl, g, stream, ws_bytes = self.wl, self.g, self.stream, self.ws_bytes
+
+        def call():
+            g.gemm_bf16_grouped(probs, 0, 0, 1, wl["alpha"], wl["beta"], ws, ws_bytes, stream=stream)
+        return _DeviceSet([(h, twin[id(d)]) for h, d in self.pairs], call, outs)
 
     def oracle_rate(self, target_s, fixed_rows=None):
         A, B = self.bits[0]
@@ -413,19 +451,44 @@ def _run_ours(args, wl_name, wl, ws, rank, local):
         total_ms = max_over_ranks(total_ms, dev)
 
     # ---- end to end through the public API with host buffers
-    e2e_steps = max(1, min(args.steps, 10))
+    # ---- end to end: every step uploads its inputs from pinned host memory,
+    # runs the GEMM and reads its result back. Steps are pipelined the way a
+    # stream of independent GEMMs would be: uploads, compute and downloads on
+    # three streams over two device buffer sets, so step i+1 uploads while
+    # step i computes and step i-1 downloads (events guard each set's reuse).
+    e2e_steps = max(2, min(args.steps, 20))
+    sets = [job, job.second_set()]
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev = lambda: torch.cuda.Event(enable_timing=False)  # noqa: E731
+    ev_in, ev_cmp, ev_out = ([ev() for _ in range(e2e_steps)] for _ in range(3))
+    for S in sets:  # first use of the second set's call outside the timed region
+        with torch.cuda.stream(stream):
+            S.step()
+    torch.cuda.synchronize(dev)
     barrier()
-    with torch.cuda.stream(stream):
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            for h, d in job.pairs:
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(s_in)
+    for i in range(e2e_steps):
+        S = sets[i % 2]
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(ev_cmp[i - 2])  # this set's inputs are free once its last GEMM ran
+            for h, d in S.pairs:
                 d.copy_(h, non_blocking=True)
-            job.step()
-            for d, h in job.outputs():
+            ev_in[i].record(s_in)
+        stream.wait_event(ev_in[i])
+        if i >= 2:
+            stream.wait_event(ev_out[i - 2])  # its output buffer has been read back
+        S.step()
+        ev_cmp[i].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_cmp[i])
+            for d, h in S.outputs():
                 h.copy_(d, non_blocking=True)
-        e1.record(stream)
+            ev_out[i].record(s_out)
+    s_out.wait_event(ev_in[e2e_steps - 1])
+    e1.record(s_out)
     barrier()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     h2d = sum(d.numel() * d.element_size() for _, d in job.pairs)
