@@ -48,8 +48,9 @@ WORKLOADS = {
              "cta_group::2 CTA pairs, persistent tile scheduler"),
     "square4096_bf16": dict(
         M=4096, N=4096, K=4096, a_major="K", b_major="K", out="bf16", alpha=1.0, beta=0.0, dist="normal",
-        scale=0.1, seed=10, options=dict(cta_group=1, tile_n=256),
-        desc="4096^3 bf16, A and B K-major, N(0,1)*0.1, bf16 out, SW128, cta_group::1"),
+        scale=0.1, seed=10, options=dict(cta_group=1, tile_n=256, workspace=True),
+        desc="4096^3 bf16, A and B K-major, N(0,1)*0.1, bf16 out, SW128, cta_group::1; stream-K workspace "
+             "given, so the ragged last wave (512 tiles on 152 CTAs) is split"),
     "skinny_m16384_n128_k8192": dict(
         M=16384, N=128, K=8192, a_major="K", b_major="K", out="bf16", alpha=1.0, beta=0.0, dist="normal",
         scale=1.0, seed=30, options=None, bound="hbm", desc="M=16384 N=128 K=8192 bf16, N(0,1), bf16 out"),
@@ -70,7 +71,7 @@ WORKLOADS = {
         M=8192, N=8192, K=8192, a_major="K", b_major="K", out="bf16", alpha=1.0, beta=0.0, dist="uniform",
         scale=1.0, seed=50, options=None, in_fmt="e4m3", b_fmt="e4m3", mx=True, peak_ratio=2.0,
         desc="8192^3 block-scaled fp8 (MXFP8: E4M3 with one E8M0 scale per 32 elements of K, codes U{124..130}; "
-             "tcgen05 kind::mxf8f6f4), A and B K-major, U[-1,1], fp32 accumulate, bf16 out, 128x128 tiles"),
+             "tcgen05 kind::mxf8f6f4), A and B K-major, U[-1,1], fp32 accumulate, bf16 out, 256x256 CTA-pair tiles"),
     "square8192_nvfp4": dict(
         M=8192, N=8192, K=8192, a_major="K", b_major="K", out="bf16", alpha=1.0, beta=0.0, dist="fp4",
         scale=1.0, seed=60, options=None, fp4="nvfp4", peak_ratio=6.0,

@@ -243,9 +243,12 @@ gemm_status_t gemm_fp8_ex(int64_t M, int64_t N, int64_t K,
  * gemm_mx_scale_bytes(M, K) and gemm_mx_scale_bytes(N, K) bytes; entries
  * for rows past M (N) or blocks past K are read and multiply only zeros, so
  * they must not be NaN (255).
- * Tiles are 128 x 128 per CTA: single CTAs (default), or CTA pairs
- * (cta_group 2) sharing a 256 x 128 tile, where each CTA holds the scales
- * of its own A rows and a copy of the tile's B scales. 256
+ * Tiles: CTA pairs sharing a 256 x 256 tile (the default from M, N >= 2048;
+ * one accumulator buffer, so each tile's epilogue is not overlapped and
+ * stream_k is not applied), single CTAs of 128 x 128 (the default below
+ * that), or pairs sharing 256 x 128 (cta_group 2 with tile_n 128). In a
+ * pair each CTA holds the scales of its own A rows and a copy of all the
+ * tile's B scales. 256
  * elements of K per pipeline stage (single CTAs may ask block_k = 128);
  * options asking for other tiles return GEMM_ERR_UNSUPPORTED. stream_k
  * applies as for gemm_ex.

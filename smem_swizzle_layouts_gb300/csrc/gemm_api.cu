@@ -326,14 +326,18 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
         // block-scaled tiles: 128 x 128 per CTA (MXFP8 CTA pairs: 256 x 128);
         // K bytes per stage: MXFP8 256 (single CTAs also 128), NVFP4 128, MXFP4 256
         const int bk_fixed = sf == kScaleNv4 ? 128 : 256;
-        if ((opt.tile_m && opt.tile_m != 128) || (opt.tile_n && opt.tile_n != 128) ||
+        // MXFP8 pairs also come as 256 x 256 tiles (one accumulator buffer):
+        // the default from 2048 rows and columns (2588 against 1897 TFLOP/s
+        // for single CTAs at 8192^3; 256 x 128 pairs measured 1773)
+        const bool mx_wide = sf == kScaleMx8 && opt.cta_group == 0 && opt.tile_n == 0 &&
+                             (opt.block_k == 0 || opt.block_k == 256) && M >= 2048 && N >= 2048;
+        const bool wide_ok = sf == kScaleMx8 && (opt.cta_group == 2 || mx_wide);
+        if ((opt.tile_m && opt.tile_m != 128) || (opt.tile_n && opt.tile_n != 128 && !(wide_ok && opt.tile_n == 256)) ||
             (opt.block_k && opt.block_k != bk_fixed && !(sf == kScaleMx8 && opt.block_k == 128)) ||
             (sf != kScaleMx8 && opt.cta_group > 1))
             return GEMM_ERR_UNSUPPORTED;
-        // single CTAs by default: 256 x 128 pair tiles measured slower (1773 vs
-        // 1931 TFLOP/s at 8192^3), their MMAs being no wider per SM
-        cg = opt.cta_group ? opt.cta_group : 1;
-        bn = 128;
+        cg = opt.cta_group ? opt.cta_group : (mx_wide ? 2 : 1);
+        bn = opt.tile_n ? opt.tile_n : (mx_wide ? 256 : 128);
         bk = opt.block_k ? opt.block_k : bk_fixed;
         bm = 128;
     }
@@ -536,7 +540,8 @@ gemm_status_t run_single(const InFmt &f, int64_t M, int64_t N, int64_t K, const 
         p.sf_groups = static_cast<int>((K + sf_atom_kbytes(f.sf) - 1) / sf_atom_kbytes(f.sf));
     }
     la.grid = grid_for(pl, *v, dev, sms, tiles);
-    if (pl.workspace && pl.bm == 128 && K > 0) {
+    // stream-K needs a spare accumulator buffer: not for block-scaled 256-wide tiles
+    if (pl.workspace && pl.bm == 128 && K > 0 && !(f.sf != kScaleNone && pl.bn == 256)) {
         // stream-K runs on every resident cluster
         const int full = grid_for(pl, *v, dev, sms, static_cast<int64_t>(1) << 40);
         const int64_t kbt = (K + pl.bk - 1) / pl.bk;

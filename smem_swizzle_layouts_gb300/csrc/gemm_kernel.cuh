@@ -193,8 +193,13 @@ struct Cfg {
     static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack to align the base
     // TMEM: two accumulators, then (block-scaled) per stage 4 columns of A
     // scales and 4 of B scales for each K group
-    static constexpr int SF_COL0 = 2 * BN;
-    static constexpr int SF_COLS = 8 * KGROUPS;
+    // Accumulator buffers: two (the epilogue of one tile overlaps the next
+    // tile's MMAs), except for block-scaled 256-wide tiles, whose two
+    // accumulators would leave no TMEM for the scale slots
+    static constexpr int ACC_BUFS = (SF && BN == 256) ? 1 : 2;
+    static constexpr int SF_COL0 = ACC_BUFS * BN;
+    static constexpr int SF_GROUP_COLS = 4 + 4 * (BN / 128);  // A atom, then the B atoms of one K group
+    static constexpr int SF_COLS = SF_GROUP_COLS * KGROUPS;
     static constexpr int TMEM_COLS = BMT == 64 ? BN : SF ? 512 : 2 * BN;
     static constexpr int UMMA_M = BM * CG;
     static constexpr int EPI_ROWS = BM / 4;    // output rows per epilogue warp
@@ -206,9 +211,9 @@ struct Cfg {
                   "TMEM allocation: power of two, 32..512 columns");
     static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
     static_assert(CG == 1 || BN % 32 == 0, "pair tiles split N in halves of whole atoms");
-    static_assert(!SF || (BMT == 128 && BN == 128 && ESIZE == 1 && BK % sf_atom_kbytes(SF) == 0 &&
-                          SF_COL0 + STAGES * SF_COLS <= 512),
-                  "block-scaled tiles: 128 x 128 per CTA (256 x 128 per pair), byte operands, whole scale atoms");
+    static_assert(!SF || (BMT == 128 && (BN == 128 || (BN == 256 && CG == 2)) && ESIZE == 1 &&
+                          BK % sf_atom_kbytes(SF) == 0 && SF_COL0 + STAGES * SF_COLS <= 512),
+                  "block-scaled tiles: 128-wide per CTA, or 256-wide for pairs; byte operands; whole atoms");
 };
 
 // ---------------------------------------------------------------- waits
@@ -713,16 +718,20 @@ __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uin
                 const uint32_t tsf = tmem_base + static_cast<uint32_t>(C::SF_COL0 + stage * C::SF_COLS);
 #pragma unroll
                 for (int g = 0; g < C::KGROUPS; ++g) {
-                    tmem_cp_32x128b_warpx4<CG>(tsf + 8 * g, make_smem_desc(sSF + 512 * g, 128, 128, 0));
-                    tmem_cp_32x128b_warpx4<CG>(tsf + 8 * g + 4,
-                                               make_smem_desc(sSF + C::SF_A_BYTES + 512 * g, 128, 128, 0));
+                    const uint32_t tg = tsf + static_cast<uint32_t>(C::SF_GROUP_COLS * g);
+                    tmem_cp_32x128b_warpx4<CG>(tg, make_smem_desc(sSF + 512 * g, 128, 128, 0));
+                    // B scales of columns 128h..128h+127 in the next 4 columns each
+#pragma unroll
+                    for (int h = 0; h < BN / 128; ++h)
+                        tmem_cp_32x128b_warpx4<CG>(
+                            tg + 4 + 4 * h, make_smem_desc(sSF + C::SF_A_BYTES + 512 * (g * (BN / 128) + h), 128, 128, 0));
                 }
                 // each 32-byte K slice (one MMA) reads the atom holding its blocks
                 // and, by its scale factor ID, the first of its bytes in each column
                 constexpr int kPerAtom = sf_atom_kbytes(SF) / 32;  // MMAs per atom: 4, 1, 2
 #pragma unroll
                 for (int j = 0; j < C::KSLICES; ++j) {
-                    const uint32_t ts = tsf + 8 * (j / kPerAtom);
+                    const uint32_t ts = tsf + static_cast<uint32_t>(C::SF_GROUP_COLS * (j / kPerAtom));
                     const int id = (j % kPerAtom) * (4 / kPerAtom);
                     mma_scaled<CG, SF>(d_tmem, a_desc0 + sdelta + a_off[j], b_desc0 + sdelta + b_off[j],
                                        idesc_sf_ids(idesc, id, id), ts, ts + 4, ((kb - kb_lo) | j) != 0);
@@ -752,9 +761,10 @@ __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uin
             mma_commit_pair_multicast(bar_acc_full + 8 * acc);
         else
             mma_commit<CG>(bar_acc_full + 8 * acc);
-        acc ^= 1;
-        if (acc == 0)
+        if (++acc == C::ACC_BUFS) {
+            acc = 0;
             acc_phase ^= 1u;
+        }
     }
     if (stats) {
         unsigned long long *o = stats + blockIdx.x * kStatSlots;
@@ -953,7 +963,7 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
     long long t_last_acc = 0;
     const long long t_start = clock64();
     // stream-K: this CTA's partial-sum slot, and its row in every slot
-    constexpr bool kStreamK = C::BM == 128 && !GROUPED;
+    constexpr bool kStreamK = C::BM == 128 && !GROUPED && C::ACC_BUFS == 2;  // the gather needs the spare buffer
     const bool split = kStreamK && sched.sk_iters > 0;
     float4 *const partials = reinterpret_cast<float4 *>(p.sk_partials);
     uint32_t *const sk_flags = p.sk_flags;
@@ -1039,9 +1049,10 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
                 else
                     mbar_arrive(bar_acc_empty + 8 * acc);
             }
-            acc ^= 1;
-            if (acc == 0)
+            if (++acc == C::ACC_BUFS) {
+                acc = 0;
                 acc_phase ^= 1u;
+            }
             continue;
         }
         for (int c = 0; c < BN / CW; ++c) {
@@ -1136,9 +1147,10 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
                 else
                     mbar_arrive(bar_acc_empty + 8 * acc);
             }
-            acc ^= 1;
-            if (acc == 0)
+            if (++acc == C::ACC_BUFS) {
+                acc = 0;
                 acc_phase ^= 1u;
+            }
         }
     }
     if (stats && ew == 0 && lane == 0) {

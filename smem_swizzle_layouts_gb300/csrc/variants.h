@@ -40,6 +40,7 @@ cudaError_t resident_ctas(int *ctas);
     X(1, 128, 256, 3, false, 1, 128, 0) \
     X(1, 128, 128, 4, false, 2, 64, 0) \
     X(1, 256, 64, 4, false, 2, 64, 0) \
+    X(2, 256, 256, 3, false, 1, 128, 1) \
     X(2, 128, 256, 4, false, 1, 128, 1) \
     X(1, 128, 256, 3, false, 1, 128, 1) \
     X(1, 128, 128, 5, false, 1, 128, 1) \

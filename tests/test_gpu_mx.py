@@ -147,6 +147,27 @@ def test_mx_cta_pairs_stream_k_and_tolerance(g):
     run_mx(g, 1024, 640, 1024, dist="normal", out="bf16", alpha=1.5, beta=0.5, seed=37, options=dict(cta_group=2))
 
 
+@pytest.mark.parametrize("M,N,K", [(512, 512, 512), (700, 600, 1000), (2048, 2048, 768), (256, 200, 96)])
+def test_mx_wide_pairs_exact(g, M, N, K):
+    # 256 x 256 pair tiles with a single accumulator buffer; each CTA's TMEM
+    # holds the scales of its A rows and both B atoms of the tile
+    run_mx(g, M, N, K, exact=True, seed=5 * M + K, options=dict(cta_group=2, tile_n=256))
+
+
+def test_mx_wide_pairs_majors_formats_and_tolerance(g):
+    run_mx(g, 512, 768, 640, a_major="MN", b_major="MN", a_fmt="e5m2", b_fmt="e4m3", exact=True, seed=41,
+           options=dict(cta_group=2, tile_n=256))
+    run_mx(g, 1024, 768, 1024, dist="normal", out="bf16", alpha=0.5, beta=1.5, seed=43,
+           options=dict(cta_group=2, tile_n=256))
+
+
+def test_mx_wide_pairs_ignore_stream_k(g):
+    # no spare accumulator buffer: the split is not applied, the result is unchanged
+    ws = torch.zeros(g.gemm_streamk_workspace_size(), dtype=torch.uint8, device=DEV)
+    run_mx(g, 700, 600, 1500, exact=True, seed=47, options=dict(cta_group=2, tile_n=256, workspace=ws, stream_k=2,
+                                                                  max_ctas=6))
+
+
 def test_mx_stream_k_exact(g):
     ws = torch.zeros(g.gemm_streamk_workspace_size(), dtype=torch.uint8, device=DEV)
     run_mx(g, 700, 300, 1500, exact=True, seed=19, options=dict(workspace=ws, stream_k=2, max_ctas=5))

@@ -75,12 +75,17 @@ def test_mn_major_swizzle_fits_the_tile_extent(g):
 
 
 def test_block_scaled_formats_have_fixed_tiles(g):
-    assert plan(g, 8192, 8192, 8192, MXFP8) == dict(cta_group=1, tile_n=128, block_k=256, tile_m=128, swizzle_a=3,
+    # large MXFP8: 256 x 256 pair tiles; smaller problems and fp4: single CTAs of 128 x 128
+    assert plan(g, 8192, 8192, 8192, MXFP8) == dict(cta_group=2, tile_n=256, block_k=256, tile_m=128, swizzle_a=3,
                                                     swizzle_b=3, epilogue_swizzle=1, group_m=8)
+    assert plan(g, 1024, 8192, 8192, MXFP8) == dict(cta_group=1, tile_n=128, block_k=256, tile_m=128, swizzle_a=3,
+                                                    swizzle_b=3, epilogue_swizzle=1, group_m=8)
+    assert plan(g, 8192, 8192, 8192, MXFP8, cta_group=2)["tile_n"] == 128
+    assert plan(g, 8192, 8192, 8192, MXFP8, cta_group=2, tile_n=256)["tile_n"] == 256
     assert plan(g, 8192, 8192, 8192, MXFP8, block_k=128)["block_k"] == 128
     assert plan(g, 8192, 8192, 8192, NVFP4)["block_k"] == 128    # bytes: 256 E2M1 per stage
     assert plan(g, 8192, 8192, 8192, MXFP4)["block_k"] == 256
-    for kind, opts in [(MXFP8, dict(tile_n=256)), (NVFP4, dict(cta_group=2)), (MXFP4, dict(block_k=128)),
+    for kind, opts in [(MXFP8, dict(tile_n=256, cta_group=1)), (NVFP4, dict(cta_group=2)), (MXFP4, dict(block_k=128)),
                        (NVFP4, dict(tile_m=64))]:
         with pytest.raises(g.GemmError) as ei:
             plan(g, 4096, 4096, 4096, kind, **opts)
