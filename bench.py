@@ -76,12 +76,14 @@ WORKLOADS = {
         M=8192, N=8192, K=8192, a_major="K", b_major="K", out="bf16", alpha=1.0, beta=0.0, dist="fp4",
         scale=1.0, seed=60, options=None, fp4="nvfp4", peak_ratio=6.0,
         desc="8192^3 block-scaled fp4 (NVFP4: packed E2M1, all sixteen codes, one UE4M3 scale per 16 elements "
-             "of K from {1/4..6}; tcgen05 kind::mxf4nvf4), A and B K-major, fp32 accumulate, bf16 out, 128x128 tiles"),
+             "of K from {1/4..6}; tcgen05 kind::mxf4nvf4), A and B K-major, fp32 accumulate, bf16 out, "
+             "256x256 CTA-pair tiles"),
     "square8192_mxfp4": dict(
         M=8192, N=8192, K=8192, a_major="K", b_major="K", out="bf16", alpha=1.0, beta=0.0, dist="fp4",
         scale=1.0, seed=70, options=None, fp4="mxfp4", peak_ratio=6.0,
         desc="8192^3 block-scaled fp4 (MXFP4: packed E2M1, all sixteen codes, one E8M0 scale per 32 elements "
-             "of K, codes U{124..130}; tcgen05 kind::mxf4), A and B K-major, fp32 accumulate, bf16 out, 128x128 tiles"),
+             "of K, codes U{124..130}; tcgen05 kind::mxf4), A and B K-major, fp32 accumulate, bf16 out, "
+             "256x256 CTA-pair tiles"),
     "single_tile_128x128x32_f16": dict(
         M=128, N=128, K=32, a_major="K", b_major="MN", out="f32", alpha=1.0, beta=0.0, dist="uniform",
         scale=1.0, seed=0, options=None, in_fmt="f16",

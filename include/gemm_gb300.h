@@ -290,8 +290,9 @@ typedef enum {
  * gemm_fp4_scale_bytes(M, K, kind) and gemm_fp4_scale_bytes(N, K, kind)
  * bytes, 16-byte aligned; entries for rows past M (N) or blocks past K
  * multiply only zeros but must be finite scales (a NaN code there, UE4M3
- * 0x7F or E8M0 255, makes the whole result NaN). Tiles are 128 x 128 with
- * one CTA each; stream_k
+ * 0x7F or E8M0 255, makes the whole result NaN). Tiles: 256 x 256 CTA pairs
+ * with one accumulator buffer (default from M, N >= 2048; cta_group 2) or
+ * single CTAs of 128 x 128; stream_k (single CTAs)
  * applies as for gemm_ex; other tile options return GEMM_ERR_UNSUPPORTED.
  */
 gemm_status_t gemm_fp4(int64_t M, int64_t N, int64_t K,

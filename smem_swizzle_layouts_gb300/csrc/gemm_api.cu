@@ -222,13 +222,14 @@ gemm_status_t encode_operand(CUtensorMap *m, int dcode, const void *ptr, int mn_
 }
 
 // Scale-atom map of a block-scaled operand: the atoms viewed as rows of 256
-// bytes (atom a = rows 2a, 2a + 1), one atom per 256 x 2 box.
-gemm_status_t encode_scales(CUtensorMap *m, const void *ptr, int64_t rows, int64_t k_bytes, int sf)
+// bytes (atom a = rows 2a, 2a + 1); one box holds the `groups` consecutive
+// atoms a stage of the kernel needs for one row block.
+gemm_status_t encode_scales(CUtensorMap *m, const void *ptr, int64_t rows, int64_t k_bytes, int sf, int groups)
 {
     const int64_t per = sf_atom_kbytes(sf);
     const uint64_t atoms = static_cast<uint64_t>((rows + 127) / 128) * static_cast<uint64_t>((k_bytes + per - 1) / per);
-    return encode_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, ptr, 256, 2 * atoms, 256, 256, 2,
-                     CU_TENSOR_MAP_SWIZZLE_NONE);
+    return encode_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, ptr, 256, 2 * atoms, 256, 256,
+                     static_cast<uint32_t>(2 * groups), CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 // Output (and C) map: boxes of 128 bytes x the rows one epilogue warp owns
@@ -323,23 +324,24 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
     if (bm == 64 && opt.block_k == 0)
         bk = bn == 256 ? 64 : 128;
     if (sf != kScaleNone) {
-        // block-scaled tiles: 128 x 128 per CTA (MXFP8 CTA pairs: 256 x 128);
-        // K bytes per stage: MXFP8 256 (single CTAs also 128), NVFP4 128, MXFP4 256
-        const int bk_fixed = sf == kScaleNv4 ? 128 : 256;
-        // MXFP8 pairs also come as 256 x 256 tiles (one accumulator buffer):
-        // the default from 2048 rows and columns (2588 against 1897 TFLOP/s
-        // for single CTAs at 8192^3; 256 x 128 pairs measured 1773)
-        const bool mx_wide = sf == kScaleMx8 && opt.cta_group == 0 && opt.tile_n == 0 &&
-                             (opt.block_k == 0 || opt.block_k == 256) && M >= 2048 && N >= 2048;
-        const bool wide_ok = sf == kScaleMx8 && (opt.cta_group == 2 || mx_wide);
-        if ((opt.tile_m && opt.tile_m != 128) || (opt.tile_n && opt.tile_n != 128 && !(wide_ok && opt.tile_n == 256)) ||
-            (opt.block_k && opt.block_k != bk_fixed && !(sf == kScaleMx8 && opt.block_k == 128)) ||
-            (sf != kScaleMx8 && opt.cta_group > 1))
+        // Block-scaled tiles: 256 x 256 CTA pairs with one accumulator buffer
+        // (the default from 2048 rows and columns; MXFP8 8192^3 2588 against
+        // 1897 TFLOP/s for single CTAs), single CTAs of 128 x 128, and MXFP8
+        // pairs of 256 x 128 (1773). K bytes per stage: MXFP8 256 (single CTAs
+        // also 128), NVFP4 128, MXFP4 256 single and 128 in pairs; the variant
+        // lookup below refuses anything else.
+        if (opt.tile_m && opt.tile_m != 128)
             return GEMM_ERR_UNSUPPORTED;
-        cg = opt.cta_group ? opt.cta_group : (mx_wide ? 2 : 1);
-        bn = opt.tile_n ? opt.tile_n : (mx_wide ? 256 : 128);
-        bk = opt.block_k ? opt.block_k : bk_fixed;
+        auto depth = [&](int c) { return sf == kScaleMx8 ? 256 : sf == kScaleNv4 ? 128 : (c == 2 ? 128 : 256); };
+        const bool wide = opt.cta_group == 0 && opt.tile_n == 0 && M >= 2048 && N >= 2048;
+        cg = opt.cta_group ? opt.cta_group : (wide ? 2 : 1);
+        bn = opt.tile_n ? opt.tile_n : (cg == 2 && (wide || sf != kScaleMx8) ? 256 : 128);
+        bk = opt.block_k ? opt.block_k : depth(cg);
         bm = 128;
+        if (wide && !find_variant(cg, bn, bk, grouped, esize, bm, sf)) {
+            cg = 1;  // a stage depth only single CTAs are built for
+            bn = 128;
+        }
     }
     if (!find_variant(cg, bn, bk, grouped, esize, bm, sf))
         return GEMM_ERR_UNSUPPORTED;
@@ -534,8 +536,9 @@ gemm_status_t run_single(const InFmt &f, int64_t M, int64_t N, int64_t K, const 
     p.num_tiles = static_cast<int>(tiles);
     fill_common(p, pl, f, a_mn, b_mn, d_type, alpha, beta, status);
     if (f.sf != kScaleNone && K > 0) {
-        if ((s = encode_scales(&la.sfa, sfa, M, K, f.sf)) != GEMM_OK ||
-            (s = encode_scales(&la.sfb, sfb, N, K, f.sf)) != GEMM_OK)
+        const int groups = pl.bk / sf_atom_kbytes(f.sf);  // atoms per stage and row block
+        if ((s = encode_scales(&la.sfa, sfa, M, K, f.sf, groups)) != GEMM_OK ||
+            (s = encode_scales(&la.sfb, sfb, N, K, f.sf, groups)) != GEMM_OK)
             return s;
         p.sf_groups = static_cast<int>((K + sf_atom_kbytes(f.sf) - 1) / sf_atom_kbytes(f.sf));
     }

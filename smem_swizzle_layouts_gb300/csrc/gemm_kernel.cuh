@@ -593,31 +593,27 @@ __device__ void role_producer(const KParams &p, const CUtensorMap *tmA, const CU
             if constexpr (SF) {
                 // the scale atoms of this K range: this CTA's A rows, and every B
                 // column of the tile (the pair's MMA reads all of them from each
-                // CTA). The scale tensors are viewed as rows of 256 bytes, one
-                // atom being rows 2a and 2a + 1, so that pair CTAs signal the
-                // even CTA's barrier like the operand boxes do.
+                // CTA). The scale tensors are viewed as rows of 256 bytes, atom a
+                // being rows 2a and 2a + 1; a row block's atoms of consecutive K
+                // groups are adjacent, so one box of 2 x KGROUPS rows brings all
+                // of a stage's atoms of one row block. Atoms past the last K group
+                // (the tail of the last stage: the next row block's, or TMA's zero
+                // fill past the end) multiply only the zeros TMA fills in for K.
+                // Pair CTAs signal the even CTA's barrier like the operand boxes.
                 const uint32_t sSF = sA + C::SF_OFF;
                 const int g0 = k0 / sf_atom_kbytes(SF);
                 const int ra = m0 / 128, rb = ti.n_blk * BN / 128;
+                if constexpr (CG == 1)
+                    tma_load_2d(sSF, tmSFA, fb, 0, 2 * (ra * sf_groups + g0));
+                else
+                    tma_load_2d_pair(sSF, tmSFA, fb, 0, 2 * (ra * sf_groups + g0));
 #pragma unroll
-                for (int g = 0; g < C::KGROUPS; ++g) {
-                    // a group past K (the tail of the last stage) multiplies only
-                    // the zeros TMA fills in: any valid atom serves, take the last
-                    const int gg = min(g0 + g, sf_groups - 1);
-                    const int atom_a = ra * sf_groups + gg;
+                for (int h = 0; h < BN / 128; ++h) {
+                    const uint32_t dst = sSF + C::SF_A_BYTES + 512 * C::KGROUPS * h;
                     if constexpr (CG == 1)
-                        tma_load_2d(sSF + 512 * g, tmSFA, fb, 0, 2 * atom_a);
+                        tma_load_2d(dst, tmSFB, fb, 0, 2 * ((rb + h) * sf_groups + g0));
                     else
-                        tma_load_2d_pair(sSF + 512 * g, tmSFA, fb, 0, 2 * atom_a);
-#pragma unroll
-                    for (int h = 0; h < BN / 128; ++h) {
-                        const int atom_b = (rb + h) * sf_groups + gg;
-                        const uint32_t dst = sSF + C::SF_A_BYTES + 512 * (g * (BN / 128) + h);
-                        if constexpr (CG == 1)
-                            tma_load_2d(dst, tmSFB, fb, 0, 2 * atom_b);
-                        else
-                            tma_load_2d_pair(dst, tmSFB, fb, 0, 2 * atom_b);
-                    }
+                        tma_load_2d_pair(dst, tmSFB, fb, 0, 2 * ((rb + h) * sf_groups + g0));
                 }
             }
             ++issued;
@@ -724,7 +720,7 @@ __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uin
 #pragma unroll
                     for (int h = 0; h < BN / 128; ++h)
                         tmem_cp_32x128b_warpx4<CG>(
-                            tg + 4 + 4 * h, make_smem_desc(sSF + C::SF_A_BYTES + 512 * (g * (BN / 128) + h), 128, 128, 0));
+                            tg + 4 + 4 * h, make_smem_desc(sSF + C::SF_A_BYTES + 512 * (C::KGROUPS * h + g), 128, 128, 0));
                 }
                 // each 32-byte K slice (one MMA) reads the atom holding its blocks
                 // and, by its scale factor ID, the first of its bytes in each column

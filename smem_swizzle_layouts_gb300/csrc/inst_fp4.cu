@@ -3,3 +3,5 @@
 
 G300_INSTANTIATE(1, 128, 128, 5, false, 1, 128, 2)
 G300_INSTANTIATE(1, 128, 256, 3, false, 1, 128, 3)
+G300_INSTANTIATE(2, 256, 128, 5, false, 1, 128, 2)
+G300_INSTANTIATE(2, 256, 128, 5, false, 1, 128, 3)

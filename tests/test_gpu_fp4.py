@@ -107,6 +107,19 @@ def test_fp4_stream_k(g, kind):
     run_fp4(g, 700, 300, 1536, kind, seed=17, options=dict(workspace=ws, stream_k=2, max_ctas=5))
 
 
+@pytest.mark.parametrize("kind", ["nvfp4", "mxfp4"])
+@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (700, 600, 1000), (2048, 2048, 512), (300, 130, 96)])
+def test_fp4_cta_pairs(g, kind, M, N, K):
+    # 256 x 256 pair tiles (one accumulator buffer): each CTA holds its A rows' scales
+    # and both B atoms of the tile
+    run_fp4(g, M, N, K, kind, seed=2 * M + K, options=dict(cta_group=2))
+
+
+@pytest.mark.parametrize("kind", ["nvfp4", "mxfp4"])
+def test_fp4_cta_pairs_alpha_beta(g, kind):
+    run_fp4(g, 512, 768, 640, kind, out="bf16", alpha=1.5, beta=-0.5, seed=19, options=dict(cta_group=2))
+
+
 def test_fp4_argument_errors(g):
     M, N, K = 128, 128, 256
     A = torch.zeros(M * K // 2, dtype=torch.uint8, device=DEV)
@@ -117,7 +130,7 @@ def test_fp4_argument_errors(g):
         g.gemm_fp4(M, N, k, A, lda, S, A, lda, S, kind, None, 0, D, N, 0, 1.0, 0.0, options=opts or None)
 
     for kw, status in [(dict(k=255), g.ERR_INVALID_ARG), (dict(kind=2), g.ERR_INVALID_ARG),
-                       (dict(lda=272), g.ERR_ALIGNMENT), (dict(cta_group=2), g.ERR_UNSUPPORTED),
+                       (dict(lda=272), g.ERR_ALIGNMENT), (dict(cta_group=2, tile_n=128), g.ERR_UNSUPPORTED),
                        (dict(block_k=64), g.ERR_UNSUPPORTED)]:
         with pytest.raises(g.GemmError) as ei:
             call(**kw)

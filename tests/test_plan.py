@@ -82,11 +82,17 @@ def test_block_scaled_formats_have_fixed_tiles(g):
                                                     swizzle_b=3, epilogue_swizzle=1, group_m=8)
     assert plan(g, 8192, 8192, 8192, MXFP8, cta_group=2)["tile_n"] == 128
     assert plan(g, 8192, 8192, 8192, MXFP8, cta_group=2, tile_n=256)["tile_n"] == 256
-    assert plan(g, 8192, 8192, 8192, MXFP8, block_k=128)["block_k"] == 128
-    assert plan(g, 8192, 8192, 8192, NVFP4)["block_k"] == 128    # bytes: 256 E2M1 per stage
-    assert plan(g, 8192, 8192, 8192, MXFP4)["block_k"] == 256
-    for kind, opts in [(MXFP8, dict(tile_n=256, cta_group=1)), (NVFP4, dict(cta_group=2)), (MXFP4, dict(block_k=128)),
-                       (NVFP4, dict(tile_m=64))]:
+    # a stage depth only single CTAs are built for keeps large problems on single CTAs
+    assert plan(g, 8192, 8192, 8192, MXFP8, block_k=128)["cta_group"] == 1
+    # fp4 (K in bytes): 256 x 256 pairs by default for large problems, 128 bytes per stage
+    for kind in (NVFP4, MXFP4):
+        p = plan(g, 8192, 8192, 8192, kind)
+        assert (p["cta_group"], p["tile_n"], p["block_k"]) == (2, 256, 128), kind
+    assert plan(g, 1024, 8192, 8192, NVFP4)["block_k"] == 128    # single CTAs: 256 E2M1 per stage
+    assert plan(g, 1024, 8192, 8192, MXFP4)["block_k"] == 256
+    assert plan(g, 1024, 1024, 8192, NVFP4, cta_group=2)["tile_n"] == 256
+    for kind, opts in [(MXFP8, dict(tile_n=256, cta_group=1)), (NVFP4, dict(cta_group=2, tile_n=128)),
+                       (MXFP4, dict(cta_group=1, block_k=128)), (NVFP4, dict(tile_m=64))]:
         with pytest.raises(g.GemmError) as ei:
             plan(g, 4096, 4096, 4096, kind, **opts)
         assert ei.value.status == g.ERR_UNSUPPORTED, (kind, opts)
