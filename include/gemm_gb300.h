@@ -101,7 +101,10 @@ typedef enum {
  *                 operand panel read different parts of it at a time.
  *                 Bit 3 gives the operand loads an L2 evict_last policy and
  *                 the C loads and D stores evict_first (ablation; no
- *                 measured effect at 4096^3 or 8192^3).
+ *                 measured effect at 4096^3 or 8192^3). Bit 4 (single
+ *                 problems with 128-row tiles) reads C from global memory
+ *                 straight into the epilogue's registers instead of staging
+ *                 it in shared memory by TMA (ablation: 1 % slower at 8192^3).
  *   stats         diagnostics: NULL, or device memory of 16 uint64 per CTA
  *                 of the grid (at least 16 * number of SMs), where each CTA
  *                 writes cycles its roles spent waiting (slots 0-1 producer,

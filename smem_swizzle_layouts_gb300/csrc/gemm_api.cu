@@ -273,7 +273,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
     if (opt.cta_group < 0 || opt.cta_group > 2 || opt.tile_n < 0 || opt.swizzle_a < 0 ||
         opt.swizzle_a > 4 || opt.swizzle_b < 0 || opt.swizzle_b > 4 || opt.max_ctas < 0 ||
         opt.group_m < 0 || opt.timeout_ms < 0 || opt.epilogue_swizzle < -1 ||
-        opt.epilogue_swizzle > 1 || opt.flags < 0 || opt.flags > 15 || opt.block_k < 0 ||
+        opt.epilogue_swizzle > 1 || opt.flags < 0 || opt.flags > 31 || opt.block_k < 0 ||
         opt.stream_k < -1 || opt.stream_k > 3)
         return GEMM_ERR_INVALID_ARG;
     if (opt.workspace && (reinterpret_cast<uintptr_t>(opt.workspace) & 255u) != 0)
@@ -535,6 +535,8 @@ gemm_status_t run_single(const InFmt &f, int64_t M, int64_t N, int64_t K, const 
         return GEMM_ERR_UNSUPPORTED;
     p.num_tiles = static_cast<int>(tiles);
     fill_common(p, pl, f, a_mn, b_mn, d_type, alpha, beta, status);
+    p.c_ptr = beta != 0.0f ? C : nullptr;
+    p.ldc = ldc;
     if (f.sf != kScaleNone && K > 0) {
         const int groups = pl.bk / sf_atom_kbytes(f.sf);  // atoms per stage and row block
         if ((s = encode_scales(&la.sfa, sfa, M, K, f.sf, groups)) != GEMM_OK ||

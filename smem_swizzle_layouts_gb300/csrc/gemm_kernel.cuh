@@ -111,6 +111,10 @@ struct KParams {
     // Block-scaled operands: K groups (128 elements) per row block of the
     // scale tensors; atom (i * sf_groups + g) holds row block i, K group g
     int sf_groups;
+    // C of a single problem (row-major, ldc elements per row), for the epilogue
+    // reading it straight into registers (kFlagDirectC)
+    const void *c_ptr;
+    long long ldc;
 };
 
 // Diagnostics: per-CTA counters written when KParams::stats is set.
@@ -136,6 +140,7 @@ enum : int {
     kFlagAllClusterWaits = 2,  // CTA pairs: cluster-scope acquire on every wait (ablation)
     kFlagRotateK = 4,          // start each tile's K loop at a per-cluster offset
     kFlagCacheHints = 8,       // operands evict_last, C loads and D stores evict_first in L2
+    kFlagDirectC = 16,         // single problems, 128-row tiles: C read into registers, not staged
 };
 
 // K block processed at iteration `it` of a tile: with kFlagRotateK the
@@ -817,11 +822,52 @@ struct EpiConst {
     uint32_t key_mask;  // 7 when staging rows are SW128-swizzled, else 0
 };
 
-// One 32-row x 128-byte chunk: fp32 output covers 32 columns, 16-bit output 64.
-// `acc` holds this thread's row (lane) of the chunk in fp32.
+// This thread's 128 bytes of C for one chunk (row `row`, columns col0..),
+// read from global memory into registers: whole 16-byte units inside N,
+// single elements (predicated, fixed indices) at the N edge, zeros past the
+// matrix.
 template <int CW>
+__device__ __forceinline__ void load_c_row(uint32_t (&cr)[32], const void *c_ptr, long long ldc, int row, int col0,
+                                           int M, int N)
+{
+    constexpr int OB = CW == 32 ? 4 : 2;  // output element bytes
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        cr[i] = 0u;
+    if (row >= M)
+        return;
+    const char *rp = static_cast<const char *>(c_ptr) + (static_cast<long long>(row) * ldc + col0) * OB;
+    const int nv = N - col0;  // valid columns of the chunk
+    if (nv >= CW) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const uint4 x = __ldg(reinterpret_cast<const uint4 *>(rp) + u);
+            cr[4 * u] = x.x;
+            cr[4 * u + 1] = x.y;
+            cr[4 * u + 2] = x.z;
+            cr[4 * u + 3] = x.w;
+        }
+    } else if constexpr (OB == 4) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (i < nv)
+                cr[i] = __ldg(reinterpret_cast<const uint32_t *>(rp) + i);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const uint32_t lo = 2 * i < nv ? __ldg(reinterpret_cast<const unsigned short *>(rp) + 2 * i) : 0u;
+            const uint32_t hi = 2 * i + 1 < nv ? __ldg(reinterpret_cast<const unsigned short *>(rp) + 2 * i + 1) : 0u;
+            cr[i] = lo | (hi << 16);
+        }
+    }
+}
+
+// One 32-row x 128-byte chunk: fp32 output covers 32 columns, 16-bit output 64.
+// `acc` holds this thread's row (lane) of the chunk in fp32. C comes from the
+// staging buffer (swizzled like the output), or from `creg` when CREG.
+template <int CW, bool CREG = false>
 __device__ __forceinline__ void epilogue_chunk_math(float (&acc)[CW], const EpiConst &e,
-                                                    uint32_t sbuf, int r, bool use_c)
+                                                    uint32_t sbuf, int r, bool use_c, const uint32_t *creg = nullptr)
 {
     const uint32_t row = sbuf + static_cast<uint32_t>(r) * 128u;
     const uint32_t key = static_cast<uint32_t>(r) & e.key_mask;
@@ -835,7 +881,14 @@ __device__ __forceinline__ void epilogue_chunk_math(float (&acc)[CW], const EpiC
             v[i] *= e.alpha;
         if (use_c) {
             uint32_t c[4];
-            ld_shared_v4(addr, c[0], c[1], c[2], c[3]);
+            if constexpr (CREG) {
+                c[0] = creg[4 * u];
+                c[1] = creg[4 * u + 1];
+                c[2] = creg[4 * u + 2];
+                c[3] = creg[4 * u + 3];
+            } else {
+                ld_shared_v4(addr, c[0], c[1], c[2], c[3]);
+            }
             if constexpr (CW == 32) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
@@ -945,6 +998,11 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
     const uint32_t buf0 = epi_base + static_cast<uint32_t>(ew * C::EPI_BUFS * kEpiBufBytes);
     const uint32_t ebar0 = bar_epi + static_cast<uint32_t>(16 * ew);
     const bool use_c = ec.beta != 0.0f;
+    // C straight into registers: single problems with 128-row tiles (each
+    // thread owns one output row of a chunk)
+    const bool direct_c = use_c && !GROUPED && C::BM == 128 && (p.flags & kFlagDirectC) != 0;
+    const void *const c_ptr = p.c_ptr;
+    const long long ldc = p.ldc;
     // C and D pass through once: let them leave L2 first
     const bool hints = (p.flags & kFlagCacheHints) != 0;
     const uint64_t stream_once = hints ? l2_policy_evict_first() : 0;
@@ -1061,7 +1119,10 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
             if (lane == 0)
                 bulk_wait_group_read<C::EPI_BUFS - 1>();
             __syncwarp();
-            if (use_c && lane == 0) {
+            uint32_t creg[32];
+            if (direct_c)  // issued before the TMEM load so that the two overlap
+                load_c_row<CW>(creg, c_ptr, ldc, m0 + trow, col0, ti.M, ti.N);
+            if (use_c && !direct_c && lane == 0) {
                 fence_proxy_async_smem();
                 mbar_arrive_expect_tx(sbar, R * 128);
                 if (hints)
@@ -1110,7 +1171,7 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
                         v[32 * h + i] += __uint_as_float(r[i]);
                 }
             }
-            if (use_c) {
+            if (use_c && !direct_c) {
                 const long long tw = stats ? clock64() : 0;
                 bool ok = w.wait(sbar, epi_phase[sel], kRoleEpilogue | kWaitEpiC);
                 if (stats)
@@ -1119,7 +1180,9 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
                 if (!__all_sync(0xffffffffu, ok))
                     return;
             }
-            if (active)
+            if (direct_c)
+                epilogue_chunk_math<CW, true>(v, ec, sbuf, trow, true, creg);
+            else if (active)
                 epilogue_chunk_math<CW>(v, ec, sbuf, trow, use_c);
             fence_proxy_async_smem();
             __syncwarp();
