@@ -110,7 +110,8 @@ typedef enum {
  *                 writes cycles its roles spent waiting (slots 0-1 producer,
  *                 2-4 and 8-9 MMA issuer, 5-7 and 10-12 first epilogue warp:
  *                 10-11 stream-K flag waits and partial-sum gathers, 12 the
- *                 cycles after its last accumulator became ready).
+ *                 cycles after its last accumulator became ready; 13 the
+ *                 scale copier of the block-scaled kinds).
  *   stream_k      K-split scheduling of single (not grouped) problems with
  *                 128-row tiles, so that a last, partly filled wave of tiles
  *                 does not leave SMs idle: the tiles of whole waves run one
@@ -373,7 +374,8 @@ gemm_status_t gemm_bf16_grouped_noalloc(const gemm_problem_t *problems, int num_
 /* Synchronises `stream`, reads the device status word of this library,
  * clears it, and returns GEMM_OK or GEMM_ERR_TIMEOUT (GEMM_ERR_CUDA if the
  * read fails). `detail` (may be NULL) receives the raw word: bits 0-7 the
- * role that gave up (1 producer, 2 MMA, 3 epilogue), bits 8-15 the wait. */
+ * role that gave up (1 producer, 2 MMA, 3 epilogue, 4 scale copier of the
+ * block-scaled kinds), bits 8-15 the wait. */
 gemm_status_t gemm_last_device_status(gemm_stream_t stream, uint32_t *detail);
 
 const char *gemm_status_string(gemm_status_t status);

@@ -47,8 +47,10 @@
 
 namespace g300 {
 
-constexpr int kThreads = 192;
 constexpr int kEpiWarps = 4;
+// warp 0 producer, warp 1 MMA issuer, warps 2-5 epilogue, warp 6 scale copier
+constexpr int kSfCopyWarp = 2 + kEpiWarps;
+constexpr int kThreads = 32 * (kSfCopyWarp + 1);
 constexpr int kEpiBufBytes = 32 * 128;  // one 32-row x 128 B staging chunk
 
 // Roles in the status word (bits 0-7) and waits (bits 8-15).
@@ -56,6 +58,7 @@ enum : uint32_t {
     kRoleProducer = 1,
     kRoleMma = 2,
     kRoleEpilogue = 3,
+    kRoleSfCopy = 4,
     kWaitEmpty = 1 << 8,
     kWaitFull = 2 << 8,
     kWaitAccEmpty = 3 << 8,
@@ -64,6 +67,7 @@ enum : uint32_t {
     kWaitInjected = 6 << 8,
     kWaitDrain = 7 << 8,
     kWaitPartial = 8 << 8,
+    kWaitSfReady = 9 << 8,
 };
 
 struct GroupedProblemDev {
@@ -132,6 +136,7 @@ enum : int {
     kStatEpiPartialWaitCycles = 10,  // stream-K head: waiting for contributors' flags
     kStatEpiPartialCycles = 11,      // stream-K head: gathering partial sums into TMEM
     kStatEpiTailCycles = 12,         // from the last accumulator-full wait to the end
+    kStatSfCopyWaitCycles = 13,      // scale copier: waiting for stages to land
     kStatSlots = 16,
 };
 
@@ -192,8 +197,8 @@ struct Cfg {
     static constexpr int EPI_BUFS = SF ? 1 : 2;
     static constexpr int EPI_BYTES = kEpiWarps * EPI_BUFS * kEpiBufBytes;
     static constexpr int BAR_OFF = EPI_OFF + EPI_BYTES;
-    // full[S], empty[S], acc_full[2], acc_empty[2], epi[4][2], drain, inject
-    static constexpr int NUM_BARS = 2 * STAGES + 2 + 2 + 2 * kEpiWarps + 2;
+    // full[S], empty[S], acc_full[2], acc_empty[2], epi[4][2], drain, inject, sf_ready[S]
+    static constexpr int NUM_BARS = 3 * STAGES + 2 + 2 + 2 * kEpiWarps + 2;
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack to align the base
     // TMEM: two accumulators, then (block-scaled) per stage 4 columns of A
@@ -646,9 +651,76 @@ __device__ void role_producer(const KParams &p, const CUtensorMap *tmA, const CU
     }
 }
 
+// Scale copier (block-scaled kinds, warp 6 of the even CTA): for every stage
+// of every unit, in the order the MMA issuer consumes them, waits until the
+// stage has landed, copies its scale atoms from shared memory into the stage's
+// TMEM scale columns (tcgen05.cp, 32x128b.warpx4) and commits to sf_ready of
+// the stage, which arrives once the copies have completed. The MMA issuer
+// waits on sf_ready before the stage's MMAs and so issues only MMAs. A
+// stage's scale columns are rewritten only after the stage was refilled, that
+// is after the MMAs that read their previous contents completed.
+template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF>
+__device__ void role_sf_copy(const KParams &p, uint32_t smem, uint32_t bar_full, uint32_t bar_sf,
+                             uint32_t tmem_base, const Waiter &w)
+{
+    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF>;
+    if constexpr (SF != 0) {
+        if (p.inject_timeout)
+            return;
+        const Sched sched = make_sched(p);
+        unsigned long long *const stats = p.stats;
+        unsigned long long st_wait = 0;
+        const int cluster_id = blockIdx.x / CG, num_clusters = gridDim.x / CG;
+        int stage = 0;
+        uint32_t phase = 0;
+        UnitIter units(sched, cluster_id, num_clusters);
+        Unit u;
+        while (units.next(u)) {
+            TileInfo ti;
+            decode_tile<GROUPED>(sched, u.tile, ti);
+            const int num_kb = ceil_div_i(ti.K, BK);
+            const int kb_lo = u.kb0, kb_hi = u.kb1 < 0 ? num_kb : u.kb1;
+            for (int kb = kb_lo; kb < kb_hi; ++kb) {
+                const long long t0 = stats ? clock64() : 0;
+                if (!w.wait(bar_full + 8 * stage, phase, kRoleSfCopy | kWaitFull))
+                    return;
+                if (stats)
+                    st_wait += static_cast<unsigned long long>(clock64() - t0);
+                tc_fence_after_sync();
+                const uint32_t sSF = smem + stage * C::STAGE_BYTES + C::SF_OFF;
+                const uint32_t tsf = tmem_base + static_cast<uint32_t>(C::SF_COL0 + stage * C::SF_COLS);
+#pragma unroll
+                for (int g = 0; g < C::KGROUPS; ++g) {
+                    const uint32_t tg = tsf + static_cast<uint32_t>(C::SF_GROUP_COLS * g);
+                    tmem_cp_32x128b_warpx4<CG>(tg, make_smem_desc(sSF + 512 * g, 128, 128, 0));
+                    // B scales of columns 128h..128h+127 in the next 4 columns each
+#pragma unroll
+                    for (int h = 0; h < BN / 128; ++h)
+                        tmem_cp_32x128b_warpx4<CG>(
+                            tg + 4 + 4 * h, make_smem_desc(sSF + C::SF_A_BYTES + 512 * (C::KGROUPS * h + g), 128, 128, 0));
+                }
+                mma_commit<CG>(bar_sf + 8 * stage);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (stats)
+            stats[blockIdx.x * kStatSlots + kStatSfCopyWaitCycles] = st_wait;
+    } else {
+        (void)p;
+        (void)smem;
+        (void)bar_full;
+        (void)bar_sf;
+        (void)tmem_base;
+        (void)w;
+    }
+}
+
 template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF>
 __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uint32_t bar_empty,
-                         uint32_t bar_acc_full, uint32_t bar_acc_empty, uint32_t bar_inject,
+                         uint32_t bar_acc_full, uint32_t bar_acc_empty, uint32_t bar_inject, uint32_t bar_sf,
                          uint32_t tmem_base, const Waiter &w)
 {
     using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF>;
@@ -713,20 +785,12 @@ __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uin
             tc_fence_after_sync();
             const uint64_t sdelta = static_cast<uint64_t>((stage * C::STAGE_BYTES) >> 4);
             if constexpr (SF) {
-                // scale atoms -> this stage's TMEM scale columns; the MMAs below
-                // are issued after the copies by this thread and run after them
-                const uint32_t sSF = smem + stage * C::STAGE_BYTES + C::SF_OFF;
+                // the copier warp has put this stage's scale atoms in its TMEM
+                // scale columns; its commit arrives once the copies completed
+                if (!w.wait(bar_sf + 8 * stage, phase, kRoleMma | kWaitSfReady))
+                    return;
+                tc_fence_after_sync();
                 const uint32_t tsf = tmem_base + static_cast<uint32_t>(C::SF_COL0 + stage * C::SF_COLS);
-#pragma unroll
-                for (int g = 0; g < C::KGROUPS; ++g) {
-                    const uint32_t tg = tsf + static_cast<uint32_t>(C::SF_GROUP_COLS * g);
-                    tmem_cp_32x128b_warpx4<CG>(tg, make_smem_desc(sSF + 512 * g, 128, 128, 0));
-                    // B scales of columns 128h..128h+127 in the next 4 columns each
-#pragma unroll
-                    for (int h = 0; h < BN / 128; ++h)
-                        tmem_cp_32x128b_warpx4<CG>(
-                            tg + 4 + 4 * h, make_smem_desc(sSF + C::SF_A_BYTES + 512 * (C::KGROUPS * h + g), 128, 128, 0));
-                }
                 // each 32-byte K slice (one MMA) reads the atom holding its blocks
                 // and, by its scale factor ID, the first of its bytes in each column
                 constexpr int kPerAtom = sf_atom_kbytes(SF) / 32;  // MMAs per atom: 4, 1, 2
@@ -1254,6 +1318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bar_epi = bar_acc_empty + 16;
     const uint32_t bar_drain = bar_epi + 8 * 2 * kEpiWarps;
     const uint32_t bar_inject = bar_drain + 8;
+    const uint32_t bar_sf = bar_inject + 8;  // sf_ready[STAGES]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + C::MISC_OFF + 4);
 
@@ -1270,6 +1335,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar_epi + 8 * i, 1);
         mbar_init(bar_drain, 1);
         mbar_init(bar_inject, 1);
+        for (int s = 0; s < STAGES; ++s)
+            mbar_init(bar_sf + 8 * s, 1);
         *abort_flag = 0u;
         fence_mbar_init();
     }
@@ -1307,12 +1374,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {
             role_mma<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF>(p, stage_base, bar_full, bar_empty,
-                                                  bar_acc_full, bar_acc_empty, bar_inject,
+                                                  bar_acc_full, bar_acc_empty, bar_inject, bar_sf,
                                                   tmem_base, w);
             // every MMA issued by this thread has completed before TMEM is freed
             mma_commit<CG>(bar_drain);
             w.drain(bar_drain, 0u, 100000000ull);
         }
+    } else if (warp == kSfCopyWarp) {
+        // the even CTA copies the scales of both CTAs of a pair (cta_group::2)
+        if (lane == 0 && rank == 0)
+            role_sf_copy<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF>(p, stage_base, bar_full, bar_sf, tmem_base, w);
     } else {
         if (p.out_type == 0)
             role_epilogue<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, 32>(p, &tmC, &tmD, base + C::EPI_OFF,
