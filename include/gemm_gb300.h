@@ -375,7 +375,8 @@ gemm_status_t gemm_bf16_grouped_noalloc(const gemm_problem_t *problems, int num_
  * clears it, and returns GEMM_OK or GEMM_ERR_TIMEOUT (GEMM_ERR_CUDA if the
  * read fails). `detail` (may be NULL) receives the raw word: bits 0-7 the
  * role that gave up (1 producer, 2 MMA, 3 epilogue, 4 scale copier of the
- * block-scaled kinds), bits 8-15 the wait. */
+ * block-scaled kinds, 5 launch setup: 10 in bits 8-15 means the dynamic
+ * shared memory was not 1024-byte aligned), bits 8-15 the wait. */
 gemm_status_t gemm_last_device_status(gemm_stream_t stream, uint32_t *detail);
 
 const char *gemm_status_string(gemm_status_t status);

@@ -328,11 +328,13 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
         // (the default from 2048 rows and columns; MXFP8 8192^3 2588 against
         // 1897 TFLOP/s for single CTAs), single CTAs of 128 x 128, and MXFP8
         // pairs of 256 x 128 (1773). K bytes per stage: MXFP8 256 (single CTAs
-        // also 128), NVFP4 128, MXFP4 256 single and 128 in pairs; the variant
-        // lookup below refuses anything else.
+        // also 128), NVFP4 128, MXFP4 256 (pairs also 128); the variant lookup
+        // below refuses anything else. A 128-byte fp4 stage on a pair holds
+        // four MMAs, less tensor work than the MMA thread needs to issue a
+        // stage, so MXFP4 pairs default to 256 bytes.
         if (opt.tile_m && opt.tile_m != 128)
             return GEMM_ERR_UNSUPPORTED;
-        auto depth = [&](int c) { return sf == kScaleMx8 ? 256 : sf == kScaleNv4 ? 128 : (c == 2 ? 128 : 256); };
+        auto depth = [&](int) { return sf == kScaleNv4 ? 128 : 256; };
         const bool wide = opt.cta_group == 0 && opt.tile_n == 0 && M >= 2048 && N >= 2048;
         cg = opt.cta_group ? opt.cta_group : (wide ? 2 : 1);
         bn = opt.tile_n ? opt.tile_n : (cg == 2 && (wide || sf != kScaleMx8) ? 256 : 128);

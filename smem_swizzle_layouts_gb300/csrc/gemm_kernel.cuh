@@ -68,6 +68,8 @@ enum : uint32_t {
     kWaitDrain = 7 << 8,
     kWaitPartial = 8 << 8,
     kWaitSfReady = 9 << 8,
+    kRoleSetup = 5,
+    kSetupAlignment = 10 << 8,
 };
 
 struct GroupedProblemDev {
@@ -200,7 +202,11 @@ struct Cfg {
     // full[S], empty[S], acc_full[2], acc_empty[2], epi[4][2], drain, inject, sf_ready[S]
     static constexpr int NUM_BARS = 3 * STAGES + 2 + 2 + 2 * kEpiWarps + 2;
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
-    static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack to align the base
+    // + slack to round the base up to 1024 bytes; the dynamic shared memory is
+    // declared 1024-aligned, so a variant that would not fit with the slack
+    // goes without it and checks the alignment at launch instead
+    static constexpr int ALIGN_SLACK = MISC_OFF + 16 + 1024 <= 232448 ? 1024 : 0;
+    static constexpr int SMEM_BYTES = MISC_OFF + 16 + ALIGN_SLACK;
     // TMEM: two accumulators, then (block-scaled) per stage 4 columns of A
     // scales and 4 of B scales for each K group
     // Accumulator buffers: two (the epilogue of one tile overlaps the next
@@ -1302,6 +1308,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
+    if (C::ALIGN_SLACK == 0 && (raw & 1023u) != 0u) {
+        // no room to round the base up: report and leave before any setup
+        if (threadIdx.x == 0)
+            atomicCAS(p.status, 0u, kRoleSetup | kSetupAlignment);
+        return;
+    }
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *smem = smem_raw + (base - raw);
 

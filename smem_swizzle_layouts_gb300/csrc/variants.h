@@ -47,6 +47,7 @@ cudaError_t resident_ctas(int *ctas);
     X(1, 128, 128, 5, false, 1, 128, 2) \
     X(1, 128, 256, 3, false, 1, 128, 3) \
     X(2, 256, 128, 5, false, 1, 128, 2) \
-    X(2, 256, 128, 5, false, 1, 128, 3)
+    X(2, 256, 128, 5, false, 1, 128, 3) \
+    X(2, 256, 256, 3, false, 1, 128, 3)
 
 }  // namespace g300

@@ -115,6 +115,12 @@ def test_fp4_cta_pairs(g, kind, M, N, K):
     run_fp4(g, M, N, K, kind, seed=2 * M + K, options=dict(cta_group=2))
 
 
+@pytest.mark.parametrize("M,N,K", [(512, 512, 1024), (700, 600, 1000)])
+def test_mxfp4_pairs_128_byte_stages(g, M, N, K):
+    # MXFP4 pairs default to 256 bytes of K per stage; 128-byte stages stay available
+    run_fp4(g, M, N, K, "mxfp4", seed=3 * M + K, options=dict(cta_group=2, block_k=128))
+
+
 @pytest.mark.parametrize("kind", ["nvfp4", "mxfp4"])
 def test_fp4_cta_pairs_alpha_beta(g, kind):
     run_fp4(g, 512, 768, 640, kind, out="bf16", alpha=1.5, beta=-0.5, seed=19, options=dict(cta_group=2))

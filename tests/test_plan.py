@@ -84,10 +84,13 @@ def test_block_scaled_formats_have_fixed_tiles(g):
     assert plan(g, 8192, 8192, 8192, MXFP8, cta_group=2, tile_n=256)["tile_n"] == 256
     # a stage depth only single CTAs are built for keeps large problems on single CTAs
     assert plan(g, 8192, 8192, 8192, MXFP8, block_k=128)["cta_group"] == 1
-    # fp4 (K in bytes): 256 x 256 pairs by default for large problems, 128 bytes per stage
-    for kind in (NVFP4, MXFP4):
+    # fp4 (K in bytes): 256 x 256 pairs by default for large problems, 128 bytes per
+    # stage for NVFP4 and 256 for MXFP4 (a pair stage of four MMAs issues too slowly);
+    # MXFP4 pairs also run 128-byte stages when asked
+    for kind, bk in ((NVFP4, 128), (MXFP4, 256)):
         p = plan(g, 8192, 8192, 8192, kind)
-        assert (p["cta_group"], p["tile_n"], p["block_k"]) == (2, 256, 128), kind
+        assert (p["cta_group"], p["tile_n"], p["block_k"]) == (2, 256, bk), kind
+    assert plan(g, 8192, 8192, 8192, MXFP4, block_k=128)["block_k"] == 128
     assert plan(g, 1024, 8192, 8192, NVFP4)["block_k"] == 128    # single CTAs: 256 E2M1 per stage
     assert plan(g, 1024, 8192, 8192, MXFP4)["block_k"] == 256
     assert plan(g, 1024, 1024, 8192, NVFP4, cta_group=2)["tile_n"] == 256
@@ -99,7 +102,7 @@ def test_block_scaled_formats_have_fixed_tiles(g):
 
 
 def test_invalid_options_are_rejected(g):
-    for opts, status in [(dict(flags=16), g.ERR_INVALID_ARG), (dict(stream_k=4), g.ERR_INVALID_ARG),
+    for opts, status in [(dict(flags=32), g.ERR_INVALID_ARG), (dict(stream_k=4), g.ERR_INVALID_ARG),
                          (dict(swizzle_a=5), g.ERR_INVALID_ARG), (dict(tile_m=96), g.ERR_INVALID_ARG),
                          (dict(workspace=0x1010), g.ERR_ALIGNMENT), (dict(tile_n=96), g.ERR_UNSUPPORTED)]:
         with pytest.raises(g.GemmError) as ei:
