@@ -1179,6 +1179,77 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
             }
             continue;
         }
+        if constexpr (C::ACC_BUFS == 1 && C::BM == 128 && CW == 64) {
+            if (has_acc && !use_c && !head) {
+                // One accumulator buffer, 16-bit output, no C: read the whole row
+                // and round it in registers first, then release the accumulator,
+                // so that the next tile's MMAs run while the stores drain.
+                constexpr int NCH = BN / CW;
+                uint32_t pk[NCH][32];
+#pragma unroll
+                for (int c = 0; c < NCH; ++c) {
+                    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(c * CW);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t r[32];
+                        tmem_ld_32x32b_x32(taddr + 32 * h, r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            float v[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                v[i] = ec.alpha * __uint_as_float(r[8 * u + i]);
+                            uint32_t o[4];
+                            pack_out(v, ec.out_type, o);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                pk[c][16 * h + 4 * u + i] = o[i];
+                        }
+                    }
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) {
+                    if constexpr (CG == 2)
+                        mbar_arrive_cluster(acc_empty_target + 8 * acc);
+                    else
+                        mbar_arrive(bar_acc_empty + 8 * acc);
+                }
+                if (++acc == C::ACC_BUFS) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+                const uint32_t key = static_cast<uint32_t>(trow) & ec.key_mask;
+#pragma unroll
+                for (int c = 0; c < NCH; ++c) {
+                    const int col0 = ti.n_blk * BN + c * CW;
+                    if (col0 >= ti.N)
+                        break;
+                    const uint32_t sbuf = buf0 + static_cast<uint32_t>(sel * kEpiBufBytes);
+                    if (lane == 0)
+                        bulk_wait_group_read<C::EPI_BUFS - 1>();
+                    __syncwarp();
+                    const uint32_t row = sbuf + static_cast<uint32_t>(trow) * 128u;
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        st_shared_v4(row + ((static_cast<uint32_t>(u) ^ key) << 4), pk[c][4 * u], pk[c][4 * u + 1],
+                                     pk[c][4 * u + 2], pk[c][4 * u + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (hints)
+                            tma_store_2d_hint(mD, sbuf, col0, m0, stream_once);
+                        else
+                            tma_store_2d(mD, sbuf, col0, m0);
+                        bulk_commit_group();
+                    }
+                    if constexpr (C::EPI_BUFS == 2)
+                        sel ^= 1;
+                }
+                continue;
+            }
+        }
         for (int c = 0; c < BN / CW; ++c) {
             const int col0 = ti.n_blk * BN + c * CW;
             if (col0 >= ti.N)

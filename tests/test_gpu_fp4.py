@@ -115,6 +115,16 @@ def test_fp4_cta_pairs(g, kind, M, N, K):
     run_fp4(g, M, N, K, kind, seed=2 * M + K, options=dict(cta_group=2))
 
 
+@pytest.mark.parametrize("kind", ["nvfp4", "mxfp4"])
+@pytest.mark.parametrize("out", ["bf16", "f16"])
+@pytest.mark.parametrize("M,N,K", [(512, 520, 512), (700, 600, 1000), (2048, 2048, 256)])
+def test_fp4_pairs_16bit_out_without_c(g, kind, out, M, N, K):
+    # one-accumulator pair tiles with 16-bit output and no C read the whole
+    # accumulator row before storing: ragged N chunks, rows past M, and several
+    # tiles per cluster (grid capped at four clusters)
+    run_fp4(g, M, N, K, kind, out=out, alpha=0.75, seed=M + 7 * K, options=dict(cta_group=2, max_ctas=8))
+
+
 @pytest.mark.parametrize("M,N,K", [(512, 512, 1024), (700, 600, 1000)])
 def test_mxfp4_pairs_128_byte_stages(g, M, N, K):
     # MXFP4 pairs default to 256 bytes of K per stage; 128-byte stages stay available

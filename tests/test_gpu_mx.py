@@ -161,6 +161,16 @@ def test_mx_wide_pairs_majors_formats_and_tolerance(g):
            options=dict(cta_group=2, tile_n=256))
 
 
+@pytest.mark.parametrize("out", ["bf16", "f16"])
+@pytest.mark.parametrize("M,N,K", [(512, 520, 512), (700, 600, 1000), (2048, 2048, 256)])
+def test_mx_wide_pairs_16bit_out_without_c(g, out, M, N, K):
+    # one-accumulator pair tiles, 16-bit output, no C: the epilogue reads the whole
+    # accumulator row before its stores (ragged N chunks, rows past M, several
+    # tiles per cluster with the grid capped at four clusters)
+    run_mx(g, M, N, K, out=out, alpha=0.75, exact=True, seed=11 * M + K,
+           options=dict(cta_group=2, tile_n=256, max_ctas=8))
+
+
 def test_mx_wide_pairs_ignore_stream_k(g):
     # no spare accumulator buffer: the split is not applied, the result is unchanged
     ws = torch.zeros(g.gemm_streamk_workspace_size(), dtype=torch.uint8, device=DEV)
