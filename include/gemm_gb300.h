@@ -111,7 +111,8 @@ typedef enum {
  *                 2-4 and 8-9 MMA issuer, 5-7 and 10-12 first epilogue warp:
  *                 10-11 stream-K flag waits and partial-sum gathers, 12 the
  *                 cycles after its last accumulator became ready; 13 the
- *                 scale copier of the block-scaled kinds).
+ *                 scale copier of the block-scaled kinds, 14 the MMA issuer
+ *                 waiting for a stage's scales).
  *   stream_k      K-split scheduling of single (not grouped) problems with
  *                 128-row tiles, so that a last, partly filled wave of tiles
  *                 does not leave SMs idle: the tiles of whole waves run one

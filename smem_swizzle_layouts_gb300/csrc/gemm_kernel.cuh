@@ -139,6 +139,7 @@ enum : int {
     kStatEpiPartialCycles = 11,      // stream-K head: gathering partial sums into TMEM
     kStatEpiTailCycles = 12,         // from the last accumulator-full wait to the end
     kStatSfCopyWaitCycles = 13,      // scale copier: waiting for stages to land
+    kStatMmaSfWaitCycles = 14,       // MMA issuer: waiting for a stage's scales in TMEM
     kStatSlots = 16,
 };
 
@@ -755,7 +756,7 @@ __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uin
     uint32_t phase = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
-    unsigned long long st_full = 0, st_acc = 0, st_blocked = 0, st_tiles = 0;
+    unsigned long long st_full = 0, st_acc = 0, st_blocked = 0, st_tiles = 0, st_sf = 0;
     const long long t_start = clock64();
     UnitIter units(sched, cluster_id, num_clusters);
     Unit u;
@@ -793,8 +794,11 @@ __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uin
             if constexpr (SF) {
                 // the copier warp has put this stage's scale atoms in its TMEM
                 // scale columns; its commit arrives once the copies completed
+                const long long t0 = stats ? clock64() : 0;
                 if (!w.wait(bar_sf + 8 * stage, phase, kRoleMma | kWaitSfReady))
                     return;
+                if (stats)
+                    st_sf += static_cast<unsigned long long>(clock64() - t0);
                 tc_fence_after_sync();
                 const uint32_t tsf = tmem_base + static_cast<uint32_t>(C::SF_COL0 + stage * C::SF_COLS);
                 // each 32-byte K slice (one MMA) reads the atom holding its blocks
@@ -844,6 +848,7 @@ __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uin
         o[kStatMmaLoopCycles] = static_cast<unsigned long long>(clock64() - t_start);
         o[kStatMmaFullBlocked] = st_blocked;
         o[kStatTiles] = st_tiles;
+        o[kStatMmaSfWaitCycles] = st_sf;
     }
 }
 
