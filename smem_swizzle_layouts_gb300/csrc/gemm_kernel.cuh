@@ -48,9 +48,8 @@
 namespace g300 {
 
 constexpr int kEpiWarps = 4;
-// warp 0 producer, warp 1 MMA issuer, warps 2-5 epilogue, warp 6 scale copier
+// warp 0 producer, warp 1 MMA issuer, warps 2-5 epilogue, warp 6 scale copier (block-scaled only)
 constexpr int kSfCopyWarp = 2 + kEpiWarps;
-constexpr int kThreads = 32 * (kSfCopyWarp + 1);
 constexpr int kEpiBufBytes = 32 * 128;  // one 32-row x 128 B staging chunk
 
 // Roles in the status word (bits 0-7) and waits (bits 8-15).
@@ -202,6 +201,8 @@ struct Cfg {
     static constexpr int BAR_OFF = EPI_OFF + EPI_BYTES;
     // full[S], empty[S], acc_full[2], acc_empty[2], epi[4][2], drain, inject, sf_ready[S]
     static constexpr int NUM_BARS = 3 * STAGES + 2 + 2 + 2 * kEpiWarps + 2;
+    // threads per CTA: the scale copier warp exists only for block-scaled kinds
+    static constexpr int THREADS = 32 * (kSfCopyWarp + (SF ? 1 : 0));
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     // + slack to round the base up to 1024 bytes; the dynamic shared memory is
     // declared 1024-aligned, so a variant that would not fit with the slack
@@ -1373,7 +1374,7 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
 // ---------------------------------------------------------------- kernel
 
 template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF>::THREADS, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC,
