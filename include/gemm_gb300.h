@@ -53,7 +53,7 @@ typedef enum {
     GEMM_OK = 0,
     GEMM_ERR_INVALID_ARG = 1,        /* bad size, pointer, enum or option */
     GEMM_ERR_ALIGNMENT = 2,          /* pointer or leading dimension breaks a TMA rule */
-    GEMM_ERR_UNSUPPORTED = 3,        /* valid request this build does not implement */
+    GEMM_ERR_UNSUPPORTED = 3,        /* valid request no compiled kernel variant implements */
     GEMM_ERR_CUDA = 4,               /* a CUDA runtime/driver call failed */
     GEMM_ERR_TIMEOUT = 5             /* a bounded device wait ran out */
 } gemm_status_t;

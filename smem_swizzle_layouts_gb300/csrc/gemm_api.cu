@@ -263,7 +263,7 @@ struct Plan {
 int swz_bits_of(int opt) { return opt == GEMM_SWIZZLE_NONE ? 0 : opt; }
 
 // Choose the tile configuration; fills `plan` or returns an error for options
-// this build cannot honour.
+// the compiled kernel variants cannot honour.
 gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int sms,
                         const gemm_options_t *o, bool grouped, Plan *plan, int esize = 2, int sf = kScaleNone)
 {
