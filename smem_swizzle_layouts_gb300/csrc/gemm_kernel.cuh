@@ -202,7 +202,9 @@ struct Cfg {
     // full[S], empty[S], acc_full[2], acc_empty[2], epi[4][2], drain, inject, sf_ready[S]
     static constexpr int NUM_BARS = 3 * STAGES + 2 + 2 + 2 * kEpiWarps + 2;
     // threads per CTA: the scale copier warp exists only for block-scaled kinds
-    static constexpr int THREADS = 32 * (kSfCopyWarp + (SF ? 1 : 0));
+    // scale copier warps: NVFP4 stages carry three times the atoms of the others
+    static constexpr int SF_COPIERS = SF == kScaleNv4 ? 2 : SF ? 1 : 0;
+    static constexpr int THREADS = 32 * (kSfCopyWarp + SF_COPIERS);
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     // + slack to round the base up to 1024 bytes; the dynamic shared memory is
     // declared 1024-aligned, so a variant that would not fit with the slack
@@ -669,7 +671,7 @@ __device__ void role_producer(const KParams &p, const CUtensorMap *tmA, const CU
 // is after the MMAs that read their previous contents completed.
 template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF>
 __device__ void role_sf_copy(const KParams &p, uint32_t smem, uint32_t bar_full, uint32_t bar_sf,
-                             uint32_t tmem_base, const Waiter &w)
+                             uint32_t tmem_base, const Waiter &w, int copier)
 {
     using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF>;
     if constexpr (SF != 0) {
@@ -697,8 +699,11 @@ __device__ void role_sf_copy(const KParams &p, uint32_t smem, uint32_t bar_full,
                 tc_fence_after_sync();
                 const uint32_t sSF = smem + stage * C::STAGE_BYTES + C::SF_OFF;
                 const uint32_t tsf = tmem_base + static_cast<uint32_t>(C::SF_COL0 + stage * C::SF_COLS);
+                // with several copiers, copier c takes the K groups g = c mod copiers
 #pragma unroll
                 for (int g = 0; g < C::KGROUPS; ++g) {
+                    if (g % C::SF_COPIERS != copier)
+                        continue;
                     const uint32_t tg = tsf + static_cast<uint32_t>(C::SF_GROUP_COLS * g);
                     tmem_cp_32x128b_warpx4<CG>(tg, make_smem_desc(sSF + 512 * g, 128, 128, 0));
                     // B scales of columns 128h..128h+127 in the next 4 columns each
@@ -714,7 +719,7 @@ __device__ void role_sf_copy(const KParams &p, uint32_t smem, uint32_t bar_full,
                 }
             }
         }
-        if (stats)
+        if (stats && copier == 0)
             stats[blockIdx.x * kStatSlots + kStatSfCopyWaitCycles] = st_wait;
     } else {
         (void)p;
@@ -723,6 +728,7 @@ __device__ void role_sf_copy(const KParams &p, uint32_t smem, uint32_t bar_full,
         (void)bar_sf;
         (void)tmem_base;
         (void)w;
+        (void)copier;
     }
 }
 
@@ -787,7 +793,8 @@ __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uin
                     return;
                 st_full += static_cast<unsigned long long>(clock64() - t0);
                 st_blocked += ready ? 0 : 1;
-            } else if (!w.wait(bar_full + 8 * stage, phase, kRoleMma | kWaitFull)) {
+            } else if (!mbar_try_wait(bar_full + 8 * stage, phase) &&
+                       !w.wait(bar_full + 8 * stage, phase, kRoleMma | kWaitFull)) {
                 return;
             }
             tc_fence_after_sync();
@@ -796,7 +803,8 @@ __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uin
                 // the copier warp has put this stage's scale atoms in its TMEM
                 // scale columns; its commit arrives once the copies completed
                 const long long t0 = stats ? clock64() : 0;
-                if (!w.wait(bar_sf + 8 * stage, phase, kRoleMma | kWaitSfReady))
+                if (!mbar_try_wait(bar_sf + 8 * stage, phase) &&
+                    !w.wait(bar_sf + 8 * stage, phase, kRoleMma | kWaitSfReady))
                     return;
                 if (stats)
                     st_sf += static_cast<unsigned long long>(clock64() - t0);
@@ -1425,7 +1433,7 @@ __global__ void __launch_bounds__(Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF>::THREA
         mbar_init(bar_drain, 1);
         mbar_init(bar_inject, 1);
         for (int s = 0; s < STAGES; ++s)
-            mbar_init(bar_sf + 8 * s, 1);
+            mbar_init(bar_sf + 8 * s, C::SF_COPIERS > 0 ? C::SF_COPIERS : 1);
         *abort_flag = 0u;
         fence_mbar_init();
     }
@@ -1469,10 +1477,11 @@ __global__ void __launch_bounds__(Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF>::THREA
             mma_commit<CG>(bar_drain);
             w.drain(bar_drain, 0u, 100000000ull);
         }
-    } else if (warp == kSfCopyWarp) {
+    } else if (warp >= kSfCopyWarp) {
         // the even CTA copies the scales of both CTAs of a pair (cta_group::2)
         if (lane == 0 && rank == 0)
-            role_sf_copy<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF>(p, stage_base, bar_full, bar_sf, tmem_base, w);
+            role_sf_copy<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF>(p, stage_base, bar_full, bar_sf, tmem_base, w,
+                                                                    warp - kSfCopyWarp);
     } else {
         if (p.out_type == 0)
             role_epilogue<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, 32>(p, &tmC, &tmD, base + C::EPI_OFF,
