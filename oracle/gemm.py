@@ -75,6 +75,10 @@ def _load():
                                             ctypes.c_int, vp, ctypes.c_int, i64, ctypes.c_double, ctypes.c_double,
                                             dp, dp, ctypes.c_int]
             lib.oracle_gemm_fp4.restype = ctypes.c_int
+            lib.oracle_gemm_fp4_entries.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, ctypes.c_int,
+                                                    ctypes.c_int, vp, ctypes.c_int, i64, ctypes.c_double,
+                                                    ctypes.c_double, i64, vp, vp, dp, dp, ctypes.c_int]
+            lib.oracle_gemm_fp4_entries.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -210,6 +214,32 @@ def gemm_fp4(M, N, K, A, B, SA, SB, *, block, scale="ue4m3", lda=None, ldb=None,
                              float(beta), _ptr(D), _ptr(S), int(threads))
     if rc:
         raise ValueError("oracle_gemm_fp4 rejected its arguments")
+    return D, S
+
+
+def gemm_fp4_entries(M, N, K, A, B, SA, SB, rows, cols, *, block, scale="ue4m3", lda=None, ldb=None, C=None,
+                     c_fmt="f32", ldc=None, alpha=1.0, beta=0.0, threads=0):
+    """The block-scaled fp4 product of ``gemm_fp4`` at the listed entries (rows[e], cols[e]) only."""
+    lib = _load()
+    A = np.ascontiguousarray(A, dtype=np.uint8)
+    B = np.ascontiguousarray(B, dtype=np.uint8)
+    SA = np.ascontiguousarray(SA, dtype=np.uint8)
+    SB = np.ascontiguousarray(SB, dtype=np.uint8)
+    lda = lda if lda is not None else K
+    ldb = ldb if ldb is not None else K
+    if C is not None:
+        C = np.ascontiguousarray(C)
+        ldc = ldc if ldc is not None else N
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    cols = np.ascontiguousarray(cols, dtype=np.int64)
+    D = np.empty(rows.size, dtype=np.float64)
+    S = np.empty(rows.size, dtype=np.float64)
+    rc = lib.oracle_gemm_fp4_entries(M, N, K, _ptr(A), lda, _ptr(SA), SA.shape[1], _ptr(B), ldb, _ptr(SB),
+                                     SB.shape[1], int(block), 1 if scale == "e8m0" else 0, _ptr(C), FMT[c_fmt],
+                                     ldc or 0, float(alpha), float(beta), rows.size, _ptr(rows), _ptr(cols),
+                                     _ptr(D), _ptr(S), int(threads))
+    if rc:
+        raise ValueError("oracle_gemm_fp4_entries: bad arguments")
     return D, S
 
 

@@ -418,6 +418,49 @@ int oracle_gemm_fp4(int64_t M, int64_t N, int64_t K,
     return 0;
 }
 
+/* The block-scaled fp4 product of oracle_gemm_fp4 at the listed entries only
+ * (rows[e], cols[e]), for sampled checks of problems too large to evaluate
+ * whole; the same sum over k in the same order. */
+int oracle_gemm_fp4_entries(int64_t M, int64_t N, int64_t K,
+                            const uint8_t *A, int64_t lda, const uint8_t *sa, int64_t ldsa,
+                            const uint8_t *B, int64_t ldb, const uint8_t *sb, int64_t ldsb,
+                            int block, int scale_e8m0,
+                            const void *C, int c_fmt, int64_t ldc,
+                            double alpha, double beta,
+                            int64_t n_entries, const int64_t *rows, const int64_t *cols,
+                            double *D, double *S, int nthreads)
+{
+    if (M < 0 || N < 0 || K < 0 || (block != 16 && block != 32) || (lda & 1) || (ldb & 1) ||
+        ldsa < (K + block - 1) / block || ldsb < (K + block - 1) / block || n_entries < 0)
+        return 1;
+    for (int64_t e = 0; e < n_entries; ++e)
+        if (rows[e] < 0 || rows[e] >= M || cols[e] < 0 || cols[e] >= N)
+            return 1;
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    int64_t e;
+#pragma omp parallel for schedule(dynamic, 16)
+    for (e = 0; e < n_entries; ++e) {
+        const int64_t i = rows[e], j = cols[e];
+        double acc = 0.0, sab = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double p = (fp4_scale(sa, ldsa, i, k / block, scale_e8m0) * fp4_at(A, lda, i, k)) *
+                       (fp4_scale(sb, ldsb, j, k / block, scale_e8m0) * fp4_at(B, ldb, j, k));
+            acc += p;
+            sab += fabs(p);
+        }
+        double c = (beta != 0.0 && C) ? load(C, c_fmt, i * ldc + j) : 0.0;
+        D[e] = alpha * acc + beta * c;
+        if (S)
+            S[e] = fabs(alpha) * sab + fabs(beta * c);
+    }
+    return 0;
+}
+
 /*
  * Round-to-nearest-even of x to a binary format with p significand bits
  * (hidden bit included), minimum normal exponent emin and maximum exponent

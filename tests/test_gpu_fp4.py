@@ -11,6 +11,7 @@ import pytest
 
 import seeded_inputs as si
 from oracle import gemm as og
+from test_gpu_parity import sample_entries
 
 torch = pytest.importorskip("torch")
 
@@ -152,3 +153,40 @@ def test_fp4_argument_errors(g):
             call(**kw)
         assert ei.value.status == status, kw
     assert g.gemm_fp4_scale_bytes(300, 600, 0) == 3 * 10 * 512 and g.gemm_fp4_scale_bytes(300, 600, 1) == 3 * 5 * 512
+
+
+@pytest.fixture(scope="module")
+def fp4_full_operands():
+    # 8192 x 8192 packed E2M1 operands, all sixteen codes, shared by both kinds
+    M = N = K = 8192
+    return M, N, K, si.pack_fp4(si.fp4_codes(60, M, K)), si.pack_fp4(si.fp4_codes(61, N, K))
+
+
+@pytest.mark.parametrize("kind", ["nvfp4", "mxfp4"])
+def test_fp4_full_size_bench_launch(g, fp4_full_operands, kind):
+    # 8192^3 in the launch bench.py times (default options: 256 x 256 CTA pairs, one
+    # accumulator, copier warps, early accumulator release) on its input recipe;
+    # sampled entries against the oracle within the fp32-accumulation tolerance
+    M, N, K, A, B = fp4_full_operands
+    code, block, scale = KINDS[kind]
+    nb = K // block
+    if scale == "ue4m3":
+        z = si.scale_codes(62, M + N, nb, 0, len(UE4M3_POOL) - 1)
+        sa, sb = UE4M3_POOL[z[:M]], UE4M3_POOL[z[M:]]
+    else:
+        sa, sb = si.scale_codes(62, M, nb), si.scale_codes(63, N, nb)
+    fill = 0x38 if scale == "ue4m3" else 127
+    SA = torch.from_numpy(si.mx_scale_atoms(sa, M, K, block, fill)).to(DEV)
+    SB = torch.from_numpy(si.mx_scale_atoms(sb, N, K, block, fill)).to(DEV)
+    At = torch.from_numpy(A.reshape(-1).copy()).to(DEV)
+    Bt = torch.from_numpy(B.reshape(-1).copy()).to(DEV)
+    Dt = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=DEV)
+    g.gemm_fp4(M, N, K, At, K, SA, Bt, K, SB, code, None, 0, Dt, N, OUT["bf16"], 1.0, 0.0)
+    st, word = g.gemm_last_device_status()
+    assert st == g.OK, f"device status word {word:#x}"
+    rows, cols = sample_entries(M, N, n=1024, seed=60 + code)
+    ref, S = og.gemm_fp4_entries(M, N, K, A, B, sa, sb, rows, cols, block=block, scale=scale)
+    got = si.bits_to_float64(_out_bits(Dt, "bf16")[rows, cols], "bf16")
+    err = np.abs(got - ref)
+    bad = err > og.tolerance(S, ref, "bf16")
+    assert not bad.any(), f"{int(bad.sum())} of {rows.size} sampled entries outside tolerance"

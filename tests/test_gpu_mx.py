@@ -11,6 +11,7 @@ import pytest
 
 import seeded_inputs as si
 from oracle import gemm as og
+from test_gpu_parity import sample_entries
 
 torch = pytest.importorskip("torch")
 
@@ -189,6 +190,14 @@ def test_mx_large_sampled(g):
     rows = np.concatenate([rng.integers(0, M, 2048), [0, 127, 128, M - 1]])
     cols = np.concatenate([rng.integers(0, N, 2048), [0, 127, 128, N - 1]])
     run_mx(g, M, N, K, dist="normal", out="bf16", seed=23, sample=(rows, cols))
+
+
+def test_mx_full_size_bench_launch(g):
+    # 8192^3 in the launch bench.py times (default options: 256 x 256 CTA pairs with
+    # one accumulator, copier warp, early accumulator release) on its input recipe
+    M = N = K = 8192
+    rows, cols = sample_entries(M, N, n=1024, seed=50)
+    run_mx(g, M, N, K, dist="uniform", out="bf16", seed=50, sample=(rows, cols))
 
 
 def test_mx_argument_errors(g):

@@ -320,6 +320,15 @@ def test_config2_square_4096_bf16_out(g):
              options=dict(cta_group=1, tile_n=256), sample=sample_entries(M, N))
 
 
+def test_config2_square_4096_bench_launch_with_streamk(g):
+    # the launch bench.py times: single CTAs of 128 x 256 with a stream-K workspace,
+    # so the ragged fourth wave of 512 tiles is split across the grid
+    M = N = K = 4096
+    ws = torch.zeros(g.gemm_streamk_workspace_size(), dtype=torch.uint8, device=DEV)
+    run_case(g, M, N, K, a_major="K", b_major="K", out="bf16", dist="normal", scale=0.1, seed=10,
+             options=dict(cta_group=1, tile_n=256, workspace=ws), sample=sample_entries(M, N, n=1024, seed=7))
+
+
 def test_config3_square_8192_pair_fp32_beta(g):
     M = N = K = 8192
     run_case(g, M, N, K, a_major="K", b_major="MN", out="f32", alpha=1.0, beta=1.0, dist="uniform", seed=20,

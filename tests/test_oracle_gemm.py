@@ -395,3 +395,40 @@ def test_fp4_block_size_matters():
     D16u, _ = G.gemm_fp4(M, N, K, si.pack_fp4(ca), si.pack_fp4(cb), np.full((M, 4), 0x38, np.uint8),
                          np.full((N, 4), 0x38, np.uint8), block=16)
     assert not np.array_equal(D16, D16u)
+
+
+@pytest.mark.parametrize("block,scale", [(16, "ue4m3"), (32, "e8m0")])
+def test_fp4_entries_are_the_exact_scaled_product(block, scale):
+    # the per-entry form (for sampled checks of large problems) against the exact
+    # block-scaled sum written out with numpy, with a padded lda, a K that ends
+    # inside a scale block, and beta * C; and equal to the whole-matrix form
+    M, N, K, lda = 9, 14, 200, 224
+    ca = np.zeros((M, lda), np.uint8)
+    ca[:, :K] = si.fp4_codes(121, M, K)
+    cb = si.fp4_codes(122, N, K)
+    nb = (K + block - 1) // block
+    rng = np.random.default_rng(123)
+    if scale == "ue4m3":
+        pool = np.array([(e << 3) | m for e in (5, 6, 7, 8, 9) for m in (0, 4)], np.uint8)
+        sa, sb = rng.choice(pool, (M, nb)), rng.choice(pool, (N, nb))
+        dec = lambda c: np.array([[2.0 ** (int(x) // 8 - 7) * (1 + (int(x) % 8) / 8) for x in r] for r in c])
+    else:
+        sa, sb = si.scale_codes(124, M, nb), si.scale_codes(125, N, nb)
+        dec = lambda c: np.exp2(c.astype(np.float64) - 127.0)
+    C = (rng.integers(-8, 9, (M, N)) * 0.25).astype(np.float32)
+    rows = np.array([0, 8, 3, 5, 8, 0])
+    cols = np.array([0, 13, 7, 2, 0, 13])
+    A, B = si.pack_fp4(ca), si.pack_fp4(cb)
+    D, S = G.gemm_fp4_entries(M, N, K, A, B, sa, sb, rows, cols, block=block, scale=scale, lda=lda, C=C,
+                              c_fmt="f32", alpha=0.5, beta=-2.0)
+    table = np.array(E2M1_TABLE + [-v for v in E2M1_TABLE])
+    a, b = table[ca[:, :K]], table[cb]
+    exact = np.zeros((M, N))
+    for blk in range(nb):
+        s = slice(block * blk, min(K, block * blk + block))
+        exact += dec(sa)[:, blk:blk + 1] * (a[:, s] @ b[:, s].T) * dec(sb)[:, blk][None, :]
+    ref = 0.5 * exact - 2.0 * C.astype(np.float64)
+    assert np.array_equal(D, ref[rows, cols])
+    Dfull, Sfull = G.gemm_fp4(M, N, K, A, B, sa, sb, block=block, scale=scale, lda=lda, C=C, c_fmt="f32",
+                              alpha=0.5, beta=-2.0)
+    assert np.array_equal(D, Dfull[rows, cols]) and np.array_equal(S, Sfull[rows, cols])
