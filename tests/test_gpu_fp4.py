@@ -190,3 +190,25 @@ def test_fp4_full_size_bench_launch(g, fp4_full_operands, kind):
     err = np.abs(got - ref)
     bad = err > og.tolerance(S, ref, "bf16")
     assert not bad.any(), f"{int(bad.sum())} of {rows.size} sampled entries outside tolerance"
+
+
+@pytest.mark.parametrize("kind,options", [("nvfp4", dict(cta_group=2, tile_n=256)), ("nvfp4", dict(cta_group=1)),
+                                          ("mxfp4", dict(cta_group=2, tile_n=256))])
+def test_fp4_injected_wait_times_out_and_the_context_survives(g, kind, options):
+    # the block-scaled kernels add scale copier warps: a wait that nothing satisfies
+    # must still end every role within its bound, report the status, and leave the
+    # context usable
+    code, block, scale = KINDS[kind]
+    M = N = 512
+    K = 512
+    fill = 0x38 if scale == "ue4m3" else 127
+    A = torch.zeros(M * K // 2, dtype=torch.uint8, device=DEV)
+    B = torch.zeros(N * K // 2, dtype=torch.uint8, device=DEV)
+    SA = torch.full((g.gemm_fp4_scale_bytes(M, K, code),), fill, dtype=torch.uint8, device=DEV)
+    SB = torch.full((g.gemm_fp4_scale_bytes(N, K, code),), fill, dtype=torch.uint8, device=DEV)
+    D = torch.zeros(M, N, dtype=torch.bfloat16, device=DEV)
+    g.gemm_debug_inject_timeout(20)
+    g.gemm_fp4(M, N, K, A, K, SA, B, K, SB, code, None, 0, D, N, OUT["bf16"], 1.0, 0.0, options=options)
+    st, word = g.gemm_last_device_status()
+    assert st == g.ERR_TIMEOUT and word != 0
+    run_fp4(g, 256, 264, 512, kind, out="bf16", seed=71, options=options)

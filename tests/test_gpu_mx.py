@@ -200,6 +200,23 @@ def test_mx_full_size_bench_launch(g):
     run_mx(g, M, N, K, dist="uniform", out="bf16", seed=50, sample=(rows, cols))
 
 
+def test_mx_injected_wait_times_out_and_the_context_survives(g):
+    # the MXFP8 pair kernel with its scale copier warp: an injected wait runs out,
+    # every role ends within its bound, and the next call computes correctly
+    M = N = K = 512
+    A = torch.zeros(M * K, dtype=torch.uint8, device=DEV)
+    B = torch.zeros(N * K, dtype=torch.uint8, device=DEV)
+    SA = torch.full((g.gemm_mx_scale_bytes(M, K),), 127, dtype=torch.uint8, device=DEV)
+    SB = torch.full((g.gemm_mx_scale_bytes(N, K),), 127, dtype=torch.uint8, device=DEV)
+    D = torch.zeros(M, N, dtype=torch.bfloat16, device=DEV)
+    g.gemm_debug_inject_timeout(20)
+    g.gemm_mxfp8(M, N, K, A, 0, 0, K, SA, B, 0, 0, K, SB, None, 0, D, N, 1, 1.0, 0.0,
+                 options=dict(cta_group=2, tile_n=256))
+    st, word = g.gemm_last_device_status()
+    assert st == g.ERR_TIMEOUT and word != 0
+    run_mx(g, 512, 264, 512, exact=True, seed=73, options=dict(cta_group=2, tile_n=256))
+
+
 def test_mx_argument_errors(g):
     M, N, K = 128, 128, 128
     A = torch.zeros(M * K, dtype=torch.uint8, device=DEV)
