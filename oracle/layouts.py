@@ -60,10 +60,20 @@ def xor_grid(r: int, c: int) -> tuple[int, int]:
 
 
 # ---------------------------------------------------------------------------
-# The swizzle functor ("CUTLASS swizzling notation", "What about base?").
-# An offset's bit field YYY (``bits`` wide, sitting ``base + shift`` bits
-# up) is XORed onto the field ZZZ (``bits`` wide, ``base`` bits up); the
-# low ``base`` bits never move. A negative shift moves YYY to the left.
+# The swizzle functor Swizzle(bits, base, shift) ("CUTLASS swizzling
+# notation", "What about base?"), built from the XOR grid above.
+#
+# The page reads the functor's parameters as the shape of a grid laid out in
+# raster order inside an offset: ``base`` is log2 of the atom (the bytes that
+# move together, e.g. 16 for a ldmatrix row), ``shift`` is the number of
+# column bits of a grid row, and ``bits`` the number of row bits. So an
+# offset, from its least significant bit up, holds the position inside an
+# atom (``base`` bits, never changed), the atom's column c, and above it the
+# grid row r. Swizzling replaces c by c XOR r on the low ``bits`` bits of
+# each: the grid map f(r, c) = (r, c XOR r). The row must not have more bits
+# than the column ("Why does that work?", part 3), hence |shift| >= bits. A
+# negative shift is the notation's mirror image: the row field sits at
+# ``base`` and the column field |shift| bits above it.
 # ---------------------------------------------------------------------------
 
 
@@ -75,20 +85,34 @@ class Swizzle:
 
     def __post_init__(self):
         if self.bits < 0 or self.base < 0 or abs(self.shift) < self.bits:
-            raise ValueError("need bits >= 0, base >= 0, |shift| >= bits")
+            raise ValueError("a grid needs bits >= 0, base >= 0 and no more row bits than column bits")
+
+    @property
+    def row_pos(self) -> int:
+        """Lowest offset bit of the grid row."""
+        return self.base + self.shift if self.shift >= 0 else self.base
+
+    @property
+    def col_pos(self) -> int:
+        """Lowest offset bit of the atom's column."""
+        return self.base if self.shift >= 0 else self.base - self.shift
 
     @property
     def yyy_mask(self) -> int:
-        return ((1 << self.bits) - 1) << (self.base + max(0, self.shift))
+        """Offset bits of the row that takes part (YYY in the notation)."""
+        return ((1 << self.bits) - 1) << self.row_pos
 
     @property
     def zzz_mask(self) -> int:
-        return ((1 << self.bits) - 1) << (self.base - min(0, self.shift))
+        """Offset bits of the column that is rewritten (ZZZ)."""
+        return ((1 << self.bits) - 1) << self.col_pos
 
     def __call__(self, offset: int) -> int:
-        y = offset & self.yyy_mask
-        moved = y >> self.shift if self.shift >= 0 else y << (-self.shift)
-        return offset ^ moved
+        size = 1 << self.bits                   # rows (and columns) of the grid
+        r = (offset >> self.row_pos) % size
+        c = (offset >> self.col_pos) % size
+        _, c_new = xor_grid(r, c)               # the cell's new column in the same row
+        return offset + ((c_new - c) << self.col_pos)
 
 
 # Canonical modes ("32B, 64B and 128B swizzles"): 16-byte atoms (base 4),
