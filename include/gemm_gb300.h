@@ -347,20 +347,24 @@ gemm_status_t gemm_grouped_ex(int in_type, const gemm_problem_t *problems, int n
 
 /*
  * gemm_bf16_grouped_noalloc: the grouped bf16 GEMM for callers that cannot
- * allocate device memory when they launch it -- for instance code running
- * while a stream is being captured into a CUDA graph, programs whose memory
- * pool owns the whole device, or latency-bound loops that may not enter the
- * driver's allocator. There is no counterpart on the pages; it is a service
- * of this library. Instead of a caller workspace, the problem table and TMA
- * descriptors go into a fixed array inside the library (about 68 KB, room for
- * GEMM_NOALLOC_MAX_PROBLEMS problems) that every GPU which loads the library
- * keeps until the process exits. The call allocates nothing, host or device.
+ * allocate device memory when they launch it: programs whose allocator has
+ * reserved the whole device and forbids side allocations, plug-ins that a
+ * host runtime hands only their input and output buffers, and real-time
+ * loops that may not block in the driver's allocator (cudaMalloc can
+ * synchronise the device). There is no counterpart on the pages; it is a
+ * service of this library. Instead of a caller workspace, the problem table
+ * and TMA descriptors go into a fixed array inside the library (about 68 KB,
+ * room for GEMM_NOALLOC_MAX_PROBLEMS problems) that every GPU which loads the
+ * library keeps until the process exits. The call allocates no device
+ * memory and calls no allocating library routine; the table is staged in a
+ * fixed host array and copied to the device array with cudaMemcpyAsync on
+ * `stream` before the kernel launch.
  *   - Same arguments and results as gemm_bf16_grouped, minus the workspace.
  *   - num_problems > GEMM_NOALLOC_MAX_PROBLEMS returns GEMM_ERR_INVALID_ARG
  *     and enqueues nothing.
- *   - The first call on a device looks up the array's device address there
- *     (with that device current); make that first call before any stream
- *     capture.
+ *   - Set-up: the first call on a device looks up the array's device address
+ *     there (cudaGetSymbolAddress, with that device current) and keeps it.
+ *     Make that first call before any stream capture begins.
  *   - All calls share the array and each call rewrites the part it uses, so
  *     calls whose kernels may overlap on the GPU (other streams, or no
  *     ordering between them) race: order them on one stream or synchronise.

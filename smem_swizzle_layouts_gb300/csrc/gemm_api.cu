@@ -579,19 +579,21 @@ gemm_status_t run_single(const InFmt &f, int64_t M, int64_t N, int64_t K, const 
 // Device-side problem table followed by four tensor maps per problem.
 size_t table_bytes(int n) { return (static_cast<size_t>(n) * sizeof(GroupedProblemDev) + 127) & ~size_t(127); }
 
-gemm_status_t run_grouped(int in_bf16, const gemm_problem_t *probs, int n, int a_major, int b_major,
-                          int d_type, float alpha, float beta, void *ws, size_t ws_bytes,
-                          const gemm_options_t *opts, cudaStream_t stream)
+// A validated, planned grouped call, before its table exists anywhere.
+struct GroupedCall {
+    int in_bf16, a_mn, b_mn, d_type;
+    float alpha, beta;
+    int dev, sms;
+    unsigned int *status;
+    Plan pl;
+    Variant *v;
+};
+
+// Argument checks of every problem, then the plan shared by all of them
+// (from the largest M, N and K of the list).
+gemm_status_t plan_grouped(int in_bf16, const gemm_problem_t *probs, int n, int a_major, int b_major, int d_type,
+                           float alpha, float beta, const gemm_options_t *opts, GroupedCall *gc)
 {
-    if (n < 0 || (n > 0 && !probs) || !valid_enum(a_major) || !valid_enum(b_major) || d_type < 0 ||
-        d_type > 2)
-        return GEMM_ERR_INVALID_ARG;
-    if (n == 0)
-        return GEMM_OK;
-    if (!ws || ws_bytes < gemm_grouped_workspace_size(n))
-        return GEMM_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(ws) & 127u) != 0)
-        return GEMM_ERR_ALIGNMENT;
     const int a_mn = a_major, b_mn = b_major;
     int64_t maxM = 0, maxN = 0, maxK = 0;
     for (int i = 0; i < n; ++i) {
@@ -604,9 +606,7 @@ gemm_status_t run_grouped(int in_bf16, const gemm_problem_t *probs, int n, int a
         maxN = std::max(maxN, q.N);
         maxK = std::max(maxK, q.K);
     }
-    int dev = 0, sms = 0;
-    unsigned int *status = nullptr;
-    gemm_status_t s = device_state(&dev, &status, &sms);
+    gemm_status_t s = device_state(&gc->dev, &gc->status, &gc->sms);
     if (s != GEMM_OK)
         return s;
     gemm_options_t o = {};
@@ -616,16 +616,30 @@ gemm_status_t run_grouped(int in_bf16, const gemm_problem_t *probs, int n, int a
         o.cta_group = 1;
     if (o.tile_n == 0)  // grouped pairs are built for 256-wide tiles only
         o.tile_n = (maxN >= 192 || o.cta_group == 2) ? 256 : 128;
-    Plan pl;
-    if ((s = make_plan(maxM, maxN, maxK, a_mn, b_mn, sms, &o, true, &pl)) != GEMM_OK)
+    if ((s = make_plan(maxM, maxN, maxK, a_mn, b_mn, gc->sms, &o, true, &gc->pl)) != GEMM_OK)
         return s;
-    Variant *v = find_variant(pl.cg, pl.bn, pl.bk, true);
+    gc->v = find_variant(gc->pl.cg, gc->pl.bn, gc->pl.bk, true);
+    gc->in_bf16 = in_bf16;
+    gc->a_mn = a_mn;
+    gc->b_mn = b_mn;
+    gc->d_type = d_type;
+    gc->alpha = alpha;
+    gc->beta = beta;
+    return GEMM_OK;
+}
 
-    const size_t tb = table_bytes(n);
-    std::vector<unsigned char> host(gemm_grouped_workspace_size(n), 0);
-    auto *table = reinterpret_cast<GroupedProblemDev *>(host.data());
-    auto *maps = reinterpret_cast<CUtensorMap *>(host.data() + tb);
+// Writes the problem table and the tensor maps of `n` problems into the host
+// buffer `img` (table_bytes(n) + n * 4 maps, zeroed by the caller) and counts
+// the tiles of the launch.
+gemm_status_t build_grouped_image(const GroupedCall &gc, const gemm_problem_t *probs, int n, unsigned char *img,
+                                  int64_t *tiles_out)
+{
+    const Plan &pl = gc.pl;
+    const int dcode = fmt16(gc.in_bf16).dcode;
+    auto *table = reinterpret_cast<GroupedProblemDev *>(img);
+    auto *maps = reinterpret_cast<CUtensorMap *>(img + table_bytes(n));
     int64_t tiles = 0;
+    gemm_status_t s = GEMM_OK;
     for (int i = 0; i < n; ++i) {
         const gemm_problem_t &q = probs[i];
         GroupedProblemDev &g = table[i];
@@ -643,43 +657,79 @@ gemm_status_t run_grouped(int in_bf16, const gemm_problem_t *probs, int n, int a
             continue;
         CUtensorMap *m = maps + 4 * i;
         if (q.K > 0) {
-            if ((s = encode_operand(&m[0], fmt16(in_bf16).dcode, q.A, a_mn, pl.a_swz, q.M, q.K, q.lda, 128, pl.bk)) != GEMM_OK)
+            if ((s = encode_operand(&m[0], dcode, q.A, gc.a_mn, pl.a_swz, q.M, q.K, q.lda, 128, pl.bk)) != GEMM_OK)
                 return s;
-            if ((s = encode_operand(&m[1], fmt16(in_bf16).dcode, q.B, b_mn, pl.b_swz, q.N, q.K, q.ldb, pl.bn / pl.cg,
-                                    pl.bk)) != GEMM_OK)
+            if ((s = encode_operand(&m[1], dcode, q.B, gc.b_mn, pl.b_swz, q.N, q.K, q.ldb, pl.bn / pl.cg, pl.bk)) !=
+                GEMM_OK)
                 return s;
         }
-        if ((s = encode_output(&m[3], d_type, q.D, q.M, q.N, q.ldd, pl.epi_swizzle)) != GEMM_OK)
+        if ((s = encode_output(&m[3], gc.d_type, q.D, q.M, q.N, q.ldd, pl.epi_swizzle)) != GEMM_OK)
             return s;
-        if (beta != 0.0f) {
-            if ((s = encode_output(&m[2], d_type, q.C, q.M, q.N, q.ldc, pl.epi_swizzle)) != GEMM_OK)
+        if (gc.beta != 0.0f) {
+            if ((s = encode_output(&m[2], gc.d_type, q.C, q.M, q.N, q.ldc, pl.epi_swizzle)) != GEMM_OK)
                 return s;
         } else {
             m[2] = m[3];
         }
     }
-    if (tiles == 0)
-        return GEMM_OK;
-    // pageable source: the copy is staged before this call returns
-    cudaError_t e = cudaMemcpyAsync(ws, host.data(), host.size(), cudaMemcpyHostToDevice, stream);
+    *tiles_out = tiles;
+    return GEMM_OK;
+}
+
+// Copies the image (pageable source: staged before cudaMemcpyAsync returns)
+// to `ws` on `stream` and launches the grouped kernel that reads it there.
+gemm_status_t upload_and_launch_grouped(const GroupedCall &gc, int n, int64_t tiles, const unsigned char *img,
+                                        size_t img_bytes, unsigned char *ws, cudaStream_t stream)
+{
+    cudaError_t e = cudaMemcpyAsync(ws, img, img_bytes, cudaMemcpyHostToDevice, stream);
     if (e != cudaSuccess)
         return cuda_fail(e);
-
     LaunchArgs la;
     std::memset(&la, 0, sizeof(la));
     KParams &p = la.p;
     p.num_tiles = static_cast<int>(tiles);
     p.problems = reinterpret_cast<const GroupedProblemDev *>(ws);
-    p.maps = reinterpret_cast<const CUtensorMap *>(static_cast<unsigned char *>(ws) + tb);
+    p.maps = reinterpret_cast<const CUtensorMap *>(ws + table_bytes(n));
     p.num_problems = n;
-    fill_common(p, pl, fmt16(in_bf16), a_mn, b_mn, d_type, alpha, beta, status);
-    la.grid = grid_for(pl, *v, dev, sms, tiles);
+    fill_common(p, gc.pl, fmt16(gc.in_bf16), gc.a_mn, gc.b_mn, gc.d_type, gc.alpha, gc.beta, gc.status);
+    la.grid = grid_for(gc.pl, *gc.v, gc.dev, gc.sms, tiles);
     la.stream = stream;
-    e = v->launch(la);
+    e = gc.v->launch(la);
     if (e != cudaSuccess)
         return cuda_fail(e);
     g_launches.fetch_add(1);
     return GEMM_OK;
+}
+
+bool grouped_args_ok(const gemm_problem_t *probs, int n, int a_major, int b_major, int d_type)
+{
+    return n >= 0 && (n == 0 || probs) && valid_enum(a_major) && valid_enum(b_major) && d_type >= 0 && d_type <= 2;
+}
+
+gemm_status_t run_grouped(int in_bf16, const gemm_problem_t *probs, int n, int a_major, int b_major,
+                          int d_type, float alpha, float beta, void *ws, size_t ws_bytes,
+                          const gemm_options_t *opts, cudaStream_t stream)
+{
+    if (!grouped_args_ok(probs, n, a_major, b_major, d_type))
+        return GEMM_ERR_INVALID_ARG;
+    if (n == 0)
+        return GEMM_OK;
+    if (!ws || ws_bytes < gemm_grouped_workspace_size(n))
+        return GEMM_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(ws) & 127u) != 0)
+        return GEMM_ERR_ALIGNMENT;
+    GroupedCall gc;
+    gemm_status_t s = plan_grouped(in_bf16, probs, n, a_major, b_major, d_type, alpha, beta, opts, &gc);
+    if (s != GEMM_OK)
+        return s;
+    std::vector<unsigned char> host(gemm_grouped_workspace_size(n), 0);
+    int64_t tiles = 0;
+    if ((s = build_grouped_image(gc, probs, n, host.data(), &tiles)) != GEMM_OK)
+        return s;
+    if (tiles == 0)
+        return GEMM_OK;
+    return upload_and_launch_grouped(gc, n, tiles, host.data(), host.size(), static_cast<unsigned char *>(ws),
+                                     stream);
 }
 
 // ---------------------------------------------------------------- inspection kernels
@@ -745,13 +795,14 @@ __global__ void debug_stage_kernel(const __grid_constant__ CUtensorMap map, int 
 // ---------------------------------------------------------------- grouped GEMM without allocation
 //
 // Some callers cannot allocate device memory at the moment they launch a
-// GEMM: code running while a stream is being captured into a CUDA graph
-// (an allocation there breaks or serialises the capture), allocators that
-// own the whole device pool and forbid side allocations, or real-time loops
-// that may not block in the driver's allocator. For them the grouped GEMM's
-// workspace (problem table plus one TMA descriptor per operand per problem)
-// lives in the fixed array below, sized for kNoAllocMaxProblems problems.
-// Every GPU that loads the library holds it until the process exits.
+// GEMM: programs whose allocator has reserved the whole device and forbids
+// side allocations, plug-ins that are handed their input and output buffers
+// by a host runtime and own no memory budget of their own, and real-time
+// loops that may not block in the driver's allocator (cudaMalloc can
+// synchronise the device). For them the grouped GEMM's workspace (problem
+// table plus one TMA descriptor per operand per problem) lives in the fixed
+// array below, sized for kNoAllocMaxProblems problems. Every GPU that loads
+// the library holds it until the process exits.
 
 constexpr int kNoAllocMaxProblems = GEMM_NOALLOC_MAX_PROBLEMS;
 constexpr size_t kNoAllocScratchBytes =
@@ -785,103 +836,30 @@ gemm_status_t run_grouped_noalloc(int in_bf16, const gemm_problem_t *probs, int 
                                   int b_major, int d_type, float alpha, float beta,
                                   cudaStream_t stream)
 {
-    if (n < 0 || (n > 0 && !probs) || !valid_enum(a_major) || !valid_enum(b_major) || d_type < 0 ||
-        d_type > 2)
+    if (!grouped_args_ok(probs, n, a_major, b_major, d_type))
         return GEMM_ERR_INVALID_ARG;
     if (n > kNoAllocMaxProblems)
         return GEMM_ERR_INVALID_ARG;  // more problems than the fixed scratch holds
     if (n == 0)
         return GEMM_OK;
-    const int a_mn = a_major, b_mn = b_major;
-    int64_t maxM = 0, maxN = 0, maxK = 0;
-    for (int i = 0; i < n; ++i) {
-        const gemm_problem_t &q = probs[i];
-        gemm_status_t s = check_problem(q.M, q.N, q.K, q.A, a_mn, q.lda, q.B, b_mn, q.ldb, q.C, q.ldc,
-                                        q.D, q.ldd, d_type, beta);
-        if (s != GEMM_OK)
-            return s;
-        maxM = std::max(maxM, q.M);
-        maxN = std::max(maxN, q.N);
-        maxK = std::max(maxK, q.K);
-    }
-    int dev = 0, sms = 0;
-    unsigned int *status = nullptr;
-    gemm_status_t s = device_state(&dev, &status, &sms);
+    GroupedCall gc;
+    gemm_status_t s = plan_grouped(in_bf16, probs, n, a_major, b_major, d_type, alpha, beta, nullptr, &gc);
     if (s != GEMM_OK)
         return s;
-    gemm_options_t o = {};
-    o.tile_n = (maxN >= 192) ? 256 : 128;
-    o.cta_group = 1;
-    Plan pl;
-    if ((s = make_plan(maxM, maxN, maxK, a_mn, b_mn, sms, &o, true, &pl)) != GEMM_OK)
-        return s;
-    Variant *v = find_variant(pl.cg, pl.bn, pl.bk, true);
-
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
     unsigned char *ws = nullptr;
-    if ((s = noalloc_scratch(dev, &ws)) != GEMM_OK)
+    if ((s = noalloc_scratch(gc.dev, &ws)) != GEMM_OK)
         return s;
-    const size_t tb = table_bytes(n);
-    const size_t used = tb + static_cast<size_t>(n) * 4 * sizeof(CUtensorMap);
+    const size_t used = table_bytes(n) + static_cast<size_t>(n) * 4 * sizeof(CUtensorMap);
     // the whole used region is rewritten on every call: nothing is left over
     // from an earlier call with more problems or other pointers
     std::memset(g_noalloc_host, 0, used);
-    auto *table = reinterpret_cast<GroupedProblemDev *>(g_noalloc_host);
-    auto *maps = reinterpret_cast<CUtensorMap *>(g_noalloc_host + tb);
     int64_t tiles = 0;
-    for (int i = 0; i < n; ++i) {
-        const gemm_problem_t &q = probs[i];
-        GroupedProblemDev &g = table[i];
-        g.M = static_cast<int>(q.M);
-        g.N = static_cast<int>(q.N);
-        g.K = static_cast<int>(q.K);
-        const bool empty = q.M == 0 || q.N == 0;
-        g.tiles_m = empty ? 0 : static_cast<int>((q.M + 128 * pl.cg - 1) / (128 * pl.cg));
-        g.tiles_n = empty ? 0 : static_cast<int>((q.N + pl.bn - 1) / pl.bn);
-        g.tile_start = static_cast<int>(tiles);
-        tiles += static_cast<int64_t>(g.tiles_m) * g.tiles_n;
-        if (tiles >= (static_cast<int64_t>(1) << 31))
-            return GEMM_ERR_UNSUPPORTED;
-        if (empty)
-            continue;
-        CUtensorMap *m = maps + 4 * i;
-        if (q.K > 0) {
-            if ((s = encode_operand(&m[0], fmt16(in_bf16).dcode, q.A, a_mn, pl.a_swz, q.M, q.K, q.lda, 128, pl.bk)) != GEMM_OK)
-                return s;
-            if ((s = encode_operand(&m[1], fmt16(in_bf16).dcode, q.B, b_mn, pl.b_swz, q.N, q.K, q.ldb, pl.bn / pl.cg,
-                                    pl.bk)) != GEMM_OK)
-                return s;
-        }
-        if ((s = encode_output(&m[3], d_type, q.D, q.M, q.N, q.ldd, pl.epi_swizzle)) != GEMM_OK)
-            return s;
-        if (beta != 0.0f) {
-            if ((s = encode_output(&m[2], d_type, q.C, q.M, q.N, q.ldc, pl.epi_swizzle)) != GEMM_OK)
-                return s;
-        } else {
-            m[2] = m[3];
-        }
-    }
+    if ((s = build_grouped_image(gc, probs, n, g_noalloc_host, &tiles)) != GEMM_OK)
+        return s;
     if (tiles == 0)
         return GEMM_OK;
-    cudaError_t e = cudaMemcpyAsync(ws, g_noalloc_host, used, cudaMemcpyHostToDevice, stream);
-    if (e != cudaSuccess)
-        return cuda_fail(e);
-
-    LaunchArgs la;
-    std::memset(&la, 0, sizeof(la));
-    KParams &p = la.p;
-    p.num_tiles = static_cast<int>(tiles);
-    p.problems = reinterpret_cast<const GroupedProblemDev *>(ws);
-    p.maps = reinterpret_cast<const CUtensorMap *>(ws + tb);
-    p.num_problems = n;
-    fill_common(p, pl, fmt16(in_bf16), a_mn, b_mn, d_type, alpha, beta, status);
-    la.grid = grid_for(pl, *v, dev, sms, tiles);
-    la.stream = stream;
-    e = v->launch(la);
-    if (e != cudaSuccess)
-        return cuda_fail(e);
-    g_launches.fetch_add(1);
-    return GEMM_OK;
+    return upload_and_launch_grouped(gc, n, tiles, g_noalloc_host, used, ws, stream);
 }
 
 }  // namespace
