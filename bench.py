@@ -108,6 +108,14 @@ def _peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+# Published (not measured) per-GPU figures, reported beside the measured
+# denominators: NVIDIA's HGX B300 sheet gives 36 PFLOP/s bf16 per 8 GPUs with
+# 2:4 sparsity, i.e. 2.25 PFLOP/s dense per GPU, and 8 TB/s of HBM3e.
+NOMINAL_BF16_TFLOPS = 2250.0
+NOMINAL_BF16_SOURCE = "nominal dense bf16 2250 TFLOP/s (NVIDIA HGX B300: 36 PFLOP/s sparse per 8 GPUs)"
+NOMINAL_HBM_GBS = 8000.0
+NOMINAL_HBM_SOURCE = "nominal HBM3e 8000 GB/s (NVIDIA GB300 sheet)"
+
 KERNEL_SOURCES = ("gemm_kernel.cuh", "ptx.cuh", "descriptors.cuh")
 
 
@@ -189,8 +197,26 @@ class ClockSampler:
                 if val.lower() in ("active", "1"):
                     reasons.add(name)
         if not sm:
+            # the region was shorter than the sampling period: report the
+            # nearest sample on each side of it, labelled as such
+            before = [(t, ln) for t, ln in self.lines if t < t0]
+            after = [(t, ln) for t, ln in self.lines if t > t1 + 0.02]
+            near = {}
+            for label, pick in (("before", before[-1:]), ("after", after[:1])):
+                for t, ln in pick:
+                    parts = [p.strip() for p in ln.split(",")]
+                    if len(parts) < 10:
+                        continue
+                    try:
+                        near[label] = {"sm_mhz": float(parts[2]), "sm_max_mhz": float(parts[3]),
+                                       "ms_from_region": round(1e3 * (t - t0 if label == "before" else t - t1), 1),
+                                       "reasons": [n for n, v in zip(names, parts[6:10])
+                                                   if v.lower() in ("active", "1")]}
+                    except ValueError:
+                        continue
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
-                    "note": "no nvidia-smi sample fell inside the timed region"}
+                    "note": "no nvidia-smi sample fell inside the timed region; nearest samples outside it follow",
+                    "nearest_outside": near}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
                 "samples": len(sm)}
 
@@ -631,15 +657,20 @@ def main():
     config["l2"] = ("operands larger than L2 (129 MB): no flush between steps" if bytes_alg > 129e6 else
                     "operands fit in L2; steps run back to back without a flush")
     value = job_throughput(flops * args.steps, ws, r["total_ms"]) / 1e12
+    # the roofline's achieved rate uses the mean launch time; median and min
+    # over the same launches are reported beside it
     kernel_ms = statistics.mean(r["per_launch"])
+    kernel_stats = {"kernel_ms_median": statistics.median(r["per_launch"]), "kernel_ms_min": min(r["per_launch"]),
+                    "launches_timed": len(r["per_launch"])}
     peaks, peak_src = _peaks()
     traffic = _profiled_traffic(args.workload) if not args.options else None
     if wl.get("bound") == "hbm":
         achieved = bytes_alg / (kernel_ms / 1e3) / 1e9
         peak = float(peaks.get("hbm_gbs", 6800.0))
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "peak_source": f"{peak_src} hbm_gbs", "traffic": traffic, "kernel_ms": kernel_ms,
-                "algorithmic_bytes": bytes_alg}
+                "peak_source": f"{peak_src} hbm_gbs", "traffic": traffic, "kernel_ms": kernel_ms, **kernel_stats,
+                "algorithmic_bytes": bytes_alg,
+                "frac_of_nominal": achieved / NOMINAL_HBM_GBS, "nominal_source": NOMINAL_HBM_SOURCE}
     else:
         achieved = flops / (kernel_ms / 1e3) / 1e12
         ratio = float(wl.get("peak_ratio", 1.0))  # nominal dense peaks over bf16: fp8 4.5/2.25, fp4 13.5/2.25
@@ -648,7 +679,9 @@ def main():
                 "peak_source": f"{peak_src} bf16_tflops (burst)" + (
                     f" x {ratio:g} (nominal {'fp4' if wl.get('fp4') else 'fp8'}/bf16 dense ratio)" if ratio != 1.0 else ""),
                 "frac_of_sustained": achieved / (float(peaks.get("bf16_tflops_sustained", peak)) * ratio),
-                "traffic": traffic, "kernel_ms": kernel_ms, "algorithmic_bytes": bytes_alg}
+                "frac_of_nominal": achieved / (NOMINAL_BF16_TFLOPS * ratio),
+                "nominal_source": NOMINAL_BF16_SOURCE + (f" x {ratio:g}" if ratio != 1.0 else ""),
+                "traffic": traffic, "kernel_ms": kernel_ms, **kernel_stats, "algorithmic_bytes": bytes_alg}
     line = {"metric": metric, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": r["total_ms"] / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "e2m1" if wl.get("fp4") else wl.get("in_fmt", "bf16"),

@@ -3,12 +3,12 @@
 //   D = alpha * A * B + beta * C,  fp16/bf16 in, fp32 accumulate in TMEM.
 //
 // One CTA (cta_group::1) or one CTA pair (cta_group::2, cluster of 2) per
-// SM / SM pair walks a static round-robin list of output tiles. Six warps:
+// SM / SM pair walks a static round-robin list of output tiles. Warp roles:
 //   warp 0     TMA producer: one thread fills an S-stage shared-memory ring
 //              (full/empty mbarriers, "Tensor Cores, layouts, and swizzling",
 //              TMA section and 6.6.1: expect_tx bytes, parity (k/S)&1);
 //   warp 1     TMEM allocator and MMA issuer: one thread issues
-//              tcgen05.mma for every K=16 slice and commits completion to
+//              tcgen05.mma for every K slice and commits completion to
 //              mbarriers ("06 Blackwell Tensor Core - tcgen05 MMA", "How
 //              tcgen05.mma Executes"); the accumulator is double-buffered
 //              in TMEM (2 x BN fp32 columns) so the epilogue of tile i
@@ -16,19 +16,24 @@
 //   warps 2-5  epilogue: warp w reads TMEM lanes 32*(w%4)..+31 (the lane
 //              quarter rule of "Tensor Cores, layouts, and swizzling",
 //              tcgen05 section) with tcgen05.ld, applies alpha/beta against
-//              C (TMA-loaded), converts, stages 32-row chunks in a
-//              swizzled shared-memory buffer and writes them with TMA stores.
+//              C (TMA-loaded, or read into registers), converts, stages
+//              32-row chunks in a swizzled shared-memory buffer and writes
+//              them with TMA stores;
+//   warp 6     block-scaled kinds only: scale copier (tcgen05.cp of each
+//   (and 7)    stage's scale atoms into TMEM); NVFP4 runs two copiers on
+//              alternate K groups. So 192 threads, or 224/256 with copiers.
 //
 // CTA pairs: the even CTA holds accumulator rows 0-127 and the odd CTA rows
 // 128-255 ("How cta_group Sets the Operation Scope", cta_group::2, M=256).
 // Each CTA TMA-loads its own 128 rows of A and its own half of the tile's N
-// columns of B into its own shared memory (no multicast); completion bytes
-// of both land on the even CTA's full barrier, whose one thread issues the
-// M=256 MMAs and commits their completion to the even CTA's barriers. The
-// even CTA forwards each release to the odd CTA with a remote
-// mbarrier.arrive: its producer, once a stage is free again, and its first
-// epilogue warp, once an accumulator is complete. The odd CTA's epilogue
+// columns of B into its own shared memory (no multicast); the .cta_group::2
+// form of the load completes the bytes of both on the even CTA's full
+// barrier, whose one thread issues the M=256 MMAs. Their completion reaches
+// both CTAs through one multicast tcgen05.commit (mask 0b11) on the stage's
+// empty barrier and on the accumulator-full barrier; the odd CTA's epilogue
 // warps release accumulators by remote arrives on the even CTA's barrier.
+// (Forwarding each release from the even CTA to the odd one by a remote
+// mbarrier.arrive is kept as the kFlagPairForward ablation.)
 //
 // Every mbarrier wait is bounded: past the time limit the waiting role
 // records a code in the status word, raises a CTA-wide abort flag and

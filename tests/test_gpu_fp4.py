@@ -45,7 +45,10 @@ def _out_bits(t, fmt):
     return a.view(torch.int16).numpy().view(np.uint16)
 
 
-def run_fp4(g, M, N, K, kind, *, out="f32", alpha=1.0, beta=0.0, seed=0, options=None, pad=0):
+def run_fp4(g, M, N, K, kind, *, out="f32", alpha=1.0, beta=0.0, seed=0, options=None, pad=0, a_pool=None,
+            b_pool=None):
+    """One fp4 GEMM through the C ABI, bit for bit against the oracle. ``a_pool`` /
+    ``b_pool`` (scale codes to draw from) replace the default scale distribution."""
     code, block, scale = KINDS[kind]
     lda = ldb = _ru(K, 32) + pad
     ca = np.zeros((M, lda), np.uint8)
@@ -54,7 +57,12 @@ def run_fp4(g, M, N, K, kind, *, out="f32", alpha=1.0, beta=0.0, seed=0, options
     cb[:, :K] = si.fp4_codes(seed + 1, N, K)
     A, B = si.pack_fp4(ca), si.pack_fp4(cb)
     nb = (K + block - 1) // block
-    if scale == "ue4m3":
+    if a_pool is not None or b_pool is not None:
+        rng = np.random.default_rng(seed + 2)
+        default = UE4M3_POOL if scale == "ue4m3" else np.arange(124, 131, dtype=np.uint8)
+        sa = rng.choice(np.asarray(a_pool if a_pool is not None else default, np.uint8), (M, nb))
+        sb = rng.choice(np.asarray(b_pool if b_pool is not None else default, np.uint8), (N, nb))
+    elif scale == "ue4m3":
         rng = np.random.default_rng(seed + 2)
         sa, sb = rng.choice(UE4M3_POOL, (M, nb)), rng.choice(UE4M3_POOL, (N, nb))
     else:

@@ -49,7 +49,9 @@ def _out_bits(t, fmt):
 
 
 def run_mx(g, M, N, K, *, a_fmt="e4m3", b_fmt=None, a_major="K", b_major="K", out="f32", alpha=1.0, beta=0.0,
-           dist="int4", seed=0, exact=False, options=None, sample=None, lo=124, hi=130):
+           dist="int4", seed=0, exact=False, options=None, sample=None, lo=124, hi=130, b_lo=None, b_hi=None):
+    """One MXFP8 GEMM through the C ABI against the oracle. A's E8M0 codes are drawn
+    from [lo, hi], B's from [b_lo, b_hi] (default: the same range)."""
     b_fmt = b_fmt or a_fmt
     lda = _ru(K if a_major == "K" else M, 16)
     ldb = _ru(K if b_major == "K" else N, 16)
@@ -59,7 +61,7 @@ def run_mx(g, M, N, K, *, a_fmt="e4m3", b_fmt=None, a_major="K", b_major="K", ou
     C = si.matrix_bits(seed + 2, M, N, dist, out, ld=ldd) if beta != 0.0 else None
     nb = max(1, (K + 31) // 32)
     sa = si.scale_codes(seed + 3, M, nb, lo, hi)
-    sb = si.scale_codes(seed + 4, N, nb, lo, hi)
+    sb = si.scale_codes(seed + 4, N, nb, lo if b_lo is None else b_lo, hi if b_hi is None else b_hi)
     SA = torch.from_numpy(si.mx_scale_atoms(sa, M, K)).to(DEV) if K > 0 else None
     SB = torch.from_numpy(si.mx_scale_atoms(sb, N, K)).to(DEV) if K > 0 else None
     if K > 0:
