@@ -66,13 +66,22 @@ typedef enum { GEMM_OUT_F32 = 0, GEMM_OUT_BF16 = 1, GEMM_OUT_F16 = 2 } gemm_out_
  * "32B, 64B and 128B swizzles"; raw descriptor codes on the LBO/SBO page,
  * section 4). GEMM_SWIZZLE_AUTO lets the library choose (SW128);
  * GEMM_SWIZZLE_NONE stores plain 8-row x 16-byte core matrices (descriptor
- * code 0, LBO and SBO alone define the layout). */
+ * code 0, LBO and SBO alone define the layout). GEMM_SWIZZLE_128B_ATOM32 is
+ * the page's "128-byte mode with 32-byte atomicity" (descriptor code 1):
+ * 128-byte rows whose 32-byte units are XORed with the row index mod 4
+ * (Swizzle<2,5,2>, written by TMA's 128B_ATOM_32B mode), read as an MN-major
+ * operand with K rows in bands of 4. The inspection entry points accept it
+ * (descriptor words, TMA stage images); GEMM calls return
+ * GEMM_ERR_UNSUPPORTED, because the MMA kinds this library issues
+ * (kind::f16, kind::f8f6f4, block-scaled) read such operands as zeros on
+ * GB300 (measured). */
 typedef enum {
     GEMM_SWIZZLE_AUTO = 0,
     GEMM_SWIZZLE_32B = 1,
     GEMM_SWIZZLE_64B = 2,
     GEMM_SWIZZLE_128B = 3,
-    GEMM_SWIZZLE_NONE = 4
+    GEMM_SWIZZLE_NONE = 4,
+    GEMM_SWIZZLE_128B_ATOM32 = 5
 } gemm_swizzle_t;
 
 /*

@@ -120,15 +120,26 @@ class Swizzle:
 MODE_BITS = {"none": 0, "sw32": 1, "sw64": 2, "sw128": 3}
 SWIZZLE = {m: Swizzle(b, 4, 3) for m, b in MODE_BITS.items()}
 
+# The 128-byte swizzle with 32-byte atoms (raw SWZ value 1, "LBO, SBO and SWZ
+# for a tcgen05 tile", section 4, which names the mode and nothing more).
+# Reading, through "What about base?" (base = log2 of the atom): 32-byte
+# atoms (base 5), four of them to a 128-byte row (shift 2) and a square grid
+# of four rows (bits 2), i.e. Swizzle(2, 5, 2): the pattern repeats every
+# four 128-byte rows. As an MMA operand the mode is read for MN-major tiles
+# with K rows in bands of ATOM32_K_BAND rows (SBO steps between bands).
+ATOM32 = "sw128_base32b"
+SWIZZLE[ATOM32] = Swizzle(2, 5, 2)
+ATOM32_K_BAND = 4
+
 
 def swizzle_width(mode: str) -> int:
-    """Bytes per swizzled row: 16 (none), 32, 64 or 128."""
-    return 16 << MODE_BITS[mode]
+    """Bytes per swizzled row: 16 (none), 32, 64 or 128 (both 128-byte modes)."""
+    return 128 if mode == ATOM32 else 16 << MODE_BITS[mode]
 
 
 def swizzle_repeat(mode: str) -> int:
-    """Bytes after which the XOR pattern repeats (natural boundary): 8 rows."""
-    return 8 * swizzle_width(mode)
+    """Bytes after which the XOR pattern repeats (natural boundary): 8 rows, 4 for 32-byte atoms."""
+    return (4 if mode == ATOM32 else 8) * swizzle_width(mode)
 
 
 # Raw SWZ field values ("LBO, SBO and SWZ for a tcgen05 tile", section 4).
@@ -273,29 +284,40 @@ def desc_fixed_bits(word: int) -> int:
 # ---------------------------------------------------------------------------
 
 
-def _xor_absolute(addr: int, bits: int) -> int:
-    """Flip bits [4, 4+B) of the address with its bits [7, 7+B)."""
+def _xor_field(mode: str) -> tuple[int, int]:
+    """(width, lowest address bit) of the field the mode's XOR rewrites: the 16-byte
+    cell index [4, 4+B) for the 16-byte-atom modes, the 32-byte unit [5, 7) for ATOM32."""
+    if mode == ATOM32:
+        return 2, 5
+    return MODE_BITS[mode], 4
+
+
+def _xor_absolute(addr: int, bits: int, lo: int = 4) -> int:
+    """Flip address bits [lo, lo+B) with the bits of the 128-byte row above them, [7, 7+B)."""
     if bits == 0:
         return addr
     mask = (1 << bits) - 1
-    return addr ^ (((addr >> 7) & mask) << 4)
+    return addr ^ (((addr >> 7) & mask) << lo)
 
 
-def _xor_relative(addr: int, pattern_start: int, mbo: int, bits: int) -> int:
+def _xor_relative(addr: int, pattern_start: int, mbo: int, bits: int, lo: int = 4) -> int:
     """Same XOR, taking the row phase from the offset to the pattern start plus MBO."""
     if bits == 0:
         return addr
     mask = (1 << bits) - 1
     rel = addr - pattern_start
     key = ((rel >> 7) + mbo) & mask
-    return addr ^ (key << 4)
+    return addr ^ (key << lo)
 
 
 def desc_pre_swizzle_addr(d: SmemDesc, major: str, esize: int, mn: int, k: int) -> int:
     mode = SWZ_MODE[d.swz]
-    if mode == "sw128_base32b":
-        raise NotImplementedError("128B swizzle with 32B atoms is not modelled")
     W = swizzle_width(mode)
+    if mode == ATOM32:
+        if major != "MN":
+            raise ValueError("the 32-byte-atom mode is read for MN-major operands only")
+        T, R = W // esize, ATOM32_K_BAND
+        return d.start + (mn // T) * d.lbo + (k // R) * d.sbo + (k % R) * W + (mn % T) * esize
     if major == "K":
         if mode == "none":
             cell = 16 // esize
@@ -313,14 +335,14 @@ def desc_pre_swizzle_addr(d: SmemDesc, major: str, esize: int, mn: int, k: int) 
 def desc_element_addr(d: SmemDesc, major: str, esize: int, mn: int, k: int) -> int:
     """Physical byte address of element (mn, k) of the slice (absolute-address XOR)."""
     pre = desc_pre_swizzle_addr(d, major, esize, mn, k)
-    return _xor_absolute(pre, MODE_BITS[SWZ_MODE[d.swz]])
+    return _xor_absolute(pre, *_xor_field(SWZ_MODE[d.swz]))
 
 
 def desc_element_addr_relative(d: SmemDesc, major: str, esize: int, mn: int, k: int,
                                pattern_start: int) -> int:
     """Same address from the pattern-relative XOR with the descriptor's MBO."""
     pre = desc_pre_swizzle_addr(d, major, esize, mn, k)
-    return _xor_relative(pre, pattern_start, d.base_offset, MODE_BITS[SWZ_MODE[d.swz]])
+    return _xor_relative(pre, pattern_start, d.base_offset, *_xor_field(SWZ_MODE[d.swz]))
 
 
 # ---------------------------------------------------------------------------
@@ -388,14 +410,17 @@ def stage_slice_desc(major: str, mode: str, rows: int, bk: int, esize: int, j: i
     kbytes = 32                 # K bytes per row consumed by one MMA
     kper = kbytes // esize      # K elements per MMA slice
     if major == "K":
+        if mode == ATOM32:
+            raise ValueError("the 32-byte-atom mode is read for MN-major operands only")
         off = j * kbytes
         start = base + (off // W) * rows * W + off % W
         lbo = rows * 16 if mode == "none" else 16
         return SmemDesc(start=start, lbo=lbo, sbo=8 * W, base_offset=0, swz=SWZ_CODE[mode])
     if mode == "none":
         return SmemDesc(start=base + j * (kper // 8) * 128, lbo=128, sbo=bk * 16, base_offset=0, swz=0)
-    sbo = 8 * W
-    return SmemDesc(start=base + j * (kper // 8) * sbo, lbo=bk * W, sbo=sbo, base_offset=0, swz=SWZ_CODE[mode])
+    band = ATOM32_K_BAND if mode == ATOM32 else 8   # K rows between SBO steps
+    # the slice's kper K rows start kper rows (of W bytes) into the box
+    return SmemDesc(start=base + j * kper * W, lbo=bk * W, sbo=band * W, base_offset=0, swz=SWZ_CODE[mode])
 
 
 # ---------------------------------------------------------------------------

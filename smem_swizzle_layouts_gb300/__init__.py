@@ -9,7 +9,7 @@ from __future__ import annotations
 
 from ._lib import (  # noqa: F401
     ERR_ALIGNMENT, ERR_CUDA, ERR_INVALID_ARG, FP4_MXFP4, FP4_NVFP4, FP8_E4M3, FP8_E5M2, ERR_TIMEOUT, ERR_UNSUPPORTED, EXPORTED, K_MAJOR, LIB_PATH,
-    MN_MAJOR, NOALLOC_MAX_PROBLEMS, OK, OUT_BF16, OUT_F16, OUT_F32, SWIZZLE_128B, SWIZZLE_32B, SWIZZLE_64B, SWIZZLE_AUTO, SWIZZLE_NONE,
+    MN_MAJOR, NOALLOC_MAX_PROBLEMS, OK, OUT_BF16, OUT_F16, OUT_F32, SWIZZLE_128B, SWIZZLE_128B_ATOM32, SWIZZLE_32B, SWIZZLE_64B, SWIZZLE_AUTO, SWIZZLE_NONE,
     GemmCall, GemmError, GemmOptions, GemmProblem, gemm_bf16, gemm_bf16_grouped, gemm_bf16_grouped_noalloc, gemm_debug_descriptors,
     gemm_debug_inject_timeout, gemm_debug_stage_image, gemm_debug_streamk_units, gemm_ex, gemm_f16, gemm_f16_grouped, gemm_fp4, gemm_fp4_scale_bytes, gemm_fp8, gemm_fp8_ex,
     gemm_grouped_ex, gemm_grouped_workspace_size, gemm_mx_scale_bytes, gemm_mxfp8, gemm_streamk_workspace_size, gemm_last_device_status, gemm_launch_count, gemm_status_string,

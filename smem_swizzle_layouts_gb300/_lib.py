@@ -26,7 +26,7 @@ K_MAJOR, MN_MAJOR = 0, 1
 OUT_F32, OUT_BF16, OUT_F16 = 0, 1, 2
 FP8_E4M3, FP8_E5M2 = 0, 1
 FP4_NVFP4, FP4_MXFP4 = 0, 1
-SWIZZLE_AUTO, SWIZZLE_32B, SWIZZLE_64B, SWIZZLE_128B, SWIZZLE_NONE = 0, 1, 2, 3, 4
+SWIZZLE_AUTO, SWIZZLE_32B, SWIZZLE_64B, SWIZZLE_128B, SWIZZLE_NONE, SWIZZLE_128B_ATOM32 = 0, 1, 2, 3, 4, 5
 
 _i64, _vp, _f, _int, _u32, _u64 = (ctypes.c_int64, ctypes.c_void_p, ctypes.c_float, ctypes.c_int,
                                    ctypes.c_uint32, ctypes.c_uint64)

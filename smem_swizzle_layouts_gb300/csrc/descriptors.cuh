@@ -20,7 +20,8 @@
 //            K=16 slice j starts at (32 j / W) * rows * W + (32 j mod W).
 //   MN-major (BK x rows): boxes of W/2 MN-elements x BK K-rows, one after
 //            another along MN. LBO = BK W (next MN atom), SBO = 8 W (next
-//            8-row K band), slice j starts at j * 2 * SBO.
+//            8-row K band; 4 W for the 32-byte-atom mode's 4-row bands), and
+//            slice j starts at j * (32 / esize) * W.
 // Without swizzle (bits 0, W = 16) the 16-byte core-matrix cells are the
 // atoms: K-major LBO = rows * 16 (next K cell, one box away), SBO = 128 (next
 // 8-row group); MN-major LBO = 128 (next 8-row K band), SBO = BK * 16 (next
@@ -37,15 +38,24 @@
 
 namespace g300 {
 
-// Swizzle "bits" B: 1 = 32 B, 2 = 64 B, 3 = 128 B rows ("Swizzling explained
-// properly": Swizzle<B,4,3>).
-G300_HD uint32_t swizzle_row_bytes(int bits) { return 16u << bits; }
+// Swizzle "bits" B: 1 = 32 B, 2 = 64 B, 3 = 128 B rows of 16-byte atoms
+// ("Swizzling explained properly": Swizzle<B,4,3>). The value kSwzAtom32
+// stands for the 128-byte rows of 32-byte atoms (Swizzle<2,5,2>: the 32-byte
+// unit of a row is XORed with the row index mod 4), descriptor code 1, read
+// for MN-major operands whose K rows come in bands of kAtom32KBand. The GEMM
+// kernels do not issue MMAs on such operands (a kind::f16 or kind::f8f6f4
+// MMA reads them as zeros on GB300); the builder serves the inspection
+// entry points.
+constexpr int kSwzAtom32 = 4;
+constexpr int kAtom32KBand = 4;
+
+G300_HD uint32_t swizzle_row_bytes(int bits) { return bits == kSwzAtom32 ? 128u : 16u << bits; }
 
 // Raw descriptor code of a swizzle mode (LBO/SBO page, section 4):
-// none 0, SW32 6, SW64 4, SW128 2.
+// none 0, SW32 6, SW64 4, SW128 2, 128 B with 32-byte atoms 1.
 G300_HD uint32_t swizzle_code(int bits)
 {
-    return bits == 3 ? 2u : bits == 2 ? 4u : bits == 1 ? 6u : 0u;
+    return bits == kSwzAtom32 ? 1u : bits == 3 ? 2u : bits == 2 ? 4u : bits == 1 ? 6u : 0u;
 }
 
 G300_HD uint64_t make_smem_desc(uint32_t smem_addr, uint32_t lbo_bytes, uint32_t sbo_bytes,
@@ -77,7 +87,9 @@ G300_HD OperandPacking operand_packing(int mn_major, int swz_bits, int rows, int
         return p;
     }
     p.lbo = mn_major ? static_cast<uint32_t>(bk) * W : 16u;
-    p.sbo = 8u * W;
+    // SBO steps over one band of K rows (MN-major) or 8 rows (K-major); the
+    // stage holds its rows contiguously, so a band is its rows times W
+    p.sbo = static_cast<uint32_t>(swz_bits == kSwzAtom32 ? kAtom32KBand : 8) * W;
     return p;
 }
 

@@ -143,7 +143,8 @@ CUtensorMapDataType out_dtype(int d_type)
 
 CUtensorMapSwizzle tma_swizzle(int bits)
 {
-    return bits == 3 ? CU_TENSOR_MAP_SWIZZLE_128B
+    return bits == kSwzAtom32 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B
+           : bits == 3 ? CU_TENSOR_MAP_SWIZZLE_128B
            : bits == 2 ? CU_TENSOR_MAP_SWIZZLE_64B
            : bits == 1 ? CU_TENSOR_MAP_SWIZZLE_32B
                        : CU_TENSOR_MAP_SWIZZLE_NONE;
@@ -211,7 +212,7 @@ gemm_status_t encode_operand(CUtensorMap *m, int dcode, const void *ptr, int mn_
                                    : dcode == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const uint32_t esize = dcode == 2 ? 1u : 2u;
-    const uint32_t per = (16u << swz_bits) / esize;
+    const uint32_t per = swizzle_row_bytes(swz_bits) / esize;
     if (!mn_major)
         return encode_2d(m, dt, ptr, static_cast<uint64_t>(k_total), static_cast<uint64_t>(mn_total),
                          static_cast<uint64_t>(ld) * esize, per, static_cast<uint32_t>(rows),
@@ -259,8 +260,12 @@ struct Plan {
     size_t workspace_bytes;
 };
 
-// gemm_swizzle_t -> swizzle bits (B of Swizzle<B,4,3>): 32B 1, 64B 2, 128B 3, none 0.
-int swz_bits_of(int opt) { return opt == GEMM_SWIZZLE_NONE ? 0 : opt; }
+// gemm_swizzle_t -> swizzle bits (B of Swizzle<B,4,3>): 32B 1, 64B 2, 128B 3, none 0;
+// 128B with 32-byte atoms kSwzAtom32.
+int swz_bits_of(int opt)
+{
+    return opt == GEMM_SWIZZLE_NONE ? 0 : opt == GEMM_SWIZZLE_128B_ATOM32 ? kSwzAtom32 : opt;
+}
 
 // Choose the tile configuration; fills `plan` or returns an error for options
 // the compiled kernel variants cannot honour.
@@ -271,7 +276,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
     if (o)
         opt = *o;
     if (opt.cta_group < 0 || opt.cta_group > 2 || opt.tile_n < 0 || opt.swizzle_a < 0 ||
-        opt.swizzle_a > 4 || opt.swizzle_b < 0 || opt.swizzle_b > 4 || opt.max_ctas < 0 ||
+        opt.swizzle_a > 5 || opt.swizzle_b < 0 || opt.swizzle_b > 5 || opt.max_ctas < 0 ||
         opt.group_m < 0 || opt.timeout_ms < 0 || opt.epilogue_swizzle < -1 ||
         opt.epilogue_swizzle > 1 || opt.flags < 0 || opt.flags > 31 || opt.block_k < 0 ||
         opt.stream_k < -1 || opt.stream_k > 3)
@@ -362,9 +367,13 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
     plan->a_swz = pick_swz(opt.swizzle_a, a_mn, bm);
     plan->b_swz = pick_swz(opt.swizzle_b, b_mn, bn / cg);
     // a K-major swizzled row may not be wider than the K block; an MN-major
-    // atom may not be wider than the tile's MN extent
+    // atom may not be wider than the tile's MN extent. The 32-byte-atom mode
+    // is not an operand layout of the MMA kinds issued here: on GB300 a
+    // kind::f16 or kind::f8f6f4 MMA reads such an operand as zeros
     auto fits = [&](int bits, int mn_major, int rows) {
-        const int per = (16 << bits) / esize;
+        if (bits == kSwzAtom32)
+            return false;
+        const int per = static_cast<int>(swizzle_row_bytes(bits)) / esize;
         return mn_major ? (rows % per == 0) : (bk % per == 0);
     };
     if (!fits(plan->a_swz, a_mn, bm) || !fits(plan->b_swz, b_mn, bn / cg))
@@ -1046,7 +1055,7 @@ gemm_status_t gemm_debug_descriptors(int major, int swizzle, int rows, int bk, u
                                      int n_slices, int cta_group, int tile_n, int in_type, int a_major,
                                      int b_major, uint64_t *out, gemm_stream_t stream)
 {
-    if (!valid_enum(major) || swizzle < 1 || swizzle > 4 || rows <= 0 || bk <= 0 || n_slices < 0 ||
+    if (!valid_enum(major) || swizzle < 1 || swizzle > 5 || rows <= 0 || bk <= 0 || n_slices < 0 ||
         (cta_group != 1 && cta_group != 2) || tile_n <= 0 || !out || in_type < 0 || in_type > 3 ||
         !valid_enum(a_major) || !valid_enum(b_major))
         return GEMM_ERR_INVALID_ARG;
@@ -1067,12 +1076,12 @@ gemm_status_t gemm_debug_stage_image(const void *src, int major, int swizzle, in
                                      int64_t k_total, int64_t ld, int rows, int bk, int64_t mn0, int64_t k0,
                                      void *out, gemm_stream_t stream)
 {
-    if (!src || !out || !valid_enum(major) || swizzle < 1 || swizzle > 4 || rows <= 0 || rows > 256 ||
+    if (!src || !out || !valid_enum(major) || swizzle < 1 || swizzle > 5 || rows <= 0 || rows > 256 ||
         bk <= 0 || bk > 256 || rows_total <= 0 || k_total <= 0 || mn0 < 0 || k0 < 0 ||
         mn0 > INT32_MAX || k0 > INT32_MAX || rows_total > INT32_MAX || k_total > INT32_MAX)
         return GEMM_ERR_INVALID_ARG;
     const int bits = swz_bits_of(swizzle);
-    const int per = (16 << bits) / 2;
+    const int per = static_cast<int>(swizzle_row_bytes(bits)) / 2;
     if (major == GEMM_K_MAJOR ? (bk % per != 0) : (rows % per != 0))
         return GEMM_ERR_UNSUPPORTED;
     if (ld < (major == GEMM_K_MAJOR ? k_total : rows_total))

@@ -88,7 +88,7 @@ struct KParams {
     int tiles_m, tiles_n, num_tiles;
     float alpha, beta;
     int a_mn, b_mn;        // 0 K-major, 1 MN-major
-    int a_swz, b_swz;      // swizzle bits: 0 none, 1 SW32, 2 SW64, 3 SW128
+    int a_swz, b_swz;      // swizzle bits: 0 none, 1 SW32, 2 SW64, 3 SW128, 4 SW128 with 32-byte atoms
     int a_fmt, b_fmt;      // MMA operand formats (kind::f16: 0 fp16, 1 bf16; kind::f8f6f4: 0 E4M3, 1 E5M2)
     int out_type;          // 0 f32, 1 bf16, 2 f16
     int epi_swizzle;       // 1: staging chunks in SW128 layout; 0: plain rows
@@ -474,7 +474,7 @@ struct OperandBoxes {
 __device__ __forceinline__ OperandBoxes operand_boxes(int mn_major, int swz_bits, int rows, int bk,
                                                       int esize)
 {
-    const int W = 16 << swz_bits;
+    const int W = static_cast<int>(swizzle_row_bytes(swz_bits));
     const int per = W / esize;  // elements per swizzled row
     OperandBoxes o;
     o.mn_major = mn_major;

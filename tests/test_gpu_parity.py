@@ -29,7 +29,7 @@ def g():
 
 
 DEV = "cuda:0"
-SWZ_PARAM = {"sw32": 1, "sw64": 2, "sw128": 3, "none": 4}  # gemm_swizzle_t
+SWZ_PARAM = {"sw32": 1, "sw64": 2, "sw128": 3, "none": 4, "sw128_base32b": 5}  # gemm_swizzle_t
 TDT = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}
 
 
@@ -122,12 +122,14 @@ def sample_entries(M, N, n=2048, seed=0):
 # ---------------------------------------------------------------- address tables (bit-exact)
 
 @pytest.mark.parametrize("major", ["K", "MN"])
-@pytest.mark.parametrize("mode", ["sw32", "sw64", "sw128", "none"])
+@pytest.mark.parametrize("mode", ["sw32", "sw64", "sw128", "none", "sw128_base32b"])
 @pytest.mark.parametrize("rows,bk", [(128, 64), (256, 64), (128, 32), (64, 64), (128, 128)])
 def test_device_descriptor_words_match_oracle(g, major, mode, rows, bk):
     W = L.swizzle_width(mode)
     if major == "K" and W > 2 * bk:
         pytest.skip("swizzled K row wider than the K block")
+    if major == "K" and mode == L.ATOM32:
+        pytest.skip("the 32-byte-atom mode is read for MN-major operands only")
     if major == "MN" and rows % (W // 2):
         pytest.skip("MN atom wider than the tile")
     n = bk // 16
@@ -174,9 +176,10 @@ def _stage_image(g, major, mode, rows, bk, rows_total=None, k_total=None, mn0=0,
 
 
 @pytest.mark.parametrize("major", ["K", "MN"])
-@pytest.mark.parametrize("mode", ["sw32", "sw64", "sw128", "none"])
+@pytest.mark.parametrize("mode", ["sw32", "sw64", "sw128", "none", "sw128_base32b"])
 @pytest.mark.parametrize("rows,bk", [(128, 64), (128, 32), (256, 64), (128, 128)])
 def test_tma_stage_image_matches_swizzle_map(g, major, mode, rows, bk):
+    # sw128_base32b: TMA's 128B_ATOM_32B mode against the oracle's Swizzle(2, 5, 2)
     W = L.swizzle_width(mode)
     if (major == "K" and W > 2 * bk) or (major == "MN" and rows % (W // 2)):
         pytest.skip("box wider than the stage")
@@ -433,12 +436,14 @@ def test_small_m_defaults_to_64_row_tiles(g):
 # ---------------------------------------------------------------- fp8 operands (kind::f8f6f4)
 
 @pytest.mark.parametrize("major", ["K", "MN"])
-@pytest.mark.parametrize("mode", ["sw64", "sw128", "none"])
+@pytest.mark.parametrize("mode", ["sw64", "sw128", "none", "sw128_base32b"])
 @pytest.mark.parametrize("rows,bk", [(128, 128), (128, 256), (256, 128)])
 def test_fp8_descriptor_words_match_oracle(g, major, mode, rows, bk):
     W = L.swizzle_width(mode)
     if (major == "K" and W > bk) or (major == "MN" and rows % W):
         pytest.skip("box wider than the stage")
+    if major == "K" and mode == L.ATOM32:
+        pytest.skip("the 32-byte-atom mode is read for MN-major operands only")
     n = bk // 32
     out = torch.zeros(n + 1, dtype=torch.int64, device=DEV)
     g.gemm_debug_descriptors(0 if major == "K" else 1, SWZ_PARAM[mode], rows, bk, 8192, n, 1, 256, 2, 0, 1, out)

@@ -384,3 +384,70 @@ def test_fp8_stage_packing_matches_descriptor_for_every_slice(major, mode, rows,
 def test_idesc_mixed_ab_formats():
     w = L.encode_idesc(128, 128, L.FMT_E4M3, L.DFMT_F32, 0, 1, b_fmt=L.FMT_E5M2)
     assert (w >> 7) & 7 == 0 and (w >> 10) & 7 == 1 and (w >> 16) & 1 == 1
+
+
+# ---------------------------------------------------------------------------
+# The 128-byte swizzle with 32-byte atoms (raw SWZ value 1; "LBO, SBO and SWZ
+# for a tcgen05 tile", section 4, read through "What about base?").
+# ---------------------------------------------------------------------------
+
+def test_atom32_functor_is_the_4x4_xor_grid_of_32_byte_atoms():
+    sw = L.SWIZZLE[L.ATOM32]
+    assert (sw.bits, sw.base, sw.shift) == (2, 5, 2)
+    for r in range(4):
+        for c in range(4):
+            for b in range(32):           # every byte of the atom moves with it
+                off = r * 128 + c * 32 + b
+                assert sw(off) == r * 128 + L.xor_grid(r, c)[1] * 32 + b
+    # a bijection on each 512-byte pattern, repeating every 512 bytes, 16-byte cells stay whole
+    span = list(range(4096))
+    out = [sw(o) for o in span]
+    assert sorted(out) == span
+    assert all(out[o + 512] == out[o] + 512 for o in range(4096 - 512))
+    assert L.swizzle_repeat(L.ATOM32) == 512 and L.swizzle_width(L.ATOM32) == 128
+
+
+def test_atom32_interpreter_xor_equals_the_functor_on_absolute_addresses():
+    sw = L.SWIZZLE[L.ATOM32]
+    for addr in range(0, 1 << 13, 16):
+        assert L._xor_absolute(addr, 2, 5) == sw(addr)
+        # pattern-relative form with MBO = the start's row phase gives the same address
+        for start in (0, 128, 256, 384, 1024):
+            if addr >= start:
+                assert L._xor_relative(addr, start, (start >> 7) & 3, 2, 5) == sw(addr)
+
+
+def test_atom32_column_reads_spread_over_four_32_byte_units():
+    # reading one 32-byte unit of 4 consecutive 128-byte rows touches 4 distinct units
+    sw = L.SWIZZLE[L.ATOM32]
+    for c in range(4):
+        assert len({sw(r * 128 + c * 32) % 128 for r in range(4)}) == 4
+
+
+@pytest.mark.parametrize("esize", [2, 1])
+@pytest.mark.parametrize("rows,bk", [(128, 64), (256, 64), (128, 128), (64, 256)])
+def test_atom32_mn_major_stage_packing_matches_descriptor(esize, rows, bk):
+    if esize == 2 and bk > 128:
+        pytest.skip("16-bit stages of this width are not built")
+    if rows % (128 // esize):
+        pytest.skip("an MN atom (128 bytes of MN) wider than the tile")
+    kper = 32 // esize
+    seen = set()
+    for j in range(bk // kper):
+        d = L.stage_slice_desc("MN", L.ATOM32, rows, bk, esize, j, P_BASE)
+        assert d.swz == 1 and d.sbo == L.ATOM32_K_BAND * 128 and d.lbo == bk * 128
+        for mn in range(rows):
+            for kk in range(kper):
+                addr = L.desc_element_addr(d, "MN", esize, mn, kk)
+                assert addr == P_BASE + L.stage_element_offset("MN", L.ATOM32, rows, bk, esize, mn, kper * j + kk)
+                assert addr == L.desc_element_addr_relative(d, "MN", esize, mn, kk, pattern_start=P_BASE)
+                seen.add(addr)
+    assert len(seen) == rows * bk and min(seen) == P_BASE and max(seen) < P_BASE + rows * bk * esize
+
+
+def test_atom32_is_not_offered_for_k_major_operands():
+    with pytest.raises(ValueError):
+        L.stage_slice_desc("K", L.ATOM32, 128, 64, 2, 0, P_BASE)
+    d = L.SmemDesc(start=P_BASE, lbo=16, sbo=1024, base_offset=0, swz=1)
+    with pytest.raises(ValueError):
+        L.desc_element_addr(d, "K", 2, 0, 0)

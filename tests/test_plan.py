@@ -103,8 +103,19 @@ def test_block_scaled_formats_have_fixed_tiles(g):
 
 def test_invalid_options_are_rejected(g):
     for opts, status in [(dict(flags=32), g.ERR_INVALID_ARG), (dict(stream_k=4), g.ERR_INVALID_ARG),
-                         (dict(swizzle_a=5), g.ERR_INVALID_ARG), (dict(tile_m=96), g.ERR_INVALID_ARG),
+                         (dict(swizzle_a=6), g.ERR_INVALID_ARG), (dict(tile_m=96), g.ERR_INVALID_ARG),
                          (dict(workspace=0x1010), g.ERR_ALIGNMENT), (dict(tile_n=96), g.ERR_UNSUPPORTED)]:
         with pytest.raises(g.GemmError) as ei:
             plan(g, 1024, 1024, 1024, **opts)
         assert ei.value.status == status, opts
+
+
+def test_32_byte_atom_swizzle_is_refused_for_gemm_operands(g):
+    # GEMM_SWIZZLE_128B_ATOM32 (descriptor code 1) is read as zeros by the MMA kinds the
+    # library issues, so the planner refuses it for either operand and major
+    for kind in (BF16, FP8):
+        for a, b, opts in ((MN_MAJOR, MN_MAJOR, dict(swizzle_a=5)), (MN_MAJOR, MN_MAJOR, dict(swizzle_b=5)),
+                           (K_MAJOR, K_MAJOR, dict(swizzle_a=5))):
+            with pytest.raises(g.GemmError) as ei:
+                plan(g, 1024, 1024, 1024, kind, a=a, b=b, **opts)
+            assert ei.value.status == g.ERR_UNSUPPORTED, (kind, opts)
