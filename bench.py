@@ -57,6 +57,11 @@ WORKLOADS = {
     "skinny_m128_n16384_k4096": dict(
         M=128, N=16384, K=4096, a_major="K", b_major="K", out="bf16", alpha=1.0, beta=0.0, dist="normal",
         scale=1.0, seed=31, options=None, bound="hbm", desc="M=128 N=16384 K=4096 bf16, N(0,1), bf16 out"),
+    "smallm_m32_n16384_k8192": dict(
+        M=32, N=16384, K=8192, a_major="K", b_major="K", out="bf16", alpha=1.0, beta=0.0, dist="normal",
+        scale=1.0, seed=32, options=None, bound="hbm",
+        desc="M=32 N=16384 K=8192 bf16 (a decode-like small-M shape: B streamed from HBM), N(0,1), bf16 out, "
+             "default plan: weight-stationary tcgen05.mma.ws tiles of 64 x 128"),
     "grouped64_n4096_k2048": dict(
         kind="grouped", M=0, N=4096, K=2048, problems=64, m_seed=5, a_major="K", b_major="K", out="bf16",
         alpha=1.0, beta=0.0, dist="uniform", scale=1.0, seed=100, options=None,

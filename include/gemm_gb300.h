@@ -92,7 +92,9 @@ typedef enum {
  *   tile_m        accumulator rows per CTA: 128, or 64 (cta_group::1 only:
  *                 tcgen05.mma M = 64 with the TMEM accumulator in Layout F,
  *                 "06 Blackwell Tensor Core - tcgen05 MMA", cta_group::1
- *                 M = 64; default for M <= 64 with 16-bit operands).
+ *                 M = 64; default for M <= 64 with 16-bit operands), or 32
+ *                 (the weight-stationary tcgen05.mma.ws with M = 32; 16-bit
+ *                 operands, single problems, tile_n 256).
  *   tile_n        MMA N per tile: 64, 128 or 256 (cta_group::2: 128 or 256).
  *   block_k       K elements per pipeline stage: 32, 64 or 128 where built.
  *   swizzle_a/b   operand swizzle (gemm_swizzle_t).
@@ -107,7 +109,10 @@ typedef enum {
  *                 mbarrier arrives (ablation), bit 1 makes every wait
  *                 acquire at cluster scope (ablation). Bit 2 starts each
  *                 tile's K loop at a per-CTA offset so that CTAs sharing an
- *                 operand panel read different parts of it at a time.
+ *                 operand panel read different parts of it at a time; with
+ *                 flags 0 the library sets it for single problems of at most
+ *                 one wave of tiles and at least 16 K blocks (HBM-bound
+ *                 shapes such as 16384 x 128 x 8192).
  *                 Bit 3 gives the operand loads an L2 evict_last policy and
  *                 the C loads and D stores evict_first (ablation; no
  *                 measured effect at 4096^3 or 8192^3). Bit 4 (single
@@ -146,6 +151,15 @@ typedef enum {
  *                 (the library leaves it reusable: each launch tags its
  *                 flags with a new value). Calls that may run at the same
  *                 time, on different streams, need different workspaces.
+ *   mma_ws        weight-stationary MMA (tcgen05.mma.ws, "How cta_group Sets
+ *                 the Operation Scope": one of the choices that fix the
+ *                 accumulator layout): 0 the library chooses, 1 use it,
+ *                 -1 do not. It serves tiles of 32 or 64 rows of single
+ *                 problems with 16-bit operands on one CTA (tile_n 128 or 256
+ *                 for 64 rows, 256 for 32); its accumulator is spread over
+ *                 the four TMEM lane quarters by column parts, so all four
+ *                 epilogue warps store full 32-row chunks. Other tiles with
+ *                 mma_ws 1 return GEMM_ERR_UNSUPPORTED.
  */
 typedef struct {
     int cta_group;
@@ -163,6 +177,7 @@ typedef struct {
     int stream_k;
     void *workspace;
     size_t workspace_bytes;
+    int mma_ws;
 } gemm_options_t;
 
 /* Bytes of stream-K workspace for any single GEMM on the current device:
@@ -439,9 +454,10 @@ gemm_status_t gemm_debug_stage_image(const void *src, int major, int swizzle,
  * Host-side tile plan (no GPU needed): the configuration a call would launch
  * on a device with `sms` SMs. kind: 0 fp16/bf16, 1 fp8, 2 MXFP8, 3 NVFP4,
  * 4 MXFP4 (K in elements); grouped: nonzero for the grouped entry points.
- * Writes 8 int32: cta_group, tile N, K per stage (bytes for fp4), rows per
- * CTA, swizzle bits of A and B (0 none, 1 32B, 2 64B, 3 128B), epilogue
- * swizzle, group height. Returns the status the call's planning would.
+ * Writes 9 int32: cta_group, tile N, K per stage (bytes for fp4), rows per
+ * CTA, swizzle bits of A and B (0 none, 1 32B, 2 64B, 3 128B, 4 128B with
+ * 32-byte atoms), epilogue swizzle, group height, and 1 when the tiles use
+ * tcgen05.mma.ws. Returns the status the call's planning would.
  */
 gemm_status_t gemm_debug_plan(int64_t M, int64_t N, int64_t K, int kind, int a_major, int b_major, int grouped,
                               const gemm_options_t *opts, int sms, int32_t *out);

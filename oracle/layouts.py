@@ -43,6 +43,8 @@ Readings where the pages are silent (each listed in the design notes):
   absolute shared-memory address (B = 1, 2, 3 for SW32/64/128).
 * Layout B columns: the page gives only the lane; the column is read as
   ``n mod (N/2)``.
+* The .ws accumulator (``tmem_ws``): the page names it without printing it;
+  read as column parts spread over the lane quarters (see the function).
 """
 from __future__ import annotations
 
@@ -482,6 +484,27 @@ def tmem_cta2_m256(m: int, n: int) -> tuple[int, int, int]:
 def tmem_layout_b(m: int, n: int, N: int) -> tuple[int, int, int]:
     half = N // 2
     return m // 64, m % 64 + (64 if n >= half else 0), n % half
+
+
+def tmem_ws(m: int, n: int, M: int, N: int) -> tuple[int, int, int]:
+    """Accumulator map of the weight-stationary tcgen05.mma.ws (cta_group::1).
+
+    The page lists .ws among the four choices that fix the accumulator layout
+    but prints only the ordinary layouts. Reading (recorded with the other
+    readings): for M = 128 the .ws accumulator is the M = 128 one (row m in
+    lane m); for M = 32 and 64 the 128 lanes are filled by cutting N into
+    4 / (M / 32) equal column parts. Lane quarter q holds row block q % (M/32)
+    (rows 32 (q % (M/32)) .. +31) of column part q // (M/32), so every quarter
+    holds whole 32-row blocks and the accumulator takes N / parts columns.
+    """
+    if M == 128:
+        return 0, m, n
+    if M not in (32, 64):
+        raise ValueError(".ws accumulators have 32, 64 or 128 rows")
+    row_blocks = M // 32
+    width = N // (4 // row_blocks)
+    q = (n // width) * row_blocks + m // 32
+    return 0, 32 * q + m % 32, n % width
 
 
 def tmem_warp_lanes(warp: int) -> range:

@@ -42,13 +42,14 @@ struct Variant {
     int esize;
     int bm;
     int sf;  // scale kind (kScale*)
+    int ws;  // 1: tcgen05.mma.ws (weight-stationary accumulator layout)
     cudaError_t (*launch)(const LaunchArgs &);
     cudaError_t (*resident)(int *);
     int resident_cache[kMaxDevices];
 };
 
-#define G300_VARIANT_ROW(CG, BN, BK, ST, GR, ES, BM, SF) \
-    {CG, BN, BK, ST, GR, ES, BM, SF, &launch_gemm<CG, BN, BK, ST, GR, ES, BM, SF>, &resident_ctas<CG, BN, BK, ST, GR, ES, BM, SF>, {0}},
+#define G300_VARIANT_ROW(CG, BN, BK, ST, GR, ES, BM, SF, WS) \
+    {CG, BN, BK, ST, GR, ES, BM, SF, WS, &launch_gemm<CG, BN, BK, ST, GR, ES, BM, SF, WS>, &resident_ctas<CG, BN, BK, ST, GR, ES, BM, SF, WS>, {0}},
 Variant g_variants[] = {G300_VARIANTS(G300_VARIANT_ROW)};
 #undef G300_VARIANT_ROW
 
@@ -103,11 +104,12 @@ int resident_for(Variant &v, int dev)
     return v.resident_cache[dev];
 }
 
-Variant *find_variant(int cg, int bn, int bk, bool grouped, int esize = 2, int bm = 128, int sf = kScaleNone)
+Variant *find_variant(int cg, int bn, int bk, bool grouped, int esize = 2, int bm = 128, int sf = kScaleNone,
+                      int ws = 0)
 {
     for (auto &v : g_variants)
         if (v.cg == cg && v.bn == bn && v.bk == bk && v.grouped == grouped && v.esize == esize && v.bm == bm &&
-            v.sf == sf)
+            v.sf == sf && v.ws == ws)
             return &v;
     return nullptr;
 }
@@ -247,7 +249,8 @@ gemm_status_t encode_output(CUtensorMap *m, int d_type, const void *ptr, int64_t
 
 struct Plan {
     int cg, bn, bk;
-    int bm;  // accumulator rows per CTA: 128, or 64 (M = 64 MMAs)
+    int bm;  // accumulator rows per CTA: 128, 64 (M = 64 MMAs) or 32 (.ws only)
+    int ws;  // 1: tcgen05.mma.ws
     int a_swz, b_swz;
     int epi_swizzle;
     int max_ctas;
@@ -279,17 +282,17 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
         opt.swizzle_a > 5 || opt.swizzle_b < 0 || opt.swizzle_b > 5 || opt.max_ctas < 0 ||
         opt.group_m < 0 || opt.timeout_ms < 0 || opt.epilogue_swizzle < -1 ||
         opt.epilogue_swizzle > 1 || opt.flags < 0 || opt.flags > 31 || opt.block_k < 0 ||
-        opt.stream_k < -1 || opt.stream_k > 3)
+        opt.stream_k < -1 || opt.stream_k > 3 || opt.mma_ws < -1 || opt.mma_ws > 1)
         return GEMM_ERR_INVALID_ARG;
     if (opt.workspace && (reinterpret_cast<uintptr_t>(opt.workspace) & 255u) != 0)
         return GEMM_ERR_ALIGNMENT;
 
-    if (opt.tile_m != 0 && opt.tile_m != 64 && opt.tile_m != 128)
+    if (opt.tile_m != 0 && opt.tile_m != 32 && opt.tile_m != 64 && opt.tile_m != 128)
         return GEMM_ERR_INVALID_ARG;
     int cg = opt.cta_group;
-    if (opt.tile_m == 64 && cg == 2)
+    if ((opt.tile_m == 64 || opt.tile_m == 32) && cg == 2)
         return GEMM_ERR_UNSUPPORTED;
-    if (opt.tile_m == 64)
+    if (opt.tile_m == 64 || opt.tile_m == 32)
         cg = 1;
     if (cg == 0) {
         // CTA pairs for large problems: each SM then loads half of B.
@@ -328,6 +331,25 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
                         : (cg == 1 && M <= 64 && esize == 2 && !grouped && bn >= 128 ? 64 : 128);
     if (bm == 64 && opt.block_k == 0)
         bk = bn == 256 ? 64 : 128;
+    // Weight-stationary tiles (tcgen05.mma.ws): 32 rows (M = 32 exists only in
+    // the .ws form) when asked for, or 64 rows; single CTAs, 16-bit operands,
+    // single problems. 32-row tiles are 256 wide so that each epilogue warp
+    // holds whole 64-column chunks of its column part. The .ws form is the
+    // default for the 64 x 128 tiles of M <= 64 (32 x 16384 x 8192: 0.79 of
+    // the measured HBM rate against 0.77 for Layout F and 0.71 for 32 x 256
+    // .ws tiles); an explicit tile_m 64 keeps the page's Layout F.
+    int ws = 0;
+    const bool ws_default = opt.mma_ws == 0 && opt.tile_m == 0 && bm == 64 && bn == 128;
+    if (opt.tile_m == 32 || opt.mma_ws == 1 || ws_default) {
+        if (opt.mma_ws == -1 || opt.tile_m == 128 || sf != kScaleNone || esize != 2 || grouped || cg != 1)
+            return GEMM_ERR_UNSUPPORTED;
+        ws = 1;
+        bm = opt.tile_m ? opt.tile_m : 64;
+        if (bm == 32)
+            bn = opt.tile_n ? opt.tile_n : 256;
+        if (opt.block_k == 0)
+            bk = bn == 256 ? 64 : 128;
+    }
     if (sf != kScaleNone) {
         // Block-scaled tiles: 256 x 256 CTA pairs with one accumulator buffer
         // (the default from 2048 rows and columns; MXFP8 8192^3 2588 against
@@ -350,7 +372,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
             bn = 128;
         }
     }
-    if (!find_variant(cg, bn, bk, grouped, esize, bm, sf))
+    if (!find_variant(cg, bn, bk, grouped, esize, bm, sf, ws))
         return GEMM_ERR_UNSUPPORTED;
 
     // the widest swizzle whose row fits the stage: along K for K-major
@@ -379,11 +401,23 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
     if (!fits(plan->a_swz, a_mn, bm) || !fits(plan->b_swz, b_mn, bn / cg))
         return GEMM_ERR_UNSUPPORTED;
     plan->bm = bm;
+    plan->ws = ws;
     plan->epi_swizzle = opt.epilogue_swizzle == -1 ? 0 : 1;
     plan->max_ctas = opt.max_ctas;
     plan->group_m = opt.group_m ? opt.group_m : 8;
     plan->timeout_ns = static_cast<unsigned long long>(opt.timeout_ms ? opt.timeout_ms : 2000) * 1000000ull;
     plan->flags = opt.flags;
+    // Problems of at most one wave of tiles with long K stream their operands
+    // from HBM (each tile reads its own panel once): every CTA then starts its
+    // K loop at its own offset, so that the CTAs do not all request the same
+    // columns of their row panels at the same moment (16384 x 128 x 8192:
+    // 0.70 -> 0.75 of the measured HBM rate). Explicit flags are kept as given.
+    if (opt.flags == 0 && !grouped) {
+        const int64_t tiles = ((M + bm * cg - 1) / (bm * cg)) * ((N + bn - 1) / bn);
+        const int64_t kblocks = (K + bk - 1) / bk;
+        if (tiles <= sms / cg && kblocks >= 16)
+            plan->flags |= kFlagRotateK;
+    }
     plan->stats = opt.stats;
     plan->stream_k = opt.stream_k;
     plan->workspace = opt.workspace;
@@ -515,7 +549,8 @@ gemm_status_t run_single(const InFmt &f, int64_t M, int64_t N, int64_t K, const 
     Plan pl;
     if ((s = make_plan(M, N, K, a_mn, b_mn, sms, opts, false, &pl, f.esize, f.sf)) != GEMM_OK)
         return s;
-    Variant *v = find_variant(pl.cg, pl.bn, pl.bk, false, f.esize, pl.bm, f.sf);
+    Variant *v = find_variant(pl.cg, pl.bn, pl.bk, false, f.esize, pl.bm, f.sf, pl.ws);
+    const int epi_rows = pl.ws ? 32 : pl.bm / 4;  // output rows one epilogue warp stores per chunk
 
     LaunchArgs la;
     std::memset(&la, 0, sizeof(la));
@@ -526,10 +561,10 @@ gemm_status_t run_single(const InFmt &f, int64_t M, int64_t N, int64_t K, const 
             GEMM_OK)
             return s;
     }
-    if ((s = encode_output(&la.d, d_type, D, M, N, ldd, pl.epi_swizzle, pl.bm / 4)) != GEMM_OK)
+    if ((s = encode_output(&la.d, d_type, D, M, N, ldd, pl.epi_swizzle, epi_rows)) != GEMM_OK)
         return s;
     if (beta != 0.0f) {
-        if ((s = encode_output(&la.c, d_type, C, M, N, ldc, pl.epi_swizzle, pl.bm / 4)) != GEMM_OK)
+        if ((s = encode_output(&la.c, d_type, C, M, N, ldc, pl.epi_swizzle, epi_rows)) != GEMM_OK)
             return s;
     } else {
         la.c = la.d;
@@ -1133,6 +1168,7 @@ gemm_status_t gemm_debug_plan(int64_t M, int64_t N, int64_t K, int kind, int a_m
     out[5] = pl.b_swz;
     out[6] = pl.epi_swizzle;
     out[7] = pl.group_m;
+    out[8] = pl.ws;
     return GEMM_OK;
 }
 

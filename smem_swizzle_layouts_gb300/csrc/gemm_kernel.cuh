@@ -183,7 +183,7 @@ __host__ __device__ constexpr int sf_atom_kbytes(int sf)
 // rows per CTA, 128 (row m in TMEM lane m) or 64 (cta_group::1 only, Layout F:
 // rows 16g..16g+15 in lanes 32g+a..32g+a+15; the two accumulators of the
 // double buffer take lane alignments a = 0 and 16 and share their columns).
-template <int CG, int BN, int BK, int STAGES, int ESIZE = 2, int BMT = 128, int SF = 0>
+template <int CG, int BN, int BK, int STAGES, int ESIZE = 2, int BMT = 128, int SF = 0, int WS = 0>
 struct Cfg {
     static constexpr int BM = BMT;             // accumulator rows per CTA
     static constexpr int BN_LOCAL = BN / CG;   // B columns loaded by each CTA
@@ -225,10 +225,20 @@ struct Cfg {
     static constexpr int SF_COL0 = ACC_BUFS * BN;
     static constexpr int SF_GROUP_COLS = 4 + 4 * (BN / 128);  // A atom, then the B atoms of one K group
     static constexpr int SF_COLS = SF_GROUP_COLS * KGROUPS;
-    static constexpr int TMEM_COLS = BMT == 64 ? BN : SF ? 512 : 2 * BN;
+    // Weight-stationary tiles (WS, tcgen05.mma.ws with M = BM = 32 or 64): the
+    // accumulator is spread over the four TMEM lane quarters by column parts.
+    // Quarter q holds rows 32 (q % RB) .. +31 (RB = BM / 32 row blocks) of
+    // column part q / RB, COL_PARTS = 4 / RB parts of BN / COL_PARTS columns,
+    // at TMEM column n - part * (BN / COL_PARTS); one buffer takes ACC_COLS.
+    static constexpr int WS_ROW_BLOCKS = WS ? BM / 32 : 1;
+    static constexpr int COL_PARTS = WS ? 4 / WS_ROW_BLOCKS : 1;
+    static constexpr int ACC_COLS = BN / COL_PARTS;
+    static constexpr int TMEM_COLS = WS ? (2 * ACC_COLS < 32 ? 32 : 2 * ACC_COLS) : BMT == 64 ? BN : SF ? 512 : 2 * BN;
     static constexpr int UMMA_M = BM * CG;
-    static constexpr int EPI_ROWS = BM / 4;    // output rows per epilogue warp
-    static_assert(BMT == 128 || (BMT == 64 && CG == 1), "64-row tiles are single-CTA");
+    static constexpr int EPI_ROWS = WS ? 32 : BM / 4;    // output rows per epilogue warp
+    static_assert(BMT == 128 || (BMT == 64 && CG == 1) || (BMT == 32 && WS), "64-row tiles are single-CTA");
+    static_assert(!WS || ((BMT == 32 || BMT == 64) && CG == 1 && ESIZE == 2 && SF == 0 && (BN / COL_PARTS) % 64 == 0),
+                  ".ws tiles: 32 or 64 rows, single CTA, 16-bit operands, whole 64-column chunks per warp");
     static constexpr int KSLICES = BK * ESIZE / 32;  // MMAs per stage (32 bytes of K each)
     static_assert(STAGE_BYTES % 1024 == 0, "stages must stay 1024-aligned");
     static_assert(A_BYTES % 1024 == 0, "B tile must start 1024-aligned");
@@ -529,13 +539,13 @@ __device__ __forceinline__ int ceil_div_i(int a, int b) { return (a + b - 1) / b
 
 // ---------------------------------------------------------------- roles
 
-template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF>
+template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF, int WS>
 __device__ void role_producer(const KParams &p, const CUtensorMap *tmA, const CUtensorMap *tmB,
                               const CUtensorMap *tmSFA, const CUtensorMap *tmSFB,
                               uint32_t smem, uint32_t bar_full, uint32_t bar_empty,
                               uint32_t rank, const Waiter &w)
 {
-    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF>;
+    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, WS>;
     const Sched sched = make_sched(p);
     const int flags = p.flags;
     unsigned long long *const stats = p.stats;
@@ -674,11 +684,11 @@ __device__ void role_producer(const KParams &p, const CUtensorMap *tmA, const CU
 // waits on sf_ready before the stage's MMAs and so issues only MMAs. A
 // stage's scale columns are rewritten only after the stage was refilled, that
 // is after the MMAs that read their previous contents completed.
-template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF>
+template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF, int WS>
 __device__ void role_sf_copy(const KParams &p, uint32_t smem, uint32_t bar_full, uint32_t bar_sf,
                              uint32_t tmem_base, const Waiter &w, int copier)
 {
-    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF>;
+    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, WS>;
     if constexpr (SF != 0) {
         if (p.inject_timeout)
             return;
@@ -737,12 +747,12 @@ __device__ void role_sf_copy(const KParams &p, uint32_t smem, uint32_t bar_full,
     }
 }
 
-template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF>
+template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF, int WS>
 __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uint32_t bar_empty,
                          uint32_t bar_acc_full, uint32_t bar_acc_empty, uint32_t bar_inject, uint32_t bar_sf,
                          uint32_t tmem_base, const Waiter &w)
 {
-    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF>;
+    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, WS>;
     if (p.inject_timeout) {
         // Test hook: wait on a barrier nothing arrives at; the bound runs out.
         w.wait(bar_inject, 0u, kRoleMma | kWaitInjected);
@@ -788,8 +798,9 @@ __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uin
             ++st_tiles;
         }
         tc_fence_after_sync();
-        const uint32_t d_tmem = C::BM == 64 ? tmem_base + (static_cast<uint32_t>(16 * acc) << 16)
-                                            : tmem_base + static_cast<uint32_t>(acc * BN);
+        const uint32_t d_tmem = WS           ? tmem_base + static_cast<uint32_t>(acc * C::ACC_COLS)
+                                : C::BM == 64 ? tmem_base + (static_cast<uint32_t>(16 * acc) << 16)
+                                              : tmem_base + static_cast<uint32_t>(acc * BN);
         for (int kb = kb_lo; kb < kb_hi; ++kb) {
             if (stats) {
                 const long long t0 = clock64();
@@ -829,7 +840,10 @@ __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uin
 #pragma unroll
                 for (int j = 0; j < C::KSLICES; ++j) {
                     // the first MMA of a unit overwrites the accumulator, the rest add
-                    if constexpr (ESIZE == 2)
+                    if constexpr (WS)
+                        mma_ws_f16(d_tmem, a_desc0 + sdelta + a_off[j], b_desc0 + sdelta + b_off[j], idesc,
+                                   ((kb - kb_lo) | j) != 0);
+                    else if constexpr (ESIZE == 2)
                         mma_f16<CG>(d_tmem, a_desc0 + sdelta + a_off[j], b_desc0 + sdelta + b_off[j], idesc,
                                     ((kb - kb_lo) | j) != 0);
                     else
@@ -1065,13 +1079,13 @@ __device__ bool sk_gather(const Sched &sched, const Unit &ua, int n32, int buf, 
     return true;
 }
 
-template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF, int CW>
+template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF, int WS, int CW>
 __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CUtensorMap *tmD,
                               uint32_t epi_base, uint32_t bar_acc_full, uint32_t bar_acc_empty,
                               uint32_t bar_epi, uint32_t tmem_base, uint32_t rank, int warp,
                               int lane, const Waiter &w)
 {
-    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF>;
+    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, WS>;
     const Sched sched = make_sched(p);
     unsigned long long *const stats = p.stats;
     const CUtensorMap *const maps = p.maps;
@@ -1081,8 +1095,16 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
     ec.out_type = p.out_type;
     ec.key_mask = p.epi_swizzle ? 7u : 0u;
     const bool forward = CG == 2 && rank == 0 && (p.flags & kFlagPairForward);
-    const int q = warp & 3;   // TMEM lane quarter 32q..32q+31 = output rows EPI_ROWS*q..
+    const int q = warp & 3;   // TMEM lane quarter 32q..32q+31
     constexpr int R = C::EPI_ROWS;
+    // The rows and column chunks this warp stores: 128-row tiles and Layout F
+    // give each warp R rows (lane quarter q = rows R q..) of every chunk; .ws
+    // tiles give it 32 rows of one column part (rows 32 (q % RB) .., chunks
+    // [part * NCH / COL_PARTS, (part + 1) * NCH / COL_PARTS))
+    constexpr int NCH = BN / CW;
+    const int wrow = WS ? 32 * (q % C::WS_ROW_BLOCKS) : R * q;
+    const int c_lo = WS ? (q / C::WS_ROW_BLOCKS) * (NCH / C::COL_PARTS) : 0;
+    const int c_hi = c_lo + NCH / C::COL_PARTS;
     const int ew = warp - 2;  // staging slot
     const uint32_t buf0 = epi_base + static_cast<uint32_t>(ew * C::EPI_BUFS * kEpiBufBytes);
     const uint32_t ebar0 = bar_epi + static_cast<uint32_t>(16 * ew);
@@ -1142,11 +1164,12 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
             fence_tensormap_acquire(mD);
         }
         const bool has_acc = ti.K > 0;
-        const int m0 = ti.m_blk * C::UMMA_M + C::BM * static_cast<int>(rank) + R * q;
-        // 128-row tiles: thread t holds row t. 64-row tiles (Layout F): the
-        // accumulator with lane alignment 16*acc sits in threads 16*acc..+15.
-        const bool active = C::BM == 128 || (lane >> 4) == acc;
-        const int trow = C::BM == 128 ? lane : (lane & 15);
+        const int m0 = ti.m_blk * C::UMMA_M + C::BM * static_cast<int>(rank) + wrow;
+        // 128-row and .ws tiles: thread t holds row t of the warp's rows. 64-row
+        // tiles (Layout F): the accumulator with lane alignment 16*acc sits in
+        // threads 16*acc..+15.
+        const bool active = WS || C::BM == 128 || (lane >> 4) == acc;
+        const int trow = (WS || C::BM == 128) ? lane : (lane & 15);
         if (has_acc) {
             const long long tw = stats ? clock64() : 0;
             bool ok = w.wait(bar_acc_full + 8 * acc, acc_phase, kRoleEpilogue | kWaitAccFull, rank != 0);
@@ -1203,7 +1226,6 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
                 // One accumulator buffer, 16-bit output, no C: read the whole row
                 // and round it in registers first, then release the accumulator,
                 // so that the next tile's MMAs run while the stores drain.
-                constexpr int NCH = BN / CW;
                 uint32_t pk[NCH][32];
 #pragma unroll
                 for (int c = 0; c < NCH; ++c) {
@@ -1269,7 +1291,7 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
                 continue;
             }
         }
-        for (int c = 0; c < BN / CW; ++c) {
+        for (int c = c_lo; c < c_hi; ++c) {
             const int col0 = ti.n_blk * BN + c * CW;
             if (col0 >= ti.N)
                 break;
@@ -1293,7 +1315,8 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
             __syncwarp();  // tcgen05.ld is .sync.aligned: the warp must be converged
             float v[CW];
             if (has_acc) {
-                const uint32_t col = static_cast<uint32_t>((C::BM == 128 ? acc * BN : 0) + c * CW);
+                const uint32_t col = static_cast<uint32_t>(WS ? acc * C::ACC_COLS + (c - c_lo) * CW
+                                                              : (C::BM == 128 ? acc * BN : 0) + c * CW);
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + col;
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(taddr, r);
@@ -1386,8 +1409,8 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
 
 // ---------------------------------------------------------------- kernel
 
-template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF>
-__global__ void __launch_bounds__(Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF>::THREADS, 1)
+template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF, int WS>
+__global__ void __launch_bounds__(Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, WS>::THREADS, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC,
@@ -1395,7 +1418,7 @@ __global__ void __launch_bounds__(Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF>::THREA
                         const __grid_constant__ CUtensorMap tmSFA,
                         const __grid_constant__ CUtensorMap tmSFB, const __grid_constant__ KParams p)
 {
-    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF>;
+    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, WS>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     if (C::ALIGN_SLACK == 0 && (raw & 1023u) != 0u) {
@@ -1471,11 +1494,11 @@ __global__ void __launch_bounds__(Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF>::THREA
     const uint32_t stage_base = base;
     if (warp == 0) {
         if (lane == 0)
-            role_producer<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF>(p, &tmA, &tmB, &tmSFA, &tmSFB, stage_base, bar_full,
+            role_producer<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, WS>(p, &tmA, &tmB, &tmSFA, &tmSFB, stage_base, bar_full,
                                                               bar_empty, rank, w);
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {
-            role_mma<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF>(p, stage_base, bar_full, bar_empty,
+            role_mma<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, WS>(p, stage_base, bar_full, bar_empty,
                                                   bar_acc_full, bar_acc_empty, bar_inject, bar_sf,
                                                   tmem_base, w);
             // every MMA issued by this thread has completed before TMEM is freed
@@ -1485,15 +1508,15 @@ __global__ void __launch_bounds__(Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF>::THREA
     } else if (warp >= kSfCopyWarp) {
         // the even CTA copies the scales of both CTAs of a pair (cta_group::2)
         if (lane == 0 && rank == 0)
-            role_sf_copy<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF>(p, stage_base, bar_full, bar_sf, tmem_base, w,
+            role_sf_copy<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, WS>(p, stage_base, bar_full, bar_sf, tmem_base, w,
                                                                     warp - kSfCopyWarp);
     } else {
         if (p.out_type == 0)
-            role_epilogue<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, 32>(p, &tmC, &tmD, base + C::EPI_OFF,
+            role_epilogue<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, WS, 32>(p, &tmC, &tmD, base + C::EPI_OFF,
                                                            bar_acc_full, bar_acc_empty, bar_epi,
                                                            tmem_base, rank, warp, lane, w);
         else
-            role_epilogue<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, 64>(p, &tmC, &tmD, base + C::EPI_OFF,
+            role_epilogue<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, WS, 64>(p, &tmC, &tmD, base + C::EPI_OFF,
                                                            bar_acc_full, bar_acc_empty, bar_epi,
                                                            tmem_base, rank, warp, lane, w);
         if (lane == 0)

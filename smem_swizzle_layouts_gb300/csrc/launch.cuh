@@ -41,15 +41,15 @@ cudaError_t ensure_smem_attribute(Kern kern, int bytes, std::atomic<uint64_t> (&
 }
 
 // One record per kernel variant.
-template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF>
+template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF, int WS>
 std::atomic<uint64_t> smem_attribute_set[2] = {{0}, {0}};
 
-template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF>
+template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF, int WS>
 cudaError_t launch_gemm(const LaunchArgs &a)
 {
-    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF>;
-    auto kern = gemm_tcgen05_kernel<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF>;
-    cudaError_t e = ensure_smem_attribute(kern, C::SMEM_BYTES, smem_attribute_set<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF>);
+    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, WS>;
+    auto kern = gemm_tcgen05_kernel<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, WS>;
+    cudaError_t e = ensure_smem_attribute(kern, C::SMEM_BYTES, smem_attribute_set<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, WS>);
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};
@@ -70,12 +70,12 @@ cudaError_t launch_gemm(const LaunchArgs &a)
 }
 
 // Largest number of CTAs of this variant that can be resident at once.
-template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF>
+template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF, int WS>
 cudaError_t resident_ctas(int *ctas)
 {
-    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF>;
-    auto kern = gemm_tcgen05_kernel<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF>;
-    cudaError_t e = ensure_smem_attribute(kern, C::SMEM_BYTES, smem_attribute_set<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF>);
+    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, WS>;
+    auto kern = gemm_tcgen05_kernel<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, WS>;
+    cudaError_t e = ensure_smem_attribute(kern, C::SMEM_BYTES, smem_attribute_set<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, WS>);
     if (e != cudaSuccess)
         return e;
     if (CG == 1) {
@@ -107,6 +107,6 @@ cudaError_t resident_ctas(int *ctas)
 
 }  // namespace g300
 
-#define G300_INSTANTIATE(CG, BN, BK, ST, GR, ES, BM, SF)                                             \
-    template cudaError_t g300::launch_gemm<CG, BN, BK, ST, GR, ES, BM, SF>(const g300::LaunchArgs &); \
-    template cudaError_t g300::resident_ctas<CG, BN, BK, ST, GR, ES, BM, SF>(int *);
+#define G300_INSTANTIATE(CG, BN, BK, ST, GR, ES, BM, SF, WS)                                             \
+    template cudaError_t g300::launch_gemm<CG, BN, BK, ST, GR, ES, BM, SF, WS>(const g300::LaunchArgs &); \
+    template cudaError_t g300::resident_ctas<CG, BN, BK, ST, GR, ES, BM, SF, WS>(int *);

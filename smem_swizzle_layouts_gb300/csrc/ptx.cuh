@@ -276,6 +276,21 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_
                      : "memory");
 }
 
+// Weight-stationary form, kind::f16, cta_group::1 only ("06 Blackwell Tensor
+// Core - tcgen05 MMA", "How cta_group Sets the Operation Scope": .ws is one of
+// the choices that fix the accumulator layout). M is 32, 64 or 128 and N 64,
+// 128 or 256; for M = 32 and 64 the accumulator is spread over the four TMEM
+// lane quarters by column blocks (the layout the epilogue reads back).
+__device__ __forceinline__ void mma_ws_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.ws.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
 // D[tmem] (+)= A * B, kind::f8f6f4 with 8-bit A/B (E4M3 or E5M2), fp32 accumulate.
 template <int CG>
 __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,

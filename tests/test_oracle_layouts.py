@@ -451,3 +451,41 @@ def test_atom32_is_not_offered_for_k_major_operands():
     d = L.SmemDesc(start=P_BASE, lbo=16, sbo=1024, base_offset=0, swz=1)
     with pytest.raises(ValueError):
         L.desc_element_addr(d, "K", 2, 0, 0)
+
+
+# ---------------------------------------------------------------------------
+# Weight-stationary (.ws) accumulator maps ("06 Blackwell Tensor Core -
+# tcgen05 MMA", "How cta_group Sets the Operation Scope": .ws is one of the
+# four choices that fix the layout; the map itself is a reading).
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("M,N", [(32, 64), (32, 128), (32, 256), (64, 64), (64, 128), (64, 256), (128, 128)])
+def test_ws_map_is_a_bijection_onto_all_lanes(M, N):
+    cells = {L.tmem_ws(m, n, M, N) for m in range(M) for n in range(N)}
+    parts = 4 // (M // 32) if M < 128 else 1
+    assert len(cells) == M * N
+    assert {c[1] for c in cells} == set(range(128))               # every lane is used
+    assert {c[2] for c in cells} == set(range(N // parts))        # N / parts columns
+    assert all(c[0] == 0 for c in cells)                          # cta_group::1: this CTA's TMEM
+
+
+@pytest.mark.parametrize("M,N", [(32, 256), (64, 128), (64, 256)])
+def test_ws_lane_quarters_hold_whole_32_row_blocks_of_one_column_part(M, N):
+    # what an epilogue warp reading its lane quarter (32q .. 32q+31) gets
+    for q in range(4):
+        lanes = L.tmem_warp_lanes(4 + q)
+        held = [(m, n) for m in range(M) for n in range(N) if L.tmem_ws(m, n, M, N)[1] in lanes]
+        rows = sorted({m for m, _ in held})
+        cols = sorted({n for _, n in held})
+        assert len(rows) == 32 and rows == list(range(rows[0], rows[0] + 32))
+        assert cols == list(range(cols[0], cols[0] + len(cols))) and len(held) == 32 * len(cols)
+        for m, n in held:   # lane = 32 q + row within the block, column = offset in the part
+            assert L.tmem_ws(m, n, M, N)[1:] == (32 * q + m - rows[0], n - cols[0])
+
+
+def test_ws_m128_is_the_ordinary_m128_map_and_m64_differs_from_layout_f():
+    assert all(L.tmem_ws(m, n, 128, 128) == L.tmem_cta1_m128(m, n) for m in range(128) for n in range(128))
+    # Layout F leaves half of each lane quarter empty; the .ws map uses every lane
+    f_lanes = {L.tmem_layout_f(m, n)[1] for m in range(64) for n in range(128)}
+    assert len(f_lanes) == 64
+    assert any(L.tmem_ws(m, n, 64, 128) != L.tmem_layout_f(m, n) for m in range(64) for n in range(128))

@@ -77,9 +77,9 @@ def test_mn_major_swizzle_fits_the_tile_extent(g):
 def test_block_scaled_formats_have_fixed_tiles(g):
     # large MXFP8: 256 x 256 pair tiles; smaller problems and fp4: single CTAs of 128 x 128
     assert plan(g, 8192, 8192, 8192, MXFP8) == dict(cta_group=2, tile_n=256, block_k=256, tile_m=128, swizzle_a=3,
-                                                    swizzle_b=3, epilogue_swizzle=1, group_m=8)
+                                                    swizzle_b=3, epilogue_swizzle=1, group_m=8, mma_ws=0)
     assert plan(g, 1024, 8192, 8192, MXFP8) == dict(cta_group=1, tile_n=128, block_k=256, tile_m=128, swizzle_a=3,
-                                                    swizzle_b=3, epilogue_swizzle=1, group_m=8)
+                                                    swizzle_b=3, epilogue_swizzle=1, group_m=8, mma_ws=0)
     assert plan(g, 8192, 8192, 8192, MXFP8, cta_group=2)["tile_n"] == 128
     assert plan(g, 8192, 8192, 8192, MXFP8, cta_group=2, tile_n=256)["tile_n"] == 256
     # a stage depth only single CTAs are built for keeps large problems on single CTAs
@@ -104,7 +104,8 @@ def test_block_scaled_formats_have_fixed_tiles(g):
 def test_invalid_options_are_rejected(g):
     for opts, status in [(dict(flags=32), g.ERR_INVALID_ARG), (dict(stream_k=4), g.ERR_INVALID_ARG),
                          (dict(swizzle_a=6), g.ERR_INVALID_ARG), (dict(tile_m=96), g.ERR_INVALID_ARG),
-                         (dict(workspace=0x1010), g.ERR_ALIGNMENT), (dict(tile_n=96), g.ERR_UNSUPPORTED)]:
+                         (dict(workspace=0x1010), g.ERR_ALIGNMENT), (dict(tile_n=96), g.ERR_UNSUPPORTED),
+                         (dict(mma_ws=2), g.ERR_INVALID_ARG), (dict(tile_m=16), g.ERR_INVALID_ARG)]:
         with pytest.raises(g.GemmError) as ei:
             plan(g, 1024, 1024, 1024, **opts)
         assert ei.value.status == status, opts
@@ -119,3 +120,32 @@ def test_32_byte_atom_swizzle_is_refused_for_gemm_operands(g):
             with pytest.raises(g.GemmError) as ei:
                 plan(g, 1024, 1024, 1024, kind, a=a, b=b, **opts)
             assert ei.value.status == g.ERR_UNSUPPORTED, (kind, opts)
+
+
+def test_weight_stationary_tiles(g):
+    # tile_m 32 exists only as tcgen05.mma.ws (256 wide, 64 K per stage); mma_ws 1 picks
+    # .ws for 64-row tiles too; both are single-CTA, 16-bit, single-problem tiles
+    p = plan(g, 20, 4096, 4096, tile_m=32)
+    assert (p["tile_m"], p["mma_ws"], p["tile_n"], p["block_k"], p["cta_group"]) == (32, 1, 256, 64, 1)
+    p = plan(g, 20, 4096, 4096, mma_ws=1)
+    assert (p["tile_m"], p["mma_ws"], p["tile_n"]) == (64, 1, 128)
+    p = plan(g, 64, 16384, 4096, mma_ws=1)
+    assert (p["tile_m"], p["mma_ws"], p["tile_n"], p["block_k"]) == (64, 1, 128, 128)
+    p = plan(g, 64, 16384, 4096, tile_m=64, tile_n=256, mma_ws=1)
+    assert (p["tile_m"], p["mma_ws"], p["tile_n"], p["block_k"]) == (64, 1, 256, 64)
+    # M <= 64 defaults to .ws 64 x 128 tiles; an explicit tile_m 64 (or mma_ws -1) keeps Layout F
+    assert (plan(g, 64, 16384, 4096)["mma_ws"], plan(g, 20, 16384, 4096)["tile_m"]) == (1, 64)
+    assert plan(g, 64, 16384, 4096, tile_m=64)["mma_ws"] == 0
+    assert plan(g, 64, 16384, 4096, mma_ws=-1)["mma_ws"] == 0
+    assert plan(g, 64, 65536, 4096)["mma_ws"] == 0        # 256-wide 64-row tiles stay in Layout F
+    # M-major A of 32 rows: a 64-byte swizzle row (32 elements) fits the tile
+    assert plan(g, 32, 4096, 4096, a=MN_MAJOR, tile_m=32)["swizzle_a"] == 2
+    for kind, opts in [(BF16, dict(tile_m=32, cta_group=2)), (BF16, dict(tile_m=32, mma_ws=-1)),
+                       (BF16, dict(tile_m=128, mma_ws=1)), (FP8, dict(tile_m=32)), (MXFP8, dict(mma_ws=1)),
+                       (BF16, dict(tile_m=32, tile_n=128))]:
+        with pytest.raises(g.GemmError) as ei:
+            plan(g, 32, 4096, 4096, kind, **opts)
+        assert ei.value.status == g.ERR_UNSUPPORTED, (kind, opts)
+    with pytest.raises(g.GemmError) as ei:
+        g.gemm_debug_plan(32, 4096, 4096, BF16, K_MAJOR, K_MAJOR, grouped=True, options=dict(mma_ws=1), sms=SMS)
+    assert ei.value.status == g.ERR_UNSUPPORTED
