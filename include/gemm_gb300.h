@@ -481,6 +481,11 @@ int gemm_debug_streamk_units(int mode, int64_t tiles, int clusters, int kb_per_t
  * then gives up and the kernel exits with GEMM_ERR_TIMEOUT recorded. */
 void gemm_debug_inject_timeout(int timeout_ms);
 
+/* The same for a chosen role: 1 the TMA producer (in both CTAs of a pair,
+ * before it issues any load), 2 the MMA issuer. Other roles are ignored. The
+ * status word then names that role with wait code 6 (injected). */
+void gemm_debug_inject_timeout_at(int timeout_ms, int role);
+
 #ifdef __cplusplus
 }
 #endif

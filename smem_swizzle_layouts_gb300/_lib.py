@@ -82,6 +82,8 @@ _lib.gemm_debug_streamk_units.argtypes = [_int, _i64, _int, _int, _int, ctypes.P
 _lib.gemm_debug_streamk_units.restype = _int
 _lib.gemm_debug_inject_timeout.argtypes = [_int]
 _lib.gemm_debug_inject_timeout.restype = None
+_lib.gemm_debug_inject_timeout_at.argtypes = [_int, _int]
+_lib.gemm_debug_inject_timeout_at.restype = None
 for _name in ("gemm_bf16", "gemm_f16", "gemm_ex", "gemm_fp8", "gemm_fp8_ex", "gemm_mxfp8", "gemm_fp4", "gemm_bf16_grouped",
               "gemm_f16_grouped",
               "gemm_bf16_grouped_noalloc",
@@ -95,7 +97,7 @@ EXPORTED = ("gemm_bf16", "gemm_f16", "gemm_ex", "gemm_fp8", "gemm_fp8_ex", "gemm
             "gemm_bf16_grouped", "gemm_grouped_ex",
             "gemm_f16_grouped", "gemm_bf16_grouped_noalloc", "gemm_last_device_status", "gemm_status_string", "gemm_launch_count",
             "gemm_debug_descriptors", "gemm_debug_stage_image", "gemm_debug_plan", "gemm_debug_streamk_units",
-            "gemm_debug_inject_timeout")
+            "gemm_debug_inject_timeout", "gemm_debug_inject_timeout_at")
 
 
 class GemmError(RuntimeError):
@@ -329,5 +331,6 @@ def gemm_debug_stage_image(src, major, swizzle, rows_total, k_total, ld, rows, b
                                        _addr(out), _stream(stream)), "gemm_debug_stage_image")
 
 
-def gemm_debug_inject_timeout(timeout_ms: int) -> None:
-    _lib.gemm_debug_inject_timeout(timeout_ms)
+def gemm_debug_inject_timeout(timeout_ms: int, role: int = 2) -> None:
+    """Make the next launch's MMA issuer (role 2) or producer (role 1) wait until `timeout_ms` runs out."""
+    _lib.gemm_debug_inject_timeout_at(timeout_ms, role)

@@ -27,6 +27,7 @@ __device__ unsigned int g_status_word;
 
 std::atomic<uint64_t> g_launches{0};
 std::atomic<int> g_inject_timeout_ms{0};
+std::atomic<int> g_inject_role{kRoleMma};
 // Tag of the latest stream-K launch; a split tile's head accepts a partial
 // sum only when the contributor's flag carries its own launch's tag.
 std::atomic<uint32_t> g_sk_epoch{0};
@@ -484,7 +485,7 @@ void fill_common(KParams &p, const Plan &pl, const InFmt &f, int a_mn, int b_mn,
     p.stats = pl.stats;
     p.status = status;
     const int inj = g_inject_timeout_ms.exchange(0);
-    p.inject_timeout = inj > 0;
+    p.inject_timeout = inj > 0 ? g_inject_role.load() : 0;
     if (inj > 0)
         p.timeout_ns = static_cast<unsigned long long>(inj) * 1000000ull;
 }
@@ -1211,6 +1212,14 @@ int gemm_debug_streamk_units(int mode, int64_t tiles, int clusters, int kb_per_t
     return n;
 }
 
-void gemm_debug_inject_timeout(int timeout_ms) { g_inject_timeout_ms.store(timeout_ms > 0 ? timeout_ms : 0); }
+void gemm_debug_inject_timeout(int timeout_ms) { gemm_debug_inject_timeout_at(timeout_ms, kRoleMma); }
+
+void gemm_debug_inject_timeout_at(int timeout_ms, int role)
+{
+    if (role != kRoleProducer && role != kRoleMma)
+        return;
+    g_inject_role.store(role);
+    g_inject_timeout_ms.store(timeout_ms > 0 ? timeout_ms : 0);
+}
 
 }  // extern "C"

@@ -94,7 +94,7 @@ struct KParams {
     int epi_swizzle;       // 1: staging chunks in SW128 layout; 0: plain rows
     int group_m;           // raster group height (tiles)
     unsigned long long timeout_ns;
-    int inject_timeout;
+    int inject_timeout;    // test hook: role (kRoleProducer or kRoleMma) that waits on a barrier nothing arrives at
     unsigned int *status;
     const GroupedProblemDev *problems;  // grouped launches only
     const CUtensorMap *maps;            // [num_problems][4]: A, B, C, D
@@ -204,8 +204,8 @@ struct Cfg {
     static constexpr int EPI_BUFS = SF ? 1 : 2;
     static constexpr int EPI_BYTES = kEpiWarps * EPI_BUFS * kEpiBufBytes;
     static constexpr int BAR_OFF = EPI_OFF + EPI_BYTES;
-    // full[S], empty[S], acc_full[2], acc_empty[2], epi[4][2], drain, inject, sf_ready[S]
-    static constexpr int NUM_BARS = 3 * STAGES + 2 + 2 + 2 * kEpiWarps + 2;
+    // full[S], empty[S], acc_full[2], acc_empty[2], epi[4][2], drain, inject, sf_ready[S], copier drain
+    static constexpr int NUM_BARS = 3 * STAGES + 2 + 2 + 2 * kEpiWarps + 3;
     // threads per CTA: the scale copier warp exists only for block-scaled kinds
     // scale copier warps: NVFP4 stages carry three times the atoms of the others
     static constexpr int SF_COPIERS = SF == kScaleNv4 ? 2 : SF ? 1 : 0;
@@ -539,13 +539,26 @@ __device__ __forceinline__ int ceil_div_i(int a, int b) { return (a + b - 1) / b
 
 // ---------------------------------------------------------------- roles
 
+// The producer's loads that may still be in flight when it stops: the last
+// `inflight` stages it filled, the newest being the one before (stage, phase).
+struct ProducerTail {
+    int inflight;
+    int stage;
+    uint32_t phase;
+};
+
 template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF, int WS>
-__device__ void role_producer(const KParams &p, const CUtensorMap *tmA, const CUtensorMap *tmB,
-                              const CUtensorMap *tmSFA, const CUtensorMap *tmSFB,
-                              uint32_t smem, uint32_t bar_full, uint32_t bar_empty,
-                              uint32_t rank, const Waiter &w)
+__device__ ProducerTail role_producer(const KParams &p, const CUtensorMap *tmA, const CUtensorMap *tmB,
+                                      const CUtensorMap *tmSFA, const CUtensorMap *tmSFB,
+                                      uint32_t smem, uint32_t bar_full, uint32_t bar_empty, uint32_t bar_inject,
+                                      uint32_t rank, const Waiter &w)
 {
     using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, WS>;
+    if (p.inject_timeout == kRoleProducer) {
+        // Test hook: wait on a barrier nothing arrives at; the bound runs out.
+        w.wait(bar_inject, 0u, kRoleProducer | kWaitInjected);
+        return ProducerTail{0, 0, 0u};
+    }
     const Sched sched = make_sched(p);
     const int flags = p.flags;
     unsigned long long *const stats = p.stats;
@@ -662,17 +675,26 @@ __device__ void role_producer(const KParams &p, const CUtensorMap *tmA, const CU
         stats[blockIdx.x * kStatSlots + kStatProducerWaitCycles] = st_wait;
         stats[blockIdx.x * kStatSlots + kStatProducerBlocked] = st_blocked;
     }
-    if (!ok && CG == 1) {
-        // Let the loads still in flight land before the CTA can exit.
-        const int n = issued < STAGES ? issued : STAGES;
-        for (int i = 1; i <= n; ++i) {
-            int s = stage - i, ph = static_cast<int>(phase);
-            if (s < 0) {
-                s += STAGES;
-                ph ^= 1;
-            }
-            w.drain(bar_full + 8 * s, static_cast<uint32_t>(ph), 20000000ull);
+    return ProducerTail{issued < STAGES ? issued : STAGES, stage, phase};
+}
+
+// After an abort: wait (bounded) until the loads of the last stages the
+// producer filled have landed, so that no copy writes into shared memory of a
+// CTA that has exited. The full barrier of a stage completes once all its
+// bytes arrived (for a CTA pair, the even CTA's barrier counts the bytes of
+// both CTAs); a stage already consumed has completed its phase and returns at
+// once.
+template <int STAGES>
+__device__ void drain_producer_tail(const ProducerTail &t, uint32_t bar_full, const Waiter &w)
+{
+    for (int i = 1; i <= t.inflight; ++i) {
+        int s = t.stage - i;
+        uint32_t ph = t.phase;
+        if (s < 0) {
+            s += STAGES;
+            ph ^= 1u;
         }
+        w.drain(bar_full + 8 * s, ph, 2000000ull);
     }
 }
 
@@ -690,7 +712,7 @@ __device__ void role_sf_copy(const KParams &p, uint32_t smem, uint32_t bar_full,
 {
     using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, WS>;
     if constexpr (SF != 0) {
-        if (p.inject_timeout)
+        if (p.inject_timeout == kRoleMma)
             return;
         const Sched sched = make_sched(p);
         unsigned long long *const stats = p.stats;
@@ -753,7 +775,7 @@ __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uin
                          uint32_t tmem_base, const Waiter &w)
 {
     using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, WS>;
-    if (p.inject_timeout) {
+    if (p.inject_timeout == kRoleMma) {
         // Test hook: wait on a barrier nothing arrives at; the bound runs out.
         w.wait(bar_inject, 0u, kRoleMma | kWaitInjected);
         return;
@@ -1444,6 +1466,7 @@ __global__ void __launch_bounds__(Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, WS>::T
     const uint32_t bar_drain = bar_epi + 8 * 2 * kEpiWarps;
     const uint32_t bar_inject = bar_drain + 8;
     const uint32_t bar_sf = bar_inject + 8;  // sf_ready[STAGES]
+    const uint32_t bar_cp_drain = bar_sf + 8 * STAGES;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + C::MISC_OFF + 4);
 
@@ -1462,6 +1485,7 @@ __global__ void __launch_bounds__(Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, WS>::T
         mbar_init(bar_inject, 1);
         for (int s = 0; s < STAGES; ++s)
             mbar_init(bar_sf + 8 * s, C::SF_COPIERS > 0 ? C::SF_COPIERS : 1);
+        mbar_init(bar_cp_drain, C::SF_COPIERS > 0 ? C::SF_COPIERS : 1);
         *abort_flag = 0u;
         fence_mbar_init();
     }
@@ -1492,10 +1516,11 @@ __global__ void __launch_bounds__(Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, WS>::T
     w.all_cluster_scope = (CG == 2) && (p.flags & kFlagAllClusterWaits);
 
     const uint32_t stage_base = base;
+    ProducerTail tail{0, 0, 0u};
     if (warp == 0) {
         if (lane == 0)
-            role_producer<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, WS>(p, &tmA, &tmB, &tmSFA, &tmSFB, stage_base, bar_full,
-                                                              bar_empty, rank, w);
+            tail = role_producer<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, WS>(
+                p, &tmA, &tmB, &tmSFA, &tmSFB, stage_base, bar_full, bar_empty, bar_inject, rank, w);
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {
             role_mma<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, WS>(p, stage_base, bar_full, bar_empty,
@@ -1507,9 +1532,12 @@ __global__ void __launch_bounds__(Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, WS>::T
         }
     } else if (warp >= kSfCopyWarp) {
         // the even CTA copies the scales of both CTAs of a pair (cta_group::2)
-        if (lane == 0 && rank == 0)
+        if (lane == 0 && rank == 0) {
             role_sf_copy<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, WS>(p, stage_base, bar_full, bar_sf, tmem_base, w,
                                                                     warp - kSfCopyWarp);
+            // arrives once every tcgen05.cp this thread issued has completed
+            mma_commit<CG>(bar_cp_drain);
+        }
     } else {
         if (p.out_type == 0)
             role_epilogue<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, WS, 32>(p, &tmC, &tmD, base + C::EPI_OFF,
@@ -1523,9 +1551,20 @@ __global__ void __launch_bounds__(Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, WS>::T
             bulk_wait_group<0>();  // stores have finished reading shared memory
     }
     __syncwarp();
+    __syncthreads();  // every role has returned: the abort flag is final
 
     if (*abort_flag) {
-        // give copies and MMAs still in flight time to land before teardown
+        // The MMA thread has already waited for its MMAs (bar_drain). Wait for
+        // the producer's loads in flight (this CTA's full barriers; for a pair
+        // the even CTA's, which count both CTAs' bytes) and for the scale
+        // copiers' tcgen05.cp, each with a bound, before TMEM is freed.
+        if (warp == 0 && lane == 0 && (CG == 1 || rank == 0))
+            drain_producer_tail<STAGES>(tail, bar_full, w);
+        if constexpr (C::SF_COPIERS > 0)
+            if (warp == kSfCopyWarp && lane == 0 && rank == 0)
+                w.drain(bar_cp_drain, 0u, 100000000ull);
+        // loads an odd CTA issued for a stage its even CTA never armed land on
+        // no barrier this kernel can observe: a short pause covers them
         const uint64_t t0 = globaltimer_ns();
         while (globaltimer_ns() - t0 < 20000ull)
             __nanosleep(1000);

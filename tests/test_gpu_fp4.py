@@ -220,3 +220,9 @@ def test_fp4_injected_wait_times_out_and_the_context_survives(g, kind, options):
     st, word = g.gemm_last_device_status()
     assert st == g.ERR_TIMEOUT and word != 0
     run_fp4(g, 256, 264, 512, kind, out="bf16", seed=71, options=options)
+    # the producer stuck instead (the copier warps then end on the abort flag)
+    g.gemm_debug_inject_timeout(20, role=1)
+    g.gemm_fp4(M, N, K, A, K, SA, B, K, SB, code, None, 0, D, N, OUT["bf16"], 1.0, 0.0, options=options)
+    st, word = g.gemm_last_device_status()
+    assert st == g.ERR_TIMEOUT and (word & 0xFF, (word >> 8) & 0xFF) == (1, 6), hex(word)
+    run_fp4(g, 256, 264, 512, kind, out="bf16", seed=72, options=options)

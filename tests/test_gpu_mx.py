@@ -217,6 +217,14 @@ def test_mx_injected_wait_times_out_and_the_context_survives(g):
     st, word = g.gemm_last_device_status()
     assert st == g.ERR_TIMEOUT and word != 0
     run_mx(g, 512, 264, 512, exact=True, seed=73, options=dict(cta_group=2, tile_n=256))
+    # the producer stuck instead: the copier warp ends on the abort flag and its
+    # tcgen05.cp drain barrier is awaited before TMEM is freed
+    g.gemm_debug_inject_timeout(20, role=1)
+    g.gemm_mxfp8(M, N, K, A, 0, 0, K, SA, B, 0, 0, K, SB, None, 0, D, N, 1, 1.0, 0.0,
+                 options=dict(cta_group=2, tile_n=256))
+    st, word = g.gemm_last_device_status()
+    assert st == g.ERR_TIMEOUT and (word & 0xFF, (word >> 8) & 0xFF) == (1, 6), hex(word)
+    run_mx(g, 512, 264, 512, exact=True, seed=74, options=dict(cta_group=2, tile_n=256))
 
 
 def test_mx_argument_errors(g):

@@ -501,3 +501,20 @@ def test_injected_wait_times_out_and_the_context_survives(g):
     assert st == g.ERR_TIMEOUT and word != 0
     # the library and the context still work afterwards
     run_case(g, 256, 128, 64, dist="int4", exact=True)
+
+
+@pytest.mark.parametrize("cta_group", [1, 2])
+def test_injected_producer_wait_times_out_and_the_context_survives(g, cta_group):
+    # the producer (of both CTAs of a pair) waits on a barrier nothing arrives at before
+    # its first load: every other role gives up on the abort flag, the status names the
+    # producer and the injected wait, and the next calls compute correctly
+    g.gemm_debug_inject_timeout(20, role=1)
+    M = N = K = 512
+    A = torch.zeros(M, K, dtype=torch.bfloat16, device=DEV)
+    B = torch.zeros(N, K, dtype=torch.bfloat16, device=DEV)
+    D = torch.zeros(M, N, dtype=torch.float32, device=DEV)
+    g.gemm_ex(1, M, N, K, A, 0, K, B, 0, K, None, 0, D, N, 0, 1.0, 0.0, options=dict(cta_group=cta_group))
+    st, word = g.gemm_last_device_status()
+    assert st == g.ERR_TIMEOUT and (word & 0xFF, (word >> 8) & 0xFF) == (1, 6), hex(word)
+    run_case(g, 512, 384, 256, dist="int4", exact=True, options=dict(cta_group=cta_group))
+    run_case(g, 300, 200, 192, dist="int4", exact=True, options=dict(cta_group=cta_group))
