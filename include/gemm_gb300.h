@@ -160,6 +160,15 @@ typedef enum {
  *                 the four TMEM lane quarters by column parts, so all four
  *                 epilogue warps store full 32-row chunks. Other tiles with
  *                 mma_ws 1 return GEMM_ERR_UNSUPPORTED.
+ *   multicast_b   single-CTA (cta_group::1) 128 x 256 tiles run in clusters
+ *                 of two CTAs on vertically adjacent tiles that share their
+ *                 B panel: each CTA loads half of every B stage and TMA
+ *                 multicasts it into both CTAs' shared memory, so each CTA
+ *                 reads half as many B bytes from L2; each CTA's MMA
+ *                 completion releases the stage in both. 0 the library
+ *                 chooses, 1 use it, -1 do not; other tiles with 1 return
+ *                 GEMM_ERR_UNSUPPORTED. Multicast stays within this GPU's
+ *                 memory (the operands of one call).
  */
 typedef struct {
     int cta_group;
@@ -178,6 +187,7 @@ typedef struct {
     void *workspace;
     size_t workspace_bytes;
     int mma_ws;
+    int multicast_b;
 } gemm_options_t;
 
 /* Bytes of stream-K workspace for any single GEMM on the current device:
@@ -454,10 +464,11 @@ gemm_status_t gemm_debug_stage_image(const void *src, int major, int swizzle,
  * Host-side tile plan (no GPU needed): the configuration a call would launch
  * on a device with `sms` SMs. kind: 0 fp16/bf16, 1 fp8, 2 MXFP8, 3 NVFP4,
  * 4 MXFP4 (K in elements); grouped: nonzero for the grouped entry points.
- * Writes 9 int32: cta_group, tile N, K per stage (bytes for fp4), rows per
+ * Writes 10 int32: cta_group, tile N, K per stage (bytes for fp4), rows per
  * CTA, swizzle bits of A and B (0 none, 1 32B, 2 64B, 3 128B, 4 128B with
- * 32-byte atoms), epilogue swizzle, group height, and 1 when the tiles use
- * tcgen05.mma.ws. Returns the status the call's planning would.
+ * 32-byte atoms), epilogue swizzle, group height, 1 when the tiles use
+ * tcgen05.mma.ws, and 1 when two CTAs share B by multicast. Returns the
+ * status the call's planning would.
  */
 gemm_status_t gemm_debug_plan(int64_t M, int64_t N, int64_t K, int kind, int a_major, int b_major, int grouped,
                               const gemm_options_t *opts, int sms, int32_t *out);

@@ -36,7 +36,8 @@ class GemmOptions(ctypes.Structure):
     _fields_ = [("cta_group", _int), ("tile_m", _int), ("tile_n", _int), ("block_k", _int), ("swizzle_a", _int), ("swizzle_b", _int),
                 ("epilogue_swizzle", _int), ("max_ctas", _int), ("group_m", _int),
                 ("timeout_ms", _int), ("flags", _int), ("stats", _vp),
-                ("stream_k", _int), ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t), ("mma_ws", _int)]
+                ("stream_k", _int), ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t), ("mma_ws", _int),
+                ("multicast_b", _int)]
 
 
 class GemmProblem(ctypes.Structure):
@@ -241,12 +242,12 @@ def gemm_mx_scale_bytes(rows: int, K: int) -> int:
 
 
 PLAN_FIELDS = ("cta_group", "tile_n", "block_k", "tile_m", "swizzle_a", "swizzle_b", "epilogue_swizzle", "group_m",
-               "mma_ws")
+               "mma_ws", "multicast_b")
 
 
 def gemm_debug_plan(M, N, K, kind=0, a_major=0, b_major=0, grouped=False, options=None, sms=148):
     """The tile plan a call would launch (host only), as a dict; raises GemmError for rejected options."""
-    out = (ctypes.c_int32 * 9)()
+    out = (ctypes.c_int32 * 10)()
     _check(_lib.gemm_debug_plan(M, N, K, kind, a_major, b_major, int(grouped), _opts(options), sms, out),
            "gemm_debug_plan")
     return dict(zip(PLAN_FIELDS, list(out)))

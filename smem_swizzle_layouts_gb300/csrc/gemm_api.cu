@@ -43,14 +43,14 @@ struct Variant {
     int esize;
     int bm;
     int sf;  // scale kind (kScale*)
-    int ws;  // 1: tcgen05.mma.ws (weight-stationary accumulator layout)
+    int mode;  // kModeOrdinary, kModeWs (tcgen05.mma.ws) or kModeMcastB (B multicast in a 2-CTA cluster)
     cudaError_t (*launch)(const LaunchArgs &);
     cudaError_t (*resident)(int *);
     int resident_cache[kMaxDevices];
 };
 
-#define G300_VARIANT_ROW(CG, BN, BK, ST, GR, ES, BM, SF, WS) \
-    {CG, BN, BK, ST, GR, ES, BM, SF, WS, &launch_gemm<CG, BN, BK, ST, GR, ES, BM, SF, WS>, &resident_ctas<CG, BN, BK, ST, GR, ES, BM, SF, WS>, {0}},
+#define G300_VARIANT_ROW(CG, BN, BK, ST, GR, ES, BM, SF, MO) \
+    {CG, BN, BK, ST, GR, ES, BM, SF, MO, &launch_gemm<CG, BN, BK, ST, GR, ES, BM, SF, MO>, &resident_ctas<CG, BN, BK, ST, GR, ES, BM, SF, MO>, {0}},
 Variant g_variants[] = {G300_VARIANTS(G300_VARIANT_ROW)};
 #undef G300_VARIANT_ROW
 
@@ -106,11 +106,11 @@ int resident_for(Variant &v, int dev)
 }
 
 Variant *find_variant(int cg, int bn, int bk, bool grouped, int esize = 2, int bm = 128, int sf = kScaleNone,
-                      int ws = 0)
+                      int mode = kModeOrdinary)
 {
     for (auto &v : g_variants)
         if (v.cg == cg && v.bn == bn && v.bk == bk && v.grouped == grouped && v.esize == esize && v.bm == bm &&
-            v.sf == sf && v.ws == ws)
+            v.sf == sf && v.mode == mode)
             return &v;
     return nullptr;
 }
@@ -252,6 +252,7 @@ struct Plan {
     int cg, bn, bk;
     int bm;  // accumulator rows per CTA: 128, 64 (M = 64 MMAs) or 32 (.ws only)
     int ws;  // 1: tcgen05.mma.ws
+    int mcb;  // 1: clusters of two cta_group::1 CTAs sharing B by TMA multicast
     int a_swz, b_swz;
     int epi_swizzle;
     int max_ctas;
@@ -263,6 +264,9 @@ struct Plan {
     void *workspace;
     size_t workspace_bytes;
 };
+
+// CTAs per cluster of a plan: CTA pairs and B-multicast clusters have two.
+int cluster_ctas(const Plan &pl) { return (pl.cg == 2 || pl.mcb) ? 2 : 1; }
 
 // gemm_swizzle_t -> swizzle bits (B of Swizzle<B,4,3>): 32B 1, 64B 2, 128B 3, none 0;
 // 128B with 32-byte atoms kSwzAtom32.
@@ -283,7 +287,8 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
         opt.swizzle_a > 5 || opt.swizzle_b < 0 || opt.swizzle_b > 5 || opt.max_ctas < 0 ||
         opt.group_m < 0 || opt.timeout_ms < 0 || opt.epilogue_swizzle < -1 ||
         opt.epilogue_swizzle > 1 || opt.flags < 0 || opt.flags > 31 || opt.block_k < 0 ||
-        opt.stream_k < -1 || opt.stream_k > 3 || opt.mma_ws < -1 || opt.mma_ws > 1)
+        opt.stream_k < -1 || opt.stream_k > 3 || opt.mma_ws < -1 || opt.mma_ws > 1 || opt.multicast_b < -1 ||
+        opt.multicast_b > 1)
         return GEMM_ERR_INVALID_ARG;
     if (opt.workspace && (reinterpret_cast<uintptr_t>(opt.workspace) & 255u) != 0)
         return GEMM_ERR_ALIGNMENT;
@@ -373,7 +378,24 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
             bn = 128;
         }
     }
-    if (!find_variant(cg, bn, bk, grouped, esize, bm, sf, ws))
+    // B multicast between two single-CTA tiles of one cluster: when asked for,
+    // and by default for 128 x 256 single-CTA tiles whose B is MN-major or
+    // whose operands overflow L2 (measured, TFLOP/s without -> with: 8192^3
+    // K/MN fp32 out + C 914 -> 1452, 4096^3 K/MN 815 -> 1175, 8192^3 K/K
+    // 1599 -> 1665, 6144^3 K/K 1383 -> 1433; 4096^3 and 8192^2 x 2048 K/K,
+    // operands in L2: within 1 %)
+    int mcb = 0;
+    if (opt.multicast_b == 1) {
+        if (cg != 1 || bm != 128 || ws || sf != kScaleNone || grouped)
+            return GEMM_ERR_UNSUPPORTED;
+        mcb = 1;
+    } else if (opt.multicast_b == 0 && cg == 1 && bm == 128 && bn == 256 && !ws && sf == kScaleNone && !grouped &&
+               M > 128 && (b_mn || (M + N) * K * esize > (static_cast<int64_t>(128) << 20)) &&
+               find_variant(cg, bn, bk, grouped, esize, bm, sf, kModeMcastB)) {
+        mcb = 1;
+    }
+    const int mode = ws ? kModeWs : mcb ? kModeMcastB : kModeOrdinary;
+    if (!find_variant(cg, bn, bk, grouped, esize, bm, sf, mode))
         return GEMM_ERR_UNSUPPORTED;
 
     // the widest swizzle whose row fits the stage: along K for K-major
@@ -403,6 +425,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
         return GEMM_ERR_UNSUPPORTED;
     plan->bm = bm;
     plan->ws = ws;
+    plan->mcb = mcb;
     plan->epi_swizzle = opt.epilogue_swizzle == -1 ? 0 : 1;
     plan->max_ctas = opt.max_ctas;
     plan->group_m = opt.group_m ? opt.group_m : 8;
@@ -414,9 +437,10 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
     // columns of their row panels at the same moment (16384 x 128 x 8192:
     // 0.70 -> 0.75 of the measured HBM rate). Explicit flags are kept as given.
     if (opt.flags == 0 && !grouped) {
-        const int64_t tiles = ((M + bm * cg - 1) / (bm * cg)) * ((N + bn - 1) / bn);
+        const int64_t rows = static_cast<int64_t>(bm) * (mcb ? 2 : cg);
+        const int64_t tiles = ((M + rows - 1) / rows) * ((N + bn - 1) / bn);
         const int64_t kblocks = (K + bk - 1) / bk;
-        if (tiles <= sms / cg && kblocks >= 16)
+        if (tiles <= sms / (mcb ? 2 : cg) && kblocks >= 16)
             plan->flags |= kFlagRotateK;
     }
     plan->stats = opt.stats;
@@ -459,7 +483,7 @@ int grid_for(const Plan &pl, Variant &v, int dev, int sms, int64_t tiles)
         cap = sms;
     if (pl.max_ctas > 0)
         cap = std::min(cap, pl.max_ctas);
-    const int64_t per_cluster = pl.cg;
+    const int64_t per_cluster = cluster_ctas(pl);
     int64_t clusters = std::min<int64_t>(tiles, cap / per_cluster);
     if (clusters < 1)
         clusters = 1;
@@ -550,7 +574,9 @@ gemm_status_t run_single(const InFmt &f, int64_t M, int64_t N, int64_t K, const 
     Plan pl;
     if ((s = make_plan(M, N, K, a_mn, b_mn, sms, opts, false, &pl, f.esize, f.sf)) != GEMM_OK)
         return s;
-    Variant *v = find_variant(pl.cg, pl.bn, pl.bk, false, f.esize, pl.bm, f.sf, pl.ws);
+    Variant *v = find_variant(pl.cg, pl.bn, pl.bk, false, f.esize, pl.bm, f.sf,
+                              pl.ws ? kModeWs : pl.mcb ? kModeMcastB : kModeOrdinary);
+    const int ccta = cluster_ctas(pl);
     const int epi_rows = pl.ws ? 32 : pl.bm / 4;  // output rows one epilogue warp stores per chunk
 
     LaunchArgs la;
@@ -558,8 +584,8 @@ gemm_status_t run_single(const InFmt &f, int64_t M, int64_t N, int64_t K, const 
     if (K > 0) {
         if ((s = encode_operand(&la.a, f.dcode, A, a_mn, pl.a_swz, M, K, lda, pl.bm, pl.bk)) != GEMM_OK)
             return s;
-        if ((s = encode_operand(&la.b, f.dcode, B, b_mn, pl.b_swz, N, K, ldb, pl.bn / pl.cg, pl.bk)) !=
-            GEMM_OK)
+        // B rows (K-major boxes) one CTA loads: half the tile for pairs and for B multicast
+        if ((s = encode_operand(&la.b, f.dcode, B, b_mn, pl.b_swz, N, K, ldb, pl.bn / ccta, pl.bk)) != GEMM_OK)
             return s;
     }
     if ((s = encode_output(&la.d, d_type, D, M, N, ldd, pl.epi_swizzle, epi_rows)) != GEMM_OK)
@@ -575,7 +601,7 @@ gemm_status_t run_single(const InFmt &f, int64_t M, int64_t N, int64_t K, const 
     p.M = static_cast<int>(M);
     p.N = static_cast<int>(N);
     p.K = static_cast<int>(K);
-    p.tiles_m = static_cast<int>((M + pl.bm * pl.cg - 1) / (pl.bm * pl.cg));
+    p.tiles_m = static_cast<int>((M + pl.bm * ccta - 1) / (pl.bm * ccta));
     p.tiles_n = static_cast<int>((N + pl.bn - 1) / pl.bn);
     const int64_t tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
     if (tiles >= (static_cast<int64_t>(1) << 31))
@@ -597,7 +623,7 @@ gemm_status_t run_single(const InFmt &f, int64_t M, int64_t N, int64_t K, const 
         // stream-K runs on every resident cluster
         const int full = grid_for(pl, *v, dev, sms, static_cast<int64_t>(1) << 40);
         const int64_t kbt = (K + pl.bk - 1) / pl.bk;
-        const int64_t dp = sk_split(pl.stream_k, tiles, full / pl.cg, kbt);
+        const int64_t dp = sk_split(pl.stream_k, tiles, full / ccta, kbt);
         if (dp >= 0) {
             if (pl.workspace_bytes < sk_bytes(full, pl.bn))
                 return GEMM_ERR_INVALID_ARG;
@@ -1170,6 +1196,7 @@ gemm_status_t gemm_debug_plan(int64_t M, int64_t N, int64_t K, int kind, int a_m
     out[6] = pl.epi_swizzle;
     out[7] = pl.group_m;
     out[8] = pl.ws;
+    out[9] = pl.mcb;
     return GEMM_OK;
 }
 

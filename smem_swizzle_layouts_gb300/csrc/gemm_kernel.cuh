@@ -183,8 +183,16 @@ __host__ __device__ constexpr int sf_atom_kbytes(int sf)
 // rows per CTA, 128 (row m in TMEM lane m) or 64 (cta_group::1 only, Layout F:
 // rows 16g..16g+15 in lanes 32g+a..32g+a+15; the two accumulators of the
 // double buffer take lane alignments a = 0 and 16 and share their columns).
-template <int CG, int BN, int BK, int STAGES, int ESIZE = 2, int BMT = 128, int SF = 0, int WS = 0>
+// Tile modes (the MODE template argument): ordinary MMAs; the weight-stationary
+// tcgen05.mma.ws (32- and 64-row tiles); or a cluster of two cta_group::1 CTAs
+// on vertically adjacent tiles that each load half of the shared B panel and
+// TMA-multicast it to both (B bytes read from L2 per CTA halved).
+enum : int { kModeOrdinary = 0, kModeWs = 1, kModeMcastB = 2 };
+
+template <int CG, int BN, int BK, int STAGES, int ESIZE = 2, int BMT = 128, int SF = 0, int MODE = 0>
 struct Cfg {
+    static constexpr bool WS = MODE == kModeWs;
+    static constexpr bool MCB = MODE == kModeMcastB;
     static constexpr int BM = BMT;             // accumulator rows per CTA
     static constexpr int BN_LOCAL = BN / CG;   // B columns loaded by each CTA
     static constexpr int A_BYTES = BM * BK * ESIZE;
@@ -235,6 +243,13 @@ struct Cfg {
     static constexpr int ACC_COLS = BN / COL_PARTS;
     static constexpr int TMEM_COLS = WS ? (2 * ACC_COLS < 32 ? 32 : 2 * ACC_COLS) : BMT == 64 ? BN : SF ? 512 : 2 * BN;
     static constexpr int UMMA_M = BM * CG;
+    // CTAs per cluster (CTA pairs, or the two CTAs sharing B by multicast) and
+    // the output rows of one cluster tile; B rows/atoms one CTA's TMA loads
+    static constexpr int CLUSTER = (CG == 2 || MCB) ? 2 : 1;
+    static constexpr int TILE_M = BM * CLUSTER;
+    static constexpr int B_LOAD = MCB ? BN / 2 : BN_LOCAL;
+    static_assert(!MCB || (CG == 1 && BMT == 128 && SF == 0 && BN % 128 == 0),
+                  "B multicast: two single-CTA 128-row tiles sharing a B panel split in halves");
     static constexpr int EPI_ROWS = WS ? 32 : BM / 4;    // output rows per epilogue warp
     static_assert(BMT == 128 || (BMT == 64 && CG == 1) || (BMT == 32 && WS), "64-row tiles are single-CTA");
     static_assert(!WS || ((BMT == 32 || BMT == 64) && CG == 1 && ESIZE == 2 && SF == 0 && (BN / COL_PARTS) % 64 == 0),
@@ -547,13 +562,13 @@ struct ProducerTail {
     uint32_t phase;
 };
 
-template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF, int WS>
+template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF, int MODE>
 __device__ ProducerTail role_producer(const KParams &p, const CUtensorMap *tmA, const CUtensorMap *tmB,
                                       const CUtensorMap *tmSFA, const CUtensorMap *tmSFB,
                                       uint32_t smem, uint32_t bar_full, uint32_t bar_empty, uint32_t bar_inject,
                                       uint32_t rank, const Waiter &w)
 {
-    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, WS>;
+    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, MODE>;
     if (p.inject_timeout == kRoleProducer) {
         // Test hook: wait on a barrier nothing arrives at; the bound runs out.
         w.wait(bar_inject, 0u, kRoleProducer | kWaitInjected);
@@ -564,7 +579,19 @@ __device__ ProducerTail role_producer(const KParams &p, const CUtensorMap *tmA, 
     unsigned long long *const stats = p.stats;
     const CUtensorMap *const maps = p.maps;
     const OperandBoxes boxA = operand_boxes(p.a_mn, p.a_swz, C::BM, BK, ESIZE);
-    const OperandBoxes boxB = operand_boxes(p.b_mn, p.b_swz, C::BN_LOCAL, BK, ESIZE);
+    OperandBoxes boxB = operand_boxes(p.b_mn, p.b_swz, C::B_LOAD, BK, ESIZE);
+    // B multicast: this CTA loads half of the tile's B (rows of each K-major
+    // box, or MN atoms) into its place in the full B tile of both CTAs
+    uint32_t b_own = 0;
+    if constexpr (C::MCB) {
+        const uint32_t W = swizzle_row_bytes(p.b_swz);
+        if (!p.b_mn) {
+            boxB.smem_step = static_cast<uint32_t>(BN) * W;
+            b_own = rank * static_cast<uint32_t>(C::B_LOAD) * W;
+        } else {
+            b_own = rank * static_cast<uint32_t>(boxB.nbox) * boxB.smem_step;
+        }
+    }
     const int nbox = boxA.nbox > boxB.nbox ? boxA.nbox : boxB.nbox;
     const bool forward = CG == 2 && rank == 0 && (flags & kFlagPairForward);
     const int sf_groups = p.sf_groups;
@@ -574,7 +601,7 @@ __device__ ProducerTail role_producer(const KParams &p, const CUtensorMap *tmA, 
 
     const uint32_t full_target = (CG == 2) ? mapa_shared(bar_full, 0) : bar_full;
     const uint32_t peer_empty = (CG == 2 && rank == 0) ? mapa_shared(bar_empty, 1) : 0u;
-    const int cluster_id = blockIdx.x / CG, num_clusters = gridDim.x / CG;
+    const int cluster_id = blockIdx.x / C::CLUSTER, num_clusters = gridDim.x / C::CLUSTER;
     int stage = 0;
     uint32_t phase = 0;
     int issued = 0;
@@ -599,31 +626,44 @@ __device__ ProducerTail role_producer(const KParams &p, const CUtensorMap *tmA, 
         const int num_kb = ceil_div_i(ti.K, BK);
         const int kb_lo = u.kb0, kb_hi = u.kb1 < 0 ? num_kb : u.kb1;
         const bool whole = u.kb1 < 0;
-        const int m0 = ti.m_blk * C::UMMA_M + C::BM * static_cast<int>(rank);
-        const int n0 = ti.n_blk * BN + C::BN_LOCAL * static_cast<int>(rank);
+        const int m0 = ti.m_blk * C::TILE_M + C::BM * static_cast<int>(rank);
+        const int n0 = ti.n_blk * BN + C::B_LOAD * static_cast<int>(rank);
+        // a stage is released by arrivals from the other CTA of the cluster too
+        // (pairs: the odd CTA's; B multicast: both CTAs' MMA commits)
+        const bool remote_release = rank != 0 || C::MCB;
         for (int kb = kb_lo; kb < kb_hi; ++kb) {
             if (stats) {
                 const long long t0 = clock64();
                 const bool ready = mbar_try_wait(bar_empty + 8 * stage, phase ^ 1u);
-                ok = ready || w.wait(bar_empty + 8 * stage, phase ^ 1u, kRoleProducer | kWaitEmpty, rank != 0);
+                ok = ready || w.wait(bar_empty + 8 * stage, phase ^ 1u, kRoleProducer | kWaitEmpty, remote_release);
                 st_wait += static_cast<unsigned long long>(clock64() - t0);
                 st_blocked += ready ? 0 : 1;
             } else {
-                ok = w.wait(bar_empty + 8 * stage, phase ^ 1u, kRoleProducer | kWaitEmpty, rank != 0);
+                ok = w.wait(bar_empty + 8 * stage, phase ^ 1u, kRoleProducer | kWaitEmpty, remote_release);
             }
             if (!ok)
                 break;
             // pass a real release (not the first trip round the ring) on to the odd CTA
             if (forward && issued >= STAGES)
                 mbar_arrive_cluster(peer_empty + 8 * stage);
-            if (rank == 0)
+            if (rank == 0 || C::MCB)
                 mbar_arrive_expect_tx(bar_full + 8 * stage, C::TX_BYTES);
             const uint32_t sA = smem + stage * C::STAGE_BYTES;
             const uint32_t sB = sA + C::A_BYTES;
             const uint32_t fb = full_target + 8 * stage;
             const int k0 = (whole ? kblock_at(kb, num_kb, flags, cluster_id) : kb) * BK;
             // A and B boxes alternate, so both operands of the stage are in flight together
-            if (hints) {
+            if constexpr (C::MCB) {
+                for (int b = 0; b < nbox; ++b) {
+                    if (b < boxA.nbox)
+                        issue_box<1>(mA, sA, fb, boxA, b, m0, k0);
+                    if (b < boxB.nbox) {
+                        const int x = boxB.mn_major ? n0 + b * boxB.step : k0 + b * boxB.step;
+                        const int y = boxB.mn_major ? k0 : n0;
+                        tma_load_2d_mcast2(sB + b_own + static_cast<uint32_t>(b) * boxB.smem_step, mB, fb, x, y);
+                    }
+                }
+            } else if (hints) {
                 for (int b = 0; b < nbox; ++b) {
                     if (b < boxA.nbox)
                         issue_box_hint<CG>(mA, sA, fb, boxA, b, m0, k0, keep);
@@ -706,18 +746,18 @@ __device__ void drain_producer_tail(const ProducerTail &t, uint32_t bar_full, co
 // waits on sf_ready before the stage's MMAs and so issues only MMAs. A
 // stage's scale columns are rewritten only after the stage was refilled, that
 // is after the MMAs that read their previous contents completed.
-template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF, int WS>
+template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF, int MODE>
 __device__ void role_sf_copy(const KParams &p, uint32_t smem, uint32_t bar_full, uint32_t bar_sf,
                              uint32_t tmem_base, const Waiter &w, int copier)
 {
-    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, WS>;
+    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, MODE>;
     if constexpr (SF != 0) {
         if (p.inject_timeout == kRoleMma)
             return;
         const Sched sched = make_sched(p);
         unsigned long long *const stats = p.stats;
         unsigned long long st_wait = 0;
-        const int cluster_id = blockIdx.x / CG, num_clusters = gridDim.x / CG;
+        const int cluster_id = blockIdx.x / C::CLUSTER, num_clusters = gridDim.x / C::CLUSTER;
         int stage = 0;
         uint32_t phase = 0;
         UnitIter units(sched, cluster_id, num_clusters);
@@ -769,12 +809,12 @@ __device__ void role_sf_copy(const KParams &p, uint32_t smem, uint32_t bar_full,
     }
 }
 
-template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF, int WS>
+template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF, int MODE>
 __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uint32_t bar_empty,
                          uint32_t bar_acc_full, uint32_t bar_acc_empty, uint32_t bar_inject, uint32_t bar_sf,
                          uint32_t tmem_base, const Waiter &w)
 {
-    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, WS>;
+    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, MODE>;
     if (p.inject_timeout == kRoleMma) {
         // Test hook: wait on a barrier nothing arrives at; the bound runs out.
         w.wait(bar_inject, 0u, kRoleMma | kWaitInjected);
@@ -783,6 +823,8 @@ __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uin
     const Sched sched = make_sched(p);
     unsigned long long *const stats = p.stats;
     const bool multicast = CG == 2 && !(p.flags & kFlagPairForward);
+    // B multicast: a stage is refilled in both CTAs at once, so each CTA's MMA
+    // completion releases the stage in both
     const uint32_t idesc = SF ? make_idesc_mx(C::UMMA_M, BN, p.a_fmt, p.b_fmt, p.a_mn, p.b_mn, SF != kScaleNv4)
                               : make_idesc(C::UMMA_M, BN, p.a_fmt, p.b_fmt, p.a_mn, p.b_mn);
     const OperandPacking pa = operand_packing(p.a_mn, p.a_swz, C::BM, BK);
@@ -795,7 +837,7 @@ __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uin
         a_off[j] = slice_byte_offset(p.a_mn, p.a_swz, C::BM, j, ESIZE) >> 4;
         b_off[j] = slice_byte_offset(p.b_mn, p.b_swz, C::BN_LOCAL, j, ESIZE) >> 4;
     }
-    const int cluster_id = blockIdx.x / CG, num_clusters = gridDim.x / CG;
+    const int cluster_id = blockIdx.x / C::CLUSTER, num_clusters = gridDim.x / C::CLUSTER;
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
@@ -820,7 +862,7 @@ __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uin
             ++st_tiles;
         }
         tc_fence_after_sync();
-        const uint32_t d_tmem = WS           ? tmem_base + static_cast<uint32_t>(acc * C::ACC_COLS)
+        const uint32_t d_tmem = C::WS        ? tmem_base + static_cast<uint32_t>(acc * C::ACC_COLS)
                                 : C::BM == 64 ? tmem_base + (static_cast<uint32_t>(16 * acc) << 16)
                                               : tmem_base + static_cast<uint32_t>(acc * BN);
         for (int kb = kb_lo; kb < kb_hi; ++kb) {
@@ -862,7 +904,7 @@ __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uin
 #pragma unroll
                 for (int j = 0; j < C::KSLICES; ++j) {
                     // the first MMA of a unit overwrites the accumulator, the rest add
-                    if constexpr (WS)
+                    if constexpr (C::WS)
                         mma_ws_f16(d_tmem, a_desc0 + sdelta + a_off[j], b_desc0 + sdelta + b_off[j], idesc,
                                    ((kb - kb_lo) | j) != 0);
                     else if constexpr (ESIZE == 2)
@@ -873,7 +915,9 @@ __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uin
                                    ((kb - kb_lo) | j) != 0);
                 }
             }
-            if (multicast)
+            if constexpr (C::MCB)
+                mma_commit_cg1_multicast(bar_empty + 8 * stage);
+            else if (multicast)
                 mma_commit_pair_multicast(bar_empty + 8 * stage);
             else
                 mma_commit<CG>(bar_empty + 8 * stage);
@@ -1043,7 +1087,7 @@ __device__ __forceinline__ void epilogue_chunk_math(float (&acc)[CW], const EpiC
 // split tile `ua`, then writes the sum of their fp32 partial sums into TMEM
 // accumulator buffer `buf` (the first n32 32-column groups), the buffer the
 // head's own MMAs do not use. False if a flag did not come in time.
-template <int CG, int BN>
+template <int CL, int BN>
 __device__ bool sk_gather(const Sched &sched, const Unit &ua, int n32, int buf, uint32_t tmem_base, int q,
                           int prow, const float4 *partials, const uint32_t *sk_flags, uint32_t epoch, int rank,
                           int num_clusters, const Waiter &w, unsigned long long *st_wait)
@@ -1057,7 +1101,7 @@ __device__ bool sk_gather(const Sched &sched, const Unit &ua, int n32, int buf, 
     for (int cc = c_lo; cc <= c_hi && ok; ++cc) {
         if (S * cc / num_clusters == S * (cc + 1) / num_clusters)
             continue;  // empty share: nothing to wait for
-        ok = w.wait_flag(sk_flags + (cc * CG + rank) * 4 + q, epoch, kRoleEpilogue | kWaitPartial);
+        ok = w.wait_flag(sk_flags + (cc * CL + rank) * 4 + q, epoch, kRoleEpilogue | kWaitPartial);
     }
     if (!__all_sync(0xffffffffu, ok))
         return false;
@@ -1077,7 +1121,7 @@ __device__ bool sk_gather(const Sched &sched, const Unit &ua, int n32, int buf, 
         for (int cc = c_lo; cc <= c_hi; ++cc) {
             if (S * cc / num_clusters == S * (cc + 1) / num_clusters)
                 continue;
-            const float4 *slot = partials + static_cast<size_t>(cc * CG + rank) * kSlotVec + prow;
+            const float4 *slot = partials + static_cast<size_t>(cc * CL + rank) * kSlotVec + prow;
 #pragma unroll
             for (int b = 0; b < kGroups; ++b) {
                 // groups past n32 reload the last one (in the slot) and are not stored
@@ -1101,13 +1145,13 @@ __device__ bool sk_gather(const Sched &sched, const Unit &ua, int n32, int buf, 
     return true;
 }
 
-template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF, int WS, int CW>
+template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF, int MODE, int CW>
 __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CUtensorMap *tmD,
                               uint32_t epi_base, uint32_t bar_acc_full, uint32_t bar_acc_empty,
                               uint32_t bar_epi, uint32_t tmem_base, uint32_t rank, int warp,
                               int lane, const Waiter &w)
 {
-    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, WS>;
+    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, MODE>;
     const Sched sched = make_sched(p);
     unsigned long long *const stats = p.stats;
     const CUtensorMap *const maps = p.maps;
@@ -1124,8 +1168,8 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
     // tiles give it 32 rows of one column part (rows 32 (q % RB) .., chunks
     // [part * NCH / COL_PARTS, (part + 1) * NCH / COL_PARTS))
     constexpr int NCH = BN / CW;
-    const int wrow = WS ? 32 * (q % C::WS_ROW_BLOCKS) : R * q;
-    const int c_lo = WS ? (q / C::WS_ROW_BLOCKS) * (NCH / C::COL_PARTS) : 0;
+    const int wrow = C::WS ? 32 * (q % C::WS_ROW_BLOCKS) : R * q;
+    const int c_lo = C::WS ? (q / C::WS_ROW_BLOCKS) * (NCH / C::COL_PARTS) : 0;
     const int c_hi = c_lo + NCH / C::COL_PARTS;
     const int ew = warp - 2;  // staging slot
     const uint32_t buf0 = epi_base + static_cast<uint32_t>(ew * C::EPI_BUFS * kEpiBufBytes);
@@ -1141,7 +1185,7 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
     const uint64_t stream_once = hints ? l2_policy_evict_first() : 0;
     const uint32_t acc_empty_target = (CG == 2) ? mapa_shared(bar_acc_empty, 0) : bar_acc_empty;
     const uint32_t peer_acc_full = (CG == 2 && rank == 0) ? mapa_shared(bar_acc_full, 1) : 0u;
-    const int cluster_id = blockIdx.x / CG, num_clusters = gridDim.x / CG;
+    const int cluster_id = blockIdx.x / C::CLUSTER, num_clusters = gridDim.x / C::CLUSTER;
     uint32_t epi_phase[2] = {0u, 0u};
     int sel = 0;
     int acc = 0;
@@ -1170,7 +1214,7 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
         if (head) {
             const int n_cols = min(BN, ti.N - ti.n_blk * BN);
             const long long t0 = stats ? clock64() : 0;
-            const bool ok = sk_gather<CG, BN>(sched, u, (n_cols + 31) / 32, acc ^ 1, tmem_base, q, prow, partials,
+            const bool ok = sk_gather<C::CLUSTER, BN>(sched, u, (n_cols + 31) / 32, acc ^ 1, tmem_base, q, prow, partials,
                                               sk_flags, epoch, static_cast<int>(rank), num_clusters, w,
                                               stats ? &st_pw : nullptr);
             if (stats)
@@ -1186,12 +1230,12 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
             fence_tensormap_acquire(mD);
         }
         const bool has_acc = ti.K > 0;
-        const int m0 = ti.m_blk * C::UMMA_M + C::BM * static_cast<int>(rank) + wrow;
+        const int m0 = ti.m_blk * C::TILE_M + C::BM * static_cast<int>(rank) + wrow;
         // 128-row and .ws tiles: thread t holds row t of the warp's rows. 64-row
         // tiles (Layout F): the accumulator with lane alignment 16*acc sits in
         // threads 16*acc..+15.
-        const bool active = WS || C::BM == 128 || (lane >> 4) == acc;
-        const int trow = (WS || C::BM == 128) ? lane : (lane & 15);
+        const bool active = C::WS || C::BM == 128 || (lane >> 4) == acc;
+        const int trow = (C::WS || C::BM == 128) ? lane : (lane & 15);
         if (has_acc) {
             const long long tw = stats ? clock64() : 0;
             bool ok = w.wait(bar_acc_full + 8 * acc, acc_phase, kRoleEpilogue | kWaitAccFull, rank != 0);
@@ -1337,7 +1381,7 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
             __syncwarp();  // tcgen05.ld is .sync.aligned: the warp must be converged
             float v[CW];
             if (has_acc) {
-                const uint32_t col = static_cast<uint32_t>(WS ? acc * C::ACC_COLS + (c - c_lo) * CW
+                const uint32_t col = static_cast<uint32_t>(C::WS ? acc * C::ACC_COLS + (c - c_lo) * CW
                                                               : (C::BM == 128 ? acc * BN : 0) + c * CW);
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + col;
                 uint32_t r[32];
@@ -1431,8 +1475,8 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
 
 // ---------------------------------------------------------------- kernel
 
-template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF, int WS>
-__global__ void __launch_bounds__(Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, WS>::THREADS, 1)
+template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF, int MODE>
+__global__ void __launch_bounds__(Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, MODE>::THREADS, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC,
@@ -1440,7 +1484,7 @@ __global__ void __launch_bounds__(Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, WS>::T
                         const __grid_constant__ CUtensorMap tmSFA,
                         const __grid_constant__ CUtensorMap tmSFB, const __grid_constant__ KParams p)
 {
-    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, WS>;
+    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, MODE>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     if (C::ALIGN_SLACK == 0 && (raw & 1023u) != 0u) {
@@ -1455,7 +1499,7 @@ __global__ void __launch_bounds__(Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, WS>::T
     const int warp = static_cast<int>(threadIdx.x >> 5);
     const int lane = static_cast<int>(threadIdx.x & 31);
     uint32_t rank = 0;
-    if constexpr (CG == 2)
+    if constexpr (C::CLUSTER == 2)
         rank = cluster_ctarank() & 1u;
 
     const uint32_t bar_full = base + C::BAR_OFF;
@@ -1473,7 +1517,7 @@ __global__ void __launch_bounds__(Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, WS>::T
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar_full + 8 * s, 1);
-            mbar_init(bar_empty + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, C::MCB ? 2 : 1);  // B multicast: both CTAs' MMAs release it
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_acc_full + 8 * b, 1);
@@ -1504,7 +1548,7 @@ __global__ void __launch_bounds__(Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, WS>::T
     }
     tc_fence_before_sync();
     __syncthreads();
-    if constexpr (CG == 2)
+    if constexpr (C::CLUSTER == 2)
         cluster_sync_all();  // the peer's barriers exist before anything signals them
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
@@ -1519,11 +1563,12 @@ __global__ void __launch_bounds__(Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, WS>::T
     ProducerTail tail{0, 0, 0u};
     if (warp == 0) {
         if (lane == 0)
-            tail = role_producer<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, WS>(
+            tail = role_producer<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, MODE>(
                 p, &tmA, &tmB, &tmSFA, &tmSFB, stage_base, bar_full, bar_empty, bar_inject, rank, w);
     } else if (warp == 1) {
-        if (lane == 0 && rank == 0) {
-            role_mma<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, WS>(p, stage_base, bar_full, bar_empty,
+        // CTA pairs: the even CTA issues the pair's MMAs; every other CTA its own
+        if (lane == 0 && (CG == 1 || rank == 0)) {
+            role_mma<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, MODE>(p, stage_base, bar_full, bar_empty,
                                                   bar_acc_full, bar_acc_empty, bar_inject, bar_sf,
                                                   tmem_base, w);
             // every MMA issued by this thread has completed before TMEM is freed
@@ -1533,18 +1578,18 @@ __global__ void __launch_bounds__(Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, WS>::T
     } else if (warp >= kSfCopyWarp) {
         // the even CTA copies the scales of both CTAs of a pair (cta_group::2)
         if (lane == 0 && rank == 0) {
-            role_sf_copy<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, WS>(p, stage_base, bar_full, bar_sf, tmem_base, w,
+            role_sf_copy<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, MODE>(p, stage_base, bar_full, bar_sf, tmem_base, w,
                                                                     warp - kSfCopyWarp);
             // arrives once every tcgen05.cp this thread issued has completed
             mma_commit<CG>(bar_cp_drain);
         }
     } else {
         if (p.out_type == 0)
-            role_epilogue<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, WS, 32>(p, &tmC, &tmD, base + C::EPI_OFF,
+            role_epilogue<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, MODE, 32>(p, &tmC, &tmD, base + C::EPI_OFF,
                                                            bar_acc_full, bar_acc_empty, bar_epi,
                                                            tmem_base, rank, warp, lane, w);
         else
-            role_epilogue<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, WS, 64>(p, &tmC, &tmD, base + C::EPI_OFF,
+            role_epilogue<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, MODE, 64>(p, &tmC, &tmD, base + C::EPI_OFF,
                                                            bar_acc_full, bar_acc_empty, bar_epi,
                                                            tmem_base, rank, warp, lane, w);
         if (lane == 0)
@@ -1571,8 +1616,8 @@ __global__ void __launch_bounds__(Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, WS>::T
     }
     tc_fence_before_sync();
     __syncthreads();
-    if constexpr (CG == 2)
-        cluster_sync_all();
+    if constexpr (C::CLUSTER == 2)
+        cluster_sync_all();  // no CTA exits while the other may still write into it
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc<CG>(tmem_base, C::TMEM_COLS);

@@ -41,15 +41,15 @@ cudaError_t ensure_smem_attribute(Kern kern, int bytes, std::atomic<uint64_t> (&
 }
 
 // One record per kernel variant.
-template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF, int WS>
+template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF, int MODE>
 std::atomic<uint64_t> smem_attribute_set[2] = {{0}, {0}};
 
-template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF, int WS>
+template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF, int MODE>
 cudaError_t launch_gemm(const LaunchArgs &a)
 {
-    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, WS>;
-    auto kern = gemm_tcgen05_kernel<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, WS>;
-    cudaError_t e = ensure_smem_attribute(kern, C::SMEM_BYTES, smem_attribute_set<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, WS>);
+    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, MODE>;
+    auto kern = gemm_tcgen05_kernel<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, MODE>;
+    cudaError_t e = ensure_smem_attribute(kern, C::SMEM_BYTES, smem_attribute_set<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, MODE>);
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};
@@ -58,7 +58,7 @@ cudaError_t launch_gemm(const LaunchArgs &a)
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = a.stream;
     cudaLaunchAttribute attr[1];
-    if (CG == 2) {
+    if (C::CLUSTER == 2) {
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 2;
         attr[0].val.clusterDim.y = 1;
@@ -70,15 +70,15 @@ cudaError_t launch_gemm(const LaunchArgs &a)
 }
 
 // Largest number of CTAs of this variant that can be resident at once.
-template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF, int WS>
+template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF, int MODE>
 cudaError_t resident_ctas(int *ctas)
 {
-    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, WS>;
-    auto kern = gemm_tcgen05_kernel<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, WS>;
-    cudaError_t e = ensure_smem_attribute(kern, C::SMEM_BYTES, smem_attribute_set<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, WS>);
+    using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, MODE>;
+    auto kern = gemm_tcgen05_kernel<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, MODE>;
+    cudaError_t e = ensure_smem_attribute(kern, C::SMEM_BYTES, smem_attribute_set<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, MODE>);
     if (e != cudaSuccess)
         return e;
-    if (CG == 1) {
+    if (C::CLUSTER == 1) {
         int per_sm = 0, sms = 0, dev = 0;
         if ((e = cudaGetDevice(&dev)) != cudaSuccess)
             return e;
@@ -107,6 +107,6 @@ cudaError_t resident_ctas(int *ctas)
 
 }  // namespace g300
 
-#define G300_INSTANTIATE(CG, BN, BK, ST, GR, ES, BM, SF, WS)                                             \
-    template cudaError_t g300::launch_gemm<CG, BN, BK, ST, GR, ES, BM, SF, WS>(const g300::LaunchArgs &); \
-    template cudaError_t g300::resident_ctas<CG, BN, BK, ST, GR, ES, BM, SF, WS>(int *);
+#define G300_INSTANTIATE(CG, BN, BK, ST, GR, ES, BM, SF, MO)                                             \
+    template cudaError_t g300::launch_gemm<CG, BN, BK, ST, GR, ES, BM, SF, MO>(const g300::LaunchArgs &); \
+    template cudaError_t g300::resident_ctas<CG, BN, BK, ST, GR, ES, BM, SF, MO>(int *);

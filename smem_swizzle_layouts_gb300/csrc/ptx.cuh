@@ -128,6 +128,18 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *map, uint3
 
 // CTA-pair form: the completion may be signalled on the peer CTA's barrier
 // (`bar` is a shared::cluster address, e.g. the leader's full barrier).
+// TMA box load multicast to both CTAs of a two-CTA cluster: the box lands at
+// shared offset `dst` in each of them and completes bytes on the barrier at
+// `bar` in each (the tensor map covers this GPU's own memory).
+__device__ __forceinline__ void tma_load_2d_mcast2(uint32_t dst, const void *map, uint32_t bar, int c0, int c1)
+{
+    asm volatile("{\n\t.reg .b16 m;\n\tmov.b16 m, 3;\n\t"
+                 "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+                 " [%0], [%1, {%3, %4}], [%2], m;\n\t}" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void *map, uint32_t bar,
                                                  int c0, int c1)
 {
@@ -328,6 +340,16 @@ __device__ __forceinline__ void mma_commit(uint32_t bar)
 // CTA pairs: arrive once on the barrier at the same shared-memory offset in
 // both CTAs of the pair (cluster ranks 0 and 1) when this thread's tcgen05
 // operations have completed.
+// cta_group::1 commit that arrives on the barrier at `bar` in both CTAs of a
+// two-CTA cluster (each CTA's MMAs read its own copy of a multicast stage).
+__device__ __forceinline__ void mma_commit_cg1_multicast(uint32_t bar)
+{
+    asm volatile("{\n\t.reg .b16 m;\n\tmov.b16 m, 3;\n\t"
+                 "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+                 " [%0], m;\n\t}" ::"r"(bar)
+                 : "memory");
+}
+
 __device__ __forceinline__ void mma_commit_pair_multicast(uint32_t bar)
 {
     asm volatile("{\n\t.reg .b16 m;\n\tmov.b16 m, 3;\n\t"

@@ -7,13 +7,13 @@ namespace g300 {
 
 struct LaunchArgs;
 
-template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF, int WS>
+template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF, int MODE>
 cudaError_t launch_gemm(const LaunchArgs &a);
 
-template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF, int WS>
+template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, int SF, int MODE>
 cudaError_t resident_ctas(int *ctas);
 
-// X(cta_group, BN, BK, stages, grouped, element bytes, tile rows, scale kind, ws).
+// X(cta_group, BN, BK, stages, grouped, element bytes, tile rows, scale kind, mode).
 // BN is the MMA N of one tile, BK counts elements; stages fill ~192 KB of
 // shared memory next to 32 KB of epilogue staging. Element bytes 2 =
 // fp16/bf16, 1 = fp8. Tile rows 128, or 64 for single-CTA M=64 MMAs (TMEM
@@ -21,8 +21,9 @@ cudaError_t resident_ctas(int *ctas);
 // elements of K for each row of A and column of B, kind::mxf8f6f4); 2 = NVFP4
 // (packed E2M1, one UE4M3 scale per 16, kind::mxf4nvf4); 3 = MXFP4 (packed
 // E2M1, one E8M0 per 32, kind::mxf4). fp4 tiles count BK in bytes; the scale
-// atoms ride in each stage next to the operand tiles. ws 1: tcgen05.mma.ws
-// (weight-stationary accumulator layout) on 32- or 64-row single-CTA tiles.
+// atoms ride in each stage next to the operand tiles. Mode 1: tcgen05.mma.ws
+// (weight-stationary accumulator layout) on 32- or 64-row single-CTA tiles;
+// mode 2: clusters of two cta_group::1 CTAs sharing B by TMA multicast.
 #define G300_VARIANTS(X)        \
     X(1, 256, 64, 4, false, 2, 128, 0, 0)     \
     X(1, 128, 64, 6, false, 2, 128, 0, 0)     \
@@ -52,6 +53,8 @@ cudaError_t resident_ctas(int *ctas);
     X(2, 256, 256, 3, false, 1, 128, 3, 0) \
     X(1, 256, 64, 5, false, 2, 32, 0, 1) \
     X(1, 128, 128, 4, false, 2, 64, 0, 1) \
-    X(1, 256, 64, 4, false, 2, 64, 0, 1)
+    X(1, 256, 64, 4, false, 2, 64, 0, 1) \
+    X(1, 256, 64, 4, false, 2, 128, 0, 2) \
+    X(1, 256, 128, 4, false, 1, 128, 0, 2)
 
 }  // namespace g300

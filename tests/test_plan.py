@@ -77,9 +77,11 @@ def test_mn_major_swizzle_fits_the_tile_extent(g):
 def test_block_scaled_formats_have_fixed_tiles(g):
     # large MXFP8: 256 x 256 pair tiles; smaller problems and fp4: single CTAs of 128 x 128
     assert plan(g, 8192, 8192, 8192, MXFP8) == dict(cta_group=2, tile_n=256, block_k=256, tile_m=128, swizzle_a=3,
-                                                    swizzle_b=3, epilogue_swizzle=1, group_m=8, mma_ws=0)
+                                                    swizzle_b=3, epilogue_swizzle=1, group_m=8, mma_ws=0,
+                                                    multicast_b=0)
     assert plan(g, 1024, 8192, 8192, MXFP8) == dict(cta_group=1, tile_n=128, block_k=256, tile_m=128, swizzle_a=3,
-                                                    swizzle_b=3, epilogue_swizzle=1, group_m=8, mma_ws=0)
+                                                    swizzle_b=3, epilogue_swizzle=1, group_m=8, mma_ws=0,
+                                                    multicast_b=0)
     assert plan(g, 8192, 8192, 8192, MXFP8, cta_group=2)["tile_n"] == 128
     assert plan(g, 8192, 8192, 8192, MXFP8, cta_group=2, tile_n=256)["tile_n"] == 256
     # a stage depth only single CTAs are built for keeps large problems on single CTAs
@@ -149,3 +151,30 @@ def test_weight_stationary_tiles(g):
     with pytest.raises(g.GemmError) as ei:
         g.gemm_debug_plan(32, 4096, 4096, BF16, K_MAJOR, K_MAJOR, grouped=True, options=dict(mma_ws=1), sms=SMS)
     assert ei.value.status == g.ERR_UNSUPPORTED
+
+
+def test_b_multicast_clusters(g):
+    # two single-CTA 128 x 256 tiles share their B panel by multicast when asked
+    p = plan(g, 4096, 4096, 4096, cta_group=1, tile_n=256, multicast_b=1)
+    assert (p["cta_group"], p["tile_n"], p["block_k"], p["tile_m"], p["multicast_b"]) == (1, 256, 64, 128, 1)
+    p = plan(g, 8192, 8192, 8192, FP8, cta_group=1, tile_n=256, multicast_b=1)
+    assert (p["block_k"], p["multicast_b"]) == (128, 1)
+    for kind, opts in [(BF16, dict(cta_group=2, multicast_b=1)), (BF16, dict(tile_m=64, multicast_b=1)),
+                       (MXFP8, dict(multicast_b=1)), (BF16, dict(cta_group=1, tile_n=128, multicast_b=1))]:
+        with pytest.raises(g.GemmError) as ei:
+            plan(g, 4096, 4096, 4096, kind, **opts)
+        assert ei.value.status == g.ERR_UNSUPPORTED, (kind, opts)
+    with pytest.raises(g.GemmError) as ei:
+        plan(g, 4096, 4096, 4096, multicast_b=2)
+    assert ei.value.status == g.ERR_INVALID_ARG
+
+
+def test_b_multicast_default_rule(g):
+    # single-CTA 128 x 256 tiles share B by default when B is MN-major or A + B overflow L2
+    assert plan(g, 4096, 4096, 4096, cta_group=1, tile_n=256)["multicast_b"] == 0           # K/K, 64 MB
+    assert plan(g, 4096, 4096, 4096, b=MN_MAJOR, cta_group=1, tile_n=256)["multicast_b"] == 1
+    assert plan(g, 8192, 8192, 8192, cta_group=1, tile_n=256)["multicast_b"] == 1           # 256 MB
+    assert plan(g, 8192, 8192, 2048, cta_group=1, tile_n=256)["multicast_b"] == 0           # 64 MB
+    assert plan(g, 8192, 8192, 8192, cta_group=1, tile_n=256, multicast_b=-1)["multicast_b"] == 0
+    assert plan(g, 128, 8192, 8192, cta_group=1, tile_n=256)["multicast_b"] == 0            # one row tile
+    assert plan(g, 8192, 8192, 8192)["cta_group"] == 2                                     # pairs stay the default
