@@ -70,11 +70,10 @@ typedef enum { GEMM_OUT_F32 = 0, GEMM_OUT_BF16 = 1, GEMM_OUT_F16 = 2 } gemm_out_
  * the page's "128-byte mode with 32-byte atomicity" (descriptor code 1):
  * 128-byte rows whose 32-byte units are XORed with the row index mod 4
  * (Swizzle<2,5,2>, written by TMA's 128B_ATOM_32B mode), read as an MN-major
- * operand with K rows in bands of 4. The inspection entry points accept it
- * (descriptor words, TMA stage images); GEMM calls return
- * GEMM_ERR_UNSUPPORTED, because the MMA kinds this library issues
- * (kind::f16, kind::f8f6f4, block-scaled) read such operands as zeros on
- * GB300 (measured). */
+ * operand with K rows in bands of 4. It is the layout of MN-major TF32
+ * operands (gemm_ex in_type 2, the default there); 16- and 8-bit operands
+ * refuse it with GEMM_ERR_UNSUPPORTED, because kind::f16 and kind::f8f6f4
+ * read such operands as zeros on GB300 (measured). */
 typedef enum {
     GEMM_SWIZZLE_AUTO = 0,
     GEMM_SWIZZLE_32B = 1,
@@ -228,7 +227,15 @@ gemm_status_t gemm_f16(int64_t M, int64_t N, int64_t K,
                        void *D, int64_t ldd, gemm_out_t d_type,
                        float alpha, float beta, gemm_stream_t stream);
 
-/* The same with explicit options (opts may be NULL). in_type: 0 fp16, 1 bf16. */
+/* The same with explicit options (opts may be NULL). in_type: 0 fp16, 1 bf16,
+ * 2 TF32: A and B hold fp32 words (leading dimensions in elements, multiples
+ * of 4) and tcgen05 kind::tf32 multiplies their TF32 part -- sign, exponent
+ * and the top 10 fraction bits; the low 13 fraction bits are dropped (a
+ * reading of the hardware, pinned by the tests). MN-major TF32 operands are
+ * staged in the 128-byte swizzle with 32-byte atoms (GEMM_SWIZZLE_128B_ATOM32,
+ * descriptor code 1): kind::tf32 reads an MN-major operand in that layout and
+ * as zeros in SW128 (measured); K-major TF32 operands use the 32/64/128-byte
+ * swizzles of the 16-bit types. */
 gemm_status_t gemm_ex(int in_type, int64_t M, int64_t N, int64_t K,
                       const void *A, gemm_major_t a_major, int64_t lda,
                       const void *B, gemm_major_t b_major, int64_t ldb,
@@ -463,7 +470,8 @@ gemm_status_t gemm_debug_stage_image(const void *src, int major, int swizzle,
 /*
  * Host-side tile plan (no GPU needed): the configuration a call would launch
  * on a device with `sms` SMs. kind: 0 fp16/bf16, 1 fp8, 2 MXFP8, 3 NVFP4,
- * 4 MXFP4 (K in elements); grouped: nonzero for the grouped entry points.
+ * 4 MXFP4 (K in elements), 5 TF32; grouped: nonzero for the grouped entry
+ * points.
  * Writes 10 int32: cta_group, tile N, K per stage (bytes for fp4), rows per
  * CTA, swizzle bits of A and B (0 none, 1 32B, 2 64B, 3 128B, 4 128B with
  * 32-byte atoms), epilogue swizzle, group height, 1 when the tiles use

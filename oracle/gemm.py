@@ -21,7 +21,7 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-FMT = {"f16": 0, "bf16": 1, "f32": 2, "e4m3": 3, "e5m2": 4}
+FMT = {"f16": 0, "bf16": 1, "f32": 2, "e4m3": 3, "e5m2": 4, "tf32": 5}
 MAJOR = {"K": 0, "MN": 1}
 
 

@@ -37,7 +37,19 @@
 #include <omp.h>
 #endif
 
-enum { ORC_F16 = 0, ORC_BF16 = 1, ORC_F32 = 2, ORC_E4M3 = 3, ORC_E5M2 = 4 };
+enum { ORC_F16 = 0, ORC_BF16 = 1, ORC_F32 = 2, ORC_E4M3 = 3, ORC_E5M2 = 4, ORC_TF32 = 5 };
+
+/* TF32 operand read from fp32 storage (tcgen05 kind::tf32 operands are fp32
+ * words). Reading: the tensor core keeps the sign, the 8 exponent bits and the
+ * top 10 of the 23 fraction bits, i.e. the low 13 fraction bits are dropped
+ * (truncation, not rounding); values representable in TF32 are unchanged. */
+static double decode_tf32(uint32_t u)
+{
+    u &= ~(uint32_t)0x1FFF;
+    float x;
+    memcpy(&x, &u, sizeof x);
+    return (double)x;
+}
 
 /* IEEE binary16: 1 sign, 5 exponent (bias 15), 10 fraction bits. */
 static double decode_f16(uint16_t h)
@@ -110,6 +122,7 @@ double oracle_decode(int fmt, uint32_t bits)
     case ORC_BF16: return decode_bf16((uint16_t)bits);
     case ORC_E4M3: return decode_e4m3((uint8_t)bits);
     case ORC_E5M2: return decode_e5m2((uint8_t)bits);
+    case ORC_TF32: return decode_tf32(bits);
     default: {
         float x;
         memcpy(&x, &bits, sizeof x);
@@ -132,6 +145,7 @@ static double load(const void *p, int fmt, int64_t idx)
     case ORC_BF16: return decode_bf16(((const uint16_t *)p)[idx]);
     case ORC_E4M3: return decode_e4m3(((const uint8_t *)p)[idx]);
     case ORC_E5M2: return decode_e5m2(((const uint8_t *)p)[idx]);
+    case ORC_TF32: return decode_tf32(((const uint32_t *)p)[idx]);
     default: return decode_f32(((const uint32_t *)p)[idx]);
     }
 }

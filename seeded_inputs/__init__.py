@@ -78,7 +78,7 @@ def _draw(seed: int, dist: str, start: int, count: int, scale: float) -> np.ndar
 
 
 def to_storage(x: np.ndarray, dtype: str) -> np.ndarray:
-    """Round float64 values to ``dtype`` ('f16', 'bf16', 'f32', 'e4m3', 'e5m2'); return the bits.
+    """Round float64 values to ``dtype`` ('f16', 'bf16', 'f32', 'tf32', 'e4m3', 'e5m2'); return the bits.
 
     fp8 rounding (ties to even, through float32) uses PyTorch's float8_e4m3fn and
     float8_e5m2 conversions; the inputs stay far inside both formats' ranges.
@@ -92,6 +92,12 @@ def to_storage(x: np.ndarray, dtype: str) -> np.ndarray:
         return x.astype(np.float16).view(np.uint16)
     if dtype == "f32":
         return x.astype(np.float32).view(np.uint32)
+    if dtype == "tf32":
+        # fp32 words holding values representable in TF32 (10 fraction bits): round the
+        # fp32 value to nearest-even at fraction bit 10 and clear the 13 bits below it
+        b = x.astype(np.float32).view(np.uint32).astype(np.uint64)
+        b = (b + np.uint64(0xFFF) + ((b >> np.uint64(13)) & np.uint64(1))) & np.uint64(0xFFFFE000)
+        return b.astype(np.uint32)
     if dtype == "bf16":
         b = x.astype(np.float32).view(np.uint32).astype(np.uint64)
         b = (b + np.uint64(0x7FFF) + ((b >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)
@@ -119,7 +125,7 @@ def matrix_bits(seed: int, rows: int, cols: int, dist: str, dtype: str,
     The result is a 2-D array of the stored shape (with the padding columns).
     """
     n = rows * cols
-    bits_dtype = np.uint32 if dtype == "f32" else (np.uint8 if dtype in ("e4m3", "e5m2") else np.uint16)
+    bits_dtype = np.uint32 if dtype in ("f32", "tf32") else (np.uint8 if dtype in ("e4m3", "e5m2") else np.uint16)
     flat = np.empty(n, dtype=bits_dtype)
     for s in range(0, n, _CHUNK):
         c = min(_CHUNK, n - s)
@@ -141,7 +147,7 @@ def bits_to_float64(bits: np.ndarray, dtype: str) -> np.ndarray:
     """Exact float64 values of stored bit patterns (for building expected tables)."""
     if dtype == "f16":
         return bits.view(np.float16).astype(np.float64)
-    if dtype == "f32":
+    if dtype in ("f32", "tf32"):
         return bits.view(np.float32).astype(np.float64)
     if dtype == "bf16":
         return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
@@ -159,7 +165,7 @@ def torch_from_bits(bits: np.ndarray, dtype: str):
     if dtype in ("f16", "bf16"):
         t = torch.from_numpy(b.view(np.int16))
         return t.view(torch.float16 if dtype == "f16" else torch.bfloat16)
-    if dtype == "f32":
+    if dtype in ("f32", "tf32"):
         return torch.from_numpy(b.view(np.int32)).view(torch.float32)
     if dtype in ("e4m3", "e5m2"):
         return torch.from_numpy(b.view(np.uint8))  # raw bytes; the library reads them as fp8

@@ -127,6 +127,9 @@ InFmt fmt16(int in_bf16) { return InFmt{in_bf16, 2, in_bf16, in_bf16, kScaleNone
 
 InFmt fmt8(int a_fmt, int b_fmt) { return InFmt{2, 1, a_fmt, b_fmt, kScaleNone}; }
 
+// TF32: fp32 words in memory (tensor-map type FLOAT32), MMA format code 2 in kind::tf32.
+InFmt fmt32() { return InFmt{3, 4, 2, 2, kScaleNone}; }
+
 // Block-scaled fp8: the same operand bytes plus E8M0 scale atoms.
 InFmt fmtmx(int a_fmt, int b_fmt) { return InFmt{2, 1, a_fmt, b_fmt, kScaleMx8}; }
 
@@ -211,10 +214,11 @@ gemm_status_t encode_operand(CUtensorMap *m, int dcode, const void *ptr, int mn_
                              int swz_bits, int64_t mn_total, int64_t k_total, int64_t ld, int rows,
                              int bk)
 {
-    const CUtensorMapDataType dt = dcode == 2   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+    const CUtensorMapDataType dt = dcode == 3   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : dcode == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                    : dcode == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    const uint32_t esize = dcode == 2 ? 1u : 2u;
+    const uint32_t esize = dcode == 3 ? 4u : dcode == 2 ? 1u : 2u;
     const uint32_t per = swizzle_row_bytes(swz_bits) / esize;
     if (!mn_major)
         return encode_2d(m, dt, ptr, static_cast<uint64_t>(k_total), static_cast<uint64_t>(mn_total),
@@ -326,6 +330,8 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
     if (bk == 0) {
         if (esize == 1)
             bk = (cg == 1 && bn == 256) ? 128 : 256;  // the same stage bytes as bf16
+        else if (esize == 4)
+            bk = (cg == 1 && bn == 256) ? 32 : 64;
         else if (!grouped && cg == 1 && bn == 128 && K <= 32 && opt.tile_n == 0)
             bk = 32;
         else
@@ -403,6 +409,8 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
     auto pick_swz = [&](int requested, int mn_major, int rows) -> int {
         if (requested)
             return swz_bits_of(requested);
+        if (esize == 4 && mn_major)
+            return kSwzAtom32;  // the MN-major layout kind::tf32 reads
         const int span = (mn_major ? rows : bk) * esize;
         return span >= 128 ? 3 : span >= 64 ? 2 : 1;
     };
@@ -412,11 +420,12 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
     plan->a_swz = pick_swz(opt.swizzle_a, a_mn, bm);
     plan->b_swz = pick_swz(opt.swizzle_b, b_mn, bn / cg);
     // a K-major swizzled row may not be wider than the K block; an MN-major
-    // atom may not be wider than the tile's MN extent. The 32-byte-atom mode
-    // is not an operand layout of the MMA kinds issued here: on GB300 a
-    // kind::f16 or kind::f8f6f4 MMA reads such an operand as zeros
+    // atom may not be wider than the tile's MN extent. MN-major operands of
+    // kind::tf32 take the 32-byte-atom mode and no other (on GB300 an MN-major
+    // TF32 operand in SW128 reads as zeros), and 16- and 8-bit operands never
+    // take it (kind::f16 and kind::f8f6f4 read it as zeros)
     auto fits = [&](int bits, int mn_major, int rows) {
-        if (bits == kSwzAtom32)
+        if ((bits == kSwzAtom32) != (esize == 4 && mn_major != 0))
             return false;
         const int per = static_cast<int>(swizzle_row_bytes(bits)) / esize;
         return mn_major ? (rows % per == 0) : (bk % per == 0);
@@ -962,10 +971,10 @@ gemm_status_t gemm_ex(int in_type, int64_t M, int64_t N, int64_t K, const void *
                       int64_t ldc, void *D, int64_t ldd, gemm_out_t d_type, float alpha, float beta,
                       const gemm_options_t *opts, gemm_stream_t stream)
 {
-    if (in_type != 0 && in_type != 1)
+    if (in_type < 0 || in_type > 2)
         return GEMM_ERR_INVALID_ARG;
-    return run_single(fmt16(in_type), M, N, K, A, a_major, lda, B, b_major, ldb, C, ldc, D, ldd, d_type, alpha,
-                      beta, opts, reinterpret_cast<cudaStream_t>(stream));
+    return run_single(in_type == 2 ? fmt32() : fmt16(in_type), M, N, K, A, a_major, lda, B, b_major, ldb, C, ldc,
+                      D, ldd, d_type, alpha, beta, opts, reinterpret_cast<cudaStream_t>(stream));
 }
 
 gemm_status_t gemm_fp8_ex(int64_t M, int64_t N, int64_t K, const void *A, gemm_fp8_t a_format,
@@ -1118,12 +1127,12 @@ gemm_status_t gemm_debug_descriptors(int major, int swizzle, int rows, int bk, u
                                      int b_major, uint64_t *out, gemm_stream_t stream)
 {
     if (!valid_enum(major) || swizzle < 1 || swizzle > 5 || rows <= 0 || bk <= 0 || n_slices < 0 ||
-        (cta_group != 1 && cta_group != 2) || tile_n <= 0 || !out || in_type < 0 || in_type > 3 ||
+        (cta_group != 1 && cta_group != 2) || tile_n <= 0 || !out || in_type < 0 || in_type > 4 ||
         !valid_enum(a_major) || !valid_enum(b_major))
         return GEMM_ERR_INVALID_ARG;
-    // in_type 0 fp16, 1 bf16 (kind::f16); 2 E4M3, 3 E5M2 (kind::f8f6f4)
-    const int esize = in_type >= 2 ? 1 : 2;
-    const int fmt = in_type >= 2 ? in_type - 2 : in_type;
+    // in_type 0 fp16, 1 bf16 (kind::f16); 2 E4M3, 3 E5M2 (kind::f8f6f4); 4 TF32 (kind::tf32)
+    const int esize = in_type == 4 ? 4 : in_type >= 2 ? 1 : 2;
+    const int fmt = in_type == 4 ? 2 : in_type >= 2 ? in_type - 2 : in_type;
     debug_descriptor_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
         major, swz_bits_of(swizzle), rows, bk, stage_addr, n_slices, 128 * cta_group, tile_n, fmt, esize,
         a_major, b_major, out);
@@ -1176,11 +1185,12 @@ gemm_status_t gemm_debug_stage_image(const void *src, int major, int swizzle, in
 gemm_status_t gemm_debug_plan(int64_t M, int64_t N, int64_t K, int kind, int a_major, int b_major, int grouped,
                               const gemm_options_t *opts, int sms, int32_t *out)
 {
-    if (!out || sms <= 0 || kind < 0 || kind > 4 || !valid_enum(a_major) || !valid_enum(b_major) || M < 0 ||
+    if (!out || sms <= 0 || kind < 0 || kind > 5 || !valid_enum(a_major) || !valid_enum(b_major) || M < 0 ||
         N < 0 || K < 0)
         return GEMM_ERR_INVALID_ARG;
-    // kind: 0 fp16/bf16, 1 fp8, 2 MXFP8, 3 NVFP4, 4 MXFP4 (fp4: K counted in elements, planned in bytes)
-    const int esize = kind == 0 ? 2 : 1;
+    // kind: 0 fp16/bf16, 1 fp8, 2 MXFP8, 3 NVFP4, 4 MXFP4 (fp4: K counted in elements, planned in
+    // bytes), 5 TF32
+    const int esize = kind == 5 ? 4 : kind == 0 ? 2 : 1;
     const int sf = kind == 2 ? kScaleMx8 : kind == 3 ? kScaleNv4 : kind == 4 ? kScaleMx4 : kScaleNone;
     const int64_t k_plan = kind >= 3 ? K / 2 : K;
     Plan pl;

@@ -178,8 +178,8 @@ __host__ __device__ constexpr int sf_atom_kbytes(int sf)
     return sf == kScaleMx8 ? 128 : sf == kScaleNv4 ? 32 : 64;
 }
 
-// ESIZE: bytes per operand element, 2 (fp16/bf16, tcgen05 kind::f16) or
-// 1 (fp8, kind::f8f6f4). BK counts elements of K per stage. BMT: accumulator
+// ESIZE: bytes per operand element, 2 (fp16/bf16, tcgen05 kind::f16),
+// 1 (fp8, kind::f8f6f4) or 4 (fp32 words read as TF32, kind::tf32). BK counts elements of K per stage. BMT: accumulator
 // rows per CTA, 128 (row m in TMEM lane m) or 64 (cta_group::1 only, Layout F:
 // rows 16g..16g+15 in lanes 32g+a..32g+a+15; the two accumulators of the
 // double buffer take lane alignments a = 0 and 16 and share their columns).
@@ -910,6 +910,9 @@ __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uin
                     else if constexpr (ESIZE == 2)
                         mma_f16<CG>(d_tmem, a_desc0 + sdelta + a_off[j], b_desc0 + sdelta + b_off[j], idesc,
                                     ((kb - kb_lo) | j) != 0);
+                    else if constexpr (ESIZE == 4)
+                        mma_tf32<CG>(d_tmem, a_desc0 + sdelta + a_off[j], b_desc0 + sdelta + b_off[j], idesc,
+                                     ((kb - kb_lo) | j) != 0);
                     else
                         mma_f8<CG>(d_tmem, a_desc0 + sdelta + a_off[j], b_desc0 + sdelta + b_off[j], idesc,
                                    ((kb - kb_lo) | j) != 0);

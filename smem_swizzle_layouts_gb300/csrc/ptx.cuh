@@ -303,6 +303,25 @@ __device__ __forceinline__ void mma_ws_f16(uint32_t d_tmem, uint64_t adesc, uint
                  : "memory");
 }
 
+// D[tmem] (+)= A * B, kind::tf32: fp32 operand words read as TF32 (K = 8 per MMA), fp32 accumulate.
+template <int CG>
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate)
+{
+    if constexpr (CG == 1)
+        asm volatile("{\n\t.reg .pred p;\n\t"
+                     "setp.ne.b32 p, %4, 0;\n\t"
+                     "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                     "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+                     : "memory");
+    else
+        asm volatile("{\n\t.reg .pred p;\n\t"
+                     "setp.ne.b32 p, %4, 0;\n\t"
+                     "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                     "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+                     : "memory");
+}
+
 // D[tmem] (+)= A * B, kind::f8f6f4 with 8-bit A/B (E4M3 or E5M2), fp32 accumulate.
 template <int CG>
 __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,

@@ -16,7 +16,7 @@ cudaError_t resident_ctas(int *ctas);
 // X(cta_group, BN, BK, stages, grouped, element bytes, tile rows, scale kind, mode).
 // BN is the MMA N of one tile, BK counts elements; stages fill ~192 KB of
 // shared memory next to 32 KB of epilogue staging. Element bytes 2 =
-// fp16/bf16, 1 = fp8. Tile rows 128, or 64 for single-CTA M=64 MMAs (TMEM
+// fp16/bf16, 1 = fp8, 4 = fp32 words read as TF32. Tile rows 128, or 64 for single-CTA M=64 MMAs (TMEM
 // Layout F). Scale kind 0 = none; 1 = MXFP8 (fp8, one E8M0 scale per 32
 // elements of K for each row of A and column of B, kind::mxf8f6f4); 2 = NVFP4
 // (packed E2M1, one UE4M3 scale per 16, kind::mxf4nvf4); 3 = MXFP4 (packed
@@ -54,6 +54,9 @@ cudaError_t resident_ctas(int *ctas);
     X(1, 256, 64, 5, false, 2, 32, 0, 1) \
     X(1, 128, 128, 4, false, 2, 64, 0, 1) \
     X(1, 256, 64, 4, false, 2, 64, 0, 1) \
+    X(1, 256, 32, 4, false, 4, 128, 0, 0) \
+    X(1, 128, 64, 3, false, 4, 128, 0, 0) \
+    X(2, 256, 64, 3, false, 4, 128, 0, 0) \
     X(1, 256, 64, 4, false, 2, 128, 0, 2) \
     X(1, 256, 128, 4, false, 1, 128, 0, 2)
 

@@ -74,7 +74,7 @@ def run_case(g, M, N, K, *, in_fmt="bf16", b_fmt=None, a_major="K", b_major="K",
         g.gemm_fp8_ex(M, N, K, At, FP8[in_fmt], am, lda, Bt, FP8[b_fmt], bm, ldb, Ct, ldd if C is not None else 0,
                       Dt, ldd, dt, alpha, beta, options=options)
     else:
-        in_type = 1 if in_fmt == "bf16" else 0
+        in_type = {"f16": 0, "bf16": 1, "tf32": 2}[in_fmt]
         g.gemm_ex(in_type, M, N, K, At, am, lda, Bt, bm, ldb, Ct, ldd if C is not None else 0, Dt, ldd, dt,
                   alpha, beta, options=options)
     st, word = g.gemm_last_device_status()

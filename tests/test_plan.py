@@ -8,7 +8,7 @@ formats, and the options it must refuse.
 import pytest
 
 SMS = 148
-BF16, FP8, MXFP8, NVFP4, MXFP4 = 0, 1, 2, 3, 4
+BF16, FP8, MXFP8, NVFP4, MXFP4, TF32 = 0, 1, 2, 3, 4, 5
 K_MAJOR, MN_MAJOR = 0, 1
 
 
@@ -178,3 +178,18 @@ def test_b_multicast_default_rule(g):
     assert plan(g, 8192, 8192, 8192, cta_group=1, tile_n=256, multicast_b=-1)["multicast_b"] == 0
     assert plan(g, 128, 8192, 8192, cta_group=1, tile_n=256)["multicast_b"] == 0            # one row tile
     assert plan(g, 8192, 8192, 8192)["cta_group"] == 2                                     # pairs stay the default
+
+
+def test_tf32_tiles_and_swizzles(g):
+    # TF32 stages hold the bytes of the 16-bit ones; MN-major TF32 operands take the
+    # 32-byte-atom swizzle (bits 4) and nothing else, K-major ones SW128
+    p = plan(g, 4096, 4096, 4096, TF32, b=MN_MAJOR, cta_group=1, tile_n=256)
+    assert (p["block_k"], p["swizzle_a"], p["swizzle_b"]) == (32, 3, 4)
+    p = plan(g, 8192, 8192, 8192, TF32, a=MN_MAJOR, b=MN_MAJOR)
+    assert (p["cta_group"], p["block_k"], p["swizzle_a"], p["swizzle_b"]) == (2, 64, 4, 4)
+    for opts in (dict(swizzle_b=3), dict(swizzle_b=4), dict(swizzle_b=2)):
+        with pytest.raises(g.GemmError) as ei:
+            plan(g, 4096, 4096, 4096, TF32, b=MN_MAJOR, **opts)
+        assert ei.value.status == g.ERR_UNSUPPORTED, opts
+    with pytest.raises(g.GemmError):
+        plan(g, 4096, 4096, 4096, TF32, swizzle_a=5)      # K-major TF32: not the 32-byte-atom mode
