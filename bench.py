@@ -403,10 +403,18 @@ class GroupedJob:
         self.ws_bytes = g.gemm_grouped_workspace_size(len(self.Ms))
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
         self.flops = float(sum(2.0 * M * N * K for M in self.Ms))
+        self.options = options
+
+    def _launch(self, probs, ws):
+        if self.options:
+            self.g.gemm_grouped_ex(1, probs, 0, 0, 1, self.wl["alpha"], self.wl["beta"], ws, self.ws_bytes,
+                                   options=self.options, stream=self.stream)
+        else:
+            self.g.gemm_bf16_grouped(probs, 0, 0, 1, self.wl["alpha"], self.wl["beta"], ws, self.ws_bytes,
+                                     stream=self.stream)
 
     def step(self):
-        self.g.gemm_bf16_grouped(self.probs, 0, 0, 1, self.wl["alpha"], self.wl["beta"], self.ws, self.ws_bytes,
-                                 stream=self.stream)
+        self._launch(self.probs, self.ws)
 
     def outputs(self):
         return self.outs
@@ -418,10 +426,9 @@ class GroupedJob:
         outs = [(torch.empty_like(d), h) for d, h in self.outs]
         probs = [dict(q, A=twin[id(q["A"])], B=twin[id(q["B"])], D=o[0]) for q, o in zip(self.probs, outs)]
         ws = torch.empty_like(self.ws)
-        wl, g, stream, ws_bytes = self.wl, self.g, self.stream, self.ws_bytes
 
         def call():
-            g.gemm_bf16_grouped(probs, 0, 0, 1, wl["alpha"], wl["beta"], ws, ws_bytes, stream=stream)
+            self._launch(probs, ws)
         return _DeviceSet([(h, twin[id(d)]) for h, d in self.pairs], call, outs)
 
     def oracle_rate(self, target_s, fixed_rows=None):

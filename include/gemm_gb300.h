@@ -379,7 +379,9 @@ gemm_status_t gemm_f16_grouped(const gemm_problem_t *problems, int num_problems,
                                gemm_stream_t stream);
 
 /* The grouped call with explicit options (opts may be NULL; tile_m, timeout
- * and flags as for gemm_ex). in_type: 0 fp16, 1 bf16. */
+ * and flags as for gemm_ex). in_type: 0 fp16, 1 bf16. Without a cta_group
+ * option, lists whose widest problem has N >= 2048 and whose tallest has
+ * M >= 256 run on CTA pairs (256 x 256 tiles), others on single CTAs. */
 gemm_status_t gemm_grouped_ex(int in_type, const gemm_problem_t *problems, int num_problems,
                               gemm_major_t a_major, gemm_major_t b_major,
                               gemm_out_t d_type, float alpha, float beta,

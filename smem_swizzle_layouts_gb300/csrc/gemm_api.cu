@@ -692,8 +692,11 @@ gemm_status_t plan_grouped(int in_bf16, const gemm_problem_t *probs, int n, int 
     gemm_options_t o = {};
     if (opts)
         o = *opts;
+    // CTA pairs for lists of wide problems, as for single ones (64 problems of
+    // M_i in 128..4096, N = 4096, K = 2048: 1651 against 1596 TFLOP/s for
+    // single CTAs); single CTAs otherwise
     if (o.cta_group == 0)
-        o.cta_group = 1;
+        o.cta_group = (maxN >= 2048 && maxM >= 256) ? 2 : 1;
     if (o.tile_n == 0)  // grouped pairs are built for 256-wide tiles only
         o.tile_n = (maxN >= 192 || o.cta_group == 2) ? 256 : 128;
     if ((s = make_plan(maxM, maxN, maxK, a_mn, b_mn, gc->sms, &o, true, &gc->pl)) != GEMM_OK)
