@@ -411,8 +411,9 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
             return swz_bits_of(requested);
         if (esize == 4 && mn_major)
             return kSwzAtom32;  // the MN-major layout kind::tf32 reads
+        // widest row that divides the extent (a 192-byte K stage takes 64-byte rows)
         const int span = (mn_major ? rows : bk) * esize;
-        return span >= 128 ? 3 : span >= 64 ? 2 : 1;
+        return span % 128 == 0 ? 3 : span % 64 == 0 ? 2 : 1;
     };
     plan->cg = cg;
     plan->bn = bn;
