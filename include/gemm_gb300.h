@@ -118,6 +118,12 @@ typedef enum {
  *                 problems with 128-row tiles) reads C from global memory
  *                 straight into the epilogue's registers instead of staging
  *                 it in shared memory by TMA (ablation: 1 % slower at 8192^3).
+ *                 Bit 5 splits each stage's loads between two producer
+ *                 warps, one for the A boxes (and A scale atoms), one for
+ *                 the B boxes (and B scale atoms); NVFP4 kernels, which have
+ *                 no room for the second warp, ignore it (ablation: no
+ *                 measured effect, the loads are bound by L2 delivery, not
+ *                 by the issuing thread).
  *   stats         diagnostics: NULL, or device memory of 16 uint64 per CTA
  *                 of the grid (at least 16 * number of SMs), where each CTA
  *                 writes cycles its roles spent waiting (slots 0-1 producer,

@@ -153,6 +153,7 @@ enum : int {
     kFlagRotateK = 4,          // start each tile's K loop at a per-cluster offset
     kFlagCacheHints = 8,       // operands evict_last, C loads and D stores evict_first in L2
     kFlagDirectC = 16,         // single problems, 128-row tiles: C read into registers, not staged
+    kFlagSplitLoad = 32,       // two producer warps: A boxes (and scale atoms) from one, B boxes from the other
 };
 
 // K block processed at iteration `it` of a tile: with kFlagRotateK the
@@ -217,7 +218,12 @@ struct Cfg {
     // threads per CTA: the scale copier warp exists only for block-scaled kinds
     // scale copier warps: NVFP4 stages carry three times the atoms of the others
     static constexpr int SF_COPIERS = SF == kScaleNv4 ? 2 : SF ? 1 : 0;
-    static constexpr int THREADS = 32 * (kSfCopyWarp + SF_COPIERS);
+    // the second producer warp (B boxes when loads are split) comes last; the
+    // NVFP4 kernels, with two copier warps, go without it: a ninth warp puts
+    // three warps on one SM sub-partition and caps registers below their need
+    static constexpr bool HAS_LOADB = kSfCopyWarp + SF_COPIERS < 8;
+    static constexpr int LOADB_WARP = HAS_LOADB ? kSfCopyWarp + SF_COPIERS : -1;
+    static constexpr int THREADS = 32 * (kSfCopyWarp + SF_COPIERS + (HAS_LOADB ? 1 : 0));
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     // + slack to round the base up to 1024 bytes; the dynamic shared memory is
     // declared 1024-aligned, so a variant that would not fit with the slack
@@ -566,14 +572,23 @@ template <int CG, int BN, int BK, int STAGES, bool GROUPED, int ESIZE, int BMT, 
 __device__ ProducerTail role_producer(const KParams &p, const CUtensorMap *tmA, const CUtensorMap *tmB,
                                       const CUtensorMap *tmSFA, const CUtensorMap *tmSFB,
                                       uint32_t smem, uint32_t bar_full, uint32_t bar_empty, uint32_t bar_inject,
-                                      uint32_t rank, const Waiter &w)
+                                      uint32_t rank, const Waiter &w, int part)
 {
     using C = Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, MODE>;
     if (p.inject_timeout == kRoleProducer) {
         // Test hook: wait on a barrier nothing arrives at; the bound runs out.
-        w.wait(bar_inject, 0u, kRoleProducer | kWaitInjected);
+        // The B warp of split loads stays idle, so nothing is in flight.
+        if (part != 2)
+            w.wait(bar_inject, 0u, kRoleProducer | kWaitInjected);
         return ProducerTail{0, 0, 0u};
     }
+    // part 0 loads whole stages; with split loads part 1 loads the A boxes and
+    // A scale atoms and part 2 the B boxes and B scale atoms, each arming the
+    // stage's full barrier (two arrivals) with the bytes it loads
+    const bool do_a = part != 2, do_b = part != 1;
+    const uint32_t tx = part == 0   ? static_cast<uint32_t>(C::TX_BYTES)
+                        : part == 1 ? static_cast<uint32_t>((C::A_BYTES + C::SF_A_BYTES) * CG)
+                                    : static_cast<uint32_t>((C::B_BYTES + C::SF_B_BYTES) * CG);
     const Sched sched = make_sched(p);
     const int flags = p.flags;
     unsigned long long *const stats = p.stats;
@@ -593,7 +608,7 @@ __device__ ProducerTail role_producer(const KParams &p, const CUtensorMap *tmA, 
         }
     }
     const int nbox = boxA.nbox > boxB.nbox ? boxA.nbox : boxB.nbox;
-    const bool forward = CG == 2 && rank == 0 && (flags & kFlagPairForward);
+    const bool forward = CG == 2 && rank == 0 && (flags & kFlagPairForward) && part != 2;
     const int sf_groups = p.sf_groups;
     // operand tiles are re-read by other tiles of the wave: keep them in L2
     const bool hints = (flags & kFlagCacheHints) != 0;
@@ -647,7 +662,7 @@ __device__ ProducerTail role_producer(const KParams &p, const CUtensorMap *tmA, 
             if (forward && issued >= STAGES)
                 mbar_arrive_cluster(peer_empty + 8 * stage);
             if (rank == 0 || C::MCB)
-                mbar_arrive_expect_tx(bar_full + 8 * stage, C::TX_BYTES);
+                mbar_arrive_expect_tx(bar_full + 8 * stage, tx);
             const uint32_t sA = smem + stage * C::STAGE_BYTES;
             const uint32_t sB = sA + C::A_BYTES;
             const uint32_t fb = full_target + 8 * stage;
@@ -655,9 +670,9 @@ __device__ ProducerTail role_producer(const KParams &p, const CUtensorMap *tmA, 
             // A and B boxes alternate, so both operands of the stage are in flight together
             if constexpr (C::MCB) {
                 for (int b = 0; b < nbox; ++b) {
-                    if (b < boxA.nbox)
+                    if (do_a && b < boxA.nbox)
                         issue_box<1>(mA, sA, fb, boxA, b, m0, k0);
-                    if (b < boxB.nbox) {
+                    if (do_b && b < boxB.nbox) {
                         const int x = boxB.mn_major ? n0 + b * boxB.step : k0 + b * boxB.step;
                         const int y = boxB.mn_major ? k0 : n0;
                         tma_load_2d_mcast2(sB + b_own + static_cast<uint32_t>(b) * boxB.smem_step, mB, fb, x, y);
@@ -665,43 +680,48 @@ __device__ ProducerTail role_producer(const KParams &p, const CUtensorMap *tmA, 
                 }
             } else if (hints) {
                 for (int b = 0; b < nbox; ++b) {
-                    if (b < boxA.nbox)
+                    if (do_a && b < boxA.nbox)
                         issue_box_hint<CG>(mA, sA, fb, boxA, b, m0, k0, keep);
-                    if (b < boxB.nbox)
+                    if (do_b && b < boxB.nbox)
                         issue_box_hint<CG>(mB, sB, fb, boxB, b, n0, k0, keep);
                 }
             } else {
                 for (int b = 0; b < nbox; ++b) {
-                    if (b < boxA.nbox)
+                    if (do_a && b < boxA.nbox)
                         issue_box<CG>(mA, sA, fb, boxA, b, m0, k0);
-                    if (b < boxB.nbox)
+                    if (do_b && b < boxB.nbox)
                         issue_box<CG>(mB, sB, fb, boxB, b, n0, k0);
                 }
             }
             if constexpr (SF) {
-                // the scale atoms of this K range: this CTA's A rows, and every B
-                // column of the tile (the pair's MMA reads all of them from each
-                // CTA). The scale tensors are viewed as rows of 256 bytes, atom a
-                // being rows 2a and 2a + 1; a row block's atoms of consecutive K
-                // groups are adjacent, so one box of 2 x KGROUPS rows brings all
-                // of a stage's atoms of one row block. Atoms past the last K group
-                // (the tail of the last stage: the next row block's, or TMA's zero
-                // fill past the end) multiply only the zeros TMA fills in for K.
-                // Pair CTAs signal the even CTA's barrier like the operand boxes.
+                // the scale atoms of this K range: this CTA's A rows (with the A
+                // boxes), and every B column of the tile (with the B boxes; the
+                // pair's MMA reads all of them from each CTA). The scale tensors
+                // are viewed as rows of 256 bytes, atom a being rows 2a and 2a + 1;
+                // a row block's atoms of consecutive K groups are adjacent, so one
+                // box of 2 x KGROUPS rows brings all of a stage's atoms of one row
+                // block. Atoms past the last K group (the tail of the last stage:
+                // the next row block's, or TMA's zero fill past the end) multiply
+                // only the zeros TMA fills in for K. Pair CTAs signal the even
+                // CTA's barrier like the operand boxes.
                 const uint32_t sSF = sA + C::SF_OFF;
                 const int g0 = k0 / sf_atom_kbytes(SF);
                 const int ra = m0 / 128, rb = ti.n_blk * BN / 128;
-                if constexpr (CG == 1)
-                    tma_load_2d(sSF, tmSFA, fb, 0, 2 * (ra * sf_groups + g0));
-                else
-                    tma_load_2d_pair(sSF, tmSFA, fb, 0, 2 * (ra * sf_groups + g0));
-#pragma unroll
-                for (int h = 0; h < BN / 128; ++h) {
-                    const uint32_t dst = sSF + C::SF_A_BYTES + 512 * C::KGROUPS * h;
+                if (do_a) {
                     if constexpr (CG == 1)
-                        tma_load_2d(dst, tmSFB, fb, 0, 2 * ((rb + h) * sf_groups + g0));
+                        tma_load_2d(sSF, tmSFA, fb, 0, 2 * (ra * sf_groups + g0));
                     else
-                        tma_load_2d_pair(dst, tmSFB, fb, 0, 2 * ((rb + h) * sf_groups + g0));
+                        tma_load_2d_pair(sSF, tmSFA, fb, 0, 2 * (ra * sf_groups + g0));
+                }
+                if (do_b) {
+#pragma unroll
+                    for (int h = 0; h < BN / 128; ++h) {
+                        const uint32_t dst = sSF + C::SF_A_BYTES + 512 * C::KGROUPS * h;
+                        if constexpr (CG == 1)
+                            tma_load_2d(dst, tmSFB, fb, 0, 2 * ((rb + h) * sf_groups + g0));
+                        else
+                            tma_load_2d_pair(dst, tmSFB, fb, 0, 2 * ((rb + h) * sf_groups + g0));
+                    }
                 }
             }
             ++issued;
@@ -711,7 +731,7 @@ __device__ ProducerTail role_producer(const KParams &p, const CUtensorMap *tmA, 
             }
         }
     }
-    if (stats) {
+    if (stats && part != 2) {
         stats[blockIdx.x * kStatSlots + kStatProducerWaitCycles] = st_wait;
         stats[blockIdx.x * kStatSlots + kStatProducerBlocked] = st_blocked;
     }
@@ -1517,9 +1537,10 @@ __global__ void __launch_bounds__(Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, MODE>:
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + C::MISC_OFF + 4);
 
+    const bool split = C::HAS_LOADB && (p.flags & kFlagSplitLoad) != 0;
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_full + 8 * s, split ? 2 : 1);  // split loads: both producer warps arm it
             mbar_init(bar_empty + 8 * s, C::MCB ? 2 : 1);  // B multicast: both CTAs' MMAs release it
         }
         for (int b = 0; b < 2; ++b) {
@@ -1567,7 +1588,11 @@ __global__ void __launch_bounds__(Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, MODE>:
     if (warp == 0) {
         if (lane == 0)
             tail = role_producer<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, MODE>(
-                p, &tmA, &tmB, &tmSFA, &tmSFB, stage_base, bar_full, bar_empty, bar_inject, rank, w);
+                p, &tmA, &tmB, &tmSFA, &tmSFB, stage_base, bar_full, bar_empty, bar_inject, rank, w, split ? 1 : 0);
+    } else if (warp == C::LOADB_WARP) {
+        if (lane == 0 && split)
+            tail = role_producer<CG, BN, BK, STAGES, GROUPED, ESIZE, BMT, SF, MODE>(
+                p, &tmA, &tmB, &tmSFA, &tmSFB, stage_base, bar_full, bar_empty, bar_inject, rank, w, 2);
     } else if (warp == 1) {
         // CTA pairs: the even CTA issues the pair's MMAs; every other CTA its own
         if (lane == 0 && (CG == 1 || rank == 0)) {
@@ -1606,7 +1631,7 @@ __global__ void __launch_bounds__(Cfg<CG, BN, BK, STAGES, ESIZE, BMT, SF, MODE>:
         // the producer's loads in flight (this CTA's full barriers; for a pair
         // the even CTA's, which count both CTAs' bytes) and for the scale
         // copiers' tcgen05.cp, each with a bound, before TMEM is freed.
-        if (warp == 0 && lane == 0 && (CG == 1 || rank == 0))
+        if ((warp == 0 || warp == C::LOADB_WARP) && lane == 0 && (CG == 1 || rank == 0))
             drain_producer_tail<STAGES>(tail, bar_full, w);
         if constexpr (C::SF_COPIERS > 0)
             if (warp == kSfCopyWarp && lane == 0 && rank == 0)
