@@ -93,7 +93,12 @@ typedef enum {
  *                 "06 Blackwell Tensor Core - tcgen05 MMA", cta_group::1
  *                 M = 64; default for M <= 64 with 16-bit operands), or 32
  *                 (the weight-stationary tcgen05.mma.ws with M = 32; 16-bit
- *                 operands, single problems, tile_n 256).
+ *                 operands, single problems, tile_n 256), or 256
+ *                 (cta_group::1 only: two M = 128 MMAs per K slice share
+ *                 each B slice, their accumulators filling the 512 TMEM
+ *                 columns; 16-bit operands, single problems, tile_n 256,
+ *                 swizzled operand layouts; the epilogue of a tile does not
+ *                 overlap the next tile's MMAs).
  *   tile_n        MMA N per tile: 64, 128 or 256 (cta_group::2: 128 or 256).
  *   block_k       K elements per pipeline stage: 32, 64 or 128 where built.
  *   swizzle_a/b   operand swizzle (gemm_swizzle_t).
@@ -196,7 +201,8 @@ typedef struct {
 } gemm_options_t;
 
 /* Bytes of stream-K workspace for any single GEMM on the current device:
- * one 4 x uint32 flag row and one 128 x 256 fp32 partial-sum slot per SM.
+ * one 4 x uint32 flag row and one 256 x 256 fp32 partial-sum slot per SM
+ * (the largest tile; 128-row tiles use half of each slot).
  * 0 if the device cannot be queried. */
 size_t gemm_streamk_workspace_size(void);
 

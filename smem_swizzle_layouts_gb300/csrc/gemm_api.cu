@@ -297,19 +297,21 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
     if (opt.workspace && (reinterpret_cast<uintptr_t>(opt.workspace) & 255u) != 0)
         return GEMM_ERR_ALIGNMENT;
 
-    if (opt.tile_m != 0 && opt.tile_m != 32 && opt.tile_m != 64 && opt.tile_m != 128)
+    if (opt.tile_m != 0 && opt.tile_m != 32 && opt.tile_m != 64 && opt.tile_m != 128 && opt.tile_m != 256)
         return GEMM_ERR_INVALID_ARG;
     int cg = opt.cta_group;
-    if ((opt.tile_m == 64 || opt.tile_m == 32) && cg == 2)
+    if ((opt.tile_m == 64 || opt.tile_m == 32 || opt.tile_m == 256) && cg == 2)
         return GEMM_ERR_UNSUPPORTED;
-    if (opt.tile_m == 64 || opt.tile_m == 32)
+    if (opt.tile_m == 64 || opt.tile_m == 32 || opt.tile_m == 256)
         cg = 1;
     if (cg == 0) {
         // CTA pairs for large problems: each SM then loads half of B.
         cg = (!grouped && M >= 2048 && N >= 2048) ? 2 : 1;
     }
     int bn = opt.tile_n;
-    if (bn == 0) {
+    if (bn == 0 && opt.tile_m == 256) {
+        bn = 256;  // the only width two-half tiles are built for
+    } else if (bn == 0) {
         if (cg == 2) {
             bn = N <= 128 ? 128 : 256;
         } else {
@@ -343,6 +345,20 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
                         : (cg == 1 && M <= 64 && esize == 2 && !grouped && bn >= 128 ? 64 : 128);
     if (bm == 64 && opt.block_k == 0)
         bk = bn == 256 ? 64 : 128;
+    // Two-half tiles (256 rows on one CTA: two M = 128 MMAs per B slice, half
+    // the operand bytes per flop of a 128 x 256 tile) for large single-CTA
+    // 16-bit problems with long K. Measured, TFLOP/s, 128 x 256 (B multicast
+    // where that is the default) -> 256 x 256: 8192^3 1666 -> 1843, 8192^3
+    // MN-major 1482 -> 1697, 6144^3 1580 -> 1699, 3072^2 x 8192 1283 -> 1390,
+    // 4096^3 1360 -> 1389, 4096^3 K/MN 1258 -> 1307; K = 2048 (8192^2) 1423 ->
+    // 1344, where the epilogue, which no longer overlaps, weighs more.
+    if (opt.tile_m == 0 && cg == 1 && esize == 2 && !grouped && sf == kScaleNone && bm == 128 &&
+        (opt.tile_n == 0 || opt.tile_n == 256) && (opt.block_k == 0 || opt.block_k == 64) && opt.mma_ws != 1 &&
+        opt.multicast_b != 1 && M >= 2048 && N >= 2048 && K >= 4096 && find_variant(1, 256, 64, false, 2, 256)) {
+        bm = 256;
+        bn = 256;
+        bk = 64;
+    }
     // Weight-stationary tiles (tcgen05.mma.ws): 32 rows (M = 32 exists only in
     // the .ws form) when asked for, or 64 rows; single CTAs, 16-bit operands,
     // single problems. 32-row tiles are 256 wide so that each epilogue warp
@@ -353,7 +369,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
     int ws = 0;
     const bool ws_default = opt.mma_ws == 0 && opt.tile_m == 0 && bm == 64 && bn == 128;
     if (opt.tile_m == 32 || opt.mma_ws == 1 || ws_default) {
-        if (opt.mma_ws == -1 || opt.tile_m == 128 || sf != kScaleNone || esize != 2 || grouped || cg != 1)
+        if (opt.mma_ws == -1 || opt.tile_m >= 128 || sf != kScaleNone || esize != 2 || grouped || cg != 1)
             return GEMM_ERR_UNSUPPORTED;
         ws = 1;
         bm = opt.tile_m ? opt.tile_m : 64;
@@ -463,7 +479,12 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
 // Stream-K workspace: a row of 4 flags per CTA, then one 128 x BN fp32 slot per CTA.
 size_t sk_flag_bytes(int ctas) { return (static_cast<size_t>(ctas) * 4 * sizeof(uint32_t) + 1023) & ~size_t(1023); }
 
-size_t sk_bytes(int ctas, int bn) { return sk_flag_bytes(ctas) + static_cast<size_t>(ctas) * 128 * bn * sizeof(float); }
+// flags, then one rows x bn fp32 partial-sum slot per CTA (rows 128, or 256
+// for two-half tiles)
+size_t sk_bytes(int ctas, int bn, int rows)
+{
+    return sk_flag_bytes(ctas) + static_cast<size_t>(ctas) * rows * bn * sizeof(float);
+}
 
 // Stream-K split of `tiles` tiles of `kbt` K blocks over `clusters` clusters:
 // the number of tiles that stay data-parallel, or -1 for no split.
@@ -587,7 +608,8 @@ gemm_status_t run_single(const InFmt &f, int64_t M, int64_t N, int64_t K, const 
     Variant *v = find_variant(pl.cg, pl.bn, pl.bk, false, f.esize, pl.bm, f.sf,
                               pl.ws ? kModeWs : pl.mcb ? kModeMcastB : kModeOrdinary);
     const int ccta = cluster_ctas(pl);
-    const int epi_rows = pl.ws ? 32 : pl.bm / 4;  // output rows one epilogue warp stores per chunk
+    // output rows one epilogue warp stores per chunk (two-half tiles: per half)
+    const int epi_rows = (pl.ws || pl.bm == 256) ? 32 : pl.bm / 4;
 
     LaunchArgs la;
     std::memset(&la, 0, sizeof(la));
@@ -628,14 +650,19 @@ gemm_status_t run_single(const InFmt &f, int64_t M, int64_t N, int64_t K, const 
         p.sf_groups = static_cast<int>((K + sf_atom_kbytes(f.sf) - 1) / sf_atom_kbytes(f.sf));
     }
     la.grid = grid_for(pl, *v, dev, sms, tiles);
-    // stream-K needs a spare accumulator buffer: not for block-scaled 256-wide tiles
-    if (pl.workspace && pl.bm == 128 && K > 0 && !(f.sf != kScaleNone && pl.bn == 256)) {
+    // stream-K: 128-row tiles gather partial sums in a spare accumulator buffer
+    // (none for block-scaled 256-wide tiles); two-half tiles add them per chunk
+    if (pl.workspace && (pl.bm == 128 || pl.bm == 256) && K > 0 && !(f.sf != kScaleNone && pl.bn == 256)) {
         // stream-K runs on every resident cluster
         const int full = grid_for(pl, *v, dev, sms, static_cast<int64_t>(1) << 40);
         const int64_t kbt = (K + pl.bk - 1) / pl.bk;
-        const int64_t dp = sk_split(pl.stream_k, tiles, full / ccta, kbt);
+        // two-half tiles add the partial sums in the head's epilogue, chunk by
+        // chunk: measured slower than the unsplit launch (4096^3 105 against
+        // 97 us, 6144^3 308 against 266 us), so only an explicit mode splits them
+        const int mode = (pl.bm == 256 && pl.stream_k == 0) ? -1 : pl.stream_k;
+        const int64_t dp = sk_split(mode, tiles, full / ccta, kbt);
         if (dp >= 0) {
-            if (pl.workspace_bytes < sk_bytes(full, pl.bn))
+            if (pl.workspace_bytes < sk_bytes(full, pl.bn, pl.bm == 256 ? 256 : 128))
                 return GEMM_ERR_INVALID_ARG;
             uint32_t epoch = g_sk_epoch.fetch_add(1) + 1;
             if (epoch == 0)
@@ -1052,7 +1079,7 @@ size_t gemm_streamk_workspace_size(void)
     unsigned int *status = nullptr;
     if (device_state(&dev, &status, &sms) != GEMM_OK || sms <= 0)
         return 0;
-    return sk_bytes(sms, 256);
+    return sk_bytes(sms, 256, 256);
 }
 
 size_t gemm_grouped_workspace_size(int num_problems)

@@ -235,7 +235,11 @@ struct Cfg {
     // Accumulator buffers: two (the epilogue of one tile overlaps the next
     // tile's MMAs), except for block-scaled 256-wide tiles, whose two
     // accumulators would leave no TMEM for the scale slots
-    static constexpr int ACC_BUFS = (SF && BN == 256) ? 1 : 2;
+    // Two-half tiles (BMT 256, single CTAs): two 128-row accumulators side by
+    // side fill the TMEM columns, so they have one buffer and the epilogue of a
+    // tile does not overlap the next tile's MMAs
+    static constexpr int M_HALVES = BMT == 256 ? 2 : 1;
+    static constexpr int ACC_BUFS = ((SF && BN == 256) || M_HALVES == 2) ? 1 : 2;
     static constexpr int SF_COL0 = ACC_BUFS * BN;
     static constexpr int SF_GROUP_COLS = 4 + 4 * (BN / 128);  // A atom, then the B atoms of one K group
     static constexpr int SF_COLS = SF_GROUP_COLS * KGROUPS;
@@ -248,7 +252,7 @@ struct Cfg {
     static constexpr int COL_PARTS = WS ? 4 / WS_ROW_BLOCKS : 1;
     static constexpr int ACC_COLS = BN / COL_PARTS;
     static constexpr int TMEM_COLS = WS ? (2 * ACC_COLS < 32 ? 32 : 2 * ACC_COLS) : BMT == 64 ? BN : SF ? 512 : 2 * BN;
-    static constexpr int UMMA_M = BM * CG;
+    static constexpr int UMMA_M = BM / M_HALVES * CG;
     // CTAs per cluster (CTA pairs, or the two CTAs sharing B by multicast) and
     // the output rows of one cluster tile; B rows/atoms one CTA's TMA loads
     static constexpr int CLUSTER = (CG == 2 || MCB) ? 2 : 1;
@@ -256,8 +260,11 @@ struct Cfg {
     static constexpr int B_LOAD = MCB ? BN / 2 : BN_LOCAL;
     static_assert(!MCB || (CG == 1 && BMT == 128 && SF == 0 && BN % 128 == 0),
                   "B multicast: two single-CTA 128-row tiles sharing a B panel split in halves");
-    static constexpr int EPI_ROWS = WS ? 32 : BM / 4;    // output rows per epilogue warp
-    static_assert(BMT == 128 || (BMT == 64 && CG == 1) || (BMT == 32 && WS), "64-row tiles are single-CTA");
+    static constexpr int EPI_ROWS = (WS || M_HALVES == 2) ? 32 : BM / 4;  // output rows per epilogue warp (and half)
+    static_assert(BMT == 128 || BMT == 256 || (BMT == 64 && CG == 1) || (BMT == 32 && WS),
+                  "64-row tiles are single-CTA");
+    static_assert(M_HALVES == 1 || (CG == 1 && !WS && !MCB && SF == 0 && BN * M_HALVES <= 512),
+                  "two-half tiles: single CTAs, ordinary kind::f16/f8f6f4 MMAs, both accumulators in TMEM");
     static_assert(!WS || ((BMT == 32 || BMT == 64) && CG == 1 && ESIZE == 2 && SF == 0 && (BN / COL_PARTS) % 64 == 0),
                   ".ws tiles: 32 or 64 rows, single CTA, 16-bit operands, whole 64-column chunks per warp");
     static constexpr int KSLICES = BK * ESIZE / 32;  // MMAs per stage (32 bytes of K each)
@@ -852,6 +859,9 @@ __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uin
     const uint64_t a_desc0 = make_smem_desc(smem, pa.lbo, pa.sbo, pa.swz);
     const uint64_t b_desc0 = make_smem_desc(smem + C::A_BYTES, pb.lbo, pb.sbo, pb.swz);
     uint32_t a_off[C::KSLICES], b_off[C::KSLICES];
+    // two-half tiles: rows 128..255 of the A tile start 128 K-major rows (W
+    // bytes each) or 128 MN elements (BK rows of K per element) further on
+    const uint32_t a_half = C::M_HALVES == 2 ? (p.a_mn ? 128u * ESIZE * BK : 128u * swizzle_row_bytes(p.a_swz)) >> 4 : 0u;
 #pragma unroll
     for (int j = 0; j < C::KSLICES; ++j) {
         a_off[j] = slice_byte_offset(p.a_mn, p.a_swz, C::BM, j, ESIZE) >> 4;
@@ -927,15 +937,23 @@ __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uin
                     if constexpr (C::WS)
                         mma_ws_f16(d_tmem, a_desc0 + sdelta + a_off[j], b_desc0 + sdelta + b_off[j], idesc,
                                    ((kb - kb_lo) | j) != 0);
-                    else if constexpr (ESIZE == 2)
+                    else if constexpr (ESIZE == 2) {
                         mma_f16<CG>(d_tmem, a_desc0 + sdelta + a_off[j], b_desc0 + sdelta + b_off[j], idesc,
                                     ((kb - kb_lo) | j) != 0);
+                        if constexpr (C::M_HALVES == 2)  // the same B slice, rows 128..255 of A
+                            mma_f16<CG>(d_tmem + BN, a_desc0 + sdelta + a_off[j] + a_half, b_desc0 + sdelta + b_off[j],
+                                        idesc, ((kb - kb_lo) | j) != 0);
+                    }
                     else if constexpr (ESIZE == 4)
                         mma_tf32<CG>(d_tmem, a_desc0 + sdelta + a_off[j], b_desc0 + sdelta + b_off[j], idesc,
                                      ((kb - kb_lo) | j) != 0);
-                    else
+                    else {
                         mma_f8<CG>(d_tmem, a_desc0 + sdelta + a_off[j], b_desc0 + sdelta + b_off[j], idesc,
                                    ((kb - kb_lo) | j) != 0);
+                        if constexpr (C::M_HALVES == 2)
+                            mma_f8<CG>(d_tmem + BN, a_desc0 + sdelta + a_off[j] + a_half, b_desc0 + sdelta + b_off[j],
+                                       idesc, ((kb - kb_lo) | j) != 0);
+                    }
                 }
             }
             if constexpr (C::MCB)
@@ -1110,19 +1128,33 @@ __device__ __forceinline__ void epilogue_chunk_math(float (&acc)[CW], const EpiC
 // split tile `ua`, then writes the sum of their fp32 partial sums into TMEM
 // accumulator buffer `buf` (the first n32 32-column groups), the buffer the
 // head's own MMAs do not use. False if a flag did not come in time.
-template <int CL, int BN>
-__device__ bool sk_gather(const Sched &sched, const Unit &ua, int n32, int buf, uint32_t tmem_base, int q,
-                          int prow, const float4 *partials, const uint32_t *sk_flags, uint32_t epoch, int rank,
-                          int num_clusters, const Waiter &w, unsigned long long *st_wait)
+// The clusters that hold the rest of split tile `ua` (its head): [*lo, *hi];
+// a cluster whose share of the split iterations is empty holds nothing.
+__device__ __forceinline__ void sk_contributors(const Sched &sched, const Unit &ua, int num_clusters, int *lo, int *hi)
 {
-    const long long S = sched.sk_iters;
     const long long first = static_cast<long long>(ua.tile - sched.sk_dp) * sched.kbt;
-    const int c_lo = sk_owner(first + ua.kb1, S, num_clusters);
-    const int c_hi = sk_owner(first + sched.kbt - 1, S, num_clusters);
+    *lo = sk_owner(first + ua.kb1, sched.sk_iters, num_clusters);
+    *hi = sk_owner(first + sched.kbt - 1, sched.sk_iters, num_clusters);
+}
+
+__device__ __forceinline__ bool sk_share_empty(long long S, int cc, int num_clusters)
+{
+    return S * cc / num_clusters == S * (cc + 1) / num_clusters;
+}
+
+// Waits until every contributor of split tile `ua` has published the partial
+// sum of this warp's lane quarter (flag row of CTA cc * CL + rank, word q).
+template <int CL>
+__device__ bool sk_wait_contributors(const Sched &sched, const Unit &ua, int q, const uint32_t *sk_flags,
+                                     uint32_t epoch, int rank, int num_clusters, const Waiter &w,
+                                     unsigned long long *st_wait)
+{
+    int c_lo, c_hi;
+    sk_contributors(sched, ua, num_clusters, &c_lo, &c_hi);
     const long long t0 = st_wait ? clock64() : 0;
     bool ok = true;
     for (int cc = c_lo; cc <= c_hi && ok; ++cc) {
-        if (S * cc / num_clusters == S * (cc + 1) / num_clusters)
+        if (sk_share_empty(sched.sk_iters, cc, num_clusters))
             continue;  // empty share: nothing to wait for
         ok = w.wait_flag(sk_flags + (cc * CL + rank) * 4 + q, epoch, kRoleEpilogue | kWaitPartial);
     }
@@ -1130,6 +1162,19 @@ __device__ bool sk_gather(const Sched &sched, const Unit &ua, int n32, int buf, 
         return false;
     if (st_wait)
         *st_wait += static_cast<unsigned long long>(clock64() - t0);
+    return true;
+}
+
+template <int CL, int BN>
+__device__ bool sk_gather(const Sched &sched, const Unit &ua, int n32, int buf, uint32_t tmem_base, int q,
+                          int prow, const float4 *partials, const uint32_t *sk_flags, uint32_t epoch, int rank,
+                          int num_clusters, const Waiter &w, unsigned long long *st_wait)
+{
+    const long long S = sched.sk_iters;
+    if (!sk_wait_contributors<CL>(sched, ua, q, sk_flags, epoch, rank, num_clusters, w, st_wait))
+        return false;
+    int c_lo, c_hi;
+    sk_contributors(sched, ua, num_clusters, &c_lo, &c_hi);
     constexpr int kSlotVec = 128 * BN / 4;  // float4 per slot
     constexpr int kGroups = 2;              // 32-column groups per batch of loads
     const uint32_t tbase = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(buf * BN);
@@ -1142,7 +1187,7 @@ __device__ bool sk_gather(const Sched &sched, const Unit &ua, int n32, int buf, 
                 v[b][i] = 0.0f;
 #pragma unroll 1
         for (int cc = c_lo; cc <= c_hi; ++cc) {
-            if (S * cc / num_clusters == S * (cc + 1) / num_clusters)
+            if (sk_share_empty(S, cc, num_clusters))
                 continue;
             const float4 *slot = partials + static_cast<size_t>(cc * CL + rank) * kSlotVec + prow;
 #pragma unroll
@@ -1217,13 +1262,17 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
     long long t_last_acc = 0;
     const long long t_start = clock64();
     // stream-K: this CTA's partial-sum slot, and its row in every slot
-    constexpr bool kStreamK = C::BM == 128 && !GROUPED && C::ACC_BUFS == 2;  // the gather needs the spare buffer
+    // 128-row tiles gather partial sums into the spare accumulator buffer;
+    // two-half tiles (no spare buffer) add them from the workspace per chunk
+    constexpr bool kStreamK = !GROUPED && ((C::BM == 128 && C::ACC_BUFS == 2) || C::M_HALVES == 2);
     const bool split = kStreamK && sched.sk_iters > 0;
     float4 *const partials = reinterpret_cast<float4 *>(p.sk_partials);
     uint32_t *const sk_flags = p.sk_flags;
     const uint32_t epoch = p.sk_epoch;
     const int prow = R * q + lane;
-    constexpr int kSlotVec = 128 * BN / 4;  // float4 per slot
+    constexpr int kSlotRows = 128 * C::M_HALVES;   // rows of a partial-sum slot
+    constexpr int kSlotVec = kSlotRows * BN / 4;   // float4 per slot
+    int sk_lo = 0, sk_hi = -1;                     // a two-half head's contributors
     UnitIter units(sched, cluster_id, num_clusters);
     Unit u;
     while (units.next(u)) {
@@ -1237,9 +1286,16 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
         if (head) {
             const int n_cols = min(BN, ti.N - ti.n_blk * BN);
             const long long t0 = stats ? clock64() : 0;
-            const bool ok = sk_gather<C::CLUSTER, BN>(sched, u, (n_cols + 31) / 32, acc ^ 1, tmem_base, q, prow, partials,
-                                              sk_flags, epoch, static_cast<int>(rank), num_clusters, w,
-                                              stats ? &st_pw : nullptr);
+            bool ok;
+            if constexpr (C::M_HALVES == 2) {
+                ok = sk_wait_contributors<C::CLUSTER>(sched, u, q, sk_flags, epoch, static_cast<int>(rank),
+                                                      num_clusters, w, stats ? &st_pw : nullptr);
+                sk_contributors(sched, u, num_clusters, &sk_lo, &sk_hi);
+            } else {
+                ok = sk_gather<C::CLUSTER, BN>(sched, u, (n_cols + 31) / 32, acc ^ 1, tmem_base, q, prow, partials,
+                                               sk_flags, epoch, static_cast<int>(rank), num_clusters, w,
+                                               stats ? &st_pw : nullptr);
+            }
             if (stats)
                 st_pe += static_cast<unsigned long long>(clock64() - t0);
             if (!ok)
@@ -1257,8 +1313,8 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
         // 128-row and .ws tiles: thread t holds row t of the warp's rows. 64-row
         // tiles (Layout F): the accumulator with lane alignment 16*acc sits in
         // threads 16*acc..+15.
-        const bool active = C::WS || C::BM == 128 || (lane >> 4) == acc;
-        const int trow = (C::WS || C::BM == 128) ? lane : (lane & 15);
+        const bool active = C::WS || C::BM >= 128 || (lane >> 4) == acc;
+        const int trow = (C::WS || C::BM >= 128) ? lane : (lane & 15);
         if (has_acc) {
             const long long tw = stats ? clock64() : 0;
             bool ok = w.wait(bar_acc_full + 8 * acc, acc_phase, kRoleEpilogue | kWaitAccFull, rank != 0);
@@ -1277,21 +1333,23 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
             // laid out [column / 4][row][4] so that a warp writes 512
             // contiguous bytes per store
             float4 *const slot = partials + static_cast<size_t>(blockIdx.x) * kSlotVec;
-            for (int c = 0; c < BN / CW; ++c) {
-                if (ti.n_blk * BN + c * CW >= ti.N)
-                    break;
-                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
-                                       static_cast<uint32_t>(acc * BN + c * CW);
-                uint32_t r[32];
+            for (int half = 0; half < C::M_HALVES; ++half) {
+                for (int c = 0; c < BN / CW; ++c) {
+                    if (ti.n_blk * BN + c * CW >= ti.N)
+                        break;
+                    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
+                                           static_cast<uint32_t>((C::M_HALVES == 2 ? half : acc) * BN + c * CW);
+                    uint32_t r[32];
 #pragma unroll
-                for (int h = 0; h < CW / 32; ++h) {
-                    tmem_ld_32x32b_x32(taddr + 32 * h, r);
-                    tmem_ld_wait();
+                    for (int h = 0; h < CW / 32; ++h) {
+                        tmem_ld_32x32b_x32(taddr + 32 * h, r);
+                        tmem_ld_wait();
 #pragma unroll
-                    for (int g = 0; g < 8; ++g)
-                        __stcg(slot + (c * (CW / 4) + h * 8 + g) * 128 + prow,
-                               make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
-                                           __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3])));
+                        for (int g = 0; g < 8; ++g)
+                            __stcg(slot + (c * (CW / 4) + h * 8 + g) * kSlotRows + 128 * half + prow,
+                                   make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
+                                               __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3])));
+                    }
                 }
             }
             tc_fence_before_sync();
@@ -1380,93 +1438,119 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
                 continue;
             }
         }
-        for (int c = c_lo; c < c_hi; ++c) {
-            const int col0 = ti.n_blk * BN + c * CW;
-            if (col0 >= ti.N)
-                break;
-            const uint32_t sbuf = buf0 + static_cast<uint32_t>(sel * kEpiBufBytes);
-            const uint32_t sbar = ebar0 + static_cast<uint32_t>(8 * sel);
-            // the store issued from this buffer (EPI_BUFS chunks ago) must have read it
-            if (lane == 0)
-                bulk_wait_group_read<C::EPI_BUFS - 1>();
-            __syncwarp();
-            uint32_t creg[32];
-            if (direct_c)  // issued before the TMEM load so that the two overlap
-                load_c_row<CW>(creg, c_ptr, ldc, m0 + trow, col0, ti.M, ti.N);
-            if (use_c && !direct_c && lane == 0) {
-                fence_proxy_async_smem();
-                mbar_arrive_expect_tx(sbar, R * 128);
-                if (hints)
-                    tma_load_2d_hint(sbuf, mC, sbar, col0, m0, stream_once);
-                else
-                    tma_load_2d(sbuf, mC, sbar, col0, m0);
-            }
-            __syncwarp();  // tcgen05.ld is .sync.aligned: the warp must be converged
-            float v[CW];
-            if (has_acc) {
-                const uint32_t col = static_cast<uint32_t>(C::WS ? acc * C::ACC_COLS + (c - c_lo) * CW
-                                                              : (C::BM == 128 ? acc * BN : 0) + c * CW);
-                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + col;
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(taddr, r);
-                if constexpr (CW == 64) {
-                    uint32_t r2[32];
-                    tmem_ld_32x32b_x32(taddr + 32, r2);
-                    tmem_ld_wait();
+        // two-half tiles store the rows of one half after the other (row
+        // offset 128 h, accumulator columns from h BN); other tiles have one
+        for (int half = 0; half < C::M_HALVES; ++half) {
+            for (int c = c_lo; c < c_hi; ++c) {
+                const int col0 = ti.n_blk * BN + c * CW;
+                if (col0 >= ti.N)
+                    break;
+                const int m0h = m0 + 128 * half;
+                const uint32_t sbuf = buf0 + static_cast<uint32_t>(sel * kEpiBufBytes);
+                const uint32_t sbar = ebar0 + static_cast<uint32_t>(8 * sel);
+                // the store issued from this buffer (EPI_BUFS chunks ago) must have read it
+                if (lane == 0)
+                    bulk_wait_group_read<C::EPI_BUFS - 1>();
+                __syncwarp();
+                uint32_t creg[32];
+                if (direct_c)  // issued before the TMEM load so that the two overlap
+                    load_c_row<CW>(creg, c_ptr, ldc, m0h + trow, col0, ti.M, ti.N);
+                if (use_c && !direct_c && lane == 0) {
+                    fence_proxy_async_smem();
+                    mbar_arrive_expect_tx(sbar, R * 128);
+                    if (hints)
+                        tma_load_2d_hint(sbuf, mC, sbar, col0, m0h, stream_once);
+                    else
+                        tma_load_2d(sbuf, mC, sbar, col0, m0h);
+                }
+                __syncwarp();  // tcgen05.ld is .sync.aligned: the warp must be converged
+                float v[CW];
+                if (has_acc) {
+                    const uint32_t col = static_cast<uint32_t>(
+                        C::WS ? acc * C::ACC_COLS + (c - c_lo) * CW
+                              : (C::BM == 128 ? acc * BN : C::M_HALVES == 2 ? half * BN : 0) + c * CW);
+                    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + col;
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(taddr, r);
+                    if constexpr (CW == 64) {
+                        uint32_t r2[32];
+                        tmem_ld_32x32b_x32(taddr + 32, r2);
+                        tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        v[i] = __uint_as_float(r[i]);
-                        v[32 + i] = __uint_as_float(r2[i]);
+                        for (int i = 0; i < 32; ++i) {
+                            v[i] = __uint_as_float(r[i]);
+                            v[32 + i] = __uint_as_float(r2[i]);
+                        }
+                    } else {
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            v[i] = __uint_as_float(r[i]);
                     }
                 } else {
-                    tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        v[i] = __uint_as_float(r[i]);
+                    for (int i = 0; i < CW; ++i)
+                        v[i] = 0.0f;
                 }
-            } else {
+                if (head && C::M_HALVES == 2) {
+                    // the contributors' partial sums of this chunk, from their slots
+#pragma unroll 1
+                    for (int cc = sk_lo; cc <= sk_hi; ++cc) {
+                        if (sk_share_empty(sched.sk_iters, cc, num_clusters))
+                            continue;
+                        const float4 *slot = partials + static_cast<size_t>(cc * C::CLUSTER + rank) * kSlotVec +
+                                             128 * half + prow;
+                        float4 x[CW / 4];
 #pragma unroll
-                for (int i = 0; i < CW; ++i)
-                    v[i] = 0.0f;
-            }
-            if (head) {
-                // the contributors' partial sums, gathered into the other buffer
-                const uint32_t paddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
-                                       static_cast<uint32_t>((acc ^ 1) * BN + c * CW);
+                        for (int g = 0; g < CW / 4; ++g)
+                            x[g] = __ldcg(slot + (c * (CW / 4) + g) * kSlotRows);
 #pragma unroll
-                for (int h = 0; h < CW / 32; ++h) {
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(paddr + 32 * h, r);
-                    tmem_ld_wait();
+                        for (int g = 0; g < CW / 4; ++g) {
+                            v[4 * g] += x[g].x;
+                            v[4 * g + 1] += x[g].y;
+                            v[4 * g + 2] += x[g].z;
+                            v[4 * g + 3] += x[g].w;
+                        }
+                    }
+                } else if (head) {
+                    // the contributors' partial sums, gathered into the other buffer
+                    const uint32_t paddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
+                                           static_cast<uint32_t>((acc ^ 1) * BN + c * CW);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        v[32 * h + i] += __uint_as_float(r[i]);
+                    for (int h = 0; h < CW / 32; ++h) {
+                        uint32_t r[32];
+                        tmem_ld_32x32b_x32(paddr + 32 * h, r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            v[32 * h + i] += __uint_as_float(r[i]);
+                    }
                 }
+                if (use_c && !direct_c) {
+                    const long long tw = stats ? clock64() : 0;
+                    bool ok = w.wait(sbar, epi_phase[sel], kRoleEpilogue | kWaitEpiC);
+                    if (stats)
+                        st_cw += static_cast<unsigned long long>(clock64() - tw);
+                    epi_phase[sel] ^= 1u;
+                    if (!__all_sync(0xffffffffu, ok))
+                        return;
+                }
+                if (direct_c)
+                    epilogue_chunk_math<CW, true>(v, ec, sbuf, trow, true, creg);
+                else if (active)
+                    epilogue_chunk_math<CW>(v, ec, sbuf, trow, use_c);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if (hints)
+                        tma_store_2d_hint(mD, sbuf, col0, m0h, stream_once);
+                    else
+                        tma_store_2d(mD, sbuf, col0, m0h);
+                    bulk_commit_group();
+                }
+                if constexpr (C::EPI_BUFS == 2)
+                    sel ^= 1;
             }
-            if (use_c && !direct_c) {
-                const long long tw = stats ? clock64() : 0;
-                bool ok = w.wait(sbar, epi_phase[sel], kRoleEpilogue | kWaitEpiC);
-                if (stats)
-                    st_cw += static_cast<unsigned long long>(clock64() - tw);
-                epi_phase[sel] ^= 1u;
-                if (!__all_sync(0xffffffffu, ok))
-                    return;
-            }
-            if (direct_c)
-                epilogue_chunk_math<CW, true>(v, ec, sbuf, trow, true, creg);
-            else if (active)
-                epilogue_chunk_math<CW>(v, ec, sbuf, trow, use_c);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                if (hints)
-                    tma_store_2d_hint(mD, sbuf, col0, m0, stream_once);
-                else
-                    tma_store_2d(mD, sbuf, col0, m0);
-                bulk_commit_group();
-            }
-            if constexpr (C::EPI_BUFS == 2)
-                sel ^= 1;
         }
         if (has_acc) {
             // all tcgen05.ld of this accumulator have completed (wait::ld above)

@@ -17,7 +17,7 @@ cudaError_t resident_ctas(int *ctas);
 // BN is the MMA N of one tile, BK counts elements; stages fill ~192 KB of
 // shared memory next to 32 KB of epilogue staging. Element bytes 2 =
 // fp16/bf16, 1 = fp8, 4 = fp32 words read as TF32. Tile rows 128, or 64 for single-CTA M=64 MMAs (TMEM
-// Layout F). Scale kind 0 = none; 1 = MXFP8 (fp8, one E8M0 scale per 32
+// Layout F), or 256 for single CTAs that issue two 128-row MMAs per K slice on one B slice. Scale kind 0 = none; 1 = MXFP8 (fp8, one E8M0 scale per 32
 // elements of K for each row of A and column of B, kind::mxf8f6f4); 2 = NVFP4
 // (packed E2M1, one UE4M3 scale per 16, kind::mxf4nvf4); 3 = MXFP4 (packed
 // E2M1, one E8M0 per 32, kind::mxf4). fp4 tiles count BK in bytes; the scale
@@ -58,6 +58,7 @@ cudaError_t resident_ctas(int *ctas);
     X(1, 128, 64, 3, false, 4, 128, 0, 0) \
     X(2, 256, 64, 3, false, 4, 128, 0, 0) \
     X(1, 256, 64, 4, false, 2, 128, 0, 2) \
-    X(1, 256, 128, 4, false, 1, 128, 0, 2)
+    X(1, 256, 128, 4, false, 1, 128, 0, 2) \
+    X(1, 256, 64, 3, false, 2, 256, 0, 0)
 
 }  // namespace g300

@@ -36,7 +36,7 @@ def test_pairs_only_from_2048_rows_and_columns(g):
 
 
 def test_single_cta_256_wide_tiles_keep_four_stages_of_64(g):
-    p = plan(g, 4096, 4096, 4096, cta_group=1, tile_n=256)
+    p = plan(g, 4096, 4096, 4096, cta_group=1, tile_n=256, tile_m=128)
     assert (p["tile_n"], p["block_k"], p["swizzle_a"]) == (256, 64, 3)
 
 
@@ -107,7 +107,8 @@ def test_invalid_options_are_rejected(g):
     for opts, status in [(dict(flags=64), g.ERR_INVALID_ARG), (dict(stream_k=4), g.ERR_INVALID_ARG),
                          (dict(swizzle_a=6), g.ERR_INVALID_ARG), (dict(tile_m=96), g.ERR_INVALID_ARG),
                          (dict(workspace=0x1010), g.ERR_ALIGNMENT), (dict(tile_n=96), g.ERR_UNSUPPORTED),
-                         (dict(mma_ws=2), g.ERR_INVALID_ARG), (dict(tile_m=16), g.ERR_INVALID_ARG)]:
+                         (dict(mma_ws=2), g.ERR_INVALID_ARG), (dict(tile_m=16), g.ERR_INVALID_ARG),
+                         (dict(tile_m=512), g.ERR_INVALID_ARG)]:
         with pytest.raises(g.GemmError) as ei:
             plan(g, 1024, 1024, 1024, **opts)
         assert ei.value.status == status, opts
@@ -171,13 +172,38 @@ def test_b_multicast_clusters(g):
 
 def test_b_multicast_default_rule(g):
     # single-CTA 128 x 256 tiles share B by default when B is MN-major or A + B overflow L2
-    assert plan(g, 4096, 4096, 4096, cta_group=1, tile_n=256)["multicast_b"] == 0           # K/K, 64 MB
-    assert plan(g, 4096, 4096, 4096, b=MN_MAJOR, cta_group=1, tile_n=256)["multicast_b"] == 1
-    assert plan(g, 8192, 8192, 8192, cta_group=1, tile_n=256)["multicast_b"] == 1           # 256 MB
-    assert plan(g, 8192, 8192, 2048, cta_group=1, tile_n=256)["multicast_b"] == 0           # 64 MB
-    assert plan(g, 8192, 8192, 8192, cta_group=1, tile_n=256, multicast_b=-1)["multicast_b"] == 0
-    assert plan(g, 128, 8192, 8192, cta_group=1, tile_n=256)["multicast_b"] == 0            # one row tile
-    assert plan(g, 8192, 8192, 8192)["cta_group"] == 2                                     # pairs stay the default
+    one = dict(cta_group=1, tile_n=256, tile_m=128)
+    assert plan(g, 4096, 4096, 4096, **one)["multicast_b"] == 0           # K/K, 64 MB
+    assert plan(g, 4096, 4096, 4096, b=MN_MAJOR, **one)["multicast_b"] == 1
+    assert plan(g, 8192, 8192, 8192, **one)["multicast_b"] == 1           # 256 MB
+    assert plan(g, 8192, 8192, 2048, **one)["multicast_b"] == 0           # 64 MB
+    assert plan(g, 8192, 8192, 8192, multicast_b=-1, **one)["multicast_b"] == 0
+    assert plan(g, 128, 8192, 8192, **one)["multicast_b"] == 0            # one row tile
+    assert plan(g, 8192, 8192, 2048, b=MN_MAJOR, cta_group=1, tile_n=256)["multicast_b"] == 1  # short K: 128 rows
+    assert plan(g, 8192, 8192, 8192)["cta_group"] == 2                   # pairs stay the default
+
+
+def test_two_half_tiles_for_large_single_cta_problems_with_long_k(g):
+    # 256 rows on one CTA (two M = 128 MMAs per B slice, both accumulators in TMEM)
+    p = plan(g, 4096, 4096, 4096, cta_group=1, tile_n=256)
+    assert (p["tile_m"], p["tile_n"], p["block_k"], p["cta_group"], p["multicast_b"]) == (256, 256, 64, 1, 0)
+    assert plan(g, 8192, 8192, 8192, a=MN_MAJOR, b=MN_MAJOR, cta_group=1)["tile_m"] == 256
+    assert plan(g, 8192, 8192, 2048, cta_group=1)["tile_m"] == 128       # short K: the epilogue would weigh more
+    assert plan(g, 2047, 8192, 8192, cta_group=1)["tile_m"] == 128       # fewer than 2048 rows
+    assert plan(g, 8192, 8192, 8192, cta_group=1, tile_m=128)["tile_m"] == 128
+    assert plan(g, 8192, 8192, 8192, cta_group=1, tile_n=128)["tile_m"] == 128
+    assert plan(g, 8192, 8192, 8192, FP8, cta_group=1)["tile_m"] == 128  # 16-bit operands only
+    assert plan(g, 8192, 8192, 8192)["cta_group"] == 2                   # pairs stay the default
+    p = plan(g, 512, 512, 256, tile_m=256)
+    assert (p["tile_m"], p["tile_n"], p["cta_group"], p["block_k"]) == (256, 256, 1, 64)
+    for opts in (dict(tile_m=256, cta_group=2), dict(tile_m=256, tile_n=128), dict(tile_m=256, mma_ws=1),
+                 dict(tile_m=256, multicast_b=1)):
+        with pytest.raises(g.GemmError) as ei:
+            plan(g, 4096, 4096, 4096, **opts)
+        assert ei.value.status == g.ERR_UNSUPPORTED, opts
+    with pytest.raises(g.GemmError) as ei:
+        plan(g, 4096, 4096, 4096, FP8, tile_m=256)
+    assert ei.value.status == g.ERR_UNSUPPORTED
 
 
 def test_tf32_tiles_and_swizzles(g):
