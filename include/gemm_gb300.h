@@ -128,7 +128,11 @@ typedef enum {
  *                 the B boxes (and B scale atoms); NVFP4 kernels, which have
  *                 no room for the second warp, ignore it (ablation: no
  *                 measured effect, the loads are bound by L2 delivery, not
- *                 by the issuing thread).
+ *                 by the issuing thread). Bit 6 (single problems, 128- and
+ *                 256-row tiles) writes D from the epilogue's registers with
+ *                 16-byte stores, and reads C into them, instead of staging
+ *                 chunks in shared memory for TMA (ablation: equal or up to
+ *                 5 % slower at 4096^3 and 8192^3).
  *   stats         diagnostics: NULL, or device memory of 16 uint64 per CTA
  *                 of the grid (at least 16 * number of SMs), where each CTA
  *                 writes cycles its roles spent waiting (slots 0-1 producer,

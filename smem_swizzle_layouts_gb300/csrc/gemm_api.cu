@@ -290,7 +290,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
     if (opt.cta_group < 0 || opt.cta_group > 2 || opt.tile_n < 0 || opt.swizzle_a < 0 ||
         opt.swizzle_a > 5 || opt.swizzle_b < 0 || opt.swizzle_b > 5 || opt.max_ctas < 0 ||
         opt.group_m < 0 || opt.timeout_ms < 0 || opt.epilogue_swizzle < -1 ||
-        opt.epilogue_swizzle > 1 || opt.flags < 0 || opt.flags > 63 || opt.block_k < 0 ||
+        opt.epilogue_swizzle > 1 || opt.flags < 0 || opt.flags > 127 || opt.block_k < 0 ||
         opt.stream_k < -1 || opt.stream_k > 3 || opt.mma_ws < -1 || opt.mma_ws > 1 || opt.multicast_b < -1 ||
         opt.multicast_b > 1)
         return GEMM_ERR_INVALID_ARG;
@@ -642,6 +642,8 @@ gemm_status_t run_single(const InFmt &f, int64_t M, int64_t N, int64_t K, const 
     fill_common(p, pl, f, a_mn, b_mn, d_type, alpha, beta, status);
     p.c_ptr = beta != 0.0f ? C : nullptr;
     p.ldc = ldc;
+    p.d_ptr = D;
+    p.ldd = ldd;
     if (f.sf != kScaleNone && K > 0) {
         const int groups = pl.bk / sf_atom_kbytes(f.sf);  // atoms per stage and row block
         if ((s = encode_scales(&la.sfa, sfa, M, K, f.sf, groups)) != GEMM_OK ||

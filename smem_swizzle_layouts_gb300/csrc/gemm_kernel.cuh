@@ -106,12 +106,14 @@ struct KParams {
     // (sk_iters = (num_tiles - sk_dp_tiles) * kb_per_tile) are split evenly
     // across the clusters. A tile cut between clusters is finished by the one
     // holding its first K block (its head). The others leave their fp32
-    // partial sums in sk_partials (slot cluster * CG + rank, 128 x BN) and
+    // partial sums in sk_partials (slot cluster * CG + rank, 128 x BN, or
+    // 256 x BN for two-half tiles) and
     // raise their flags (sk_flags[(cluster * CG + rank) * 4 + warp] =
     // sk_epoch). A head is always its cluster's last unit, so the other TMEM
     // accumulator buffer is free while the head's MMAs run: the epilogue
     // warps gather the partial sums into it meanwhile and add both buffers
-    // in the head's epilogue.
+    // in the head's epilogue. Two-half tiles have no other buffer: their
+    // head adds the partial sums from the slots chunk by chunk.
     int sk_dp_tiles;
     int kb_per_tile;
     long long sk_iters;
@@ -121,10 +123,13 @@ struct KParams {
     // Block-scaled operands: K groups (128 elements) per row block of the
     // scale tensors; atom (i * sf_groups + g) holds row block i, K group g
     int sf_groups;
-    // C of a single problem (row-major, ldc elements per row), for the epilogue
-    // reading it straight into registers (kFlagDirectC)
+    // C and D of a single problem (row-major, ldc / ldd elements per row), for
+    // the epilogue reading C straight into registers (kFlagDirectC) and writing
+    // D straight from them (kFlagDirectD)
     const void *c_ptr;
     long long ldc;
+    void *d_ptr;
+    long long ldd;
 };
 
 // Diagnostics: per-CTA counters written when KParams::stats is set.
@@ -154,6 +159,7 @@ enum : int {
     kFlagCacheHints = 8,       // operands evict_last, C loads and D stores evict_first in L2
     kFlagDirectC = 16,         // single problems, 128-row tiles: C read into registers, not staged
     kFlagSplitLoad = 32,       // two producer warps: A boxes (and scale atoms) from one, B boxes from the other
+    kFlagDirectD = 64,         // single problems, 128- and 256-row tiles: D stored from registers, not staged
 };
 
 // K block processed at iteration `it` of a tile: with kFlagRotateK the
@@ -1072,6 +1078,79 @@ __device__ __forceinline__ void load_c_row(uint32_t (&cr)[32], const void *c_ptr
     }
 }
 
+// This thread's 128 bytes of D for one chunk (row `row`, columns col0..),
+// written from registers: whole 16-byte units inside N, single elements at
+// the N edge, nothing past the matrix. `o` holds the chunk in the output type.
+template <int CW>
+__device__ __forceinline__ void store_d_row(const uint32_t (&o)[32], void *d_ptr, long long ldd, int row, int col0,
+                                            int M, int N)
+{
+    constexpr int OB = CW == 32 ? 4 : 2;  // output element bytes
+    if (row >= M)
+        return;
+    char *rp = static_cast<char *>(d_ptr) + (static_cast<long long>(row) * ldd + col0) * OB;
+    const int nv = N - col0;  // valid columns of the chunk
+    if (nv >= CW) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            reinterpret_cast<uint4 *>(rp)[u] = make_uint4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
+    } else if constexpr (OB == 4) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (i < nv)
+                reinterpret_cast<uint32_t *>(rp)[i] = o[i];
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            if (2 * i < nv)
+                reinterpret_cast<unsigned short *>(rp)[2 * i] = static_cast<unsigned short>(o[i] & 0xFFFFu);
+            if (2 * i + 1 < nv)
+                reinterpret_cast<unsigned short *>(rp)[2 * i + 1] = static_cast<unsigned short>(o[i] >> 16);
+        }
+    }
+}
+
+// alpha * acc + beta * C for one chunk of this thread's row, in the output
+// type, C from registers (`creg`, as load_c_row leaves it)
+template <int CW>
+__device__ __forceinline__ void chunk_math_regs(float (&acc)[CW], const EpiConst &e, bool use_c, const uint32_t (&creg)[32],
+                                                uint32_t (&o)[32])
+{
+    constexpr int PER16 = (CW == 32) ? 4 : 8;  // elements per 16-byte unit
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        float *v = acc + u * PER16;
+#pragma unroll
+        for (int i = 0; i < PER16; ++i)
+            v[i] *= e.alpha;
+        if (use_c) {
+            const uint32_t c[4] = {creg[4 * u], creg[4 * u + 1], creg[4 * u + 2], creg[4 * u + 3]};
+            if constexpr (CW == 32) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    v[i] = fmaf(e.beta, __uint_as_float(c[i]), v[i]);
+            } else {
+                float cf[8];
+                unpack_in(c, e.out_type, cf);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    v[i] = fmaf(e.beta, cf[i], v[i]);
+            }
+        }
+        uint32_t w[4];
+        if constexpr (CW == 32) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                w[i] = __float_as_uint(v[i]);
+        } else {
+            pack_out(v, e.out_type, w);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            o[4 * u + i] = w[i];
+    }
+}
+
 // One 32-row x 128-byte chunk: fp32 output covers 32 columns, 16-bit output 64.
 // `acc` holds this thread's row (lane) of the chunk in fp32. C comes from the
 // staging buffer (swizzled like the output), or from `creg` when CREG.
@@ -1123,11 +1202,6 @@ __device__ __forceinline__ void epilogue_chunk_math(float (&acc)[CW], const EpiC
     }
 }
 
-// Stream-K head gather, one epilogue warp (TMEM lane quarter q, rows
-// 32q..32q+31): waits for the flags of the clusters that hold the rest of
-// split tile `ua`, then writes the sum of their fp32 partial sums into TMEM
-// accumulator buffer `buf` (the first n32 32-column groups), the buffer the
-// head's own MMAs do not use. False if a flag did not come in time.
 // The clusters that hold the rest of split tile `ua` (its head): [*lo, *hi];
 // a cluster whose share of the split iterations is empty holds nothing.
 __device__ __forceinline__ void sk_contributors(const Sched &sched, const Unit &ua, int num_clusters, int *lo, int *hi)
@@ -1165,6 +1239,11 @@ __device__ bool sk_wait_contributors(const Sched &sched, const Unit &ua, int q, 
     return true;
 }
 
+// Stream-K head gather, one epilogue warp (TMEM lane quarter q, rows
+// 32q..32q+31): waits for the flags of the clusters that hold the rest of
+// split tile `ua`, then writes the sum of their fp32 partial sums into TMEM
+// accumulator buffer `buf` (the first n32 32-column groups), the buffer the
+// head's own MMAs do not use. False if a flag did not come in time.
 template <int CL, int BN>
 __device__ bool sk_gather(const Sched &sched, const Unit &ua, int n32, int buf, uint32_t tmem_base, int q,
                           int prow, const float4 *partials, const uint32_t *sk_flags, uint32_t epoch, int rank,
@@ -1245,9 +1324,14 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
     const bool use_c = ec.beta != 0.0f;
     // C straight into registers: single problems with 128-row tiles (each
     // thread owns one output row of a chunk)
-    const bool direct_c = use_c && !GROUPED && C::BM == 128 && (p.flags & kFlagDirectC) != 0;
+    // D straight from registers (single problems, tiles whose rows are the
+    // threads' lanes); C then comes into registers too
+    const bool direct_d = !GROUPED && C::BM >= 128 && !C::WS && (p.flags & kFlagDirectD) != 0;
+    const bool direct_c = use_c && !GROUPED && C::BM >= 128 && !C::WS && ((p.flags & kFlagDirectC) != 0 || direct_d);
     const void *const c_ptr = p.c_ptr;
     const long long ldc = p.ldc;
+    void *const d_ptr = p.d_ptr;
+    const long long ldd = p.ldd;
     // C and D pass through once: let them leave L2 first
     const bool hints = (p.flags & kFlagCacheHints) != 0;
     const uint64_t stream_once = hints ? l2_policy_evict_first() : 0;
@@ -1449,7 +1533,7 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
                 const uint32_t sbuf = buf0 + static_cast<uint32_t>(sel * kEpiBufBytes);
                 const uint32_t sbar = ebar0 + static_cast<uint32_t>(8 * sel);
                 // the store issued from this buffer (EPI_BUFS chunks ago) must have read it
-                if (lane == 0)
+                if (lane == 0 && !direct_d)
                     bulk_wait_group_read<C::EPI_BUFS - 1>();
                 __syncwarp();
                 uint32_t creg[32];
@@ -1534,6 +1618,12 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
                     epi_phase[sel] ^= 1u;
                     if (!__all_sync(0xffffffffu, ok))
                         return;
+                }
+                if (direct_d) {
+                    uint32_t o[32];
+                    chunk_math_regs<CW>(v, ec, use_c, creg, o);
+                    store_d_row<CW>(o, d_ptr, ldd, m0h + trow, col0, ti.M, ti.N);
+                    continue;
                 }
                 if (direct_c)
                     epilogue_chunk_math<CW, true>(v, ec, sbuf, trow, true, creg);

@@ -104,7 +104,7 @@ def test_block_scaled_formats_have_fixed_tiles(g):
 
 
 def test_invalid_options_are_rejected(g):
-    for opts, status in [(dict(flags=64), g.ERR_INVALID_ARG), (dict(stream_k=4), g.ERR_INVALID_ARG),
+    for opts, status in [(dict(flags=128), g.ERR_INVALID_ARG), (dict(stream_k=4), g.ERR_INVALID_ARG),
                          (dict(swizzle_a=6), g.ERR_INVALID_ARG), (dict(tile_m=96), g.ERR_INVALID_ARG),
                          (dict(workspace=0x1010), g.ERR_ALIGNMENT), (dict(tile_n=96), g.ERR_UNSUPPORTED),
                          (dict(mma_ws=2), g.ERR_INVALID_ARG), (dict(tile_m=16), g.ERR_INVALID_ARG),
