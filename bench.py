@@ -125,13 +125,27 @@ NOMINAL_HBM_SOURCE = "nominal HBM3e 8000 GB/s (NVIDIA GB300 sheet)"
 KERNEL_SOURCES = ("gemm_kernel.cuh", "ptx.cuh", "descriptors.cuh")
 
 
-def _source_hash():
-    """Hash of the device-code sources; a stored ncu traffic figure is valid only for this hash."""
+def _code_lines(text):
+    """The source without its // comments and blank lines (what the compiler sees of it)."""
+    out = []
+    for line in text.splitlines():
+        code = re.sub(r"//.*$", "", line).rstrip()
+        if code.strip():
+            out.append(code)
+    return "\n".join(out)
+
+
+def _source_hash(read=None):
+    """Hash of the device-code sources, comments left out; a stored ncu traffic figure is valid
+    only for this hash. `read(name)` returns a source's text (default: the working tree)."""
+    if read is None:
+        def read(name):
+            with open(os.path.join(ROOT, "smem_swizzle_layouts_gb300", "csrc", name)) as f:
+                return f.read()
     h = hashlib.sha256()
     for name in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "smem_swizzle_layouts_gb300", "csrc", name), "rb") as f:
-            h.update(name.encode())
-            h.update(f.read())
+        h.update(name.encode())
+        h.update(_code_lines(read(name)).encode())
     return h.hexdigest()[:16]
 
 

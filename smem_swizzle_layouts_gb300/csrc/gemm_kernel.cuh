@@ -12,7 +12,9 @@
 //              mbarriers ("06 Blackwell Tensor Core - tcgen05 MMA", "How
 //              tcgen05.mma Executes"); the accumulator is double-buffered
 //              in TMEM (2 x BN fp32 columns) so the epilogue of tile i
-//              overlaps the main loop of tile i+1;
+//              overlaps the main loop of tile i+1 (two-half 256-row tiles
+//              on one CTA: two M=128 MMAs per K slice, both accumulators in
+//              TMEM, one buffer);
 //   warps 2-5  epilogue: warp w reads TMEM lanes 32*(w%4)..+31 (the lane
 //              quarter rule of "Tensor Cores, layouts, and swizzling",
 //              tcgen05 section) with tcgen05.ld, applies alpha/beta against
@@ -21,7 +23,10 @@
 //              them with TMA stores;
 //   warp 6     block-scaled kinds only: scale copier (tcgen05.cp of each
 //   (and 7)    stage's scale atoms into TMEM); NVFP4 runs two copiers on
-//              alternate K groups. So 192 threads, or 224/256 with copiers.
+//              alternate K groups;
+//   last warp  second producer, issuing the B boxes when the loads are
+//              split (kFlagSplitLoad; not in the NVFP4 kernels). So 224
+//              threads, or 256 with copiers.
 //
 // CTA pairs: the even CTA holds accumulator rows 0-127 and the odd CTA rows
 // 128-255 ("How cta_group Sets the Operation Scope", cta_group::2, M=256).
