@@ -1392,6 +1392,7 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
     constexpr int kSlotRows = 128 * C::M_HALVES;   // rows of a partial-sum slot
     constexpr int kSlotVec = kSlotRows * BN / 4;   // float4 per slot
     int sk_lo = 0, sk_hi = -1;                     // a two-half head's contributors
+    int last_prob = -1;                            // grouped: problem whose C/D maps were acquired
     UnitIter units(sched, cluster_id, num_clusters);
     Unit u;
     while (units.next(u)) {
@@ -1424,8 +1425,11 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
         if constexpr (GROUPED) {
             mC = maps + 4 * ti.prob + 2;
             mD = mC + 1;
-            fence_tensormap_acquire(mC);
-            fence_tensormap_acquire(mD);
+            if (ti.prob != last_prob) {  // once per problem, as the producer does for A and B
+                fence_tensormap_acquire(mC);
+                fence_tensormap_acquire(mD);
+                last_prob = ti.prob;
+            }
         }
         const bool has_acc = ti.K > 0;
         const int m0 = ti.m_blk * C::TILE_M + C::BM * static_cast<int>(rank) + wrow;
