@@ -97,8 +97,8 @@ typedef enum {
  *                 (cta_group::1 only: two M = 128 MMAs per K slice share
  *                 each B slice, their accumulators filling the 512 TMEM
  *                 columns; 16-bit operands, single problems, tile_n 256,
- *                 swizzled operand layouts; the epilogue of a tile does not
- *                 overlap the next tile's MMAs).
+ *                 the epilogue of a tile does not overlap the next tile's
+ *                 MMAs; by default two such CTAs share B, see multicast_b).
  *   tile_n        MMA N per tile: 64, 128 or 256 (cta_group::2: 128 or 256).
  *   block_k       K elements per pipeline stage: 32, 64 or 128 where built.
  *   swizzle_a/b   operand swizzle (gemm_swizzle_t).
@@ -174,15 +174,17 @@ typedef enum {
  *                 the four TMEM lane quarters by column parts, so all four
  *                 epilogue warps store full 32-row chunks. Other tiles with
  *                 mma_ws 1 return GEMM_ERR_UNSUPPORTED.
- *   multicast_b   single-CTA (cta_group::1) 128 x 256 tiles run in clusters
- *                 of two CTAs on vertically adjacent tiles that share their
- *                 B panel: each CTA loads half of every B stage and TMA
- *                 multicasts it into both CTAs' shared memory, so each CTA
- *                 reads half as many B bytes from L2; each CTA's MMA
- *                 completion releases the stage in both. 0 the library
- *                 chooses, 1 use it, -1 do not; other tiles with 1 return
- *                 GEMM_ERR_UNSUPPORTED. Multicast stays within this GPU's
- *                 memory (the operands of one call).
+ *   multicast_b   single-CTA (cta_group::1) tiles 256 wide (128 or 256 rows)
+ *                 run in clusters of two CTAs on vertically adjacent tiles
+ *                 that share their B panel: each CTA loads half of every B
+ *                 stage and TMA multicasts it into both CTAs' shared memory,
+ *                 so each CTA reads half as many B bytes from L2; each CTA's
+ *                 MMA completion releases the stage in both. 0 the library
+ *                 chooses (256-row tiles of more than 256 rows in all; 128-row
+ *                 tiles when B is MN-major or A and B overflow L2), 1 use it,
+ *                 -1 do not; other tiles with 1 return GEMM_ERR_UNSUPPORTED.
+ *                 Multicast stays within this GPU's memory (the operands of
+ *                 one call).
  */
 typedef struct {
     int cta_group;

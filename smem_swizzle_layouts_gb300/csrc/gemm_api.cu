@@ -408,12 +408,18 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
     // operands in L2: within 1 %)
     int mcb = 0;
     if (opt.multicast_b == 1) {
-        if (cg != 1 || bm != 128 || ws || sf != kScaleNone || grouped)
+        if (cg != 1 || (bm != 128 && bm != 256) || ws || sf != kScaleNone || grouped)
             return GEMM_ERR_UNSUPPORTED;
         mcb = 1;
     } else if (opt.multicast_b == 0 && cg == 1 && bm == 128 && bn == 256 && !ws && sf == kScaleNone && !grouped &&
                M > 128 && (b_mn || (M + N) * K * esize > (static_cast<int64_t>(128) << 20)) &&
                find_variant(cg, bn, bk, grouped, esize, bm, sf, kModeMcastB)) {
+        mcb = 1;
+    } else if (opt.multicast_b == 0 && bm == 256 && M > 256 && !grouped &&
+               find_variant(cg, bn, bk, grouped, esize, bm, sf, kModeMcastB)) {
+        // two-half tiles share B in pairs of CTAs by default (measured, TFLOP/s
+        // without -> with: 4096^3 1389 -> 1404-1417, K/MN 1295-1307 -> 1418,
+        // 6144^3 1738 -> 1758-1765, 8192^3 1856-1862 -> 1888, MN/MN 1700 -> 1791)
         mcb = 1;
     }
     const int mode = ws ? kModeWs : mcb ? kModeMcastB : kModeOrdinary;

@@ -269,12 +269,12 @@ struct Cfg {
     static constexpr int CLUSTER = (CG == 2 || MCB) ? 2 : 1;
     static constexpr int TILE_M = BM * CLUSTER;
     static constexpr int B_LOAD = MCB ? BN / 2 : BN_LOCAL;
-    static_assert(!MCB || (CG == 1 && BMT == 128 && SF == 0 && BN % 128 == 0),
-                  "B multicast: two single-CTA 128-row tiles sharing a B panel split in halves");
+    static_assert(!MCB || (CG == 1 && (BMT == 128 || BMT == 256) && SF == 0 && BN % 128 == 0),
+                  "B multicast: two single-CTA 128- or 256-row tiles sharing a B panel split in halves");
     static constexpr int EPI_ROWS = (WS || M_HALVES == 2) ? 32 : BM / 4;  // output rows per epilogue warp (and half)
     static_assert(BMT == 128 || BMT == 256 || (BMT == 64 && CG == 1) || (BMT == 32 && WS),
                   "64-row tiles are single-CTA");
-    static_assert(M_HALVES == 1 || (CG == 1 && !WS && !MCB && SF == 0 && BN * M_HALVES <= 512),
+    static_assert(M_HALVES == 1 || (CG == 1 && !WS && SF == 0 && BN * M_HALVES <= 512),
                   "two-half tiles: single CTAs, ordinary kind::f16/f8f6f4 MMAs, both accumulators in TMEM");
     static_assert(!WS || ((BMT == 32 || BMT == 64) && CG == 1 && ESIZE == 2 && SF == 0 && (BN / COL_PARTS) % 64 == 0),
                   ".ws tiles: 32 or 64 rows, single CTA, 16-bit operands, whole 64-column chunks per warp");

@@ -8,7 +8,9 @@ starting 128 rows further into the stage ("LBO, SBO and SWZ for a tcgen05
 tile": 8-row groups SBO apart for K-major tiles, MN atoms LBO apart for
 MN-major ones), into accumulators at columns 0 and N. A wrong half offset or
 column base would mix up the two halves, so the integer cases compare bit for
-bit; normal inputs are held to the parity tolerance.
+bit; normal inputs are held to the parity tolerance. By default two such CTAs
+form a cluster that shares B by TMA multicast (each loads half of the B
+panel into both); every case runs with and without that sharing.
 """
 import pytest
 
@@ -18,7 +20,8 @@ torch = pytest.importorskip("torch")
 
 pytestmark = pytest.mark.gpu
 
-TH = dict(tile_m=256)
+SHARING = [dict(tile_m=256), dict(tile_m=256, multicast_b=-1)]
+IDS = ["sharedB", "ownB"]
 
 
 @pytest.fixture(scope="module")
@@ -31,63 +34,74 @@ def g():
     return g
 
 
-def test_two_half_single_tile_exact(g):
-    run_case(g, 256, 256, 64, dist="int4", exact=True, options=TH)
+@pytest.mark.parametrize("opts", SHARING, ids=IDS)
+def test_two_half_single_tile_exact(g, opts):
+    run_case(g, 256, 256, 64, dist="int4", exact=True, options=opts)
+    run_case(g, 512, 256, 64, dist="int4", exact=True, options=opts)  # one cluster tile when B is shared
 
 
-@pytest.mark.parametrize("M,N,K", [(1000, 1000, 776), (130, 300, 72), (257, 513, 1000), (768, 256, 2048), (1, 256, 64)])
-def test_two_half_ragged_shapes_exact(g, M, N, K):
-    # several row tiles, a second half partly or wholly past M, ragged N and K tails
-    run_case(g, M, N, K, dist="int4", exact=True, seed=M + N + K, options=TH)
+@pytest.mark.parametrize("opts", SHARING, ids=IDS)
+@pytest.mark.parametrize("M,N,K", [(1000, 1000, 776), (130, 300, 72), (257, 513, 1000), (768, 256, 2048), (1, 256, 64),
+                                   (1300, 520, 200)])
+def test_two_half_ragged_shapes_exact(g, opts, M, N, K):
+    # several row tiles, a second half (or a cluster's second CTA) partly or wholly
+    # past M, ragged N and K tails
+    run_case(g, M, N, K, dist="int4", exact=True, seed=M + N + K, options=opts)
 
 
+@pytest.mark.parametrize("opts", SHARING, ids=IDS)
 @pytest.mark.parametrize("a_major,b_major", [("K", "MN"), ("MN", "K"), ("MN", "MN")])
-def test_two_half_operand_majors_exact(g, a_major, b_major):
-    run_case(g, 700, 520, 200, a_major=a_major, b_major=b_major, dist="int4", exact=True, options=TH)
+def test_two_half_operand_majors_exact(g, opts, a_major, b_major):
+    run_case(g, 700, 520, 200, a_major=a_major, b_major=b_major, dist="int4", exact=True, options=opts)
 
 
+@pytest.mark.parametrize("opts", SHARING, ids=IDS)
 @pytest.mark.parametrize("swz", [1, 2, 3, 4], ids=["sw32", "sw64", "sw128", "none"])
 @pytest.mark.parametrize("a_major", ["K", "MN"])
-def test_two_half_swizzles_exact(g, swz, a_major):
-    run_case(g, 512, 512, 256, a_major=a_major, b_major=a_major, dist="int4", exact=True,
-             options=dict(TH, swizzle_a=swz, swizzle_b=swz))
+def test_two_half_swizzles_exact(g, opts, swz, a_major):
+    run_case(g, 768, 512, 256, a_major=a_major, b_major=a_major, dist="int4", exact=True,
+             options=dict(opts, swizzle_a=swz, swizzle_b=swz))
 
 
+@pytest.mark.parametrize("opts", SHARING, ids=IDS)
 @pytest.mark.parametrize("out", ["f32", "bf16", "f16"])
-def test_two_half_outputs_alpha_beta_within_tolerance(g, out):
-    run_case(g, 600, 700, 384, dist="normal", out=out, alpha=0.75, beta=-1.5, seed=11, options=TH)
+def test_two_half_outputs_alpha_beta_within_tolerance(g, opts, out):
+    run_case(g, 600, 700, 384, dist="normal", out=out, alpha=0.75, beta=-1.5, seed=11, options=opts)
 
 
-def test_two_half_in_place_fp16_and_k_zero(g):
-    run_case(g, 300, 520, 136, in_fmt="f16", dist="uniform", out="f32", beta=1.0, inplace=True, options=TH)
-    run_case(g, 300, 300, 0, dist="uniform", out="f32", beta=0.5, options=TH)
+@pytest.mark.parametrize("opts", SHARING, ids=IDS)
+def test_two_half_in_place_fp16_and_k_zero(g, opts):
+    run_case(g, 300, 520, 136, in_fmt="f16", dist="uniform", out="f32", beta=1.0, inplace=True, options=opts)
+    run_case(g, 300, 300, 0, dist="uniform", out="f32", beta=0.5, options=opts)
 
 
+@pytest.mark.parametrize("opts", SHARING, ids=IDS)
 @pytest.mark.parametrize("mode", [1, 2, 3])
-def test_two_half_stream_k_exact(g, mode):
+def test_two_half_stream_k_exact(g, opts, mode):
     # split tiles: the head adds its contributors' 256-row partial sums chunk by chunk
     ws = torch.zeros(g.gemm_streamk_workspace_size(), dtype=torch.uint8, device=DEV)
     run_case(g, 2048, 2304, 3000, dist="int4", exact=True, out="f32", beta=0.5, seed=mode,
-             options=dict(TH, workspace=ws, stream_k=mode))
+             options=dict(opts, workspace=ws, stream_k=mode))
 
 
 def test_two_half_is_the_default_for_large_single_cta_problems(g):
     # 4096^3 with cta_group 1 and the stream-K workspace (the bench launch):
-    # two-half tiles, unsplit; sampled entries of the full product
+    # two-half tiles sharing B, unsplit; sampled entries of the full product
     ws = torch.zeros(g.gemm_streamk_workspace_size(), dtype=torch.uint8, device=DEV)
     M = N = K = 4096
     run_case(g, M, N, K, dist="normal", scale=0.1, out="bf16", seed=10,
              options=dict(cta_group=1, tile_n=256, workspace=ws), sample=sample_entries(M, N, 2048, seed=5))
 
 
+@pytest.mark.parametrize("opts", SHARING, ids=IDS)
 @pytest.mark.parametrize("role", [1, 2], ids=["producer", "mma"])
-def test_two_half_injected_timeout_and_the_context_survives(g, role):
+def test_two_half_injected_timeout_and_the_context_survives(g, opts, role):
     g.gemm_debug_inject_timeout(20, role=role)
     M = N = K = 512
     A = torch.zeros(M, K, dtype=torch.bfloat16, device=DEV)
     B = torch.zeros(N, K, dtype=torch.bfloat16, device=DEV)
     D = torch.zeros(M, N, dtype=torch.float32, device=DEV)
-    g.gemm_ex(1, M, N, K, A, 0, K, B, 0, K, None, 0, D, N, 0, 1.0, 0.0, options=TH)
+    g.gemm_ex(1, M, N, K, A, 0, K, B, 0, K, None, 0, D, N, 0, 1.0, 0.0, options=opts)
     st, word = g.gemm_last_device_status()
     assert st == g.ERR_TIMEOUT and word != 0, hex(word)
-    run_case(g, 512, 384, 256, dist="int4", exact=True, options=TH)
+    run_case(g, 512, 384, 256, dist="int4", exact=True, options=opts)

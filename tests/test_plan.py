@@ -186,7 +186,9 @@ def test_b_multicast_default_rule(g):
 def test_two_half_tiles_for_large_single_cta_problems_with_long_k(g):
     # 256 rows on one CTA (two M = 128 MMAs per B slice, both accumulators in TMEM)
     p = plan(g, 4096, 4096, 4096, cta_group=1, tile_n=256)
-    assert (p["tile_m"], p["tile_n"], p["block_k"], p["cta_group"], p["multicast_b"]) == (256, 256, 64, 1, 0)
+    assert (p["tile_m"], p["tile_n"], p["block_k"], p["cta_group"], p["multicast_b"]) == (256, 256, 64, 1, 1)
+    assert plan(g, 4096, 4096, 4096, cta_group=1, multicast_b=-1)["multicast_b"] == 0   # pairs of CTAs share B unless refused
+    assert plan(g, 256, 4096, 4096, tile_m=256)["multicast_b"] == 0                        # one row tile: nothing to share
     assert plan(g, 8192, 8192, 8192, a=MN_MAJOR, b=MN_MAJOR, cta_group=1)["tile_m"] == 256
     assert plan(g, 8192, 8192, 2048, cta_group=1)["tile_m"] == 128       # short K: the epilogue would weigh more
     assert plan(g, 2047, 8192, 8192, cta_group=1)["tile_m"] == 128       # fewer than 2048 rows
@@ -195,9 +197,8 @@ def test_two_half_tiles_for_large_single_cta_problems_with_long_k(g):
     assert plan(g, 8192, 8192, 8192, FP8, cta_group=1)["tile_m"] == 128  # 16-bit operands only
     assert plan(g, 8192, 8192, 8192)["cta_group"] == 2                   # pairs stay the default
     p = plan(g, 512, 512, 256, tile_m=256)
-    assert (p["tile_m"], p["tile_n"], p["cta_group"], p["block_k"]) == (256, 256, 1, 64)
-    for opts in (dict(tile_m=256, cta_group=2), dict(tile_m=256, tile_n=128), dict(tile_m=256, mma_ws=1),
-                 dict(tile_m=256, multicast_b=1)):
+    assert (p["tile_m"], p["tile_n"], p["cta_group"], p["block_k"], p["multicast_b"]) == (256, 256, 1, 64, 1)
+    for opts in (dict(tile_m=256, cta_group=2), dict(tile_m=256, tile_n=128), dict(tile_m=256, mma_ws=1)):
         with pytest.raises(g.GemmError) as ei:
             plan(g, 4096, 4096, 4096, **opts)
         assert ei.value.status == g.ERR_UNSUPPORTED, opts
