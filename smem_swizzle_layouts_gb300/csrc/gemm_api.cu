@@ -354,7 +354,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
     // 1344, where the epilogue, which no longer overlaps, weighs more.
     if (opt.tile_m == 0 && cg == 1 && esize == 2 && !grouped && sf == kScaleNone && bm == 128 &&
         (opt.tile_n == 0 || opt.tile_n == 256) && (opt.block_k == 0 || opt.block_k == 64) && opt.mma_ws != 1 &&
-        opt.multicast_b != 1 && M >= 2048 && N >= 2048 && K >= 4096 && find_variant(1, 256, 64, false, 2, 256)) {
+        M >= 2048 && N >= 2048 && K >= 4096 && find_variant(1, 256, 64, false, 2, 256)) {
         bm = 256;
         bn = 256;
         bk = 64;

@@ -274,7 +274,7 @@ struct Cfg {
     static constexpr int EPI_ROWS = (WS || M_HALVES == 2) ? 32 : BM / 4;  // output rows per epilogue warp (and half)
     static_assert(BMT == 128 || BMT == 256 || (BMT == 64 && CG == 1) || (BMT == 32 && WS),
                   "64-row tiles are single-CTA");
-    static_assert(M_HALVES == 1 || (CG == 1 && !WS && SF == 0 && BN * M_HALVES <= 512),
+    static_assert(M_HALVES == 1 || (CG == 1 && !WS && SF == 0 && ESIZE != 4 && BN * M_HALVES <= 512),
                   "two-half tiles: single CTAs, ordinary kind::f16/f8f6f4 MMAs, both accumulators in TMEM");
     static_assert(!WS || ((BMT == 32 || BMT == 64) && CG == 1 && ESIZE == 2 && SF == 0 && (BN / COL_PARTS) % 64 == 0),
                   ".ws tiles: 32 or 64 rows, single CTA, 16-bit operands, whole 64-column chunks per warp");
@@ -870,8 +870,9 @@ __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uin
     const uint64_t a_desc0 = make_smem_desc(smem, pa.lbo, pa.sbo, pa.swz);
     const uint64_t b_desc0 = make_smem_desc(smem + C::A_BYTES, pb.lbo, pb.sbo, pb.swz);
     uint32_t a_off[C::KSLICES], b_off[C::KSLICES];
-    // two-half tiles: rows 128..255 of the A tile start 128 K-major rows (W
-    // bytes each) or 128 MN elements (BK rows of K per element) further on
+    // two-half tiles: rows 128..255 of the A tile start 128 * W bytes further
+    // on in a K-major stage (rows of W bytes), 128 * ESIZE * BK bytes in an
+    // MN-major one (each MN element holds BK rows of K)
     const uint32_t a_half = C::M_HALVES == 2 ? (p.a_mn ? 128u * ESIZE * BK : 128u * swizzle_row_bytes(p.a_swz)) >> 4 : 0u;
 #pragma unroll
     for (int j = 0; j < C::KSLICES; ++j) {

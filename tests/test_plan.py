@@ -189,6 +189,8 @@ def test_two_half_tiles_for_large_single_cta_problems_with_long_k(g):
     assert (p["tile_m"], p["tile_n"], p["block_k"], p["cta_group"], p["multicast_b"]) == (256, 256, 64, 1, 1)
     assert plan(g, 4096, 4096, 4096, cta_group=1, multicast_b=-1)["multicast_b"] == 0   # pairs of CTAs share B unless refused
     assert plan(g, 256, 4096, 4096, tile_m=256)["multicast_b"] == 0                        # one row tile: nothing to share
+    p = plan(g, 8192, 8192, 8192, cta_group=1, multicast_b=1)                              # asked for: two-half tiles share B
+    assert (p["tile_m"], p["multicast_b"]) == (256, 1)
     assert plan(g, 8192, 8192, 8192, a=MN_MAJOR, b=MN_MAJOR, cta_group=1)["tile_m"] == 256
     assert plan(g, 8192, 8192, 2048, cta_group=1)["tile_m"] == 128       # short K: the epilogue would weigh more
     assert plan(g, 2047, 8192, 8192, cta_group=1)["tile_m"] == 128       # fewer than 2048 rows
