@@ -156,8 +156,10 @@ def test_weight_stationary_tiles(g):
 
 def test_b_multicast_clusters(g):
     # two single-CTA 128 x 256 tiles share their B panel by multicast when asked
-    p = plan(g, 4096, 4096, 4096, cta_group=1, tile_n=256, multicast_b=1)
+    p = plan(g, 4096, 4096, 4096, cta_group=1, tile_n=256, tile_m=128, multicast_b=1)
     assert (p["cta_group"], p["tile_n"], p["block_k"], p["tile_m"], p["multicast_b"]) == (1, 256, 64, 128, 1)
+    p = plan(g, 4096, 4096, 2048, cta_group=1, tile_n=256, multicast_b=1)   # short K: 128-row tiles
+    assert (p["tile_m"], p["multicast_b"]) == (128, 1)
     p = plan(g, 8192, 8192, 8192, FP8, cta_group=1, tile_n=256, multicast_b=1)
     assert (p["block_k"], p["multicast_b"]) == (128, 1)
     for kind, opts in [(BF16, dict(cta_group=2, multicast_b=1)), (BF16, dict(tile_m=64, multicast_b=1)),
