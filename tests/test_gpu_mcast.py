@@ -5,7 +5,8 @@ cluster: each CTA loads half of every B stage and multicasts it into both
 CTAs' shared memory, and each CTA's MMA completion releases the stage in
 both. Integer-valued cases compare bit for bit; normal inputs are held to the
 parity tolerance. Ragged shapes put the second CTA of a cluster past M (it
-still loads its half of B for the first) and cut N inside a B half.
+still loads its half of B for the first) and cut N inside a B half. The
+256-row tiles that share B the same way are covered in test_gpu_two_half.py.
 """
 import pytest
 
@@ -15,7 +16,7 @@ torch = pytest.importorskip("torch")
 
 pytestmark = pytest.mark.gpu
 
-MC = dict(cta_group=1, tile_n=256, multicast_b=1)
+MC = dict(cta_group=1, tile_n=256, tile_m=128, multicast_b=1)
 
 
 @pytest.fixture(scope="module")
