@@ -259,6 +259,29 @@ def test_stage_packing_matches_descriptor_for_every_slice(major, mode, rows, bk)
     assert len(seen) == rows * bk and min(seen) == P_BASE and max(seen) < P_BASE + rows * bk * 2
 
 
+@pytest.mark.parametrize("major", ["K", "MN"])
+@pytest.mark.parametrize("mode", ["none", "sw32", "sw64", "sw128"])
+def test_second_half_of_a_256_row_stage_is_a_shifted_start(major, mode):
+    # A 256-row A stage read by two M = 128 MMAs ("06 Blackwell Tensor Core -
+    # tcgen05 MMA": cta_group::1 MMAs have at most 128 rows): the descriptor
+    # of rows 128..255 is the stage's own slice descriptor with its start moved
+    # by 128 rows' worth of the packing ("LBO, SBO and SWZ for a tcgen05 tile":
+    # 8-row groups SBO = 8 W apart for K-major stages, so 16 groups = 128 W;
+    # MN-major atoms of W / esize elements LBO = BK W apart, so 128 esize / W
+    # atoms = 128 esize BK). Every element of every slice lands where the
+    # stage packing puts row 128 + m.
+    rows, bk, esize = 256, 64, 2
+    W = L.swizzle_width(mode)
+    shift = 128 * W if major == "K" else 128 * esize * bk
+    for j in range(bk // 16):
+        d = L.stage_slice_desc(major, mode, rows, bk, esize, j, P_BASE)
+        d2 = L.SmemDesc(start=d.start + shift, lbo=d.lbo, sbo=d.sbo, base_offset=d.base_offset, swz=d.swz)
+        for m in range(128):
+            for kk in range(16):
+                assert L.desc_element_addr(d2, major, esize, m, kk) == \
+                    P_BASE + L.stage_element_offset(major, mode, rows, bk, esize, 128 + m, 16 * j + kk)
+
+
 def test_transposed_operand_reading_is_caught():
     # a plausible slip -- reading an MN-major stage with the K-major formula -- changes addresses
     d = L.stage_slice_desc("MN", "sw128", 128, 64, 2, 0, P_BASE)
