@@ -48,10 +48,10 @@ WORKLOADS = {
              "cta_group::2 CTA pairs, persistent tile scheduler"),
     "square4096_bf16": dict(
         M=4096, N=4096, K=4096, a_major="K", b_major="K", out="bf16", alpha=1.0, beta=0.0, dist="normal",
-        scale=0.1, seed=10, options=dict(cta_group=1, tile_n=256, workspace=True),
+        scale=0.1, seed=10, options=dict(cta_group=1, workspace=True),
         desc="4096^3 bf16, A and B K-major, N(0,1)*0.1, bf16 out, SW128, cta_group::1 with the library's default "
-             "tile for the shape (256x256 on one CTA, two M=128 MMAs per B slice, pairs of CTAs sharing B: 256 "
-             "tiles, unsplit); the stream-K workspace it is given would split the ragged last wave of 128-row tiles"),
+             "tile for the shape (256x224 on one CTA, two M=128 MMAs per B slice: 304 tiles, two full rounds, "
+             "unsplit); the stream-K workspace it is given would split the ragged last wave of 128-row tiles"),
     "skinny_m16384_n128_k8192": dict(
         M=16384, N=128, K=8192, a_major="K", b_major="K", out="bf16", alpha=1.0, beta=0.0, dist="normal",
         scale=1.0, seed=30, options=None, bound="hbm", desc="M=16384 N=128 K=8192 bf16, N(0,1), bf16 out"),

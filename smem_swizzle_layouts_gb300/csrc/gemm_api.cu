@@ -337,7 +337,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
         else if (!grouped && cg == 1 && bn == 128 && K <= 32 && opt.tile_n == 0)
             bk = 32;
         else
-            bk = (cg == 1 && bn == 256) ? 64 : 128;
+            bk = (cg == 1 && (bn == 256 || opt.tile_m == 256)) ? 64 : 128;  // two-half tiles: 64
     }
     // 64-row tiles (M = 64 MMAs) when asked, or for problems of at most 64 rows
     // (compiled for 128- and 256-wide N tiles)
@@ -358,6 +358,23 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
         bm = 256;
         bn = 256;
         bk = 64;
+        // 224 wide instead when that takes fewer column-rounds of the grid
+        // (the time of a round goes with the tile width): 4096^2 is 128
+        // B-sharing cluster tiles of 512 x 256 on 76 clusters, two rounds for
+        // 1.68 waves of work, but exactly two rounds of 304 tiles of 256 x 224
+        // on 152 CTAs. 224-wide tiles keep their own B: sharing it measured
+        // slower there (4096^3, TFLOP/s: 256 wide shared 1389, 224 wide shared
+        // 1449, 224 wide own 1481). K-major B only (measured).
+        if (opt.tile_n == 0 && opt.multicast_b != 1 && !b_mn && find_variant(1, 224, 64, false, 2, 256)) {
+            auto rounds = [&](int64_t rows, int64_t w, int64_t units) {
+                const int64_t tiles = ((M + rows - 1) / rows) * ((N + w - 1) / w);
+                return (tiles + units - 1) / units;
+            };
+            const bool shared256 = opt.multicast_b != -1;
+            const int64_t r256 = shared256 ? rounds(512, 256, sms / 2) : rounds(256, 256, sms);
+            if (rounds(256, 224, sms) * 224 < r256 * 256)
+                bn = 224;
+        }
     }
     // Weight-stationary tiles (tcgen05.mma.ws): 32 rows (M = 32 exists only in
     // the .ws form) when asked for, or 64 rows; single CTAs, 16-bit operands,
@@ -408,14 +425,15 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
     // operands in L2: within 1 %)
     int mcb = 0;
     if (opt.multicast_b == 1) {
-        if (cg != 1 || (bm != 128 && bm != 256) || ws || sf != kScaleNone || grouped)
+        // each CTA loads half of B: for MN-major B, whole swizzle atoms of it
+        if (cg != 1 || (bm != 128 && bm != 256) || ws || sf != kScaleNone || grouped || (b_mn && bn % 256 != 0))
             return GEMM_ERR_UNSUPPORTED;
         mcb = 1;
     } else if (opt.multicast_b == 0 && cg == 1 && bm == 128 && bn == 256 && !ws && sf == kScaleNone && !grouped &&
                M > 128 && (b_mn || (M + N) * K * esize > (static_cast<int64_t>(128) << 20)) &&
                find_variant(cg, bn, bk, grouped, esize, bm, sf, kModeMcastB)) {
         mcb = 1;
-    } else if (opt.multicast_b == 0 && bm == 256 && M > 256 && !grouped &&
+    } else if (opt.multicast_b == 0 && bm == 256 && bn == 256 && M > 256 && !grouped &&
                find_variant(cg, bn, bk, grouped, esize, bm, sf, kModeMcastB)) {
         // two-half tiles share B in pairs of CTAs by default (measured, TFLOP/s
         // without -> with: 4096^3 1389 -> 1404-1417, K/MN 1295-1307 -> 1418,

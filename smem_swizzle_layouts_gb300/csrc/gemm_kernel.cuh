@@ -250,6 +250,10 @@ struct Cfg {
     // side fill the TMEM columns, so they have one buffer and the epilogue of a
     // tile does not overlap the next tile's MMAs
     static constexpr int M_HALVES = BMT == 256 ? 2 : 1;
+    // TMEM column of the second half's accumulator: 256 whatever the width,
+    // so that a 64-column epilogue chunk of a 224-wide tile reads past its
+    // own columns only into columns no accumulator uses
+    static constexpr int HALF_COL = 256;
     static constexpr int ACC_BUFS = ((SF && BN == 256) || M_HALVES == 2) ? 1 : 2;
     static constexpr int SF_COL0 = ACC_BUFS * BN;
     static constexpr int SF_GROUP_COLS = 4 + 4 * (BN / 128);  // A atom, then the B atoms of one K group
@@ -262,19 +266,20 @@ struct Cfg {
     static constexpr int WS_ROW_BLOCKS = WS ? BM / 32 : 1;
     static constexpr int COL_PARTS = WS ? 4 / WS_ROW_BLOCKS : 1;
     static constexpr int ACC_COLS = BN / COL_PARTS;
-    static constexpr int TMEM_COLS = WS ? (2 * ACC_COLS < 32 ? 32 : 2 * ACC_COLS) : BMT == 64 ? BN : SF ? 512 : 2 * BN;
+    static constexpr int TMEM_COLS = WS ? (2 * ACC_COLS < 32 ? 32 : 2 * ACC_COLS) : BMT == 64 ? BN : (SF || M_HALVES == 2) ? 512 : 2 * BN;
     static constexpr int UMMA_M = BM / M_HALVES * CG;
     // CTAs per cluster (CTA pairs, or the two CTAs sharing B by multicast) and
     // the output rows of one cluster tile; B rows/atoms one CTA's TMA loads
     static constexpr int CLUSTER = (CG == 2 || MCB) ? 2 : 1;
     static constexpr int TILE_M = BM * CLUSTER;
     static constexpr int B_LOAD = MCB ? BN / 2 : BN_LOCAL;
-    static_assert(!MCB || (CG == 1 && (BMT == 128 || BMT == 256) && SF == 0 && BN % 128 == 0),
-                  "B multicast: two single-CTA 128- or 256-row tiles sharing a B panel split in halves");
+    static_assert(!MCB || (CG == 1 && (BMT == 128 || BMT == 256) && SF == 0 && BN % 32 == 0),
+                  "B multicast: two single-CTA 128- or 256-row tiles sharing a B panel split in halves of whole "
+                  "8-row groups (MN-major halves of whole atoms are checked by the host)");
     static constexpr int EPI_ROWS = (WS || M_HALVES == 2) ? 32 : BM / 4;  // output rows per epilogue warp (and half)
     static_assert(BMT == 128 || BMT == 256 || (BMT == 64 && CG == 1) || (BMT == 32 && WS),
                   "64-row tiles are single-CTA");
-    static_assert(M_HALVES == 1 || (CG == 1 && !WS && SF == 0 && ESIZE != 4 && BN * M_HALVES <= 512),
+    static_assert(M_HALVES == 1 || (CG == 1 && !WS && SF == 0 && ESIZE != 4 && BN <= HALF_COL && BN % 32 == 0),
                   "two-half tiles: single CTAs, ordinary kind::f16/f8f6f4 MMAs, both accumulators in TMEM");
     static_assert(!WS || ((BMT == 32 || BMT == 64) && CG == 1 && ESIZE == 2 && SF == 0 && (BN / COL_PARTS) % 64 == 0),
                   ".ws tiles: 32 or 64 rows, single CTA, 16-bit operands, whole 64-column chunks per warp");
@@ -953,7 +958,7 @@ __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uin
                         mma_f16<CG>(d_tmem, a_desc0 + sdelta + a_off[j], b_desc0 + sdelta + b_off[j], idesc,
                                     ((kb - kb_lo) | j) != 0);
                         if constexpr (C::M_HALVES == 2)  // the same B slice, rows 128..255 of A
-                            mma_f16<CG>(d_tmem + BN, a_desc0 + sdelta + a_off[j] + a_half, b_desc0 + sdelta + b_off[j],
+                            mma_f16<CG>(d_tmem + C::HALF_COL, a_desc0 + sdelta + a_off[j] + a_half, b_desc0 + sdelta + b_off[j],
                                         idesc, ((kb - kb_lo) | j) != 0);
                     }
                     else if constexpr (ESIZE == 4)
@@ -963,7 +968,7 @@ __device__ void role_mma(const KParams &p, uint32_t smem, uint32_t bar_full, uin
                         mma_f8<CG>(d_tmem, a_desc0 + sdelta + a_off[j], b_desc0 + sdelta + b_off[j], idesc,
                                    ((kb - kb_lo) | j) != 0);
                         if constexpr (C::M_HALVES == 2)
-                            mma_f8<CG>(d_tmem + BN, a_desc0 + sdelta + a_off[j] + a_half, b_desc0 + sdelta + b_off[j],
+                            mma_f8<CG>(d_tmem + C::HALF_COL, a_desc0 + sdelta + a_off[j] + a_half, b_desc0 + sdelta + b_off[j],
                                        idesc, ((kb - kb_lo) | j) != 0);
                     }
                 }
@@ -1096,10 +1101,12 @@ __device__ __forceinline__ void store_d_row(const uint32_t (&o)[32], void *d_ptr
         return;
     char *rp = static_cast<char *>(d_ptr) + (static_cast<long long>(row) * ldd + col0) * OB;
     const int nv = N - col0;  // valid columns of the chunk
-    if (nv >= CW) {
+    constexpr int PER16 = 16 / OB;  // elements per 16-byte unit
+    if (nv >= CW || nv % PER16 == 0) {  // whole 16-byte units (all, or the first nv / PER16)
 #pragma unroll
         for (int u = 0; u < 8; ++u)
-            reinterpret_cast<uint4 *>(rp)[u] = make_uint4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
+            if (u * PER16 < nv)
+                reinterpret_cast<uint4 *>(rp)[u] = make_uint4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
     } else if constexpr (OB == 4) {
 #pragma unroll
         for (int i = 0; i < 32; ++i)
@@ -1350,7 +1357,9 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
     // give each warp R rows (lane quarter q = rows R q..) of every chunk; .ws
     // tiles give it 32 rows of one column part (rows 32 (q % RB) .., chunks
     // [part * NCH / COL_PARTS, (part + 1) * NCH / COL_PARTS))
-    constexpr int NCH = BN / CW;
+    // chunks per row; a two-half tile 224 wide ends in a chunk of 32 columns
+    // (16-bit output), which the epilogue writes from registers
+    constexpr int NCH = (BN + CW - 1) / CW;
     const int wrow = C::WS ? 32 * (q % C::WS_ROW_BLOCKS) : R * q;
     const int c_lo = C::WS ? (q / C::WS_ROW_BLOCKS) * (NCH / C::COL_PARTS) : 0;
     const int c_hi = c_lo + NCH / C::COL_PARTS;
@@ -1458,22 +1467,21 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
             // contiguous bytes per store
             float4 *const slot = partials + static_cast<size_t>(blockIdx.x) * kSlotVec;
             for (int half = 0; half < C::M_HALVES; ++half) {
-                for (int c = 0; c < BN / CW; ++c) {
-                    if (ti.n_blk * BN + c * CW >= ti.N)
+                // 32-column groups of the tile (BN is a multiple of 32)
+                for (int c32 = 0; c32 < BN / 32; ++c32) {
+                    if (ti.n_blk * BN + c32 * 32 >= ti.N)
                         break;
                     const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
-                                           static_cast<uint32_t>((C::M_HALVES == 2 ? half : acc) * BN + c * CW);
+                                           static_cast<uint32_t>((C::M_HALVES == 2 ? half * C::HALF_COL : acc * BN) +
+                                                                 c32 * 32);
                     uint32_t r[32];
+                    tmem_ld_32x32b_x32(taddr, r);
+                    tmem_ld_wait();
 #pragma unroll
-                    for (int h = 0; h < CW / 32; ++h) {
-                        tmem_ld_32x32b_x32(taddr + 32 * h, r);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int g = 0; g < 8; ++g)
-                            __stcg(slot + (c * (CW / 4) + h * 8 + g) * kSlotRows + 128 * half + prow,
-                                   make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
-                                               __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3])));
-                    }
+                    for (int g = 0; g < 8; ++g)
+                        __stcg(slot + (c32 * 8 + g) * kSlotRows + 128 * half + prow,
+                               make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
+                                           __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3])));
                 }
             }
             tc_fence_before_sync();
@@ -1570,16 +1578,22 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
                 if (col0 >= ti.N)
                     break;
                 const int m0h = m0 + 128 * half;
+                // a chunk that runs past the tile (the last one of a 224-wide
+                // tile with 16-bit output) is read and written from registers,
+                // its columns cut at the tile's edge
+                const bool part = (c + 1) * CW > BN;
+                const bool dd = direct_d || part, dc = direct_c || (part && use_c);
+                const int n_lim = part ? min(ti.N, ti.n_blk * BN + BN) : ti.N;
                 const uint32_t sbuf = buf0 + static_cast<uint32_t>(sel * kEpiBufBytes);
                 const uint32_t sbar = ebar0 + static_cast<uint32_t>(8 * sel);
                 // the store issued from this buffer (EPI_BUFS chunks ago) must have read it
-                if (lane == 0 && !direct_d)
+                if (lane == 0 && !dd)
                     bulk_wait_group_read<C::EPI_BUFS - 1>();
                 __syncwarp();
                 uint32_t creg[32];
-                if (direct_c)  // issued before the TMEM load so that the two overlap
-                    load_c_row<CW>(creg, c_ptr, ldc, m0h + trow, col0, ti.M, ti.N);
-                if (use_c && !direct_c && lane == 0) {
+                if (dc)  // issued before the TMEM load so that the two overlap
+                    load_c_row<CW>(creg, c_ptr, ldc, m0h + trow, col0, ti.M, n_lim);
+                if (use_c && !dc && lane == 0) {
                     fence_proxy_async_smem();
                     mbar_arrive_expect_tx(sbar, R * 128);
                     if (hints)
@@ -1592,7 +1606,7 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
                 if (has_acc) {
                     const uint32_t col = static_cast<uint32_t>(
                         C::WS ? acc * C::ACC_COLS + (c - c_lo) * CW
-                              : (C::BM == 128 ? acc * BN : C::M_HALVES == 2 ? half * BN : 0) + c * CW);
+                              : (C::BM == 128 ? acc * BN : C::M_HALVES == 2 ? half * C::HALF_COL : 0) + c * CW);
                     const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + col;
                     uint32_t r[32];
                     tmem_ld_32x32b_x32(taddr, r);
@@ -1626,8 +1640,9 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
                                              128 * half + prow;
                         float4 x[CW / 4];
 #pragma unroll
-                        for (int g = 0; g < CW / 4; ++g)
-                            x[g] = __ldcg(slot + (c * (CW / 4) + g) * kSlotRows);
+                        for (int g = 0; g < CW / 4; ++g)  // the slot holds BN columns
+                            x[g] = c * CW + 4 * g < BN ? __ldcg(slot + (c * (CW / 4) + g) * kSlotRows)
+                                                      : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                         for (int g = 0; g < CW / 4; ++g) {
                             v[4 * g] += x[g].x;
@@ -1650,7 +1665,7 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
                             v[32 * h + i] += __uint_as_float(r[i]);
                     }
                 }
-                if (use_c && !direct_c) {
+                if (use_c && !dc) {
                     const long long tw = stats ? clock64() : 0;
                     bool ok = w.wait(sbar, epi_phase[sel], kRoleEpilogue | kWaitEpiC);
                     if (stats)
@@ -1659,13 +1674,13 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
                     if (!__all_sync(0xffffffffu, ok))
                         return;
                 }
-                if (direct_d) {
+                if (dd) {
                     uint32_t o[32];
                     chunk_math_regs<CW>(v, ec, use_c, creg, o);
-                    store_d_row<CW>(o, d_ptr, ldd, m0h + trow, col0, ti.M, ti.N);
+                    store_d_row<CW>(o, d_ptr, ldd, m0h + trow, col0, ti.M, n_lim);
                     continue;
                 }
-                if (direct_c)
+                if (dc)
                     epilogue_chunk_math<CW, true>(v, ec, sbuf, trow, true, creg);
                 else if (active)
                     epilogue_chunk_math<CW>(v, ec, sbuf, trow, use_c);

@@ -4,3 +4,5 @@
 
 G300_INSTANTIATE(1, 256, 64, 3, false, 2, 256, 0, 0)
 G300_INSTANTIATE(1, 256, 64, 3, false, 2, 256, 0, 2)
+G300_INSTANTIATE(1, 224, 64, 3, false, 2, 256, 0, 0)
+G300_INSTANTIATE(1, 224, 64, 3, false, 2, 256, 0, 2)

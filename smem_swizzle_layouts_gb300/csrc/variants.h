@@ -60,6 +60,8 @@ cudaError_t resident_ctas(int *ctas);
     X(1, 256, 64, 4, false, 2, 128, 0, 2) \
     X(1, 256, 128, 4, false, 1, 128, 0, 2) \
     X(1, 256, 64, 3, false, 2, 256, 0, 0) \
-    X(1, 256, 64, 3, false, 2, 256, 0, 2)
+    X(1, 256, 64, 3, false, 2, 256, 0, 2) \
+    X(1, 224, 64, 3, false, 2, 256, 0, 0) \
+    X(1, 224, 64, 3, false, 2, 256, 0, 2)
 
 }  // namespace g300

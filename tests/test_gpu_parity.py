@@ -318,18 +318,20 @@ def test_k_tail_and_single_column(g):
 # ---------------------------------------------------------------- full-size configurations (sampled)
 
 def test_config2_square_4096_bf16_out(g):
-    M = N = K = 4096
-    run_case(g, M, N, K, a_major="K", b_major="K", out="bf16", dist="normal", scale=0.1, seed=10,
-             options=dict(cta_group=1, tile_n=256), sample=sample_entries(M, N))
-
-
-def test_config2_square_4096_bench_launch_with_streamk(g):
-    # the launch bench.py times: single CTAs of 128 x 256 with a stream-K workspace,
-    # so the ragged fourth wave of 512 tiles is split across the grid
+    # single CTAs of 128 x 256 (the 128-row tile, split over the ragged fourth wave)
     M = N = K = 4096
     ws = torch.zeros(g.gemm_streamk_workspace_size(), dtype=torch.uint8, device=DEV)
     run_case(g, M, N, K, a_major="K", b_major="K", out="bf16", dist="normal", scale=0.1, seed=10,
-             options=dict(cta_group=1, tile_n=256, workspace=ws), sample=sample_entries(M, N, n=1024, seed=7))
+             options=dict(cta_group=1, tile_n=256, tile_m=128, workspace=ws), sample=sample_entries(M, N))
+
+
+def test_config2_square_4096_bench_launch(g):
+    # the launch bench.py times: cta_group 1 and a stream-K workspace, the library
+    # choosing the tile (two-half 256 x 224: two full rounds on 152 SMs, unsplit)
+    M = N = K = 4096
+    ws = torch.zeros(g.gemm_streamk_workspace_size(), dtype=torch.uint8, device=DEV)
+    run_case(g, M, N, K, a_major="K", b_major="K", out="bf16", dist="normal", scale=0.1, seed=10,
+             options=dict(cta_group=1, workspace=ws), sample=sample_entries(M, N, n=1024, seed=7))
 
 
 def test_config3_square_8192_pair_fp32_beta(g):

@@ -189,6 +189,18 @@ def test_two_half_tiles_for_large_single_cta_problems_with_long_k(g):
     # 256 rows on one CTA (two M = 128 MMAs per B slice, both accumulators in TMEM)
     p = plan(g, 4096, 4096, 4096, cta_group=1, tile_n=256)
     assert (p["tile_m"], p["tile_n"], p["block_k"], p["cta_group"], p["multicast_b"]) == (256, 256, 64, 1, 1)
+    # 224 wide where that takes fewer rounds of the grid: 4096^2 on 152 SMs is two
+    # full rounds of 256 x 224 tiles against two of 256-wide clusters for 1.68 waves
+    p = plan(g, 4096, 4096, 4096, cta_group=1, sms=152)
+    assert (p["tile_m"], p["tile_n"], p["block_k"], p["multicast_b"]) == (256, 224, 64, 0)
+    assert plan(g, 8192, 8192, 8192, cta_group=1, sms=152)["tile_n"] == 256        # 7 rounds either way
+    assert plan(g, 4096, 4096, 4096, b=MN_MAJOR, cta_group=1, sms=152)["tile_n"] == 256  # K-major B only
+    p = plan(g, 700, 900, 200, tile_m=256, tile_n=224)
+    assert (p["tile_n"], p["block_k"], p["multicast_b"]) == (224, 64, 0)   # 224 wide keeps its own B
+    assert plan(g, 700, 900, 200, tile_m=256, tile_n=224, multicast_b=1)["multicast_b"] == 1
+    with pytest.raises(g.GemmError) as ei:
+        plan(g, 700, 900, 200, b=MN_MAJOR, tile_m=256, tile_n=224, multicast_b=1)  # halves of 112: not whole atoms
+    assert ei.value.status == g.ERR_UNSUPPORTED
     assert plan(g, 4096, 4096, 4096, cta_group=1, multicast_b=-1)["multicast_b"] == 0   # pairs of CTAs share B unless refused
     assert plan(g, 256, 4096, 4096, tile_m=256)["multicast_b"] == 0                        # one row tile: nothing to share
     p = plan(g, 8192, 8192, 8192, cta_group=1, multicast_b=1)                              # asked for: two-half tiles share B
