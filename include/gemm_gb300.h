@@ -96,10 +96,13 @@ typedef enum {
  *                 operands, single problems, tile_n 256), or 256
  *                 (cta_group::1 only: two M = 128 MMAs per K slice share
  *                 each B slice, their accumulators filling the 512 TMEM
- *                 columns; 16-bit operands, single problems, tile_n 256,
- *                 the epilogue of a tile does not overlap the next tile's
- *                 MMAs; by default two such CTAs share B, see multicast_b).
- *   tile_n        MMA N per tile: 64, 128 or 256 (cta_group::2: 128 or 256).
+ *                 columns; 16-bit operands, single problems, tile_n 256 or
+ *                 224; the epilogue of a tile does not overlap the next
+ *                 tile's MMAs; by default 256-wide ones run in pairs of CTAs
+ *                 that share B, see multicast_b, and the library takes 224
+ *                 where that needs fewer rounds of the grid).
+ *   tile_n        MMA N per tile: 64, 128 or 256 (cta_group::2: 128 or 256;
+ *                 tile_m 256: 224 or 256).
  *   block_k       K elements per pipeline stage: 32, 64 or 128 where built.
  *   swizzle_a/b   operand swizzle (gemm_swizzle_t).
  *   epilogue_swizzle  1 (default) stages output tiles in SW128 layout;
@@ -180,7 +183,7 @@ typedef enum {
  *                 stage and TMA multicasts it into both CTAs' shared memory,
  *                 so each CTA reads half as many B bytes from L2; each CTA's
  *                 MMA completion releases the stage in both. 0 the library
- *                 chooses (256-row tiles of more than 256 rows in all; 128-row
+ *                 chooses (256 x 256 tiles of more than 256 rows in all; 128-row
  *                 tiles when B is MN-major or A and B overflow L2), 1 use it,
  *                 -1 do not; other tiles with 1 return GEMM_ERR_UNSUPPORTED.
  *                 Multicast stays within this GPU's memory (the operands of
