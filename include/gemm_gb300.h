@@ -177,7 +177,8 @@ typedef enum {
  *                 the four TMEM lane quarters by column parts, so all four
  *                 epilogue warps store full 32-row chunks. Other tiles with
  *                 mma_ws 1 return GEMM_ERR_UNSUPPORTED.
- *   multicast_b   single-CTA (cta_group::1) tiles 256 wide (128 or 256 rows)
+ *   multicast_b   single-CTA (cta_group::1) tiles 256 wide (128 or 256 rows),
+ *                 or 224 wide with 256 rows and K-major B,
  *                 run in clusters of two CTAs on vertically adjacent tiles
  *                 that share their B panel: each CTA loads half of every B
  *                 stage and TMA multicasts it into both CTAs' shared memory,
