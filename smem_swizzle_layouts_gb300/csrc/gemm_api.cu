@@ -364,8 +364,10 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
         // 1.68 waves of work, but exactly two rounds of 304 tiles of 256 x 224
         // on 152 CTAs. 224-wide tiles keep their own B: sharing it measured
         // slower there (4096^3, TFLOP/s: 256 wide shared 1389, 224 wide shared
-        // 1449, 224 wide own 1481). K-major B only (measured).
-        if (opt.tile_n == 0 && opt.multicast_b != 1 && !b_mn && find_variant(1, 224, 64, false, 2, 256)) {
+        // 1449, 224 wide own 1481). A and B K-major only: with MN-major B 224 own
+        // measured 941-954 against 1411-1418 for 256 shared, with MN-major A
+        // 1259 against 1360.
+        if (opt.tile_n == 0 && opt.multicast_b != 1 && !a_mn && !b_mn && find_variant(1, 224, 64, false, 2, 256)) {
             auto rounds = [&](int64_t rows, int64_t w, int64_t units) {
                 const int64_t tiles = ((M + rows - 1) / rows) * ((N + w - 1) / w);
                 return (tiles + units - 1) / units;

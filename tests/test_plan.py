@@ -194,7 +194,8 @@ def test_two_half_tiles_for_large_single_cta_problems_with_long_k(g):
     p = plan(g, 4096, 4096, 4096, cta_group=1, sms=152)
     assert (p["tile_m"], p["tile_n"], p["block_k"], p["multicast_b"]) == (256, 224, 64, 0)
     assert plan(g, 8192, 8192, 8192, cta_group=1, sms=152)["tile_n"] == 256        # 7 rounds either way
-    assert plan(g, 4096, 4096, 4096, b=MN_MAJOR, cta_group=1, sms=152)["tile_n"] == 256  # K-major B only
+    assert plan(g, 4096, 4096, 4096, b=MN_MAJOR, cta_group=1, sms=152)["tile_n"] == 256  # K-major A and B only
+    assert plan(g, 4096, 4096, 4096, a=MN_MAJOR, cta_group=1, sms=152)["tile_n"] == 256
     p = plan(g, 700, 900, 200, tile_m=256, tile_n=224)
     assert (p["tile_n"], p["block_k"], p["multicast_b"]) == (224, 64, 0)   # 224 wide keeps its own B
     assert plan(g, 700, 900, 200, tile_m=256, tile_n=224, multicast_b=1)["multicast_b"] == 1
