@@ -502,11 +502,10 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int a_mn, int b_mn, int
     return GEMM_OK;
 }
 
-// Stream-K workspace: a row of 4 flags per CTA, then one 128 x BN fp32 slot per CTA.
+// Stream-K workspace: a row of 4 flags per CTA, then one rows x BN fp32
+// partial-sum slot per CTA (rows 128, or 256 for two-half tiles).
 size_t sk_flag_bytes(int ctas) { return (static_cast<size_t>(ctas) * 4 * sizeof(uint32_t) + 1023) & ~size_t(1023); }
 
-// flags, then one rows x bn fp32 partial-sum slot per CTA (rows 128, or 256
-// for two-half tiles)
 size_t sk_bytes(int ctas, int bn, int rows)
 {
     return sk_flag_bytes(ctas) + static_cast<size_t>(ctas) * rows * bn * sizeof(float);
