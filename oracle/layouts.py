@@ -507,6 +507,18 @@ def tmem_ws(m: int, n: int, M: int, N: int) -> tuple[int, int, int]:
     return 0, 32 * q + m % 32, n % width
 
 
+def tmem_two_half(m: int, n: int, N: int, half_col: int = 256) -> tuple[int, int, int]:
+    """Accumulator map of a 256-row tile held by one CTA as two cta_group::1
+    M = 128 MMAs on the same B slice (the page's M = 128 layout twice: rows
+    0..127 in lanes 0..127 from column 0, rows 128..255 in the same lanes from
+    column ``half_col``). The second half starts at a fixed column, not at N,
+    so that N may be any width up to ``half_col``.
+    """
+    if not 0 < N <= half_col or half_col + N > TMEM_COLS:
+        raise ValueError("both halves must fit the TMEM columns side by side")
+    return 0, m % 128, (m // 128) * half_col + n
+
+
 def tmem_warp_lanes(warp: int) -> range:
     """Lanes a warp may touch: warp w of a warpgroup owns lanes 32*(w%4) .. +31."""
     q = warp % 4

@@ -512,3 +512,23 @@ def test_ws_m128_is_the_ordinary_m128_map_and_m64_differs_from_layout_f():
     f_lanes = {L.tmem_layout_f(m, n)[1] for m in range(64) for n in range(128)}
     assert len(f_lanes) == 64
     assert any(L.tmem_ws(m, n, 64, 128) != L.tmem_layout_f(m, n) for m in range(64) for n in range(128))
+
+
+@pytest.mark.parametrize("N", [224, 256, 128])
+def test_two_half_map_is_two_m128_maps_side_by_side(N):
+    # rows 0..127 are the M = 128 map; rows 128..255 the same map 256 columns on;
+    # every cell distinct, inside 128 lanes x 512 columns, each half in the lane
+    # quarter of its row (the epilogue warp that owns those lanes reads both halves)
+    cells = {L.tmem_two_half(m, n, N) for m in range(256) for n in range(N)}
+    assert len(cells) == 256 * N
+    assert all(0 <= lane < L.TMEM_LANES and 0 <= col < L.TMEM_COLS for _, lane, col in cells)
+    for m in range(128):
+        for n in range(0, N, 7):
+            assert L.tmem_two_half(m, n, N) == L.tmem_cta1_m128(m, n)
+            _, lane, col = L.tmem_two_half(m + 128, n, N)
+            assert (lane, col) == (m, 256 + n)
+            assert lane in L.tmem_warp_lanes(m // 32)  # the warp of lane quarter m // 32
+    # a 64-column chunk read at column 192 of a 224-wide first half stays clear of the second half
+    assert max(col for _, _, col in cells if col < 256) == N - 1 < 256
+    with pytest.raises(ValueError):
+        L.tmem_two_half(0, 0, 320)
