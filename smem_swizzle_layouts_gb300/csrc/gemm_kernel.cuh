@@ -1571,7 +1571,7 @@ __device__ void role_epilogue(const KParams &p, const CUtensorMap *tmC, const CU
             }
         }
         // two-half tiles store the rows of one half after the other (row
-        // offset 128 h, accumulator columns from h BN); other tiles have one
+        // offset 128 h, accumulator columns from h HALF_COL); other tiles have one
         for (int half = 0; half < C::M_HALVES; ++half) {
             for (int c = c_lo; c < c_hi; ++c) {
                 const int col0 = ti.n_blk * BN + c * CW;
